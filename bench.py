@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark: one DWC training step (forward, backward data, backward filter) on GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input: dwc_fwd,
+dwc_bwd_data and dwc_bwd_filter on the same problem.  Default workload: fp32,
+N=64, 56x56, C=128, 7x7 filter, stride 1, pad 3 (the ConvNeXt-stage shape), inputs drawn
+as described in depthwise_convolution_nhwc_gb300/inputs.py.
+
+Prints ONE JSON line (rank 0).  `value` is device-timed throughput with inputs resident in
+HBM (CUDA events on the launching stream around each step, L2 flushed between steps by a
+256 MiB write that is not timed); `e2e` is the same metric through the C ABI with the inputs
+copied from pinned host memory and the outputs copied back inside the timed region.
+`--impl reference` times the fp64 CPU oracle on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DWC fwd+bwd TFLOP/s and GB/s on 1 GB300, % of roofline, per filter size"
+PASSES_ALL = ("fwd", "bwd_data", "bwd_filter")
+# launches of this library's kernels per pass on the fast path
+LAUNCHES = {"fwd": 1, "bwd_data": 1, "bwd_filter": 2}
+KERNEL_NAMES = {"fwd": "rows_kernel<flip=false>", "bwd_data": "rows_kernel<flip=true>",
+                "bwd_filter": "fgrad_kernel + reduce_slices_kernel"}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="f32_n64_56x56_c128_f7")
+    ap.add_argument("--passes", default=",".join(PASSES_ALL))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def get_case(name):
+    from depthwise_convolution_nhwc_gb300.inputs import WORKLOADS, sweep_cases
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    for c in sweep_cases():
+        if c.name == name:
+            return c
+    raise SystemExit(f"unknown workload {name!r}")
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        sm, mx, reasons, n = [], None, set(), 0
+        for t, line in self.lines:
+            if not (t0 - 0.15 <= t <= t1 + 0.15):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            n += 1
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": n}
+
+
+# ---------------------------------------------------------------------------- oracle timing
+def oracle_sample_run(case, passes, frac, host):
+    """Run the oracle on a `frac` sample of every pass's outputs; returns (seconds, flops)."""
+    import numpy as np
+
+    import oracle
+    rng = np.random.default_rng(12345)
+    s, p = case.stride, case.pad
+    x, w, dy = host
+    flops = 0
+    t0 = time.perf_counter()
+    for name in passes:
+        if name == "fwd":
+            n_out = case.N * case.OH * case.OW * case.C
+            k = max(1, int(round(frac * n_out)))
+            oracle.fwd_at(x, w, rng.integers(0, n_out, k), s, p)
+            flops += k * 2 * case.FH * case.FW
+        elif name == "bwd_data":
+            n_out = case.N * case.H * case.W * case.C
+            k = max(1, int(round(frac * n_out)))
+            oracle.bwd_data_at(dy, w, (case.H, case.W), rng.integers(0, n_out, k), s, p)
+            flops += k * 2 * case.FH * case.FW * (case.N * case.OH * case.OW) // (case.N * case.H * case.W)
+        else:
+            n_out = case.FH * case.FW * case.C
+            k = max(1, int(round(frac * n_out)))
+            oracle.bwd_filter_at(x, dy, (case.FH, case.FW), rng.integers(0, n_out, k), s, p)
+            flops += k * 2 * case.N * case.OH * case.OW
+    return time.perf_counter() - t0, flops
+
+
+def oracle_host_inputs(case):
+    x, w, dy = case.x(), case.w(), case.dy()
+    return tuple(t.double().numpy() for t in (x, w, dy))
+
+
+def calibrate_fraction(case, passes, host, seconds):
+    frac = 1e-5
+    for _ in range(8):
+        dt, _ = oracle_sample_run(case, passes, frac, host)
+        if dt > 0.3 or frac >= 1.0:
+            break
+        frac = min(1.0, frac * 8)
+    return min(1.0, frac * seconds / max(dt, 1e-6))
+
+
+def cpu_baseline(case, passes, seconds):
+    import oracle
+    host = oracle_host_inputs(case)
+    frac = calibrate_fraction(case, passes, host, seconds)
+    dt, flops = oracle_sample_run(case, passes, frac, host)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{frac:.3g} of the outputs of each pass ({'+'.join(passes)}), random "
+                      f"positions, fp64 C oracle with OpenMP; {dt:.1f} s"}
+
+
+def run_reference(args, case, passes):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    host = oracle_host_inputs(case)
+    budget = 150.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    frac = calibrate_fraction(case, passes, host, per_step)
+    for _ in range(args.warmup):
+        oracle_sample_run(case, passes, frac, host)
+    tot_t, tot_f = 0.0, 0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample_run(case, passes, frac, host)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(case, passes),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                             "kind": "oracle",
+                             "sample": f"{frac:.3g} of the outputs of each pass per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(case, passes):
+    return {"workload": f"{case.dtype} N={case.N} {case.H}x{case.W} C={case.C} "
+                        f"{case.FH}x{case.FW} stride={case.stride} pad={case.pad}: "
+                        + " + ".join(passes),
+            "N": case.N, "H": case.H, "W": case.W, "C": case.C, "FH": case.FH, "FW": case.FW,
+            "stride": case.stride, "pad": case.pad, "input_dtype": case.dtype,
+            "output_dtype": "f32", "layout": "NHWC / FHxFWxC",
+            "l2": "flushed between timed steps by an untimed 256 MiB write",
+            "inputs": f"{case.dist} draws, seed {case.seed}"}
+
+
+def load_traffic(kernel_key):
+    """ncu DRAM bytes per launch for a kernel, if captured against the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            tab = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = tab.get(kernel_key)
+    if not ent:
+        return None
+    import hashlib
+    h = hashlib.sha256()
+    for rel in ent.get("sources", []):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != ent.get("source_sha256"):
+        return None
+    return ent.get("bytes_per_launch")
+
+
+def run_ours(args, case, passes):
+    import torch
+    import depthwise_convolution_nhwc_gb300 as dwc
+    from depthwise_convolution_nhwc_gb300 import roofline as rl
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    dwc.load_library()
+    stream = torch.cuda.current_stream()
+
+    x, w, dy = (t.to(dev) for t in (case.x(), case.w(), case.dy()))
+    y = torch.empty((case.N, case.OH, case.OW, case.C), device=dev, dtype=torch.float32)
+    dx = torch.empty((case.N, case.H, case.W, case.C), device=dev, dtype=torch.float32)
+    dw = torch.empty((case.FH, case.FW, case.C), device=dev, dtype=torch.float32)
+    ws = dwc.workspace(dwc.bwd_filter_workspace_size(x.shape, (case.FH, case.FW), case.stride,
+                                                     case.pad, x.dtype), dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def run_pass(name, xx, ww, dyy):
+        if name == "fwd":
+            dwc.fwd(xx, ww, case.stride, case.pad, out=y)
+        elif name == "bwd_data":
+            dwc.bwd_data(dyy, ww, (case.H, case.W), case.stride, case.pad, out=dx)
+        else:
+            dwc.bwd_filter(xx, dyy, (case.FH, case.FW), case.stride, case.pad, out=dw, ws=ws)
+
+    for _ in range(args.warmup):
+        for name in passes:
+            run_pass(name, x, w, dy)
+    torch.cuda.synchronize()
+    if dwc.device_status() != 0:
+        raise SystemExit("a kernel reported a timed-out wait during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(passes) + 1)]
+          for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
+        for k in range(args.steps):
+            flush.fill_(float(k))
+            ev[k][0].record(stream)
+            for j, name in enumerate(passes):
+                run_pass(name, x, w, dy)
+                ev[k][j + 1].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        t_wall1 = time.time()
+    clocks = clk.summary(t_wall0, t_wall1)
+    if dwc.device_status() != 0:
+        raise SystemExit("a kernel reported a timed-out wait in the timed region")
+
+    per_pass = {name: [] for name in passes}
+    step_ms = []
+    for k in range(args.steps):
+        step_ms.append(ev[k][0].elapsed_time(ev[k][-1]))
+        for j, name in enumerate(passes):
+            per_pass[name].append(ev[k][j].elapsed_time(ev[k][j + 1]))
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    flops_step = rl.nominal_flops(case) * len(passes)
+    value = world * args.steps * flops_step / (total_ms * 1e-3) / 1e12
+
+    # --- e2e through the C ABI with pinned host buffers -------------------------------
+    hx, hw, hdy = (t.pin_memory() for t in (case.x(), case.w(), case.dy()))
+    hy = torch.empty(y.shape, dtype=torch.float32).pin_memory()
+    hdx = torch.empty(dx.shape, dtype=torch.float32).pin_memory()
+    hdw = torch.empty(dw.shape, dtype=torch.float32).pin_memory()
+    dxb, dwb, ddy = torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)
+    h2d = sum(t.numel() * t.element_size() for t, nm in ((hx, "x"), (hw, "w"), (hdy, "dy"))
+              if nm == "w" or (nm == "x" and ("fwd" in passes or "bwd_filter" in passes))
+              or (nm == "dy" and ("bwd_data" in passes or "bwd_filter" in passes)))
+    d2h = sum({"fwd": hy, "bwd_data": hdx, "bwd_filter": hdw}[n].numel() * 4 for n in passes)
+
+    def e2e_step():
+        dxb.copy_(hx, non_blocking=True)
+        dwb.copy_(hw, non_blocking=True)
+        ddy.copy_(hdy, non_blocking=True)
+        for name in passes:
+            run_pass(name, dxb, dwb, ddy)
+        if "fwd" in passes:
+            hy.copy_(y, non_blocking=True)
+        if "bwd_data" in passes:
+            hdx.copy_(dx, non_blocking=True)
+        if "bwd_filter" in passes:
+            hdw.copy_(dw, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * args.e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    # --- roofline of the dominant kernel ----------------------------------------------
+    peaks = rl.load_peaks()
+    mean_ms = {n: statistics.fmean(v) for n, v in per_pass.items()}
+    dom = max(mean_ms, key=mean_ms.get)
+    t_dom = mean_ms[dom] * 1e-3
+    t_roof, bound = rl.roofline_time_s(case, dom, peaks)
+    if bound == "hbm":
+        achieved = rl.compulsory_bytes(case, dom) / t_dom / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved = rl.valid_flops(case) / t_dom / 1e12
+        peak, unit = peaks["fp32_tflops"], "TFLOP/s"
+    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": load_traffic(f"{dom}:{case.name or 'default'}"),
+            "kernel": KERNEL_NAMES[dom], "pass": dom,
+            "peak_source": ("measured HBM copy (MEASURED_PEAKS.json)" if bound == "hbm" and
+                            peaks["source"] == "measured" else
+                            "fp32 FFMA peak derived: 152 SMs x 128 lanes x 2 x 2070 MHz"
+                            if bound == "alu" else "fallback")}
+    passes_out = {}
+    for n in passes:
+        t = mean_ms[n] * 1e-3
+        tr, b = rl.roofline_time_s(case, n, peaks)
+        passes_out[n] = {"ms": mean_ms[n], "ms_median": statistics.median(per_pass[n]),
+                         "tflops_nominal": rl.nominal_flops(case) / t / 1e12,
+                         "tflops_valid": rl.valid_flops(case) / t / 1e12,
+                         "gbs": rl.compulsory_bytes(case, n) / t / 1e9,
+                         "roofline_frac": tr / t, "roofline_bound": b}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": config_dict(case, passes),
+            "gbs": sum(rl.compulsory_bytes(case, n) for n in passes) * args.steps * world
+                   / (total_ms * 1e-3) / 1e9,
+            "roofline": roof, "per_pass": passes_out,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+            "gpu_launches": args.steps * sum(LAUNCHES[n] for n in passes),
+            "clocks": clocks}
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(case, passes, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    case = get_case(args.workload)
+    passes = tuple(p for p in args.passes.split(",") if p)
+    for p in passes:
+        if p not in PASSES_ALL:
+            raise SystemExit(f"unknown pass {p}")
+    if args.impl == "reference":
+        run_reference(args, case, passes)
+    else:
+        run_ours(args, case, passes)
+
+
+if __name__ == "__main__":
+    main()

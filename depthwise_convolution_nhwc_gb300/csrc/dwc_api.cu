@@ -1,0 +1,298 @@
+// dwc_api.cu -- the C ABI declared in include/dwc.h: argument validation, choice between
+// the fast and the general kernels, TMA descriptor encoding and the device status word.
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/dwc.h"
+#include "dwc_host.h"
+
+namespace dwc {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Status word the kernels set when a wait runs out of time (one per device, in this
+// module's global memory; its address is looked up once per device).
+__device__ unsigned int g_status_word;
+
+struct PerDevice {
+    bool ready = false;
+    DeviceInfo info{};
+    unsigned int* status = nullptr;
+};
+
+PerDevice g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// One-time set-up for the current device; nullptr if CUDA is unusable.
+PerDevice* device_state() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    PerDevice& s = g_dev[d];
+    if (!s.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, d) != cudaSuccess) return nullptr;
+        s.info.sm_count = prop.multiProcessorCount;
+        s.info.max_smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;
+        s.status = static_cast<unsigned int*>(addr);
+        s.ready = true;
+    }
+    return &s;
+}
+
+}  // namespace
+
+const DeviceInfo& device_info() {
+    static const DeviceInfo fallback{148, 232448};
+    PerDevice* s = device_state();
+    return s ? s->info : fallback;
+}
+
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* base,
+                      const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+                      const cuuint32_t* box) {
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (g_encode == nullptr) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return CUDA_ERROR_NOT_FOUND;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return g_encode(map, type, rank, base, dims, strides_bytes, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+static unsigned int* status_word() {
+    PerDevice* s = device_state();
+    return s ? s->status : nullptr;
+}
+
+}  // namespace dwc
+
+using namespace dwc;
+
+namespace {
+
+enum Pass { kPassFwd = 0, kPassBwdData = 1, kPassBwdFilter = 2 };
+
+int out_dim(int n_in, int f, int s, int p) {
+    const long long num = static_cast<long long>(n_in) + 2LL * p - f;
+    if (s < 1 || num < 0) return 0;
+    return static_cast<int>(num / s) + 1;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Problem {
+    int N, H, W, C, FH, FW, s, p, OH, OW, e, dtype;
+};
+
+// Host-side validation shared by every entry point.
+dwc_status_t check_problem(int N, int H, int W, int C, int FH, int FW, int stride, int pad,
+                           dwc_dtype_t dtype, Problem& P) {
+    if (dtype != DWC_F32 && dtype != DWC_BF16 && dtype != DWC_F16) return DWC_ERR_INVALID_ARG;
+    if (N < 0 || C < 0 || H < 1 || W < 1 || FH < 1 || FW < 1 || stride < 1 || pad < 0)
+        return DWC_ERR_INVALID_ARG;
+    P.N = N; P.H = H; P.W = W; P.C = C; P.FH = FH; P.FW = FW; P.s = stride; P.p = pad;
+    P.OH = out_dim(H, FH, stride, pad);
+    P.OW = out_dim(W, FW, stride, pad);
+    if (P.OH < 1 || P.OW < 1) return DWC_ERR_INVALID_ARG;
+    P.e = dtype == DWC_F32 ? 4 : 2;
+    P.dtype = static_cast<int>(dtype);
+    const long long in_elems = static_cast<long long>(N) * H * W * C;
+    const long long out_elems = static_cast<long long>(N) * P.OH * P.OW * C;
+    if (in_elems > (1LL << 40) || out_elems > (1LL << 40) ||
+        static_cast<long long>(FH) * FW * C > (1LL << 36) ||
+        static_cast<long long>(N) * P.OH > INT_MAX / 2 ||
+        static_cast<long long>(N) * H > INT_MAX / 2)
+        return DWC_ERR_UNSUPPORTED;
+    return DWC_OK;
+}
+
+dwc_status_t check_pointers(const Problem& P, const void* a, long long a_elems, const void* b,
+                            long long b_elems, const void* out, long long out_elems) {
+    if ((a_elems > 0 && a == nullptr) || (b_elems > 0 && b == nullptr) ||
+        (out_elems > 0 && out == nullptr))
+        return DWC_ERR_INVALID_ARG;
+    if (!aligned(a, P.e) || !aligned(b, P.e) || !aligned(out, 4)) return DWC_ERR_ALIGNMENT;
+    return DWC_OK;
+}
+
+bool fast_eligible(const Problem& P, const void* a, const void* b, const void* out) {
+    if (P.s != 1) return false;
+    if (!rows_supported(P.FH, P.FW)) return false;
+    if (P.C % (16 / P.e) != 0) return false;  // TMA strides must be multiples of 16 bytes
+    for (const void* q : {a, b, out})
+        if (q != nullptr && !aligned(q, 16)) return false;
+    return true;
+}
+
+dwc_status_t map_cuda(cudaError_t err) { return err == cudaSuccess ? DWC_OK : DWC_ERR_CUDA; }
+
+cudaError_t launch_rows(const RowConv& rc) {
+    switch (rc.dtype) {
+        case kF32: return launch_rows_f32(rc);
+        case kBF16: return launch_rows_bf16(rc);
+        default: return launch_rows_f16(rc);
+    }
+}
+
+cudaError_t launch_fgrad(const FilterGrad& fg) {
+    switch (fg.dtype) {
+        case kF32: return launch_filter_grad_f32(fg);
+        case kBF16: return launch_filter_grad_bf16(fg);
+        default: return launch_filter_grad_f16(fg);
+    }
+}
+
+size_t fast_fgrad_floats(const Problem& P) {
+    return filter_grad_workspace_floats(P.N, P.OH, P.OW, P.C, P.FH, P.FW, P.e);
+}
+
+}  // namespace
+
+extern "C" {
+
+dwc_status_t dwc_fwd(const void* x, const void* w, float* y, int N, int H, int W, int C, int FH,
+                     int FW, int stride, int pad, dwc_dtype_t dtype, dwc_stream_t stream) {
+    Problem P;
+    dwc_status_t st = check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P);
+    if (st != DWC_OK) return st;
+    const long long nx = static_cast<long long>(N) * H * W * C;
+    const long long ny = static_cast<long long>(N) * P.OH * P.OW * C;
+    st = check_pointers(P, x, nx, w, static_cast<long long>(FH) * FW * C, y, ny);
+    if (st != DWC_OK) return st;
+    if (ny == 0) return DWC_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (fast_eligible(P, x, w, y)) {
+        RowConv rc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype, s, status_word()};
+        const cudaError_t err = launch_rows(rc);
+        if (err != cudaErrorNotSupported) return map_cuda(err);
+        (void)cudaGetLastError();
+    }
+    GeneralConv gc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, stride, pad, P.dtype, nullptr, 0, s};
+    return map_cuda(launch_general_fwd(gc));
+}
+
+dwc_status_t dwc_bwd_data(const void* dy, const void* w, float* dx, int N, int H, int W, int C,
+                          int FH, int FW, int stride, int pad, dwc_dtype_t dtype,
+                          dwc_stream_t stream) {
+    Problem P;
+    dwc_status_t st = check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P);
+    if (st != DWC_OK) return st;
+    const long long ndy = static_cast<long long>(N) * P.OH * P.OW * C;
+    const long long ndx = static_cast<long long>(N) * H * W * C;
+    st = check_pointers(P, dy, ndy, w, static_cast<long long>(FH) * FW * C, dx, ndx);
+    if (st != DWC_OK) return st;
+    if (ndx == 0) return DWC_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (fast_eligible(P, dy, w, dx)) {
+        // stride 1: forward pass over dy with the filter rotated by 180 degrees and the
+        // complementary padding FH-1-pad (rows) / FW-1-pad (columns); output is H x W.
+        RowConv rc{dy, w, dx, N, P.OH, P.OW, C, H, W, FH, FW, FH - 1 - pad, FW - 1 - pad, true,
+                   P.dtype, s, status_word()};
+        const cudaError_t err = launch_rows(rc);
+        if (err != cudaErrorNotSupported) return map_cuda(err);
+        (void)cudaGetLastError();
+    }
+    GeneralConv gc{dy, w, dx, N, H, W, C, P.OH, P.OW, FH, FW, stride, pad, P.dtype, nullptr, 0, s};
+    return map_cuda(launch_general_bwd_data(gc));
+}
+
+size_t dwc_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int FW, int stride,
+                                     int pad, dwc_dtype_t dtype) {
+    Problem P;
+    if (check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P) != DWC_OK) return 0;
+    size_t floats = general_bwd_filter_workspace_floats(N, P.OH, C, FH, FW);
+    if (fast_eligible(P, nullptr, nullptr, nullptr)) floats = std::max(floats, fast_fgrad_floats(P));
+    return floats * sizeof(float);
+}
+
+dwc_status_t dwc_bwd_filter(const void* x, const void* dy, float* dw, int N, int H, int W, int C,
+                            int FH, int FW, int stride, int pad, dwc_dtype_t dtype,
+                            void* workspace, size_t workspace_bytes, dwc_stream_t stream) {
+    Problem P;
+    dwc_status_t st = check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P);
+    if (st != DWC_OK) return st;
+    const long long nx = static_cast<long long>(N) * H * W * C;
+    const long long ndy = static_cast<long long>(N) * P.OH * P.OW * C;
+    const long long ndw = static_cast<long long>(FH) * FW * C;
+    st = check_pointers(P, x, nx, dy, ndy, dw, ndw);
+    if (st != DWC_OK) return st;
+    if (ndw == 0) return DWC_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 0) return map_cuda(cudaMemsetAsync(dw, 0, sizeof(float) * ndw, s));
+    const size_t need = dwc_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, pad, dtype);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
+        return DWC_ERR_WORKSPACE;
+    float* ws = static_cast<float*>(workspace);
+    const size_t ws_floats = workspace_bytes / sizeof(float);
+    if (fast_eligible(P, x, dy, dw) && fast_fgrad_floats(P) > 0) {
+        FilterGrad fg{x, dy, dw, N, H, W, C, P.OH, P.OW, FH, FW, pad, P.dtype, ws, ws_floats, s,
+                      status_word()};
+        const cudaError_t err = launch_fgrad(fg);
+        if (err != cudaErrorNotSupported) return map_cuda(err);
+        (void)cudaGetLastError();
+    }
+    GeneralConv gc{x, dy, dw, N, H, W, C, P.OH, P.OW, FH, FW, stride, pad, P.dtype, ws, ws_floats, s};
+    return map_cuda(launch_general_bwd_filter(gc));
+}
+
+dwc_status_t dwc_device_status(dwc_stream_t stream) {
+    unsigned int* word = status_word();
+    if (word == nullptr) return DWC_ERR_CUDA;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DWC_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DWC_ERR_CUDA;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return DWC_ERR_CUDA;
+        return DWC_ERR_TIMEOUT;
+    }
+    return DWC_OK;
+}
+
+const char* dwc_status_string(dwc_status_t status) {
+    switch (status) {
+        case DWC_OK: return "ok";
+        case DWC_ERR_INVALID_ARG: return "invalid argument";
+        case DWC_ERR_UNSUPPORTED: return "problem size beyond the library's limits";
+        case DWC_ERR_ALIGNMENT: return "tensor pointer not aligned to its element size";
+        case DWC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case DWC_ERR_CUDA: return "CUDA runtime or launch error";
+        case DWC_ERR_TIMEOUT: return "a kernel wait ran out of time";
+        default: return "unknown status";
+    }
+}
+
+int dwc_version(void) { return 100; }
+
+int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int H, int W, int C,
+             int FH, int FW, int stride, int pad, dwc_dtype_t dtype) {
+    Problem P;
+    if (pass < 0 || pass > 2) return -1;
+    if (check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P) != DWC_OK) return -1;
+    if (!fast_eligible(P, a, b, out)) return 0;
+    if (pass == kPassBwdFilter && fast_fgrad_floats(P) == 0) return 0;
+    return 1;
+}
+
+}  // extern "C"

@@ -1,0 +1,158 @@
+// dwc_device.cuh -- device-side building blocks shared by the DWC kernels (sm_103a).
+//
+// mbarrier + TMA (cp.async.bulk.tensor) staging with bounded waits, packed fp32x2 FMA,
+// and 16-bit -> fp32 pair conversion.  Every wait on an mbarrier has a time limit: when
+// it runs out the kernel records DWC_DEVSTAT_TIMEOUT in the status word it was given
+// and winds down instead of spinning forever.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dwc {
+
+// Bits of the device status word (a 32-bit word in global memory, read by the host).
+enum : unsigned int {
+    DWC_DEVSTAT_TIMEOUT = 1u,   // an mbarrier wait ran out of time
+};
+
+// Upper bound on one mbarrier wait.  A healthy wait lasts microseconds; this only ends a
+// kernel whose copies never arrive.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Returns false if the time limit
+// ran out (the caller then records the timeout and winds down).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void record_status(unsigned int* status, unsigned int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// --- TMA tiled loads (global -> shared, completion counted on an mbarrier) -------------
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// --- arithmetic ------------------------------------------------------------------------
+// acc += a * b on two fp32 lanes at once (one packed FMA instruction on sm_100+).
+__device__ __forceinline__ void fma2(float2& acc, float2 a, float2 b) {
+    acc = __ffma2_rn(a, b, acc);
+}
+
+// Element type traits: how two adjacent channels are loaded from shared memory and
+// widened to fp32 (exact for bf16 and fp16).
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    using pair_t = float2;
+    static constexpr int kBytes = 4;
+    static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    __device__ static __forceinline__ float2 load_pair(const float* p) {
+        return *reinterpret_cast<const float2*>(p);
+    }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    using pair_t = __nv_bfloat162;
+    static constexpr int kBytes = 2;
+    static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    __device__ static __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+    }
+};
+
+template <>
+struct Elem<__half> {
+    using pair_t = __half2;
+    static constexpr int kBytes = 2;
+    static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    __device__ static __forceinline__ float2 load_pair(const __half* p) {
+        return __half22float2(*reinterpret_cast<const __half2*>(p));
+    }
+};
+
+// Scalar widening for the generic kernels.
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+
+// Streaming store of an fp32 pair (outputs are written once and not re-read).
+__device__ __forceinline__ void store_pair_streaming(float* p, float2 v) {
+    __stcs(reinterpret_cast<float2*>(p), v);
+}
+
+}  // namespace dwc

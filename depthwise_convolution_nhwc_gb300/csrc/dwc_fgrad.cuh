@@ -1,0 +1,396 @@
+// dwc_fgrad.cuh -- filter-gradient kernel ("backward filter convolution").
+//
+//   dw[fh, fw, c] = sum_{n, oh, ow} x[n, oh + fh - pad, ow + fw - pad, c] * dy[n, oh, ow, c]
+//
+// ("Flash-DWC: Making Depthwise Convolution Compute-Efficient on GPUs", §5.1: the output is
+// only FH x FW x C and does not grow with batch or resolution, so the work is spread over
+// the accumulation axis N*OH*OW.)  GB300 restatement:
+//  * The accumulation axis (flattened output rows n*OH + oh) is cut into Z slices; a CTA
+//    owns one slice, one block of 64 channels and one chunk of FHC filter rows.  Z is chosen
+//    from the SM count so that the grid fills the GPU.
+//  * Instead of the pages' fp32 atomics, every CTA writes its partial gradient to its own
+//    slot of a workspace [Z][FH][FW][C]; a second kernel sums the Z slots in a fixed order.
+//    Within a CTA the column strips of the warps are summed in a fixed order through shared
+//    memory.  Results are therefore bit-identical from run to run.
+//  * A producer warp streams, with TMA, the dy rows of the slice and the x rows they pair
+//    with.  The x rows form a window of FHC rows that slides by one row per output row, so
+//    every x row enters shared memory once per CTA.
+//  * Each compute warp owns RF filter rows and one strip of output columns; a lane owns two
+//    channels and keeps RF x FW fp32x2 accumulators plus, per owned row, a circular register
+//    window of the FW x values that the current output column multiplies.  Each dy element
+//    is loaded once and used for RF*FW packed FMAs.
+#pragma once
+
+#include "dwc_rows.cuh"
+
+namespace dwc {
+
+// Filter rows per warp: as many as fit ~120 accumulator+window registers.
+template <int FH, int FW>
+struct FgradTile {
+    static constexpr int kFit = 120 / (4 * FW);
+    static constexpr int RF = kFit < 1 ? 1 : (kFit > FH ? FH : kFit);
+};
+
+struct FgradArgs {
+    float* part;           // [Z][FH][FW][C] partial sums
+    unsigned int* status;
+    int N, OH, C, pad;
+    int nwf, nwc;          // compute warps: filter-row groups x column strips
+    int fhc, chunks, cblocks, Z;
+    int rows_per_slice;    // flattened output rows per slice
+    int nblocks, bps;      // FW-wide column blocks per row, blocks per strip
+    int nx, ny;            // ring slots for x rows and dy rows
+    uint32_t x_bytes, y_bytes;
+    uint32_t y_off;        // byte offset of the dy ring after the x ring
+};
+
+template <typename T, int FH, int FW>
+__global__ void __launch_bounds__(kRowsMaxThreads, 1)
+fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
+             const FgradArgs a) {
+    constexpr int RF = FgradTile<FH, FW>::RF;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* xfull = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* xempty = xfull + a.nx;
+    uint64_t* yfull = xempty + a.nx;
+    uint64_t* yempty = yfull + a.ny;
+    unsigned char* xring = smem + 512;
+    unsigned char* yring = xring + a.y_off;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int ncompute = a.nwf * a.nwc;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.nx; ++s) {
+            mbar_init(&xfull[s], 1);
+            mbar_init(&xempty[s], ncompute);
+        }
+        for (int s = 0; s < a.ny; ++s) {
+            mbar_init(&yfull[s], 1);
+            mbar_init(&yempty[s], ncompute);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // CTA -> (slice z, channel block cb, filter-row chunk); chunks of one slice are adjacent
+    // so that they read the same rows out of L2.
+    int b = blockIdx.x;
+    const int chunk = b % a.chunks; b /= a.chunks;
+    const int cb = b % a.cblocks; b /= a.cblocks;
+    const int z = b;
+    const int fh0 = chunk * a.fhc;
+    const long long total_rows = static_cast<long long>(a.N) * a.OH;
+    const long long q0 = static_cast<long long>(z) * a.rows_per_slice;
+    const long long q1 = std::min<long long>(q0 + a.rows_per_slice, total_rows);
+
+    // ---------------- producer ----------------------------------------------------------
+    if (warp == ncompute) {
+        if (lane != 0) return;
+        prefetch_tensormap(&xmap);
+        prefetch_tensormap(&ymap);
+        long long gx = 0, gy = 0;
+        bool ok = true;
+        auto put_x = [&](int n, int ih) -> bool {
+            const int slot = static_cast<int>(gx % a.nx);
+            const long long use = gx / a.nx;
+            if (use > 0 && !mbar_wait(&xempty[slot], static_cast<uint32_t>((use - 1) & 1)))
+                return false;
+            mbar_arrive_expect_tx(&xfull[slot], a.x_bytes);
+            tma_load_4d(xring + static_cast<size_t>(slot) * a.x_bytes, &xmap, &xfull[slot],
+                        cb * kBN, -a.pad, ih, n);
+            ++gx;
+            return true;
+        };
+        auto put_y = [&](int n, int oh) -> bool {
+            const int slot = static_cast<int>(gy % a.ny);
+            const long long use = gy / a.ny;
+            if (use > 0 && !mbar_wait(&yempty[slot], static_cast<uint32_t>((use - 1) & 1)))
+                return false;
+            mbar_arrive_expect_tx(&yfull[slot], a.y_bytes);
+            tma_load_4d(yring + static_cast<size_t>(slot) * a.y_bytes, &ymap, &yfull[slot],
+                        cb * kBN, 0, oh, n);
+            ++gy;
+            return true;
+        };
+        for (long long q = q0; q < q1 && ok;) {
+            const int n = static_cast<int>(q / a.OH);
+            const int oha = static_cast<int>(q % a.OH);
+            const int ohb = static_cast<int>(std::min<long long>(q1 - static_cast<long long>(n) * a.OH, a.OH));
+            const int ih0 = oha + fh0 - a.pad;
+            for (int r = 0; r < a.fhc - 1 && ok; ++r) ok = put_x(n, ih0 + r);
+            for (int oh = oha; oh < ohb && ok; ++oh) {
+                ok = put_x(n, ih0 + (oh - oha) + a.fhc - 1);
+                if (ok) ok = put_y(n, oh);
+            }
+            q = static_cast<long long>(n) * a.OH + ohb;
+        }
+        if (!ok) record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+        // drain: the last copies of both rings must land before the CTA may exit
+        for (long long j = gx > a.nx ? gx - a.nx : 0; j < gx; ++j)
+            if (!mbar_wait(&xfull[j % a.nx], static_cast<uint32_t>((j / a.nx) & 1))) {
+                record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+                break;
+            }
+        for (long long j = gy > a.ny ? gy - a.ny : 0; j < gy; ++j)
+            if (!mbar_wait(&yfull[j % a.ny], static_cast<uint32_t>((j / a.ny) & 1))) {
+                record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+                break;
+            }
+        return;
+    }
+
+    // ---------------- compute warps -----------------------------------------------------
+    const int wf = warp % a.nwf;
+    const int wc = warp / a.nwf;
+    const int frow0 = wf * RF;                     // first owned row within the chunk
+    const int blk0 = wc * a.bps;
+    const int blk1 = std::min(blk0 + a.bps, a.nblocks);
+
+    float2 acc[RF][FW];
+#pragma unroll
+    for (int f = 0; f < RF; ++f)
+#pragma unroll
+        for (int t = 0; t < FW; ++t) acc[f][t] = make_float2(0.f, 0.f);
+
+    bool live[RF];
+#pragma unroll
+    for (int f = 0; f < RF; ++f) live[f] = (frow0 + f < a.fhc) && (fh0 + frow0 + f < FH);
+
+    long long gx = 0, gy = 0;
+    bool ok = true;
+    for (long long q = q0; q < q1 && ok;) {
+        const int n = static_cast<int>(q / a.OH);
+        const int oha = static_cast<int>(q % a.OH);
+        const int ohb = static_cast<int>(std::min<long long>(q1 - static_cast<long long>(n) * a.OH, a.OH));
+        const long long gx0 = gx;
+        const int L = ohb - oha;
+        for (int yr = 0; yr < L && ok; ++yr) {
+            // wait for the x rows this output row needs (all of them at the segment start)
+            for (long long j = (yr == 0 ? gx0 : gx0 + yr + a.fhc - 1); j <= gx0 + yr + a.fhc - 1; ++j)
+                if (!mbar_wait(&xfull[j % a.nx], static_cast<uint32_t>((j / a.nx) & 1))) {
+                    ok = false;
+                    break;
+                }
+            if (ok && !mbar_wait(&yfull[gy % a.ny], static_cast<uint32_t>((gy / a.ny) & 1)))
+                ok = false;
+            if (!ok) break;
+
+            const T* ys = reinterpret_cast<const T*>(yring + static_cast<size_t>(gy % a.ny) * a.y_bytes) + 2 * lane;
+            const T* xs[RF];
+#pragma unroll
+            for (int f = 0; f < RF; ++f) {
+                const long long j = gx0 + yr + frow0 + f;
+                xs[f] = reinterpret_cast<const T*>(xring + static_cast<size_t>(j % a.nx) * a.x_bytes) + 2 * lane;
+            }
+            if (blk0 < blk1) {
+                // circular window: column c of the padded x row sits in slot c mod FW
+                float2 win[RF][FW];
+                const int c0 = blk0 * FW;
+#pragma unroll
+                for (int f = 0; f < RF; ++f)
+#pragma unroll
+                    for (int m = 0; m < FW - 1; ++m)
+                        win[f][m] = live[f] ? Elem<T>::load_pair(xs[f] + (c0 + m) * kBN)
+                                            : make_float2(0.f, 0.f);
+#pragma unroll 1
+                for (int blk = blk0; blk < blk1; ++blk) {
+                    const int cb0 = blk * FW;
+#pragma unroll
+                    for (int u = 0; u < FW; ++u) {
+                        const float2 g = Elem<T>::load_pair(ys + (cb0 + u) * kBN);
+#pragma unroll
+                        for (int f = 0; f < RF; ++f) {
+                            if (!live[f]) continue;
+                            win[f][(u + FW - 1) % FW] = Elem<T>::load_pair(xs[f] + (cb0 + u + FW - 1) * kBN);
+#pragma unroll
+                            for (int t = 0; t < FW; ++t) fma2(acc[f][t], win[f][(u + t) % FW], g);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&yempty[gy % a.ny]);
+                mbar_arrive(&xempty[(gx0 + yr) % a.nx]);
+            }
+            ++gy;
+        }
+        if (!ok) break;
+        // rows gx0+L .. gx0+L+fhc-2 are not needed by later output rows of this segment
+        __syncwarp();
+        if (lane == 0)
+            for (long long j = gx0 + L; j < gx0 + L + a.fhc - 1; ++j) mbar_arrive(&xempty[j % a.nx]);
+        gx = gx0 + L + a.fhc - 1;
+        q = static_cast<long long>(n) * a.OH + ohb;
+    }
+    // A warp that gave up still goes through the two CTA barriers below, so that no
+    // compute warp can wait on them forever; the status word reports the failure.
+    if (!ok) record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+
+    // ---- fixed-order sum over the column strips, through shared memory ----------------
+    // All ring copies have landed (every stage was waited on), so the ring is reused.
+    asm volatile("bar.sync 1, %0;" ::"r"(ncompute * 32) : "memory");
+    float2* red = reinterpret_cast<float2*>(xring);
+    // layout: [wc][wf][f][t][lane]
+    const size_t per_warp = static_cast<size_t>(RF) * FW * 32;
+    float2* mine = red + (static_cast<size_t>(wc) * a.nwf + wf) * per_warp;
+#pragma unroll
+    for (int f = 0; f < RF; ++f)
+#pragma unroll
+        for (int t = 0; t < FW; ++t) mine[(f * FW + t) * 32 + lane] = acc[f][t];
+    asm volatile("bar.sync 1, %0;" ::"r"(ncompute * 32) : "memory");
+    if (wc == 0) {
+        const int c = cb * kBN + 2 * lane;
+        for (int f = 0; f < RF; ++f) {
+            const int fh = fh0 + frow0 + f;
+            if (!live[f] || c >= a.C) continue;
+            for (int t = 0; t < FW; ++t) {
+                float2 s = red[(static_cast<size_t>(wf) * per_warp) + (f * FW + t) * 32 + lane];
+                for (int k = 1; k < a.nwc; ++k) {
+                    const float2 v = red[(static_cast<size_t>(k) * a.nwf + wf) * per_warp + (f * FW + t) * 32 + lane];
+                    s.x += v.x;
+                    s.y += v.y;
+                }
+                float* dst = a.part + ((static_cast<size_t>(z) * FH + fh) * FW + t) * a.C + c;
+                *reinterpret_cast<float2*>(dst) = s;
+            }
+        }
+    }
+}
+
+template <int FH, int FW>
+struct FgradPlan {
+    int nwf, nwc, fhc, chunks, cblocks, Z, rows_per_slice, nblocks, bps, nx, ny;
+    uint32_t x_bytes, y_bytes, y_off;
+    size_t smem;
+    int pwx, owp;
+};
+
+// Shapes of the launch for one problem (shared by the workspace query and the launch).
+template <int FH, int FW>
+bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW>& P) {
+    constexpr int RF = FgradTile<FH, FW>::RF;
+    const DeviceInfo& dev = device_info();
+    P.nblocks = (OW + FW - 1) / FW;
+    P.owp = P.nblocks * FW;
+    P.pwx = P.owp + FW - 1;
+    if (P.pwx > 256) return false;
+    P.x_bytes = static_cast<uint32_t>(P.pwx * kBN * e);
+    P.y_bytes = static_cast<uint32_t>(P.owp * kBN * e);
+    P.ny = 2;
+    // largest row group whose x window fits in shared memory ...
+    const int groups = (FH + RF - 1) / RF;  // RF-row groups needed to cover the filter
+    int nwf_max = std::min(groups, kMaxComputeWarps);
+    for (; nwf_max >= 1; --nwf_max) {
+        const size_t need = 512 + static_cast<size_t>(nwf_max * RF + 2) * P.x_bytes +
+                            static_cast<size_t>(P.ny) * P.y_bytes;
+        if (need <= static_cast<size_t>(dev.max_smem_optin)) break;
+    }
+    if (nwf_max < 1) return false;
+    // ... then the fewest chunks, with the groups spread evenly over them
+    const int chunks = (groups + nwf_max - 1) / nwf_max;
+    P.nwf = (groups + chunks - 1) / chunks;
+    P.fhc = P.nwf * RF;
+    P.nx = P.fhc + 2;
+    P.smem = 512 + static_cast<size_t>(P.nx) * P.x_bytes + static_cast<size_t>(P.ny) * P.y_bytes;
+    P.chunks = (FH + P.fhc - 1) / P.fhc;
+    P.nwc = std::max(1, std::min(kMaxComputeWarps / P.nwf, P.nblocks));
+    P.bps = (P.nblocks + P.nwc - 1) / P.nwc;
+    P.nwc = (P.nblocks + P.bps - 1) / P.bps;
+    // strip reduction buffer reuses the ring
+    const size_t red = static_cast<size_t>(P.nwc) * P.nwf * RF * FW * 32 * sizeof(float2);
+    if (red > P.smem - 512) P.smem = 512 + red;
+    P.y_off = static_cast<uint32_t>(P.nx) * P.x_bytes;
+    P.cblocks = (C + kBN - 1) / kBN;
+    const long long rows = static_cast<long long>(N) * OH;
+    const long long per_z = static_cast<long long>(P.cblocks) * P.chunks;
+    const int ctas_per_sm = P.smem * 2 + 2048 <= 233472u ? 2 : 1;
+    long long Z = (static_cast<long long>(dev.sm_count) * ctas_per_sm + per_z - 1) / per_z;
+    Z = std::max<long long>(1, std::min<long long>(Z, rows));
+    P.rows_per_slice = static_cast<int>((rows + Z - 1) / Z);
+    P.Z = static_cast<int>((rows + P.rows_per_slice - 1) / P.rows_per_slice);
+    return true;
+}
+
+template <typename T, int FH, int FW>
+cudaError_t launch_fgrad_inst(const FilterGrad& p) {
+    const int e = static_cast<int>(sizeof(T));
+    FgradPlan<FH, FW> P;
+    if (!fgrad_plan<FH, FW>(p.N, p.OH, p.OW, p.C, e, P)) return cudaErrorNotSupported;
+    if (p.N == 0 || p.OH == 0 || p.OW == 0) {
+        return cudaMemsetAsync(p.dw, 0, sizeof(float) * FH * FW * p.C, p.stream);
+    }
+    const size_t need = static_cast<size_t>(P.Z) * FH * FW * p.C;
+    if (p.workspace_floats < need || p.workspace == nullptr) return cudaErrorInvalidValue;
+
+    CUtensorMap xmap, ymap;
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)p.C, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.N};
+        const cuuint64_t strides[3] = {(cuuint64_t)p.C * e, (cuuint64_t)p.W * p.C * e,
+                                       (cuuint64_t)p.H * p.W * p.C * e};
+        const cuuint32_t box[4] = {(cuuint32_t)kBN, (cuuint32_t)P.pwx, 1u, 1u};
+        if (encode_tiled(&xmap, Elem<T>::kTmaType, 4, const_cast<void*>(p.x), dims, strides, box) !=
+            CUDA_SUCCESS)
+            return cudaErrorNotSupported;
+    }
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)p.C, (cuuint64_t)p.OW, (cuuint64_t)p.OH, (cuuint64_t)p.N};
+        const cuuint64_t strides[3] = {(cuuint64_t)p.C * e, (cuuint64_t)p.OW * p.C * e,
+                                       (cuuint64_t)p.OH * p.OW * p.C * e};
+        const cuuint32_t box[4] = {(cuuint32_t)kBN, (cuuint32_t)P.owp, 1u, 1u};
+        if (encode_tiled(&ymap, Elem<T>::kTmaType, 4, const_cast<void*>(p.dy), dims, strides, box) !=
+            CUDA_SUCCESS)
+            return cudaErrorNotSupported;
+    }
+    FgradArgs a;
+    a.part = p.workspace;
+    a.status = p.status;
+    a.N = p.N; a.OH = p.OH; a.C = p.C; a.pad = p.pad;
+    a.nwf = P.nwf; a.nwc = P.nwc; a.fhc = P.fhc; a.chunks = P.chunks; a.cblocks = P.cblocks;
+    a.Z = P.Z; a.rows_per_slice = P.rows_per_slice; a.nblocks = P.nblocks; a.bps = P.bps;
+    a.nx = P.nx; a.ny = P.ny; a.x_bytes = P.x_bytes; a.y_bytes = P.y_bytes; a.y_off = P.y_off;
+
+    auto kern = fgrad_kernel<T, FH, FW>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               device_info().max_smem_optin);
+        if (err != cudaSuccess) return err;
+        attr_set = true;
+    }
+    const int threads = (P.nwf * P.nwc + 1) * 32;
+    const unsigned grid = static_cast<unsigned>(P.Z) * P.cblocks * P.chunks;
+    kern<<<grid, threads, P.smem, p.stream>>>(xmap, ymap, a);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_reduce_slices(p.workspace, P.Z, static_cast<size_t>(FH) * FW * p.C, p.dw, p.stream);
+}
+
+template <int FH, int FW>
+size_t fgrad_workspace_inst(int N, int OH, int OW, int C, int e) {
+    FgradPlan<FH, FW> P;
+    if (!fgrad_plan<FH, FW>(N, OH, OW, C, e, P)) return 0;
+    return static_cast<size_t>(P.Z) * FH * FW * static_cast<size_t>(C);
+}
+
+#define DWC_FGRAD_FILTERS(X) X(3) X(5) X(7) X(9) X(11) X(13) X(15) X(17) X(19) X(21) X(23) X(25) X(27) X(29) X(31)
+
+template <typename T>
+cudaError_t launch_fgrad_dispatch(const FilterGrad& p) {
+    if (p.FH != p.FW) return cudaErrorNotSupported;
+    switch (p.FH) {
+#define DWC_FGRAD_CASE(F) \
+    case F:               \
+        return launch_fgrad_inst<T, F, F>(p);
+        DWC_FGRAD_FILTERS(DWC_FGRAD_CASE)
+#undef DWC_FGRAD_CASE
+        default:
+            return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace dwc
+

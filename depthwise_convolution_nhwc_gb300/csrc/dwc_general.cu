@@ -1,0 +1,198 @@
+// dwc_general.cu -- fallback kernels for any stride, channel count, alignment or filter
+// size, and the fixed-order reduction of filter-gradient slices.
+//
+// These follow the definitions directly ("Flash-DWC: Making Depthwise Convolution
+// Compute-Efficient on GPUs", §2.1 / Fig. 1 for the forward pass, §5.1 for the two backward
+// passes) with one thread per output element and fp32 accumulation; they serve the shapes
+// the row-streaming kernels do not cover (strides above 1, odd channel counts, unaligned
+// pointers, even or very large filters).
+#include <algorithm>
+
+#include "dwc_device.cuh"
+#include "dwc_host.h"
+
+namespace dwc {
+
+template <typename T>
+__global__ void general_fwd_kernel(const T* __restrict__ x, const T* __restrict__ w,
+                                   float* __restrict__ y, int N, int H, int W, int C, int OH,
+                                   int OW, int FH, int FW, int s, int p) {
+    const long long total = static_cast<long long>(N) * OH * OW * C;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        long long q = i;
+        const int c = static_cast<int>(q % C); q /= C;
+        const int ow = static_cast<int>(q % OW); q /= OW;
+        const int oh = static_cast<int>(q % OH); q /= OH;
+        const int n = static_cast<int>(q);
+        float acc = 0.f;
+        for (int fh = 0; fh < FH; ++fh) {
+            const int ih = oh * s + fh - p;
+            if (ih < 0 || ih >= H) continue;
+            for (int fw = 0; fw < FW; ++fw) {
+                const int iw = ow * s + fw - p;
+                if (iw < 0 || iw >= W) continue;
+                acc = fmaf(to_f32(x[((static_cast<size_t>(n) * H + ih) * W + iw) * C + c]),
+                           to_f32(w[(static_cast<size_t>(fh) * FW + fw) * C + c]), acc);
+            }
+        }
+        y[i] = acc;
+    }
+}
+
+// dx[n, ih, iw, c] = sum over taps whose forward product read x[n, ih, iw, c].
+template <typename T>
+__global__ void general_bwd_data_kernel(const T* __restrict__ dy, const T* __restrict__ w,
+                                        float* __restrict__ dx, int N, int H, int W, int C,
+                                        int OH, int OW, int FH, int FW, int s, int p) {
+    const long long total = static_cast<long long>(N) * H * W * C;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        long long q = i;
+        const int c = static_cast<int>(q % C); q /= C;
+        const int iw = static_cast<int>(q % W); q /= W;
+        const int ih = static_cast<int>(q % H); q /= H;
+        const int n = static_cast<int>(q);
+        float acc = 0.f;
+        for (int fh = 0; fh < FH; ++fh) {
+            const int th = ih + p - fh;
+            if (th < 0 || th % s) continue;
+            const int oh = th / s;
+            if (oh >= OH) continue;
+            for (int fw = 0; fw < FW; ++fw) {
+                const int tw = iw + p - fw;
+                if (tw < 0 || tw % s) continue;
+                const int ow = tw / s;
+                if (ow >= OW) continue;
+                acc = fmaf(to_f32(dy[((static_cast<size_t>(n) * OH + oh) * OW + ow) * C + c]),
+                           to_f32(w[(static_cast<size_t>(fh) * FW + fw) * C + c]), acc);
+            }
+        }
+        dx[i] = acc;
+    }
+}
+
+// part[z, fh, fw, c] = sum over output rows of slice z of x * dy.
+template <typename T>
+__global__ void general_bwd_filter_kernel(const T* __restrict__ x, const T* __restrict__ dy,
+                                          float* __restrict__ part, int N, int H, int W, int C,
+                                          int OH, int OW, int FH, int FW, int s, int p,
+                                          int rows_per_slice, int Z) {
+    const long long per_z = static_cast<long long>(FH) * FW * C;
+    const long long total = per_z * Z;
+    const long long rows = static_cast<long long>(N) * OH;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int z = static_cast<int>(i / per_z);
+        long long q = i % per_z;
+        const int c = static_cast<int>(q % C); q /= C;
+        const int fw = static_cast<int>(q % FW); q /= FW;
+        const int fh = static_cast<int>(q);
+        float acc = 0.f;
+        const long long r1 = std::min<long long>(static_cast<long long>(z + 1) * rows_per_slice, rows);
+        for (long long r = static_cast<long long>(z) * rows_per_slice; r < r1; ++r) {
+            const int n = static_cast<int>(r / OH), oh = static_cast<int>(r % OH);
+            const int ih = oh * s + fh - p;
+            if (ih < 0 || ih >= H) continue;
+            for (int ow = 0; ow < OW; ++ow) {
+                const int iw = ow * s + fw - p;
+                if (iw < 0 || iw >= W) continue;
+                acc = fmaf(to_f32(x[((static_cast<size_t>(n) * H + ih) * W + iw) * C + c]),
+                           to_f32(dy[((static_cast<size_t>(n) * OH + oh) * OW + ow) * C + c]), acc);
+            }
+        }
+        part[i] = acc;
+    }
+}
+
+__global__ void reduce_slices_kernel(const float* __restrict__ part, int slices, size_t count,
+                                     float* __restrict__ out) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < count;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        float s = 0.f;
+        for (int z = 0; z < slices; ++z) s += part[static_cast<size_t>(z) * count + i];
+        out[i] = s;
+    }
+}
+
+cudaError_t launch_reduce_slices(const float* part, int slices, size_t count, float* out,
+                                 cudaStream_t stream) {
+    if (count == 0) return cudaSuccess;
+    const int threads = 256;
+    const size_t blocks = std::min<size_t>((count + threads - 1) / threads,
+                                           static_cast<size_t>(device_info().sm_count) * 8);
+    reduce_slices_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(part, slices,
+                                                                               count, out);
+    return cudaGetLastError();
+}
+
+static unsigned grid_for(long long total, int threads) {
+    const long long cap = static_cast<long long>(device_info().sm_count) * 16;
+    return static_cast<unsigned>(std::max<long long>(1, std::min(cap, (total + threads - 1) / threads)));
+}
+
+template <typename T>
+static cudaError_t general_fwd_t(const GeneralConv& p) {
+    const long long total = static_cast<long long>(p.N) * p.OH * p.OW * p.C;
+    if (total == 0) return cudaSuccess;
+    general_fwd_kernel<T><<<grid_for(total, 256), 256, 0, p.stream>>>(
+        static_cast<const T*>(p.a), static_cast<const T*>(p.b), p.out, p.N, p.H, p.W, p.C, p.OH,
+        p.OW, p.FH, p.FW, p.stride, p.pad);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t general_bwd_data_t(const GeneralConv& p) {
+    const long long total = static_cast<long long>(p.N) * p.H * p.W * p.C;
+    if (total == 0) return cudaSuccess;
+    general_bwd_data_kernel<T><<<grid_for(total, 256), 256, 0, p.stream>>>(
+        static_cast<const T*>(p.a), static_cast<const T*>(p.b), p.out, p.N, p.H, p.W, p.C, p.OH,
+        p.OW, p.FH, p.FW, p.stride, p.pad);
+    return cudaGetLastError();
+}
+
+static int general_slices(int N, int OH, int C, int FH, int FW) {
+    const long long outs = static_cast<long long>(FH) * FW * C;
+    const long long target = static_cast<long long>(device_info().sm_count) * 1024;
+    long long z = (target + outs - 1) / std::max<long long>(outs, 1);
+    const long long rows = static_cast<long long>(N) * OH;
+    z = std::max<long long>(1, std::min<long long>(z, std::max<long long>(rows, 1)));
+    return static_cast<int>(z);
+}
+
+size_t general_bwd_filter_workspace_floats(int N, int OH, int C, int FH, int FW) {
+    return static_cast<size_t>(general_slices(N, OH, C, FH, FW)) * FH * FW * C;
+}
+
+template <typename T>
+static cudaError_t general_bwd_filter_t(const GeneralConv& p) {
+    const size_t count = static_cast<size_t>(p.FH) * p.FW * p.C;
+    if (count == 0) return cudaSuccess;
+    const long long rows = static_cast<long long>(p.N) * p.OH;
+    if (rows == 0 || p.OW == 0) return cudaMemsetAsync(p.out, 0, count * sizeof(float), p.stream);
+    int Z = general_slices(p.N, p.OH, p.C, p.FH, p.FW);
+    const int rps = static_cast<int>((rows + Z - 1) / Z);
+    Z = static_cast<int>((rows + rps - 1) / rps);
+    if (p.workspace == nullptr || p.workspace_floats < count * Z) return cudaErrorInvalidValue;
+    const long long total = static_cast<long long>(count) * Z;
+    general_bwd_filter_kernel<T><<<grid_for(total, 256), 256, 0, p.stream>>>(
+        static_cast<const T*>(p.a), static_cast<const T*>(p.b), p.workspace, p.N, p.H, p.W, p.C,
+        p.OH, p.OW, p.FH, p.FW, p.stride, p.pad, rps, Z);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_reduce_slices(p.workspace, Z, count, p.out, p.stream);
+}
+
+#define DWC_BY_DTYPE(fn, p)                                         \
+    switch ((p).dtype) {                                            \
+        case kF32: return fn<float>(p);                             \
+        case kBF16: return fn<__nv_bfloat16>(p);                    \
+        case kF16: return fn<__half>(p);                            \
+        default: return cudaErrorInvalidValue;                      \
+    }
+
+cudaError_t launch_general_fwd(const GeneralConv& p) { DWC_BY_DTYPE(general_fwd_t, p) }
+cudaError_t launch_general_bwd_data(const GeneralConv& p) { DWC_BY_DTYPE(general_bwd_data_t, p) }
+cudaError_t launch_general_bwd_filter(const GeneralConv& p) { DWC_BY_DTYPE(general_bwd_filter_t, p) }
+
+}  // namespace dwc

@@ -1,0 +1,101 @@
+// dwc_host.h -- internal host-side interface between the C ABI and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dwc {
+
+enum ElemType { kF32 = 0, kBF16 = 1, kF16 = 2 };
+
+inline int elem_bytes(int t) { return t == kF32 ? 4 : 2; }
+
+// One stride-1 convolution over channels-last tensors, as the row-streaming kernel sees it:
+//   out[n, oh, ow, c] = sum_{fh, fw} in[n, oh + fh - pad_h, ow + fw - pad_w, c] * filt(fh, fw, c)
+// with filt(fh, fw, c) = w[fh, fw, c], or w[FH-1-fh, FW-1-fw, c] when flip is set
+// (backward data).  in is N x H x W x C, out is N x OH x OW x C (fp32), w is FH x FW x C.
+struct RowConv {
+    const void* in;
+    const void* w;
+    float* out;
+    int N, H, W, C;
+    int OH, OW;
+    int FH, FW;
+    int pad_h, pad_w;
+    bool flip;
+    int dtype;
+    cudaStream_t stream;
+    unsigned int* status;
+};
+
+// Filter-gradient problem: dw[fh, fw, c] = sum_{n,oh,ow} x[n, oh+fh-pad, ow+fw-pad, c] * dy[n,oh,ow,c].
+struct FilterGrad {
+    const void* x;
+    const void* dy;
+    float* dw;
+    int N, H, W, C;
+    int OH, OW;
+    int FH, FW;
+    int pad;
+    int dtype;
+    float* workspace;        // partial sums, see filter_grad_workspace_floats
+    size_t workspace_floats;
+    cudaStream_t stream;
+    unsigned int* status;
+};
+
+// General problem for the fallback kernels (any stride, any channel count or alignment).
+struct GeneralConv {
+    const void* a;     // x (fwd, bwd_filter) or dy (bwd_data)
+    const void* b;     // w (fwd, bwd_data) or dy (bwd_filter)
+    float* out;
+    int N, H, W, C;    // forward input dims
+    int OH, OW;
+    int FH, FW;
+    int stride, pad;
+    int dtype;
+    float* workspace;
+    size_t workspace_floats;
+    cudaStream_t stream;
+};
+
+// Device properties cached per device.
+struct DeviceInfo {
+    int sm_count;
+    int max_smem_optin;
+};
+const DeviceInfo& device_info();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda needed).
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* base,
+                      const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+                      const cuuint32_t* box);
+
+// Row-streaming kernels (stride 1, C even, 16-byte aligned tensors, filter sizes with a
+// compiled instantiation).  Return cudaErrorNotSupported when no instantiation fits.
+cudaError_t launch_rows_f32(const RowConv& p);
+cudaError_t launch_rows_bf16(const RowConv& p);
+cudaError_t launch_rows_f16(const RowConv& p);
+bool rows_supported(int FH, int FW);
+
+cudaError_t launch_filter_grad_f32(const FilterGrad& p);
+cudaError_t launch_filter_grad_bf16(const FilterGrad& p);
+cudaError_t launch_filter_grad_f16(const FilterGrad& p);
+bool filter_grad_supported(int FH, int FW);
+// Workspace floats the filter-gradient kernel needs (0 if it cannot run this shape).
+size_t filter_grad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int elem_bytes);
+
+// Fallback kernels.
+cudaError_t launch_general_fwd(const GeneralConv& p);
+cudaError_t launch_general_bwd_data(const GeneralConv& p);
+cudaError_t launch_general_bwd_filter(const GeneralConv& p);
+size_t general_bwd_filter_workspace_floats(int N, int OH, int C, int FH, int FW);
+
+// Deterministic fixed-order sum of `slices` partial filter gradients laid out as
+// [slices][count] into out[count].
+cudaError_t launch_reduce_slices(const float* part, int slices, size_t count, float* out,
+                                 cudaStream_t stream);
+
+}  // namespace dwc

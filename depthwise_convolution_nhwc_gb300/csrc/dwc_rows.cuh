@@ -1,0 +1,371 @@
+// dwc_rows.cuh -- row-streaming depthwise convolution kernel (forward and backward data).
+//
+// Computes, for stride 1,
+//   out[n, oh, ow, c] = sum_{fh < FH, fw < FW} in[n, oh + fh - pad_h, ow + fw - pad_w, c] * filt(fh, fw, c)
+// over channels-last tensors ("Flash-DWC: Making Depthwise Convolution Compute-Efficient on
+// GPUs", §2.1 / Fig. 1 for the operation, §2.3 for the unified channels-last layout).  For
+// backward data, filt(fh, fw, c) = w[FH-1-fh, FW-1-fw, c] (the 180-degree rotation of §5.1),
+// folded into the filter index so no rotated copy of w is ever written.
+//
+// Design (GB300 restatement of the §3 dataflow, not a copy of it):
+//  * Work unit = (image n, block of 64 channels, band of R output rows, tile of TW = nwc*TM
+//    output columns) -- the output tiling of §3.1 with BN = 64 channels.  A persistent grid
+//    walks the units; the band index is fastest so that CTAs running at the same time read
+//    overlapping input rows out of L2.
+//  * One producer warp streams, per unit, the R + FH - 1 input rows of the band (each a
+//    64-channel x (TW + FW - 1)-pixel box) and the filter rows through a ring of shared
+//    memory stages with TMA.  Out-of-image rows, columns and channels arrive zero-filled,
+//    which is the zero padding (the predicated loads of §4.4 become TMA bounds handling).
+//  * Each compute lane owns two adjacent channels (one packed fp32x2 FMA per tap) and a
+//    block of R rows x TM columns of outputs in registers.  Input rows are consumed in order;
+//    every input element is loaded from shared memory once and used for up to R*FW taps
+//    (width-first reuse inside a row, §3.3, plus reuse across the R output rows the lane
+//    holds).  The filter rows in use live in registers as a window of R rows that slides
+//    by one row per input row (filter reuse across TM*R outputs, §3.2).
+//  * 16-bit inputs are widened to fp32 once per shared-memory load, not per FMA (§4.1).
+#pragma once
+
+#include <utility>
+
+#include "dwc_device.cuh"
+#include "dwc_host.h"
+
+namespace dwc {
+
+constexpr int kBN = 64;                 // channels per work unit (32 lanes x 2)
+constexpr int kMaxComputeWarps = 8;
+constexpr int kRowsMaxThreads = (kMaxComputeWarps + 1) * 32;
+
+// Register tile per filter size: R output rows x TM output columns per lane.
+template <int FH, int FW>
+struct RowsTile {
+    static constexpr int R = (FH <= 9) ? 4 : (FH <= 15 ? 2 : 1);
+    static constexpr int TM = (FH <= 9) ? 8 : (FH <= 15 ? 16 : 32);
+};
+
+struct RowsArgs {
+    float* out;
+    unsigned int* status;
+    int OH, OW, C;
+    int pad_h, pad_w;
+    int nwc;              // compute warps per CTA
+    int ns;               // pipeline stages
+    int cblocks, bands, ctiles;
+    long long units;
+    uint32_t x_bytes;     // bytes of one staged input row box
+    uint32_t w_bytes;     // bytes of one staged filter row box
+    uint32_t stage_stride;
+};
+
+template <int I>
+using IntC = std::integral_constant<int, I>;
+
+template <class F, int... Is>
+__device__ __forceinline__ void static_for_impl(F&& f, std::integer_sequence<int, Is...>) {
+    (f(IntC<Is>{}), ...);
+}
+
+template <int N, class F>
+__device__ __forceinline__ void static_for(F&& f) {
+    static_for_impl(f, std::make_integer_sequence<int, N>{});
+}
+
+// Valid output rows r of the lane's band for input row i: 0 <= i - r < FH.
+template <int R, int FH>
+__host__ __device__ constexpr unsigned valid_rows(int i) {
+    unsigned m = 0;
+    for (int r = 0; r < R; ++r)
+        if (i - r >= 0 && i - r < FH) m |= 1u << r;
+    return m;
+}
+
+// Accumulate one staged input row into the lane's R x TM outputs.
+template <typename T, int FW, int R, int TM, unsigned MASK>
+__device__ __forceinline__ void consume_row(const T* __restrict__ xs, float2 (&acc)[R][TM],
+                                            const float2 (&wwin)[R][FW]) {
+#pragma unroll
+    for (int j = 0; j < TM + FW - 1; ++j) {
+        const float2 x = Elem<T>::load_pair(xs + j * kBN);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (!((MASK >> r) & 1u)) continue;
+#pragma unroll
+            for (int fw = 0; fw < FW; ++fw) {
+                const int t = j - fw;
+                if (t >= 0 && t < TM) fma2(acc[r][t], x, wwin[r][fw]);
+            }
+        }
+    }
+}
+
+template <typename T, int FH, int FW, bool FLIP>
+__global__ void __launch_bounds__(kRowsMaxThreads, 1)
+rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+            const RowsArgs a) {
+    constexpr int R = RowsTile<FH, FW>::R;
+    constexpr int TM = RowsTile<FH, FW>::TM;
+    constexpr int S = R + FH - 1;  // input rows per band
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + a.ns;
+    unsigned char* stages = smem + 128;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.ns; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], a.nwc);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int TW = a.nwc * TM;
+
+    // ---------------- producer warp: TMA streaming of input and filter rows -------------
+    if (warp == a.nwc) {
+        if (lane != 0) return;
+        prefetch_tensormap(&xmap);
+        prefetch_tensormap(&wmap);
+        long long k = 0;
+        bool ok = true;
+        for (long long u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            long long q = u;
+            const int band = static_cast<int>(q % a.bands); q /= a.bands;
+            const int ct = static_cast<int>(q % a.ctiles); q /= a.ctiles;
+            const int cb = static_cast<int>(q % a.cblocks); q /= a.cblocks;
+            const int n = static_cast<int>(q);
+            const int oh0 = band * R, ow0 = ct * TW;
+            for (int i = 0; i < S; ++i, ++k) {
+                const int slot = static_cast<int>(k % a.ns);
+                const long long use = k / a.ns;
+                if (use > 0 && !mbar_wait(&empty[slot], static_cast<uint32_t>((use - 1) & 1))) {
+                    record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                unsigned char* st = stages + static_cast<size_t>(slot) * a.stage_stride;
+                const bool wrow = i < FH;
+                mbar_arrive_expect_tx(&full[slot], a.x_bytes + (wrow ? a.w_bytes : 0u));
+                tma_load_4d(st, &xmap, &full[slot], cb * kBN, ow0 - a.pad_w, oh0 - a.pad_h + i, n);
+                if (wrow)
+                    tma_load_3d(st + a.x_bytes, &wmap, &full[slot], cb * kBN, 0,
+                                FLIP ? FH - 1 - i : i);
+            }
+        }
+        // Never leave the CTA with copies in flight: wait (bounded) for the last stages.
+        const long long first = k > a.ns ? k - a.ns : 0;
+        for (long long j = first; j < k; ++j)
+            if (!mbar_wait(&full[j % a.ns], static_cast<uint32_t>((j / a.ns) & 1))) {
+                record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+                break;
+            }
+        return;
+    }
+
+    // ---------------- compute warps ----------------------------------------------------
+    const int wc = warp;
+    long long k = 0;
+    for (long long u = blockIdx.x; u < a.units; u += gridDim.x) {
+        long long q = u;
+        const int band = static_cast<int>(q % a.bands); q /= a.bands;
+        const int ct = static_cast<int>(q % a.ctiles); q /= a.ctiles;
+        const int cb = static_cast<int>(q % a.cblocks); q /= a.cblocks;
+        const int n = static_cast<int>(q);
+        const int oh0 = band * R;
+        const int owl = ct * TW + wc * TM;  // first output column of this lane
+        const int c = cb * kBN + 2 * lane;
+
+        float2 acc[R][TM];
+        float2 wwin[R][FW];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+#pragma unroll
+            for (int t = 0; t < TM; ++t) acc[r][t] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int f = 0; f < FW; ++f) wwin[r][f] = make_float2(0.f, 0.f);
+        }
+
+        bool ok = true;
+        // Wait for stage k, slide the filter window by one row, return the row pointers.
+        auto begin_row = [&](int i, const T*& xs) -> bool {
+            const int slot = static_cast<int>(k % a.ns);
+            if (!mbar_wait(&full[slot], static_cast<uint32_t>((k / a.ns) & 1))) {
+                record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+                return false;
+            }
+            const unsigned char* st = stages + static_cast<size_t>(slot) * a.stage_stride;
+#pragma unroll
+            for (int r = R - 1; r > 0; --r)
+#pragma unroll
+                for (int f = 0; f < FW; ++f) wwin[r][f] = wwin[r - 1][f];
+            if (i < FH) {
+                const T* ws = reinterpret_cast<const T*>(st + a.x_bytes) + 2 * lane;
+#pragma unroll
+                for (int f = 0; f < FW; ++f)
+                    wwin[0][f] = Elem<T>::load_pair(ws + (FLIP ? FW - 1 - f : f) * kBN);
+            }
+            xs = reinterpret_cast<const T*>(st) + (wc * TM) * kBN + 2 * lane;
+            return true;
+        };
+        auto end_row = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[k % a.ns]);
+            ++k;
+        };
+
+        // prologue: input rows 0 .. R-2 (not every output row of the band is reached yet)
+        static_for<R - 1>([&](auto I) {
+            constexpr int i = decltype(I)::value;
+            if (!ok) return;
+            const T* xs;
+            if (!begin_row(i, xs)) { ok = false; return; }
+            consume_row<T, FW, R, TM, valid_rows<R, FH>(i)>(xs, acc, wwin);
+            end_row();
+        });
+        // steady state: every output row of the band takes this input row
+#pragma unroll 1
+        for (int i = R - 1; i < FH && ok; ++i) {
+            const T* xs;
+            if (!begin_row(i, xs)) { ok = false; break; }
+            consume_row<T, FW, R, TM, (1u << R) - 1u>(xs, acc, wwin);
+            end_row();
+        }
+        // epilogue: input rows FH .. FH+R-2 (the top output rows are complete)
+        constexpr int E0 = (FH > R - 1) ? FH : R - 1;
+        static_for<S - E0>([&](auto I) {
+            constexpr int i = E0 + decltype(I)::value;
+            if (!ok) return;
+            const T* xs;
+            if (!begin_row(i, xs)) { ok = false; return; }
+            consume_row<T, FW, R, TM, valid_rows<R, FH>(i)>(xs, acc, wwin);
+            end_row();
+        });
+        if (!ok) return;
+
+        if (c < a.C) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int oh = oh0 + r;
+                if (oh >= a.OH) break;
+                float* row = a.out + ((static_cast<size_t>(n) * a.OH + oh) * a.OW) * a.C + c;
+#pragma unroll
+                for (int t = 0; t < TM; ++t) {
+                    const int ow = owl + t;
+                    if (ow < a.OW) store_pair_streaming(row + static_cast<size_t>(ow) * a.C, acc[r][t]);
+                }
+            }
+        }
+    }
+}
+
+template <typename T, int FH, int FW, bool FLIP>
+cudaError_t launch_rows_inst(const RowConv& p) {
+    constexpr int TM = RowsTile<FH, FW>::TM;
+    const int e = static_cast<int>(sizeof(T));
+    const DeviceInfo& dev = device_info();
+
+    // compute warps side by side along the row; the staged box (TW + FW - 1 pixels) must
+    // stay within the TMA box limit of 256
+    const int nwc = std::min(std::min(kMaxComputeWarps, (p.OW + TM - 1) / TM), (257 - FW) / TM);
+    if (nwc < 1) return cudaErrorNotSupported;
+    const int TW = nwc * TM;
+    const int TWH = TW + FW - 1;
+
+    CUtensorMap xmap, wmap;
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)p.C, (cuuint64_t)p.W, (cuuint64_t)p.H,
+                                    (cuuint64_t)p.N};
+        const cuuint64_t strides[3] = {(cuuint64_t)p.C * e, (cuuint64_t)p.W * p.C * e,
+                                       (cuuint64_t)p.H * p.W * p.C * e};
+        const cuuint32_t box[4] = {(cuuint32_t)kBN, (cuuint32_t)TWH, 1u, 1u};
+        if (encode_tiled(&xmap, Elem<T>::kTmaType, 4, const_cast<void*>(p.in), dims, strides,
+                         box) != CUDA_SUCCESS)
+            return cudaErrorNotSupported;  // the caller falls back to the general kernels
+    }
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)p.C, (cuuint64_t)FW, (cuuint64_t)FH};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.C * e, (cuuint64_t)FW * p.C * e};
+        const cuuint32_t box[3] = {(cuuint32_t)kBN, (cuuint32_t)FW, 1u};
+        if (encode_tiled(&wmap, Elem<T>::kTmaType, 3, const_cast<void*>(p.w), dims, strides,
+                         box) != CUDA_SUCCESS)
+            return cudaErrorNotSupported;
+    }
+
+    RowsArgs a;
+    a.out = p.out;
+    a.status = p.status;
+    a.OH = p.OH; a.OW = p.OW; a.C = p.C;
+    a.pad_h = p.pad_h; a.pad_w = p.pad_w;
+    a.nwc = nwc;
+    a.cblocks = (p.C + kBN - 1) / kBN;
+    a.bands = (p.OH + RowsTile<FH, FW>::R - 1) / RowsTile<FH, FW>::R;
+    a.ctiles = (p.OW + TW - 1) / TW;
+    a.units = static_cast<long long>(p.N) * a.cblocks * a.bands * a.ctiles;
+    a.x_bytes = static_cast<uint32_t>(TWH * kBN * e);
+    a.w_bytes = static_cast<uint32_t>(FW * kBN * e);
+    a.stage_stride = (a.x_bytes + a.w_bytes + 127u) & ~127u;
+    if (a.units == 0) return cudaSuccess;
+
+    auto kern = rows_kernel<T, FH, FW, FLIP>;
+    const int threads = (nwc + 1) * 32;
+    static int regs = -1;  // per instantiation
+    if (regs < 0) {
+        cudaFuncAttributes fa;
+        cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+        if (err != cudaSuccess) return err;
+        regs = fa.numRegs;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   dev.max_smem_optin);
+        if (err != cudaSuccess) return err;
+    }
+    // CTAs per SM allowed by registers, then split shared memory between them.
+    const int regs_per_cta = ((regs * 32 + 255) / 256) * 256 * (nwc + 1);
+    int ctas = std::max(1, std::min(65536 / std::max(regs_per_cta, 1), 2048 / threads));
+    int ns = 0;
+    for (; ctas >= 1; --ctas) {
+        const int budget = std::min(dev.max_smem_optin, 233472 / ctas - 1024) - 128;
+        ns = std::min(6, budget / static_cast<int>(a.stage_stride));
+        if (ns >= 2) break;
+    }
+    if (ns < 2) return cudaErrorNotSupported;
+    a.ns = ns;
+    const size_t smem = 128 + static_cast<size_t>(ns) * a.stage_stride;
+    const long long grid = std::min<long long>(a.units, static_cast<long long>(dev.sm_count) * ctas);
+    kern<<<static_cast<unsigned>(grid), threads, smem, p.stream>>>(xmap, wmap, a);
+    return cudaGetLastError();
+}
+
+// Dispatch over the compiled odd square filter sizes.
+template <typename T>
+cudaError_t launch_rows_dispatch(const RowConv& p) {
+    if (p.FH != p.FW) return cudaErrorNotSupported;
+#define DWC_ROWS_CASE(F)                                                              \
+    case F:                                                                           \
+        return p.flip ? launch_rows_inst<T, F, F, true>(p) : launch_rows_inst<T, F, F, false>(p);
+    switch (p.FH) {
+        DWC_ROWS_CASE(3)
+        DWC_ROWS_CASE(5)
+        DWC_ROWS_CASE(7)
+        DWC_ROWS_CASE(9)
+        DWC_ROWS_CASE(11)
+        DWC_ROWS_CASE(13)
+        DWC_ROWS_CASE(15)
+        DWC_ROWS_CASE(17)
+        DWC_ROWS_CASE(19)
+        DWC_ROWS_CASE(21)
+        DWC_ROWS_CASE(23)
+        DWC_ROWS_CASE(25)
+        DWC_ROWS_CASE(27)
+        DWC_ROWS_CASE(29)
+        DWC_ROWS_CASE(31)
+        default:
+            return cudaErrorNotSupported;
+    }
+#undef DWC_ROWS_CASE
+}
+
+}  // namespace dwc

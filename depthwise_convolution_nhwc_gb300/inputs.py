@@ -19,7 +19,7 @@ the filter is FH x FW x C.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 
 import torch
 
@@ -91,7 +91,7 @@ class Case:
 
 
 # The benchmark workloads, named by what they are.
-WORKLOADS = {
+_WORKLOADS = {
     # latency / correctness case: U(-1,1), seed 0
     "fwd_f32_n1_14x14_c32_f3": Case(1, 14, 14, 32, 3, 3, 1, 1, "f32", "uniform", 0),
     # ConvNeXt-stage shape, 7x7 filter
@@ -102,6 +102,7 @@ WORKLOADS = {
     "f32_n64_28x28_c256_f13": Case(64, 28, 28, 256, 13, 13, 1, 6, "f32", "normal", 3),
     "bf16_n64_28x28_c256_f13": Case(64, 28, 28, 256, 13, 13, 1, 6, "bf16", "normal", 3),
 }
+WORKLOADS = {k: replace(v, name=k) for k, v in _WORKLOADS.items()}
 
 SWEEP_FILTERS = (3, 5, 7, 9, 13, 17, 21, 27, 31)
 SWEEP_SHAPES = ((64, 56, 56, 128), (64, 28, 28, 256), (64, 14, 14, 512), (64, 7, 7, 1024))

@@ -1,0 +1,128 @@
+/*
+ * dwc.h -- C ABI of the GB300 depthwise 2-D convolution library (libdwc_gb300.so).
+ *
+ * Operation ("Flash-DWC: Making Depthwise Convolution Compute-Efficient on GPUs",
+ * §2.1 and Fig. 1): every channel c has its own FH x FW filter and
+ *
+ *     Y[n, oh, ow, c] = sum_{fh < FH, fw < FW} X[n, oh*s + fh - p, ow*s + fw - p, c] * W[fh, fw, c]
+ *
+ * with taps outside the image contributing zero (zero padding p on all four sides, one
+ * stride s for both axes), OH = floor((H + 2p - FH) / s) + 1, OW = floor((W + 2p - FW) / s) + 1.
+ * The forward pass is a cross-correlation (no filter flip).
+ *
+ * Layout (§2.3, "unified channels-last layout"), all tensors dense and row-major:
+ *     X, dX : N x H  x W  x C      (input of the forward pass and its gradient)
+ *     Y, dY : N x OH x OW x C      (output of the forward pass and its gradient)
+ *     W, dW : FH x FW x C          (filter and its gradient; channel last)
+ *
+ * Data types: the inputs (X, W, dY) of one call share one dtype (fp32, bf16 or fp16);
+ * every output (Y, dX, dW) is fp32.  All arithmetic is fp32 multiply-add; 16-bit inputs
+ * are widened to fp32 exactly before use.
+ *
+ * Pointers and ownership: every tensor pointer is a DEVICE pointer allocated and owned by
+ * the caller.  Inputs are only read; outputs are overwritten (never accumulated into).
+ * Outputs must not overlap inputs.  Calls are asynchronous on `stream` (0 = legacy default
+ * stream): they enqueue work and return; the caller synchronises.  The library allocates
+ * no device memory in any call.
+ *
+ * Errors: every call validates its arguments on the host and returns a dwc_status_t
+ * without launching anything when they are wrong.  No call aborts or throws.  A CUDA
+ * launch failure is returned as DWC_ERR_CUDA.  Kernels never spin without limit: a wait
+ * inside a kernel that runs out of time sets a device-side status bit and the kernel
+ * ends; dwc_device_status() reports it as DWC_ERR_TIMEOUT.
+ *
+ * Every fp32 tensor must be 4-byte aligned and every 16-bit tensor 2-byte aligned.  The
+ * fast kernels are used when stride == 1, the filter is square with odd FH in [3, 31],
+ * C is a multiple of 4 (fp32) or 8 (16-bit) and all pointers are 16-byte aligned;
+ * everything else runs on the general kernels (same results, slower).
+ */
+#ifndef DWC_GB300_H
+#define DWC_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dwc_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    DWC_F32 = 0,  /* IEEE fp32 inputs */
+    DWC_BF16 = 1, /* bfloat16 inputs, fp32 accumulation and output */
+    DWC_F16 = 2   /* IEEE fp16 inputs, fp32 accumulation and output */
+} dwc_dtype_t;
+
+typedef enum {
+    DWC_OK = 0,
+    DWC_ERR_INVALID_ARG = 1, /* null pointer, negative size, stride < 1, pad < 0, empty filter,
+                                unknown dtype, output does not fit (OH or OW < 1) */
+    DWC_ERR_UNSUPPORTED = 2, /* a size beyond the library's limits (int32 index overflow) */
+    DWC_ERR_ALIGNMENT = 3,   /* a tensor pointer is not aligned to its element size */
+    DWC_ERR_WORKSPACE = 4,   /* workspace missing or smaller than the query says */
+    DWC_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+    DWC_ERR_TIMEOUT = 6      /* a kernel gave up waiting (reported by dwc_device_status) */
+} dwc_status_t;
+
+/* Forward pass Y = DWC(X, W) (§2.1, Fig. 1; §3 and §4 of the paper give the GPU dataflow).
+ *   x : N x H x W x C, dtype      w : FH x FW x C, dtype      y : N x OH x OW x C, fp32 (out)
+ */
+dwc_status_t dwc_fwd(const void* x, const void* w, float* y,
+                     int N, int H, int W, int C, int FH, int FW, int stride, int pad,
+                     dwc_dtype_t dtype, dwc_stream_t stream);
+
+/* Backward data ("BDC", §5.1): dX = the adjoint of the forward pass in X, i.e.
+ *   dX[n, ih, iw, c] = sum over (oh, ow, fh, fw) with oh*s + fh - p = ih and ow*s + fw - p = iw
+ *                      of dY[n, oh, ow, c] * W[fh, fw, c];
+ * for stride 1 this is the forward pass over dY with W rotated by 180 degrees and pad
+ * FH-1-p (the rotation is folded into the kernel's filter indexing; no copy is made).
+ *   dy : N x OH x OW x C, dtype   w : FH x FW x C, dtype   dx : N x H x W x C, fp32 (out)
+ * N, H, W, C, FH, FW, stride, pad describe the FORWARD problem (H, W = forward input size).
+ */
+dwc_status_t dwc_bwd_data(const void* dy, const void* w, float* dx,
+                          int N, int H, int W, int C, int FH, int FW, int stride, int pad,
+                          dwc_dtype_t dtype, dwc_stream_t stream);
+
+/* Bytes of device workspace dwc_bwd_filter needs for this problem on the CURRENT device
+ * (0 means none).  Returns 0 for invalid arguments as well; dwc_bwd_filter then reports the
+ * argument error. */
+size_t dwc_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int FW, int stride,
+                                     int pad, dwc_dtype_t dtype);
+
+/* Backward filter ("BFC", §5.1): dW[fh, fw, c] = sum_{n, oh, ow} X[n, oh*s+fh-p, ow*s+fw-p, c]
+ *                                                             * dY[n, oh, ow, c].
+ * The accumulation axis N*OH*OW is split into slices (§5.1, "accumulation-axis
+ * parallelism"); slice partials go to `workspace` and are summed in a fixed order, so the
+ * result is bit-identical from run to run (no atomics).
+ *   x : N x H x W x C, dtype   dy : N x OH x OW x C, dtype   dw : FH x FW x C, fp32 (out)
+ *   workspace : device buffer of at least dwc_bwd_filter_workspace_size(...) bytes, owned by
+ *               the caller, 16-byte aligned, contents ignored on entry and clobbered.
+ */
+dwc_status_t dwc_bwd_filter(const void* x, const void* dy, float* dw,
+                            int N, int H, int W, int C, int FH, int FW, int stride, int pad,
+                            dwc_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                            dwc_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device status word that the kernels
+ * set when a wait runs out of time.  DWC_OK if no kernel reported a problem since the last
+ * call, DWC_ERR_TIMEOUT if one did, DWC_ERR_CUDA if the synchronisation failed. */
+dwc_status_t dwc_device_status(dwc_stream_t stream);
+
+/* Static text for a status code (never NULL). */
+const char* dwc_status_string(dwc_status_t status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int dwc_version(void);
+
+/* Which kernel family a call with these arguments would use: 1 = fast (row-streaming /
+ * filter-gradient) kernels, 0 = general kernels, -1 = invalid arguments.  `pass` is 0 for
+ * dwc_fwd, 1 for dwc_bwd_data, 2 for dwc_bwd_filter.  Pointer alignment is checked with
+ * the pointers given (they may be NULL to mean "16-byte aligned"). */
+int dwc_path(int pass, const void* a, const void* b, const void* out,
+             int N, int H, int W, int C, int FH, int FW, int stride, int pad, dwc_dtype_t dtype);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DWC_GB300_H */

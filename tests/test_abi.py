@@ -1,0 +1,110 @@
+"""C ABI checks that need no GPU: the library loads, exports every symbol include/dwc.h
+declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import depthwise_convolution_nhwc_gb300 as dwc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dwc.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(dwc.LIB_PATH):
+        dwc.build()
+    return dwc.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dwc_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(dwc.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_refuses_missing_path(tmp_path):
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        dwc.load_library(str(tmp_path / "nope.so"))
+
+
+def test_status_strings_and_version(lib):
+    assert lib.dwc_version() >= 100
+    for code in range(7):
+        assert lib.dwc_status_string(code)
+    assert lib.dwc_status_string(99) == b"unknown status"
+
+
+GOOD = dict(N=1, H=8, W=8, C=16, FH=3, FW=3, stride=1, pad=1, dtype=0)
+FAKE = 0x10000  # never dereferenced: every case below fails validation first
+
+
+def call_fwd(lib, x=FAKE, w=FAKE, y=FAKE, **kw):
+    a = dict(GOOD, **kw)
+    return lib.dwc_fwd(x, w, y, a["N"], a["H"], a["W"], a["C"], a["FH"], a["FW"], a["stride"],
+                       a["pad"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw", [dict(dtype=7), dict(N=-1), dict(C=-2), dict(H=0), dict(W=0),
+                                dict(FH=0), dict(FW=0), dict(stride=0), dict(pad=-1),
+                                dict(H=2, W=2, FH=7, FW=7, pad=1)])
+def test_invalid_arguments_rejected_on_host(lib, kw):
+    assert call_fwd(lib, **kw) == 1
+    a = dict(GOOD, **kw)
+    assert lib.dwc_bwd_data(FAKE, FAKE, FAKE, a["N"], a["H"], a["W"], a["C"], a["FH"], a["FW"],
+                            a["stride"], a["pad"], a["dtype"], None) == 1
+    assert lib.dwc_bwd_filter(FAKE, FAKE, FAKE, a["N"], a["H"], a["W"], a["C"], a["FH"], a["FW"],
+                              a["stride"], a["pad"], a["dtype"], FAKE, 1 << 20, None) == 1
+    assert lib.dwc_bwd_filter_workspace_size(a["N"], a["H"], a["W"], a["C"], a["FH"], a["FW"],
+                                             a["stride"], a["pad"], a["dtype"]) == 0
+    assert lib.dwc_path(0, None, None, None, a["N"], a["H"], a["W"], a["C"], a["FH"], a["FW"],
+                        a["stride"], a["pad"], a["dtype"]) == -1
+
+
+def test_null_pointers_rejected(lib):
+    assert call_fwd(lib, x=None) == 1
+    assert call_fwd(lib, w=None) == 1
+    assert call_fwd(lib, y=None) == 1
+
+
+def test_misaligned_pointers_rejected(lib):
+    assert call_fwd(lib, x=FAKE + 2) == 3          # fp32 needs 4-byte alignment
+    assert call_fwd(lib, y=FAKE + 1) == 3
+    assert call_fwd(lib, x=FAKE + 1, dtype=1) == 3  # bf16 needs 2-byte alignment
+
+
+def test_size_limits(lib):
+    assert call_fwd(lib, N=1 << 20, H=1 << 12, W=1 << 12, C=1 << 10) == 2
+
+
+def test_workspace_rejected_when_small(lib):
+    a = GOOD
+    code = lib.dwc_bwd_filter(FAKE, FAKE, FAKE, a["N"], a["H"], a["W"], a["C"], a["FH"], a["FW"],
+                              a["stride"], a["pad"], a["dtype"], None, 0, None)
+    assert code == 4
+
+
+def test_path_selection_host_logic(lib):
+    p = lambda pass_, **kw: lib.dwc_path(pass_, None, None, None, *[dict(GOOD, **kw)[k] for k in
+                                          ("N", "H", "W", "C", "FH", "FW", "stride", "pad", "dtype")])
+    assert p(0) == 1 and p(1) == 1
+    assert p(0, stride=2) == 0                 # stride 2 runs on the general kernels
+    assert p(0, FH=4, FW=4) == 0               # even filter
+    assert p(0, FH=3, FW=5) == 0               # non-square filter
+    assert p(0, C=6) == 0                      # fp32 rows must be 16-byte multiples
+    assert p(0, C=8, dtype=1) == 1
+    assert p(0, C=12, dtype=1) == 0            # bf16 needs C % 8 == 0
+    assert p(0, FH=33, FW=33, pad=16, H=40, W=40) == 0
+    # an unaligned (but element-aligned) pointer falls back to the general kernels
+    assert lib.dwc_path(0, FAKE + 4, None, None, 1, 8, 8, 16, 3, 3, 1, 1, 0) == 0

@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element by element,
+on identical seeded inputs.  Full tensors at sizes the oracle finishes in seconds (several
+tiles, ragged tails in every dimension), sampled outputs at the full workload sizes."""
+import numpy as np
+import pytest
+import torch
+
+import depthwise_convolution_nhwc_gb300 as dwc
+import oracle
+from depthwise_convolution_nhwc_gb300.inputs import WORKLOADS, Case, sweep_cases
+from parity_util import TOL, mare, normalized_error
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    dwc.build()
+    dwc.load_library()
+    yield
+    assert dwc.device_status() == 0, "a kernel reported a timed-out wait"
+
+
+def run_all(case: Case, passes=("fwd", "bwd_data", "bwd_filter")):
+    x, w, dy = case.x(), case.w(), case.dy()
+    xd, wd, dyd = x.cuda(), w.cuda(), dy.cuda()
+    out = {}
+    if "fwd" in passes:
+        out["fwd"] = dwc.fwd(xd, wd, case.stride, case.pad)
+    if "bwd_data" in passes:
+        out["bwd_data"] = dwc.bwd_data(dyd, wd, (case.H, case.W), case.stride, case.pad)
+    if "bwd_filter" in passes:
+        out["bwd_filter"] = dwc.bwd_filter(xd, dyd, (case.FH, case.FW), case.stride, case.pad)
+    torch.cuda.synchronize()
+    return x, w, dy, {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def check_full(case: Case, passes=("fwd", "bwd_data", "bwd_filter")):
+    x, w, dy, got = run_all(case, passes)
+    s, p = case.stride, case.pad
+    x, w, dy = (t.double().numpy() for t in (x, w, dy))
+    ax, aw, ady = np.abs(x), np.abs(w), np.abs(dy)
+    for name, g in got.items():
+        if name == "fwd":
+            ref, den = oracle.fwd(x, w, s, p), oracle.fwd(ax, aw, s, p)
+        elif name == "bwd_data":
+            ref = oracle.bwd_data(dy, w, (case.H, case.W), s, p)
+            den = oracle.bwd_data(ady, aw, (case.H, case.W), s, p)
+        else:
+            ref = oracle.bwd_filter(x, dy, (case.FH, case.FW), s, p)
+            den = oracle.bwd_filter(ax, ady, (case.FH, case.FW), s, p)
+        assert g.shape == ref.shape, (name, g.shape, ref.shape)
+        err = normalized_error(g, ref, den)
+        assert err <= TOL[case.dtype], f"{name} {case}: normalized error {err:.3e} (MARE {mare(g, ref):.2e})"
+
+
+def C_(N, H, W, C, F, s=1, p=None, dtype="f32", seed=7, FW=None):
+    FW = F if FW is None else FW
+    return Case(N, H, W, C, F, FW, s, (F - 1) // 2 if p is None else p, dtype, "normal", seed)
+
+
+# Fast-path cases: several column tiles, ragged widths/heights, channel blocks with a tail.
+FAST = [
+    C_(2, 17, 19, 64, 3),
+    C_(1, 23, 37, 128, 7),
+    C_(2, 9, 70, 96, 5),            # two column tiles, channel tail of 32
+    C_(1, 14, 14, 32, 3, p=1),      # fewer channels than one block
+    C_(3, 11, 13, 8, 9),            # 8 channels
+    C_(1, 30, 30, 64, 13),
+    C_(1, 21, 45, 64, 17),
+    C_(1, 40, 33, 64, 31),          # largest filter, ragged
+    C_(2, 7, 7, 128, 31),           # filter much larger than the map
+    C_(1, 12, 300, 64, 7),          # wide rows: several column tiles
+    C_(1, 9, 9, 64, 5, p=0),        # no padding
+    C_(1, 9, 9, 64, 5, p=4),        # padding larger than (F-1)/2
+    C_(1, 1, 1, 64, 3),             # single pixel
+    C_(2, 5, 40, 64, 11),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("case", FAST, ids=lambda c: f"n{c.N}_{c.H}x{c.W}_c{c.C}_f{c.FH}_p{c.pad}")
+def test_fast_path_full_tensors(case, dtype):
+    case = Case(**{**case.__dict__, "dtype": dtype})
+    if dtype != "f32" and case.C % 8:
+        pytest.skip("16-bit fast path needs C % 8 == 0")
+    assert dwc.path("fwd", None, None, None, case.N, case.H, case.W, case.C, case.FH, case.FW,
+                    case.stride, case.pad, {"f32": 0, "bf16": 1, "f16": 2}[dtype]) == 1
+    check_full(case)
+
+
+# General-kernel cases: strides, even/non-square filters, odd channel counts.
+GENERAL = [
+    C_(2, 9, 11, 5, 3, s=2, p=1),
+    C_(1, 12, 10, 6, 4, p=1),
+    C_(2, 8, 9, 3, 3, FW=5, p=1),
+    C_(1, 10, 10, 7, 5, s=3, p=2),
+    C_(1, 6, 6, 16, 33, p=16),
+    C_(1, 8, 8, 12, 7, dtype="bf16"),
+]
+
+
+@pytest.mark.parametrize("case", GENERAL, ids=lambda c: f"s{c.stride}_f{c.FH}x{c.FW}_c{c.C}_{c.dtype}")
+def test_general_path_full_tensors(case):
+    check_full(case)
+
+
+def test_unaligned_pointers_use_general_path_correctly():
+    case = C_(1, 9, 10, 16, 5)
+    x, w, dy = case.x(), case.w(), case.dy()
+    # offset every tensor by one element inside a larger buffer: element-aligned, not 16-B
+    def shifted(t):
+        buf = torch.zeros(t.numel() + 1, dtype=t.dtype, device="cuda")
+        v = buf[1:].view(t.shape)
+        v.copy_(t.cuda())
+        return v
+    xd, wd, dyd = shifted(x), shifted(w), shifted(dy)
+    y = dwc.fwd(xd, wd, 1, case.pad)
+    dw = dwc.bwd_filter(xd, dyd, (5, 5), 1, case.pad)
+    torch.cuda.synchronize()
+    assert normalized_error(y.cpu().numpy(), oracle.fwd(x, w, 1, 2),
+                            oracle.fwd(x.abs(), w.abs(), 1, 2)) <= TOL["f32"]
+    assert normalized_error(dw.cpu().numpy(), oracle.bwd_filter(x, dy, (5, 5), 1, 2),
+                            oracle.bwd_filter(x.abs(), dy.abs(), (5, 5), 1, 2)) <= TOL["f32"]
+
+
+def test_delta_filter_is_identity_bit_exact():
+    for dt in ("f32", "bf16"):
+        case = C_(2, 13, 21, 64, 7, dtype=dt)
+        x = case.x().cuda()
+        w = torch.zeros(7, 7, 64, dtype=x.dtype, device="cuda")
+        w[3, 3] = 1
+        y = dwc.fwd(x, w, 1, 3)
+        assert torch.equal(y, x.float())
+        dx = dwc.bwd_data(x, w, (13, 21), 1, 3)
+        assert torch.equal(dx, x.float())
+
+
+def test_bwd_filter_is_deterministic():
+    case = C_(4, 28, 28, 128, 13)
+    x, dy = case.x().cuda(), case.dy().cuda()
+    a = dwc.bwd_filter(x, dy, (13, 13), 1, 6).clone()
+    for _ in range(3):
+        b = dwc.bwd_filter(x, dy, (13, 13), 1, 6)
+        assert torch.equal(a, b)
+
+
+def test_outputs_do_not_write_outside_their_buffers():
+    """Canary bytes around every output buffer stay untouched (bounds check of the stores)."""
+    case = C_(2, 11, 19, 96, 7)
+    x, w, dy = case.x().cuda(), case.w().cuda(), case.dy().cuda()
+    pad = 4096
+    for name, shape in (("fwd", (2, 11, 19, 96)), ("bwd_data", (2, 11, 19, 96)), ("bwd_filter", (7, 7, 96))):
+        n = int(np.prod(shape))
+        buf = torch.full((n + 2 * pad,), 1234.5, dtype=torch.float32, device="cuda")
+        out = buf[pad:pad + n].view(shape)
+        if name == "fwd":
+            dwc.fwd(x, w, 1, 3, out=out)
+        elif name == "bwd_data":
+            dwc.bwd_data(dy, w, (11, 19), 1, 3, out=out)
+        else:
+            dwc.bwd_filter(x, dy, (7, 7), 1, 3, out=out)
+        torch.cuda.synchronize()
+        assert torch.all(buf[:pad] == 1234.5) and torch.all(buf[pad + n:] == 1234.5), name
+
+
+def test_empty_batch():
+    x = torch.zeros(0, 8, 8, 64, device="cuda")
+    w = torch.randn(3, 3, 64, device="cuda")
+    assert dwc.fwd(x, w, 1, 1).shape == (0, 8, 8, 64)
+    dw = dwc.bwd_filter(x, torch.zeros(0, 8, 8, 64, device="cuda"), (3, 3), 1, 1)
+    torch.cuda.synchronize()
+    assert torch.all(dw == 0)
+
+
+# ---- full workload sizes: sampled outputs the oracle computes one by one ----------------
+
+def check_sampled(case: Case, passes, n_samples=2048, seed=0):
+    x, w, dy, got = run_all(case, passes)
+    rng = np.random.default_rng(seed)
+    s, p = case.stride, case.pad
+    x, w, dy = (t.double().numpy() for t in (x, w, dy))   # exact widening, once
+    ax, aw, ady = np.abs(x), np.abs(w), np.abs(dy)
+    for name, g in got.items():
+        flat = g.ravel()
+        idx = rng.integers(0, flat.size, n_samples)
+        # always include the corners of the tensor (borders and the ragged tail)
+        idx = np.concatenate([idx, [0, flat.size - 1, flat.size // 2]])
+        if name == "fwd":
+            ref, den = oracle.fwd_at(x, w, idx, s, p), oracle.fwd_at(ax, aw, idx, s, p)
+        elif name == "bwd_data":
+            ref = oracle.bwd_data_at(dy, w, (case.H, case.W), idx, s, p)
+            den = oracle.bwd_data_at(ady, aw, (case.H, case.W), idx, s, p)
+        else:
+            ref = oracle.bwd_filter_at(x, dy, (case.FH, case.FW), idx, s, p)
+            den = oracle.bwd_filter_at(ax, ady, (case.FH, case.FW), idx, s, p)
+        err = normalized_error(flat[idx], ref, den)
+        assert err <= TOL[case.dtype], f"{name} {case}: normalized error {err:.3e}"
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_workloads_full_size_sampled(name):
+    case = WORKLOADS[name]
+    passes = ("fwd",) if name.startswith("fwd_") else ("fwd", "bwd_data", "bwd_filter")
+    if name == "fwd_f32_n1_14x14_c32_f3":
+        check_full(case, passes)
+    else:
+        check_sampled(case, passes)
+
+
+def test_sweep_full_size_sampled():
+    """Every filter size of the sweep on every stage shape, fp32 and bf16, all passes."""
+    for case in sweep_cases():
+        check_sampled(case, ("fwd", "bwd_data", "bwd_filter"), n_samples=256, seed=case.seed)
