@@ -179,8 +179,10 @@ def cpu_baseline(case, passes, seconds):
     dt, flops = oracle_sample_run(case, passes, frac, host)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
             "kind": "oracle",
-            "sample": f"{frac:.3g} of the outputs of each pass ({'+'.join(passes)}), random "
-                      f"positions, fp64 C oracle with OpenMP; {dt:.1f} s"}
+            "sample": (f"{frac:.3g} of the outputs of each pass ({'+'.join(passes)}) at random "
+                       f"positions" if frac < 1 else
+                       f"every output of every pass ({'+'.join(passes)}), the full step")
+                      + f", fp64 C oracle with OpenMP; {dt:.1f} s"}
 
 
 def run_reference(args, case, passes):
@@ -243,6 +245,54 @@ def load_traffic(kernel_key):
     if h.hexdigest() != ent.get("source_sha256"):
         return None
     return ent.get("bytes_per_launch")
+
+
+def run_e2e(args, case, passes, run_pass, x, w, dy, y, dx, dw, stream, world, flops_step):
+    """Same step through the C ABI with inputs copied from pinned host memory and outputs
+    copied back, all inside the timed region."""
+    import torch
+    hx, hw, hdy = (t.pin_memory() for t in (case.x(), case.w(), case.dy()))
+    hy = torch.empty(y.shape, dtype=torch.float32).pin_memory()
+    hdx = torch.empty(dx.shape, dtype=torch.float32).pin_memory()
+    hdw = torch.empty(dw.shape, dtype=torch.float32).pin_memory()
+    dxb, dwb, ddy = torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)
+    h2d = sum(t.numel() * t.element_size() for t, nm in ((hx, "x"), (hw, "w"), (hdy, "dy"))
+              if nm == "w" or (nm == "x" and ("fwd" in passes or "bwd_filter" in passes))
+              or (nm == "dy" and ("bwd_data" in passes or "bwd_filter" in passes)))
+    d2h = sum({"fwd": hy, "bwd_data": hdx, "bwd_filter": hdw}[n].numel() * 4 for n in passes)
+
+    def e2e_step():
+        dxb.copy_(hx, non_blocking=True)
+        dwb.copy_(hw, non_blocking=True)
+        ddy.copy_(hdy, non_blocking=True)
+        for name in passes:
+            run_pass(name, dxb, dwb, ddy)
+        if "fwd" in passes:
+            hy.copy_(y, non_blocking=True)
+        if "bwd_data" in passes:
+            hdx.copy_(dx, non_blocking=True)
+        if "bwd_filter" in passes:
+            hdw.copy_(dw, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * args.e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
+
+    return e2e_value, h2d, d2h
 
 
 def run_ours(args, case, passes):
@@ -320,47 +370,10 @@ def run_ours(args, case, passes):
     flops_step = rl.nominal_flops(case) * len(passes)
     value = world * args.steps * flops_step / (total_ms * 1e-3) / 1e12
 
-    # --- e2e through the C ABI with pinned host buffers -------------------------------
-    hx, hw, hdy = (t.pin_memory() for t in (case.x(), case.w(), case.dy()))
-    hy = torch.empty(y.shape, dtype=torch.float32).pin_memory()
-    hdx = torch.empty(dx.shape, dtype=torch.float32).pin_memory()
-    hdw = torch.empty(dw.shape, dtype=torch.float32).pin_memory()
-    dxb, dwb, ddy = torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)
-    h2d = sum(t.numel() * t.element_size() for t, nm in ((hx, "x"), (hw, "w"), (hdy, "dy"))
-              if nm == "w" or (nm == "x" and ("fwd" in passes or "bwd_filter" in passes))
-              or (nm == "dy" and ("bwd_data" in passes or "bwd_filter" in passes)))
-    d2h = sum({"fwd": hy, "bwd_data": hdx, "bwd_filter": hdw}[n].numel() * 4 for n in passes)
-
-    def e2e_step():
-        dxb.copy_(hx, non_blocking=True)
-        dwb.copy_(hw, non_blocking=True)
-        ddy.copy_(hdy, non_blocking=True)
-        for name in passes:
-            run_pass(name, dxb, dwb, ddy)
-        if "fwd" in passes:
-            hy.copy_(y, non_blocking=True)
-        if "bwd_data" in passes:
-            hdx.copy_(dx, non_blocking=True)
-        if "bwd_filter" in passes:
-            hdw.copy_(dw, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * args.e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
+    e2e_value, h2d, d2h = None, 0, 0
+    if args.e2e_steps > 0:
+        e2e_value, h2d, d2h = run_e2e(args, case, passes, run_pass, x, w, dy, y, dx, dw, stream,
+                                      world, flops_step)
 
     if rank != 0:
         if world > 1:
@@ -402,8 +415,9 @@ def run_ours(args, case, passes):
             "gbs": sum(rl.compulsory_bytes(case, n) for n in passes) * args.steps * world
                    / (total_ms * 1e-3) / 1e9,
             "roofline": roof, "per_pass": passes_out,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+            "e2e": ({"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
+                    if e2e_value is not None else None),
             "gpu_launches": args.steps * sum(LAUNCHES[n] for n in passes),
             "clocks": clocks}
     if not args.no_cpu_baseline and world == 1:

@@ -76,6 +76,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return true;
 }
 
+// Position in a ring of `n` pipeline stages: the slot and the parity of its current use.
+// Advanced by one stage at a time, so no division is ever needed in the hot loops.
+struct Ring {
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ void next(uint32_t n) {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
 __device__ __forceinline__ void record_status(unsigned int* status, unsigned int bits) {
     if (status) atomicOr(status, bits);
 }
@@ -109,6 +121,65 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 __device__ __forceinline__ void fma2(float2& acc, float2 a, float2 b) {
     acc = __ffma2_rn(a, b, acc);
 }
+
+// Arithmetic on a pair of adjacent channels held as one 64-bit register (two fp32 lanes).
+// Keeping the pair as a single 64-bit value from the shared-memory load to the packed FMA
+// lets the register allocator place it in an aligned register pair once, instead of
+// assembling pairs around every packed FMA.
+struct Pair64 {
+    using V = unsigned long long;
+    __device__ static __forceinline__ V zero() { return 0ull; }
+    __device__ static __forceinline__ void fma(V& acc, V a, V b) {
+        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+    }
+    __device__ static __forceinline__ V pack(float lo, float hi) {
+        V r;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+        return r;
+    }
+    __device__ static __forceinline__ float2 unpack(V v) {
+        float2 f;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+        return f;
+    }
+    __device__ static __forceinline__ V load(const float* p) {
+        return *reinterpret_cast<const unsigned long long*>(p);
+    }
+    __device__ static __forceinline__ V load(const __nv_bfloat16* p) {
+        // bf16 -> fp32 is exact: the 16 bits become the high half of the fp32 word
+        const unsigned u = *reinterpret_cast<const unsigned*>(p);
+        V r;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(u << 16), "r"(u & 0xffff0000u));
+        return r;
+    }
+    __device__ static __forceinline__ V load(const __half* p) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(p));
+        return pack(f.x, f.y);
+    }
+};
+
+// The same pair arithmetic on float2 values with the packed-FMA builtin.
+struct PairF2 {
+    using V = float2;
+    __device__ static __forceinline__ V zero() { return make_float2(0.f, 0.f); }
+    __device__ static __forceinline__ void fma(V& acc, V a, V b) { acc = __ffma2_rn(a, b, acc); }
+    __device__ static __forceinline__ float2 unpack(V v) { return v; }
+    template <typename T>
+    __device__ static __forceinline__ V load(const T* p);
+};
+
+// Two scalar FMAs per pair (no packed instruction).
+struct PairScalar {
+    using V = float2;
+    __device__ static __forceinline__ V zero() { return make_float2(0.f, 0.f); }
+    __device__ static __forceinline__ void fma(V& acc, V a, V b) {
+        acc.x = fmaf(a.x, b.x, acc.x);
+        acc.y = fmaf(a.y, b.y, acc.y);
+    }
+    __device__ static __forceinline__ float2 unpack(V v) { return v; }
+    template <typename T>
+    __device__ static __forceinline__ V load(const T* p);
+};
 
 // Element type traits: how two adjacent channels are loaded from shared memory and
 // widened to fp32 (exact for bf16 and fp16).
@@ -154,5 +225,10 @@ __device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
 __device__ __forceinline__ void store_pair_streaming(float* p, float2 v) {
     __stcs(reinterpret_cast<float2*>(p), v);
 }
+
+template <typename T>
+__device__ __forceinline__ float2 PairF2::load(const T* p) { return Elem<T>::load_pair(p); }
+template <typename T>
+__device__ __forceinline__ float2 PairScalar::load(const T* p) { return Elem<T>::load_pair(p); }
 
 }  // namespace dwc

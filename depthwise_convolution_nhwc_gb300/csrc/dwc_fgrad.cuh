@@ -45,8 +45,11 @@ struct FgradArgs {
     uint32_t y_off;        // byte offset of the dy ring after the x ring
 };
 
+constexpr int kFgradMaxComputeWarps = 8;
+constexpr int kFgradMaxThreads = (kFgradMaxComputeWarps + 1) * 32;
+
 template <typename T, int FH, int FW>
-__global__ void __launch_bounds__(kRowsMaxThreads, 1)
+__global__ void __launch_bounds__(kFgradMaxThreads, 1)
 fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
              const FgradArgs a) {
     constexpr int RF = FgradTile<FH, FW>::RF;
@@ -91,28 +94,27 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         if (lane != 0) return;
         prefetch_tensormap(&xmap);
         prefetch_tensormap(&ymap);
-        long long gx = 0, gy = 0;
+        Ring xr, yr;
+        uint32_t xissued = 0, yissued = 0;  // saturating counts, compared with the ring sizes
         bool ok = true;
         auto put_x = [&](int n, int ih) -> bool {
-            const int slot = static_cast<int>(gx % a.nx);
-            const long long use = gx / a.nx;
-            if (use > 0 && !mbar_wait(&xempty[slot], static_cast<uint32_t>((use - 1) & 1)))
+            if (xissued >= static_cast<uint32_t>(a.nx) && !mbar_wait(&xempty[xr.slot], xr.phase ^ 1u))
                 return false;
-            mbar_arrive_expect_tx(&xfull[slot], a.x_bytes);
-            tma_load_4d(xring + static_cast<size_t>(slot) * a.x_bytes, &xmap, &xfull[slot],
+            if (xissued < static_cast<uint32_t>(a.nx)) ++xissued;
+            mbar_arrive_expect_tx(&xfull[xr.slot], a.x_bytes);
+            tma_load_4d(xring + static_cast<size_t>(xr.slot) * a.x_bytes, &xmap, &xfull[xr.slot],
                         cb * kBN, -a.pad, ih, n);
-            ++gx;
+            xr.next(a.nx);
             return true;
         };
         auto put_y = [&](int n, int oh) -> bool {
-            const int slot = static_cast<int>(gy % a.ny);
-            const long long use = gy / a.ny;
-            if (use > 0 && !mbar_wait(&yempty[slot], static_cast<uint32_t>((use - 1) & 1)))
+            if (yissued >= static_cast<uint32_t>(a.ny) && !mbar_wait(&yempty[yr.slot], yr.phase ^ 1u))
                 return false;
-            mbar_arrive_expect_tx(&yfull[slot], a.y_bytes);
-            tma_load_4d(yring + static_cast<size_t>(slot) * a.y_bytes, &ymap, &yfull[slot],
+            if (yissued < static_cast<uint32_t>(a.ny)) ++yissued;
+            mbar_arrive_expect_tx(&yfull[yr.slot], a.y_bytes);
+            tma_load_4d(yring + static_cast<size_t>(yr.slot) * a.y_bytes, &ymap, &yfull[yr.slot],
                         cb * kBN, 0, oh, n);
-            ++gy;
+            yr.next(a.ny);
             return true;
         };
         for (long long q = q0; q < q1 && ok;) {
@@ -128,17 +130,19 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             q = static_cast<long long>(n) * a.OH + ohb;
         }
         if (!ok) record_status(a.status, DWC_DEVSTAT_TIMEOUT);
-        // drain: the last copies of both rings must land before the CTA may exit
-        for (long long j = gx > a.nx ? gx - a.nx : 0; j < gx; ++j)
-            if (!mbar_wait(&xfull[j % a.nx], static_cast<uint32_t>((j / a.nx) & 1))) {
-                record_status(a.status, DWC_DEVSTAT_TIMEOUT);
-                break;
+        // drain: the copies still outstanding in both rings must land before the CTA exits
+        auto drain = [&](Ring r, uint32_t issued, uint32_t n, uint64_t* full) {
+            for (uint32_t j = 0; j < issued; ++j) {
+                r.slot = r.slot == 0 ? n - 1 : r.slot - 1;
+                if (r.slot == n - 1) r.phase ^= 1u;
+                if (!mbar_wait(&full[r.slot], r.phase)) {
+                    record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+                    return;
+                }
             }
-        for (long long j = gy > a.ny ? gy - a.ny : 0; j < gy; ++j)
-            if (!mbar_wait(&yfull[j % a.ny], static_cast<uint32_t>((j / a.ny) & 1))) {
-                record_status(a.status, DWC_DEVSTAT_TIMEOUT);
-                break;
-            }
+        };
+        drain(xr, xissued, a.nx, xfull);
+        drain(yr, yissued, a.ny, yfull);
         return;
     }
 
@@ -159,31 +163,43 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 #pragma unroll
     for (int f = 0; f < RF; ++f) live[f] = (frow0 + f < a.fhc) && (fh0 + frow0 + f < FH);
 
-    long long gx = 0, gy = 0;
+    Ring xbase, yr;  // oldest x row of the current window; current dy row
     bool ok = true;
+    // slot and parity of the x row `d` rows after the window base (d < nx)
+    auto xslot = [&](uint32_t d, uint32_t& phase) -> uint32_t {
+        uint32_t s = xbase.slot + d;
+        phase = xbase.phase;
+        if (s >= static_cast<uint32_t>(a.nx)) {
+            s -= a.nx;
+            phase ^= 1u;
+        }
+        return s;
+    };
     for (long long q = q0; q < q1 && ok;) {
         const int n = static_cast<int>(q / a.OH);
         const int oha = static_cast<int>(q % a.OH);
         const int ohb = static_cast<int>(std::min<long long>(q1 - static_cast<long long>(n) * a.OH, a.OH));
-        const long long gx0 = gx;
         const int L = ohb - oha;
-        for (int yr = 0; yr < L && ok; ++yr) {
-            // wait for the x rows this output row needs (all of them at the segment start)
-            for (long long j = (yr == 0 ? gx0 : gx0 + yr + a.fhc - 1); j <= gx0 + yr + a.fhc - 1; ++j)
-                if (!mbar_wait(&xfull[j % a.nx], static_cast<uint32_t>((j / a.nx) & 1))) {
+        for (int row = 0; row < L && ok; ++row) {
+            // wait for the x rows this output row needs (the whole window at the segment start)
+            for (int d = (row == 0 ? 0 : a.fhc - 1); d < a.fhc; ++d) {
+                uint32_t ph;
+                const uint32_t sl = xslot(static_cast<uint32_t>(d), ph);
+                if (!mbar_wait(&xfull[sl], ph)) {
                     ok = false;
                     break;
                 }
-            if (ok && !mbar_wait(&yfull[gy % a.ny], static_cast<uint32_t>((gy / a.ny) & 1)))
-                ok = false;
+            }
+            if (ok && !mbar_wait(&yfull[yr.slot], yr.phase)) ok = false;
             if (!ok) break;
 
-            const T* ys = reinterpret_cast<const T*>(yring + static_cast<size_t>(gy % a.ny) * a.y_bytes) + 2 * lane;
+            const T* ys = reinterpret_cast<const T*>(yring + static_cast<size_t>(yr.slot) * a.y_bytes) + 2 * lane;
             const T* xs[RF];
 #pragma unroll
             for (int f = 0; f < RF; ++f) {
-                const long long j = gx0 + yr + frow0 + f;
-                xs[f] = reinterpret_cast<const T*>(xring + static_cast<size_t>(j % a.nx) * a.x_bytes) + 2 * lane;
+                uint32_t ph;
+                const uint32_t sl = xslot(static_cast<uint32_t>(frow0 + f), ph);
+                xs[f] = reinterpret_cast<const T*>(xring + static_cast<size_t>(sl) * a.x_bytes) + 2 * lane;
             }
             if (blk0 < blk1) {
                 // circular window: column c of the padded x row sits in slot c mod FW
@@ -213,17 +229,19 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             }
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&yempty[gy % a.ny]);
-                mbar_arrive(&xempty[(gx0 + yr) % a.nx]);
+                mbar_arrive(&yempty[yr.slot]);
+                mbar_arrive(&xempty[xbase.slot]);  // the oldest row has no later use
             }
-            ++gy;
+            yr.next(a.ny);
+            xbase.next(a.nx);
         }
         if (!ok) break;
-        // rows gx0+L .. gx0+L+fhc-2 are not needed by later output rows of this segment
+        // the last fhc-1 rows of the window are not needed by later output rows
         __syncwarp();
-        if (lane == 0)
-            for (long long j = gx0 + L; j < gx0 + L + a.fhc - 1; ++j) mbar_arrive(&xempty[j % a.nx]);
-        gx = gx0 + L + a.fhc - 1;
+        for (int d = 0; d < a.fhc - 1; ++d) {
+            if (lane == 0) mbar_arrive(&xempty[xbase.slot]);
+            xbase.next(a.nx);
+        }
         q = static_cast<long long>(n) * a.OH + ohb;
     }
     // A warp that gave up still goes through the two CTA barriers below, so that no
@@ -283,7 +301,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW>& P) {
     P.ny = 2;
     // largest row group whose x window fits in shared memory ...
     const int groups = (FH + RF - 1) / RF;  // RF-row groups needed to cover the filter
-    int nwf_max = std::min(groups, kMaxComputeWarps);
+    int nwf_max = std::min(groups, kFgradMaxComputeWarps);
     for (; nwf_max >= 1; --nwf_max) {
         const size_t need = 512 + static_cast<size_t>(nwf_max * RF + 2) * P.x_bytes +
                             static_cast<size_t>(P.ny) * P.y_bytes;
@@ -297,7 +315,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW>& P) {
     P.nx = P.fhc + 2;
     P.smem = 512 + static_cast<size_t>(P.nx) * P.x_bytes + static_cast<size_t>(P.ny) * P.y_bytes;
     P.chunks = (FH + P.fhc - 1) / P.fhc;
-    P.nwc = std::max(1, std::min(kMaxComputeWarps / P.nwf, P.nblocks));
+    P.nwc = std::max(1, std::min(kFgradMaxComputeWarps / P.nwf, P.nblocks));
     P.bps = (P.nblocks + P.nwc - 1) / P.nwc;
     P.nwc = (P.nblocks + P.bps - 1) / P.bps;
     // strip reduction buffer reuses the ring

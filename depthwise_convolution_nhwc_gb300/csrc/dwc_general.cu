@@ -105,13 +105,31 @@ __global__ void general_bwd_filter_kernel(const T* __restrict__ x, const T* __re
     }
 }
 
+// out[i] = sum_z part[z * count + i].  Eight lanes share one output: lane g of the group
+// sums the contiguous slice range [g*zc, (g+1)*zc) and the eight partial sums are combined
+// by a fixed butterfly, so the order of additions is the same on every run.
+constexpr int kReduceGroup = 8;
+
 __global__ void reduce_slices_kernel(const float* __restrict__ part, int slices, size_t count,
                                      float* __restrict__ out) {
-    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < count;
-         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    constexpr int kGroupsPerWarp = 32 / kReduceGroup;
+    const int lane = threadIdx.x & 31;
+    const int g = lane % kReduceGroup;
+    const int zc = (slices + kReduceGroup - 1) / kReduceGroup;
+    const int z0 = g * zc, z1 = min(slices, z0 + zc);
+    const size_t warp = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const size_t warps = (static_cast<size_t>(gridDim.x) * blockDim.x) >> 5;
+    // the loop bound depends only on the warp, so every lane reaches every shuffle
+    for (size_t base = warp * kGroupsPerWarp; base < count; base += warps * kGroupsPerWarp) {
+        const size_t i = base + lane / kReduceGroup;
         float s = 0.f;
-        for (int z = 0; z < slices; ++z) s += part[static_cast<size_t>(z) * count + i];
-        out[i] = s;
+        if (i < count) {
+#pragma unroll 4
+            for (int z = z0; z < z1; ++z) s += part[static_cast<size_t>(z) * count + i];
+        }
+#pragma unroll
+        for (int m = 1; m < kReduceGroup; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+        if (g == 0 && i < count) out[i] = s;
     }
 }
 
@@ -119,8 +137,9 @@ cudaError_t launch_reduce_slices(const float* part, int slices, size_t count, fl
                                  cudaStream_t stream) {
     if (count == 0) return cudaSuccess;
     const int threads = 256;
-    const size_t blocks = std::min<size_t>((count + threads - 1) / threads,
-                                           static_cast<size_t>(device_info().sm_count) * 8);
+    const size_t per_block = threads / kReduceGroup;
+    const size_t blocks = std::min<size_t>((count + per_block - 1) / per_block,
+                                           static_cast<size_t>(device_info().sm_count) * 16);
     reduce_slices_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(part, slices,
                                                                                count, out);
     return cudaGetLastError();

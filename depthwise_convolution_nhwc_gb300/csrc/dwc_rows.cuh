@@ -25,6 +25,7 @@
 //  * 16-bit inputs are widened to fp32 once per shared-memory load, not per FMA (§4.1).
 #pragma once
 
+#include <climits>
 #include <utility>
 
 #include "dwc_device.cuh"
@@ -33,25 +34,31 @@
 namespace dwc {
 
 constexpr int kBN = 64;                 // channels per work unit (32 lanes x 2)
-constexpr int kMaxComputeWarps = 8;
+constexpr int kMaxComputeWarps = 7;   // + 1 producer warp = 256 threads per CTA
 constexpr int kRowsMaxThreads = (kMaxComputeWarps + 1) * 32;
 
 // Register tile per filter size: R output rows x TM output columns per lane.
+// R > 1 unrolls all R + FH - 1 input rows of a band (compile-time filter-register slots),
+// so it is used for the smaller filters only; large filters take one output row per lane
+// and a rolled row loop.
+// Chosen by timing candidate tiles on the filter sizes of the benchmark shapes.
 template <int FH, int FW>
 struct RowsTile {
-    static constexpr int R = (FH <= 9) ? 4 : (FH <= 15 ? 2 : 1);
-    static constexpr int TM = (FH <= 9) ? 8 : (FH <= 15 ? 16 : 32);
+    static constexpr int R = (FH <= 3) ? 8 : (FH <= 5 ? 3 : (FH <= 15 ? 2 : 1));
+    static constexpr int TM = (FH <= 3) ? 4 : (FH <= 15 ? 8 : 14);
+    static constexpr int MINB = (FH >= 7 && FH <= 9) ? 3 : 2;  // CTAs per SM for the registers
 };
 
 struct RowsArgs {
     float* out;
     unsigned int* status;
+    int H;                // input rows (for trimming rows that lie in the padding)
     int OH, OW, C;
     int pad_h, pad_w;
     int nwc;              // compute warps per CTA
     int ns;               // pipeline stages
-    int cblocks, bands, ctiles;
-    long long units;
+    uint32_t cblocks, bands, ctiles;
+    uint32_t units;
     uint32_t x_bytes;     // bytes of one staged input row box
     uint32_t w_bytes;     // bytes of one staged filter row box
     uint32_t stage_stride;
@@ -59,6 +66,15 @@ struct RowsArgs {
 
 template <int I>
 using IntC = std::integral_constant<int, I>;
+
+// Input rows i of a one-row band (output row oh0, input row oh0 - pad + i) that fall
+// inside the image: [i_lo, i_hi) intersected with the band's [i_lo, i_hi).  Rows outside
+// contribute only zeros (the trimming of shared zero rows described in §4.4).
+__device__ __forceinline__ void rows_in_image(int oh0, int pad, int H, int& i_lo, int& i_hi) {
+    i_lo = max(i_lo, pad - oh0);
+    i_hi = min(i_hi, H + pad - oh0);
+    if (i_hi < i_lo) i_hi = i_lo;
+}
 
 template <class F, int... Is>
 __device__ __forceinline__ void static_for_impl(F&& f, std::integer_sequence<int, Is...>) {
@@ -79,31 +95,31 @@ __host__ __device__ constexpr unsigned valid_rows(int i) {
     return m;
 }
 
-// Accumulate one staged input row into the lane's R x TM outputs.
-template <typename T, int FW, int R, int TM, unsigned MASK>
-__device__ __forceinline__ void consume_row(const T* __restrict__ xs, float2 (&acc)[R][TM],
-                                            const float2 (&wwin)[R][FW]) {
+// Accumulate one staged input row i into the lane's R x TM outputs.  Output row r (in
+// MASK) takes filter row i - r, held in register slot (i - r) mod R; ISLOT = i mod R.
+template <class P, typename T, int FW, int R, int TM, unsigned MASK, int ISLOT>
+__device__ __forceinline__ void consume_rows(const T* __restrict__ xs, typename P::V (&acc)[R][TM],
+                                             const typename P::V (&wwin)[R][FW]) {
 #pragma unroll
     for (int j = 0; j < TM + FW - 1; ++j) {
-        const float2 x = Elem<T>::load_pair(xs + j * kBN);
+        const typename P::V x = P::load(xs + j * kBN);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             if (!((MASK >> r) & 1u)) continue;
+            const int slot = (ISLOT - r + R) % R;
 #pragma unroll
             for (int fw = 0; fw < FW; ++fw) {
                 const int t = j - fw;
-                if (t >= 0 && t < TM) fma2(acc[r][t], x, wwin[r][fw]);
+                if (t >= 0 && t < TM) P::fma(acc[r][t], x, wwin[slot][fw]);
             }
         }
     }
 }
 
-template <typename T, int FH, int FW, bool FLIP>
-__global__ void __launch_bounds__(kRowsMaxThreads, 1)
+template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64>
+__global__ void __launch_bounds__(kRowsMaxThreads, MINB)
 rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
             const RowsArgs a) {
-    constexpr int R = RowsTile<FH, FW>::R;
-    constexpr int TM = RowsTile<FH, FW>::TM;
     constexpr int S = R + FH - 1;  // input rows per band
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -130,47 +146,54 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         if (lane != 0) return;
         prefetch_tensormap(&xmap);
         prefetch_tensormap(&wmap);
-        long long k = 0;
+        Ring ring;
+        uint32_t issued = 0;  // stages issued so far (saturating; only compared with ns)
         bool ok = true;
-        for (long long u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-            long long q = u;
+        for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            uint32_t q = u;
             const int band = static_cast<int>(q % a.bands); q /= a.bands;
             const int ct = static_cast<int>(q % a.ctiles); q /= a.ctiles;
             const int cb = static_cast<int>(q % a.cblocks); q /= a.cblocks;
             const int n = static_cast<int>(q);
             const int oh0 = band * R, ow0 = ct * TW;
-            for (int i = 0; i < S; ++i, ++k) {
-                const int slot = static_cast<int>(k % a.ns);
-                const long long use = k / a.ns;
-                if (use > 0 && !mbar_wait(&empty[slot], static_cast<uint32_t>((use - 1) & 1))) {
+            int i_lo = 0, i_hi = S;
+            if constexpr (R == 1) rows_in_image(oh0, a.pad_h, a.H, i_lo, i_hi);
+            for (int i = i_lo; i < i_hi; ++i, ring.next(a.ns)) {
+                // slot reuse: wait until every compute warp released its previous stage
+                if (issued >= static_cast<uint32_t>(a.ns) &&
+                    !mbar_wait(&empty[ring.slot], ring.phase ^ 1u)) {
                     record_status(a.status, DWC_DEVSTAT_TIMEOUT);
                     ok = false;
                     break;
                 }
-                unsigned char* st = stages + static_cast<size_t>(slot) * a.stage_stride;
+                if (issued < static_cast<uint32_t>(a.ns)) ++issued;
+                unsigned char* st = stages + static_cast<size_t>(ring.slot) * a.stage_stride;
                 const bool wrow = i < FH;
-                mbar_arrive_expect_tx(&full[slot], a.x_bytes + (wrow ? a.w_bytes : 0u));
-                tma_load_4d(st, &xmap, &full[slot], cb * kBN, ow0 - a.pad_w, oh0 - a.pad_h + i, n);
+                mbar_arrive_expect_tx(&full[ring.slot], a.x_bytes + (wrow ? a.w_bytes : 0u));
+                tma_load_4d(st, &xmap, &full[ring.slot], cb * kBN, ow0 - a.pad_w, oh0 - a.pad_h + i, n);
                 if (wrow)
-                    tma_load_3d(st + a.x_bytes, &wmap, &full[slot], cb * kBN, 0,
+                    tma_load_3d(st + a.x_bytes, &wmap, &full[ring.slot], cb * kBN, 0,
                                 FLIP ? FH - 1 - i : i);
             }
         }
-        // Never leave the CTA with copies in flight: wait (bounded) for the last stages.
-        const long long first = k > a.ns ? k - a.ns : 0;
-        for (long long j = first; j < k; ++j)
-            if (!mbar_wait(&full[j % a.ns], static_cast<uint32_t>((j / a.ns) & 1))) {
+        // Never leave the CTA with copies in flight: wait (bounded) for the stages still
+        // outstanding (the last `issued` ones, walking the ring backwards).
+        for (uint32_t j = 0; j < issued; ++j) {
+            ring.slot = ring.slot == 0 ? a.ns - 1 : ring.slot - 1;
+            if (ring.slot == static_cast<uint32_t>(a.ns) - 1) ring.phase ^= 1u;
+            if (!mbar_wait(&full[ring.slot], ring.phase)) {
                 record_status(a.status, DWC_DEVSTAT_TIMEOUT);
                 break;
             }
+        }
         return;
     }
 
     // ---------------- compute warps ----------------------------------------------------
     const int wc = warp;
-    long long k = 0;
-    for (long long u = blockIdx.x; u < a.units; u += gridDim.x) {
-        long long q = u;
+    Ring ring;
+    for (uint32_t u = blockIdx.x; u < a.units; u += gridDim.x) {
+        uint32_t q = u;
         const int band = static_cast<int>(q % a.bands); q /= a.bands;
         const int ct = static_cast<int>(q % a.ctiles); q /= a.ctiles;
         const int cb = static_cast<int>(q % a.cblocks); q /= a.cblocks;
@@ -179,71 +202,68 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         const int owl = ct * TW + wc * TM;  // first output column of this lane
         const int c = cb * kBN + 2 * lane;
 
-        float2 acc[R][TM];
-        float2 wwin[R][FW];
+        typename P::V acc[R][TM];
+        typename P::V wwin[R][FW];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
 #pragma unroll
-            for (int t = 0; t < TM; ++t) acc[r][t] = make_float2(0.f, 0.f);
+            for (int t = 0; t < TM; ++t) acc[r][t] = P::zero();
 #pragma unroll
-            for (int f = 0; f < FW; ++f) wwin[r][f] = make_float2(0.f, 0.f);
+            for (int f = 0; f < FW; ++f) wwin[r][f] = P::zero();
         }
 
-        bool ok = true;
-        // Wait for stage k, slide the filter window by one row, return the row pointers.
-        auto begin_row = [&](int i, const T*& xs) -> bool {
-            const int slot = static_cast<int>(k % a.ns);
-            if (!mbar_wait(&full[slot], static_cast<uint32_t>((k / a.ns) & 1))) {
+        // Filter row fh lives in register slot fh % R: it enters at input row i = fh and is
+        // last used at i = fh + R - 1, when row fh + R (same slot) is not yet needed.
+        // Wait for the stage of input row i, load filter row i into its slot (i < FH) and
+        // return the row's shared-memory pointer.  The slot index is a compile-time
+        // constant wherever the row loop is unrolled, so no register ever moves.
+        auto begin_row = [&](auto ic, int i, const T*& xs) -> bool {
+            if (!mbar_wait(&full[ring.slot], ring.phase)) {
                 record_status(a.status, DWC_DEVSTAT_TIMEOUT);
                 return false;
             }
-            const unsigned char* st = stages + static_cast<size_t>(slot) * a.stage_stride;
-#pragma unroll
-            for (int r = R - 1; r > 0; --r)
-#pragma unroll
-                for (int f = 0; f < FW; ++f) wwin[r][f] = wwin[r - 1][f];
+            const unsigned char* st = stages + static_cast<size_t>(ring.slot) * a.stage_stride;
+            constexpr int slot = decltype(ic)::value % R;
             if (i < FH) {
                 const T* ws = reinterpret_cast<const T*>(st + a.x_bytes) + 2 * lane;
 #pragma unroll
                 for (int f = 0; f < FW; ++f)
-                    wwin[0][f] = Elem<T>::load_pair(ws + (FLIP ? FW - 1 - f : f) * kBN);
+                    wwin[slot][f] = P::load(ws + (FLIP ? FW - 1 - f : f) * kBN);
             }
             xs = reinterpret_cast<const T*>(st) + (wc * TM) * kBN + 2 * lane;
             return true;
         };
         auto end_row = [&]() {
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[k % a.ns]);
-            ++k;
+            if (lane == 0) mbar_arrive(&empty[ring.slot]);
+            ring.next(a.ns);
         };
 
-        // prologue: input rows 0 .. R-2 (not every output row of the band is reached yet)
-        static_for<R - 1>([&](auto I) {
-            constexpr int i = decltype(I)::value;
-            if (!ok) return;
-            const T* xs;
-            if (!begin_row(i, xs)) { ok = false; return; }
-            consume_row<T, FW, R, TM, valid_rows<R, FH>(i)>(xs, acc, wwin);
-            end_row();
-        });
-        // steady state: every output row of the band takes this input row
+        bool ok = true;
+        if constexpr (R > 1) {
+            // every input row of the band unrolled: output row r takes filter row i - r
+            // from slot (i - r) % R
+            static_for<S>([&](auto I) {
+                constexpr int i = decltype(I)::value;
+                if (!ok) return;
+                const T* xs;
+                if (!begin_row(I, i, xs)) { ok = false; return; }
+                consume_rows<P, T, FW, R, TM, valid_rows<R, FH>(i), i % R>(xs, acc, wwin);
+                end_row();
+            });
+        } else {
+            // one output row: the filter row for input row i is simply row i; input rows
+            // that lie entirely in the zero padding are neither loaded nor computed
+            int i_lo = 0, i_hi = S;
+            rows_in_image(oh0, a.pad_h, a.H, i_lo, i_hi);
 #pragma unroll 1
-        for (int i = R - 1; i < FH && ok; ++i) {
-            const T* xs;
-            if (!begin_row(i, xs)) { ok = false; break; }
-            consume_row<T, FW, R, TM, (1u << R) - 1u>(xs, acc, wwin);
-            end_row();
+            for (int i = i_lo; i < i_hi && ok; ++i) {
+                const T* xs;
+                if (!begin_row(IntC<0>{}, i, xs)) { ok = false; break; }
+                consume_rows<P, T, FW, R, TM, 1u, 0>(xs, acc, wwin);
+                end_row();
+            }
         }
-        // epilogue: input rows FH .. FH+R-2 (the top output rows are complete)
-        constexpr int E0 = (FH > R - 1) ? FH : R - 1;
-        static_for<S - E0>([&](auto I) {
-            constexpr int i = E0 + decltype(I)::value;
-            if (!ok) return;
-            const T* xs;
-            if (!begin_row(i, xs)) { ok = false; return; }
-            consume_row<T, FW, R, TM, valid_rows<R, FH>(i)>(xs, acc, wwin);
-            end_row();
-        });
         if (!ok) return;
 
         if (c < a.C) {
@@ -255,23 +275,31 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
 #pragma unroll
                 for (int t = 0; t < TM; ++t) {
                     const int ow = owl + t;
-                    if (ow < a.OW) store_pair_streaming(row + static_cast<size_t>(ow) * a.C, acc[r][t]);
+                    if (ow < a.OW)
+                        store_pair_streaming(row + static_cast<size_t>(ow) * a.C, P::unpack(acc[r][t]));
                 }
             }
         }
     }
 }
 
-template <typename T, int FH, int FW, bool FLIP>
+template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64>
 cudaError_t launch_rows_inst(const RowConv& p) {
-    constexpr int TM = RowsTile<FH, FW>::TM;
     const int e = static_cast<int>(sizeof(T));
     const DeviceInfo& dev = device_info();
 
     // compute warps side by side along the row; the staged box (TW + FW - 1 pixels) must
     // stay within the TMA box limit of 256
-    const int nwc = std::min(std::min(kMaxComputeWarps, (p.OW + TM - 1) / TM), (257 - FW) / TM);
-    if (nwc < 1) return cudaErrorNotSupported;
+    const int max_nwc = std::min(kMaxComputeWarps, (257 - FW) / TM);
+    if (max_nwc < 1) return cudaErrorNotSupported;
+    // warps per row tile: fewest computed columns plus half a halo per column tile
+    int nwc = 1;
+    long long best = LLONG_MAX;
+    for (int n = 1; n <= max_nwc; ++n) {
+        const long long tiles = (p.OW + n * TM - 1) / (n * TM);
+        const long long cost = 2 * tiles * n * TM + tiles * (FW - 1);
+        if (cost <= best) { best = cost; nwc = n; }
+    }
     const int TW = nwc * TM;
     const int TWH = TW + FW - 1;
 
@@ -298,19 +326,22 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     RowsArgs a;
     a.out = p.out;
     a.status = p.status;
+    a.H = p.H;
     a.OH = p.OH; a.OW = p.OW; a.C = p.C;
     a.pad_h = p.pad_h; a.pad_w = p.pad_w;
     a.nwc = nwc;
-    a.cblocks = (p.C + kBN - 1) / kBN;
-    a.bands = (p.OH + RowsTile<FH, FW>::R - 1) / RowsTile<FH, FW>::R;
-    a.ctiles = (p.OW + TW - 1) / TW;
-    a.units = static_cast<long long>(p.N) * a.cblocks * a.bands * a.ctiles;
+    a.cblocks = static_cast<uint32_t>((p.C + kBN - 1) / kBN);
+    a.bands = static_cast<uint32_t>((p.OH + R - 1) / R);
+    a.ctiles = static_cast<uint32_t>((p.OW + TW - 1) / TW);
+    const long long units = static_cast<long long>(p.N) * a.cblocks * a.bands * a.ctiles;
+    if (units >= (1LL << 31)) return cudaErrorNotSupported;
+    a.units = static_cast<uint32_t>(units);
     a.x_bytes = static_cast<uint32_t>(TWH * kBN * e);
     a.w_bytes = static_cast<uint32_t>(FW * kBN * e);
     a.stage_stride = (a.x_bytes + a.w_bytes + 127u) & ~127u;
     if (a.units == 0) return cudaSuccess;
 
-    auto kern = rows_kernel<T, FH, FW, FLIP>;
+    auto kern = rows_kernel<T, FH, FW, R, TM, MINB, FLIP, P>;
     const int threads = (nwc + 1) * 32;
     static int regs = -1;  // per instantiation
     if (regs < 0) {
@@ -334,7 +365,7 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     if (ns < 2) return cudaErrorNotSupported;
     a.ns = ns;
     const size_t smem = 128 + static_cast<size_t>(ns) * a.stage_stride;
-    const long long grid = std::min<long long>(a.units, static_cast<long long>(dev.sm_count) * ctas);
+    const long long grid = std::min<long long>(units, static_cast<long long>(dev.sm_count) * ctas);
     kern<<<static_cast<unsigned>(grid), threads, smem, p.stream>>>(xmap, wmap, a);
     return cudaGetLastError();
 }
@@ -343,9 +374,12 @@ cudaError_t launch_rows_inst(const RowConv& p) {
 template <typename T>
 cudaError_t launch_rows_dispatch(const RowConv& p) {
     if (p.FH != p.FW) return cudaErrorNotSupported;
-#define DWC_ROWS_CASE(F)                                                              \
-    case F:                                                                           \
-        return p.flip ? launch_rows_inst<T, F, F, true>(p) : launch_rows_inst<T, F, F, false>(p);
+#define DWC_ROWS_CASE(F)                                                                     \
+    case F:                                                                                  \
+        return p.flip ? launch_rows_inst<T, F, F, RowsTile<F, F>::R, RowsTile<F, F>::TM,      \
+                                         RowsTile<F, F>::MINB, true>(p)                      \
+                      : launch_rows_inst<T, F, F, RowsTile<F, F>::R, RowsTile<F, F>::TM,      \
+                                         RowsTile<F, F>::MINB, false>(p);
     switch (p.FH) {
         DWC_ROWS_CASE(3)
         DWC_ROWS_CASE(5)
