@@ -30,7 +30,8 @@ STATUS = {0: "DWC_OK", 1: "DWC_ERR_INVALID_ARG", 2: "DWC_ERR_UNSUPPORTED",
 
 # Every symbol include/dwc.h declares (checked by the tests).
 EXPORTS = ("dwc_fwd", "dwc_bwd_data", "dwc_bwd_filter_workspace_size", "dwc_bwd_filter",
-           "dwc_device_status", "dwc_status_string", "dwc_version", "dwc_path")
+           "dwc_bwd_filter_noalloc", "dwc_device_status", "dwc_status_string", "dwc_version",
+           "dwc_path")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +71,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.dwc_bwd_filter_workspace_size.restype = sz
         lib.dwc_bwd_filter.argtypes = [vp, vp, vp] + shape + [i, vp, sz, vp]
         lib.dwc_bwd_filter.restype = i
+        lib.dwc_bwd_filter_noalloc.argtypes = [vp, vp, vp] + shape + [i, vp]
+        lib.dwc_bwd_filter_noalloc.restype = i
         lib.dwc_device_status.argtypes = [vp]
         lib.dwc_device_status.restype = i
         lib.dwc_status_string.argtypes = [i]

@@ -103,6 +103,31 @@ dwc_status_t dwc_bwd_filter(const void* x, const void* dy, float* dw,
                             dwc_dtype_t dtype, void* workspace, size_t workspace_bytes,
                             dwc_stream_t stream);
 
+/* Filter gradient without any allocation (no counterpart in the paper: an addition of this
+ * library).  Same operation, arguments, results and errors as dwc_bwd_filter, but the
+ * workspace is a fixed device array inside the library instead of a caller buffer.
+ *
+ * Who needs it: callers that cannot call cudaMalloc, e.g. code running under a fixed
+ * device-memory budget or a caching allocator that must not grow, plug-in hosts that hand
+ * the library only its input and output buffers, and code that must not trigger the
+ * implicit synchronisation an allocation can cause.
+ *
+ * Limit: the array holds 8 Mi floats (32 MiB); it is reserved on a GPU when the library's
+ * device code is loaded there (at the latest by the first call of this function on that
+ * GPU) and stays reserved until the process exits.  A problem whose
+ * dwc_bwd_filter_workspace_size() exceeds 32 MiB is rejected with DWC_ERR_UNSUPPORTED
+ * before anything is launched (every benchmark shape of this library fits).
+ *
+ * Set-up: the first call on each device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Sharing: all calls use the same array and leave their partial sums in it; nothing in it
+ * needs to start at zero.  Calls whose kernels overlap on the GPU (e.g. on two unordered
+ * streams) race on the array: order them on one stream or with events.  The call itself
+ * allocates and frees nothing. */
+dwc_status_t dwc_bwd_filter_noalloc(const void* x, const void* dy, float* dw,
+                                    int N, int H, int W, int C, int FH, int FW, int stride,
+                                    int pad, dwc_dtype_t dtype, dwc_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device status word that the kernels
  * set when a wait runs out of time.  DWC_OK if no kernel reported a problem since the last
  * call, DWC_ERR_TIMEOUT if one did, DWC_ERR_CUDA if the synchronisation failed. */
