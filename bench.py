@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--record-traffic", metavar="NCU_RAW_CSV",
+                    help="write profiles/traffic.json from an ncu raw-page CSV and exit")
     return ap.parse_args()
 
 
@@ -224,6 +226,63 @@ def config_dict(case, passes):
             "output_dtype": "f32", "layout": "NHWC / FHxFWxC",
             "l2": "flushed between timed steps by an untimed 256 MiB write",
             "inputs": f"{case.dist} draws, seed {case.seed}"}
+
+
+TRAFFIC_SOURCES = {
+    "fwd": ["dwc_rows.cuh", "dwc_device.cuh", "dwc_rows_{dt}.cu"],
+    "bwd_data": ["dwc_rows.cuh", "dwc_device.cuh", "dwc_rows_{dt}.cu"],
+    "bwd_filter": ["dwc_fgrad.cuh", "dwc_rows.cuh", "dwc_device.cuh", "dwc_general.cu",
+                   "dwc_fgrad_{dt}.cu"],
+}
+
+
+def _sources_sha(pass_name, dtype):
+    import hashlib
+    rels = [os.path.join("depthwise_convolution_nhwc_gb300", "csrc", f.format(dt=dtype))
+            for f in TRAFFIC_SOURCES[pass_name]]
+    h = hashlib.sha256()
+    for rel in rels:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return rels, h.hexdigest()
+
+
+def record_traffic(raw_csv, workload):
+    """Write profiles/traffic.json from `ncu -i <report> --page raw --csv` output that holds
+    the kernels of one timed step: DRAM bytes per launch of each pass, with a hash of the
+    kernel sources so that the entry is ignored once a kernel changes."""
+    import csv
+    case = get_case(workload)
+    rows = list(csv.reader(open(raw_csv)))
+    hdr, units, data = rows[0], rows[1], rows[2:]
+    ix = {h: i for i, h in enumerate(hdr)}
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+
+    def dram(d):
+        return sum(float(d[ix[k]]) * scale[units[ix[k]]]
+                   for k in ("dram__bytes_read.sum", "dram__bytes_write.sum"))
+    per = {"fwd": 0.0, "bwd_data": 0.0, "bwd_filter": 0.0}
+    for d in data:
+        name = d[ix["Kernel Name"]]
+        if "rows_kernel" in name:
+            flip = name.split("<", 1)[1].split(",")[6].strip()
+            per["bwd_data" if flip == "1" else "fwd"] += dram(d)
+        elif "fgrad_kernel" in name or "reduce_slices" in name:
+            per["bwd_filter"] += dram(d)
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        tab = json.load(open(path))
+    except (OSError, ValueError):
+        tab = {}
+    for p_, b in per.items():
+        if b > 0:
+            rels, sha = _sources_sha(p_, case.dtype)
+            tab[f"{p_}:{case.name}"] = {"bytes_per_launch": b, "sources": rels,
+                                        "source_sha256": sha,
+                                        "from": os.path.basename(raw_csv)}
+    with open(path, "w") as f:
+        json.dump(tab, f, indent=1, sort_keys=True)
+    print(json.dumps(tab, indent=1, sort_keys=True))
 
 
 def load_traffic(kernel_key):
@@ -429,6 +488,9 @@ def run_ours(args, case, passes):
 
 def main():
     args = parse_args()
+    if args.record_traffic:
+        record_traffic(args.record_traffic, args.workload)
+        return
     case = get_case(args.workload)
     passes = tuple(p for p in args.passes.split(",") if p)
     for p in passes:
