@@ -25,11 +25,13 @@
 
 namespace dwc {
 
-// Filter rows per warp: as many as fit ~120 accumulator+window registers.
-template <int FH, int FW>
+// Filter rows per warp (RF: accumulators + x windows take 4*RF*FW registers) and the CTAs
+// per SM the shared-memory window is sized for (MINB).
+template <int FH, int FW, int RF_ = 0, int MINB_ = 0>
 struct FgradTile {
-    static constexpr int kFit = 120 / (4 * FW);
-    static constexpr int RF = kFit < 1 ? 1 : (kFit > FH ? FH : kFit);
+    static constexpr int kFit = FH == 7 ? 2 : 120 / (4 * FW);  // 7x7: 2 rows timed fastest
+    static constexpr int RF = RF_ > 0 ? RF_ : (kFit < 1 ? 1 : (kFit > FH ? FH : kFit));
+    static constexpr int MINB = MINB_ > 0 ? MINB_ : 1;
 };
 
 struct FgradArgs {
@@ -48,11 +50,11 @@ struct FgradArgs {
 constexpr int kFgradMaxComputeWarps = 8;
 constexpr int kFgradMaxThreads = (kFgradMaxComputeWarps + 1) * 32;
 
-template <typename T, int FH, int FW>
-__global__ void __launch_bounds__(kFgradMaxThreads, 1)
+template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
+__global__ void __launch_bounds__(kFgradMaxThreads, Tile::MINB)
 fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
              const FgradArgs a) {
-    constexpr int RF = FgradTile<FH, FW>::RF;
+    constexpr int RF = Tile::RF;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* xfull = reinterpret_cast<uint64_t*>(smem);
     uint64_t* xempty = xfull + a.nx;
@@ -279,7 +281,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     }
 }
 
-template <int FH, int FW>
+template <int FH, int FW, class Tile = FgradTile<FH, FW>>
 struct FgradPlan {
     int nwf, nwc, fhc, chunks, cblocks, Z, rows_per_slice, nblocks, bps, nx, ny;
     uint32_t x_bytes, y_bytes, y_off;
@@ -288,10 +290,11 @@ struct FgradPlan {
 };
 
 // Shapes of the launch for one problem (shared by the workspace query and the launch).
-template <int FH, int FW>
-bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW>& P) {
-    constexpr int RF = FgradTile<FH, FW>::RF;
+template <int FH, int FW, class Tile = FgradTile<FH, FW>>
+bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW, Tile>& P) {
+    constexpr int RF = Tile::RF;
     const DeviceInfo& dev = device_info();
+    const size_t smem_cap = std::min<size_t>(dev.max_smem_optin, 233472 / Tile::MINB - 1024);
     P.nblocks = (OW + FW - 1) / FW;
     P.owp = P.nblocks * FW;
     P.pwx = P.owp + FW - 1;
@@ -305,7 +308,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW>& P) {
     for (; nwf_max >= 1; --nwf_max) {
         const size_t need = 512 + static_cast<size_t>(nwf_max * RF + 2) * P.x_bytes +
                             static_cast<size_t>(P.ny) * P.y_bytes;
-        if (need <= static_cast<size_t>(dev.max_smem_optin)) break;
+        if (need <= smem_cap) break;
     }
     if (nwf_max < 1) return false;
     // ... then the fewest chunks, with the groups spread evenly over them
@@ -325,7 +328,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW>& P) {
     P.cblocks = (C + kBN - 1) / kBN;
     const long long rows = static_cast<long long>(N) * OH;
     const long long per_z = static_cast<long long>(P.cblocks) * P.chunks;
-    const int ctas_per_sm = P.smem * 2 + 2048 <= 233472u ? 2 : 1;
+    const int ctas_per_sm = Tile::MINB;
     long long Z = (static_cast<long long>(dev.sm_count) * ctas_per_sm + per_z - 1) / per_z;
     Z = std::max<long long>(1, std::min<long long>(Z, rows));
     P.rows_per_slice = static_cast<int>((rows + Z - 1) / Z);
@@ -333,11 +336,11 @@ bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW>& P) {
     return true;
 }
 
-template <typename T, int FH, int FW>
+template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
 cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     const int e = static_cast<int>(sizeof(T));
-    FgradPlan<FH, FW> P;
-    if (!fgrad_plan<FH, FW>(p.N, p.OH, p.OW, p.C, e, P)) return cudaErrorNotSupported;
+    FgradPlan<FH, FW, Tile> P;
+    if (!fgrad_plan<FH, FW, Tile>(p.N, p.OH, p.OW, p.C, e, P)) return cudaErrorNotSupported;
     if (p.N == 0 || p.OH == 0 || p.OW == 0) {
         return cudaMemsetAsync(p.dw, 0, sizeof(float) * FH * FW * p.C, p.stream);
     }
@@ -371,7 +374,7 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     a.Z = P.Z; a.rows_per_slice = P.rows_per_slice; a.nblocks = P.nblocks; a.bps = P.bps;
     a.nx = P.nx; a.ny = P.ny; a.x_bytes = P.x_bytes; a.y_bytes = P.y_bytes; a.y_off = P.y_off;
 
-    auto kern = fgrad_kernel<T, FH, FW>;
+    auto kern = fgrad_kernel<T, FH, FW, Tile>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

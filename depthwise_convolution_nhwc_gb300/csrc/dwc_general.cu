@@ -105,10 +105,10 @@ __global__ void general_bwd_filter_kernel(const T* __restrict__ x, const T* __re
     }
 }
 
-// out[i] = sum_z part[z * count + i].  Eight lanes share one output: lane g of the group
-// sums the contiguous slice range [g*zc, (g+1)*zc) and the eight partial sums are combined
+// out[i] = sum_z part[z * count + i].  One warp per output: lane g of the group
+// sums the contiguous slice range [g*zc, (g+1)*zc) and the 32 partial sums are combined
 // by a fixed butterfly, so the order of additions is the same on every run.
-constexpr int kReduceGroup = 8;
+constexpr int kReduceGroup = 32;
 
 __global__ void reduce_slices_kernel(const float* __restrict__ part, int slices, size_t count,
                                      float* __restrict__ out) {

@@ -1,6 +1,7 @@
-// dwc_rows_f16.cu -- row-streaming forward / backward-data kernels, f16 inputs.
-#include "dwc_rows.cuh"
+// dwc_rows_f16.cu -- forward / backward-data kernels, f16 inputs (tensor-core kernel for
+// filters from 9 taps, row-streaming kernel below).
+#include "dwc_mma.cuh"
 
 namespace dwc {
-cudaError_t launch_rows_f16(const RowConv& p) { return launch_rows_dispatch<__half>(p); }
+cudaError_t launch_rows_f16(const RowConv& p) { return launch_rows_or_mma<__half>(p); }
 }  // namespace dwc

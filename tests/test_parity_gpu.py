@@ -75,6 +75,13 @@ FAST = [
     C_(1, 9, 9, 64, 5, p=4),        # padding larger than (F-1)/2
     C_(1, 1, 1, 64, 3),             # single pixel
     C_(2, 5, 40, 64, 11),
+    # shapes aimed at the 16-bit tensor-core kernel (filters from 9 taps): wide rows (many
+    # groups per tile, short bands), no padding, padding beyond (F-1)/2, odd sizes
+    C_(1, 20, 200, 64, 11),
+    C_(1, 9, 9, 64, 9, p=0),
+    C_(1, 9, 9, 64, 9, p=8),
+    C_(2, 37, 23, 16, 21),
+    C_(1, 3, 70, 8, 27, p=13),
 ]
 
 
