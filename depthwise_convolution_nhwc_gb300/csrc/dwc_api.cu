@@ -38,11 +38,17 @@ PerDevice* device_state() {
     PerDevice& s = g_dev[d];
     if (!s.ready) {
         cudaDeviceProp prop;
-        if (cudaGetDeviceProperties(&prop, d) != cudaSuccess) return nullptr;
+        if (cudaGetDeviceProperties(&prop, d) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
         s.info.sm_count = prop.multiProcessorCount;
         s.info.max_smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
         void* addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) {
+            (void)cudaGetLastError();  // do not leave the failure to the next launch check
+            return nullptr;
+        }
         s.status = static_cast<unsigned int*>(addr);
         s.ready = true;
     }

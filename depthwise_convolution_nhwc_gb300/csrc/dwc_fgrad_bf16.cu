@@ -1,6 +1,12 @@
-// dwc_fgrad_bf16.cu -- filter-gradient kernels, bf16 inputs.
+// dwc_fgrad_bf16.cu -- filter-gradient kernels, bf16 inputs (tensor-core and CUDA-core).
 #include "dwc_fgrad.cuh"
+#include "dwc_mma_fgrad.cuh"
 
 namespace dwc {
-cudaError_t launch_filter_grad_bf16(const FilterGrad& p) { return launch_fgrad_dispatch<__nv_bfloat16>(p); }
+cudaError_t launch_filter_grad_bf16(const FilterGrad& p) {
+    // tensor-core kernel where it serves the shape, CUDA-core kernel otherwise
+    const cudaError_t err = launch_mma_fgrad<__nv_bfloat16>(p);
+    if (err != cudaErrorNotSupported) return err;
+    return launch_fgrad_dispatch<__nv_bfloat16>(p);
+}
 }  // namespace dwc

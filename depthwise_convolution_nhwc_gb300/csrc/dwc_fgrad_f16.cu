@@ -1,6 +1,12 @@
-// dwc_fgrad_f16.cu -- filter-gradient kernels, f16 inputs.
+// dwc_fgrad_f16.cu -- filter-gradient kernels, f16 inputs (tensor-core and CUDA-core).
 #include "dwc_fgrad.cuh"
+#include "dwc_mma_fgrad.cuh"
 
 namespace dwc {
-cudaError_t launch_filter_grad_f16(const FilterGrad& p) { return launch_fgrad_dispatch<__half>(p); }
+cudaError_t launch_filter_grad_f16(const FilterGrad& p) {
+    // tensor-core kernel where it serves the shape, CUDA-core kernel otherwise
+    const cudaError_t err = launch_mma_fgrad<__half>(p);
+    if (err != cudaErrorNotSupported) return err;
+    return launch_fgrad_dispatch<__half>(p);
+}
 }  // namespace dwc

@@ -25,13 +25,14 @@ __global__ void general_fwd_kernel(const T* __restrict__ x, const T* __restrict_
         const int ow = static_cast<int>(q % OW); q /= OW;
         const int oh = static_cast<int>(q % OH); q /= OH;
         const int n = static_cast<int>(q);
+        // only the taps that land inside the image: fh in [p - oh*s, H + p - oh*s)
+        const int fh0 = max(0, p - oh * s), fh1 = min(FH, H + p - oh * s);
+        const int fw0 = max(0, p - ow * s), fw1 = min(FW, W + p - ow * s);
         float acc = 0.f;
-        for (int fh = 0; fh < FH; ++fh) {
+        for (int fh = fh0; fh < fh1; ++fh) {
             const int ih = oh * s + fh - p;
-            if (ih < 0 || ih >= H) continue;
-            for (int fw = 0; fw < FW; ++fw) {
+            for (int fw = fw0; fw < fw1; ++fw) {
                 const int iw = ow * s + fw - p;
-                if (iw < 0 || iw >= W) continue;
                 acc = fmaf(to_f32(x[((static_cast<size_t>(n) * H + ih) * W + iw) * C + c]),
                            to_f32(w[(static_cast<size_t>(fh) * FW + fw) * C + c]), acc);
             }
@@ -53,17 +54,18 @@ __global__ void general_bwd_data_kernel(const T* __restrict__ dy, const T* __res
         const int iw = static_cast<int>(q % W); q /= W;
         const int ih = static_cast<int>(q % H); q /= H;
         const int n = static_cast<int>(q);
+        // taps whose output lies inside: 0 <= ih + p - fh <= (OH - 1) * s
+        const int fh0 = max(0, ih + p - (OH - 1) * s), fh1 = min(FH, ih + p + 1);
+        const int fw0 = max(0, iw + p - (OW - 1) * s), fw1 = min(FW, iw + p + 1);
         float acc = 0.f;
-        for (int fh = 0; fh < FH; ++fh) {
+        for (int fh = fh0; fh < fh1; ++fh) {
             const int th = ih + p - fh;
-            if (th < 0 || th % s) continue;
+            if (th % s) continue;
             const int oh = th / s;
-            if (oh >= OH) continue;
-            for (int fw = 0; fw < FW; ++fw) {
+            for (int fw = fw0; fw < fw1; ++fw) {
                 const int tw = iw + p - fw;
-                if (tw < 0 || tw % s) continue;
+                if (tw % s) continue;
                 const int ow = tw / s;
-                if (ow >= OW) continue;
                 acc = fmaf(to_f32(dy[((static_cast<size_t>(n) * OH + oh) * OW + ow) * C + c]),
                            to_f32(w[(static_cast<size_t>(fh) * FW + fw) * C + c]), acc);
             }

@@ -326,12 +326,15 @@ cudaError_t launch_mma_inst(const RowConv& p) {
     return cudaGetLastError();
 }
 
-// Filter sizes from which the tensor-core kernel is used for 16-bit inputs.
-constexpr int kMmaMinFilter = 9;
+// Where the tensor-core kernel beats the row-streaming kernel for 16-bit inputs (timed on
+// the stage shapes: from 13-tap filters on rows of at least 24 outputs; on narrower maps
+// most of each tile's K-steps fall into the padding).
+constexpr int kMmaMinFilter = 13;
+constexpr int kMmaMinWidth = 24;
 
 template <typename T>
 cudaError_t launch_rows_or_mma(const RowConv& p) {
-    if (p.FH >= kMmaMinFilter || p.FW >= kMmaMinFilter) {
+    if (p.FW >= kMmaMinFilter && p.OW >= kMmaMinWidth) {
         const cudaError_t err = p.flip ? launch_mma_inst<T, true>(p) : launch_mma_inst<T, false>(p);
         if (err != cudaErrorNotSupported) return err;
     }
