@@ -28,10 +28,26 @@ sys.path.insert(0, ROOT)
 
 METRIC = "DWC fwd+bwd TFLOP/s and GB/s on 1 GB300, % of roofline, per filter size"
 PASSES_ALL = ("fwd", "bwd_data", "bwd_filter")
-# launches of this library's kernels per pass on the fast path
+PASS_CODE = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2}
+DTYPE_CODE = {"f32": 0, "bf16": 1, "f16": 2}
+# launches of this library's kernels per pass (every kernel family)
 LAUNCHES = {"fwd": 1, "bwd_data": 1, "bwd_filter": 2}
-KERNEL_NAMES = {"fwd": "rows_kernel<flip=false>", "bwd_data": "rows_kernel<flip=true>",
-                "bwd_filter": "fgrad_kernel + reduce_slices_kernel"}
+FAMILY = {0: "general", 1: "cuda-core", 2: "tensor-core"}
+# kernels per pass and family (the library's dwc_path tells which family serves a call)
+KERNEL_NAMES = {
+    ("fwd", 0): "general_fwd_kernel", ("bwd_data", 0): "general_bwd_data_kernel",
+    ("bwd_filter", 0): "general_bwd_filter_kernel + reduce_slices_kernel",
+    ("fwd", 1): "rows_kernel<flip=false>", ("bwd_data", 1): "rows_kernel<flip=true>",
+    ("bwd_filter", 1): "fgrad_kernel + reduce_slices_kernel",
+    ("fwd", 2): "mma_rows_kernel<flip=false>", ("bwd_data", 2): "mma_rows_kernel<flip=true>",
+    ("bwd_filter", 2): "mma_fgrad_kernel + reduce_slices_kernel",
+}
+
+
+def kernel_family(dwc, case, pass_name):
+    """0 general, 1 CUDA-core, 2 tensor-core kernels (asked of the library itself)."""
+    return dwc.path(pass_name, None, None, None, case.N, case.H, case.W, case.C, case.FH,
+                    case.FW, case.stride, case.pad, DTYPE_CODE[case.dtype])
 
 
 def parse_args():
@@ -47,6 +63,11 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--record-traffic", metavar="NCU_RAW_CSV",
                     help="write profiles/traffic.json from an ncu raw-page CSV and exit")
+    ap.add_argument("--sweep", metavar="DTYPES",
+                    help="time every pass of the filter sweep for these input dtypes "
+                         "(comma separated, e.g. f32,bf16): one JSON line per sweep point")
+    ap.add_argument("--sweep-steps", type=int, default=20)
+    ap.add_argument("--sweep-md", metavar="FILE", help="also write the sweep as a markdown table")
     return ap.parse_args()
 
 
@@ -228,18 +249,13 @@ def config_dict(case, passes):
             "inputs": f"{case.dist} draws, seed {case.seed}"}
 
 
-TRAFFIC_SOURCES = {
-    "fwd": ["dwc_rows.cuh", "dwc_device.cuh", "dwc_rows_{dt}.cu"],
-    "bwd_data": ["dwc_rows.cuh", "dwc_device.cuh", "dwc_rows_{dt}.cu"],
-    "bwd_filter": ["dwc_fgrad.cuh", "dwc_rows.cuh", "dwc_device.cuh", "dwc_general.cu",
-                   "dwc_fgrad_{dt}.cu"],
-}
-
-
-def _sources_sha(pass_name, dtype):
+def _sources_sha():
+    """Hash of every kernel source file: a traffic entry counts only for the exact sources
+    it was captured with."""
     import hashlib
-    rels = [os.path.join("depthwise_convolution_nhwc_gb300", "csrc", f.format(dt=dtype))
-            for f in TRAFFIC_SOURCES[pass_name]]
+    cdir = os.path.join("depthwise_convolution_nhwc_gb300", "csrc")
+    rels = sorted(os.path.join(cdir, f) for f in os.listdir(os.path.join(ROOT, cdir))
+                  if f.endswith((".cu", ".cuh", ".h")))
     h = hashlib.sha256()
     for rel in rels:
         with open(os.path.join(ROOT, rel), "rb") as f:
@@ -264,9 +280,13 @@ def record_traffic(raw_csv, workload):
     per = {"fwd": 0.0, "bwd_data": 0.0, "bwd_filter": 0.0}
     for d in data:
         name = d[ix["Kernel Name"]]
-        if "rows_kernel" in name:
-            flip = name.split("<", 1)[1].split(",")[6].strip()
-            per["bwd_data" if flip == "1" else "fwd"] += dram(d)
+        targs = name.split("<", 1)[1].split(",") if "<" in name else []
+        if "mma_rows_kernel" in name:    # <T, FLIP>
+            flip = targs[1].split(">")[0].strip()
+            per["bwd_data" if flip in ("1", "true") else "fwd"] += dram(d)
+        elif "rows_kernel" in name:      # <T, FH, FW, R, TM, MINB, FLIP, P>
+            flip = targs[6].strip()
+            per["bwd_data" if flip in ("1", "true") else "fwd"] += dram(d)
         elif "fgrad_kernel" in name or "reduce_slices" in name:
             per["bwd_filter"] += dram(d)
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -276,7 +296,7 @@ def record_traffic(raw_csv, workload):
         tab = {}
     for p_, b in per.items():
         if b > 0:
-            rels, sha = _sources_sha(p_, case.dtype)
+            rels, sha = _sources_sha()
             tab[f"{p_}:{case.name}"] = {"bytes_per_launch": b, "sources": rels,
                                         "source_sha256": sha,
                                         "from": os.path.basename(raw_csv)}
@@ -296,12 +316,8 @@ def load_traffic(kernel_key):
     ent = tab.get(kernel_key)
     if not ent:
         return None
-    import hashlib
-    h = hashlib.sha256()
-    for rel in ent.get("sources", []):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
-    if h.hexdigest() != ent.get("source_sha256"):
+    rels, sha = _sources_sha()
+    if rels != ent.get("sources") or sha != ent.get("source_sha256"):
         return None
     return ent.get("bytes_per_launch")
 
@@ -346,12 +362,115 @@ def run_e2e(args, case, passes, run_pass, x, w, dy, y, dx, dw, stream, world, fl
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        t = torch.tensor([e2e_ms], device=x.device, dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t.item())
     e2e_value = world * args.e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
 
     return e2e_value, h2d, d2h
+
+
+def roofline_entry(rl, case, pass_name, family, seconds, peaks):
+    """Roofline of one pass: achieved algorithmic bytes or FLOPs per launch over the
+    measured time, against the peak of the resource that bounds it."""
+    _, bound = rl.roofline_time_s(case, pass_name, peaks, tensor=family == 2)
+    if bound == "hbm":
+        achieved = rl.compulsory_bytes(case, pass_name) / seconds / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+        src = ("measured HBM copy (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
+               else "fallback HBM figure")
+    elif bound == "tensor":
+        achieved = rl.valid_flops(case) / seconds / 1e12
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+        src = ("measured bf16 cuBLAS burst (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
+               else "fallback bf16 figure")
+    else:
+        achieved = rl.valid_flops(case) / seconds / 1e12
+        peak, unit = peaks["fp32_tflops"], "TFLOP/s"
+        src = "fp32 FFMA peak derived: 152 SMs x 128 lanes x 2 x 2070 MHz"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": None,
+            "kernel": KERNEL_NAMES[(pass_name, family)], "pass": pass_name, "peak_source": src}
+
+
+def run_sweep(args):
+    """Every pass of every sweep point: mean device time over --sweep-steps launches, L2
+    flushed before each, one JSON line per point."""
+    import torch
+    import depthwise_convolution_nhwc_gb300 as dwc
+    from depthwise_convolution_nhwc_gb300 import roofline as rl
+    from depthwise_convolution_nhwc_gb300.inputs import sweep_cases
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    dwc.load_library()
+    stream = torch.cuda.current_stream()
+    peaks = rl.load_peaks()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    rows = []
+    for case in sweep_cases(tuple(args.sweep.split(","))):
+        x, w, dy = (t.to(dev) for t in (case.x(), case.w(), case.dy()))
+        y = torch.empty((case.N, case.OH, case.OW, case.C), device=dev, dtype=torch.float32)
+        dx = torch.empty((case.N, case.H, case.W, case.C), device=dev, dtype=torch.float32)
+        dw = torch.empty((case.FH, case.FW, case.C), device=dev, dtype=torch.float32)
+        ws = dwc.workspace(dwc.bwd_filter_workspace_size(x.shape, (case.FH, case.FW), 1,
+                                                         case.pad, x.dtype), dev)
+        run = {"fwd": lambda: dwc.fwd(x, w, 1, case.pad, out=y),
+               "bwd_data": lambda: dwc.bwd_data(dy, w, (case.H, case.W), 1, case.pad, out=dx),
+               "bwd_filter": lambda: dwc.bwd_filter(x, dy, (case.FH, case.FW), 1, case.pad,
+                                                    out=dw, ws=ws)}
+        line = {"sweep": case.name, "dtype": case.dtype, "N": case.N, "H": case.H, "W": case.W,
+                "C": case.C, "F": case.FH}
+        for name in PASSES_ALL:
+            for _ in range(3):
+                run[name]()
+            evs = []
+            for k in range(args.sweep_steps):
+                flush.fill_(float(k))
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                run[name]()
+                e1.record(stream)
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            t = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e-3
+            fam = kernel_family(dwc, case, name)
+            roof = roofline_entry(rl, case, name, fam, t, peaks)
+            line[name] = {"us": t * 1e6, "tflops": rl.nominal_flops(case) / t / 1e12,
+                          "gbs": rl.compulsory_bytes(case, name) / t / 1e9,
+                          "bound": roof["bound"], "roofline_frac": roof["frac"],
+                          "family": FAMILY[fam]}
+        if dwc.device_status() != 0:
+            raise SystemExit(f"a kernel reported a timed-out wait in {case.name}")
+        rows.append(line)
+        print(json.dumps(line), flush=True)
+    if args.sweep_md:
+        write_sweep_md(args, rows)
+
+
+def write_sweep_md(args, rows):
+    cmd = " ".join(["python", "bench.py"] + sys.argv[1:])
+    out = [f"# Filter sweep, every pass, one GB300\n",
+           f"Command: `{cmd}`\n",
+           f"Mean device time of {args.sweep_steps} launches per pass (CUDA events on the "
+           "launching stream, 256 MiB L2 flush before each launch, 3 warm-up launches). "
+           "TFLOP/s are nominal (2·N·OH·OW·C·FH·FW); roofline fraction against the bound "
+           "named (hbm: compulsory bytes at the measured HBM copy rate; alu: valid FLOPs at "
+           "the derived fp32 FFMA peak; tensor: valid FLOPs at the measured bf16 peak). "
+           "Kernel family: cc = CUDA-core, tc = tensor-core.\n",
+           "| dtype | N×H×W×C | F | fwd µs | fwd TF/s | fwd roof | bwd_data µs | bwd_data roof "
+           "| bwd_filter µs | bwd_filter TF/s | bwd_filter roof | families |",
+           "|---|---|---|---|---|---|---|---|---|---|---|---|"]
+    ab = {"cuda-core": "cc", "tensor-core": "tc", "general": "gen"}
+    for r in rows:
+        f, d, g = r["fwd"], r["bwd_data"], r["bwd_filter"]
+        out.append(f"| {r['dtype']} | {r['N']}×{r['H']}×{r['W']}×{r['C']} | {r['F']} "
+                   f"| {f['us']:.1f} | {f['tflops']:.1f} | {f['roofline_frac']:.2f} {f['bound']} "
+                   f"| {d['us']:.1f} | {d['roofline_frac']:.2f} {d['bound']} "
+                   f"| {g['us']:.1f} | {g['tflops']:.1f} | {g['roofline_frac']:.2f} {g['bound']} "
+                   f"| {ab[f['family']]}/{ab[d['family']]}/{ab[g['family']]} |")
+    with open(args.sweep_md, "w") as fh:
+        fh.write("\n".join(out) + "\n")
 
 
 def run_ours(args, case, passes):
@@ -441,35 +560,24 @@ def run_ours(args, case, passes):
 
     # --- roofline of the dominant kernel ----------------------------------------------
     peaks = rl.load_peaks()
+    fam = {n: kernel_family(dwc, case, n) for n in passes}
     mean_ms = {n: statistics.fmean(v) for n, v in per_pass.items()}
     dom = max(mean_ms, key=mean_ms.get)
-    t_dom = mean_ms[dom] * 1e-3
-    t_roof, bound = rl.roofline_time_s(case, dom, peaks)
-    if bound == "hbm":
-        achieved = rl.compulsory_bytes(case, dom) / t_dom / 1e9
-        peak, unit = peaks["hbm_gbs"], "GB/s"
-    else:
-        achieved = rl.valid_flops(case) / t_dom / 1e12
-        peak, unit = peaks["fp32_tflops"], "TFLOP/s"
-    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": load_traffic(f"{dom}:{case.name or 'default'}"),
-            "kernel": KERNEL_NAMES[dom], "pass": dom,
-            "peak_source": ("measured HBM copy (MEASURED_PEAKS.json)" if bound == "hbm" and
-                            peaks["source"] == "measured" else
-                            "fp32 FFMA peak derived: 152 SMs x 128 lanes x 2 x 2070 MHz"
-                            if bound == "alu" else "fallback")}
+    roof = roofline_entry(rl, case, dom, fam[dom], mean_ms[dom] * 1e-3, peaks)
+    roof["traffic"] = load_traffic(f"{dom}:{case.name or 'default'}")
     passes_out = {}
     for n in passes:
         t = mean_ms[n] * 1e-3
-        tr, b = rl.roofline_time_s(case, n, peaks)
+        tr, b = rl.roofline_time_s(case, n, peaks, tensor=fam[n] == 2)
         passes_out[n] = {"ms": mean_ms[n], "ms_median": statistics.median(per_pass[n]),
+                         "kernel": KERNEL_NAMES[(n, fam[n])],
                          "tflops_nominal": rl.nominal_flops(case) / t / 1e12,
                          "tflops_valid": rl.valid_flops(case) / t / 1e12,
                          "gbs": rl.compulsory_bytes(case, n) / t / 1e9,
                          "roofline_frac": tr / t, "roofline_bound": b}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
             "data": "synthetic", "config": config_dict(case, passes),
             "gbs": sum(rl.compulsory_bytes(case, n) for n in passes) * args.steps * world
                    / (total_ms * 1e-3) / 1e9,
@@ -478,6 +586,7 @@ def run_ours(args, case, passes):
                      "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
                     if e2e_value is not None else None),
             "gpu_launches": args.steps * sum(LAUNCHES[n] for n in passes),
+            "kernels": {n: KERNEL_NAMES[(n, fam[n])] for n in passes},
             "clocks": clocks}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(case, passes, args.cpu_seconds)
@@ -490,6 +599,9 @@ def main():
     args = parse_args()
     if args.record_traffic:
         record_traffic(args.record_traffic, args.workload)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     case = get_case(args.workload)
     passes = tuple(p for p in args.passes.split(",") if p)

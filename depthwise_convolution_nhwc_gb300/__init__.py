@@ -205,7 +205,8 @@ def device_status(stream=None) -> int:
 
 
 def path(pass_: str, a, b, out, N, H, W, C, FH, FW, stride, pad, dtype_code) -> int:
-    """1 if the fast kernels serve this call, 0 for the general kernels, -1 if invalid."""
+    """Kernel family of a call: 2 tensor-core kernels (16-bit inputs), 1 fast CUDA-core
+    kernels, 0 general kernels, -1 invalid arguments."""
     p = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2}[pass_]
     return int(load_library().dwc_path(p, a, b, out, N, H, W, C, FH, FW, stride, pad,
                                        dtype_code))

@@ -297,7 +297,19 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
     if (pass < 0 || pass > 2) return -1;
     if (check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P) != DWC_OK) return -1;
     if (!fast_eligible(P, a, b, out)) return 0;
-    if (pass == kPassBwdFilter && fast_fgrad_floats(P) == 0) return 0;
+    if (pass == kPassBwdFilter) {
+        if (fast_fgrad_floats(P) == 0) return 0;
+        return P.e == 2 && tensor_core_fgrad(N, C, P.OH, P.OW, FH, FW) ? 2 : 1;
+    }
+    if (P.e == 2) {
+        // the same RowConv the entry points build (backward data: over dy, output H x W)
+        const RowConv rc = pass == kPassFwd
+            ? RowConv{a, b, nullptr, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype,
+                      nullptr, nullptr}
+            : RowConv{a, b, nullptr, N, P.OH, P.OW, C, H, W, FH, FW, FH - 1 - pad, FW - 1 - pad,
+                      true, P.dtype, nullptr, nullptr};
+        if (tensor_core_rows(rc)) return 2;
+    }
     return 1;
 }
 

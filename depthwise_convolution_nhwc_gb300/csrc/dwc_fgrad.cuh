@@ -17,22 +17,50 @@
 //    every x row enters shared memory once per CTA.
 //  * Each compute warp owns RF filter rows and one strip of output columns; a lane owns two
 //    channels and keeps RF x FW fp32x2 accumulators plus, per owned row, a circular register
-//    window of the FW x values that the current output column multiplies.  Each dy element
-//    is loaded once and used for RF*FW packed FMAs.
+//    window of U >= FW x values (the FW that the current output column multiplies and the
+//    next ones).  Each dy element is loaded once and used for RF*FW packed FMAs.
 #pragma once
+
+#include <type_traits>
 
 #include "dwc_rows.cuh"
 
 namespace dwc {
 
-// Filter rows per warp (RF: accumulators + x windows take 4*RF*FW registers) and the CTAs
-// per SM the shared-memory window is sized for (MINB).
-template <int FH, int FW, int RF_ = 0, int MINB_ = 0>
+// Filter rows per warp (RF: accumulators + x windows take about 4*RF*FW registers), the
+// CTAs per SM the shared-memory window is sized for (MINB) and the period U of the circular
+// x window (any U >= FW works; output columns are processed in blocks of U, so a U that
+// divides the row width leaves no padded columns).
+template <int FH, int FW, int RF_ = 0, int MINB_ = 0, int U_ = 0>
 struct FgradTile {
     static constexpr int kFit = FH == 7 ? 2 : 120 / (4 * FW);  // 7x7: 2 rows timed fastest
     static constexpr int RF = RF_ > 0 ? RF_ : (kFit < 1 ? 1 : (kFit > FH ? FH : kFit));
     static constexpr int MINB = MINB_ > 0 ? MINB_ : 1;
+    static constexpr int U = U_ > 0 ? U_ : FW;
+    static_assert(U >= FW, "the window must hold FW columns");
 };
+
+// A second window period per filter width: a multiple of 7 (the widths of the usual
+// 224-pixel pyramids, 112/56/28/14/7, are multiples of 7) at least FW, where the longer
+// register window does not spill (none for 9, 15 and 29..31).
+template <int FW>
+struct FgradAltPeriod {
+    static constexpr int U = FW <= 3 ? 4 : (FW <= 7 ? 7 : (FW == 9 ? 9 : (FW <= 13 ? 14 :
+                             (FW == 15 ? 15 : (FW <= 27 ? 28 : FW)))));
+};
+
+// (the default tile itself where the second period equals FW, so nothing is built twice)
+template <int F>
+using FgradAltTile = typename std::conditional<FgradAltPeriod<F>::U == F, FgradTile<F, F>,
+                                               FgradTile<F, F, 0, 0, FgradAltPeriod<F>::U>>::type;
+
+// The alternative period runs when it pads the row to fewer columns than blocks of FW do.
+template <int FW>
+bool fgrad_use_alt_period(int OW) {
+    constexpr int UA = FgradAltPeriod<FW>::U;
+    if (UA == FW) return false;
+    return (OW + UA - 1) / UA * UA < (OW + FW - 1) / FW * FW;
+}
 
 struct FgradArgs {
     float* part;           // [Z][FH][FW][C] partial sums
@@ -41,7 +69,7 @@ struct FgradArgs {
     int nwf, nwc;          // compute warps: filter-row groups x column strips
     int fhc, chunks, cblocks, Z;
     int rows_per_slice;    // flattened output rows per slice
-    int nblocks, bps;      // FW-wide column blocks per row, blocks per strip
+    int nblocks, bps;      // U-wide column blocks per row, blocks per strip
     int nx, ny;            // ring slots for x rows and dy rows
     uint32_t x_bytes, y_bytes;
     uint32_t y_off;        // byte offset of the dy ring after the x ring
@@ -55,6 +83,7 @@ __global__ void __launch_bounds__(kFgradMaxThreads, Tile::MINB)
 fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
              const FgradArgs a) {
     constexpr int RF = Tile::RF;
+    constexpr int U = Tile::U;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* xfull = reinterpret_cast<uint64_t*>(smem);
     uint64_t* xempty = xfull + a.nx;
@@ -204,9 +233,9 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 xs[f] = reinterpret_cast<const T*>(xring + static_cast<size_t>(sl) * a.x_bytes) + 2 * lane;
             }
             if (blk0 < blk1) {
-                // circular window: column c of the padded x row sits in slot c mod FW
-                float2 win[RF][FW];
-                const int c0 = blk0 * FW;
+                // circular window: column c of the padded x row sits in slot c mod U
+                float2 win[RF][U];
+                const int c0 = blk0 * U;
 #pragma unroll
                 for (int f = 0; f < RF; ++f)
 #pragma unroll
@@ -215,16 +244,16 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                                             : make_float2(0.f, 0.f);
 #pragma unroll 1
                 for (int blk = blk0; blk < blk1; ++blk) {
-                    const int cb0 = blk * FW;
+                    const int cb0 = blk * U;
 #pragma unroll
-                    for (int u = 0; u < FW; ++u) {
+                    for (int u = 0; u < U; ++u) {
                         const float2 g = Elem<T>::load_pair(ys + (cb0 + u) * kBN);
 #pragma unroll
                         for (int f = 0; f < RF; ++f) {
                             if (!live[f]) continue;
-                            win[f][(u + FW - 1) % FW] = Elem<T>::load_pair(xs[f] + (cb0 + u + FW - 1) * kBN);
+                            win[f][(u + FW - 1) % U] = Elem<T>::load_pair(xs[f] + (cb0 + u + FW - 1) * kBN);
 #pragma unroll
-                            for (int t = 0; t < FW; ++t) fma2(acc[f][t], win[f][(u + t) % FW], g);
+                            for (int t = 0; t < FW; ++t) fma2(acc[f][t], win[f][(u + t) % U], g);
                         }
                     }
                 }
@@ -295,8 +324,8 @@ bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW, Tile>& P)
     constexpr int RF = Tile::RF;
     const DeviceInfo& dev = device_info();
     const size_t smem_cap = std::min<size_t>(dev.max_smem_optin, 233472 / Tile::MINB - 1024);
-    P.nblocks = (OW + FW - 1) / FW;
-    P.owp = P.nblocks * FW;
+    P.nblocks = (OW + Tile::U - 1) / Tile::U;
+    P.owp = P.nblocks * Tile::U;
     P.pwx = P.owp + FW - 1;
     if (P.pwx > 256) return false;
     P.x_bytes = static_cast<uint32_t>(P.pwx * kBN * e);
@@ -390,11 +419,18 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     return launch_reduce_slices(p.workspace, P.Z, static_cast<size_t>(FH) * FW * p.C, p.dw, p.stream);
 }
 
-template <int FH, int FW>
+template <int FH, int FW, class Tile = FgradTile<FH, FW>>
 size_t fgrad_workspace_inst(int N, int OH, int OW, int C, int e) {
-    FgradPlan<FH, FW> P;
-    if (!fgrad_plan<FH, FW>(N, OH, OW, C, e, P)) return 0;
+    FgradPlan<FH, FW, Tile> P;
+    if (!fgrad_plan<FH, FW, Tile>(N, OH, OW, C, e, P)) return 0;
     return static_cast<size_t>(P.Z) * FH * FW * static_cast<size_t>(C);
+}
+
+// Workspace of the launch that launch_fgrad_dispatch makes for this problem.
+template <int F>
+size_t fgrad_workspace_dispatch(int N, int OH, int OW, int C, int e) {
+    return fgrad_use_alt_period<F>(OW) ? fgrad_workspace_inst<F, F, FgradAltTile<F>>(N, OH, OW, C, e)
+                                       : fgrad_workspace_inst<F, F>(N, OH, OW, C, e);
 }
 
 #define DWC_FGRAD_FILTERS(X) X(3) X(5) X(7) X(9) X(11) X(13) X(15) X(17) X(19) X(21) X(23) X(25) X(27) X(29) X(31)
@@ -403,9 +439,11 @@ template <typename T>
 cudaError_t launch_fgrad_dispatch(const FilterGrad& p) {
     if (p.FH != p.FW) return cudaErrorNotSupported;
     switch (p.FH) {
-#define DWC_FGRAD_CASE(F) \
-    case F:               \
-        return launch_fgrad_inst<T, F, F>(p);
+#define DWC_FGRAD_CASE(F)                                          \
+    case F:                                                        \
+        return fgrad_use_alt_period<F>(p.OW)                       \
+                   ? launch_fgrad_inst<T, F, F, FgradAltTile<F>>(p) \
+                   : launch_fgrad_inst<T, F, F>(p);
         DWC_FGRAD_FILTERS(DWC_FGRAD_CASE)
 #undef DWC_FGRAD_CASE
         default:

@@ -9,4 +9,8 @@ cudaError_t launch_filter_grad_bf16(const FilterGrad& p) {
     if (err != cudaErrorNotSupported) return err;
     return launch_fgrad_dispatch<__nv_bfloat16>(p);
 }
+
+bool tensor_core_fgrad(int N, int C, int OH, int OW, int FH, int FW) {
+    return mma_fgrad_workspace_floats(N, C, OH, OW, FH, FW) > 0;
+}
 }  // namespace dwc

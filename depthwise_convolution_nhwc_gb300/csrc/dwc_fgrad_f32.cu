@@ -18,7 +18,7 @@ size_t cuda_core_fgrad_workspace_floats(int N, int OH, int OW, int C, int FH, in
     switch (FH) {
 #define DWC_FGRAD_WS(F) \
     case F:             \
-        return fgrad_workspace_inst<F, F>(N, OH, OW, C, e);
+        return fgrad_workspace_dispatch<F>(N, OH, OW, C, e);
         DWC_FGRAD_FILTERS(DWC_FGRAD_WS)
 #undef DWC_FGRAD_WS
         default:

@@ -107,43 +107,46 @@ __global__ void general_bwd_filter_kernel(const T* __restrict__ x, const T* __re
     }
 }
 
-// out[i] = sum_z part[z * count + i].  One warp per output: lane g of the group
-// sums the contiguous slice range [g*zc, (g+1)*zc) and the 32 partial sums are combined
-// by a fixed butterfly, so the order of additions is the same on every run.
-constexpr int kReduceGroup = 32;
+// out[i] = sum_z part[z * count + i].  A block covers 32 consecutive outputs (one per lane,
+// so every slice row is read with coalesced 128-byte loads); warp k sums the contiguous
+// slice range [k*zc, (k+1)*zc) and warp 0 adds the 8 partial sums in warp order.  The order
+// of additions depends only on `slices`, so runs are bit-identical.
+constexpr int kReduceWarps = 8;
 
-__global__ void reduce_slices_kernel(const float* __restrict__ part, int slices, size_t count,
-                                     float* __restrict__ out) {
-    constexpr int kGroupsPerWarp = 32 / kReduceGroup;
-    const int lane = threadIdx.x & 31;
-    const int g = lane % kReduceGroup;
-    const int zc = (slices + kReduceGroup - 1) / kReduceGroup;
-    const int z0 = g * zc, z1 = min(slices, z0 + zc);
-    const size_t warp = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const size_t warps = (static_cast<size_t>(gridDim.x) * blockDim.x) >> 5;
-    // the loop bound depends only on the warp, so every lane reaches every shuffle
-    for (size_t base = warp * kGroupsPerWarp; base < count; base += warps * kGroupsPerWarp) {
-        const size_t i = base + lane / kReduceGroup;
+__global__ void __launch_bounds__(kReduceWarps * 32)
+reduce_slices_kernel(const float* __restrict__ part, int slices, size_t count,
+                     float* __restrict__ out) {
+    __shared__ float partial[kReduceWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int zc = (slices + kReduceWarps - 1) / kReduceWarps;
+    const int z0 = min(slices, warp * zc), z1 = min(slices, z0 + zc);
+    for (size_t base = static_cast<size_t>(blockIdx.x) * 32; base < count;
+         base += static_cast<size_t>(gridDim.x) * 32) {
+        const size_t i = base + lane;
         float s = 0.f;
         if (i < count) {
-#pragma unroll 4
+#pragma unroll 8
             for (int z = z0; z < z1; ++z) s += part[static_cast<size_t>(z) * count + i];
         }
+        partial[warp][lane] = s;
+        __syncthreads();
+        if (warp == 0 && i < count) {
+            float t = partial[0][lane];
 #pragma unroll
-        for (int m = 1; m < kReduceGroup; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
-        if (g == 0 && i < count) out[i] = s;
+            for (int k = 1; k < kReduceWarps; ++k) t += partial[k][lane];
+            out[i] = t;
+        }
+        __syncthreads();
     }
 }
 
 cudaError_t launch_reduce_slices(const float* part, int slices, size_t count, float* out,
                                  cudaStream_t stream) {
     if (count == 0) return cudaSuccess;
-    const int threads = 256;
-    const size_t per_block = threads / kReduceGroup;
-    const size_t blocks = std::min<size_t>((count + per_block - 1) / per_block,
-                                           static_cast<size_t>(device_info().sm_count) * 16);
-    reduce_slices_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(part, slices,
-                                                                               count, out);
+    const size_t blocks = std::min<size_t>((count + 31) / 32,
+                                           static_cast<size_t>(device_info().sm_count) * 32);
+    reduce_slices_kernel<<<static_cast<unsigned>(blocks), kReduceWarps * 32, 0, stream>>>(
+        part, slices, count, out);
     return cudaGetLastError();
 }
 

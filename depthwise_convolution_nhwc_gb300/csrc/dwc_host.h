@@ -87,6 +87,11 @@ bool filter_grad_supported(int FH, int FW);
 // Workspace floats the filter-gradient kernel needs (0 if it cannot run this shape).
 size_t filter_grad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int elem_bytes);
 
+// Whether 16-bit inputs of this shape run on the tensor-core kernels rather than the
+// CUDA-core ones (forward / backward data as the RowConv describes it; filter gradient).
+bool tensor_core_rows(const RowConv& p);
+bool tensor_core_fgrad(int N, int C, int OH, int OW, int FH, int FW);
+
 // Fallback kernels.
 cudaError_t launch_general_fwd(const GeneralConv& p);
 cudaError_t launch_general_bwd_data(const GeneralConv& p);

@@ -332,9 +332,13 @@ cudaError_t launch_mma_inst(const RowConv& p) {
 constexpr int kMmaMinFilter = 13;
 constexpr int kMmaMinWidth = 24;
 
+inline bool mma_rows_wanted(const RowConv& p) {
+    return p.FW >= kMmaMinFilter && p.OW >= kMmaMinWidth;
+}
+
 template <typename T>
 cudaError_t launch_rows_or_mma(const RowConv& p) {
-    if (p.FW >= kMmaMinFilter && p.OW >= kMmaMinWidth) {
+    if (mma_rows_wanted(p)) {
         const cudaError_t err = p.flip ? launch_mma_inst<T, true>(p) : launch_mma_inst<T, false>(p);
         if (err != cudaErrorNotSupported) return err;
     }

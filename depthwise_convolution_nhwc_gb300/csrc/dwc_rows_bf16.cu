@@ -1,7 +1,13 @@
 // dwc_rows_bf16.cu -- forward / backward-data kernels, bf16 inputs (tensor-core kernel for
-// filters from 9 taps, row-streaming kernel below).
+// filters from 13 taps on rows of at least 24 outputs, row-streaming kernel otherwise).
 #include "dwc_mma.cuh"
 
 namespace dwc {
 cudaError_t launch_rows_bf16(const RowConv& p) { return launch_rows_or_mma<__nv_bfloat16>(p); }
+
+bool tensor_core_rows(const RowConv& p) {
+    MmaArgs a;
+    size_t smem = 0;
+    return mma_rows_wanted(p) && mma_plan(p, a, smem);
+}
 }  // namespace dwc

@@ -76,8 +76,13 @@ def load_peaks(path: str | None = None) -> dict:
                 "bf16_tflops_sustained": 1700.0, "fp32_tflops": fp32, "source": "fallback"}
 
 
-def roofline_time_s(c: Case, which: str, peaks: dict) -> tuple[float, str]:
-    """Lower bound on one pass's time and the resource that sets it ("hbm" or "alu")."""
+def roofline_time_s(c: Case, which: str, peaks: dict, tensor: bool = False) -> tuple[float, str]:
+    """Lower bound on one pass's time and the resource that sets it: "hbm", "alu" (fp32
+    FFMA peak, CUDA-core kernels) or "tensor" (measured 16-bit tensor peak, for the
+    tensor-core kernels)."""
     t_mem = compulsory_bytes(c, which) / (peaks["hbm_gbs"] * 1e9)
-    t_alu = valid_flops(c) / (peaks["fp32_tflops"] * 1e12)
-    return (t_mem, "hbm") if t_mem >= t_alu else (t_alu, "alu")
+    if tensor:
+        t_cmp, kind = valid_flops(c) / (peaks["bf16_tflops"] * 1e12), "tensor"
+    else:
+        t_cmp, kind = valid_flops(c) / (peaks["fp32_tflops"] * 1e12), "alu"
+    return (t_mem, "hbm") if t_mem >= t_cmp else (t_cmp, kind)

@@ -106,5 +106,11 @@ def test_path_selection_host_logic(lib):
     assert p(0, C=8, dtype=1) == 1
     assert p(0, C=12, dtype=1) == 0            # bf16 needs C % 8 == 0
     assert p(0, FH=33, FW=33, pad=16, H=40, W=40) == 0
+    # 16-bit inputs: tensor-core kernels for large filters on wide rows
+    big = dict(H=56, W=56, C=64, FH=31, FW=31, pad=15)
+    assert p(0, **big, dtype=1) == 2 and p(1, **big, dtype=2) == 2 and p(2, **big, dtype=1) == 2
+    assert p(0, **big) == 1 and p(2, **big) == 1          # fp32 stays on CUDA cores
+    assert p(0, **dict(big, FH=7, FW=7, pad=3), dtype=1) == 1
+    assert p(0, **dict(big, W=16), dtype=1) == 1          # narrow rows: row-streaming kernel
     # an unaligned (but element-aligned) pointer falls back to the general kernels
     assert lib.dwc_path(0, FAKE + 4, None, None, 1, 8, 8, 16, 3, 3, 1, 1, 0) == 0
