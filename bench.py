@@ -32,7 +32,7 @@ PASS_CODE = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2}
 DTYPE_CODE = {"f32": 0, "bf16": 1, "f16": 2}
 # launches of this library's kernels per pass (every kernel family)
 LAUNCHES = {"fwd": 1, "bwd_data": 1, "bwd_filter": 2}
-FAMILY = {0: "general", 1: "cuda-core", 2: "tensor-core"}
+FAMILY = {0: "general", 1: "cuda-core", 2: "tensor-core", 3: "small-map"}
 # kernels per pass and family (the library's dwc_path tells which family serves a call)
 KERNEL_NAMES = {
     ("fwd", 0): "general_fwd_kernel", ("bwd_data", 0): "general_bwd_data_kernel",
@@ -41,6 +41,8 @@ KERNEL_NAMES = {
     ("bwd_filter", 1): "fgrad_kernel + reduce_slices_kernel",
     ("fwd", 2): "mma_rows_kernel<flip=false>", ("bwd_data", 2): "mma_rows_kernel<flip=true>",
     ("bwd_filter", 2): "mma_fgrad_kernel + reduce_slices_kernel",
+    ("fwd", 3): "small_rows_kernel", ("bwd_data", 3): "small_rows_kernel",
+    ("bwd_filter", 3): "small_fgrad_kernel + reduce_slices_kernel",
 }
 
 
@@ -457,11 +459,12 @@ def write_sweep_md(args, rows):
            "TFLOP/s are nominal (2·N·OH·OW·C·FH·FW); roofline fraction against the bound "
            "named (hbm: compulsory bytes at the measured HBM copy rate; alu: valid FLOPs at "
            "the derived fp32 FFMA peak; tensor: valid FLOPs at the measured bf16 peak). "
-           "Kernel family: cc = CUDA-core, tc = tensor-core.\n",
+           "Kernel family: cc = CUDA-core row / filter-gradient kernels, tc = tensor-core, "
+           "sm = small-map kernels.\n",
            "| dtype | N×H×W×C | F | fwd µs | fwd TF/s | fwd roof | bwd_data µs | bwd_data roof "
            "| bwd_filter µs | bwd_filter TF/s | bwd_filter roof | families |",
            "|---|---|---|---|---|---|---|---|---|---|---|---|"]
-    ab = {"cuda-core": "cc", "tensor-core": "tc", "general": "gen"}
+    ab = {"cuda-core": "cc", "tensor-core": "tc", "general": "gen", "small-map": "sm"}
     for r in rows:
         f, d, g = r["fwd"], r["bwd_data"], r["bwd_filter"]
         out.append(f"| {r['dtype']} | {r['N']}×{r['H']}×{r['W']}×{r['C']} | {r['F']} "

@@ -205,8 +205,8 @@ def device_status(stream=None) -> int:
 
 
 def path(pass_: str, a, b, out, N, H, W, C, FH, FW, stride, pad, dtype_code) -> int:
-    """Kernel family of a call: 2 tensor-core kernels (16-bit inputs), 1 fast CUDA-core
-    kernels, 0 general kernels, -1 invalid arguments."""
+    """Kernel family of a call: 3 small-map kernels (maps up to 16x16), 2 tensor-core
+    kernels (16-bit inputs), 1 fast CUDA-core kernels, 0 general kernels, -1 invalid."""
     p = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2}[pass_]
     return int(load_library().dwc_path(p, a, b, out, N, H, W, C, FH, FW, stride, pad,
                                        dtype_code))

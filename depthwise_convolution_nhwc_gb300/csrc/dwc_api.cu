@@ -152,6 +152,15 @@ bool fast_eligible(const Problem& P, const void* a, const void* b, const void* o
 dwc_status_t map_cuda(cudaError_t err) { return err == cudaSuccess ? DWC_OK : DWC_ERR_CUDA; }
 
 cudaError_t launch_rows(const RowConv& rc) {
+    if (small_map_serves(rc.H, rc.W, rc.OH, rc.OW, rc.FW, rc.pad_w)) {
+        cudaError_t err;
+        switch (rc.dtype) {
+            case kF32: err = launch_small_rows_f32(rc); break;
+            case kBF16: err = launch_small_rows_bf16(rc); break;
+            default: err = launch_small_rows_f16(rc); break;
+        }
+        if (err != cudaErrorNotSupported) return err;
+    }
     switch (rc.dtype) {
         case kF32: return launch_rows_f32(rc);
         case kBF16: return launch_rows_bf16(rc);
@@ -160,6 +169,15 @@ cudaError_t launch_rows(const RowConv& rc) {
 }
 
 cudaError_t launch_fgrad(const FilterGrad& fg) {
+    {
+        cudaError_t err;
+        switch (fg.dtype) {
+            case kF32: err = launch_small_fgrad_f32(fg); break;
+            case kBF16: err = launch_small_fgrad_bf16(fg); break;
+            default: err = launch_small_fgrad_f16(fg); break;
+        }
+        if (err != cudaErrorNotSupported) return err;
+    }
     switch (fg.dtype) {
         case kF32: return launch_filter_grad_f32(fg);
         case kBF16: return launch_filter_grad_bf16(fg);
@@ -167,8 +185,19 @@ cudaError_t launch_fgrad(const FilterGrad& fg) {
     }
 }
 
+size_t small_fgrad_floats(const Problem& P) {
+    switch (P.dtype) {
+        case kF32: return small_fgrad_workspace_floats_f32(P.N, P.H, P.W, P.C, P.OH, P.OW, P.FH, P.FW, P.p);
+        case kBF16: return small_fgrad_workspace_floats_bf16(P.N, P.H, P.W, P.C, P.OH, P.OW, P.FH, P.FW, P.p);
+        default: return small_fgrad_workspace_floats_f16(P.N, P.H, P.W, P.C, P.OH, P.OW, P.FH, P.FW, P.p);
+    }
+}
+
+// Workspace of the fast filter-gradient kernels: the largest of the kernels that may serve
+// the call (the small-map kernel falls back to the others if its launch is refused).
 size_t fast_fgrad_floats(const Problem& P) {
-    return filter_grad_workspace_floats(P.N, P.OH, P.OW, P.C, P.FH, P.FW, P.e);
+    return std::max(filter_grad_workspace_floats(P.N, P.OH, P.OW, P.C, P.FH, P.FW, P.e),
+                    small_fgrad_floats(P));
 }
 
 }  // namespace
@@ -299,8 +328,12 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
     if (!fast_eligible(P, a, b, out)) return 0;
     if (pass == kPassBwdFilter) {
         if (fast_fgrad_floats(P) == 0) return 0;
+        if (small_fgrad_floats(P) > 0) return 3;
         return P.e == 2 && tensor_core_fgrad(N, C, P.OH, P.OW, FH, FW) ? 2 : 1;
     }
+    if (pass == kPassFwd ? small_map_serves(H, W, P.OH, P.OW, FW, pad)
+                         : small_map_serves(P.OH, P.OW, H, W, FW, FW - 1 - pad))
+        return 3;
     if (P.e == 2) {
         // the same RowConv the entry points build (backward data: over dy, output H x W)
         const RowConv rc = pass == kPassFwd

@@ -38,6 +38,9 @@ struct FgradTile {
     static constexpr int MINB = MINB_ > 0 ? MINB_ : 1;
     static constexpr int U = U_ > 0 ? U_ : FW;
     static_assert(U >= FW, "the window must hold FW columns");
+    // compute warps per CTA where one filter row per warp leaves the registers for more
+    // (the launch bound caps registers at 128 per thread for 13 warps, 168 for 12), else 8
+    static constexpr int MAXCW = (RF == 1 && FW <= 19) ? 12 : ((RF == 1 && FW <= 27) ? 11 : 8);
 };
 
 // A second window period per filter width: a multiple of 7 (the widths of the usual
@@ -75,11 +78,8 @@ struct FgradArgs {
     uint32_t y_off;        // byte offset of the dy ring after the x ring
 };
 
-constexpr int kFgradMaxComputeWarps = 8;
-constexpr int kFgradMaxThreads = (kFgradMaxComputeWarps + 1) * 32;
-
 template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
-__global__ void __launch_bounds__(kFgradMaxThreads, Tile::MINB)
+__global__ void __launch_bounds__((Tile::MAXCW + 1) * 32, Tile::MINB)
 fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
              const FgradArgs a) {
     constexpr int RF = Tile::RF;
@@ -331,25 +331,40 @@ bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW, Tile>& P)
     P.x_bytes = static_cast<uint32_t>(P.pwx * kBN * e);
     P.y_bytes = static_cast<uint32_t>(P.owp * kBN * e);
     P.ny = 2;
-    // largest row group whose x window fits in shared memory ...
+    // Filter-row groups per CTA (nwf, one warp each) and column strips (nwc): the x window of
+    // nwf*RF rows must fit in shared memory; among the fitting choices take the one with the
+    // most useful warp slots, counting warps up to 12 (about what hides the latencies of one
+    // CTA per SM), discounted by the chunk count (each chunk streams every x and dy row of
+    // its slice again); the weights were fitted to timings of the stage shapes.
     const int groups = (FH + RF - 1) / RF;  // RF-row groups needed to cover the filter
-    int nwf_max = std::min(groups, kFgradMaxComputeWarps);
-    for (; nwf_max >= 1; --nwf_max) {
-        const size_t need = 512 + static_cast<size_t>(nwf_max * RF + 2) * P.x_bytes +
+    double best = -1.0;
+    P.nwf = 0;
+    for (int nwf = std::min(groups, Tile::MAXCW); nwf >= 1; --nwf) {
+        const size_t need = 512 + static_cast<size_t>(nwf * RF + 2) * P.x_bytes +
                             static_cast<size_t>(P.ny) * P.y_bytes;
-        if (need <= smem_cap) break;
+        if (need > smem_cap) continue;
+        const int chunks = (groups + nwf - 1) / nwf;
+        if ((groups + chunks - 1) / chunks != nwf) continue;  // same chunks, fewer warps: seen
+        const int nwc0 = std::max(1, std::min(Tile::MAXCW / nwf, P.nblocks));
+        const int bps = (P.nblocks + nwc0 - 1) / nwc0;
+        const int nwc = (P.nblocks + bps - 1) / bps;
+        // the strip sums at the end reuse the ring: [nwc][nwf][RF][FW][32] float2
+        if (512 + static_cast<size_t>(nwc) * nwf * RF * FW * 32 * sizeof(float2) > smem_cap) continue;
+        const double useful = static_cast<double>(groups) / (chunks * nwf) *
+                              static_cast<double>(P.nblocks) / (nwc * bps);
+        const double score = useful * std::min(nwf * nwc, 12) / (1.0 + 0.2 * chunks);
+        if (score > best * (1.0 + 1e-9)) {
+            best = score;
+            P.nwf = nwf;
+            P.nwc = nwc;
+            P.bps = bps;
+        }
     }
-    if (nwf_max < 1) return false;
-    // ... then the fewest chunks, with the groups spread evenly over them
-    const int chunks = (groups + nwf_max - 1) / nwf_max;
-    P.nwf = (groups + chunks - 1) / chunks;
+    if (P.nwf < 1) return false;
     P.fhc = P.nwf * RF;
     P.nx = P.fhc + 2;
     P.smem = 512 + static_cast<size_t>(P.nx) * P.x_bytes + static_cast<size_t>(P.ny) * P.y_bytes;
     P.chunks = (FH + P.fhc - 1) / P.fhc;
-    P.nwc = std::max(1, std::min(kFgradMaxComputeWarps / P.nwf, P.nblocks));
-    P.bps = (P.nblocks + P.nwc - 1) / P.nwc;
-    P.nwc = (P.nblocks + P.bps - 1) / P.bps;
     // strip reduction buffer reuses the ring
     const size_t red = static_cast<size_t>(P.nwc) * P.nwf * RF * FW * 32 * sizeof(float2);
     if (red > P.smem - 512) P.smem = 512 + red;
@@ -357,8 +372,10 @@ bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW, Tile>& P)
     P.cblocks = (C + kBN - 1) / kBN;
     const long long rows = static_cast<long long>(N) * OH;
     const long long per_z = static_cast<long long>(P.cblocks) * P.chunks;
+    // One wave: every CTA runs the same number of rows, so a grid a few CTAs larger than
+    // the resident capacity would take a second wave for those few; round down.
     const int ctas_per_sm = Tile::MINB;
-    long long Z = (static_cast<long long>(dev.sm_count) * ctas_per_sm + per_z - 1) / per_z;
+    long long Z = static_cast<long long>(dev.sm_count) * ctas_per_sm / per_z;
     Z = std::max<long long>(1, std::min<long long>(Z, rows));
     P.rows_per_slice = static_cast<int>((rows + Z - 1) / Z);
     P.Z = static_cast<int>((rows + P.rows_per_slice - 1) / P.rows_per_slice);

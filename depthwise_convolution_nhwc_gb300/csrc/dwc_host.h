@@ -87,6 +87,22 @@ bool filter_grad_supported(int FH, int FW);
 // Workspace floats the filter-gradient kernel needs (0 if it cannot run this shape).
 size_t filter_grad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int elem_bytes);
 
+// Small-map kernels (H, W, OH, OW <= 16; stride 1; C a multiple of 16 bytes; 16-byte
+// aligned tensors): whole images staged per 32-channel block, only the taps that can meet
+// the image are run.  cudaErrorNotSupported when the map is larger or the filter small
+// enough for the other kernels to be faster; small_map_serves tells the forward /
+// backward-data choice, a nonzero small_fgrad_workspace_floats_* the filter-gradient one.
+bool small_map_serves(int H, int W, int OH, int OW, int FW, int pad_w);
+cudaError_t launch_small_rows_f32(const RowConv& p);
+cudaError_t launch_small_rows_bf16(const RowConv& p);
+cudaError_t launch_small_rows_f16(const RowConv& p);
+cudaError_t launch_small_fgrad_f32(const FilterGrad& p);
+cudaError_t launch_small_fgrad_bf16(const FilterGrad& p);
+cudaError_t launch_small_fgrad_f16(const FilterGrad& p);
+size_t small_fgrad_workspace_floats_f32(int N, int H, int W, int C, int OH, int OW, int FH, int FW, int pad);
+size_t small_fgrad_workspace_floats_bf16(int N, int H, int W, int C, int OH, int OW, int FH, int FW, int pad);
+size_t small_fgrad_workspace_floats_f16(int N, int H, int W, int C, int OH, int OW, int FH, int FW, int pad);
+
 // Whether 16-bit inputs of this shape run on the tensor-core kernels rather than the
 // CUDA-core ones (forward / backward data as the RowConv describes it; filter gradient).
 bool tensor_core_rows(const RowConv& p);

@@ -226,7 +226,8 @@ inline bool mma_fgrad_plan(int N, int C, int OH, int OW, int FH, int FW, MmaFgAr
     const int cblocks = C / kMmaCB;
     const int ctas = smem * 2 + 2048 <= 233472u ? 2 : 1;
     const long long total_bands = static_cast<long long>(N) * a.bands;
-    long long Z = (static_cast<long long>(device_info().sm_count) * ctas + cblocks - 1) / cblocks;
+    // one wave of equal CTAs (rounding up would leave a few CTAs for a second wave)
+    long long Z = static_cast<long long>(device_info().sm_count) * ctas / cblocks;
     Z = std::max<long long>(1, std::min<long long>(Z, total_bands));
     a.bands_per_slice = static_cast<int>((total_bands + Z - 1) / Z);
     a.Z = static_cast<int>((total_bands + a.bands_per_slice - 1) / a.bands_per_slice);

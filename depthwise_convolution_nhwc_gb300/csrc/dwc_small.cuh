@@ -1,0 +1,568 @@
+// dwc_small.cuh -- small feature maps (W, OW, H, OH <= 16): direct kernels that run only
+// the filter taps that can meet the image.
+//
+// On a small map most taps of a large filter land in the zero padding for every output
+// (a 7x7 map under a 31x31 filter: at most 49 of 961 taps are real), and the row-streaming
+// kernels, which run every tap of a row tile, spend most of their FMAs on zeros.  The pages'
+// trimming of padding rows ("Flash-DWC: Making Depthwise Convolution Compute-Efficient on
+// GPUs", §4.4) is taken here to its end for maps that fit in shared memory whole:
+//
+//  * A CTA owns a block of 32 channels (one per lane) and stages whole images of it
+//    (cp.async, 16-byte chunks, double-buffered across work units).
+//  * Forward / backward data: each warp computes one output row oh of one image; for every
+//    input row ih that meets a filter row (fh = ih - oh + pad_h), the input row is held in
+//    registers as two sets of column pairs, {x[2k], x[2k+1]} and {x[2k-1], x[2k]}, so that
+//    the packed FMA of tap offset d = fw - pad_w updates the output pair (2k, 2k+1) with the
+//    input pair starting at 2k + d.  Offsets run over [-DR, DR], the taps that can meet a
+//    map of this width; the window of filter rows that meet the image, 2*DR+1 taps each,
+//    is copied once per channel block (cp.async, zero fill for taps outside the filter).
+//  * Filter gradient: each warp owns two window rows fh (mirror images in the window, so
+//    that the warps' work is even) and accumulates dw[fh][d + pad_w] for d in [-DR, DR],
+//    two taps per packed sum of x[ow + d] * dy[ow]; slices of images are summed afterwards
+//    in a fixed order.
+//
+// MAXW (8 or 16) bounds the map width; DR (3, 7, 11, 15) bounds the tap offsets.
+#pragma once
+
+#include <algorithm>
+
+#include "dwc_device.cuh"
+#include "dwc_host.h"
+
+namespace dwc {
+
+constexpr int kSmCh = 32;        // channels per CTA (one per lane)
+constexpr int kSmMaxWarps = 16;
+constexpr int kSmMaxMap = 16;    // largest H, W, OH, OW served
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+// 16-byte copy, or 16 zero bytes when `valid` is false (nothing is read then)
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int K>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory");
+}
+
+// Pair of adjacent columns (x[i], x[i+1]) of a register row for i in [-1, MAXW - 1], with
+// zeros outside [0, MAXW): even i from `xe`, odd i from `xo` (xo[j] = (x[2j-1], x[2j])).
+template <int MAXW>
+__device__ __forceinline__ float2 col_pair(const float2 (&xe)[MAXW / 2], const float2 (&xo)[MAXW / 2 + 1],
+                                           int i) {
+    return (i & 1) == 0 ? xe[i >> 1] : xo[(i + 1) >> 1];
+}
+
+template <typename T, int MAXW>
+__device__ __forceinline__ void load_row_pairs(const T* row, int lane, float2 (&xe)[MAXW / 2],
+                                               float2 (&xo)[MAXW / 2 + 1]) {
+    float v[MAXW];
+#pragma unroll
+    for (int i = 0; i < MAXW; ++i) v[i] = to_f32(row[i * kSmCh + lane]);
+#pragma unroll
+    for (int k = 0; k < MAXW / 2; ++k) xe[k] = make_float2(v[2 * k], v[2 * k + 1]);
+    xo[0] = make_float2(0.f, v[0]);
+#pragma unroll
+    for (int k = 1; k < MAXW / 2; ++k) xo[k] = make_float2(v[2 * k - 1], v[2 * k]);
+    xo[MAXW / 2] = make_float2(v[MAXW - 1], 0.f);
+}
+
+// Stages one image block [rows][MAXW][32] of channels c0.. (columns [0, cols) copied; the
+// columns [cols, MAXW) are zeroed once at kernel start and never written by the copies).
+template <typename T, int MAXW>
+__device__ __forceinline__ void stage_image(T* dst, const T* src_img, int rows, int cols, int C,
+                                            int c0, int tid, int nthreads) {
+    constexpr int kPerChunk = 16 / static_cast<int>(sizeof(T));
+    constexpr int kChunks = kSmCh / kPerChunk;  // 16-byte chunks per pixel
+    const int cvalid = min(kSmCh, C - c0);      // a multiple of kPerChunk (host check)
+    const int total = rows * cols * kChunks;
+    for (int i = tid; i < total; i += nthreads) {
+        const int q = i % kChunks;
+        const int px = i / kChunks;
+        const int r = px / cols, col = px - r * cols;
+        if (q * kPerChunk < cvalid)
+            cp_async16(dst + (r * MAXW + col) * kSmCh + q * kPerChunk,
+                       src_img + (static_cast<size_t>(r) * cols + col) * C + c0 + q * kPerChunk);
+    }
+}
+
+struct SmallArgs {
+    const void* in;
+    const void* w;
+    float* out;
+    int N, H, W, C, OH, OW, FH, FW, pad_h, pad_w;
+    int flip;           // filter rotated by 180 degrees (backward data)
+    int fh_lo, nfh;     // filter rows that meet the image for some output row
+    int G;              // images per work unit
+    int groups;         // work units per channel block
+    uint32_t units;     // cblocks * groups, channel block slowest
+    uint32_t buf_elems; // elements of one staged buffer (G images)
+    uint32_t win_off;   // byte offset of the filter window
+};
+
+template <typename T, int MAXW, int DR>
+__global__ void __launch_bounds__(kSmMaxWarps * 32, 1) small_rows_kernel(const SmallArgs a) {
+    constexpr int NJ = 2 * DR + 1;
+    extern __shared__ __align__(128) unsigned char smem[];
+    T* xbuf = reinterpret_cast<T*>(smem);                          // [2][G][H][MAXW][32]
+    T* win = reinterpret_cast<T*>(smem + a.win_off);               // [nfh][NJ][32]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+    const T* X = static_cast<const T*>(a.in);
+    const T* Wt = static_cast<const T*>(a.w);
+    const int img = a.H * MAXW * kSmCh;
+
+    const uint32_t per_cta = (a.units + gridDim.x - 1) / gridDim.x;
+    const uint32_t u_begin = blockIdx.x * per_cta;
+    const uint32_t u_end = min(a.units, u_begin + per_cta);
+    if (u_begin >= u_end) return;
+
+    if (a.W < MAXW) {
+        const int zc = MAXW - a.W;
+        for (int i = tid; i < 2 * a.G * a.H * zc * kSmCh; i += nthreads) {
+            const int ch = i % kSmCh, px = i / kSmCh;
+            const int col = a.W + px % zc, rr = px / zc;  // rr runs over [2][G][H]
+            xbuf[(rr * MAXW + col) * kSmCh + ch] = T(0.f);
+        }
+    }
+    auto stage = [&](uint32_t u, int buf) {
+        const int cb = static_cast<int>(u / a.groups);
+        const int n0 = static_cast<int>(u % a.groups) * a.G;
+        for (int g = 0; g < a.G && n0 + g < a.N; ++g)
+            stage_image<T, MAXW>(xbuf + buf * a.buf_elems + g * img,
+                                 X + static_cast<size_t>(n0 + g) * a.H * a.W * a.C, a.H, a.W, a.C,
+                                 cb * kSmCh, tid, nthreads);
+        cp_async_commit();
+    };
+
+    // Copy groups, in commit order: image(u_begin), then per unit u [window(u) when the
+    // channel block changes], image(u + 1) (empty at the end).  Waiting for all but the
+    // newest group therefore covers the window and the image of unit u.
+    stage(u_begin, 0);
+    int cur_cb = -1;
+    for (uint32_t u = u_begin; u < u_end; ++u) {
+        const int buf = static_cast<int>((u - u_begin) & 1u);
+        const int cb = static_cast<int>(u / a.groups);
+        const int c0 = cb * kSmCh;
+        if (cb != cur_cb) {
+            // filter window of this channel block: win[r][j] = filt(fh_lo + r, j - DR + pad_w),
+            // zero where the tap lies outside the filter (whole 16-byte chunks of channels)
+            constexpr int kPerChunk = 16 / static_cast<int>(sizeof(T));
+            constexpr int kChunks = kSmCh / kPerChunk;
+            const int cvalid = min(kSmCh, a.C - c0);
+            for (int i = tid; i < a.nfh * NJ * kChunks; i += nthreads) {
+                const int q = i % kChunks, rj = i / kChunks;
+                const int fh = a.fh_lo + rj / NJ, fw = rj % NJ - DR + a.pad_w;
+                const bool valid = fw >= 0 && fw < a.FW && q * kPerChunk < cvalid;
+                const int sh = a.flip ? a.FH - 1 - fh : fh;
+                const int sw = a.flip ? a.FW - 1 - fw : fw;
+                const T* src = valid ? Wt + (static_cast<size_t>(sh) * a.FW + sw) * a.C + c0 + q * kPerChunk
+                                     : Wt;
+                cp_async16_zfill(win + rj * kSmCh + q * kPerChunk, src, valid);
+            }
+            cp_async_commit();
+            cur_cb = cb;
+        }
+        if (u + 1 < u_end) stage(u + 1, buf ^ 1);
+        else cp_async_commit();  // keeps the newest group the next image for the wait below
+        cp_async_wait<1>();
+        __syncthreads();
+
+        const int n0 = static_cast<int>(u % a.groups) * a.G;
+        const bool lane_ok = c0 + lane < a.C;
+        for (int q = warp; q < a.G * a.OH; q += nwarps) {
+            const int g = q / a.OH, oh = q - g * a.OH;
+            const int n = n0 + g;
+            if (n >= a.N) break;
+            const T* xg = xbuf + buf * a.buf_elems + g * img;
+            float2 acc[MAXW / 2];
+#pragma unroll
+            for (int k = 0; k < MAXW / 2; ++k) acc[k] = make_float2(0.f, 0.f);
+            const int ih_lo = max(0, oh - a.pad_h), ih_hi = min(a.H, oh - a.pad_h + a.FH);
+            for (int ih = ih_lo; ih < ih_hi; ++ih) {
+                float2 xe[MAXW / 2], xo[MAXW / 2 + 1];
+                load_row_pairs<T, MAXW>(xg + ih * MAXW * kSmCh, lane, xe, xo);
+                const T* wr = win + (ih - oh + a.pad_h - a.fh_lo) * NJ * kSmCh + lane;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const float wv = to_f32(wr[j * kSmCh]);
+                    const float2 w2 = make_float2(wv, wv);
+#pragma unroll
+                    for (int k = 0; k < MAXW / 2; ++k) {
+                        const int i = 2 * k + j - DR;  // first input column of the pair
+                        if (i < -1 || i > MAXW - 1) continue;
+                        fma2(acc[k], col_pair<MAXW>(xe, xo, i), w2);
+                    }
+                }
+            }
+            if (lane_ok) {
+                float* o = a.out + (static_cast<size_t>(n) * a.OH + oh) * a.OW * a.C + c0 + lane;
+#pragma unroll
+                for (int k = 0; k < MAXW / 2; ++k) {
+                    if (2 * k < a.OW) __stcs(o + static_cast<size_t>(2 * k) * a.C, acc[k].x);
+                    if (2 * k + 1 < a.OW) __stcs(o + static_cast<size_t>(2 * k + 1) * a.C, acc[k].y);
+                }
+            }
+        }
+        __syncthreads();  // the buffer is re-staged and the window may be replaced
+    }
+    cp_async_wait<0>();
+}
+
+struct SmallFgArgs {
+    const void* x;
+    const void* dy;
+    float* part;        // [Z][nfh][FW][C]
+    int N, H, W, C, OH, OW, FH, FW, pad_h, pad_w;
+    int fh_lo, nfh;
+    int cblocks;
+    int G, ipc;                   // images per staged group, images per slice
+    uint32_t xb_elems, db_elems;  // elements of one staged x / dy buffer (G images)
+    uint32_t d_off;               // byte offset of the dy buffers
+};
+
+// Filter gradient of one window row held by a warp: two taps per packed accumulator,
+// acc[p] = (tap d, tap d + 1) with d = 2p - DR, so DR + 1 pairs cover [-DR, DR] (the second
+// tap of the last pair, DR + 1, is dropped).  For output column ow the pair starting at input
+// column ow + d multiplies (dy[ow], dy[ow]).
+template <int MAXW, int DR>
+__device__ __forceinline__ void fgrad_row(float2 (&acc)[DR + 1], const float2 (&xe)[MAXW / 2],
+                                          const float2 (&xo)[MAXW / 2 + 1], const float (&dv)[MAXW]) {
+#pragma unroll
+    for (int ow = 0; ow < MAXW; ++ow) {
+        const float2 g2 = make_float2(dv[ow], dv[ow]);
+#pragma unroll
+        for (int p = 0; p <= DR; ++p) {
+            const int i = ow + 2 * p - DR;
+            if (i < -1 || i > MAXW - 1) continue;
+            fma2(acc[p], col_pair<MAXW>(xe, xo, i), g2);
+        }
+    }
+}
+
+template <typename T, int MAXW, int DR>
+__global__ void __launch_bounds__(kSmMaxWarps * 32, 1) small_fgrad_kernel(const SmallFgArgs a) {
+    constexpr int NP = DR + 1;
+    extern __shared__ __align__(128) unsigned char smem[];
+    T* xbuf = reinterpret_cast<T*>(smem);                       // [2][G][H][MAXW][32]
+    T* dbuf = reinterpret_cast<T*>(smem + a.d_off);             // [2][G][OH][MAXW][32]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthreads = blockDim.x;
+    const T* X = static_cast<const T*>(a.x);
+    const T* DY = static_cast<const T*>(a.dy);
+    const int ximg = a.H * MAXW * kSmCh, dimg = a.OH * MAXW * kSmCh;
+
+    const int cb = blockIdx.x % a.cblocks;
+    const int z = blockIdx.x / a.cblocks;
+    const int c0 = cb * kSmCh;
+    // Warp w owns window rows w and nfh - 1 - w: a row near the window edge meets few output
+    // rows and its mirror many, so every warp gets about the same work.
+    const int ra = warp, rb = a.nfh - 1 - warp;
+    const bool has_b = rb > ra;
+    const int fa = a.fh_lo + ra, fb = a.fh_lo + rb;
+    const int nb = z * a.ipc, ne = min(a.N, nb + a.ipc);
+
+    if (a.W < MAXW) {
+        const int zc = MAXW - a.W;
+        for (int i = tid; i < 2 * a.G * a.H * zc * kSmCh; i += nthreads) {
+            const int ch = i % kSmCh, px = i / kSmCh;
+            xbuf[((px / zc) * MAXW + a.W + px % zc) * kSmCh + ch] = T(0.f);
+        }
+    }
+    if (a.OW < MAXW) {
+        const int zc = MAXW - a.OW;
+        for (int i = tid; i < 2 * a.G * a.OH * zc * kSmCh; i += nthreads) {
+            const int ch = i % kSmCh, px = i / kSmCh;
+            dbuf[((px / zc) * MAXW + a.OW + px % zc) * kSmCh + ch] = T(0.f);
+        }
+    }
+    auto stage = [&](int n0, int buf) {
+        for (int g = 0; g < a.G && n0 + g < ne; ++g) {
+            stage_image<T, MAXW>(xbuf + buf * a.xb_elems + g * ximg,
+                                 X + static_cast<size_t>(n0 + g) * a.H * a.W * a.C, a.H, a.W, a.C,
+                                 c0, tid, nthreads);
+            stage_image<T, MAXW>(dbuf + buf * a.db_elems + g * dimg,
+                                 DY + static_cast<size_t>(n0 + g) * a.OH * a.OW * a.C, a.OH, a.OW,
+                                 a.C, c0, tid, nthreads);
+        }
+        cp_async_commit();
+    };
+
+    float2 acc_a[NP], acc_b[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) acc_a[p] = acc_b[p] = make_float2(0.f, 0.f);
+
+    if (nb < ne) stage(nb, 0);
+    for (int n0 = nb, it = 0; n0 < ne; n0 += a.G, ++it) {
+        const int buf = it & 1;
+        if (n0 + a.G < ne) stage(n0 + a.G, buf ^ 1);
+        else cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        for (int g = 0; g < a.G && n0 + g < ne; ++g) {
+            const T* xg = xbuf + buf * a.xb_elems + g * ximg;
+            const T* dg = dbuf + buf * a.db_elems + g * dimg;
+            for (int oh = 0; oh < a.OH; ++oh) {
+                // input rows of this output row under the warp's two filter rows
+                const int iha = oh + fa - a.pad_h, ihb = oh + fb - a.pad_h;
+                const bool va = iha >= 0 && iha < a.H;
+                const bool vb = has_b && ihb >= 0 && ihb < a.H;
+                if (!va && !vb) continue;
+                float dv[MAXW];
+#pragma unroll
+                for (int i = 0; i < MAXW; ++i) dv[i] = to_f32(dg[(oh * MAXW + i) * kSmCh + lane]);
+                if (va) {
+                    float2 xe[MAXW / 2], xo[MAXW / 2 + 1];
+                    load_row_pairs<T, MAXW>(xg + iha * MAXW * kSmCh, lane, xe, xo);
+                    fgrad_row<MAXW, DR>(acc_a, xe, xo, dv);
+                }
+                if (vb) {
+                    float2 xe[MAXW / 2], xo[MAXW / 2 + 1];
+                    load_row_pairs<T, MAXW>(xg + ihb * MAXW * kSmCh, lane, xe, xo);
+                    fgrad_row<MAXW, DR>(acc_b, xe, xo, dv);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+
+    if (c0 + lane < a.C) {
+        auto write_row = [&](int r, const float2 (&acc)[NP]) {
+            float* dst = a.part + ((static_cast<size_t>(z) * a.nfh + r) * a.FW) * a.C + c0 + lane;
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                const int fw = 2 * p - DR + a.pad_w;
+                if (fw >= 0 && fw < a.FW) dst[static_cast<size_t>(fw) * a.C] = acc[p].x;
+                if (2 * p + 1 <= 2 * DR && fw + 1 >= 0 && fw + 1 < a.FW)
+                    dst[static_cast<size_t>(fw + 1) * a.C] = acc[p].y;
+            }
+            // taps whose offset lies beyond DR never meet the map
+            for (int fw = 0; fw < a.FW; ++fw)
+                if (fw - a.pad_w < -DR || fw - a.pad_w > DR) dst[static_cast<size_t>(fw) * a.C] = 0.f;
+        };
+        if (ra < a.nfh) write_row(ra, acc_a);
+        if (has_b) write_row(rb, acc_b);
+    }
+}
+
+// ------------------------------------------------------------------------------ host side
+
+// Map-size class and tap-offset bound; false if the small kernels do not serve the map.
+inline bool small_shape(int H, int W, int OH, int OW, int FW, int pad_w, int& maxw, int& dr) {
+    if (H > kSmMaxMap || W > kSmMaxMap || OH > kSmMaxMap || OW > kSmMaxMap) return false;
+    maxw = (W <= 8 && OW <= 8) ? 8 : 16;
+    // offsets d = fw - pad_w that pair an output column with an input column
+    const int dlo = std::max(-pad_w, -(OW - 1));
+    const int dhi = std::min(FW - 1 - pad_w, W - 1);
+    const int need = std::max(std::max(-dlo, dhi), 0);
+    dr = need <= 3 ? 3 : (need <= 7 ? 7 : (need <= 11 ? 11 : 15));
+    return dr <= maxw - 1;
+}
+
+// Registers per thread of a kernel (allocation granularity of 8), or the launch bound's
+// 128 when the runtime cannot say (no device).
+template <class K>
+int kernel_regs(K kern) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 128;
+    }
+    return (fa.numRegs + 7) / 8 * 8;
+}
+
+// Resident CTAs per SM from shared memory, threads and registers (per-warp register
+// allocation rounds to 256).
+inline int small_ctas_per_sm(size_t smem, int nwarps, int regs) {
+    const int by_smem = static_cast<int>(233472 / (smem + 1024));
+    const int by_threads = 2048 / (nwarps * 32);
+    const int per_warp = (regs * 32 + 255) / 256 * 256;
+    const int by_regs = 65536 / (per_warp * nwarps);
+    return std::max(1, std::min(by_smem, std::min(by_threads, by_regs)));
+}
+
+// Where the small-map kernels beat the row-streaming / filter-gradient kernels (timed on the
+// 14x14 and 7x7 stage shapes): larger filters, whose taps mostly miss such maps, and every
+// filter from 5 taps on maps of at most 8 columns.
+inline bool small_rows_wanted(int W, int OW, int FW) {
+    return FW >= 13 || (std::max(W, OW) <= 8 && FW >= 5);
+}
+inline bool small_fgrad_wanted(int W, int OW, int FW) {
+    return FW >= 9 || (std::max(W, OW) <= 8 && FW >= 5);
+}
+
+// Filter rows fh = ih - oh + pad that meet the image for some output row.
+inline void small_window_rows(int H, int OH, int FH, int pad_h, int& fh_lo, int& nfh) {
+    fh_lo = std::max(0, pad_h - (OH - 1));
+    const int fh_hi = std::min(FH - 1, H - 1 + pad_h);
+    nfh = std::max(0, fh_hi - fh_lo + 1);
+}
+
+template <typename T, int MAXW, int DR>
+cudaError_t launch_small_rows_inst(const RowConv& p) {
+    constexpr int NJ = 2 * DR + 1;
+    SmallArgs a;
+    a.in = p.in; a.w = p.w; a.out = p.out;
+    a.N = p.N; a.H = p.H; a.W = p.W; a.C = p.C; a.OH = p.OH; a.OW = p.OW;
+    a.FH = p.FH; a.FW = p.FW; a.pad_h = p.pad_h; a.pad_w = p.pad_w; a.flip = p.flip ? 1 : 0;
+    small_window_rows(p.H, p.OH, p.FH, p.pad_h, a.fh_lo, a.nfh);
+    const size_t img_bytes = static_cast<size_t>(p.H) * MAXW * kSmCh * sizeof(T);
+    const size_t win_bytes = static_cast<size_t>(std::max(a.nfh, 1)) * NJ * kSmCh * sizeof(T);
+    const size_t cap = static_cast<size_t>(device_info().max_smem_optin);
+    // images per unit: enough output rows for the warps, within shared memory
+    int G = std::max(1, std::min(4, (kSmMaxWarps + p.OH - 1) / std::max(p.OH, 1)));
+    while (G > 1 && 2 * G * img_bytes + win_bytes > cap) --G;
+    if (2 * G * img_bytes + win_bytes > cap) return cudaErrorNotSupported;
+    a.G = G;
+    a.buf_elems = static_cast<uint32_t>(G * p.H * MAXW * kSmCh);
+    a.win_off = static_cast<uint32_t>((2 * G * img_bytes + 127) & ~size_t(127));
+    const size_t smem = a.win_off + win_bytes;
+    const int cblocks = (p.C + kSmCh - 1) / kSmCh;
+    a.groups = (p.N + G - 1) / G;
+    const long long units = static_cast<long long>(cblocks) * a.groups;
+    if (units == 0) return cudaSuccess;
+    if (units >= (1LL << 31)) return cudaErrorNotSupported;
+    a.units = static_cast<uint32_t>(units);
+    // warps: output rows of a unit spread evenly over at most 8 warps
+    const int pairs = G * p.OH;
+    const int rounds = (pairs + kSmMaxWarps - 1) / kSmMaxWarps;
+    const int nwarps = (pairs + rounds - 1) / rounds;
+    auto kern = small_rows_kernel<T, MAXW, DR>;
+    // one CTA per SM: a CTA stages the filter window of each channel block it meets, so
+    // fewer CTAs with more units each was faster on the stage shapes than two per SM
+    const int per_sm = 1;
+    const long long grid = std::min<long long>(units, static_cast<long long>(device_info().sm_count) * per_sm);
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     device_info().max_smem_optin);
+        if (err != cudaSuccess) return err;
+        attr = true;
+    }
+    kern<<<static_cast<unsigned>(grid), nwarps * 32, smem, p.stream>>>(a);
+    return cudaGetLastError();
+}
+
+// Launch plan of the small-map filter gradient (shared by the workspace query and launch).
+template <typename T, int MAXW, int DR>
+bool small_fgrad_plan(int N, int H, int W, int C, int OH, int OW, int FH, int pad_h,
+                      SmallFgArgs& a, size_t& smem, int& nwarps) {
+    small_window_rows(H, OH, FH, pad_h, a.fh_lo, a.nfh);
+    if (a.nfh <= 0 || N <= 0) return false;
+    nwarps = (a.nfh + 1) / 2;  // two window rows per warp
+    if (nwarps > kSmMaxWarps) return false;
+    a.cblocks = (C + kSmCh - 1) / kSmCh;
+    const size_t ximg = static_cast<size_t>(H) * MAXW * kSmCh * sizeof(T);
+    const size_t dimg = static_cast<size_t>(OH) * MAXW * kSmCh * sizeof(T);
+    const size_t cap = static_cast<size_t>(device_info().max_smem_optin);
+    int G = 8;
+    while (G > 1 && 2 * G * (ximg + dimg) > 114688) G >>= 1;  // two CTAs per SM where possible
+    if (2 * G * (ximg + dimg) > cap) return false;
+    a.G = G;
+    a.xb_elems = static_cast<uint32_t>(G * H * MAXW * kSmCh);
+    a.db_elems = static_cast<uint32_t>(G * OH * MAXW * kSmCh);
+    a.d_off = static_cast<uint32_t>((2 * G * ximg + 127) & ~size_t(127));
+    smem = a.d_off + 2 * G * dimg;
+    static const int regs = kernel_regs(small_fgrad_kernel<T, MAXW, DR>);
+    const int per_sm = std::min(2, small_ctas_per_sm(smem, nwarps, regs));
+    long long Z = static_cast<long long>(device_info().sm_count) * per_sm / a.cblocks;
+    Z = std::max<long long>(1, std::min<long long>(Z, N));
+    a.ipc = static_cast<int>((N + Z - 1) / Z);
+    if (a.ipc > G) a.ipc = (a.ipc + G - 1) / G * G;  // whole groups per slice
+    Z = (N + a.ipc - 1) / a.ipc;
+    if (Z * a.cblocks >= (1LL << 31)) return false;
+    a.part = nullptr;
+    return true;
+}
+
+template <typename T, int MAXW, int DR>
+cudaError_t launch_small_fgrad_inst(const FilterGrad& p) {
+    SmallFgArgs a;
+    size_t smem = 0;
+    int nwarps = 0;
+    if (!small_fgrad_plan<T, MAXW, DR>(p.N, p.H, p.W, p.C, p.OH, p.OW, p.FH, p.pad, a, smem, nwarps))
+        return cudaErrorNotSupported;
+    const int Z = (p.N + a.ipc - 1) / a.ipc;
+    const size_t count = static_cast<size_t>(a.nfh) * p.FW * p.C;
+    if (p.workspace == nullptr || p.workspace_floats < count * Z) return cudaErrorInvalidValue;
+    a.x = p.x; a.dy = p.dy; a.part = p.workspace;
+    a.N = p.N; a.H = p.H; a.W = p.W; a.C = p.C; a.OH = p.OH; a.OW = p.OW;
+    a.FH = p.FH; a.FW = p.FW; a.pad_h = p.pad; a.pad_w = p.pad;
+    auto kern = small_fgrad_kernel<T, MAXW, DR>;
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     device_info().max_smem_optin);
+        if (err != cudaSuccess) return err;
+        attr = true;
+    }
+    const unsigned grid = static_cast<unsigned>(Z) * a.cblocks;
+    kern<<<grid, nwarps * 32, smem, p.stream>>>(a);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    // rows of dw outside the window never meet the image
+    const size_t row = static_cast<size_t>(p.FW) * p.C;
+    if (a.fh_lo > 0) {
+        err = cudaMemsetAsync(p.dw, 0, a.fh_lo * row * sizeof(float), p.stream);
+        if (err != cudaSuccess) return err;
+    }
+    const int tail = p.FH - a.fh_lo - a.nfh;
+    if (tail > 0) {
+        err = cudaMemsetAsync(p.dw + (a.fh_lo + a.nfh) * row, 0, tail * row * sizeof(float), p.stream);
+        if (err != cudaSuccess) return err;
+    }
+    return launch_reduce_slices(p.workspace, Z, count, p.dw + a.fh_lo * row, p.stream);
+}
+
+#define DWC_SMALL_SHAPES(X) X(8, 3) X(8, 7) X(16, 3) X(16, 7) X(16, 11) X(16, 15)
+
+template <typename T>
+size_t small_fgrad_workspace_t(int N, int H, int W, int C, int OH, int OW, int FH, int FW, int pad) {
+    int maxw = 0, dr = 0;
+    if (!small_fgrad_wanted(W, OW, FW) || !small_shape(H, W, OH, OW, FW, pad, maxw, dr)) return 0;
+    SmallFgArgs a;
+    size_t smem = 0;
+    int nwarps = 0;
+    bool ok = false;
+#define DWC_SMALL_FG_PLAN(M, D) \
+    if (maxw == M && dr == D) ok = small_fgrad_plan<T, M, D>(N, H, W, C, OH, OW, FH, pad, a, smem, nwarps);
+    DWC_SMALL_SHAPES(DWC_SMALL_FG_PLAN)
+#undef DWC_SMALL_FG_PLAN
+    if (!ok) return 0;
+    const size_t Z = static_cast<size_t>((N + a.ipc - 1) / a.ipc);
+    return Z * a.nfh * FW * static_cast<size_t>(C);
+}
+
+
+template <typename T>
+cudaError_t launch_small_rows_t(const RowConv& p) {
+    int maxw = 0, dr = 0;
+    if (!small_rows_wanted(p.W, p.OW, p.FW) || !small_shape(p.H, p.W, p.OH, p.OW, p.FW, p.pad_w, maxw, dr))
+        return cudaErrorNotSupported;
+#define DWC_SMALL_ROWS_CASE(M, D) \
+    if (maxw == M && dr == D) return launch_small_rows_inst<T, M, D>(p);
+    DWC_SMALL_SHAPES(DWC_SMALL_ROWS_CASE)
+#undef DWC_SMALL_ROWS_CASE
+    return cudaErrorNotSupported;
+}
+
+template <typename T>
+cudaError_t launch_small_fgrad_t(const FilterGrad& p) {
+    int maxw = 0, dr = 0;
+    if (!small_fgrad_wanted(p.W, p.OW, p.FW) || !small_shape(p.H, p.W, p.OH, p.OW, p.FW, p.pad, maxw, dr))
+        return cudaErrorNotSupported;
+#define DWC_SMALL_FG_CASE(M, D) \
+    if (maxw == M && dr == D) return launch_small_fgrad_inst<T, M, D>(p);
+    DWC_SMALL_SHAPES(DWC_SMALL_FG_CASE)
+#undef DWC_SMALL_FG_CASE
+    return cudaErrorNotSupported;
+}
+
+}  // namespace dwc

@@ -1,0 +1,16 @@
+// dwc_small_f32.cu -- small-map kernels, f32 inputs.
+#include "dwc_small.cuh"
+
+namespace dwc {
+cudaError_t launch_small_rows_f32(const RowConv& p) { return launch_small_rows_t<float>(p); }
+cudaError_t launch_small_fgrad_f32(const FilterGrad& p) { return launch_small_fgrad_t<float>(p); }
+size_t small_fgrad_workspace_floats_f32(int N, int H, int W, int C, int OH, int OW, int FH, int FW,
+                                      int pad) {
+    return small_fgrad_workspace_t<float>(N, H, W, C, OH, OW, FH, FW, pad);
+}
+
+bool small_map_serves(int H, int W, int OH, int OW, int FW, int pad_w) {
+    int maxw = 0, dr = 0;
+    return small_rows_wanted(W, OW, FW) && small_shape(H, W, OH, OW, FW, pad_w, maxw, dr);
+}
+}  // namespace dwc

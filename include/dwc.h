@@ -141,7 +141,7 @@ int dwc_version(void);
 
 /* Which kernel family a call with these arguments would use: 1 = fast CUDA-core
  * (row-streaming / filter-gradient) kernels, 2 = tensor-core kernels (16-bit inputs only),
- * 0 = general kernels, -1 = invalid arguments.  `pass` is 0 for
+ * 3 = small-map kernels (maps up to 16 x 16), 0 = general kernels, -1 = invalid arguments.  `pass` is 0 for
  * dwc_fwd, 1 for dwc_bwd_data, 2 for dwc_bwd_filter.  Pointer alignment is checked with
  * the pointers given (they may be NULL to mean "16-byte aligned"). */
 int dwc_path(int pass, const void* a, const void* b, const void* out,

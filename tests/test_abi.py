@@ -98,12 +98,23 @@ def test_workspace_rejected_when_small(lib):
 def test_path_selection_host_logic(lib):
     p = lambda pass_, **kw: lib.dwc_path(pass_, None, None, None, *[dict(GOOD, **kw)[k] for k in
                                           ("N", "H", "W", "C", "FH", "FW", "stride", "pad", "dtype")])
-    assert p(0) == 1 and p(1) == 1
+    # small maps (at most 16 x 16): small-map kernels for the filters they serve best
+    f5 = dict(FH=5, FW=5, pad=2)
+    assert p(0) == 1 and p(2) == 1                          # 8x8, 3x3: row kernels
+    assert p(0, **f5) == 3 and p(1, **f5) == 3 and p(2, **f5) == 3
+    big_map = dict(H=40, W=40)
+    assert p(0, **big_map) == 1 and p(1, **big_map) == 1 and p(2, **big_map) == 1
+    f13 = dict(FH=13, FW=13, pad=6)
+    assert p(0, H=16, W=16, **f13) == 3 and p(0, H=17, W=16, **f13) == 1
+    assert p(0, H=16, W=17, **f13) == 1
+    assert p(1, H=16, W=16, FH=13, FW=13, pad=0) == 3      # dy is 4 x 4, dx 16 x 16
+    f9 = dict(H=16, W=16, FH=9, FW=9, pad=4)
+    assert p(0, **f9) == 1 and p(2, **f9) == 3             # 16 wide, 9 taps: gradient only
     assert p(0, stride=2) == 0                 # stride 2 runs on the general kernels
     assert p(0, FH=4, FW=4) == 0               # even filter
     assert p(0, FH=3, FW=5) == 0               # non-square filter
     assert p(0, C=6) == 0                      # fp32 rows must be 16-byte multiples
-    assert p(0, C=8, dtype=1) == 1
+    assert p(0, C=8, dtype=1, **f5) == 3 and p(0, C=8, dtype=1, **big_map) == 1
     assert p(0, C=12, dtype=1) == 0            # bf16 needs C % 8 == 0
     assert p(0, FH=33, FW=33, pad=16, H=40, W=40) == 0
     # 16-bit inputs: tensor-core kernels for large filters on wide rows

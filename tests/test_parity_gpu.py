@@ -82,6 +82,19 @@ FAST = [
     C_(1, 9, 9, 64, 9, p=8),
     C_(2, 37, 23, 16, 21),
     C_(1, 3, 70, 8, 27, p=13),
+    # small maps (at most 16 x 16): both width classes (8, 16), every tap-offset bound
+    # (3, 7, 11, 15), channel tails, batches that do not fill the last image group,
+    # non-square maps, filter windows over several CTAs of the filter gradient
+    C_(3, 16, 16, 40, 13),
+    C_(5, 8, 8, 64, 31),
+    C_(2, 16, 5, 32, 21),
+    C_(2, 12, 16, 64, 23),
+    C_(1, 15, 15, 32, 3, p=0),
+    C_(9, 6, 6, 16, 5),
+    C_(2, 16, 16, 8, 31),
+    C_(7, 7, 7, 96, 7),
+    C_(4, 8, 6, 32, 5),
+    C_(2, 16, 16, 24, 9),
 ]
 
 
@@ -93,7 +106,7 @@ def test_fast_path_full_tensors(case, dtype):
         pytest.skip("16-bit fast path needs C % 8 == 0")
     fam = dwc.path("fwd", None, None, None, case.N, case.H, case.W, case.C, case.FH, case.FW,
                    case.stride, case.pad, {"f32": 0, "bf16": 1, "f16": 2}[dtype])
-    assert fam == 1 or (fam == 2 and dtype != "f32")
+    assert fam in (1, 3) or (fam == 2 and dtype != "f32")
     check_full(case)
 
 
