@@ -196,7 +196,7 @@ size_t small_fgrad_floats(const Problem& P) {
 // Workspace of the fast filter-gradient kernels: the largest of the kernels that may serve
 // the call (the small-map kernel falls back to the others if its launch is refused).
 size_t fast_fgrad_floats(const Problem& P) {
-    return std::max(filter_grad_workspace_floats(P.N, P.OH, P.OW, P.C, P.FH, P.FW, P.e),
+    return std::max(filter_grad_workspace_floats(P.N, P.OH, P.OW, P.C, P.FH, P.FW, P.dtype),
                     small_fgrad_floats(P));
 }
 

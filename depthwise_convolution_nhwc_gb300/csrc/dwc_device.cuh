@@ -231,4 +231,30 @@ __device__ __forceinline__ float2 PairF2::load(const T* p) { return Elem<T>::loa
 template <typename T>
 __device__ __forceinline__ float2 PairScalar::load(const T* p) { return Elem<T>::load_pair(p); }
 
+// ------------------------------------------------------------------ host-side occupancy
+
+// Registers per thread of a kernel (allocation granularity of 8), or `fallback` when the
+// runtime cannot say (no device).
+template <class K>
+int kernel_regs(K kern, int fallback) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fallback;
+    }
+    return (fa.numRegs + 7) / 8 * 8;
+}
+
+// Resident CTAs per SM from dynamic shared memory, threads and registers (the register file
+// is allocated per warp in units of 256 registers; 1 KB of shared memory is reserved per CTA).
+inline int resident_ctas(size_t smem, int threads, int regs) {
+    const int warps = (threads + 31) / 32;
+    const int by_smem = static_cast<int>(233472 / (smem + 1024));
+    const int by_threads = 2048 / (warps * 32);
+    const int by_regs = 65536 / (((regs * 32 + 255) / 256) * 256 * warps);
+    int r = by_smem < by_threads ? by_smem : by_threads;
+    if (by_regs < r) r = by_regs;
+    return r < 1 ? 1 : r;
+}
+
 }  // namespace dwc

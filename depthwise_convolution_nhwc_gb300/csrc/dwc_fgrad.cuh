@@ -319,8 +319,9 @@ struct FgradPlan {
 };
 
 // Shapes of the launch for one problem (shared by the workspace query and the launch).
-template <int FH, int FW, class Tile = FgradTile<FH, FW>>
-bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW, Tile>& P) {
+template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
+bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
+    const int e = static_cast<int>(sizeof(T));
     constexpr int RF = Tile::RF;
     const DeviceInfo& dev = device_info();
     const size_t smem_cap = std::min<size_t>(dev.max_smem_optin, 233472 / Tile::MINB - 1024);
@@ -373,8 +374,10 @@ bool fgrad_plan(int N, int OH, int OW, int C, int e, FgradPlan<FH, FW, Tile>& P)
     const long long rows = static_cast<long long>(N) * OH;
     const long long per_z = static_cast<long long>(P.cblocks) * P.chunks;
     // One wave: every CTA runs the same number of rows, so a grid a few CTAs larger than
-    // the resident capacity would take a second wave for those few; round down.
-    const int ctas_per_sm = Tile::MINB;
+    // the resident capacity would take a second wave for those few; round down.  The
+    // capacity counts every CTA that shared memory, threads and registers let an SM hold.
+    static const int regs = kernel_regs(fgrad_kernel<T, FH, FW, Tile>, 224);
+    const int ctas_per_sm = std::max(Tile::MINB, resident_ctas(P.smem, (P.nwf * P.nwc + 1) * 32, regs));
     long long Z = static_cast<long long>(dev.sm_count) * ctas_per_sm / per_z;
     Z = std::max<long long>(1, std::min<long long>(Z, rows));
     P.rows_per_slice = static_cast<int>((rows + Z - 1) / Z);
@@ -386,7 +389,7 @@ template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
 cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     const int e = static_cast<int>(sizeof(T));
     FgradPlan<FH, FW, Tile> P;
-    if (!fgrad_plan<FH, FW, Tile>(p.N, p.OH, p.OW, p.C, e, P)) return cudaErrorNotSupported;
+    if (!fgrad_plan<T, FH, FW, Tile>(p.N, p.OH, p.OW, p.C, P)) return cudaErrorNotSupported;
     if (p.N == 0 || p.OH == 0 || p.OW == 0) {
         return cudaMemsetAsync(p.dw, 0, sizeof(float) * FH * FW * p.C, p.stream);
     }
@@ -436,21 +439,37 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     return launch_reduce_slices(p.workspace, P.Z, static_cast<size_t>(FH) * FW * p.C, p.dw, p.stream);
 }
 
-template <int FH, int FW, class Tile = FgradTile<FH, FW>>
-size_t fgrad_workspace_inst(int N, int OH, int OW, int C, int e) {
+template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
+size_t fgrad_workspace_inst(int N, int OH, int OW, int C) {
     FgradPlan<FH, FW, Tile> P;
-    if (!fgrad_plan<FH, FW, Tile>(N, OH, OW, C, e, P)) return 0;
+    if (!fgrad_plan<T, FH, FW, Tile>(N, OH, OW, C, P)) return 0;
     return static_cast<size_t>(P.Z) * FH * FW * static_cast<size_t>(C);
 }
 
 // Workspace of the launch that launch_fgrad_dispatch makes for this problem.
-template <int F>
-size_t fgrad_workspace_dispatch(int N, int OH, int OW, int C, int e) {
-    return fgrad_use_alt_period<F>(OW) ? fgrad_workspace_inst<F, F, FgradAltTile<F>>(N, OH, OW, C, e)
-                                       : fgrad_workspace_inst<F, F>(N, OH, OW, C, e);
+template <typename T, int F>
+size_t fgrad_workspace_dispatch(int N, int OH, int OW, int C) {
+    return fgrad_use_alt_period<F>(OW) ? fgrad_workspace_inst<T, F, F, FgradAltTile<F>>(N, OH, OW, C)
+                                       : fgrad_workspace_inst<T, F, F>(N, OH, OW, C);
 }
 
 #define DWC_FGRAD_FILTERS(X) X(3) X(5) X(7) X(9) X(11) X(13) X(15) X(17) X(19) X(21) X(23) X(25) X(27) X(29) X(31)
+
+// Workspace floats of the CUDA-core filter gradient for inputs of type T.
+template <typename T>
+size_t fgrad_workspace_t(int N, int OH, int OW, int C, int FH, int FW) {
+    if (FH != FW) return 0;
+    switch (FH) {
+#define DWC_FGRAD_WS(F) \
+    case F:             \
+        return fgrad_workspace_dispatch<T, F>(N, OH, OW, C);
+        DWC_FGRAD_FILTERS(DWC_FGRAD_WS)
+#undef DWC_FGRAD_WS
+        default:
+            return 0;
+    }
+}
+
 
 template <typename T>
 cudaError_t launch_fgrad_dispatch(const FilterGrad& p) {

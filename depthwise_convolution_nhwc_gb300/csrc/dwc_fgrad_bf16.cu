@@ -13,4 +13,8 @@ cudaError_t launch_filter_grad_bf16(const FilterGrad& p) {
 bool tensor_core_fgrad(int N, int C, int OH, int OW, int FH, int FW) {
     return mma_fgrad_workspace_floats(N, C, OH, OW, FH, FW) > 0;
 }
+
+size_t fgrad_workspace_floats_bf16(int N, int OH, int OW, int C, int FH, int FW) {
+    return fgrad_workspace_t<__nv_bfloat16>(N, OH, OW, C, FH, FW);
+}
 }  // namespace dwc

@@ -9,4 +9,8 @@ cudaError_t launch_filter_grad_f16(const FilterGrad& p) {
     if (err != cudaErrorNotSupported) return err;
     return launch_fgrad_dispatch<__half>(p);
 }
+
+size_t fgrad_workspace_floats_f16(int N, int OH, int OW, int C, int FH, int FW) {
+    return fgrad_workspace_t<__half>(N, OH, OW, C, FH, FW);
+}
 }  // namespace dwc

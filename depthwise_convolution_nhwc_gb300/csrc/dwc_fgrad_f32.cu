@@ -1,29 +1,22 @@
-// dwc_fgrad_f32.cu -- filter-gradient kernels, f32 inputs.
+// dwc_fgrad_f32.cu -- filter-gradient kernels, f32 inputs; workspace query of all dtypes.
 #include "dwc_fgrad.cuh"
 #include "dwc_mma_fgrad.cuh"
 
 namespace dwc {
-size_t cuda_core_fgrad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int e);
-
 cudaError_t launch_filter_grad_f32(const FilterGrad& p) { return launch_fgrad_dispatch<float>(p); }
 
-size_t filter_grad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int e) {
-    if (FH != FW) return 0;
-    // 16-bit inputs may run the tensor-core kernel: its slices must fit too
-    const size_t mma = e == 2 ? mma_fgrad_workspace_floats(N, C, OH, OW, FH, FW) : 0;
-    return std::max(mma, cuda_core_fgrad_workspace_floats(N, OH, OW, C, FH, FW, e));
+size_t fgrad_workspace_floats_f32(int N, int OH, int OW, int C, int FH, int FW) {
+    return fgrad_workspace_t<float>(N, OH, OW, C, FH, FW);
 }
 
-size_t cuda_core_fgrad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int e) {
-    switch (FH) {
-#define DWC_FGRAD_WS(F) \
-    case F:             \
-        return fgrad_workspace_dispatch<F>(N, OH, OW, C, e);
-        DWC_FGRAD_FILTERS(DWC_FGRAD_WS)
-#undef DWC_FGRAD_WS
-        default:
-            return 0;
-    }
+size_t filter_grad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int dtype) {
+    if (FH != FW) return 0;
+    if (dtype == kF32) return fgrad_workspace_floats_f32(N, OH, OW, C, FH, FW);
+    // 16-bit inputs may run the tensor-core kernel: its slices must fit too
+    const size_t mma = mma_fgrad_workspace_floats(N, C, OH, OW, FH, FW);
+    const size_t cc = dtype == kBF16 ? fgrad_workspace_floats_bf16(N, OH, OW, C, FH, FW)
+                                     : fgrad_workspace_floats_f16(N, OH, OW, C, FH, FW);
+    return std::max(mma, cc);
 }
 
 bool filter_grad_supported(int FH, int FW) { return FH == FW && FH >= 3 && FH <= 31 && (FH & 1); }

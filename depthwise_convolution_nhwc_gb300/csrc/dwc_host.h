@@ -84,8 +84,12 @@ cudaError_t launch_filter_grad_f32(const FilterGrad& p);
 cudaError_t launch_filter_grad_bf16(const FilterGrad& p);
 cudaError_t launch_filter_grad_f16(const FilterGrad& p);
 bool filter_grad_supported(int FH, int FW);
-// Workspace floats the filter-gradient kernel needs (0 if it cannot run this shape).
-size_t filter_grad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int elem_bytes);
+// Workspace floats the filter-gradient kernels need for inputs of `dtype` (an ElemType;
+// 0 if they cannot run this shape), and the CUDA-core kernel's share per dtype.
+size_t filter_grad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int dtype);
+size_t fgrad_workspace_floats_f32(int N, int OH, int OW, int C, int FH, int FW);
+size_t fgrad_workspace_floats_bf16(int N, int OH, int OW, int C, int FH, int FW);
+size_t fgrad_workspace_floats_f16(int N, int OH, int OW, int C, int FH, int FW);
 
 // Small-map kernels (H, W, OH, OW <= 16; stride 1; C a multiple of 16 bytes; 16-byte
 // aligned tensors): whole images staged per 32-channel block, only the taps that can meet

@@ -366,26 +366,9 @@ inline bool small_shape(int H, int W, int OH, int OW, int FW, int pad_w, int& ma
     return dr <= maxw - 1;
 }
 
-// Registers per thread of a kernel (allocation granularity of 8), or the launch bound's
-// 128 when the runtime cannot say (no device).
-template <class K>
-int kernel_regs(K kern) {
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 128;
-    }
-    return (fa.numRegs + 7) / 8 * 8;
-}
-
-// Resident CTAs per SM from shared memory, threads and registers (per-warp register
-// allocation rounds to 256).
+// Resident CTAs per SM of a small-map launch.
 inline int small_ctas_per_sm(size_t smem, int nwarps, int regs) {
-    const int by_smem = static_cast<int>(233472 / (smem + 1024));
-    const int by_threads = 2048 / (nwarps * 32);
-    const int per_warp = (regs * 32 + 255) / 256 * 256;
-    const int by_regs = 65536 / (per_warp * nwarps);
-    return std::max(1, std::min(by_smem, std::min(by_threads, by_regs)));
+    return resident_ctas(smem, nwarps * 32, regs);
 }
 
 // Where the small-map kernels beat the row-streaming / filter-gradient kernels (timed on the
@@ -470,7 +453,7 @@ bool small_fgrad_plan(int N, int H, int W, int C, int OH, int OW, int FH, int pa
     a.db_elems = static_cast<uint32_t>(G * OH * MAXW * kSmCh);
     a.d_off = static_cast<uint32_t>((2 * G * ximg + 127) & ~size_t(127));
     smem = a.d_off + 2 * G * dimg;
-    static const int regs = kernel_regs(small_fgrad_kernel<T, MAXW, DR>);
+    static const int regs = kernel_regs(small_fgrad_kernel<T, MAXW, DR>, 128);
     const int per_sm = std::min(2, small_ctas_per_sm(smem, nwarps, regs));
     long long Z = static_cast<long long>(device_info().sm_count) * per_sm / a.cblocks;
     Z = std::max<long long>(1, std::min<long long>(Z, N));
