@@ -374,10 +374,13 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     const long long rows = static_cast<long long>(N) * OH;
     const long long per_z = static_cast<long long>(P.cblocks) * P.chunks;
     // One wave: every CTA runs the same number of rows, so a grid a few CTAs larger than
-    // the resident capacity would take a second wave for those few; round down.  The
-    // capacity counts every CTA that shared memory, threads and registers let an SM hold.
+    // the resident capacity would take a second wave for those few; round down.  For
+    // filters up to 5 taps the capacity counts every CTA that shared memory, threads and
+    // registers let an SM hold (measured faster there); larger filters keep one CTA per SM
+    // (more, shorter slices measured slower from 7 taps on).
     static const int regs = kernel_regs(fgrad_kernel<T, FH, FW, Tile>, 224);
-    const int ctas_per_sm = std::max(Tile::MINB, resident_ctas(P.smem, (P.nwf * P.nwc + 1) * 32, regs));
+    const int ctas_per_sm = FW <= 5 ? std::max(Tile::MINB, resident_ctas(P.smem, (P.nwf * P.nwc + 1) * 32, regs))
+                                    : Tile::MINB;
     long long Z = static_cast<long long>(dev.sm_count) * ctas_per_sm / per_z;
     Z = std::max<long long>(1, std::min<long long>(Z, rows));
     P.rows_per_slice = static_cast<int>((rows + Z - 1) / Z);
