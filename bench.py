@@ -329,9 +329,9 @@ def load_traffic(kernel_key):
 def run_e2e(args, case, passes, x, w, dy, ws, world, flops_step):
     """Same step through the public API with every step's inputs copied from pinned host
     memory and its outputs copied back, inside the timed region.  Steps are pipelined over
-    two device buffer sets and five streams (two for host-to-device copies, one for the
-    kernels, two for device-to-host copies), ordered by events, so that one step's copies
-    overlap another step's kernels; every step still moves all of its own bytes."""
+    two device buffer sets and three streams (host-to-device copies, kernels, device-to-host
+    copies), ordered by events, so that one step's copies overlap another step's kernels;
+    every step still moves all of its own bytes."""
     import torch
     import depthwise_convolution_nhwc_gb300 as dwc
     dev = x.device
@@ -347,33 +347,24 @@ def run_e2e(args, case, passes, x, w, dy, ws, world, flops_step):
                      "host": {n: torch.empty(shapes[n], dtype=torch.float32).pin_memory() for n in passes}})
     h2d = sum(t.numel() * t.element_size() for t, nm in ((hx, "x"), (hw, "w"), (hdy, "dy")) if need[nm])
     d2h = sum(sets[0]["host"][n].numel() * 4 for n in passes)
-    # two streams per copy direction, so that the large tensors of a step move in parallel
-    s_in = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-    s_out = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-    s_cmp = torch.cuda.Stream(dev)
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()
-    in_ready = [[ev(), ev()], [ev(), ev()]]
-    out_done = [[ev(), ev()], [ev(), ev()]]
-    cmp_done = [ev(), ev()]
+    in_ready, cmp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     used = [False, False]
-    in_lane = {"x": 0, "w": 1, "dy": 1}
-    out_lane = {n: i % 2 for i, n in enumerate(passes)}
 
     def e2e_step(k):
         b = k % 2
         S = sets[b]
-        for lane, st in enumerate(s_in):
-            with torch.cuda.stream(st):
-                if used[b]:
-                    st.wait_event(cmp_done[b])  # the kernels of step k-2 have read this set
-                for nm, h in (("x", hx), ("w", hw), ("dy", hdy)):
-                    if need[nm] and in_lane[nm] == lane:
-                        S[nm].copy_(h, non_blocking=True)
-                in_ready[b][lane].record(st)
-        for lane in range(2):
-            s_cmp.wait_event(in_ready[b][lane])
+        with torch.cuda.stream(s_in):
             if used[b]:
-                s_cmp.wait_event(out_done[b][lane])  # step k-2's outputs have left this set
+                s_in.wait_event(cmp_done[b])  # the kernels of step k-2 have read this set
+            for nm, h in (("x", hx), ("w", hw), ("dy", hdy)):
+                if need[nm]:
+                    S[nm].copy_(h, non_blocking=True)
+            in_ready[b].record(s_in)
+        s_cmp.wait_event(in_ready[b])
+        if used[b]:
+            s_cmp.wait_event(out_done[b])     # step k-2's outputs have left this set
         for name in passes:
             o = S["out"][name]
             if name == "fwd":
@@ -384,13 +375,11 @@ def run_e2e(args, case, passes, x, w, dy, ws, world, flops_step):
                 dwc.bwd_filter(S["x"], S["dy"], (case.FH, case.FW), case.stride, case.pad, out=o,
                                ws=ws, stream=s_cmp)
         cmp_done[b].record(s_cmp)
-        for lane, st in enumerate(s_out):
-            st.wait_event(cmp_done[b])
-            with torch.cuda.stream(st):
-                for name in passes:
-                    if out_lane[name] == lane:
-                        S["host"][name].copy_(S["out"][name], non_blocking=True)
-                out_done[b][lane].record(st)
+        s_out.wait_event(cmp_done[b])
+        with torch.cuda.stream(s_out):
+            for name in passes:
+                S["host"][name].copy_(S["out"][name], non_blocking=True)
+            out_done[b].record(s_out)
         used[b] = True
 
     for k in range(4):
@@ -399,14 +388,14 @@ def run_e2e(args, case, passes, x, w, dy, ws, world, flops_step):
     if world > 1:
         torch.distributed.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in[0])
-    for st in (s_in[1], s_cmp, s_out[0], s_out[1]):
-        st.wait_event(e0)
+    e0.record(s_in)
+    s_cmp.wait_event(e0)
+    s_out.wait_event(e0)
     for k in range(args.e2e_steps):
         e2e_step(k)
-    for st in (s_in[0], s_in[1], s_cmp, s_out[1]):
-        s_out[0].wait_stream(st)
-    e1.record(s_out[0])
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_cmp)
+    e1.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     if world > 1:
@@ -631,9 +620,8 @@ def run_ours(args, case, passes):
             "roofline": roof, "per_pass": passes_out,
             "e2e": ({"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                      "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": e2e_step_ms,
-                     "pipelining": "two buffer sets; host-to-device copies (two streams), "
-                                   "kernels (one stream) and device-to-host copies (two streams) "
-                                   "ordered by events"}
+                     "pipelining": "two buffer sets; host-to-device copies, kernels and "
+                                   "device-to-host copies on three streams ordered by events"}
                     if e2e_value is not None else None),
             "gpu_launches": args.steps * sum(LAUNCHES[n] for n in passes),
             "kernels": {n: KERNEL_NAMES[(n, fam[n])] for n in passes},

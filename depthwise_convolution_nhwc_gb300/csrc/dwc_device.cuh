@@ -201,8 +201,11 @@ struct Elem<__nv_bfloat16> {
     using pair_t = __nv_bfloat162;
     static constexpr int kBytes = 2;
     static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    // bf16 -> fp32 is exact: the fp32 bit pattern is the bf16 one shifted up by 16, so the
+    // pair widens with one shift and one mask
     __device__ static __forceinline__ float2 load_pair(const __nv_bfloat16* p) {
-        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
     }
 };
 

@@ -31,9 +31,12 @@ namespace dwc {
 // CTAs per SM the shared-memory window is sized for (MINB) and the period U of the circular
 // x window (any U >= FW works; output columns are processed in blocks of U, so a U that
 // divides the row width leaves no padded columns).
-template <int FH, int FW, int RF_ = 0, int MINB_ = 0, int U_ = 0>
+template <int FH, int FW, int RF_ = 0, int MINB_ = 0, int U_ = 0, int NY_ = 2>
 struct FgradTile {
-    static constexpr int kFit = FH == 7 ? 2 : 120 / (4 * FW);  // 7x7: 2 rows timed fastest
+    static constexpr int NY = NY_;  // ring slots for dy rows
+    // rows per warp timed fastest on the stage shapes: 2 for 7x7, 1 for 5x5, 9x9 and
+    // 11x11, else what about 120 registers hold
+    static constexpr int kFit = FH == 7 ? 2 : ((FH == 5 || FH == 9 || FH == 11) ? 1 : 120 / (4 * FW));
     static constexpr int RF = RF_ > 0 ? RF_ : (kFit < 1 ? 1 : (kFit > FH ? FH : kFit));
     static constexpr int MINB = MINB_ > 0 ? MINB_ : 1;
     static constexpr int U = U_ > 0 ? U_ : FW;
@@ -45,11 +48,11 @@ struct FgradTile {
 
 // A second window period per filter width: a multiple of 7 (the widths of the usual
 // 224-pixel pyramids, 112/56/28/14/7, are multiples of 7) at least FW, where the longer
-// register window does not spill (none for 9, 15 and 29..31).
+// register window does not spill (none for 15 and 29..31).
 template <int FW>
 struct FgradAltPeriod {
-    static constexpr int U = FW <= 3 ? 4 : (FW <= 7 ? 7 : (FW == 9 ? 9 : (FW <= 13 ? 14 :
-                             (FW == 15 ? 15 : (FW <= 27 ? 28 : FW)))));
+    static constexpr int U = FW <= 3 ? 4 : (FW <= 7 ? 7 : (FW <= 13 ? 14 :
+                             (FW == 15 ? 15 : (FW <= 27 ? 28 : FW))));
 };
 
 // (the default tile itself where the second period equals FW, so nothing is built twice)
@@ -331,7 +334,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     if (P.pwx > 256) return false;
     P.x_bytes = static_cast<uint32_t>(P.pwx * kBN * e);
     P.y_bytes = static_cast<uint32_t>(P.owp * kBN * e);
-    P.ny = 2;
+    P.ny = Tile::NY;
     // Filter-row groups per CTA (nwf, one warp each) and column strips (nwc): the x window of
     // nwf*RF rows must fit in shared memory; among the fitting choices take the one with the
     // most useful warp slots, counting warps up to 12 (about what hides the latencies of one

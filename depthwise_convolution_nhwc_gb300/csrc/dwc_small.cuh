@@ -16,8 +16,8 @@
 //    input pair starting at 2k + d.  Offsets run over [-DR, DR], the taps that can meet a
 //    map of this width; the window of filter rows that meet the image, 2*DR+1 taps each,
 //    is copied once per channel block (cp.async, zero fill for taps outside the filter).
-//  * Filter gradient: each warp owns two window rows fh (mirror images in the window, so
-//    that the warps' work is even) and accumulates dw[fh][d + pad_w] for d in [-DR, DR],
+//  * Filter gradient: each warp owns two window rows fh (half a window apart, so that the
+//    warps' work is even) and accumulates dw[fh][d + pad_w] for d in [-DR, DR],
 //    two taps per packed sum of x[ow + d] * dy[ow]; slices of images are summed afterwards
 //    in a fixed order.
 //
@@ -261,10 +261,13 @@ __global__ void __launch_bounds__(kSmMaxWarps * 32, 1) small_fgrad_kernel(const 
     const int cb = blockIdx.x % a.cblocks;
     const int z = blockIdx.x / a.cblocks;
     const int c0 = cb * kSmCh;
-    // Warp w owns window rows w and nfh - 1 - w: a row near the window edge meets few output
-    // rows and its mirror many, so every warp gets about the same work.
-    const int ra = warp, rb = a.nfh - 1 - warp;
-    const bool has_b = rb > ra;
+    // Warp w owns window rows w and w + ceil(nfh / 2).  The number of output rows a window
+    // row meets rises and then falls symmetrically across the window, so a row of the
+    // rising half paired with the row half a window later (falling half) gives every warp
+    // about the same work.
+    const int half = (a.nfh + 1) / 2;
+    const int ra = warp, rb = warp + half;
+    const bool has_b = rb < a.nfh;
     const int fa = a.fh_lo + ra, fb = a.fh_lo + rb;
     const int nb = z * a.ipc, ne = min(a.N, nb + a.ipc);
 
