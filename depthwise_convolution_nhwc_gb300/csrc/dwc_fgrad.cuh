@@ -31,9 +31,11 @@ namespace dwc {
 // CTAs per SM the shared-memory window is sized for (MINB) and the period U of the circular
 // x window (any U >= FW works; output columns are processed in blocks of U, so a U that
 // divides the row width leaves no padded columns).
-template <int FH, int FW, int RF_ = 0, int MINB_ = 0, int U_ = 0, int NY_ = 2>
+template <int FH, int FW, int RF_ = 0, int MINB_ = 0, int U_ = 0, int NY_ = 0>
 struct FgradTile {
-    static constexpr int NY = NY_;  // ring slots for dy rows
+    // dy ring slots, also the x rows staged ahead of the window: deeper for small filters,
+    // whose rows are consumed fastest (timed: 4 up to 5 taps, 3 for 7, else 2)
+    static constexpr int NY = NY_ > 0 ? NY_ : (FW <= 5 ? 4 : (FW == 7 ? 3 : 2));
     // rows per warp timed fastest on the stage shapes: 2 for 7x7, 1 for 5x5, 9x9 and
     // 11x11, else what about 120 registers hold
     static constexpr int kFit = FH == 7 ? 2 : ((FH == 5 || FH == 9 || FH == 11) ? 1 : 120 / (4 * FW));
@@ -344,7 +346,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     double best = -1.0;
     P.nwf = 0;
     for (int nwf = std::min(groups, Tile::MAXCW); nwf >= 1; --nwf) {
-        const size_t need = 512 + static_cast<size_t>(nwf * RF + 2) * P.x_bytes +
+        const size_t need = 512 + static_cast<size_t>(nwf * RF + Tile::NY) * P.x_bytes +
                             static_cast<size_t>(P.ny) * P.y_bytes;
         if (need > smem_cap) continue;
         const int chunks = (groups + nwf - 1) / nwf;
@@ -366,7 +368,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     }
     if (P.nwf < 1) return false;
     P.fhc = P.nwf * RF;
-    P.nx = P.fhc + 2;
+    P.nx = P.fhc + Tile::NY;
     P.smem = 512 + static_cast<size_t>(P.nx) * P.x_bytes + static_cast<size_t>(P.ny) * P.y_bytes;
     P.chunks = (FH + P.fhc - 1) / P.fhc;
     // strip reduction buffer reuses the ring

@@ -240,7 +240,36 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         };
 
         bool ok = true;
-        if constexpr (R > 1) {
+        if constexpr (R == 2 && FH >= 11) {
+            // Two output rows, rolled in pairs of input rows (the fully unrolled band of
+            // FH + 1 rows overflows the instruction cache from 11 taps on): input row 0 feeds
+            // output row 0 only, rows 1..FH-1 both, row FH output row 1 only; filter row i
+            // goes to register slot i % 2, so the slots stay compile-time constants.
+            const T* xs;
+            if (!begin_row(IntC<0>{}, 0, xs)) {
+                ok = false;
+            } else {
+                consume_rows<P, T, FW, R, TM, 1u, 0>(xs, acc, wwin);
+                end_row();
+            }
+#pragma unroll 1
+            for (int i = 1; i < FH && ok; i += 2) {
+                if (!begin_row(IntC<1>{}, i, xs)) { ok = false; break; }
+                consume_rows<P, T, FW, R, TM, 3u, 1>(xs, acc, wwin);
+                end_row();
+                if (!begin_row(IntC<0>{}, i + 1, xs)) { ok = false; break; }
+                consume_rows<P, T, FW, R, TM, 3u, 0>(xs, acc, wwin);
+                end_row();
+            }
+            if (ok) {
+                if (!begin_row(IntC<1>{}, FH, xs)) {
+                    ok = false;
+                } else {
+                    consume_rows<P, T, FW, R, TM, 2u, 1>(xs, acc, wwin);
+                    end_row();
+                }
+            }
+        } else if constexpr (R > 1) {
             // every input row of the band unrolled: output row r takes filter row i - r
             // from slot (i - r) % R
             static_for<S>([&](auto I) {
