@@ -327,9 +327,10 @@ cudaError_t launch_mma_inst(const RowConv& p) {
 }
 
 // Where the tensor-core kernel beats the row-streaming kernel for 16-bit inputs (timed on
-// the stage shapes: from 13-tap filters on rows of at least 24 outputs; on narrower maps
-// most of each tile's K-steps fall into the padding).
-constexpr int kMmaMinFilter = 13;
+// the stage shapes: from 15-tap filters on rows of at least 24 outputs -- at 13 taps the
+// row kernel was 4-10 % faster, at 17 the tensor-core kernel 8-26 %; on narrower maps most
+// of each tile's K-steps fall into the padding).
+constexpr int kMmaMinFilter = 15;
 constexpr int kMmaMinWidth = 24;
 
 inline bool mma_rows_wanted(const RowConv& p) {

@@ -240,9 +240,9 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         };
 
         bool ok = true;
-        if constexpr (R == 2 && FH >= 11) {
+        if constexpr (R == 2 && FH >= 9) {
             // Two output rows, rolled in pairs of input rows (the fully unrolled band of
-            // FH + 1 rows overflows the instruction cache from 11 taps on): input row 0 feeds
+            // FH + 1 rows overflows the instruction cache from 9 taps on): input row 0 feeds
             // output row 0 only, rows 1..FH-1 both, row FH output row 1 only; filter row i
             // goes to register slot i % 2, so the slots stay compile-time constants.
             const T* xs;

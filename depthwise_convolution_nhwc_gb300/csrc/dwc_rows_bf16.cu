@@ -1,5 +1,5 @@
 // dwc_rows_bf16.cu -- forward / backward-data kernels, bf16 inputs (tensor-core kernel for
-// filters from 13 taps on rows of at least 24 outputs, row-streaming kernel otherwise).
+// filters from 15 taps on rows of at least 24 outputs, row-streaming kernel otherwise).
 #include "dwc_mma.cuh"
 
 namespace dwc {

@@ -82,6 +82,7 @@ FAST = [
     C_(1, 9, 9, 64, 9, p=8),
     C_(2, 37, 23, 16, 21),
     C_(1, 3, 70, 8, 27, p=13),
+    C_(2, 19, 26, 32, 15),          # smallest filter and row width of the tensor-core rule
     # small maps (at most 16 x 16): both width classes (8, 16), every tap-offset bound
     # (3, 7, 11, 15), channel tails, batches that do not fill the last image group,
     # non-square maps, filter windows over several CTAs of the filter gradient
