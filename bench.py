@@ -267,10 +267,11 @@ def _sources_sha():
     return rels, h.hexdigest()
 
 
-def record_traffic(raw_csv, workload):
+def record_traffic(raw_csv, workload, passes=PASSES_ALL):
     """Write profiles/traffic.json from `ncu -i <report> --page raw --csv` output that holds
-    the kernels of one timed step: DRAM bytes per launch of each pass, with a hash of the
-    kernel sources so that the entry is ignored once a kernel changes."""
+    the kernels of one timed step (in launch order, of the passes given): DRAM bytes per
+    launch of each pass, with a hash of the kernel sources so that the entry is ignored once
+    a kernel changes."""
     import csv
     case = get_case(workload)
     rows = list(csv.reader(open(raw_csv)))
@@ -282,10 +283,15 @@ def record_traffic(raw_csv, workload):
         return sum(float(d[ix[k]]) * scale[units[ix[k]]]
                    for k in ("dram__bytes_read.sum", "dram__bytes_write.sum"))
     per = {"fwd": 0.0, "bwd_data": 0.0, "bwd_filter": 0.0}
+    small_rows_seen = 0
     for d in data:
         name = d[ix["Kernel Name"]]
         targs = name.split("<", 1)[1].split(",") if "<" in name else []
-        if "mma_rows_kernel" in name:    # <T, FLIP>
+        if "small_rows_kernel" in name:  # rotation is a runtime argument: launch order
+            which = [p for p in passes if p in ("fwd", "bwd_data")]
+            per[which[min(small_rows_seen, len(which) - 1)]] += dram(d)
+            small_rows_seen += 1
+        elif "mma_rows_kernel" in name:  # <T, FLIP>
             flip = targs[1].split(">")[0].strip()
             per["bwd_data" if flip in ("1", "true") else "fwd"] += dram(d)
         elif "rows_kernel" in name:      # <T, FH, FW, R, TM, MINB, FLIP, P>
@@ -636,7 +642,8 @@ def run_ours(args, case, passes):
 def main():
     args = parse_args()
     if args.record_traffic:
-        record_traffic(args.record_traffic, args.workload)
+        record_traffic(args.record_traffic, args.workload,
+                       tuple(p for p in args.passes.split(",") if p))
         return
     if args.sweep:
         run_sweep(args)
