@@ -44,7 +44,7 @@ constexpr int kRowsMaxThreads = (kMaxComputeWarps + 1) * 32;
 // Chosen by timing candidate tiles on the filter sizes of the benchmark shapes.
 template <int FH, int FW>
 struct RowsTile {
-    static constexpr int R = (FH <= 3) ? 8 : (FH <= 5 ? 3 : (FH <= 15 ? 2 : 1));
+    static constexpr int R = (FH <= 3) ? 8 : (FH <= 5 ? 4 : (FH <= 15 ? 2 : 1));
     static constexpr int TM = (FH <= 3) ? 4 : (FH <= 15 ? 8 : 14);
     static constexpr int MINB = FH == 7 ? 3 : 2;  // CTAs per SM for the registers
 };
