@@ -58,7 +58,7 @@ PerDevice* device_state() {
 }  // namespace
 
 const DeviceInfo& device_info() {
-    static const DeviceInfo fallback{148, 232448};
+    static const DeviceInfo fallback{152, 232448};  // GB300, used only when no device answers
     PerDevice* s = device_state();
     return s ? s->info : fallback;
 }
