@@ -245,8 +245,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 for (int f = 0; f < RF; ++f)
 #pragma unroll
                     for (int m = 0; m < FW - 1; ++m)
-                        win[f][m] = live[f] ? Elem<T>::load_pair(xs[f] + (c0 + m) * kBN)
-                                            : make_float2(0.f, 0.f);
+                        win[f][m] = Elem<T>::load_pair(xs[f] + (c0 + m) * kBN);
 #pragma unroll 1
                 for (int blk = blk0; blk < blk1; ++blk) {
                     const int cb0 = blk * U;
@@ -255,7 +254,9 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                         const float2 g = Elem<T>::load_pair(ys + (cb0 + u) * kBN);
 #pragma unroll
                         for (int f = 0; f < RF; ++f) {
-                            if (!live[f]) continue;
+                            // a row past the filter's last row (last chunk) computes from its
+                            // staged window row like the others and is never written: no
+                            // branch in this loop
                             win[f][(u + FW - 1) % U] = Elem<T>::load_pair(xs[f] + (cb0 + u + FW - 1) * kBN);
 #pragma unroll
                             for (int t = 0; t < FW; ++t) fma2(acc[f][t], win[f][(u + t) % U], g);
