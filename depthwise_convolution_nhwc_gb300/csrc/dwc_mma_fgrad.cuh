@@ -236,10 +236,10 @@ inline bool mma_fgrad_plan(int N, int C, int OH, int OW, int FH, int FW, MmaFgAr
 }
 
 // Where the tensor-core filter gradient beats the CUDA-core one for 16-bit inputs (timed on
-// the stage shapes: the fewer MMAs per loaded band of small filters do not pay for the
-// transposed staging; very narrow rows waste most of each K-step).
+// the stage shapes: from 27 taps, and from 17 taps on rows of at least 48 outputs; below,
+// the fewer MMAs per staged band do not pay for the transposed staging).
 inline bool mma_fgrad_wanted(int FW, int OW) {
-    return OW >= 14 && (FW >= 21 || (FW >= 17 && OW >= 24) || (FW >= 13 && OW >= 48));
+    return OW >= 14 && (FW >= 27 || (FW >= 17 && OW >= 48));
 }
 
 template <typename T>
