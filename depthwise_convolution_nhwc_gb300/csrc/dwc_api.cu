@@ -149,6 +149,15 @@ bool fast_eligible(const Problem& P, const void* a, const void* b, const void* o
     return true;
 }
 
+// Stride-2 forward fast path: square 3x3, 5x5 or 7x7 filters, same layout rules.
+bool fast_s2_eligible(const Problem& P, const void* a, const void* b, const void* out) {
+    if (P.s != 2 || P.FH != P.FW || (P.FH != 3 && P.FH != 5 && P.FH != 7)) return false;
+    if (P.C % (16 / P.e) != 0) return false;
+    for (const void* q : {a, b, out})
+        if (q != nullptr && !aligned(q, 16)) return false;
+    return true;
+}
+
 dwc_status_t map_cuda(cudaError_t err) { return err == cudaSuccess ? DWC_OK : DWC_ERR_CUDA; }
 
 cudaError_t launch_rows(const RowConv& rc) {
@@ -218,6 +227,16 @@ dwc_status_t dwc_fwd(const void* x, const void* w, float* y, int N, int H, int W
     if (fast_eligible(P, x, w, y)) {
         RowConv rc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype, s, status_word()};
         const cudaError_t err = launch_rows(rc);
+        if (err != cudaErrorNotSupported) return map_cuda(err);
+        (void)cudaGetLastError();
+    } else if (fast_s2_eligible(P, x, w, y)) {
+        RowConv rc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype, s, status_word()};
+        cudaError_t err;
+        switch (rc.dtype) {
+            case kF32: err = launch_rows_s2_f32(rc); break;
+            case kBF16: err = launch_rows_s2_bf16(rc); break;
+            default: err = launch_rows_s2_f16(rc); break;
+        }
         if (err != cudaErrorNotSupported) return map_cuda(err);
         (void)cudaGetLastError();
     }
@@ -325,6 +344,7 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
     Problem P;
     if (pass < 0 || pass > 2) return -1;
     if (check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P) != DWC_OK) return -1;
+    if (pass == kPassFwd && fast_s2_eligible(P, a, b, out)) return 1;
     if (!fast_eligible(P, a, b, out)) return 0;
     if (pass == kPassBwdFilter) {
         if (fast_fgrad_floats(P) == 0) return 0;

@@ -79,6 +79,11 @@ cudaError_t launch_rows_f32(const RowConv& p);
 cudaError_t launch_rows_bf16(const RowConv& p);
 cudaError_t launch_rows_f16(const RowConv& p);
 bool rows_supported(int FH, int FW);
+// Stride-2 forward row kernels (square filters of 3, 5 or 7 taps; RowConv's OH/OW are the
+// strided output dims, pad_h/pad_w the forward pads).
+cudaError_t launch_rows_s2_f32(const RowConv& p);
+cudaError_t launch_rows_s2_bf16(const RowConv& p);
+cudaError_t launch_rows_s2_f16(const RowConv& p);
 
 cudaError_t launch_filter_grad_f32(const FilterGrad& p);
 cudaError_t launch_filter_grad_bf16(const FilterGrad& p);

@@ -97,11 +97,13 @@ __host__ __device__ constexpr unsigned valid_rows(int i) {
 
 // Accumulate one staged input row i into the lane's R x TM outputs.  Output row r (in
 // MASK) takes filter row i - r, held in register slot (i - r) mod R; ISLOT = i mod R.
-template <class P, typename T, int FW, int R, int TM, unsigned MASK, int ISLOT>
+// With column stride SD, input column j of the lane feeds output t through tap
+// fw = j - SD * t.
+template <class P, typename T, int FW, int R, int TM, unsigned MASK, int ISLOT, int SD = 1>
 __device__ __forceinline__ void consume_rows(const T* __restrict__ xs, typename P::V (&acc)[R][TM],
                                              const typename P::V (&wwin)[R][FW]) {
 #pragma unroll
-    for (int j = 0; j < TM + FW - 1; ++j) {
+    for (int j = 0; j < SD * (TM - 1) + FW; ++j) {
         const typename P::V x = P::load(xs + j * kBN);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -109,17 +111,20 @@ __device__ __forceinline__ void consume_rows(const T* __restrict__ xs, typename 
             const int slot = (ISLOT - r + R) % R;
 #pragma unroll
             for (int fw = 0; fw < FW; ++fw) {
-                const int t = j - fw;
-                if (t >= 0 && t < TM) P::fma(acc[r][t], x, wwin[slot][fw]);
+                if ((j - fw) % SD != 0) continue;
+                const int t = (j - fw) / SD;
+                if (j - fw >= 0 && t < TM) P::fma(acc[r][t], x, wwin[slot][fw]);
             }
         }
     }
 }
 
-template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64>
+// SD: stride of both spatial axes (1, or 2 with one output row per band).
+template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64, int SD = 1>
 __global__ void __launch_bounds__(kRowsMaxThreads, MINB)
 rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
             const RowsArgs a) {
+    static_assert(SD == 1 || (R == 1 && !FLIP), "strided bands hold one output row (forward)");
     constexpr int S = R + FH - 1;  // input rows per band
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -157,7 +162,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             const int n = static_cast<int>(q);
             const int oh0 = band * R, ow0 = ct * TW;
             int i_lo = 0, i_hi = S;
-            if constexpr (R == 1) rows_in_image(oh0, a.pad_h, a.H, i_lo, i_hi);
+            if constexpr (R == 1) rows_in_image(oh0 * SD, a.pad_h, a.H, i_lo, i_hi);
             for (int i = i_lo; i < i_hi; ++i, ring.next(a.ns)) {
                 // slot reuse: wait until every compute warp released its previous stage
                 if (issued >= static_cast<uint32_t>(a.ns) &&
@@ -170,7 +175,8 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
                 unsigned char* st = stages + static_cast<size_t>(ring.slot) * a.stage_stride;
                 const bool wrow = i < FH;
                 mbar_arrive_expect_tx(&full[ring.slot], a.x_bytes + (wrow ? a.w_bytes : 0u));
-                tma_load_4d(st, &xmap, &full[ring.slot], cb * kBN, ow0 - a.pad_w, oh0 - a.pad_h + i, n);
+                tma_load_4d(st, &xmap, &full[ring.slot], cb * kBN, ow0 * SD - a.pad_w,
+                            oh0 * SD - a.pad_h + i, n);
                 if (wrow)
                     tma_load_3d(st + a.x_bytes, &wmap, &full[ring.slot], cb * kBN, 0,
                                 FLIP ? FH - 1 - i : i);
@@ -230,7 +236,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
                 for (int f = 0; f < FW; ++f)
                     wwin[slot][f] = P::load(ws + (FLIP ? FW - 1 - f : f) * kBN);
             }
-            xs = reinterpret_cast<const T*>(st) + (wc * TM) * kBN + 2 * lane;
+            xs = reinterpret_cast<const T*>(st) + (wc * TM * SD) * kBN + 2 * lane;
             return true;
         };
         auto end_row = [&]() {
@@ -284,12 +290,12 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             // one output row: the filter row for input row i is simply row i; input rows
             // that lie entirely in the zero padding are neither loaded nor computed
             int i_lo = 0, i_hi = S;
-            rows_in_image(oh0, a.pad_h, a.H, i_lo, i_hi);
+            rows_in_image(oh0 * SD, a.pad_h, a.H, i_lo, i_hi);
 #pragma unroll 1
             for (int i = i_lo; i < i_hi && ok; ++i) {
                 const T* xs;
                 if (!begin_row(IntC<0>{}, i, xs)) { ok = false; break; }
-                consume_rows<P, T, FW, R, TM, 1u, 0>(xs, acc, wwin);
+                consume_rows<P, T, FW, R, TM, 1u, 0, SD>(xs, acc, wwin);
                 end_row();
             }
         }
@@ -312,14 +318,14 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     }
 }
 
-template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64>
+template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64, int SD = 1>
 cudaError_t launch_rows_inst(const RowConv& p) {
     const int e = static_cast<int>(sizeof(T));
     const DeviceInfo& dev = device_info();
 
-    // compute warps side by side along the row; the staged box (TW + FW - 1 pixels) must
-    // stay within the TMA box limit of 256
-    const int max_nwc = std::min(kMaxComputeWarps, (257 - FW) / TM);
+    // compute warps side by side along the row; the staged box (SD * (TW - 1) + FW pixels)
+    // must stay within the TMA box limit of 256
+    const int max_nwc = std::min(kMaxComputeWarps, (256 - FW + SD) / (SD * TM));
     if (max_nwc < 1) return cudaErrorNotSupported;
     // warps per row tile: fewest computed columns plus half a halo per column tile
     int nwc = 1;
@@ -330,7 +336,7 @@ cudaError_t launch_rows_inst(const RowConv& p) {
         if (cost <= best) { best = cost; nwc = n; }
     }
     const int TW = nwc * TM;
-    const int TWH = TW + FW - 1;
+    const int TWH = SD * (TW - 1) + FW;
 
     CUtensorMap xmap, wmap;
     {
@@ -370,7 +376,7 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     a.stage_stride = (a.x_bytes + a.w_bytes + 127u) & ~127u;
     if (a.units == 0) return cudaSuccess;
 
-    auto kern = rows_kernel<T, FH, FW, R, TM, MINB, FLIP, P>;
+    auto kern = rows_kernel<T, FH, FW, R, TM, MINB, FLIP, P, SD>;
     const int threads = (nwc + 1) * 32;
     static int regs = -1;  // per instantiation
     if (regs < 0) {
@@ -429,6 +435,19 @@ cudaError_t launch_rows_dispatch(const RowConv& p) {
             return cudaErrorNotSupported;
     }
 #undef DWC_ROWS_CASE
+}
+
+// Stride-2 forward: one output row per band, 8 outputs per lane (filters of 3, 5 and 7 taps,
+// the down-sampling layers of mobile networks).
+template <typename T>
+cudaError_t launch_rows_s2_dispatch(const RowConv& p) {
+    if (p.FH != p.FW || p.flip) return cudaErrorNotSupported;
+    switch (p.FH) {
+        case 3: return launch_rows_inst<T, 3, 3, 1, 8, 3, false, Pair64, 2>(p);
+        case 5: return launch_rows_inst<T, 5, 5, 1, 8, 3, false, Pair64, 2>(p);
+        case 7: return launch_rows_inst<T, 7, 7, 1, 8, 3, false, Pair64, 2>(p);
+        default: return cudaErrorNotSupported;
+    }
 }
 
 }  // namespace dwc

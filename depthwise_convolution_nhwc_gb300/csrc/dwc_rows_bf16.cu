@@ -10,4 +10,5 @@ bool tensor_core_rows(const RowConv& p) {
     size_t smem = 0;
     return mma_rows_wanted(p) && mma_plan(p, a, smem);
 }
+cudaError_t launch_rows_s2_bf16(const RowConv& p) { return launch_rows_s2_dispatch<__nv_bfloat16>(p); }
 }  // namespace dwc

@@ -4,4 +4,5 @@
 
 namespace dwc {
 cudaError_t launch_rows_f16(const RowConv& p) { return launch_rows_or_mma<__half>(p); }
+cudaError_t launch_rows_s2_f16(const RowConv& p) { return launch_rows_s2_dispatch<__half>(p); }
 }  // namespace dwc

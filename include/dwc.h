@@ -140,7 +140,8 @@ const char* dwc_status_string(dwc_status_t status);
 int dwc_version(void);
 
 /* Which kernel family a call with these arguments would use: 1 = fast CUDA-core
- * (row-streaming / filter-gradient) kernels, 2 = tensor-core kernels (16-bit inputs only),
+ * (row-streaming / filter-gradient) kernels (stride 1; stride 2 for the forward pass with
+ * 3x3, 5x5 or 7x7 filters), 2 = tensor-core kernels (16-bit inputs only),
  * 3 = small-map kernels (maps up to 16 x 16), 0 = general kernels, -1 = invalid arguments.  `pass` is 0 for
  * dwc_fwd, 1 for dwc_bwd_data, 2 for dwc_bwd_filter.  Pointer alignment is checked with
  * the pointers given (they may be NULL to mean "16-byte aligned"). */

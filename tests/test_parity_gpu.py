@@ -111,6 +111,30 @@ def test_fast_path_full_tensors(case, dtype):
     check_full(case)
 
 
+# Stride-2 forward fast path (3x3, 5x5, 7x7): ragged sizes, odd maps, pads 0..F-1, channel
+# tails; the backward passes of these cases run on the general kernels.
+STRIDE2 = [
+    C_(2, 17, 19, 64, 3, s=2),
+    C_(1, 23, 37, 128, 5, s=2),
+    C_(2, 9, 70, 96, 7, s=2),
+    C_(3, 11, 13, 8, 3, s=2, p=0),
+    C_(1, 12, 300, 64, 3, s=2),
+    C_(1, 8, 8, 64, 7, s=2, p=6),
+    C_(2, 56, 56, 32, 5, s=2),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("case", STRIDE2, ids=lambda c: f"n{c.N}_{c.H}x{c.W}_c{c.C}_f{c.FH}_p{c.pad}")
+def test_stride2_forward_fast_path(case, dtype):
+    case = Case(**{**case.__dict__, "dtype": dtype})
+    if dtype != "f32" and case.C % 8:
+        pytest.skip("16-bit fast path needs C % 8 == 0")
+    assert dwc.path("fwd", None, None, None, case.N, case.H, case.W, case.C, case.FH, case.FW,
+                    case.stride, case.pad, {"f32": 0, "bf16": 1, "f16": 2}[dtype]) == 1
+    check_full(case)
+
+
 # General-kernel cases: strides, even/non-square filters, odd channel counts.
 GENERAL = [
     C_(2, 9, 11, 5, 3, s=2, p=1),
