@@ -149,7 +149,8 @@ bool fast_eligible(const Problem& P, const void* a, const void* b, const void* o
     return true;
 }
 
-// Stride-2 forward fast path: square 3x3, 5x5 or 7x7 filters, same layout rules.
+// Stride-2 fast paths (forward, backward data, filter gradient): square 3x3, 5x5 or 7x7
+// filters, same layout rules.
 bool fast_s2_eligible(const Problem& P, const void* a, const void* b, const void* out) {
     if (P.s != 2 || P.FH != P.FW || (P.FH != 3 && P.FH != 5 && P.FH != 7)) return false;
     if (P.C % (16 / P.e) != 0) return false;
@@ -191,6 +192,22 @@ cudaError_t launch_fgrad(const FilterGrad& fg) {
         case kF32: return launch_filter_grad_f32(fg);
         case kBF16: return launch_filter_grad_bf16(fg);
         default: return launch_filter_grad_f16(fg);
+    }
+}
+
+cudaError_t launch_s2_bwd_data(const GeneralConv& gc) {
+    switch (gc.dtype) {
+        case kF32: return launch_s2_bwd_data_f32(gc);
+        case kBF16: return launch_s2_bwd_data_bf16(gc);
+        default: return launch_s2_bwd_data_f16(gc);
+    }
+}
+
+cudaError_t launch_fgrad_s2(const FilterGrad& fg) {
+    switch (fg.dtype) {
+        case kF32: return launch_filter_grad_s2_f32(fg);
+        case kBF16: return launch_filter_grad_s2_bf16(fg);
+        default: return launch_filter_grad_s2_f16(fg);
     }
 }
 
@@ -266,6 +283,11 @@ dwc_status_t dwc_bwd_data(const void* dy, const void* w, float* dx, int N, int H
         (void)cudaGetLastError();
     }
     GeneralConv gc{dy, w, dx, N, H, W, C, P.OH, P.OW, FH, FW, stride, pad, P.dtype, nullptr, 0, s};
+    if (fast_s2_eligible(P, dy, w, dx)) {
+        const cudaError_t err = launch_s2_bwd_data(gc);
+        if (err != cudaErrorNotSupported) return map_cuda(err);
+        (void)cudaGetLastError();
+    }
     return map_cuda(launch_general_bwd_data(gc));
 }
 
@@ -275,6 +297,8 @@ size_t dwc_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int FW,
     if (check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P) != DWC_OK) return 0;
     size_t floats = general_bwd_filter_workspace_floats(N, P.OH, C, FH, FW);
     if (fast_eligible(P, nullptr, nullptr, nullptr)) floats = std::max(floats, fast_fgrad_floats(P));
+    if (fast_s2_eligible(P, nullptr, nullptr, nullptr))
+        floats = std::max(floats, filter_grad_s2_workspace_floats(N, P.OH, P.OW, C, FH, FW, P.dtype));
     return floats * sizeof(float);
 }
 
@@ -301,6 +325,13 @@ dwc_status_t dwc_bwd_filter(const void* x, const void* dy, float* dw, int N, int
         FilterGrad fg{x, dy, dw, N, H, W, C, P.OH, P.OW, FH, FW, pad, P.dtype, ws, ws_floats, s,
                       status_word()};
         const cudaError_t err = launch_fgrad(fg);
+        if (err != cudaErrorNotSupported) return map_cuda(err);
+        (void)cudaGetLastError();
+    } else if (fast_s2_eligible(P, x, dy, dw) &&
+               filter_grad_s2_workspace_floats(N, P.OH, P.OW, C, FH, FW, P.dtype) > 0) {
+        FilterGrad fg{x, dy, dw, N, H, W, C, P.OH, P.OW, FH, FW, pad, P.dtype, ws, ws_floats, s,
+                      status_word()};
+        const cudaError_t err = launch_fgrad_s2(fg);
         if (err != cudaErrorNotSupported) return map_cuda(err);
         (void)cudaGetLastError();
     }
@@ -344,7 +375,11 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
     Problem P;
     if (pass < 0 || pass > 2) return -1;
     if (check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P) != DWC_OK) return -1;
-    if (pass == kPassFwd && fast_s2_eligible(P, a, b, out)) return 1;
+    if (fast_s2_eligible(P, a, b, out)) {
+        if (pass == kPassBwdFilter)
+            return filter_grad_s2_workspace_floats(N, P.OH, P.OW, C, FH, FW, P.dtype) > 0 ? 1 : 0;
+        return 1;
+    }
     if (!fast_eligible(P, a, b, out)) return 0;
     if (pass == kPassBwdFilter) {
         if (fast_fgrad_floats(P) == 0) return 0;

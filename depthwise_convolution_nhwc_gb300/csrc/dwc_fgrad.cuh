@@ -1,7 +1,8 @@
 // dwc_fgrad.cuh -- filter-gradient kernel ("backward filter convolution").
 //
-//   dw[fh, fw, c] = sum_{n, oh, ow} x[n, oh + fh - pad, ow + fw - pad, c] * dy[n, oh, ow, c]
+//   dw[fh, fw, c] = sum_{n, oh, ow} x[n, S*oh + fh - pad, S*ow + fw - pad, c] * dy[n, oh, ow, c]
 //
+// with stride S = 1, or S = 2 for square filters of 3, 5 or 7 taps.
 // ("Flash-DWC: Making Depthwise Convolution Compute-Efficient on GPUs", §5.1: the output is
 // only FH x FW x C and does not grow with batch or resolution, so the work is spread over
 // the accumulation axis N*OH*OW.)  GB300 restatement:
@@ -13,12 +14,17 @@
 //    Within a CTA the column strips of the warps are summed in a fixed order through shared
 //    memory.  Results are therefore bit-identical from run to run.
 //  * A producer warp streams, with TMA, the dy rows of the slice and the x rows they pair
-//    with.  The x rows form a window of FHC rows that slides by one row per output row, so
-//    every x row enters shared memory once per CTA.
+//    with.  The x rows form a window of FHC rows that slides by S rows per output row, so
+//    every x row enters shared memory once per CTA (at S = 2 with a one-row window, the
+//    rows between two windows are skipped).
 //  * Each compute warp owns RF filter rows and one strip of output columns; a lane owns two
 //    channels and keeps RF x FW fp32x2 accumulators plus, per owned row, a circular register
 //    window of U >= FW x values (the FW that the current output column multiplies and the
-//    next ones).  Each dy element is loaded once and used for RF*FW packed FMAs.
+//    next ones).  Each dy element is loaded once and used for RF*FW packed FMAs.  At S = 2
+//    the output column ow meets the x columns 2*ow + t: even taps t = 2j read the even
+//    column 2*(ow + j), odd taps t = 2j + 1 the odd column 2*(ow + j) + 1, so each row keeps
+//    two circular windows (even and odd columns) that advance by one column per output
+//    column.
 #pragma once
 
 #include <type_traits>
@@ -31,8 +37,13 @@ namespace dwc {
 // CTAs per SM the shared-memory window is sized for (MINB) and the period U of the circular
 // x window (any U >= FW works; output columns are processed in blocks of U, so a U that
 // divides the row width leaves no padded columns).
-template <int FH, int FW, int RF_ = 0, int MINB_ = 0, int U_ = 0, int NY_ = 0>
+template <int FH, int FW, int RF_ = 0, int MINB_ = 0, int U_ = 0, int NY_ = 0, int SD_ = 1>
 struct FgradTile {
+    // convolution stride (1, or 2 for the strided 3x3 / 5x5 / 7x7 filter gradient)
+    static constexpr int SD = SD_;
+    // x columns one output column of one parity class needs (FW at stride 1; at stride 2
+    // the even taps read the even columns and the odd taps the odd ones)
+    static constexpr int KW = (FW + SD - 1) / SD;
     // dy ring slots, also the x rows staged ahead of the window: deeper for small filters,
     // whose rows are consumed fastest (timed: 4 up to 5 taps, 3 for 7, else 2)
     static constexpr int NY = NY_ > 0 ? NY_ : (FW <= 5 ? 4 : (FW == 7 ? 3 : 2));
@@ -41,8 +52,8 @@ struct FgradTile {
     static constexpr int kFit = FH == 7 ? 2 : ((FH == 5 || FH == 9 || FH == 11) ? 1 : 120 / (4 * FW));
     static constexpr int RF = RF_ > 0 ? RF_ : (kFit < 1 ? 1 : (kFit > FH ? FH : kFit));
     static constexpr int MINB = MINB_ > 0 ? MINB_ : 1;
-    static constexpr int U = U_ > 0 ? U_ : FW;
-    static_assert(U >= FW, "the window must hold FW columns");
+    static constexpr int U = U_ > 0 ? U_ : (SD == 1 ? FW : (KW <= 4 ? 4 : KW));
+    static_assert(U >= KW, "the window must hold the columns one output column needs");
     // compute warps per CTA where one filter row per warp leaves the registers for more
     // (the launch bound caps registers at 128 per thread for 13 warps, 168 for 12), else 8
     static constexpr int MAXCW = (RF == 1 && FW <= 19) ? 12 : ((RF == 1 && FW <= 27) ? 11 : 8);
@@ -83,12 +94,51 @@ struct FgradArgs {
     uint32_t y_off;        // byte offset of the dy ring after the x ring
 };
 
+// One output row of a column strip at stride 2: acc[f][t] += x[2*ow + t] * dy[ow] over the
+// strip's output columns, for the RF x rows xs[f].  Even taps t = 2j read the even x column
+// 2*(ow + j), odd taps t = 2j + 1 the odd column 2*(ow + j) + 1; each class has its own
+// circular window (x column 2m or 2m + 1 sits in slot m mod U).
+template <typename T, int FW, int RF, int U>
+__device__ __forceinline__ void fgrad_row_s2(float2 (&acc)[RF][FW], const T* const (&xs)[RF],
+                                             const T* ys, int blk0, int blk1) {
+    constexpr int KE = (FW + 1) / 2;  // even taps
+    constexpr int KO = FW / 2;        // odd taps
+    float2 we[RF][U], wo[RF][U];
+    const int c0 = blk0 * U;
+#pragma unroll
+    for (int f = 0; f < RF; ++f) {
+#pragma unroll
+        for (int m = 0; m < KE - 1; ++m) we[f][m] = Elem<T>::load_pair(xs[f] + 2 * (c0 + m) * kBN);
+#pragma unroll
+        for (int m = 0; m < KO - 1; ++m) wo[f][m] = Elem<T>::load_pair(xs[f] + (2 * (c0 + m) + 1) * kBN);
+    }
+#pragma unroll 1
+    for (int blk = blk0; blk < blk1; ++blk) {
+        const int cb0 = blk * U;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float2 g = Elem<T>::load_pair(ys + (cb0 + u) * kBN);
+#pragma unroll
+            for (int f = 0; f < RF; ++f) {
+                we[f][(u + KE - 1) % U] = Elem<T>::load_pair(xs[f] + 2 * (cb0 + u + KE - 1) * kBN);
+                if constexpr (KO > 0)
+                    wo[f][(u + KO - 1) % U] = Elem<T>::load_pair(xs[f] + (2 * (cb0 + u + KO - 1) + 1) * kBN);
+#pragma unroll
+                for (int j = 0; j < KE; ++j) fma2(acc[f][2 * j], we[f][(u + j) % U], g);
+#pragma unroll
+                for (int j = 0; j < KO; ++j) fma2(acc[f][2 * j + 1], wo[f][(u + j) % U], g);
+            }
+        }
+    }
+}
+
 template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
 __global__ void __launch_bounds__((Tile::MAXCW + 1) * 32, Tile::MINB)
 fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
              const FgradArgs a) {
     constexpr int RF = Tile::RF;
     constexpr int U = Tile::U;
+    constexpr int SD = Tile::SD;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* xfull = reinterpret_cast<uint64_t*>(smem);
     uint64_t* xempty = xfull + a.nx;
@@ -124,6 +174,8 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     const long long total_rows = static_cast<long long>(a.N) * a.OH;
     const long long q0 = static_cast<long long>(z) * a.rows_per_slice;
     const long long q1 = std::min<long long>(q0 + a.rows_per_slice, total_rows);
+    // x rows each output row adds to the window (and drops from it afterwards)
+    const int nnew = SD == 1 ? 1 : std::min(SD, a.fhc);
 
     // ---------------- producer ----------------------------------------------------------
     if (warp == ncompute) {
@@ -157,10 +209,12 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             const int n = static_cast<int>(q / a.OH);
             const int oha = static_cast<int>(q % a.OH);
             const int ohb = static_cast<int>(std::min<long long>(q1 - static_cast<long long>(n) * a.OH, a.OH));
-            const int ih0 = oha + fh0 - a.pad;
-            for (int r = 0; r < a.fhc - 1 && ok; ++r) ok = put_x(n, ih0 + r);
+            // output row oh reads the x rows ih0 + SD*(oh - oha) + [0, fhc)
+            const int ih0 = oha * SD + fh0 - a.pad;
+            for (int r = 0; r < a.fhc - nnew && ok; ++r) ok = put_x(n, ih0 + r);
             for (int oh = oha; oh < ohb && ok; ++oh) {
-                ok = put_x(n, ih0 + (oh - oha) + a.fhc - 1);
+                const int ihn = ih0 + (oh - oha) * SD + a.fhc - nnew;
+                for (int r = 0; r < nnew && ok; ++r) ok = put_x(n, ihn + r);
                 if (ok) ok = put_y(n, oh);
             }
             q = static_cast<long long>(n) * a.OH + ohb;
@@ -218,7 +272,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         const int L = ohb - oha;
         for (int row = 0; row < L && ok; ++row) {
             // wait for the x rows this output row needs (the whole window at the segment start)
-            for (int d = (row == 0 ? 0 : a.fhc - 1); d < a.fhc; ++d) {
+            for (int d = (row == 0 ? 0 : a.fhc - nnew); d < a.fhc; ++d) {
                 uint32_t ph;
                 const uint32_t sl = xslot(static_cast<uint32_t>(d), ph);
                 if (!mbar_wait(&xfull[sl], ph)) {
@@ -237,7 +291,9 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 const uint32_t sl = xslot(static_cast<uint32_t>(frow0 + f), ph);
                 xs[f] = reinterpret_cast<const T*>(xring + static_cast<size_t>(sl) * a.x_bytes) + 2 * lane;
             }
-            if (blk0 < blk1) {
+            if constexpr (SD == 2) {
+                if (blk0 < blk1) fgrad_row_s2<T, FW, RF, U>(acc, xs, ys, blk0, blk1);
+            } else if (blk0 < blk1) {
                 // circular window: column c of the padded x row sits in slot c mod U
                 float2 win[RF][U];
                 const int c0 = blk0 * U;
@@ -265,17 +321,18 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 }
             }
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&yempty[yr.slot]);
-                mbar_arrive(&xempty[xbase.slot]);  // the oldest row has no later use
-            }
+            if (lane == 0) mbar_arrive(&yempty[yr.slot]);
             yr.next(a.ny);
-            xbase.next(a.nx);
+            // the nnew oldest rows have no later use
+            for (int d = 0; d < nnew; ++d) {
+                if (lane == 0) mbar_arrive(&xempty[xbase.slot]);
+                xbase.next(a.nx);
+            }
         }
         if (!ok) break;
-        // the last fhc-1 rows of the window are not needed by later output rows
+        // the last fhc-nnew rows of the window are not needed by later output rows
         __syncwarp();
-        for (int d = 0; d < a.fhc - 1; ++d) {
+        for (int d = 0; d < a.fhc - nnew; ++d) {
             if (lane == 0) mbar_arrive(&xempty[xbase.slot]);
             xbase.next(a.nx);
         }
@@ -333,23 +390,29 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     const size_t smem_cap = std::min<size_t>(dev.max_smem_optin, 233472 / Tile::MINB - 1024);
     P.nblocks = (OW + Tile::U - 1) / Tile::U;
     P.owp = P.nblocks * Tile::U;
-    P.pwx = P.owp + FW - 1;
+    P.pwx = Tile::SD * (P.owp - 1) + FW;
     if (P.pwx > 256) return false;
     P.x_bytes = static_cast<uint32_t>(P.pwx * kBN * e);
     P.y_bytes = static_cast<uint32_t>(P.owp * kBN * e);
-    P.ny = Tile::NY;
     // Filter-row groups per CTA (nwf, one warp each) and column strips (nwc): the x window of
     // nwf*RF rows must fit in shared memory; among the fitting choices take the one with the
     // most useful warp slots, counting warps up to 12 (about what hides the latencies of one
     // CTA per SM), discounted by the chunk count (each chunk streams every x and dy row of
     // its slice again); the weights were fitted to timings of the stage shapes.
     const int groups = (FH + RF - 1) / RF;  // RF-row groups needed to cover the filter
+    // The lookahead (dy slots, and the x rows staged ahead of the window) is Tile::NY
+    // output rows; at stride 2, whose x rows are twice as wide, the deepest that fits.
     double best = -1.0;
     P.nwf = 0;
+    int best_la = 0;
     for (int nwf = std::min(groups, Tile::MAXCW); nwf >= 1; --nwf) {
-        const size_t need = 512 + static_cast<size_t>(nwf * RF + Tile::NY) * P.x_bytes +
-                            static_cast<size_t>(P.ny) * P.y_bytes;
-        if (need > smem_cap) continue;
+        int la = Tile::NY;
+        auto need = [&](int l) {
+            return 512 + static_cast<size_t>(nwf * RF + l * Tile::SD) * P.x_bytes +
+                   static_cast<size_t>(l) * P.y_bytes;
+        };
+        while (Tile::SD > 1 && la > 1 && need(la) > smem_cap) --la;
+        if (need(la) > smem_cap) continue;
         const int chunks = (groups + nwf - 1) / nwf;
         if ((groups + chunks - 1) / chunks != nwf) continue;  // same chunks, fewer warps: seen
         const int nwc0 = std::max(1, std::min(Tile::MAXCW / nwf, P.nblocks));
@@ -365,11 +428,13 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
             P.nwf = nwf;
             P.nwc = nwc;
             P.bps = bps;
+            best_la = la;
         }
     }
     if (P.nwf < 1) return false;
     P.fhc = P.nwf * RF;
-    P.nx = P.fhc + Tile::NY;
+    P.ny = best_la;
+    P.nx = P.fhc + best_la * Tile::SD;
     P.smem = 512 + static_cast<size_t>(P.nx) * P.x_bytes + static_cast<size_t>(P.ny) * P.y_bytes;
     P.chunks = (FH + P.fhc - 1) / P.fhc;
     // strip reduction buffer reuses the ring
@@ -479,6 +544,32 @@ size_t fgrad_workspace_t(int N, int OH, int OW, int C, int FH, int FW) {
     }
 }
 
+
+// Stride-2 filter gradient: square filters of 3, 5 or 7 taps.
+template <int F>
+using FgradS2Tile = FgradTile<F, F, 0, 0, 0, 0, 2>;
+
+template <typename T>
+cudaError_t launch_fgrad_s2_dispatch(const FilterGrad& p) {
+    if (p.FH != p.FW) return cudaErrorNotSupported;
+    switch (p.FH) {
+        case 3: return launch_fgrad_inst<T, 3, 3, FgradS2Tile<3>>(p);
+        case 5: return launch_fgrad_inst<T, 5, 5, FgradS2Tile<5>>(p);
+        case 7: return launch_fgrad_inst<T, 7, 7, FgradS2Tile<7>>(p);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+template <typename T>
+size_t fgrad_s2_workspace_t(int N, int OH, int OW, int C, int FH, int FW) {
+    if (FH != FW) return 0;
+    switch (FH) {
+        case 3: return fgrad_workspace_inst<T, 3, 3, FgradS2Tile<3>>(N, OH, OW, C);
+        case 5: return fgrad_workspace_inst<T, 5, 5, FgradS2Tile<5>>(N, OH, OW, C);
+        case 7: return fgrad_workspace_inst<T, 7, 7, FgradS2Tile<7>>(N, OH, OW, C);
+        default: return 0;
+    }
+}
 
 template <typename T>
 cudaError_t launch_fgrad_dispatch(const FilterGrad& p) {

@@ -17,4 +17,8 @@ bool tensor_core_fgrad(int N, int C, int OH, int OW, int FH, int FW) {
 size_t fgrad_workspace_floats_bf16(int N, int OH, int OW, int C, int FH, int FW) {
     return fgrad_workspace_t<__nv_bfloat16>(N, OH, OW, C, FH, FW);
 }
+cudaError_t launch_filter_grad_s2_bf16(const FilterGrad& p) { return launch_fgrad_s2_dispatch<__nv_bfloat16>(p); }
+size_t fgrad_s2_workspace_floats_bf16(int N, int OH, int OW, int C, int FH, int FW) {
+    return fgrad_s2_workspace_t<__nv_bfloat16>(N, OH, OW, C, FH, FW);
+}
 }  // namespace dwc

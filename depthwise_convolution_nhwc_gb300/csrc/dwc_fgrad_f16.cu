@@ -13,4 +13,8 @@ cudaError_t launch_filter_grad_f16(const FilterGrad& p) {
 size_t fgrad_workspace_floats_f16(int N, int OH, int OW, int C, int FH, int FW) {
     return fgrad_workspace_t<__half>(N, OH, OW, C, FH, FW);
 }
+cudaError_t launch_filter_grad_s2_f16(const FilterGrad& p) { return launch_fgrad_s2_dispatch<__half>(p); }
+size_t fgrad_s2_workspace_floats_f16(int N, int OH, int OW, int C, int FH, int FW) {
+    return fgrad_s2_workspace_t<__half>(N, OH, OW, C, FH, FW);
+}
 }  // namespace dwc

@@ -21,4 +21,17 @@ size_t filter_grad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW
 
 bool filter_grad_supported(int FH, int FW) { return FH == FW && FH >= 3 && FH <= 31 && (FH & 1); }
 bool rows_supported(int FH, int FW) { return FH == FW && FH >= 3 && FH <= 31 && (FH & 1); }
+cudaError_t launch_filter_grad_s2_f32(const FilterGrad& p) { return launch_fgrad_s2_dispatch<float>(p); }
+
+size_t fgrad_s2_workspace_floats_f32(int N, int OH, int OW, int C, int FH, int FW) {
+    return fgrad_s2_workspace_t<float>(N, OH, OW, C, FH, FW);
+}
+
+size_t filter_grad_s2_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int dtype) {
+    switch (dtype) {
+        case kF32: return fgrad_s2_workspace_floats_f32(N, OH, OW, C, FH, FW);
+        case kBF16: return fgrad_s2_workspace_floats_bf16(N, OH, OW, C, FH, FW);
+        default: return fgrad_s2_workspace_floats_f16(N, OH, OW, C, FH, FW);
+    }
+}
 }  // namespace dwc

@@ -84,6 +84,11 @@ bool rows_supported(int FH, int FW);
 cudaError_t launch_rows_s2_f32(const RowConv& p);
 cudaError_t launch_rows_s2_bf16(const RowConv& p);
 cudaError_t launch_rows_s2_f16(const RowConv& p);
+// Stride-2 backward data (square filters of 3, 5 or 7 taps, C even, 8-byte aligned
+// tensors): a = dy, b = w, out = dx of the GeneralConv.
+cudaError_t launch_s2_bwd_data_f32(const GeneralConv& p);
+cudaError_t launch_s2_bwd_data_bf16(const GeneralConv& p);
+cudaError_t launch_s2_bwd_data_f16(const GeneralConv& p);
 
 cudaError_t launch_filter_grad_f32(const FilterGrad& p);
 cudaError_t launch_filter_grad_bf16(const FilterGrad& p);
@@ -95,6 +100,16 @@ size_t filter_grad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW
 size_t fgrad_workspace_floats_f32(int N, int OH, int OW, int C, int FH, int FW);
 size_t fgrad_workspace_floats_bf16(int N, int OH, int OW, int C, int FH, int FW);
 size_t fgrad_workspace_floats_f16(int N, int OH, int OW, int C, int FH, int FW);
+
+// Stride-2 filter gradient (square filters of 3, 5 or 7 taps; FilterGrad's OH/OW are the
+// strided output dims) and its workspace floats (0 if it cannot run the shape).
+cudaError_t launch_filter_grad_s2_f32(const FilterGrad& p);
+cudaError_t launch_filter_grad_s2_bf16(const FilterGrad& p);
+cudaError_t launch_filter_grad_s2_f16(const FilterGrad& p);
+size_t filter_grad_s2_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int dtype);
+size_t fgrad_s2_workspace_floats_f32(int N, int OH, int OW, int C, int FH, int FW);
+size_t fgrad_s2_workspace_floats_bf16(int N, int OH, int OW, int C, int FH, int FW);
+size_t fgrad_s2_workspace_floats_f16(int N, int OH, int OW, int C, int FH, int FW);
 
 // Small-map kernels (H, W, OH, OW <= 16; stride 1; C a multiple of 16 bytes; 16-byte
 // aligned tensors): whole images staged per 32-channel block, only the taps that can meet

@@ -1,8 +1,10 @@
 // dwc_rows_f16.cu -- forward / backward-data kernels, f16 inputs (tensor-core kernel for
 // filters from 9 taps, row-streaming kernel below).
 #include "dwc_mma.cuh"
+#include "dwc_s2data.cuh"
 
 namespace dwc {
 cudaError_t launch_rows_f16(const RowConv& p) { return launch_rows_or_mma<__half>(p); }
 cudaError_t launch_rows_s2_f16(const RowConv& p) { return launch_rows_s2_dispatch<__half>(p); }
+cudaError_t launch_s2_bwd_data_f16(const GeneralConv& p) { return launch_s2_bwd_data_dispatch<__half>(p); }
 }  // namespace dwc

@@ -110,9 +110,12 @@ def test_path_selection_host_logic(lib):
     assert p(1, H=16, W=16, FH=13, FW=13, pad=0) == 3      # dy is 4 x 4, dx 16 x 16
     f9 = dict(H=16, W=16, FH=9, FW=9, pad=4)
     assert p(0, **f9) == 1 and p(2, **f9) == 3             # 16 wide, 9 taps: gradient only
-    # stride 2: forward fast path for 3x3, 5x5, 7x7; the backward passes on the general kernels
+    # stride 2: fast paths of all three passes for 3x3, 5x5, 7x7
     assert p(0, stride=2) == 1 and p(0, stride=2, FH=5, FW=5, pad=2) == 1
-    assert p(1, stride=2) == 0 and p(2, stride=2) == 0
+    assert p(1, stride=2) == 1 and p(2, stride=2) == 1
+    assert p(1, stride=2, FH=7, FW=7, pad=3) == 1 and p(2, stride=2, FH=7, FW=7, pad=3) == 1
+    # filter gradient: a padded x row beyond one 256-column TMA box goes to the general kernel
+    assert p(2, stride=2, W=300) == 0 and p(1, stride=2, W=300) == 1
     assert p(0, stride=2, FH=9, FW=9, pad=4, H=40, W=40) == 0 and p(0, stride=3) == 0
     assert p(0, stride=2, C=6) == 0
     assert p(0, FH=4, FW=4) == 0               # even filter

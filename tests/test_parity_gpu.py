@@ -118,20 +118,34 @@ STRIDE2 = [
     C_(1, 23, 37, 128, 5, s=2),
     C_(2, 9, 70, 96, 7, s=2),
     C_(3, 11, 13, 8, 3, s=2, p=0),
-    C_(1, 12, 300, 64, 3, s=2),
+    C_(1, 12, 300, 64, 3, s=2),       # filter gradient: row too wide for one TMA box
     C_(1, 8, 8, 64, 7, s=2, p=6),
     C_(2, 56, 56, 32, 5, s=2),
+    C_(2, 20, 21, 64, 5, s=2, p=1),   # odd padding with a 5x5 filter
+    C_(1, 30, 31, 64, 7, s=2, p=2),
+    C_(6, 40, 40, 24, 3, s=2),        # many slices, C not a multiple of the channel block
+    C_(1, 5, 5, 16, 7, s=2, p=3),     # map smaller than the filter
 ]
+
+
+def s2_fgrad_fits(case):
+    """The stride-2 filter gradient stages a padded x row of 2*(OW rounded up to 4) + F - 2
+    columns in one TMA box of at most 256."""
+    ow = (case.W + 2 * case.pad - case.FW) // 2 + 1
+    return 2 * ((ow + 3) // 4 * 4 - 1) + case.FW <= 256
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("case", STRIDE2, ids=lambda c: f"n{c.N}_{c.H}x{c.W}_c{c.C}_f{c.FH}_p{c.pad}")
-def test_stride2_forward_fast_path(case, dtype):
+def test_stride2_fast_path(case, dtype):
     case = Case(**{**case.__dict__, "dtype": dtype})
     if dtype != "f32" and case.C % 8:
         pytest.skip("16-bit fast path needs C % 8 == 0")
-    assert dwc.path("fwd", None, None, None, case.N, case.H, case.W, case.C, case.FH, case.FW,
-                    case.stride, case.pad, {"f32": 0, "bf16": 1, "f16": 2}[dtype]) == 1
+    code = {"f32": 0, "bf16": 1, "f16": 2}[dtype]
+    args = (case.N, case.H, case.W, case.C, case.FH, case.FW, case.stride, case.pad, code)
+    assert dwc.path("fwd", None, None, None, *args) == 1
+    assert dwc.path("bwd_data", None, None, None, *args) == 1
+    assert dwc.path("bwd_filter", None, None, None, *args) == (1 if s2_fgrad_fits(case) else 0)
     check_full(case)
 
 
