@@ -7,7 +7,8 @@ calls it.
 
 The arithmetic lives in ``dwc_oracle.c`` (plain C, fp64, loop-by-loop definition of the
 forward pass and both backward passes, following "Flash-DWC: Making Depthwise Convolution
-Compute-Efficient on GPUs", §2.1 / Fig. 1, §2.3 and §5.1).  This module only compiles it
+Compute-Efficient on GPUs", §2.1 / Fig. 1, §2.3 and §5.1, and of the BN + Act that §5.2
+fuses in front of the forward pass).  This module only compiles it
 with the host C compiler and marshals numpy arrays through ``ctypes``.
 
 Layouts (channels last, §2.3): x, y, dx, dy are N x H x W x C; the filter is FH x FW x C.
@@ -44,7 +45,7 @@ def _compile(src: str, out: str) -> str:
         raise RuntimeError("oracle: no C compiler found (gcc/cc)")
     tmp = out + f".tmp{os.getpid()}"
     # -ffp-contract=off keeps every multiply and add a separate fp64 rounding, as written.
-    tail = ["-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off", src, "-o", tmp]
+    tail = ["-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off", src, "-o", tmp, "-lm"]
     try:
         subprocess.run([cc, "-fopenmp"] + tail, check=True, capture_output=True)
     except subprocess.CalledProcessError:
@@ -101,6 +102,9 @@ class Oracle:
         for name in ("dwc_oracle_fwd_at", "dwc_oracle_bwd_data_at", "dwc_oracle_bwd_filter_at"):
             getattr(lib, name).argtypes = [dp, dp, ip, ctypes.c_long, dp] + shape
             getattr(lib, name).restype = None
+        lib.dwc_oracle_bn_act.argtypes = [dp, dp, dp, dp, dp, ctypes.c_double, i, dp,
+                                          ctypes.c_long, i]
+        lib.dwc_oracle_bn_act.restype = None
         self.lib = lib
         self.path = lib_path
 
@@ -193,6 +197,34 @@ class Oracle:
                                           N, H, W, C, FH, FW, stride, pad)
         return out
 
+    ACTS = {"none": 0, "relu": 1, "relu6": 2}
+
+    def bn_act(self, x, mean, var, gamma, beta, eps: float, act: str) -> np.ndarray:
+        """z = act((x - mean) / sqrt(var + eps) * gamma + beta) per channel (last axis), the
+        BN + Act that precede a fused forward DWC; act is "none", "relu" or "relu6"."""
+        x = _f64(x)
+        C = int(x.shape[-1])
+        prm = [_f64(v).ravel() for v in (mean, var, gamma, beta)]
+        if any(v.size != C for v in prm):
+            raise ValueError("BN parameters need one value per channel")
+        z = np.zeros_like(x)
+        if z.size:
+            self.lib.dwc_oracle_bn_act(_ptr(x), *(_ptr(v) for v in prm), float(eps),
+                                       self.ACTS[act], _ptr(z), z.size // C, C)
+        return z
+
+    def fwd_bn_act(self, x, w, mean, var, gamma, beta, eps: float, act: str,
+                   stride: int = 1, pad: int = 0) -> np.ndarray:
+        """Y = DWC(act(BN(X)), W), in the pages' order: BN, then Act, then the DWC, whose zero
+        padding applies to act(BN(X))."""
+        return self.fwd(self.bn_act(x, mean, var, gamma, beta, eps, act), w, stride, pad)
+
+    def fwd_bn_act_at(self, x, w, mean, var, gamma, beta, eps: float, act: str, flat_idx,
+                      stride: int = 1, pad: int = 0) -> np.ndarray:
+        """Fused forward outputs at flat indices of the N x OH x OW x C output."""
+        return self.fwd_at(self.bn_act(x, mean, var, gamma, beta, eps, act), w, flat_idx,
+                           stride, pad)
+
 
 _default = None
 
@@ -256,5 +288,17 @@ def bwd_filter_at(x, dy, f_hw, flat_idx, stride=1, pad=0):
     return get().bwd_filter_at(x, dy, f_hw, flat_idx, stride, pad)
 
 
+def bn_act(x, mean, var, gamma, beta, eps, act):
+    return get().bn_act(x, mean, var, gamma, beta, eps, act)
+
+
+def fwd_bn_act(x, w, mean, var, gamma, beta, eps, act, stride=1, pad=0):
+    return get().fwd_bn_act(x, w, mean, var, gamma, beta, eps, act, stride, pad)
+
+
+def fwd_bn_act_at(x, w, mean, var, gamma, beta, eps, act, flat_idx, stride=1, pad=0):
+    return get().fwd_bn_act_at(x, w, mean, var, gamma, beta, eps, act, flat_idx, stride, pad)
+
+
 __all__ = ["Oracle", "get", "load_source_variant", "source", "build", "out_dim", "max_threads", "set_threads", "fwd", "bwd_data", "bwd_filter",
-           "fwd_at", "bwd_data_at", "bwd_filter_at"]
+           "fwd_at", "bwd_data_at", "bwd_filter_at", "bn_act", "fwd_bn_act", "fwd_bn_act_at"]

@@ -15,7 +15,9 @@
  *       the filter is FH x FW x C (channel last everywhere);
  *     §5.1 "backward propagation" -- backward data (BDC) convolves dY with the filter
  *       rotated by 180 degrees; backward filter (BFC) correlates X with dY and yields an
- *       FH x FW x C filter gradient.
+ *       FH x FW x C filter gradient;
+ *     §5.2 "kernel fusion" -- batch normalisation and an activation applied to X before
+ *       the forward DWC (BN + Act + DWC).
  *
  * Readings taken where the pages are silent (each is listed in the design notes):
  *   - forward is a cross-correlation (no filter flip), the convention of the framework
@@ -34,6 +36,7 @@
  * summation order of every output element is fixed: fh outer, fw inner for forward and
  * backward data; n, oh, ow for the filter gradient.
  */
+#include <math.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <string.h>
@@ -246,5 +249,29 @@ void dwc_oracle_bwd_filter_at(const double *x, const double *dy, const int64_t *
         int fw = (int)(i % FW); i /= FW;
         int fh = (int)i;
         out[k] = bwd_filter_one(x, dy, fh, fw, c, N, H, W, C, s, p, OH, OW);
+    }
+}
+
+/* Batch normalisation with given per-channel statistics, then an activation, element by
+ * element: the BN + Act that the pages fuse in front of a forward DWC (Flash-DWC, §5.2
+ * "kernel fusion").  For every pixel row of C channels:
+ *
+ *   z[.., c] = act((x[.., c] - mean[c]) / sqrt(var[c] + eps) * gamma[c] + beta[c])
+ *
+ * with act 0 = identity, 1 = ReLU max(v, 0), 2 = ReLU6 min(max(v, 0), 6).  The DWC that
+ * follows zero-pads z itself (its out-of-image taps contribute nothing), so the fused
+ * forward is dwc_oracle_fwd applied to z. */
+void dwc_oracle_bn_act(const double *x, const double *mean, const double *var,
+                       const double *gamma, const double *beta, double eps, int act,
+                       double *z, long pixels, int C)
+{
+#pragma omp parallel for schedule(static)
+    for (long q = 0; q < pixels; ++q) {
+        for (int c = 0; c < C; ++c) {
+            double v = (x[(size_t)q * C + c] - mean[c]) / sqrt(var[c] + eps) * gamma[c] + beta[c];
+            if (act >= 1 && v < 0.0) v = 0.0;
+            if (act == 2 && v > 6.0) v = 6.0;
+            z[(size_t)q * C + c] = v;
+        }
     }
 }

@@ -240,6 +240,72 @@ def test_linearity_and_flip_symmetry():
                           oracle.fwd(x1, w1, 1, p)[..., perm])
 
 
+# -- BN + Act + DWC (the fusion of §5.2) ------------------------------------------------
+
+def torch_fwd_bn_act(x, w, mean, var, gamma, beta, eps, act, s, p):
+    """Library form: torch's eval-mode batch_norm, relu / relu6 and grouped conv2d in fp64."""
+    xt = torch.from_numpy(x).permute(0, 3, 1, 2)
+    t = lambda v: torch.from_numpy(np.asarray(v, np.float64))
+    z = F.batch_norm(xt, t(mean), t(var), t(gamma), t(beta), training=False, eps=eps)
+    z = {"none": lambda v: v, "relu": F.relu, "relu6": F.relu6}[act](z)
+    wt = torch.from_numpy(w).permute(2, 0, 1).unsqueeze(1)
+    y = F.conv2d(z, wt, stride=s, padding=p, groups=x.shape[3])
+    return y.permute(0, 2, 3, 1).contiguous().numpy()
+
+
+def bn_params(C, spread=1.0):
+    return (RNG.uniform(-0.5, 0.5, C), RNG.uniform(0.5, 2.0, C), RNG.uniform(0.5, 1.5, C) * spread,
+            RNG.uniform(-0.5, 0.5, C))
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "relu6"])
+@pytest.mark.parametrize("shape", SHAPES[:9])
+def test_fwd_bn_act_matches_torch_fp64(shape, act):
+    N, H, W, C, FH, FW, s, p = shape
+    x, w = rand(N, H, W, C) * 3, rand(FH, FW, C)
+    mean, var, gamma, beta = bn_params(C, spread=4.0)   # wide enough that ReLU6 clips
+    got = oracle.fwd_bn_act(x, w, mean, var, gamma, beta, 1e-5, act, s, p)
+    ref = torch_fwd_bn_act(x, w, mean, var, gamma, beta, 1e-5, act, s, p)
+    assert got.shape == ref.shape and rel_err(got, ref) <= 1e-12
+
+
+@pytest.mark.parametrize("act,beta,z", [("none", -2.0, -2.0), ("relu", -2.0, 0.0), ("relu", 1.5, 1.5),
+                                        ("relu6", 7.25, 6.0), ("relu6", -0.5, 0.0), ("none", 0.0, 2.0)])
+@pytest.mark.parametrize("H,W,F_,s,p", [(7, 9, 3, 1, 1), (6, 7, 7, 1, 3), (9, 8, 3, 2, 1), (5, 5, 7, 1, 6)])
+def test_bn_act_constant_input_pads_with_zero(H, W, F_, s, p, act, beta, z):
+    """x == mean + 2 with var + eps == 4 makes the normalised value exactly 1, so the BN gives
+    gamma + beta; gamma is 0 except in the last case (gamma 2, beta 0).  A box filter then
+    gives z * b * (taps inside the image), which holds only if the padding is zero AFTER the
+    activation (padding with act(BN(0)) would add taps at the borders)."""
+    C, a, b = 2, 0.75, -1.25
+    gamma = 2.0 if z == 2.0 else 0.0
+    x = np.full((1, H, W, C), a + 2.0)
+    w = np.full((F_, F_, C), b)
+    y = oracle.fwd_bn_act(x, w, [a] * C, [3.75] * C, [gamma] * C, [beta] * C, 0.25, act, s, p)
+
+    def cnt(o, n_in):
+        lo = o * s - p
+        return max(0, min(n_in, lo + F_) - max(0, lo))
+
+    for oh, ow in itertools.product(range(y.shape[1]), range(y.shape[2])):
+        assert np.all(y[0, oh, ow] == z * b * cnt(oh, H) * cnt(ow, W))
+
+
+def test_bn_act_identity_parameters_reduce_to_plain_forward():
+    x, w = rand(2, 7, 8, 3), rand(5, 5, 3)
+    y = oracle.fwd_bn_act(x, w, [0.0] * 3, [0.75] * 3, [1.0] * 3, [0.0] * 3, 0.25, "none", 1, 2)
+    assert np.array_equal(y, oracle.fwd(x, w, 1, 2))
+
+
+def test_fwd_bn_act_sampled_equals_full():
+    x, w = rand(2, 9, 10, 4), rand(3, 3, 4)
+    prm = bn_params(4)
+    full = oracle.fwd_bn_act(x, w, *prm, 1e-5, "relu", 2, 1)
+    idx = RNG.choice(full.size, 40, replace=False)
+    assert np.array_equal(oracle.fwd_bn_act_at(x, w, *prm, 1e-5, "relu", idx, 2, 1),
+                          full.ravel()[idx])
+
+
 def test_out_dim_and_empty_outputs():
     assert oracle.out_dim(56, 7, 1, 3) == 56
     assert oracle.out_dim(56, 31, 1, 15) == 56
@@ -262,6 +328,10 @@ MUTANTS = {
                            "dx[nhwc(n, ih, iw, c, H, W, C)] += g * w[hwc(FH - 1 - fh, FW - 1 - fw, c, FW, C)];"),
     "bwd_filter_stride_ignored": ("int ih = oh * s + fh - p;\n            if (ih < 0 || ih >= H) continue;\n            for (int ow = 0; ow < OW; ++ow) {",
                                   "int ih = oh + fh - p;\n            if (ih < 0 || ih >= H) continue;\n            for (int ow = 0; ow < OW; ++ow) {"),
+    "bn_act_relu_dropped": ("if (act >= 1 && v < 0.0) v = 0.0;", "if (act >= 3 && v < 0.0) v = 0.0;"),
+    "bn_sqrt_dropped": ("- mean[c]) / sqrt(var[c] + eps) * gamma[c] + beta[c];",
+                        "- mean[c]) / (var[c] + eps) * gamma[c] + beta[c];"),
+    "bn_relu6_unclipped": ("if (act == 2 && v > 6.0) v = 6.0;", "if (act == 2 && v > 7.0) v = 7.0;"),
     "fwd_channel_mixed": ("acc += x[nhwc(n, ih, iw, c, H, W, C)] * w[hwc(fh, fw, c, FW, C)];\n        }\n    }\n    return acc;",
                           "acc += x[nhwc(n, ih, iw, c, H, W, C)] * w[hwc(fh, fw, 0, FW, C)];\n        }\n    }\n    return acc;"),
 }
@@ -281,6 +351,12 @@ def _pins_pass(o: "oracle.Oracle") -> bool:
             return False
         if rel_err(o.bwd_filter(x, dy, (FH, FW), s, p), dw_ref) > 1e-12:
             return False
+        mean, var, gamma, beta = bn_params(C, spread=4.0)
+        for act in ("none", "relu", "relu6"):
+            xs = x * 3
+            if rel_err(o.fwd_bn_act(xs, w, mean, var, gamma, beta, 1e-5, act, s, p),
+                       torch_fwd_bn_act(xs, w, mean, var, gamma, beta, 1e-5, act, s, p)) > 1e-12:
+                return False
     return True
 
 
