@@ -3,7 +3,8 @@
 Thin ctypes binding over the C ABI in ``include/dwc.h`` (``libdwc_gb300.so``, built from
 ``csrc/`` for sm_103a).  The binding only marshals arguments: it checks tensor shapes,
 allocates outputs and workspaces with PyTorch (used for device memory and streams only) and
-calls ``dwc_fwd`` / ``dwc_bwd_data`` / ``dwc_bwd_filter`` on the current CUDA stream.  Every
+calls ``dwc_fwd`` / ``dwc_fwd_bn_act`` / ``dwc_bwd_data`` / ``dwc_bwd_filter`` on the current
+CUDA stream.  Every
 step of the computation runs in the library's CUDA kernels; there is no CPU fallback, and a
 missing library is an error.
 
@@ -24,12 +25,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdwc_gb300.so")
 
 DWC_F32, DWC_BF16, DWC_F16 = 0, 1, 2
+ACTS = {"none": 0, "relu": 1, "relu6": 2}   # dwc_act_t
 STATUS = {0: "DWC_OK", 1: "DWC_ERR_INVALID_ARG", 2: "DWC_ERR_UNSUPPORTED",
           3: "DWC_ERR_ALIGNMENT", 4: "DWC_ERR_WORKSPACE", 5: "DWC_ERR_CUDA",
           6: "DWC_ERR_TIMEOUT"}
 
 # Every symbol include/dwc.h declares (checked by the tests).
-EXPORTS = ("dwc_fwd", "dwc_bwd_data", "dwc_bwd_filter_workspace_size", "dwc_bwd_filter",
+EXPORTS = ("dwc_fwd", "dwc_fwd_bn_act", "dwc_bwd_data", "dwc_bwd_filter_workspace_size", "dwc_bwd_filter",
            "dwc_bwd_filter_noalloc", "dwc_device_status", "dwc_status_string", "dwc_version",
            "dwc_path")
 
@@ -65,6 +67,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         shape = [i] * 8
         lib.dwc_fwd.argtypes = [vp, vp, vp] + shape + [i, vp]
         lib.dwc_fwd.restype = i
+        lib.dwc_fwd_bn_act.argtypes = [vp, vp, vp, vp, vp, ctypes.c_float, i, vp, vp] + shape + [i, vp]
+        lib.dwc_fwd_bn_act.restype = i
         lib.dwc_bwd_data.argtypes = [vp, vp, vp] + shape + [i, vp]
         lib.dwc_bwd_data.restype = i
         lib.dwc_bwd_filter_workspace_size.argtypes = shape + [i]
@@ -142,6 +146,29 @@ def fwd(x, w, stride: int = 1, pad: int = 0, out=None, stream=None):
     return out
 
 
+def fwd_bn_act(x, w, mean, var, gamma, beta, eps: float = 1e-5, act: str = "relu",
+               stride: int = 1, pad: int = 0, out=None, stream=None):
+    """Y = DWC(act(BN(X)), W) in one pass: BN(X) = (X - mean) / sqrt(var + eps) * gamma + beta
+    per channel, act "none" / "relu" / "relu6"; the DWC zero-pads act(BN(X)).  mean, var,
+    gamma, beta: C fp32 values each on the device (fp32 output)."""
+    torch = _torch()
+    _check_cuda(x, w, mean, var, gamma, beta)
+    N, H, W, C = x.shape
+    FH, FW, C2 = w.shape
+    if C2 != C or w.dtype != x.dtype:
+        raise ValueError("filter must be FH x FW x C with the input's dtype")
+    for t in (mean, var, gamma, beta):
+        if t.dtype != torch.float32 or t.numel() != C:
+            raise ValueError("BN parameters must be C fp32 values each")
+    OH, OW = out_dim(H, FH, stride, pad), out_dim(W, FW, stride, pad)
+    if out is None:
+        out = torch.empty((N, max(OH, 0), max(OW, 0), C), device=x.device, dtype=torch.float32)
+    _call("dwc_fwd_bn_act", x.data_ptr(), mean.data_ptr(), var.data_ptr(), gamma.data_ptr(),
+          beta.data_ptr(), float(eps), ACTS[act], w.data_ptr(), out.data_ptr(), N, H, W, C, FH,
+          FW, stride, pad, _dtype_code(x), _stream_ptr(stream))
+    return out
+
+
 def bwd_data(dy, w, in_hw, stride: int = 1, pad: int = 0, out=None, stream=None):
     """dX = adjoint of ``fwd`` in X for a forward input of spatial size in_hw (fp32 output)."""
     torch = _torch()
@@ -207,10 +234,10 @@ def device_status(stream=None) -> int:
 def path(pass_: str, a, b, out, N, H, W, C, FH, FW, stride, pad, dtype_code) -> int:
     """Kernel family of a call: 3 small-map kernels (maps up to 16x16), 2 tensor-core
     kernels (16-bit inputs), 1 fast CUDA-core kernels, 0 general kernels, -1 invalid."""
-    p = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2}[pass_]
+    p = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2, "fwd_bn_act": 3}[pass_]
     return int(load_library().dwc_path(p, a, b, out, N, H, W, C, FH, FW, stride, pad,
                                        dtype_code))
 
 
-__all__ = ["build", "load_library", "fwd", "bwd_data", "bwd_filter", "bwd_filter_workspace_size",
+__all__ = ["build", "load_library", "fwd", "fwd_bn_act", "bwd_data", "bwd_filter", "bwd_filter_workspace_size",
            "device_status", "path", "status_string", "DwcError", "EXPORTS", "LIB_PATH"]

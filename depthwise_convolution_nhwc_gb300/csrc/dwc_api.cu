@@ -1,6 +1,7 @@
 // dwc_api.cu -- the C ABI declared in include/dwc.h: argument validation, choice between
 // the fast and the general kernels, TMA descriptor encoding and the device status word.
 #include <algorithm>
+#include <cmath>
 #include <climits>
 #include <cstdint>
 #include <mutex>
@@ -159,6 +160,20 @@ bool fast_s2_eligible(const Problem& P, const void* a, const void* b, const void
     return true;
 }
 
+// BN + Act + forward fast path: square 3x3, 5x5 or 7x7 filters at stride 1 or 2.
+bool bnact_fast_eligible(const Problem& P, const void* a, const void* b, const void* out) {
+    if (P.FH != P.FW || (P.FH != 3 && P.FH != 5 && P.FH != 7)) return false;
+    return P.s == 1 ? fast_eligible(P, a, b, out) : fast_s2_eligible(P, a, b, out);
+}
+
+cudaError_t launch_rows_bnact(const RowConv& rc, int stride) {
+    switch (rc.dtype) {
+        case kF32: return launch_rows_bnact_f32(rc, stride);
+        case kBF16: return launch_rows_bnact_bf16(rc, stride);
+        default: return launch_rows_bnact_f16(rc, stride);
+    }
+}
+
 dwc_status_t map_cuda(cudaError_t err) { return err == cudaSuccess ? DWC_OK : DWC_ERR_CUDA; }
 
 cudaError_t launch_rows(const RowConv& rc) {
@@ -258,6 +273,38 @@ dwc_status_t dwc_fwd(const void* x, const void* w, float* y, int N, int H, int W
         (void)cudaGetLastError();
     }
     GeneralConv gc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, stride, pad, P.dtype, nullptr, 0, s};
+    return map_cuda(launch_general_fwd(gc));
+}
+
+dwc_status_t dwc_fwd_bn_act(const void* x, const float* mean, const float* var,
+                            const float* gamma, const float* beta, float eps, dwc_act_t act,
+                            const void* w, float* y, int N, int H, int W, int C, int FH, int FW,
+                            int stride, int pad, dwc_dtype_t dtype, dwc_stream_t stream) {
+    Problem P;
+    dwc_status_t st = check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P);
+    if (st != DWC_OK) return st;
+    if (act != DWC_ACT_NONE && act != DWC_ACT_RELU && act != DWC_ACT_RELU6)
+        return DWC_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !(eps < INFINITY)) return DWC_ERR_INVALID_ARG;
+    const long long nx = static_cast<long long>(N) * H * W * C;
+    const long long ny = static_cast<long long>(N) * P.OH * P.OW * C;
+    st = check_pointers(P, x, nx, w, static_cast<long long>(FH) * FW * C, y, ny);
+    if (st != DWC_OK) return st;
+    for (const float* q : {mean, var, gamma, beta}) {
+        if (C > 0 && q == nullptr) return DWC_ERR_INVALID_ARG;
+        if (!aligned(q, 4)) return DWC_ERR_ALIGNMENT;
+    }
+    if (ny == 0) return DWC_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (bnact_fast_eligible(P, x, w, y)) {
+        RowConv rc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype, s, status_word(),
+                   mean, var, gamma, beta, eps, static_cast<int>(act)};
+        const cudaError_t err = launch_rows_bnact(rc, stride);
+        if (err != cudaErrorNotSupported) return map_cuda(err);
+        (void)cudaGetLastError();
+    }
+    GeneralConv gc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, stride, pad, P.dtype, nullptr, 0, s,
+                   mean, var, gamma, beta, eps, static_cast<int>(act)};
     return map_cuda(launch_general_fwd(gc));
 }
 
@@ -373,8 +420,9 @@ int dwc_version(void) { return 100; }
 int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int H, int W, int C,
              int FH, int FW, int stride, int pad, dwc_dtype_t dtype) {
     Problem P;
-    if (pass < 0 || pass > 2) return -1;
+    if (pass < 0 || pass > 3) return -1;
     if (check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P) != DWC_OK) return -1;
+    if (pass == 3) return bnact_fast_eligible(P, a, b, out) ? 1 : 0;
     if (fast_s2_eligible(P, a, b, out)) {
         if (pass == kPassBwdFilter)
             return filter_grad_s2_workspace_floats(N, P.OH, P.OW, C, FH, FW, P.dtype) > 0 ? 1 : 0;

@@ -3,7 +3,7 @@
 //
 // These follow the definitions directly ("Flash-DWC: Making Depthwise Convolution
 // Compute-Efficient on GPUs", §2.1 / Fig. 1 for the forward pass, §5.1 for the two backward
-// passes) with one thread per output element and fp32 accumulation; they serve the shapes
+// passes, §5.2 for BN + Act in front of the forward pass) with one thread per output element and fp32 accumulation; they serve the shapes
 // the row-streaming kernels do not cover (strides above 1, odd channel counts, unaligned
 // pointers, even or very large filters).
 #include <algorithm>
@@ -35,6 +35,45 @@ __global__ void general_fwd_kernel(const T* __restrict__ x, const T* __restrict_
                 const int iw = ow * s + fw - p;
                 acc = fmaf(to_f32(x[((static_cast<size_t>(n) * H + ih) * W + iw) * C + c]),
                            to_f32(w[(static_cast<size_t>(fh) * FW + fw) * C + c]), acc);
+            }
+        }
+        y[i] = acc;
+    }
+}
+
+// y = DWC(act(BN(x)), w): the forward kernel with every in-image input value normalised with
+// its channel's batch statistics and activated first (taps in the padding read zero, as
+// the DWC pads the activated tensor).  act: 0 identity, 1 ReLU, 2 ReLU6.
+template <typename T>
+__global__ void general_fwd_bnact_kernel(const T* __restrict__ x, const T* __restrict__ w,
+                                         float* __restrict__ y, int N, int H, int W, int C,
+                                         int OH, int OW, int FH, int FW, int s, int p,
+                                         const float* __restrict__ mean,
+                                         const float* __restrict__ var,
+                                         const float* __restrict__ gamma,
+                                         const float* __restrict__ beta, float eps, int act) {
+    const long long total = static_cast<long long>(N) * OH * OW * C;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        long long q = i;
+        const int c = static_cast<int>(q % C); q /= C;
+        const int ow = static_cast<int>(q % OW); q /= OW;
+        const int oh = static_cast<int>(q % OH); q /= OH;
+        const int n = static_cast<int>(q);
+        const float scale = gamma[c] * rsqrtf(var[c] + eps);
+        const float shift = beta[c] - mean[c] * scale;
+        const int fh0 = max(0, p - oh * s), fh1 = min(FH, H + p - oh * s);
+        const int fw0 = max(0, p - ow * s), fw1 = min(FW, W + p - ow * s);
+        float acc = 0.f;
+        for (int fh = fh0; fh < fh1; ++fh) {
+            const int ih = oh * s + fh - p;
+            for (int fw = fw0; fw < fw1; ++fw) {
+                const int iw = ow * s + fw - p;
+                float z = fmaf(to_f32(x[((static_cast<size_t>(n) * H + ih) * W + iw) * C + c]),
+                               scale, shift);
+                if (act >= 1) z = fmaxf(z, 0.f);
+                if (act == 2) z = fminf(z, 6.f);
+                acc = fmaf(z, to_f32(w[(static_cast<size_t>(fh) * FW + fw) * C + c]), acc);
             }
         }
         y[i] = acc;
@@ -159,6 +198,13 @@ template <typename T>
 static cudaError_t general_fwd_t(const GeneralConv& p) {
     const long long total = static_cast<long long>(p.N) * p.OH * p.OW * p.C;
     if (total == 0) return cudaSuccess;
+    if (p.act >= 0) {
+        general_fwd_bnact_kernel<T><<<grid_for(total, 256), 256, 0, p.stream>>>(
+            static_cast<const T*>(p.a), static_cast<const T*>(p.b), p.out, p.N, p.H, p.W, p.C,
+            p.OH, p.OW, p.FH, p.FW, p.stride, p.pad, p.bn_mean, p.bn_var, p.bn_gamma, p.bn_beta,
+            p.bn_eps, p.act);
+        return cudaGetLastError();
+    }
     general_fwd_kernel<T><<<grid_for(total, 256), 256, 0, p.stream>>>(
         static_cast<const T*>(p.a), static_cast<const T*>(p.b), p.out, p.N, p.H, p.W, p.C, p.OH,
         p.OW, p.FH, p.FW, p.stride, p.pad);

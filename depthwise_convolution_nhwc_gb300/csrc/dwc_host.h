@@ -28,6 +28,15 @@ struct RowConv {
     int dtype;
     cudaStream_t stream;
     unsigned int* status;
+    // BN + Act fused in front of the forward pass (act < 0: plain DWC): per-channel batch
+    // statistics and affine parameters (C floats each, device memory), epsilon, activation
+    // (0 identity, 1 ReLU, 2 ReLU6).
+    const float* bn_mean = nullptr;
+    const float* bn_var = nullptr;
+    const float* bn_gamma = nullptr;
+    const float* bn_beta = nullptr;
+    float bn_eps = 0.f;
+    int act = -1;
 };
 
 // Filter-gradient problem: dw[fh, fw, c] = sum_{n,oh,ow} x[n, oh+fh-pad, ow+fw-pad, c] * dy[n,oh,ow,c].
@@ -59,6 +68,13 @@ struct GeneralConv {
     float* workspace;
     size_t workspace_floats;
     cudaStream_t stream;
+    // BN + Act in front of the forward pass, as in RowConv (act < 0: none)
+    const float* bn_mean = nullptr;
+    const float* bn_var = nullptr;
+    const float* bn_gamma = nullptr;
+    const float* bn_beta = nullptr;
+    float bn_eps = 0.f;
+    int act = -1;
 };
 
 // Device properties cached per device.
@@ -84,6 +100,12 @@ bool rows_supported(int FH, int FW);
 cudaError_t launch_rows_s2_f32(const RowConv& p);
 cudaError_t launch_rows_s2_bf16(const RowConv& p);
 cudaError_t launch_rows_s2_f16(const RowConv& p);
+// BN + Act + forward DWC on the row kernels (square filters of 3, 5 or 7 taps, stride 1 or
+// 2, the layout rules of the fast paths; RowConv carries the BN parameters and act >= 0).
+cudaError_t launch_rows_bnact_f32(const RowConv& p, int stride);
+cudaError_t launch_rows_bnact_bf16(const RowConv& p, int stride);
+cudaError_t launch_rows_bnact_f16(const RowConv& p, int stride);
+
 // Stride-2 backward data (square filters of 3, 5 or 7 taps, C even, 8-byte aligned
 // tensors): a = dy, b = w, out = dx of the GeneralConv.
 cudaError_t launch_s2_bwd_data_f32(const GeneralConv& p);

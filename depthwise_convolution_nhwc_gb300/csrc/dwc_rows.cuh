@@ -23,9 +23,14 @@
 //    holds).  The filter rows in use live in registers as a window of R rows that slides
 //    by one row per input row (filter reuse across TM*R outputs, §3.2).
 //  * 16-bit inputs are widened to fp32 once per shared-memory load, not per FMA (§4.1).
+//  * Optional BN + Act fusion (§5.2, forward only): each input value is normalised with the
+//    channel's batch statistics and activated right after its shared-memory load, before
+//    its taps; values that lie in the padding are replaced by zero (the DWC pads the
+//    activated tensor), and input rows outside the image are skipped.
 #pragma once
 
 #include <climits>
+#include <type_traits>
 #include <utility>
 
 #include "dwc_device.cuh"
@@ -52,7 +57,7 @@ struct RowsTile {
 struct RowsArgs {
     float* out;
     unsigned int* status;
-    int H;                // input rows (for trimming rows that lie in the padding)
+    int H, W;             // input rows / columns (rows and columns that lie in the padding)
     int OH, OW, C;
     int pad_h, pad_w;
     int nwc;              // compute warps per CTA
@@ -62,10 +67,51 @@ struct RowsArgs {
     uint32_t x_bytes;     // bytes of one staged input row box
     uint32_t w_bytes;     // bytes of one staged filter row box
     uint32_t stage_stride;
+    // fused BN + Act (ACT >= 0): batch statistics and affine parameters, C floats each
+    const float* bn_mean;
+    const float* bn_var;
+    const float* bn_gamma;
+    const float* bn_beta;
+    float bn_eps;
+};
+
+// Value transform between the shared-memory load and the taps.  NoXform: the plain DWC.
+struct NoXform {
+    template <class V>
+    __device__ __forceinline__ V operator()(V x, int) const { return x; }
+};
+
+// BN + Act on a pair of channels: z = act(x * scale + shift) with scale = gamma / sqrt(var +
+// eps) and shift = beta - mean * scale; ACT 0 = identity, 1 = ReLU, 2 = ReLU6.  MASKED: bit
+// j of colmask says whether staged column j lies inside the image, and a column in the
+// padding yields zero.  Every lane of a warp stages the same columns, so a warp whose
+// columns all lie inside the image runs the unmasked form.
+template <class P, int ACT, bool MASKED>
+struct BnActXform {
+    typename P::V scale, shift;
+    uint32_t colmask;
+    __device__ __forceinline__ typename P::V operator()(typename P::V x, int j) const {
+        typename P::V z = shift;
+        P::fma(z, x, scale);
+        if constexpr (ACT >= 1) {
+            float2 f = P::unpack(z);
+            f.x = fmaxf(f.x, 0.f);
+            f.y = fmaxf(f.y, 0.f);
+            if constexpr (ACT == 2) {
+                f.x = fminf(f.x, 6.f);
+                f.y = fminf(f.y, 6.f);
+            }
+            z = P::pack(f.x, f.y);
+        }
+        if constexpr (MASKED) return ((colmask >> j) & 1u) ? z : P::zero();
+        return z;
+    }
 };
 
 template <int I>
 using IntC = std::integral_constant<int, I>;
+template <unsigned U>
+using UIntC = std::integral_constant<unsigned, U>;
 
 // Input rows i of a one-row band (output row oh0, input row oh0 - pad + i) that fall
 // inside the image: [i_lo, i_hi) intersected with the band's [i_lo, i_hi).  Rows outside
@@ -99,12 +145,13 @@ __host__ __device__ constexpr unsigned valid_rows(int i) {
 // MASK) takes filter row i - r, held in register slot (i - r) mod R; ISLOT = i mod R.
 // With column stride SD, input column j of the lane feeds output t through tap
 // fw = j - SD * t.
-template <class P, typename T, int FW, int R, int TM, unsigned MASK, int ISLOT, int SD = 1>
+template <class P, typename T, int FW, int R, int TM, unsigned MASK, int ISLOT, int SD = 1,
+          class XF = NoXform>
 __device__ __forceinline__ void consume_rows(const T* __restrict__ xs, typename P::V (&acc)[R][TM],
-                                             const typename P::V (&wwin)[R][FW]) {
+                                             const typename P::V (&wwin)[R][FW], const XF& xf = XF{}) {
 #pragma unroll
     for (int j = 0; j < SD * (TM - 1) + FW; ++j) {
-        const typename P::V x = P::load(xs + j * kBN);
+        const typename P::V x = xf(P::load(xs + j * kBN), j);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             if (!((MASK >> r) & 1u)) continue;
@@ -119,12 +166,16 @@ __device__ __forceinline__ void consume_rows(const T* __restrict__ xs, typename 
     }
 }
 
-// SD: stride of both spatial axes (1, or 2 with one output row per band).
-template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64, int SD = 1>
+// SD: stride of both spatial axes (1, or 2 with one output row per band).  ACT: -1 plain
+// DWC, else BN + Act fused in front (0 identity, 1 ReLU, 2 ReLU6; forward only).
+template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64, int SD = 1,
+          int ACT = -1>
 __global__ void __launch_bounds__(kRowsMaxThreads, MINB)
 rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
             const RowsArgs a) {
     static_assert(SD == 1 || (R == 1 && !FLIP), "strided bands hold one output row (forward)");
+    static_assert(ACT < 0 || !FLIP, "BN + Act fusion precedes the forward pass only");
+    static_assert(ACT < 0 || SD * (TM - 1) + FW <= 32, "column mask holds 32 staged columns");
     constexpr int S = R + FH - 1;  // input rows per band
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -208,6 +259,42 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         const int owl = ct * TW + wc * TM;  // first output column of this lane
         const int c = cb * kBN + 2 * lane;
 
+        // BN + Act of this lane's two channels and the staged columns inside the image
+        using XFull = typename std::conditional<(ACT >= 0), BnActXform<P, ACT, false>, NoXform>::type;
+        using XMask = typename std::conditional<(ACT >= 0), BnActXform<P, ACT, true>, NoXform>::type;
+        XMask xf{};
+        bool colfull = true;
+        if constexpr (ACT >= 0) {
+            float sc[2] = {0.f, 0.f}, sh[2] = {0.f, 0.f};
+            if (c < a.C) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    sc[k] = a.bn_gamma[c + k] * rsqrtf(a.bn_var[c + k] + a.bn_eps);
+                    sh[k] = a.bn_beta[c + k] - a.bn_mean[c + k] * sc[k];
+                }
+            }
+            xf.scale = P::pack(sc[0], sc[1]);
+            xf.shift = P::pack(sh[0], sh[1]);
+            const int iw0 = ct * TW * SD - a.pad_w + wc * TM * SD;
+            uint32_t m = 0;
+#pragma unroll
+            for (int j = 0; j < SD * (TM - 1) + FW; ++j)
+                if (iw0 + j >= 0 && iw0 + j < a.W) m |= 1u << j;
+            xf.colmask = m;
+            constexpr int ncols = SD * (TM - 1) + FW;
+            colfull = m == (ncols >= 32 ? ~0u : (1u << ncols) - 1u);
+        }
+        // whether input row i of the band lies inside the image (rows in the padding add
+        // nothing to the plain DWC, whose staged copy is zero; with BN + Act they are skipped)
+        auto row_in = [&](int i) -> bool {
+            if constexpr (ACT < 0) {
+                return true;
+            } else {
+                const int ih = oh0 * SD - a.pad_h + i;
+                return ih >= 0 && ih < a.H;
+            }
+        };
+
         typename P::V acc[R][TM];
         typename P::V wwin[R][FW];
 #pragma unroll
@@ -217,6 +304,23 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
 #pragma unroll
             for (int f = 0; f < FW; ++f) wwin[r][f] = P::zero();
         }
+        // consume one staged row (output-row mask M, filter slot SL) with the transform the
+        // warp's columns need; where the band is unrolled (R > 1) a second copy of the row
+        // code costs more in instruction fetch than the mask saves, so those bands always
+        // take the masked form
+        auto consume = [&](auto mc, auto sc, const T* xs) {
+            constexpr unsigned M = decltype(mc)::value;
+            constexpr int SL = decltype(sc)::value;
+            if constexpr (ACT < 0) {
+                consume_rows<P, T, FW, R, TM, M, SL, SD>(xs, acc, wwin);
+            } else if constexpr (R > 1) {
+                consume_rows<P, T, FW, R, TM, M, SL, SD>(xs, acc, wwin, xf);
+            } else if (colfull) {
+                consume_rows<P, T, FW, R, TM, M, SL, SD>(xs, acc, wwin, XFull{xf.scale, xf.shift, 0u});
+            } else {
+                consume_rows<P, T, FW, R, TM, M, SL, SD>(xs, acc, wwin, xf);
+            }
+        };
 
         // Filter row fh lives in register slot fh % R: it enters at input row i = fh and is
         // last used at i = fh + R - 1, when row fh + R (same slot) is not yet needed.
@@ -255,23 +359,23 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             if (!begin_row(IntC<0>{}, 0, xs)) {
                 ok = false;
             } else {
-                consume_rows<P, T, FW, R, TM, 1u, 0>(xs, acc, wwin);
+                if (row_in(0)) consume(UIntC<1u>{}, IntC<0>{}, xs);
                 end_row();
             }
 #pragma unroll 1
             for (int i = 1; i < FH && ok; i += 2) {
                 if (!begin_row(IntC<1>{}, i, xs)) { ok = false; break; }
-                consume_rows<P, T, FW, R, TM, 3u, 1>(xs, acc, wwin);
+                if (row_in(i)) consume(UIntC<3u>{}, IntC<1>{}, xs);
                 end_row();
                 if (!begin_row(IntC<0>{}, i + 1, xs)) { ok = false; break; }
-                consume_rows<P, T, FW, R, TM, 3u, 0>(xs, acc, wwin);
+                if (row_in(i + 1)) consume(UIntC<3u>{}, IntC<0>{}, xs);
                 end_row();
             }
             if (ok) {
                 if (!begin_row(IntC<1>{}, FH, xs)) {
                     ok = false;
                 } else {
-                    consume_rows<P, T, FW, R, TM, 2u, 1>(xs, acc, wwin);
+                    if (row_in(FH)) consume(UIntC<2u>{}, IntC<1>{}, xs);
                     end_row();
                 }
             }
@@ -283,7 +387,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
                 if (!ok) return;
                 const T* xs;
                 if (!begin_row(I, i, xs)) { ok = false; return; }
-                consume_rows<P, T, FW, R, TM, valid_rows<R, FH>(i), i % R>(xs, acc, wwin);
+                if (row_in(i)) consume(UIntC<valid_rows<R, FH>(i)>{}, IntC<i % R>{}, xs);
                 end_row();
             });
         } else {
@@ -295,7 +399,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             for (int i = i_lo; i < i_hi && ok; ++i) {
                 const T* xs;
                 if (!begin_row(IntC<0>{}, i, xs)) { ok = false; break; }
-                consume_rows<P, T, FW, R, TM, 1u, 0, SD>(xs, acc, wwin);
+                consume(UIntC<1u>{}, IntC<0>{}, xs);
                 end_row();
             }
         }
@@ -318,7 +422,8 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     }
 }
 
-template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64, int SD = 1>
+template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64, int SD = 1,
+          int ACT = -1>
 cudaError_t launch_rows_inst(const RowConv& p) {
     const int e = static_cast<int>(sizeof(T));
     const DeviceInfo& dev = device_info();
@@ -362,6 +467,9 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     a.out = p.out;
     a.status = p.status;
     a.H = p.H;
+    a.W = p.W;
+    a.bn_mean = p.bn_mean; a.bn_var = p.bn_var; a.bn_gamma = p.bn_gamma; a.bn_beta = p.bn_beta;
+    a.bn_eps = p.bn_eps;
     a.OH = p.OH; a.OW = p.OW; a.C = p.C;
     a.pad_h = p.pad_h; a.pad_w = p.pad_w;
     a.nwc = nwc;
@@ -376,7 +484,7 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     a.stage_stride = (a.x_bytes + a.w_bytes + 127u) & ~127u;
     if (a.units == 0) return cudaSuccess;
 
-    auto kern = rows_kernel<T, FH, FW, R, TM, MINB, FLIP, P, SD>;
+    auto kern = rows_kernel<T, FH, FW, R, TM, MINB, FLIP, P, SD, ACT>;
     const int threads = (nwc + 1) * 32;
     static int regs = -1;  // per instantiation
     if (regs < 0) {
@@ -446,6 +554,45 @@ cudaError_t launch_rows_s2_dispatch(const RowConv& p) {
         case 3: return launch_rows_inst<T, 3, 3, 1, 8, 3, false, Pair64, 2>(p);
         case 5: return launch_rows_inst<T, 5, 5, 1, 8, 3, false, Pair64, 2>(p);
         case 7: return launch_rows_inst<T, 7, 7, 1, 8, 3, false, Pair64, 2>(p);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+// BN + Act + forward DWC (filters of 3, 5 and 7 taps, stride 1 or 2) on the tiles of the
+// plain forward kernels.
+template <int F>
+struct BnActTile {
+    static constexpr int R = RowsTile<F, F>::R;
+    static constexpr int TM = RowsTile<F, F>::TM;
+    static constexpr int MINB = RowsTile<F, F>::MINB;
+};
+
+template <typename T, int SD, int F, int ACT>
+cudaError_t launch_rows_bnact_inst(const RowConv& p) {
+    if constexpr (SD == 1)
+        return launch_rows_inst<T, F, F, BnActTile<F>::R, BnActTile<F>::TM, BnActTile<F>::MINB,
+                                false, Pair64, 1, ACT>(p);
+    else
+        return launch_rows_inst<T, F, F, 1, 8, 3, false, Pair64, 2, ACT>(p);
+}
+
+template <typename T, int SD, int F>
+cudaError_t launch_rows_bnact_act(const RowConv& p) {
+    switch (p.act) {
+        case 0: return launch_rows_bnact_inst<T, SD, F, 0>(p);
+        case 1: return launch_rows_bnact_inst<T, SD, F, 1>(p);
+        case 2: return launch_rows_bnact_inst<T, SD, F, 2>(p);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+template <typename T, int SD>
+cudaError_t launch_rows_bnact_dispatch(const RowConv& p) {
+    if (p.FH != p.FW || p.flip || p.bn_mean == nullptr) return cudaErrorNotSupported;
+    switch (p.FH) {
+        case 3: return launch_rows_bnact_act<T, SD, 3>(p);
+        case 5: return launch_rows_bnact_act<T, SD, 5>(p);
+        case 7: return launch_rows_bnact_act<T, SD, 7>(p);
         default: return cudaErrorNotSupported;
     }
 }

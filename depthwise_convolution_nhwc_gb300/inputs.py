@@ -16,6 +16,11 @@ GPUs", §6.1.1 and §6.3.2, which use random synthetic tensors, no dataset):
 
 Layouts are channels last: x and dy are N x H x W x C (dy has the output spatial size) and
 the filter is FH x FW x C.
+
+Batch-normalisation parameters for the fused BN + Act + DWC (role 4, fp32, C values each):
+mean ~ U(-0.5, 0.5), var ~ U(0.25, 2), gamma ~ U(0.5, 1.5) and beta ~ U(-0.5, 0.5), so that
+a ReLU clips a sizeable share of the normalised values; the fused forward input x stays
+N(0, 1), scaled by 4 for ReLU6 cases so that some values clip at 6.
 """
 from __future__ import annotations
 
@@ -23,7 +28,7 @@ from dataclasses import dataclass, field, replace
 
 import torch
 
-ROLE_X, ROLE_W, ROLE_DY = 1, 2, 3
+ROLE_X, ROLE_W, ROLE_DY, ROLE_BN = 1, 2, 3, 4
 
 DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
@@ -85,6 +90,17 @@ class Case:
     def dy(self) -> torch.Tensor:
         return draw((self.N, self.OH, self.OW, self.C), seed=self.seed, role=ROLE_DY,
                     dist=self.dist, dtype=self.dtype)
+
+    def bn(self):
+        """Batch statistics and affine parameters (mean, var, gamma, beta) of the fused
+        BN + Act + DWC: C fp32 values each."""
+        g = torch.Generator().manual_seed(1000 * int(self.seed) + ROLE_BN)
+        u = torch.rand((4, self.C), generator=g, dtype=torch.float32)
+        mean = u[0] - 0.5
+        var = 0.25 + 1.75 * u[1]
+        gamma = 0.5 + u[2]
+        beta = u[3] - 0.5
+        return tuple(t.contiguous() for t in (mean, var, gamma, beta))
 
     def elem_bytes(self) -> int:
         return torch.tensor([], dtype=DTYPES[self.dtype]).element_size()

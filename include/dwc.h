@@ -71,6 +71,33 @@ dwc_status_t dwc_fwd(const void* x, const void* w, float* y,
                      int N, int H, int W, int C, int FH, int FW, int stride, int pad,
                      dwc_dtype_t dtype, dwc_stream_t stream);
 
+/* Activation applied after the batch normalisation of dwc_fwd_bn_act. */
+typedef enum {
+    DWC_ACT_NONE = 0,  /* identity */
+    DWC_ACT_RELU = 1,  /* max(v, 0) */
+    DWC_ACT_RELU6 = 2  /* min(max(v, 0), 6) */
+} dwc_act_t;
+
+/* BN + Act + forward DWC fused in one pass ("kernel fusion", §5.2 of the paper: a DWC is
+ * commonly preceded by batch normalisation and an activation; the fused kernel normalises
+ * and activates each input value as it reads it, so the activated tensor never goes
+ * through HBM):
+ *   Z[n, h, w, c] = act((X[n, h, w, c] - mean[c]) / sqrt(var[c] + eps) * gamma[c] + beta[c])
+ *   Y = DWC(Z, W), whose zero padding applies to Z (a tap in the padding reads 0, not
+ *       act(BN(0))).
+ * Forward pass only: the batch statistics are inputs (computed beforehand, or running
+ * statistics at inference); the backward passes through BN and Act are not part of it.
+ *   x : N x H x W x C, dtype      w : FH x FW x C, dtype      y : N x OH x OW x C, fp32 (out)
+ *   mean, var, gamma, beta : C fp32 values each, device memory, read only; eps >= 0.
+ * The fused fast path covers square 3x3, 5x5 and 7x7 filters at stride 1 or 2 under the
+ * layout rules of the fast kernels; other problems run a general fused kernel.  Errors as
+ * dwc_fwd; DWC_ERR_INVALID_ARG also for a null BN pointer (C > 0), an unknown activation or
+ * a negative or non-finite eps; DWC_ERR_ALIGNMENT for a BN pointer not 4-byte aligned. */
+dwc_status_t dwc_fwd_bn_act(const void* x, const float* mean, const float* var,
+                            const float* gamma, const float* beta, float eps, dwc_act_t act,
+                            const void* w, float* y, int N, int H, int W, int C, int FH, int FW,
+                            int stride, int pad, dwc_dtype_t dtype, dwc_stream_t stream);
+
 /* Backward data ("BDC", §5.1): dX = the adjoint of the forward pass in X, i.e.
  *   dX[n, ih, iw, c] = sum over (oh, ow, fh, fw) with oh*s + fh - p = ih and ow*s + fw - p = iw
  *                      of dY[n, oh, ow, c] * W[fh, fw, c];
@@ -139,12 +166,13 @@ const char* dwc_status_string(dwc_status_t status);
 /* Library version as 10000*major + 100*minor + patch. */
 int dwc_version(void);
 
-/* Which kernel family a call with these arguments would use: 1 = fast CUDA-core
- * (row-streaming / filter-gradient) kernels (stride 1; stride 2 for the forward pass with
- * 3x3, 5x5 or 7x7 filters), 2 = tensor-core kernels (16-bit inputs only),
- * 3 = small-map kernels (maps up to 16 x 16), 0 = general kernels, -1 = invalid arguments.  `pass` is 0 for
- * dwc_fwd, 1 for dwc_bwd_data, 2 for dwc_bwd_filter.  Pointer alignment is checked with
- * the pointers given (they may be NULL to mean "16-byte aligned"). */
+/* Which kernel family a call with these arguments would use: 1 = fast CUDA-core kernels
+ * (row-streaming, stride-2 and filter-gradient kernels: stride 1, and stride 2 with 3x3,
+ * 5x5 or 7x7 filters), 2 = tensor-core kernels (16-bit inputs only), 3 = small-map kernels
+ * (maps up to 16 x 16), 0 = general kernels, -1 = invalid arguments.  `pass` is 0 for
+ * dwc_fwd, 1 for dwc_bwd_data, 2 for dwc_bwd_filter, 3 for dwc_fwd_bn_act.  Pointer
+ * alignment is checked with the pointers given (they may be NULL to mean "16-byte
+ * aligned"). */
 int dwc_path(int pass, const void* a, const void* b, const void* out,
              int N, int H, int W, int C, int FH, int FW, int stride, int pad, dwc_dtype_t dtype);
 

@@ -84,6 +84,31 @@ def test_misaligned_pointers_rejected(lib):
     assert call_fwd(lib, x=FAKE + 1, dtype=1) == 3  # bf16 needs 2-byte alignment
 
 
+def call_fwd_bn_act(lib, x=FAKE, mean=FAKE, var=FAKE, gamma=FAKE, beta=FAKE, eps=1e-5, act=1,
+                    w=FAKE, y=FAKE, **kw):
+    a = dict(GOOD, **kw)
+    return lib.dwc_fwd_bn_act(x, mean, var, gamma, beta, eps, act, w, y, a["N"], a["H"], a["W"],
+                              a["C"], a["FH"], a["FW"], a["stride"], a["pad"], a["dtype"], None)
+
+
+def test_fused_bn_act_arguments_rejected_on_host(lib):
+    for kw in (dict(mean=None), dict(var=None), dict(gamma=None), dict(beta=None), dict(x=None),
+               dict(act=3), dict(act=-1), dict(eps=-1.0), dict(eps=float("nan")),
+               dict(eps=float("inf")), dict(stride=0), dict(dtype=7)):
+        assert call_fwd_bn_act(lib, **kw) == 1, kw
+    assert call_fwd_bn_act(lib, gamma=FAKE + 2) == 3    # BN parameters are fp32
+    assert call_fwd_bn_act(lib, x=FAKE + 2) == 3
+
+
+def test_fused_bn_act_path_selection(lib):
+    p = lambda **kw: lib.dwc_path(3, None, None, None, *[dict(GOOD, **kw)[k] for k in
+                                  ("N", "H", "W", "C", "FH", "FW", "stride", "pad", "dtype")])
+    assert p() == 1 and p(FH=5, FW=5, pad=2) == 1 and p(FH=7, FW=7, pad=3, stride=2) == 1
+    assert p(FH=9, FW=9, pad=4, H=20, W=20) == 0      # larger filters: general fused kernel
+    assert p(stride=3) == 0 and p(C=6) == 0 and p(FH=3, FW=5) == 0
+    assert p(C=8, dtype=1) == 1 and p(C=12, dtype=1) == 0
+
+
 def test_size_limits(lib):
     assert call_fwd(lib, N=1 << 20, H=1 << 12, W=1 << 12, C=1 << 10) == 2
 

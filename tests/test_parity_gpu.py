@@ -272,3 +272,94 @@ def test_sweep_full_size_sampled():
     """Every filter size of the sweep on every stage shape, fp32 and bf16, all passes."""
     for case in sweep_cases():
         check_sampled(case, ("fwd", "bwd_data", "bwd_filter"), n_samples=256, seed=case.seed)
+
+
+# -- BN + Act + forward DWC (the fusion of §5.2) -----------------------------------------
+
+BNACT = [
+    C_(2, 17, 19, 64, 3),
+    C_(1, 23, 37, 128, 5),
+    C_(2, 9, 70, 96, 7),            # two column tiles, channel tail
+    C_(1, 12, 300, 64, 7),          # many column tiles: interior lanes and both borders
+    C_(3, 11, 13, 8, 3, p=0),
+    C_(1, 9, 9, 64, 5, p=4),        # padding beyond (F-1)/2: whole rows in the padding
+    C_(1, 1, 1, 64, 3),
+    C_(2, 17, 19, 64, 3, s=2),
+    C_(1, 23, 37, 128, 5, s=2),
+    C_(1, 30, 31, 64, 7, s=2, p=2),
+    C_(1, 8, 8, 64, 7, s=2, p=6),
+]
+# the general fused kernel: larger filters, stride 3, odd channel counts
+BNACT_GENERAL = [C_(1, 12, 13, 64, 9), C_(1, 10, 10, 7, 5, s=3, p=2), C_(2, 9, 11, 5, 3, s=2, p=1)]
+
+
+def bnact_denominator(xn, wn, prm, eps, stride, pad, idx=None):
+    """Error scale of a fused output: the sum over its taps of the magnitudes that form each
+    product, (|x| + |mean|) * |scale| + |beta| times |w|.  The BN value carries a rounding
+    error of that size before the activation, and the activation (1-Lipschitz) does not
+    shrink it: near zero the fp32 and fp64 values may fall on either side of the ReLU."""
+    mean, var, gamma, beta = prm
+    mag = oracle.bn_act(np.abs(xn), -np.abs(mean), var, np.abs(gamma), np.abs(beta), eps, "none")
+    if idx is None:
+        return oracle.fwd(mag, np.abs(wn), stride, pad)
+    return oracle.fwd_at(mag, np.abs(wn), idx, stride, pad)
+
+
+def check_bnact(case, act, expect_path=None):
+    x, w = case.x(), case.w()
+    if act == "relu6":
+        x = (x.float() * 4).to(x.dtype)      # some normalised values beyond 6
+    mean, var, gamma, beta = case.bn()
+    eps = 1e-5
+    if expect_path is not None:
+        code = {"f32": 0, "bf16": 1, "f16": 2}[case.dtype]
+        assert dwc.path("fwd_bn_act", None, None, None, case.N, case.H, case.W, case.C, case.FH,
+                        case.FW, case.stride, case.pad, code) == expect_path
+    y = dwc.fwd_bn_act(x.cuda(), w.cuda(), mean.cuda(), var.cuda(), gamma.cuda(), beta.cuda(),
+                       eps, act, case.stride, case.pad)
+    torch.cuda.synchronize()
+    xn, wn = x.double().numpy(), w.double().numpy()
+    prm = [t.double().numpy() for t in (mean, var, gamma, beta)]
+    ref = oracle.fwd_bn_act(xn, wn, *prm, eps, act, case.stride, case.pad)
+    den = bnact_denominator(xn, wn, prm, eps, case.stride, case.pad)
+    g = y.cpu().numpy()
+    assert g.shape == ref.shape
+    err = normalized_error(g, ref, den)
+    assert err <= TOL[case.dtype], f"fwd_bn_act {act} {case}: normalized error {err:.3e}"
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "relu6"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("case", BNACT, ids=lambda c: f"n{c.N}_{c.H}x{c.W}_c{c.C}_f{c.FH}_s{c.stride}_p{c.pad}")
+def test_fwd_bn_act_fast_path(case, dtype, act):
+    case = Case(**{**case.__dict__, "dtype": dtype})
+    if dtype != "f32" and case.C % 8:
+        pytest.skip("16-bit fast path needs C % 8 == 0")
+    check_bnact(case, act, expect_path=1)
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "relu6"])
+@pytest.mark.parametrize("case", BNACT_GENERAL, ids=lambda c: f"f{c.FH}_s{c.stride}_c{c.C}")
+def test_fwd_bn_act_general_path(case, act):
+    check_bnact(case, act, expect_path=0)
+
+
+def test_fwd_bn_act_full_workload_sampled():
+    """The fused kernel at the 7x7 benchmark shape, checked on sampled outputs."""
+    case = WORKLOADS["f32_n64_56x56_c128_f7"]
+    x, w = case.x(), case.w()
+    mean, var, gamma, beta = case.bn()
+    y = dwc.fwd_bn_act(x.cuda(), w.cuda(), mean.cuda(), var.cuda(), gamma.cuda(), beta.cuda(),
+                       1e-5, "relu", case.stride, case.pad)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    idx = rng.choice(y.numel(), 4096, replace=False)
+    # include the four corners of the first image's first channel block
+    OH, OW, C = y.shape[1], y.shape[2], y.shape[3]
+    idx = np.concatenate([idx, [0, (OW - 1) * C, (OH - 1) * OW * C, (OH * OW - 1) * C]])
+    xn, wn = x.double().numpy(), w.double().numpy()
+    prm = [t.double().numpy() for t in (mean, var, gamma, beta)]
+    ref = oracle.fwd_bn_act_at(xn, wn, *prm, 1e-5, "relu", idx, case.stride, case.pad)
+    den = bnact_denominator(xn, wn, prm, 1e-5, case.stride, case.pad, idx)
+    err = normalized_error(y.cpu().numpy().ravel()[idx], ref, den)
+    assert err <= TOL["f32"], err
