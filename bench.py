@@ -28,7 +28,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "DWC fwd+bwd TFLOP/s and GB/s on 1 GB300, % of roofline, per filter size"
 PASSES_ALL = ("fwd", "bwd_data", "bwd_filter")
-PASS_CODE = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2}
+PASS_CODE = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2, "fwd_bn_act": 3}
 DTYPE_CODE = {"f32": 0, "bf16": 1, "f16": 2}
 # launches of this library's kernels per pass (every kernel family)
 LAUNCHES = {"fwd": 1, "bwd_data": 1, "bwd_filter": 2}
@@ -43,7 +43,15 @@ KERNEL_NAMES = {
     ("bwd_filter", 2): "mma_fgrad_kernel + reduce_slices_kernel",
     ("fwd", 3): "small_rows_kernel", ("bwd_data", 3): "small_rows_kernel",
     ("bwd_filter", 3): "small_fgrad_kernel + reduce_slices_kernel",
+    ("fwd_bn_act", 0): "general_fwd_bnact_kernel", ("fwd_bn_act", 1): "rows_kernel<act>",
 }
+
+
+def kernel_name(case, pass_name, family):
+    """The kernel(s) serving a pass (the stride-2 backward data has its own kernel)."""
+    if case.stride == 2 and family == 1 and pass_name == "bwd_data":
+        return "s2_bwd_data_kernel"
+    return KERNEL_NAMES[(pass_name, family)]
 
 
 def kernel_family(dwc, case, pass_name):
@@ -68,6 +76,9 @@ def parse_args():
     ap.add_argument("--sweep", metavar="DTYPES",
                     help="time every pass of the filter sweep for these input dtypes "
                          "(comma separated, e.g. f32,bf16): one JSON line per sweep point")
+    ap.add_argument("--sweep-set", choices=("stride1", "stride2"), default="stride1",
+                    help="filter sweep over the stage shapes at stride 1, or the stride-2 "
+                         "down-sampling shapes")
     ap.add_argument("--sweep-steps", type=int, default=20)
     ap.add_argument("--sweep-md", metavar="FILE", help="also write the sweep as a markdown table")
     return ap.parse_args()
@@ -79,10 +90,10 @@ def dist_env():
 
 
 def get_case(name):
-    from depthwise_convolution_nhwc_gb300.inputs import WORKLOADS, sweep_cases
+    from depthwise_convolution_nhwc_gb300.inputs import WORKLOADS, stride2_cases, sweep_cases
     if name in WORKLOADS:
         return WORKLOADS[name]
-    for c in sweep_cases():
+    for c in sweep_cases() + stride2_cases():
         if c.name == name:
             return c
     raise SystemExit(f"unknown workload {name!r}")
@@ -432,16 +443,18 @@ def roofline_entry(rl, case, pass_name, family, seconds, peaks):
         src = "fp32 FFMA peak derived: 152 SMs x 128 lanes x 2 x 2070 MHz"
     return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "traffic": None,
-            "kernel": KERNEL_NAMES[(pass_name, family)], "pass": pass_name, "peak_source": src}
+            "kernel": kernel_name(case, pass_name, family), "pass": pass_name,
+            "peak_source": src}
 
 
 def run_sweep(args):
     """Every pass of every sweep point: mean device time over --sweep-steps launches, L2
-    flushed before each, one JSON line per point."""
+    flushed before each, one JSON line per point.  Filters of 3, 5 and 7 taps also time the
+    fused BN + ReLU + forward pass."""
     import torch
     import depthwise_convolution_nhwc_gb300 as dwc
     from depthwise_convolution_nhwc_gb300 import roofline as rl
-    from depthwise_convolution_nhwc_gb300.inputs import sweep_cases
+    from depthwise_convolution_nhwc_gb300.inputs import stride2_cases, sweep_cases
 
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
@@ -450,20 +463,25 @@ def run_sweep(args):
     peaks = rl.load_peaks()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     rows = []
-    for case in sweep_cases(tuple(args.sweep.split(","))):
+    cases = (sweep_cases if args.sweep_set == "stride1" else stride2_cases)(tuple(args.sweep.split(",")))
+    for case in cases:
+        s = case.stride
         x, w, dy = (t.to(dev) for t in (case.x(), case.w(), case.dy()))
         y = torch.empty((case.N, case.OH, case.OW, case.C), device=dev, dtype=torch.float32)
         dx = torch.empty((case.N, case.H, case.W, case.C), device=dev, dtype=torch.float32)
         dw = torch.empty((case.FH, case.FW, case.C), device=dev, dtype=torch.float32)
-        ws = dwc.workspace(dwc.bwd_filter_workspace_size(x.shape, (case.FH, case.FW), 1,
+        ws = dwc.workspace(dwc.bwd_filter_workspace_size(x.shape, (case.FH, case.FW), s,
                                                          case.pad, x.dtype), dev)
-        run = {"fwd": lambda: dwc.fwd(x, w, 1, case.pad, out=y),
-               "bwd_data": lambda: dwc.bwd_data(dy, w, (case.H, case.W), 1, case.pad, out=dx),
-               "bwd_filter": lambda: dwc.bwd_filter(x, dy, (case.FH, case.FW), 1, case.pad,
-                                                    out=dw, ws=ws)}
+        bn = [t.to(dev) for t in case.bn()]
+        run = {"fwd": lambda: dwc.fwd(x, w, s, case.pad, out=y),
+               "bwd_data": lambda: dwc.bwd_data(dy, w, (case.H, case.W), s, case.pad, out=dx),
+               "bwd_filter": lambda: dwc.bwd_filter(x, dy, (case.FH, case.FW), s, case.pad,
+                                                    out=dw, ws=ws),
+               "fwd_bn_act": lambda: dwc.fwd_bn_act(x, w, *bn, 1e-5, "relu", s, case.pad, out=y)}
         line = {"sweep": case.name, "dtype": case.dtype, "N": case.N, "H": case.H, "W": case.W,
-                "C": case.C, "F": case.FH}
-        for name in PASSES_ALL:
+                "C": case.C, "F": case.FH, "stride": s}
+        names = PASSES_ALL + (("fwd_bn_act",) if case.FH <= 7 else ())
+        for name in names:
             for _ in range(3):
                 run[name]()
             evs = []
@@ -479,6 +497,7 @@ def run_sweep(args):
             fam = kernel_family(dwc, case, name)
             roof = roofline_entry(rl, case, name, fam, t, peaks)
             line[name] = {"us": t * 1e6, "tflops": rl.nominal_flops(case) / t / 1e12,
+                          "kernel": kernel_name(case, name, fam),
                           "gbs": rl.compulsory_bytes(case, name) / t / 1e9,
                           "bound": roof["bound"], "roofline_frac": roof["frac"],
                           "family": FAMILY[fam]}
@@ -500,18 +519,20 @@ def write_sweep_md(args, rows):
            "named (hbm: compulsory bytes at the measured HBM copy rate; alu: valid FLOPs at "
            "the derived fp32 FFMA peak; tensor: valid FLOPs at the measured bf16 peak). "
            "Kernel family: cc = CUDA-core row / filter-gradient kernels, tc = tensor-core, "
-           "sm = small-map kernels.\n",
-           "| dtype | N×H×W×C | F | fwd µs | fwd TF/s | fwd roof | bwd_data µs | bwd_data roof "
-           "| bwd_filter µs | bwd_filter TF/s | bwd_filter roof | families |",
-           "|---|---|---|---|---|---|---|---|---|---|---|---|"]
+           "sm = small-map kernels.  BN+ReLU: the fused batch-norm + ReLU + forward pass "
+           "(filters up to 7 taps).\n",
+           "| dtype | N×H×W×C | F | s | fwd µs | fwd TF/s | fwd roof | bwd_data µs | bwd_data roof "
+           "| bwd_filter µs | bwd_filter TF/s | bwd_filter roof | families | BN+ReLU+fwd µs |",
+           "|---|---|---|---|---|---|---|---|---|---|---|---|---|---|"]
     ab = {"cuda-core": "cc", "tensor-core": "tc", "general": "gen", "small-map": "sm"}
     for r in rows:
         f, d, g = r["fwd"], r["bwd_data"], r["bwd_filter"]
-        out.append(f"| {r['dtype']} | {r['N']}×{r['H']}×{r['W']}×{r['C']} | {r['F']} "
+        fz = f"{r['fwd_bn_act']['us']:.1f}" if "fwd_bn_act" in r else "–"
+        out.append(f"| {r['dtype']} | {r['N']}×{r['H']}×{r['W']}×{r['C']} | {r['F']} | {r['stride']} "
                    f"| {f['us']:.1f} | {f['tflops']:.1f} | {f['roofline_frac']:.2f} {f['bound']} "
                    f"| {d['us']:.1f} | {d['roofline_frac']:.2f} {d['bound']} "
                    f"| {g['us']:.1f} | {g['tflops']:.1f} | {g['roofline_frac']:.2f} {g['bound']} "
-                   f"| {ab[f['family']]}/{ab[d['family']]}/{ab[g['family']]} |")
+                   f"| {ab[f['family']]}/{ab[d['family']]}/{ab[g['family']]} | {fz} |")
     with open(args.sweep_md, "w") as fh:
         fh.write("\n".join(out) + "\n")
 
@@ -612,7 +633,7 @@ def run_ours(args, case, passes):
         t = mean_ms[n] * 1e-3
         tr, b = rl.roofline_time_s(case, n, peaks, tensor=fam[n] == 2)
         passes_out[n] = {"ms": mean_ms[n], "ms_median": statistics.median(per_pass[n]),
-                         "kernel": KERNEL_NAMES[(n, fam[n])],
+                         "kernel": kernel_name(case, n, fam[n]),
                          "tflops_nominal": rl.nominal_flops(case) / t / 1e12,
                          "tflops_valid": rl.valid_flops(case) / t / 1e12,
                          "gbs": rl.compulsory_bytes(case, n) / t / 1e9,
@@ -630,7 +651,7 @@ def run_ours(args, case, passes):
                                    "device-to-host copies on three streams ordered by events"}
                     if e2e_value is not None else None),
             "gpu_launches": args.steps * sum(LAUNCHES[n] for n in passes),
-            "kernels": {n: KERNEL_NAMES[(n, fam[n])] for n in passes},
+            "kernels": {n: kernel_name(case, n, fam[n]) for n in passes},
             "clocks": clocks}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(case, passes, args.cpu_seconds)

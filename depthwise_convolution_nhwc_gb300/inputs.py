@@ -135,3 +135,23 @@ def sweep_cases(dtypes=("f32", "bf16")):
                 out.append(Case(N, H, W, C, F, F, 1, (F - 1) // 2, dt, "normal", k,
                                 name=f"sweep_{dt}_n{N}_{H}x{W}_c{C}_f{F}"))
     return out
+
+
+# Down-sampling layers of mobile networks (stride 2): N x H x W x C of the layer input and
+# the filter size, pad (F-1)/2.
+STRIDE2_SHAPES = ((64, 112, 112, 96, 3), (64, 56, 56, 144, 3), (64, 28, 28, 192, 3),
+                  (64, 14, 14, 576, 3), (64, 56, 56, 128, 5), (64, 28, 28, 256, 5),
+                  (64, 56, 56, 144, 7), (64, 28, 28, 256, 7))
+
+
+def stride2_cases(dtypes=("f32", "bf16")):
+    """Stride-2 sweep: the down-sampling shapes above, pad=(F-1)/2."""
+    out = []
+    k = 300
+    for dt in dtypes:
+        for (N, H, W, C, F) in STRIDE2_SHAPES:
+            k += 1
+            out.append(Case(N, H, W, C, F, F, 2, (F - 1) // 2, dt, "normal", k,
+                            name=f"s2_{dt}_n{N}_{H}x{W}_c{C}_f{F}"))
+    return out
+

@@ -54,6 +54,8 @@ def compulsory_bytes(c: Case, which: str) -> int:
     nw = c.FH * c.FW * c.C
     if which == "fwd":
         return e * (nx + nw) + 4 * ny
+    if which == "fwd_bn_act":   # plus the four per-channel BN vectors
+        return e * (nx + nw) + 4 * ny + 16 * c.C
     if which == "bwd_data":
         return e * (ny + nw) + 4 * nx
     if which == "bwd_filter":
