@@ -116,6 +116,29 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// --- division by a launch-time constant ---------------------------------------------------
+// q / d for q < 2^31 and a divisor fixed on the host, with one multiply-high, an add and a
+// shift instead of the runtime's general division (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", 1994): s = ceil(log2 d),
+// m = floor(2^32 * (2^s - d) / d) + 1, then q / d = (umulhi(q, m) + q) >> s, where the sum
+// stays below 2^32 because umulhi(q, m) <= q < 2^31.
+struct FastDiv {
+    uint32_t d = 1, m = 1, s = 0;
+    __host__ void init(uint32_t div) {
+        d = div < 1 ? 1 : div;
+        s = 0;
+        while ((1ull << s) < d) ++s;
+        m = static_cast<uint32_t>((((1ull << 32) * ((1ull << s) - d)) / d) + 1);
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t q) const { return (__umulhi(q, m) + q) >> s; }
+    // quotient, and q - quotient * d in `rem`
+    __device__ __forceinline__ uint32_t divmod(uint32_t q, uint32_t& rem) const {
+        const uint32_t t = div(q);
+        rem = q - t * d;
+        return t;
+    }
+};
+
 // --- arithmetic ------------------------------------------------------------------------
 // acc += a * b on two fp32 lanes at once (one packed FMA instruction on sm_100+).
 __device__ __forceinline__ void fma2(float2& acc, float2 a, float2 b) {

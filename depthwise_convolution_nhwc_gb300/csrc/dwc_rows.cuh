@@ -63,6 +63,7 @@ struct RowsArgs {
     int nwc;              // compute warps per CTA
     int ns;               // pipeline stages
     uint32_t cblocks, bands, ctiles;
+    FastDiv fd_bands, fd_ctiles, fd_cblocks;   // the same three, as invariant divisors
     uint32_t units;
     uint32_t x_bytes;     // bytes of one staged input row box
     uint32_t w_bytes;     // bytes of one staged filter row box
@@ -206,10 +207,9 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         uint32_t issued = 0;  // stages issued so far (saturating; only compared with ns)
         bool ok = true;
         for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-            uint32_t q = u;
-            const int band = static_cast<int>(q % a.bands); q /= a.bands;
-            const int ct = static_cast<int>(q % a.ctiles); q /= a.ctiles;
-            const int cb = static_cast<int>(q % a.cblocks); q /= a.cblocks;
+            uint32_t r0, r1, r2;
+            const uint32_t q = a.fd_cblocks.divmod(a.fd_ctiles.divmod(a.fd_bands.divmod(u, r0), r1), r2);
+            const int band = static_cast<int>(r0), ct = static_cast<int>(r1), cb = static_cast<int>(r2);
             const int n = static_cast<int>(q);
             const int oh0 = band * R, ow0 = ct * TW;
             int i_lo = 0, i_hi = S;
@@ -250,10 +250,9 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     const int wc = warp;
     Ring ring;
     for (uint32_t u = blockIdx.x; u < a.units; u += gridDim.x) {
-        uint32_t q = u;
-        const int band = static_cast<int>(q % a.bands); q /= a.bands;
-        const int ct = static_cast<int>(q % a.ctiles); q /= a.ctiles;
-        const int cb = static_cast<int>(q % a.cblocks); q /= a.cblocks;
+        uint32_t r0, r1, r2;
+        const uint32_t q = a.fd_cblocks.divmod(a.fd_ctiles.divmod(a.fd_bands.divmod(u, r0), r1), r2);
+        const int band = static_cast<int>(r0), ct = static_cast<int>(r1), cb = static_cast<int>(r2);
         const int n = static_cast<int>(q);
         const int oh0 = band * R;
         const int owl = ct * TW + wc * TM;  // first output column of this lane
@@ -297,12 +296,11 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
 
         typename P::V acc[R][TM];
         typename P::V wwin[R][FW];
+        // (every filter slot is loaded at its first row before any tap reads it)
 #pragma unroll
         for (int r = 0; r < R; ++r) {
 #pragma unroll
             for (int t = 0; t < TM; ++t) acc[r][t] = P::zero();
-#pragma unroll
-            for (int f = 0; f < FW; ++f) wwin[r][f] = P::zero();
         }
         // consume one staged row (output-row mask M, filter slot SL) with the transform the
         // warp's columns need; where the band is unrolled (R > 1) a second copy of the row
@@ -410,12 +408,16 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             for (int r = 0; r < R; ++r) {
                 const int oh = oh0 + r;
                 if (oh >= a.OH) break;
-                float* row = a.out + ((static_cast<size_t>(n) * a.OH + oh) * a.OW) * a.C + c;
+                float* row = a.out + ((static_cast<size_t>(n) * a.OH + oh) * a.OW + owl) * a.C + c;
+                if (owl + TM <= a.OW) {
 #pragma unroll
-                for (int t = 0; t < TM; ++t) {
-                    const int ow = owl + t;
-                    if (ow < a.OW)
-                        store_pair_streaming(row + static_cast<size_t>(ow) * a.C, P::unpack(acc[r][t]));
+                    for (int t = 0; t < TM; ++t)
+                        store_pair_streaming(row + static_cast<size_t>(t) * a.C, P::unpack(acc[r][t]));
+                } else {
+#pragma unroll
+                    for (int t = 0; t < TM; ++t)
+                        if (owl + t < a.OW)
+                            store_pair_streaming(row + static_cast<size_t>(t) * a.C, P::unpack(acc[r][t]));
                 }
             }
         }
@@ -476,6 +478,9 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     a.cblocks = static_cast<uint32_t>((p.C + kBN - 1) / kBN);
     a.bands = static_cast<uint32_t>((p.OH + R - 1) / R);
     a.ctiles = static_cast<uint32_t>((p.OW + TW - 1) / TW);
+    a.fd_bands.init(a.bands);
+    a.fd_ctiles.init(a.ctiles);
+    a.fd_cblocks.init(a.cblocks);
     const long long units = static_cast<long long>(p.N) * a.cblocks * a.bands * a.ctiles;
     if (units >= (1LL << 31)) return cudaErrorNotSupported;
     a.units = static_cast<uint32_t>(units);
