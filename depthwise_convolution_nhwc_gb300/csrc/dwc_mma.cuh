@@ -36,7 +36,7 @@ namespace dwc {
 constexpr int kMmaCB = 8;       // channels per work unit
 constexpr int kMmaWarps = 4;    // two channels per warp
 constexpr int kMmaTiles = 7;    // M-tiles of 16 groups per channel and warp (112 groups)
-constexpr int kMmaMaxKC = 3;    // K <= 48, i.e. FW <= 41
+constexpr int kMmaMaxKC = 4;    // K <= 64, i.e. FW <= 57
 
 struct MmaArgs {
     const void* x;
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) mma_rows_kernel(const MmaAr
 
 // Launch plan; false if the shape does not fit the kernel's limits.
 inline bool mma_plan(const RowConv& p, MmaArgs& a, size_t& smem) {
-    if (p.FW > 41 || p.FH < 1 || p.C % kMmaCB != 0) return false;
+    if (p.FW + 7 > 16 * kMmaMaxKC || p.FH < 1 || p.C % kMmaCB != 0) return false;
     a.G = (p.OW + 7) / 8;
     if (a.G > 16 * kMmaTiles) return false;
     a.RB = std::max(1, std::min(p.OH, (16 * kMmaTiles) / a.G));

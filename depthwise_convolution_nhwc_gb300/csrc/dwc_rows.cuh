@@ -51,7 +51,8 @@ template <int FH, int FW>
 struct RowsTile {
     static constexpr int R = (FH <= 3) ? 8 : (FH <= 5 ? 4 : (FH <= 15 ? 2 : 1));
     static constexpr int TM = (FH <= 3) ? 4 : (FH <= 15 ? 8 : 14);
-    static constexpr int MINB = FH == 7 ? 3 : 2;  // CTAs per SM for the registers
+    // CTAs per SM for the registers (past 31 taps a filter row alone takes ~100 registers)
+    static constexpr int MINB = FH == 7 ? 3 : (FH > 31 ? 1 : 2);
 };
 
 struct RowsArgs {
@@ -544,6 +545,16 @@ cudaError_t launch_rows_dispatch(const RowConv& p) {
         DWC_ROWS_CASE(27)
         DWC_ROWS_CASE(29)
         DWC_ROWS_CASE(31)
+        DWC_ROWS_CASE(33)
+        DWC_ROWS_CASE(35)
+        DWC_ROWS_CASE(37)
+        DWC_ROWS_CASE(39)
+        DWC_ROWS_CASE(41)
+        DWC_ROWS_CASE(43)
+        DWC_ROWS_CASE(45)
+        DWC_ROWS_CASE(47)
+        DWC_ROWS_CASE(49)
+        DWC_ROWS_CASE(51)
         default:
             return cudaErrorNotSupported;
     }

@@ -61,6 +61,10 @@ def C_(N, H, W, C, F, s=1, p=None, dtype="f32", seed=7, FW=None):
 
 # Fast-path cases: several column tiles, ragged widths/heights, channel blocks with a tail.
 FAST = [
+    C_(1, 20, 60, 64, 51),          # 51 taps: row kernels (fwd / bwd_data), general gradient
+    C_(2, 9, 40, 64, 33, p=14),
+    C_(1, 30, 45, 64, 41),
+    C_(1, 12, 13, 64, 45, p=22),    # map smaller than the filter, small-map kernels
     C_(2, 17, 19, 64, 3),
     C_(1, 23, 37, 128, 7),
     C_(2, 9, 70, 96, 5),            # two column tiles, channel tail of 32
@@ -111,8 +115,8 @@ def test_fast_path_full_tensors(case, dtype):
     check_full(case)
 
 
-# Stride-2 forward fast path (3x3, 5x5, 7x7): ragged sizes, odd maps, pads 0..F-1, channel
-# tails; the backward passes of these cases run on the general kernels.
+# Stride-2 fast paths of all three passes (3x3, 5x5, 7x7): ragged sizes, odd maps, pads
+# 0..F-1, channel tails.
 STRIDE2 = [
     C_(2, 17, 19, 64, 3, s=2),
     C_(1, 23, 37, 128, 5, s=2),
