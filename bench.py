@@ -76,9 +76,9 @@ def parse_args():
     ap.add_argument("--sweep", metavar="DTYPES",
                     help="time every pass of the filter sweep for these input dtypes "
                          "(comma separated, e.g. f32,bf16): one JSON line per sweep point")
-    ap.add_argument("--sweep-set", choices=("stride1", "stride2"), default="stride1",
-                    help="filter sweep over the stage shapes at stride 1, or the stride-2 "
-                         "down-sampling shapes")
+    ap.add_argument("--sweep-set", choices=("stride1", "stride2", "large"), default="stride1",
+                    help="filter sweep over the stage shapes at stride 1, the stride-2 "
+                         "down-sampling shapes, or 41 and 51 taps over the stage shapes")
     ap.add_argument("--sweep-steps", type=int, default=20)
     ap.add_argument("--sweep-md", metavar="FILE", help="also write the sweep as a markdown table")
     return ap.parse_args()
@@ -90,10 +90,11 @@ def dist_env():
 
 
 def get_case(name):
-    from depthwise_convolution_nhwc_gb300.inputs import WORKLOADS, stride2_cases, sweep_cases
+    from depthwise_convolution_nhwc_gb300.inputs import (WORKLOADS, large_filter_cases,
+                                                         stride2_cases, sweep_cases)
     if name in WORKLOADS:
         return WORKLOADS[name]
-    for c in sweep_cases() + stride2_cases():
+    for c in sweep_cases() + stride2_cases() + large_filter_cases():
         if c.name == name:
             return c
     raise SystemExit(f"unknown workload {name!r}")
@@ -454,7 +455,8 @@ def run_sweep(args):
     import torch
     import depthwise_convolution_nhwc_gb300 as dwc
     from depthwise_convolution_nhwc_gb300 import roofline as rl
-    from depthwise_convolution_nhwc_gb300.inputs import stride2_cases, sweep_cases
+    from depthwise_convolution_nhwc_gb300.inputs import (large_filter_cases, stride2_cases,
+                                                         sweep_cases)
 
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
@@ -463,7 +465,8 @@ def run_sweep(args):
     peaks = rl.load_peaks()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     rows = []
-    cases = (sweep_cases if args.sweep_set == "stride1" else stride2_cases)(tuple(args.sweep.split(",")))
+    cases = {"stride1": sweep_cases, "stride2": stride2_cases,
+             "large": large_filter_cases}[args.sweep_set](tuple(args.sweep.split(",")))
     for case in cases:
         s = case.stride
         x, w, dy = (t.to(dev) for t in (case.x(), case.w(), case.dy()))

@@ -37,26 +37,33 @@ namespace dwc {
 // CTAs per SM the shared-memory window is sized for (MINB) and the period U of the circular
 // x window (any U >= FW works; output columns are processed in blocks of U, so a U that
 // divides the row width leaves no padded columns).
-template <int FH, int FW, int RF_ = 0, int MINB_ = 0, int U_ = 0, int NY_ = 0, int SD_ = 1>
+template <int FH, int FW, int RF_ = 0, int MINB_ = 0, int U_ = 0, int NY_ = 0, int SD_ = 1,
+          int FWC_ = 0>
 struct FgradTile {
     // convolution stride (1, or 2 for the strided 3x3 / 5x5 / 7x7 filter gradient)
     static constexpr int SD = SD_;
-    // x columns one output column of one parity class needs (FW at stride 1; at stride 2
+    // taps of a filter row one warp owns (FWC) and the chunks a row is cut into (NFC): past
+    // 31 taps a whole row's accumulators and window no longer fit in registers, so each
+    // warp takes a chunk of consecutive taps (x read from the chunk's first tap on)
+    static constexpr int FWC = FWC_ > 0 ? FWC_ : FW;
+    static constexpr int NFC = (FW + FWC - 1) / FWC;
+    static_assert(SD == 1 || FWC == FW, "strided tiles keep whole filter rows");
+    // x columns one output column of one parity class needs (FWC at stride 1; at stride 2
     // the even taps read the even columns and the odd taps the odd ones)
-    static constexpr int KW = (FW + SD - 1) / SD;
+    static constexpr int KW = (FWC + SD - 1) / SD;
     // dy ring slots, also the x rows staged ahead of the window: deeper for small filters,
     // whose rows are consumed fastest (timed: 4 up to 5 taps, 3 for 7, else 2)
     static constexpr int NY = NY_ > 0 ? NY_ : (FW <= 5 ? 4 : (FW == 7 ? 3 : 2));
     // rows per warp timed fastest on the stage shapes: 2 for 7x7, 1 for 5x5, 9x9 and
     // 11x11, else what about 120 registers hold
-    static constexpr int kFit = FH == 7 ? 2 : ((FH == 5 || FH == 9 || FH == 11) ? 1 : 120 / (4 * FW));
+    static constexpr int kFit = FH == 7 ? 2 : ((FH == 5 || FH == 9 || FH == 11) ? 1 : 120 / (4 * FWC));
     static constexpr int RF = RF_ > 0 ? RF_ : (kFit < 1 ? 1 : (kFit > FH ? FH : kFit));
     static constexpr int MINB = MINB_ > 0 ? MINB_ : 1;
-    static constexpr int U = U_ > 0 ? U_ : (SD == 1 ? FW : (KW <= 4 ? 4 : KW));
+    static constexpr int U = U_ > 0 ? U_ : (SD == 1 ? FWC : (KW <= 4 ? 4 : KW));
     static_assert(U >= KW, "the window must hold the columns one output column needs");
     // compute warps per CTA where one filter row per warp leaves the registers for more
     // (the launch bound caps registers at 128 per thread for 13 warps, 168 for 12), else 8
-    static constexpr int MAXCW = (RF == 1 && FW <= 19) ? 12 : ((RF == 1 && FW <= 27) ? 11 : 8);
+    static constexpr int MAXCW = (RF == 1 && FWC <= 19) ? 12 : ((RF == 1 && FWC <= 27) ? 11 : 8);
 };
 
 // A second window period per filter width: a multiple of 7 (the widths of the usual
@@ -139,6 +146,8 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     constexpr int RF = Tile::RF;
     constexpr int U = Tile::U;
     constexpr int SD = Tile::SD;
+    constexpr int FC = Tile::FWC;
+    constexpr int NFC = Tile::NFC;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* xfull = reinterpret_cast<uint64_t*>(smem);
     uint64_t* xempty = xfull + a.nx;
@@ -149,7 +158,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int ncompute = a.nwf * a.nwc;
+    const int ncompute = a.nwf * NFC * a.nwc;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.nx; ++s) {
@@ -238,16 +247,17 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 
     // ---------------- compute warps -----------------------------------------------------
     const int wf = warp % a.nwf;
-    const int wc = warp / a.nwf;
+    const int fc = (warp / a.nwf) % NFC;           // tap chunk: taps fc*FC .. fc*FC + FC - 1
+    const int wc = warp / (a.nwf * NFC);
     const int frow0 = wf * RF;                     // first owned row within the chunk
     const int blk0 = wc * a.bps;
     const int blk1 = std::min(blk0 + a.bps, a.nblocks);
 
-    float2 acc[RF][FW];
+    float2 acc[RF][FC];
 #pragma unroll
     for (int f = 0; f < RF; ++f)
 #pragma unroll
-        for (int t = 0; t < FW; ++t) acc[f][t] = make_float2(0.f, 0.f);
+        for (int t = 0; t < FC; ++t) acc[f][t] = make_float2(0.f, 0.f);
 
     bool live[RF];
 #pragma unroll
@@ -289,10 +299,11 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             for (int f = 0; f < RF; ++f) {
                 uint32_t ph;
                 const uint32_t sl = xslot(static_cast<uint32_t>(frow0 + f), ph);
-                xs[f] = reinterpret_cast<const T*>(xring + static_cast<size_t>(sl) * a.x_bytes) + 2 * lane;
+                xs[f] = reinterpret_cast<const T*>(xring + static_cast<size_t>(sl) * a.x_bytes) +
+                        2 * lane + fc * FC * kBN;
             }
             if constexpr (SD == 2) {
-                if (blk0 < blk1) fgrad_row_s2<T, FW, RF, U>(acc, xs, ys, blk0, blk1);
+                if (blk0 < blk1) fgrad_row_s2<T, FC, RF, U>(acc, xs, ys, blk0, blk1);
             } else if (blk0 < blk1) {
                 // circular window: column c of the padded x row sits in slot c mod U
                 float2 win[RF][U];
@@ -300,7 +311,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 #pragma unroll
                 for (int f = 0; f < RF; ++f)
 #pragma unroll
-                    for (int m = 0; m < FW - 1; ++m)
+                    for (int m = 0; m < FC - 1; ++m)
                         win[f][m] = Elem<T>::load_pair(xs[f] + (c0 + m) * kBN);
 #pragma unroll 1
                 for (int blk = blk0; blk < blk1; ++blk) {
@@ -313,9 +324,9 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                             // a row past the filter's last row (last chunk) computes from its
                             // staged window row like the others and is never written: no
                             // branch in this loop
-                            win[f][(u + FW - 1) % U] = Elem<T>::load_pair(xs[f] + (cb0 + u + FW - 1) * kBN);
+                            win[f][(u + FC - 1) % U] = Elem<T>::load_pair(xs[f] + (cb0 + u + FC - 1) * kBN);
 #pragma unroll
-                            for (int t = 0; t < FW; ++t) fma2(acc[f][t], win[f][(u + t) % U], g);
+                            for (int t = 0; t < FC; ++t) fma2(acc[f][t], win[f][(u + t) % U], g);
                         }
                     }
                 }
@@ -346,27 +357,31 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     // All ring copies have landed (every stage was waited on), so the ring is reused.
     asm volatile("bar.sync 1, %0;" ::"r"(ncompute * 32) : "memory");
     float2* red = reinterpret_cast<float2*>(xring);
-    // layout: [wc][wf][f][t][lane]
-    const size_t per_warp = static_cast<size_t>(RF) * FW * 32;
-    float2* mine = red + (static_cast<size_t>(wc) * a.nwf + wf) * per_warp;
+    // layout: [wc][wf][fc][f][t][lane]
+    const size_t per_warp = static_cast<size_t>(RF) * FC * 32;
+    const size_t wslot = static_cast<size_t>(a.nwf) * NFC;   // warps of one column strip
+    float2* mine = red + (static_cast<size_t>(wc) * wslot + wf * NFC + fc) * per_warp;
 #pragma unroll
     for (int f = 0; f < RF; ++f)
 #pragma unroll
-        for (int t = 0; t < FW; ++t) mine[(f * FW + t) * 32 + lane] = acc[f][t];
+        for (int t = 0; t < FC; ++t) mine[(f * FC + t) * 32 + lane] = acc[f][t];
     asm volatile("bar.sync 1, %0;" ::"r"(ncompute * 32) : "memory");
     if (wc == 0) {
         const int c = cb * kBN + 2 * lane;
         for (int f = 0; f < RF; ++f) {
             const int fh = fh0 + frow0 + f;
             if (!live[f] || c >= a.C) continue;
-            for (int t = 0; t < FW; ++t) {
-                float2 s = red[(static_cast<size_t>(wf) * per_warp) + (f * FW + t) * 32 + lane];
+            for (int t = 0; t < FC; ++t) {
+                const int fw = fc * FC + t;
+                if (fw >= FW) break;
+                const size_t off = static_cast<size_t>(wf * NFC + fc) * per_warp + (f * FC + t) * 32 + lane;
+                float2 s = red[off];
                 for (int k = 1; k < a.nwc; ++k) {
-                    const float2 v = red[(static_cast<size_t>(k) * a.nwf + wf) * per_warp + (f * FW + t) * 32 + lane];
+                    const float2 v = red[static_cast<size_t>(k) * wslot * per_warp + off];
                     s.x += v.x;
                     s.y += v.y;
                 }
-                float* dst = a.part + ((static_cast<size_t>(z) * FH + fh) * FW + t) * a.C + c;
+                float* dst = a.part + ((static_cast<size_t>(z) * FH + fh) * FW + fw) * a.C + c;
                 *reinterpret_cast<float2*>(dst) = s;
             }
         }
@@ -390,7 +405,8 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     const size_t smem_cap = std::min<size_t>(dev.max_smem_optin, 233472 / Tile::MINB - 1024);
     P.nblocks = (OW + Tile::U - 1) / Tile::U;
     P.owp = P.nblocks * Tile::U;
-    P.pwx = Tile::SD * (P.owp - 1) + FW;
+    // (the last tap chunk may run past the filter's last tap: its x columns are staged too)
+    P.pwx = Tile::SD * (P.owp - 1) + Tile::NFC * Tile::FWC;
     if (P.pwx > 256) return false;
     P.x_bytes = static_cast<uint32_t>(P.pwx * kBN * e);
     P.y_bytes = static_cast<uint32_t>(P.owp * kBN * e);
@@ -405,7 +421,8 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     double best = -1.0;
     P.nwf = 0;
     int best_la = 0;
-    for (int nwf = std::min(groups, Tile::MAXCW); nwf >= 1; --nwf) {
+    constexpr int NFC = Tile::NFC;
+    for (int nwf = std::min(groups, Tile::MAXCW / NFC); nwf >= 1; --nwf) {
         int la = Tile::NY;
         auto need = [&](int l) {
             return 512 + static_cast<size_t>(nwf * RF + l * Tile::SD) * P.x_bytes +
@@ -415,14 +432,15 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
         if (need(la) > smem_cap) continue;
         const int chunks = (groups + nwf - 1) / nwf;
         if ((groups + chunks - 1) / chunks != nwf) continue;  // same chunks, fewer warps: seen
-        const int nwc0 = std::max(1, std::min(Tile::MAXCW / nwf, P.nblocks));
+        const int nwc0 = std::max(1, std::min(Tile::MAXCW / (nwf * NFC), P.nblocks));
         const int bps = (P.nblocks + nwc0 - 1) / nwc0;
         const int nwc = (P.nblocks + bps - 1) / bps;
-        // the strip sums at the end reuse the ring: [nwc][nwf][RF][FW][32] float2
-        if (512 + static_cast<size_t>(nwc) * nwf * RF * FW * 32 * sizeof(float2) > smem_cap) continue;
+        // the strip sums at the end reuse the ring: [nwc][nwf][NFC][RF][FWC][32] float2
+        if (512 + static_cast<size_t>(nwc) * nwf * NFC * RF * Tile::FWC * 32 * sizeof(float2) > smem_cap)
+            continue;
         const double useful = static_cast<double>(groups) / (chunks * nwf) *
                               static_cast<double>(P.nblocks) / (nwc * bps);
-        const double score = useful * std::min(nwf * nwc, 12) / (1.0 + 0.2 * chunks);
+        const double score = useful * std::min(nwf * NFC * nwc, 12) / (1.0 + 0.2 * chunks);
         if (score > best * (1.0 + 1e-9)) {
             best = score;
             P.nwf = nwf;
@@ -438,7 +456,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     P.smem = 512 + static_cast<size_t>(P.nx) * P.x_bytes + static_cast<size_t>(P.ny) * P.y_bytes;
     P.chunks = (FH + P.fhc - 1) / P.fhc;
     // strip reduction buffer reuses the ring
-    const size_t red = static_cast<size_t>(P.nwc) * P.nwf * RF * FW * 32 * sizeof(float2);
+    const size_t red = static_cast<size_t>(P.nwc) * P.nwf * NFC * RF * Tile::FWC * 32 * sizeof(float2);
     if (red > P.smem - 512) P.smem = 512 + red;
     P.y_off = static_cast<uint32_t>(P.nx) * P.x_bytes;
     P.cblocks = (C + kBN - 1) / kBN;
@@ -450,7 +468,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     // registers let an SM hold (measured faster there); larger filters keep one CTA per SM
     // (more, shorter slices measured slower from 7 taps on).
     static const int regs = kernel_regs(fgrad_kernel<T, FH, FW, Tile>, 224);
-    const int ctas_per_sm = FW <= 5 ? std::max(Tile::MINB, resident_ctas(P.smem, (P.nwf * P.nwc + 1) * 32, regs))
+    const int ctas_per_sm = FW <= 5 ? std::max(Tile::MINB, resident_ctas(P.smem, (P.nwf * NFC * P.nwc + 1) * 32, regs))
                                     : Tile::MINB;
     long long Z = static_cast<long long>(dev.sm_count) * ctas_per_sm / per_z;
     Z = std::max<long long>(1, std::min<long long>(Z, rows));
@@ -505,7 +523,7 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
         if (err != cudaSuccess) return err;
         attr_set = true;
     }
-    const int threads = (P.nwf * P.nwc + 1) * 32;
+    const int threads = (P.nwf * Tile::NFC * P.nwc + 1) * 32;
     const unsigned grid = static_cast<unsigned>(P.Z) * P.cblocks * P.chunks;
     kern<<<grid, threads, P.smem, p.stream>>>(xmap, ymap, a);
     cudaError_t err = cudaGetLastError();
@@ -528,6 +546,20 @@ size_t fgrad_workspace_dispatch(int N, int OH, int OW, int C) {
 }
 
 #define DWC_FGRAD_FILTERS(X) X(3) X(5) X(7) X(9) X(11) X(13) X(15) X(17) X(19) X(21) X(23) X(25) X(27) X(29) X(31)
+#define DWC_FGRAD_BIG_FILTERS(X) X(33) X(35) X(37) X(39) X(41) X(43) X(45) X(47) X(49) X(51)
+
+// 33..51 taps: each filter row in two chunks of (F + 1) / 2 taps, one warp each; window
+// period the chunk width, or 28 (a multiple of 7) where that pads the row less.
+template <int F>
+using FgradBigTile = FgradTile<F, F, 0, 0, 0, 0, 1, (F + 1) / 2>;
+template <int F>
+using FgradBigAltTile = FgradTile<F, F, 0, 0, 28, 0, 1, (F + 1) / 2>;
+
+template <int F>
+bool fgrad_big_use_alt(int OW) {
+    constexpr int UD = (F + 1) / 2;
+    return (OW + 27) / 28 * 28 < (OW + UD - 1) / UD * UD;
+}
 
 // Workspace floats of the CUDA-core filter gradient for inputs of type T.
 template <typename T>
@@ -539,6 +571,12 @@ size_t fgrad_workspace_t(int N, int OH, int OW, int C, int FH, int FW) {
         return fgrad_workspace_dispatch<T, F>(N, OH, OW, C);
         DWC_FGRAD_FILTERS(DWC_FGRAD_WS)
 #undef DWC_FGRAD_WS
+#define DWC_FGRAD_BIG_WS(F)                                                              \
+    case F:                                                                              \
+        return fgrad_big_use_alt<F>(OW) ? fgrad_workspace_inst<T, F, F, FgradBigAltTile<F>>(N, OH, OW, C) \
+                                        : fgrad_workspace_inst<T, F, F, FgradBigTile<F>>(N, OH, OW, C);
+        DWC_FGRAD_BIG_FILTERS(DWC_FGRAD_BIG_WS)
+#undef DWC_FGRAD_BIG_WS
         default:
             return 0;
     }
@@ -582,6 +620,13 @@ cudaError_t launch_fgrad_dispatch(const FilterGrad& p) {
                    : launch_fgrad_inst<T, F, F>(p);
         DWC_FGRAD_FILTERS(DWC_FGRAD_CASE)
 #undef DWC_FGRAD_CASE
+#define DWC_FGRAD_BIG_CASE(F)                                             \
+    case F:                                                               \
+        return fgrad_big_use_alt<F>(p.OW)                                 \
+                   ? launch_fgrad_inst<T, F, F, FgradBigAltTile<F>>(p)     \
+                   : launch_fgrad_inst<T, F, F, FgradBigTile<F>>(p);
+        DWC_FGRAD_BIG_FILTERS(DWC_FGRAD_BIG_CASE)
+#undef DWC_FGRAD_BIG_CASE
         default:
             return cudaErrorNotSupported;
     }

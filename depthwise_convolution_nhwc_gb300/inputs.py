@@ -137,6 +137,23 @@ def sweep_cases(dtypes=("f32", "bf16")):
     return out
 
 
+LARGE_FILTERS = (41, 51)
+
+
+def large_filter_cases(dtypes=("f32", "bf16")):
+    """Filters beyond the sweep (41 and 51 taps, the largest the pages evaluate) over the
+    four stage shapes, pad=(F-1)/2, stride 1."""
+    out = []
+    k = 500
+    for dt in dtypes:
+        for (N, H, W, C) in SWEEP_SHAPES:
+            for F in LARGE_FILTERS:
+                k += 1
+                out.append(Case(N, H, W, C, F, F, 1, (F - 1) // 2, dt, "normal", k,
+                                name=f"large_{dt}_n{N}_{H}x{W}_c{C}_f{F}"))
+    return out
+
+
 # Down-sampling layers of mobile networks (stride 2): N x H x W x C of the layer input and
 # the filter size, pad (F-1)/2.
 STRIDE2_SHAPES = ((64, 112, 112, 96, 3), (64, 56, 56, 144, 3), (64, 28, 28, 192, 3),

@@ -148,9 +148,10 @@ def test_path_selection_host_logic(lib):
     assert p(0, C=6) == 0                      # fp32 rows must be 16-byte multiples
     assert p(0, C=8, dtype=1, **f5) == 3 and p(0, C=8, dtype=1, **big_map) == 1
     assert p(0, C=12, dtype=1) == 0            # bf16 needs C % 8 == 0
-    # 33..51 taps: row kernels for the forward and data passes, general filter gradient
+    # 33..51 taps: row kernels, filter gradient in tap chunks
     f33 = dict(FH=33, FW=33, pad=16, H=40, W=40)
-    assert p(0, **f33) == 1 and p(1, **f33) == 1 and p(2, **f33) == 0
+    assert p(0, **f33) == 1 and p(1, **f33) == 1 and p(2, **f33) == 1
+    assert p(2, FH=51, FW=51, pad=25, H=60, W=60) == 1
     assert p(0, FH=51, FW=51, pad=25, H=60, W=60) == 1
     assert p(0, FH=53, FW=53, pad=26, H=60, W=60) == 0
     # 16-bit inputs: tensor-core kernels for large filters on wide rows
