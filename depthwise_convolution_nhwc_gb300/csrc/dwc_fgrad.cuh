@@ -38,7 +38,7 @@ namespace dwc {
 // x window (any U >= FW works; output columns are processed in blocks of U, so a U that
 // divides the row width leaves no padded columns).
 template <int FH, int FW, int RF_ = 0, int MINB_ = 0, int U_ = 0, int NY_ = 0, int SD_ = 1,
-          int FWC_ = 0>
+          int FWC_ = 0, int MAXCW_ = 0>
 struct FgradTile {
     // convolution stride (1, or 2 for the strided 3x3 / 5x5 / 7x7 filter gradient)
     static constexpr int SD = SD_;
@@ -61,9 +61,11 @@ struct FgradTile {
     static constexpr int MINB = MINB_ > 0 ? MINB_ : 1;
     static constexpr int U = U_ > 0 ? U_ : (SD == 1 ? FWC : (KW <= 4 ? 4 : KW));
     static_assert(U >= KW, "the window must hold the columns one output column needs");
-    // compute warps per CTA where one filter row per warp leaves the registers for more
-    // (the launch bound caps registers at 128 per thread for 13 warps, 168 for 12), else 8
-    static constexpr int MAXCW = (RF == 1 && FWC <= 19) ? 12 : ((RF == 1 && FWC <= 27) ? 11 : 8);
+    // compute warps per CTA where the registers leave room for more (the launch bound caps
+    // registers at 128 per thread for 13 warps, 168 for 12), else 8
+    // (7x7 at stride 1, two rows per warp: 12 warps timed 2.5 % faster than 8 on 56x56x128)
+    static constexpr int MAXCW = MAXCW_ > 0 ? MAXCW_ :
+        ((RF == 1 && FWC <= 19) || (FW == 7 && RF == 2 && SD == 1) ? 12 : ((RF == 1 && FWC <= 27) ? 11 : 8));
 };
 
 // A second window period per filter width: a multiple of 7 (the widths of the usual
@@ -89,9 +91,10 @@ bool fgrad_use_alt_period(int OW) {
 }
 
 struct FgradArgs {
-    float* part;           // [Z][FH][FW][C] partial sums
+    float* part;           // [Z * ncp][FH][FW][C] partial sums
     unsigned int* status;
     int N, OH, C, pad;
+    int ncp, owpart;       // column parts of a row, output columns per part
     int nwf, nwc;          // compute warps: filter-row groups x column strips
     int fhc, chunks, cblocks, Z;
     int rows_per_slice;    // flattened output rows per slice
@@ -178,7 +181,9 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     int b = blockIdx.x;
     const int chunk = b % a.chunks; b /= a.chunks;
     const int cb = b % a.cblocks; b /= a.cblocks;
+    const int cp = b % a.ncp; b /= a.ncp;   // column part: output columns cp*owpart + [0, owpart)
     const int z = b;
+    const int ow_base = cp * a.owpart;
     const int fh0 = chunk * a.fhc;
     const long long total_rows = static_cast<long long>(a.N) * a.OH;
     const long long q0 = static_cast<long long>(z) * a.rows_per_slice;
@@ -200,7 +205,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             if (xissued < static_cast<uint32_t>(a.nx)) ++xissued;
             mbar_arrive_expect_tx(&xfull[xr.slot], a.x_bytes);
             tma_load_4d(xring + static_cast<size_t>(xr.slot) * a.x_bytes, &xmap, &xfull[xr.slot],
-                        cb * kBN, -a.pad, ih, n);
+                        cb * kBN, ow_base * SD - a.pad, ih, n);
             xr.next(a.nx);
             return true;
         };
@@ -210,7 +215,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             if (yissued < static_cast<uint32_t>(a.ny)) ++yissued;
             mbar_arrive_expect_tx(&yfull[yr.slot], a.y_bytes);
             tma_load_4d(yring + static_cast<size_t>(yr.slot) * a.y_bytes, &ymap, &yfull[yr.slot],
-                        cb * kBN, 0, oh, n);
+                        cb * kBN, ow_base, oh, n);
             yr.next(a.ny);
             return true;
         };
@@ -381,7 +386,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     s.x += v.x;
                     s.y += v.y;
                 }
-                float* dst = a.part + ((static_cast<size_t>(z) * FH + fh) * FW + fw) * a.C + c;
+                float* dst = a.part + ((static_cast<size_t>(z * a.ncp + cp) * FH + fh) * FW + fw) * a.C + c;
                 *reinterpret_cast<float2*>(dst) = s;
             }
         }
@@ -394,16 +399,22 @@ struct FgradPlan {
     uint32_t x_bytes, y_bytes, y_off;
     size_t smem;
     int pwx, owp;
+    int ncp, owpart;   // column parts per row and output columns per part
 };
 
-// Shapes of the launch for one problem (shared by the workspace query and the launch).
-template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
-bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
+// One candidate launch shape: the row cut into ncp column parts (one CTA each), with the
+// deepest lookahead between min_la output rows and the tile's that fits.
+template <typename T, int FH, int FW, class Tile>
+bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
+                      FgradPlan<FH, FW, Tile>& P) {
     const int e = static_cast<int>(sizeof(T));
     constexpr int RF = Tile::RF;
     const DeviceInfo& dev = device_info();
     const size_t smem_cap = std::min<size_t>(dev.max_smem_optin, 233472 / Tile::MINB - 1024);
-    P.nblocks = (OW + Tile::U - 1) / Tile::U;
+    P.ncp = ncp;
+    P.owpart = (OW + ncp - 1) / ncp;
+    P.nblocks = (P.owpart + Tile::U - 1) / Tile::U;
+    P.owpart = P.nblocks * Tile::U;
     P.owp = P.nblocks * Tile::U;
     // (the last tap chunk may run past the filter's last tap: its x columns are staged too)
     P.pwx = Tile::SD * (P.owp - 1) + Tile::NFC * Tile::FWC;
@@ -417,7 +428,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     // its slice again); the weights were fitted to timings of the stage shapes.
     const int groups = (FH + RF - 1) / RF;  // RF-row groups needed to cover the filter
     // The lookahead (dy slots, and the x rows staged ahead of the window) is Tile::NY
-    // output rows; at stride 2, whose x rows are twice as wide, the deepest that fits.
+    // output rows, or the deepest down to min_la that fits.
     double best = -1.0;
     P.nwf = 0;
     int best_la = 0;
@@ -428,7 +439,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
             return 512 + static_cast<size_t>(nwf * RF + l * Tile::SD) * P.x_bytes +
                    static_cast<size_t>(l) * P.y_bytes;
         };
-        while (Tile::SD > 1 && la > 1 && need(la) > smem_cap) --la;
+        while (la > min_la && need(la) > smem_cap) --la;
         if (need(la) > smem_cap) continue;
         const int chunks = (groups + nwf - 1) / nwf;
         if ((groups + chunks - 1) / chunks != nwf) continue;  // same chunks, fewer warps: seen
@@ -461,7 +472,7 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     P.y_off = static_cast<uint32_t>(P.nx) * P.x_bytes;
     P.cblocks = (C + kBN - 1) / kBN;
     const long long rows = static_cast<long long>(N) * OH;
-    const long long per_z = static_cast<long long>(P.cblocks) * P.chunks;
+    const long long per_z = static_cast<long long>(P.cblocks) * P.chunks * P.ncp;
     // One wave: every CTA runs the same number of rows, so a grid a few CTAs larger than
     // the resident capacity would take a second wave for those few; round down.  For
     // filters up to 5 taps the capacity counts every CTA that shared memory, threads and
@@ -477,6 +488,27 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
     return true;
 }
 
+// Shapes of the launch for one problem (shared by the workspace query and the launch).  A
+// whole row per CTA with the tile's lookahead where it fits (stride 2: the deepest lookahead
+// that fits); otherwise a lookahead of at least two rows, then of one (two rows with fewer
+// filter rows per CTA timed faster than one row with more: 7x7 on 64x112x112x64, 177 against
+// 233 us), then the row cut into 2, 3 or 4 column parts (rows too wide for shared memory or
+// for one 256-column TMA box), each part a CTA of its own with its own partial-sum slot.
+template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
+bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
+    for (int ncp = 1; ncp <= 4; ++ncp) {
+        if (ncp > 1 && (OW + ncp - 1) / ncp < Tile::U) break;
+        if (Tile::SD > 1) {
+            if (fgrad_plan_parts<T, FH, FW, Tile>(N, OH, OW, C, ncp, 1, P)) return true;
+            continue;
+        }
+        for (int min_la : {Tile::NY, 2, 1})
+            if (min_la <= Tile::NY && fgrad_plan_parts<T, FH, FW, Tile>(N, OH, OW, C, ncp, min_la, P))
+                return true;
+    }
+    return false;
+}
+
 template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
 cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     const int e = static_cast<int>(sizeof(T));
@@ -485,7 +517,7 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     if (p.N == 0 || p.OH == 0 || p.OW == 0) {
         return cudaMemsetAsync(p.dw, 0, sizeof(float) * FH * FW * p.C, p.stream);
     }
-    const size_t need = static_cast<size_t>(P.Z) * FH * FW * p.C;
+    const size_t need = static_cast<size_t>(P.Z) * P.ncp * FH * FW * p.C;
     if (p.workspace_floats < need || p.workspace == nullptr) return cudaErrorInvalidValue;
 
     CUtensorMap xmap, ymap;
@@ -511,6 +543,7 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     a.part = p.workspace;
     a.status = p.status;
     a.N = p.N; a.OH = p.OH; a.C = p.C; a.pad = p.pad;
+    a.ncp = P.ncp; a.owpart = P.owpart;
     a.nwf = P.nwf; a.nwc = P.nwc; a.fhc = P.fhc; a.chunks = P.chunks; a.cblocks = P.cblocks;
     a.Z = P.Z; a.rows_per_slice = P.rows_per_slice; a.nblocks = P.nblocks; a.bps = P.bps;
     a.nx = P.nx; a.ny = P.ny; a.x_bytes = P.x_bytes; a.y_bytes = P.y_bytes; a.y_off = P.y_off;
@@ -524,18 +557,19 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
         attr_set = true;
     }
     const int threads = (P.nwf * Tile::NFC * P.nwc + 1) * 32;
-    const unsigned grid = static_cast<unsigned>(P.Z) * P.cblocks * P.chunks;
+    const unsigned grid = static_cast<unsigned>(P.Z) * P.ncp * P.cblocks * P.chunks;
     kern<<<grid, threads, P.smem, p.stream>>>(xmap, ymap, a);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    return launch_reduce_slices(p.workspace, P.Z, static_cast<size_t>(FH) * FW * p.C, p.dw, p.stream);
+    return launch_reduce_slices(p.workspace, P.Z * P.ncp, static_cast<size_t>(FH) * FW * p.C, p.dw,
+                                p.stream);
 }
 
 template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
 size_t fgrad_workspace_inst(int N, int OH, int OW, int C) {
     FgradPlan<FH, FW, Tile> P;
     if (!fgrad_plan<T, FH, FW, Tile>(N, OH, OW, C, P)) return 0;
-    return static_cast<size_t>(P.Z) * FH * FW * static_cast<size_t>(C);
+    return static_cast<size_t>(P.Z) * P.ncp * FH * FW * static_cast<size_t>(C);
 }
 
 // Workspace of the launch that launch_fgrad_dispatch makes for this problem.

@@ -117,6 +117,9 @@ _WORKLOADS = {
     # backward shape, 13x13 filter, fp32 and bf16
     "f32_n64_28x28_c256_f13": Case(64, 28, 28, 256, 13, 13, 1, 6, "f32", "normal", 3),
     "bf16_n64_28x28_c256_f13": Case(64, 28, 28, 256, 13, 13, 1, 6, "bf16", "normal", 3),
+    # wide maps (the early stages of 224-pixel networks), 7x7 filter
+    "f32_n64_112x112_c64_f7": Case(64, 112, 112, 64, 7, 7, 1, 3, "f32", "normal", 4),
+    "f32_n16_224x224_c32_f7": Case(16, 224, 224, 32, 7, 7, 1, 3, "f32", "normal", 5),
 }
 WORKLOADS = {k: replace(v, name=k) for k, v in _WORKLOADS.items()}
 

@@ -139,8 +139,9 @@ def test_path_selection_host_logic(lib):
     assert p(0, stride=2) == 1 and p(0, stride=2, FH=5, FW=5, pad=2) == 1
     assert p(1, stride=2) == 1 and p(2, stride=2) == 1
     assert p(1, stride=2, FH=7, FW=7, pad=3) == 1 and p(2, stride=2, FH=7, FW=7, pad=3) == 1
-    # filter gradient: a padded x row beyond one 256-column TMA box goes to the general kernel
-    assert p(2, stride=2, W=300) == 0 and p(1, stride=2, W=300) == 1
+    # filter gradient: a row too wide for one 256-column TMA box is cut into column parts
+    assert p(2, stride=2, W=300) == 1 and p(1, stride=2, W=300) == 1
+    assert p(2, W=300) == 1 and p(2, W=224, FH=31, FW=31, pad=15) == 1
     assert p(0, stride=2, FH=9, FW=9, pad=4, H=40, W=40) == 0 and p(0, stride=3) == 0
     assert p(0, stride=2, C=6) == 0
     assert p(0, FH=4, FW=4) == 0               # even filter
