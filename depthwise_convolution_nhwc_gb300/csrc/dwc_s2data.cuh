@@ -13,11 +13,10 @@
 // (r, q) of the cell receives exactly the taps fh = r + 2k, fw = q + 2j, from dy[a - k, b - j],
 // so the whole cell needs only the K x K dy values dy[a - k, b - j] (K = (F + 1) / 2) and
 // every tap of the filter once.  A thread owns two channels (one fp32x2 lane pair) of one
-// cell row a and a strip of consecutive cells b: the F x F filter taps stay in registers,
-// the dy values sit in a circular register window of K columns that advances by one column
-// per cell, and each cell costs K dy loads, F*F packed FMAs and four 8-byte stores.  The
-// kernel is bound by HBM (the dx writes and the dy reads); consecutive threads take
-// consecutive channel pairs, so every warp load and store is contiguous.
+// cell row a and a strip of S consecutive cells b: the F x F filter taps and the strip's
+// K x (S + K - 1) dy values sit in registers (7x7: a circular window of K dy columns, see
+// s2_bwd_data_stream_kernel), and each cell costs F*F packed FMAs and four 8-byte stores.  The kernel is bound by HBM (the dx writes and the dy reads); consecutive
+// threads take consecutive channel pairs, so every warp load and store is contiguous.
 #pragma once
 
 #include "dwc_device.cuh"
@@ -31,12 +30,98 @@ struct S2DataArgs {
     int ncp;            // channel pairs (C / 2)
     int na, a_lo;       // cell rows a_lo .. a_lo + na - 1
     int nb, b_lo;       // cell columns b_lo .. b_lo + nb - 1
-    int nstrips, strip; // strips per cell row, cells per strip (a multiple of K)
+    int nstrips, strip; // strips per cell row, cells per strip
+};
+
+// Cells per thread strip: the strip's whole dy window (K rows x S + K - 1 columns) is loaded
+// before any FMA, so that every load of the strip is in flight at once (loading one column
+// per cell left the kernel waiting on L2/HBM latency: ncu showed long-scoreboard stalls of
+// 12 cycles per issued instruction and DRAM half busy; 3x3 on 64x112x112x96 went from 85
+// to 64 us).  Used for 3x3 and 5x5.
+template <int F>
+struct S2DataTile {
+    static constexpr int K = (F + 1) / 2;
+    static constexpr int S = 8;
 };
 
 template <typename T, int F>
-__global__ void __launch_bounds__(128, F <= 5 ? 4 : 3)
+__global__ void __launch_bounds__(128, 4)
 s2_bwd_data_kernel(const T* __restrict__ dy, const T* __restrict__ w, const S2DataArgs a) {
+    using P = Pair64;
+    using V = P::V;
+    constexpr int K = S2DataTile<F>::K;
+    constexpr int S = S2DataTile<F>::S;
+    constexpr int NC = S + K - 1;   // dy columns of a strip
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int cp = static_cast<int>(tid % a.ncp);
+    long long rest = tid / a.ncp;
+    const int st = static_cast<int>(rest % a.nstrips);
+    rest /= a.nstrips;
+    const int ai = static_cast<int>(rest % a.na);
+    const long long n = rest / a.na;
+    if (n >= a.N) return;
+    const int c = 2 * cp;
+    const int cell_a = a.a_lo + ai;
+    const int b0 = a.b_lo + st * S;
+
+    // dy[a - k, b0 - (K - 1) + m] for m < NC; a row or column outside the map reads zero
+    V win[K][NC];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int oh = cell_a - k;
+        const bool rok = oh >= 0 && oh < a.OH;
+        const T* yrow = dy + ((n * a.OH + (rok ? oh : 0)) * a.OW) * a.C + c;
+#pragma unroll
+        for (int m = 0; m < NC; ++m) {
+            const int ow = b0 - (K - 1) + m;
+            win[k][m] = (rok && ow >= 0 && ow < a.OW) ? P::load(yrow + static_cast<size_t>(ow) * a.C)
+                                                      : P::zero();
+        }
+    }
+    V wr[F][F];
+#pragma unroll
+    for (int fh = 0; fh < F; ++fh)
+#pragma unroll
+        for (int fw = 0; fw < F; ++fw) wr[fh][fw] = P::load(w + (fh * F + fw) * a.C + c);
+
+    const int ih0 = 2 * cell_a - a.pad;
+    float* xrow0 = a.dx + ((n * a.H + ih0) * a.W) * a.C + c;
+    const bool row_ok[2] = {ih0 >= 0 && ih0 < a.H, ih0 + 1 >= 0 && ih0 + 1 < a.H};
+    // cell b0 + s: pixel (r, q) takes tap (r + 2k, q + 2j) from dy column b0 + s - j; cells
+    // past the row's last one have no pixel inside the map and store nothing
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        const int iw0 = 2 * (b0 + s) - a.pad;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                V acc = P::zero();
+#pragma unroll
+                for (int k = 0; k < K; ++k) {
+                    if (r + 2 * k >= F) continue;
+#pragma unroll
+                    for (int j = 0; j < K; ++j) {
+                        if (q + 2 * j >= F) continue;
+                        P::fma(acc, win[k][s - j + K - 1], wr[r + 2 * k][q + 2 * j]);
+                    }
+                }
+                const int iw = iw0 + q;
+                if (row_ok[r] && iw >= 0 && iw < a.W)
+                    store_pair_streaming(xrow0 + (static_cast<long long>(r) * a.W + iw) * a.C,
+                                         P::unpack(acc));
+            }
+        }
+    }
+}
+
+// The same cells for 7x7, streamed: the dy values sit in a circular register window of K
+// columns that advances by one column per cell (K loads per cell).  Holding a whole strip's
+// dy values next to the 49 taps would take ~190 registers and halve the resident warps,
+// which measured slower (7x7 on 64x56x56x144: 77.5 -> 85.8 us fp32, 90 -> 147 us bf16).
+template <typename T, int F>
+__global__ void __launch_bounds__(128, 3)
+s2_bwd_data_stream_kernel(const T* __restrict__ dy, const T* __restrict__ w, const S2DataArgs a) {
     using P = Pair64;
     using V = P::V;
     constexpr int K = (F + 1) / 2;
@@ -128,16 +213,21 @@ cudaError_t launch_s2_bwd_data_inst(const GeneralConv& p) {
     a.na = ((p.H - 1 + p.pad) >> 1) - a.a_lo + 1;
     a.b_lo = p.pad >> 1;
     a.nb = ((p.W - 1 + p.pad) >> 1) - a.b_lo + 1;
+    // whole-strip kernel: S cells per strip; streamed 7x7 kernel: about eight cells, a
+    // multiple of its window period K
     constexpr int K = (F + 1) / 2;
-    // about eight cells per strip, a multiple of the window period
-    a.strip = (8 + K - 1) / K * K;
+    a.strip = F == 7 ? (8 + K - 1) / K * K : S2DataTile<F>::S;
     a.nstrips = (a.nb + a.strip - 1) / a.strip;
     const long long threads = static_cast<long long>(p.N) * a.na * a.nstrips * a.ncp;
     if (threads == 0) return cudaSuccess;
     const long long blocks = (threads + 127) / 128;
     if (blocks > 0x7fffffffLL) return cudaErrorNotSupported;
-    s2_bwd_data_kernel<T, F><<<static_cast<unsigned>(blocks), 128, 0, p.stream>>>(
-        static_cast<const T*>(p.a), static_cast<const T*>(p.b), a);
+    if constexpr (F == 7)
+        s2_bwd_data_stream_kernel<T, F><<<static_cast<unsigned>(blocks), 128, 0, p.stream>>>(
+            static_cast<const T*>(p.a), static_cast<const T*>(p.b), a);
+    else
+        s2_bwd_data_kernel<T, F><<<static_cast<unsigned>(blocks), 128, 0, p.stream>>>(
+            static_cast<const T*>(p.a), static_cast<const T*>(p.b), a);
     return cudaGetLastError();
 }
 
