@@ -31,7 +31,7 @@ STATUS = {0: "DWC_OK", 1: "DWC_ERR_INVALID_ARG", 2: "DWC_ERR_UNSUPPORTED",
           6: "DWC_ERR_TIMEOUT"}
 
 # Every symbol include/dwc.h declares (checked by the tests).
-EXPORTS = ("dwc_fwd", "dwc_fwd_bn_act", "dwc_bwd_data", "dwc_bwd_filter_workspace_size", "dwc_bwd_filter",
+EXPORTS = ("dwc_fwd", "dwc_fwd_ex", "dwc_fwd_bn_act", "dwc_bwd_data", "dwc_bwd_data_ex", "dwc_bwd_filter_workspace_size", "dwc_bwd_filter",
            "dwc_bwd_filter_noalloc", "dwc_device_status", "dwc_status_string", "dwc_version",
            "dwc_path")
 
@@ -69,6 +69,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.dwc_fwd.restype = i
         lib.dwc_fwd_bn_act.argtypes = [vp, vp, vp, vp, vp, ctypes.c_float, i, vp, vp] + shape + [i, vp]
         lib.dwc_fwd_bn_act.restype = i
+        lib.dwc_fwd_ex.argtypes = [vp, vp, vp] + shape + [i, i, vp]
+        lib.dwc_fwd_ex.restype = i
+        lib.dwc_bwd_data_ex.argtypes = [vp, vp, vp] + shape + [i, i, vp]
+        lib.dwc_bwd_data_ex.restype = i
         lib.dwc_bwd_data.argtypes = [vp, vp, vp] + shape + [i, vp]
         lib.dwc_bwd_data.restype = i
         lib.dwc_bwd_filter_workspace_size.argtypes = shape + [i]
@@ -130,19 +134,25 @@ def _call(fn: str, *args):
         raise DwcError(fn, code)
 
 
-def fwd(x, w, stride: int = 1, pad: int = 0, out=None, stream=None):
-    """Y[n,oh,ow,c] = sum_{fh,fw} X[n,oh*s+fh-p,ow*s+fw-p,c] * W[fh,fw,c]  (fp32 output)."""
+def fwd(x, w, stride: int = 1, pad: int = 0, out=None, stream=None, out_dtype=None):
+    """Y[n,oh,ow,c] = sum_{fh,fw} X[n,oh*s+fh-p,ow*s+fw-p,c] * W[fh,fw,c].  Output fp32, or
+    out_dtype = the 16-bit input's own dtype (fp32 result rounded once at the store)."""
     torch = _torch()
     _check_cuda(x, w)
     N, H, W, C = x.shape
     FH, FW, C2 = w.shape
     if C2 != C or w.dtype != x.dtype:
         raise ValueError("filter must be FH x FW x C with the input's dtype")
+    od = torch.float32 if out_dtype is None else out_dtype
     OH, OW = out_dim(H, FH, stride, pad), out_dim(W, FW, stride, pad)
     if out is None:
-        out = torch.empty((N, max(OH, 0), max(OW, 0), C), device=x.device, dtype=torch.float32)
-    _call("dwc_fwd", x.data_ptr(), w.data_ptr(), out.data_ptr(), N, H, W, C, FH, FW, stride, pad,
-          _dtype_code(x), _stream_ptr(stream))
+        out = torch.empty((N, max(OH, 0), max(OW, 0), C), device=x.device, dtype=od)
+    if od == torch.float32:
+        _call("dwc_fwd", x.data_ptr(), w.data_ptr(), out.data_ptr(), N, H, W, C, FH, FW, stride,
+              pad, _dtype_code(x), _stream_ptr(stream))
+    else:
+        _call("dwc_fwd_ex", x.data_ptr(), w.data_ptr(), out.data_ptr(), N, H, W, C, FH, FW, stride,
+              pad, _dtype_code(x), _dtype_code(torch.empty(0, dtype=od)), _stream_ptr(stream))
     return out
 
 
@@ -169,8 +179,9 @@ def fwd_bn_act(x, w, mean, var, gamma, beta, eps: float = 1e-5, act: str = "relu
     return out
 
 
-def bwd_data(dy, w, in_hw, stride: int = 1, pad: int = 0, out=None, stream=None):
-    """dX = adjoint of ``fwd`` in X for a forward input of spatial size in_hw (fp32 output)."""
+def bwd_data(dy, w, in_hw, stride: int = 1, pad: int = 0, out=None, stream=None, out_dtype=None):
+    """dX = adjoint of ``fwd`` in X for a forward input of spatial size in_hw.  Output fp32, or
+    out_dtype = the 16-bit input's own dtype."""
     torch = _torch()
     _check_cuda(dy, w)
     N, OH, OW, C = dy.shape
@@ -178,10 +189,16 @@ def bwd_data(dy, w, in_hw, stride: int = 1, pad: int = 0, out=None, stream=None)
     H, W = (int(v) for v in in_hw)
     if (out_dim(H, FH, stride, pad), out_dim(W, FW, stride, pad)) != (OH, OW):
         raise ValueError("dy spatial size does not match the forward output of in_hw")
+    od = torch.float32 if out_dtype is None else out_dtype
     if out is None:
-        out = torch.empty((N, H, W, C), device=dy.device, dtype=torch.float32)
-    _call("dwc_bwd_data", dy.data_ptr(), w.data_ptr(), out.data_ptr(), N, H, W, C, FH, FW,
-          stride, pad, _dtype_code(dy), _stream_ptr(stream))
+        out = torch.empty((N, H, W, C), device=dy.device, dtype=od)
+    if od == torch.float32:
+        _call("dwc_bwd_data", dy.data_ptr(), w.data_ptr(), out.data_ptr(), N, H, W, C, FH, FW,
+              stride, pad, _dtype_code(dy), _stream_ptr(stream))
+    else:
+        _call("dwc_bwd_data_ex", dy.data_ptr(), w.data_ptr(), out.data_ptr(), N, H, W, C, FH, FW,
+              stride, pad, _dtype_code(dy), _dtype_code(torch.empty(0, dtype=od)),
+              _stream_ptr(stream))
     return out
 
 

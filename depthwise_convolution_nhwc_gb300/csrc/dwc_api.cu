@@ -133,12 +133,18 @@ dwc_status_t check_problem(int N, int H, int W, int C, int FH, int FW, int strid
 }
 
 dwc_status_t check_pointers(const Problem& P, const void* a, long long a_elems, const void* b,
-                            long long b_elems, const void* out, long long out_elems) {
+                            long long b_elems, const void* out, long long out_elems,
+                            int out_bytes = 4) {
     if ((a_elems > 0 && a == nullptr) || (b_elems > 0 && b == nullptr) ||
         (out_elems > 0 && out == nullptr))
         return DWC_ERR_INVALID_ARG;
-    if (!aligned(a, P.e) || !aligned(b, P.e) || !aligned(out, 4)) return DWC_ERR_ALIGNMENT;
+    if (!aligned(a, P.e) || !aligned(b, P.e) || !aligned(out, out_bytes)) return DWC_ERR_ALIGNMENT;
     return DWC_OK;
+}
+
+// Output type of a forward / backward-data call: fp32, or the input's own 16-bit type.
+bool valid_out_dtype(dwc_dtype_t dtype, dwc_dtype_t out_dtype) {
+    return out_dtype == DWC_F32 || (out_dtype == dtype && dtype != DWC_F32);
 }
 
 bool fast_eligible(const Problem& P, const void* a, const void* b, const void* out) {
@@ -241,28 +247,29 @@ size_t fast_fgrad_floats(const Problem& P) {
                     small_fgrad_floats(P));
 }
 
-}  // namespace
-
-extern "C" {
-
-dwc_status_t dwc_fwd(const void* x, const void* w, float* y, int N, int H, int W, int C, int FH,
-                     int FW, int stride, int pad, dwc_dtype_t dtype, dwc_stream_t stream) {
+dwc_status_t fwd_impl(const void* x, const void* w, void* y, int N, int H, int W, int C, int FH,
+                      int FW, int stride, int pad, dwc_dtype_t dtype, dwc_dtype_t out_dtype,
+                      dwc_stream_t stream) {
     Problem P;
     dwc_status_t st = check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P);
     if (st != DWC_OK) return st;
+    if (!valid_out_dtype(dtype, out_dtype)) return DWC_ERR_INVALID_ARG;
+    const int od = static_cast<int>(out_dtype);
     const long long nx = static_cast<long long>(N) * H * W * C;
     const long long ny = static_cast<long long>(N) * P.OH * P.OW * C;
-    st = check_pointers(P, x, nx, w, static_cast<long long>(FH) * FW * C, y, ny);
+    st = check_pointers(P, x, nx, w, static_cast<long long>(FH) * FW * C, y, ny, elem_bytes(od));
     if (st != DWC_OK) return st;
     if (ny == 0) return DWC_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (fast_eligible(P, x, w, y)) {
         RowConv rc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype, s, status_word()};
+        rc.out_dtype = od;
         const cudaError_t err = launch_rows(rc);
         if (err != cudaErrorNotSupported) return map_cuda(err);
         (void)cudaGetLastError();
     } else if (fast_s2_eligible(P, x, w, y)) {
         RowConv rc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype, s, status_word()};
+        rc.out_dtype = od;
         cudaError_t err;
         switch (rc.dtype) {
             case kF32: err = launch_rows_s2_f32(rc); break;
@@ -273,7 +280,63 @@ dwc_status_t dwc_fwd(const void* x, const void* w, float* y, int N, int H, int W
         (void)cudaGetLastError();
     }
     GeneralConv gc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, stride, pad, P.dtype, nullptr, 0, s};
+    gc.out_dtype = od;
     return map_cuda(launch_general_fwd(gc));
+}
+
+dwc_status_t bwd_data_impl(const void* dy, const void* w, void* dx, int N, int H, int W, int C,
+                           int FH, int FW, int stride, int pad, dwc_dtype_t dtype,
+                           dwc_dtype_t out_dtype, dwc_stream_t stream) {
+    Problem P;
+    dwc_status_t st = check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P);
+    if (st != DWC_OK) return st;
+    if (!valid_out_dtype(dtype, out_dtype)) return DWC_ERR_INVALID_ARG;
+    const int od = static_cast<int>(out_dtype);
+    const long long ndy = static_cast<long long>(N) * P.OH * P.OW * C;
+    const long long ndx = static_cast<long long>(N) * H * W * C;
+    st = check_pointers(P, dy, ndy, w, static_cast<long long>(FH) * FW * C, dx, ndx, elem_bytes(od));
+    if (st != DWC_OK) return st;
+    if (ndx == 0) return DWC_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (fast_eligible(P, dy, w, dx)) {
+        // stride 1: forward pass over dy with the filter rotated by 180 degrees and the
+        // complementary padding FH-1-pad (rows) / FW-1-pad (columns); output is H x W.
+        RowConv rc{dy, w, dx, N, P.OH, P.OW, C, H, W, FH, FW, FH - 1 - pad, FW - 1 - pad, true,
+                   P.dtype, s, status_word()};
+        rc.out_dtype = od;
+        const cudaError_t err = launch_rows(rc);
+        if (err != cudaErrorNotSupported) return map_cuda(err);
+        (void)cudaGetLastError();
+    }
+    GeneralConv gc{dy, w, dx, N, H, W, C, P.OH, P.OW, FH, FW, stride, pad, P.dtype, nullptr, 0, s};
+    gc.out_dtype = od;
+    if (fast_s2_eligible(P, dy, w, dx)) {
+        const cudaError_t err = launch_s2_bwd_data(gc);
+        if (err != cudaErrorNotSupported) return map_cuda(err);
+        (void)cudaGetLastError();
+    }
+    return map_cuda(launch_general_bwd_data(gc));
+}
+
+}  // namespace
+
+extern "C" {
+
+dwc_status_t dwc_fwd(const void* x, const void* w, float* y, int N, int H, int W, int C, int FH,
+                     int FW, int stride, int pad, dwc_dtype_t dtype, dwc_stream_t stream) {
+    return fwd_impl(x, w, y, N, H, W, C, FH, FW, stride, pad, dtype, DWC_F32, stream);
+}
+
+dwc_status_t dwc_fwd_ex(const void* x, const void* w, void* y, int N, int H, int W, int C, int FH,
+                        int FW, int stride, int pad, dwc_dtype_t dtype, dwc_dtype_t out_dtype,
+                        dwc_stream_t stream) {
+    return fwd_impl(x, w, y, N, H, W, C, FH, FW, stride, pad, dtype, out_dtype, stream);
+}
+
+dwc_status_t dwc_bwd_data_ex(const void* dy, const void* w, void* dx, int N, int H, int W, int C,
+                             int FH, int FW, int stride, int pad, dwc_dtype_t dtype,
+                             dwc_dtype_t out_dtype, dwc_stream_t stream) {
+    return bwd_data_impl(dy, w, dx, N, H, W, C, FH, FW, stride, pad, dtype, out_dtype, stream);
 }
 
 dwc_status_t dwc_fwd_bn_act(const void* x, const float* mean, const float* var,
@@ -311,31 +374,7 @@ dwc_status_t dwc_fwd_bn_act(const void* x, const float* mean, const float* var,
 dwc_status_t dwc_bwd_data(const void* dy, const void* w, float* dx, int N, int H, int W, int C,
                           int FH, int FW, int stride, int pad, dwc_dtype_t dtype,
                           dwc_stream_t stream) {
-    Problem P;
-    dwc_status_t st = check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P);
-    if (st != DWC_OK) return st;
-    const long long ndy = static_cast<long long>(N) * P.OH * P.OW * C;
-    const long long ndx = static_cast<long long>(N) * H * W * C;
-    st = check_pointers(P, dy, ndy, w, static_cast<long long>(FH) * FW * C, dx, ndx);
-    if (st != DWC_OK) return st;
-    if (ndx == 0) return DWC_OK;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (fast_eligible(P, dy, w, dx)) {
-        // stride 1: forward pass over dy with the filter rotated by 180 degrees and the
-        // complementary padding FH-1-pad (rows) / FW-1-pad (columns); output is H x W.
-        RowConv rc{dy, w, dx, N, P.OH, P.OW, C, H, W, FH, FW, FH - 1 - pad, FW - 1 - pad, true,
-                   P.dtype, s, status_word()};
-        const cudaError_t err = launch_rows(rc);
-        if (err != cudaErrorNotSupported) return map_cuda(err);
-        (void)cudaGetLastError();
-    }
-    GeneralConv gc{dy, w, dx, N, H, W, C, P.OH, P.OW, FH, FW, stride, pad, P.dtype, nullptr, 0, s};
-    if (fast_s2_eligible(P, dy, w, dx)) {
-        const cudaError_t err = launch_s2_bwd_data(gc);
-        if (err != cudaErrorNotSupported) return map_cuda(err);
-        (void)cudaGetLastError();
-    }
-    return map_cuda(launch_general_bwd_data(gc));
+    return bwd_data_impl(dy, w, dx, N, H, W, C, FH, FW, stride, pad, dtype, DWC_F32, stream);
 }
 
 size_t dwc_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int FW, int stride,

@@ -230,6 +230,22 @@ __device__ __forceinline__ void store_pair_streaming(float* p, float2 v) {
     __stcs(reinterpret_cast<float2*>(p), v);
 }
 
+// Streaming store of an fp32 pair as the output type: fp32 as is, bf16 / fp16 rounded to
+// nearest even (the fp32 accumulators round once, at the store).
+__device__ __forceinline__ void store_out_pair(float* p, float2 v) { store_pair_streaming(p, v); }
+__device__ __forceinline__ void store_out_pair(__nv_bfloat16* p, float2 v) {
+    const __nv_bfloat162 h = __float22bfloat162_rn(v);
+    __stcs(reinterpret_cast<unsigned int*>(p), *reinterpret_cast<const unsigned int*>(&h));
+}
+__device__ __forceinline__ void store_out_pair(__half* p, float2 v) {
+    const __half2 h = __float22half2_rn(v);
+    __stcs(reinterpret_cast<unsigned int*>(p), *reinterpret_cast<const unsigned int*>(&h));
+}
+// one value, for the general kernels
+__device__ __forceinline__ void store_out(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void store_out(__half* p, float v) { *p = __float2half_rn(v); }
+
 
 // ------------------------------------------------------------------ host-side occupancy
 

@@ -13,9 +13,9 @@
 
 namespace dwc {
 
-template <typename T>
+template <typename T, class OutT>
 __global__ void general_fwd_kernel(const T* __restrict__ x, const T* __restrict__ w,
-                                   float* __restrict__ y, int N, int H, int W, int C, int OH,
+                                   OutT* __restrict__ y, int N, int H, int W, int C, int OH,
                                    int OW, int FH, int FW, int s, int p) {
     const long long total = static_cast<long long>(N) * OH * OW * C;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -37,7 +37,7 @@ __global__ void general_fwd_kernel(const T* __restrict__ x, const T* __restrict_
                            to_f32(w[(static_cast<size_t>(fh) * FW + fw) * C + c]), acc);
             }
         }
-        y[i] = acc;
+        store_out(y + i, acc);
     }
 }
 
@@ -81,9 +81,9 @@ __global__ void general_fwd_bnact_kernel(const T* __restrict__ x, const T* __res
 }
 
 // dx[n, ih, iw, c] = sum over taps whose forward product read x[n, ih, iw, c].
-template <typename T>
+template <typename T, class OutT>
 __global__ void general_bwd_data_kernel(const T* __restrict__ dy, const T* __restrict__ w,
-                                        float* __restrict__ dx, int N, int H, int W, int C,
+                                        OutT* __restrict__ dx, int N, int H, int W, int C,
                                         int OH, int OW, int FH, int FW, int s, int p) {
     const long long total = static_cast<long long>(N) * H * W * C;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -109,7 +109,7 @@ __global__ void general_bwd_data_kernel(const T* __restrict__ dy, const T* __res
                            to_f32(w[(static_cast<size_t>(fh) * FW + fw) * C + c]), acc);
             }
         }
-        dx[i] = acc;
+        store_out(dx + i, acc);
     }
 }
 
@@ -200,14 +200,19 @@ static cudaError_t general_fwd_t(const GeneralConv& p) {
     if (total == 0) return cudaSuccess;
     if (p.act >= 0) {
         general_fwd_bnact_kernel<T><<<grid_for(total, 256), 256, 0, p.stream>>>(
-            static_cast<const T*>(p.a), static_cast<const T*>(p.b), p.out, p.N, p.H, p.W, p.C,
+            static_cast<const T*>(p.a), static_cast<const T*>(p.b), static_cast<float*>(p.out), p.N, p.H, p.W, p.C,
             p.OH, p.OW, p.FH, p.FW, p.stride, p.pad, p.bn_mean, p.bn_var, p.bn_gamma, p.bn_beta,
             p.bn_eps, p.act);
         return cudaGetLastError();
     }
-    general_fwd_kernel<T><<<grid_for(total, 256), 256, 0, p.stream>>>(
-        static_cast<const T*>(p.a), static_cast<const T*>(p.b), p.out, p.N, p.H, p.W, p.C, p.OH,
-        p.OW, p.FH, p.FW, p.stride, p.pad);
+    if (p.out_dtype != kF32)
+        general_fwd_kernel<T, T><<<grid_for(total, 256), 256, 0, p.stream>>>(
+            static_cast<const T*>(p.a), static_cast<const T*>(p.b), static_cast<T*>(p.out), p.N, p.H,
+            p.W, p.C, p.OH, p.OW, p.FH, p.FW, p.stride, p.pad);
+    else
+        general_fwd_kernel<T, float><<<grid_for(total, 256), 256, 0, p.stream>>>(
+            static_cast<const T*>(p.a), static_cast<const T*>(p.b), static_cast<float*>(p.out), p.N,
+            p.H, p.W, p.C, p.OH, p.OW, p.FH, p.FW, p.stride, p.pad);
     return cudaGetLastError();
 }
 
@@ -215,9 +220,14 @@ template <typename T>
 static cudaError_t general_bwd_data_t(const GeneralConv& p) {
     const long long total = static_cast<long long>(p.N) * p.H * p.W * p.C;
     if (total == 0) return cudaSuccess;
-    general_bwd_data_kernel<T><<<grid_for(total, 256), 256, 0, p.stream>>>(
-        static_cast<const T*>(p.a), static_cast<const T*>(p.b), p.out, p.N, p.H, p.W, p.C, p.OH,
-        p.OW, p.FH, p.FW, p.stride, p.pad);
+    if (p.out_dtype != kF32)
+        general_bwd_data_kernel<T, T><<<grid_for(total, 256), 256, 0, p.stream>>>(
+            static_cast<const T*>(p.a), static_cast<const T*>(p.b), static_cast<T*>(p.out), p.N, p.H,
+            p.W, p.C, p.OH, p.OW, p.FH, p.FW, p.stride, p.pad);
+    else
+        general_bwd_data_kernel<T, float><<<grid_for(total, 256), 256, 0, p.stream>>>(
+            static_cast<const T*>(p.a), static_cast<const T*>(p.b), static_cast<float*>(p.out), p.N,
+            p.H, p.W, p.C, p.OH, p.OW, p.FH, p.FW, p.stride, p.pad);
     return cudaGetLastError();
 }
 
@@ -239,7 +249,8 @@ static cudaError_t general_bwd_filter_t(const GeneralConv& p) {
     const size_t count = static_cast<size_t>(p.FH) * p.FW * p.C;
     if (count == 0) return cudaSuccess;
     const long long rows = static_cast<long long>(p.N) * p.OH;
-    if (rows == 0 || p.OW == 0) return cudaMemsetAsync(p.out, 0, count * sizeof(float), p.stream);
+    float* dw = static_cast<float*>(p.out);
+    if (rows == 0 || p.OW == 0) return cudaMemsetAsync(dw, 0, count * sizeof(float), p.stream);
     int Z = general_slices(p.N, p.OH, p.C, p.FH, p.FW);
     const int rps = static_cast<int>((rows + Z - 1) / Z);
     Z = static_cast<int>((rows + rps - 1) / rps);
@@ -250,7 +261,7 @@ static cudaError_t general_bwd_filter_t(const GeneralConv& p) {
         p.OH, p.OW, p.FH, p.FW, p.stride, p.pad, rps, Z);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    return launch_reduce_slices(p.workspace, Z, count, p.out, p.stream);
+    return launch_reduce_slices(p.workspace, Z, count, dw, p.stream);
 }
 
 #define DWC_BY_DTYPE(fn, p)                                         \

@@ -19,7 +19,7 @@ inline int elem_bytes(int t) { return t == kF32 ? 4 : 2; }
 struct RowConv {
     const void* in;
     const void* w;
-    float* out;
+    void* out;              // fp32, or the input's 16-bit type when out_dtype says so
     int N, H, W, C;
     int OH, OW;
     int FH, FW;
@@ -37,6 +37,7 @@ struct RowConv {
     const float* bn_beta = nullptr;
     float bn_eps = 0.f;
     int act = -1;
+    int out_dtype = kF32;   // kF32, or the input's type (kBF16 / kF16) for 16-bit outputs
 };
 
 // Filter-gradient problem: dw[fh, fw, c] = sum_{n,oh,ow} x[n, oh+fh-pad, ow+fw-pad, c] * dy[n,oh,ow,c].
@@ -59,7 +60,7 @@ struct FilterGrad {
 struct GeneralConv {
     const void* a;     // x (fwd, bwd_filter) or dy (bwd_data)
     const void* b;     // w (fwd, bwd_data) or dy (bwd_filter)
-    float* out;
+    void* out;         // fp32 (always for the filter gradient), or 16-bit per out_dtype
     int N, H, W, C;    // forward input dims
     int OH, OW;
     int FH, FW;
@@ -75,6 +76,7 @@ struct GeneralConv {
     const float* bn_beta = nullptr;
     float bn_eps = 0.f;
     int act = -1;
+    int out_dtype = kF32;
 };
 
 // Device properties cached per device.
@@ -105,6 +107,17 @@ cudaError_t launch_rows_s2_f16(const RowConv& p);
 cudaError_t launch_rows_bnact_f32(const RowConv& p, int stride);
 cudaError_t launch_rows_bnact_bf16(const RowConv& p, int stride);
 cudaError_t launch_rows_bnact_f16(const RowConv& p, int stride);
+
+// The same launches writing 16-bit outputs of the input's type (RowConv / GeneralConv with
+// out_dtype kBF16 or kF16); the entry points above route there themselves.
+cudaError_t launch_rows_o16_bf16(const RowConv& p);
+cudaError_t launch_rows_o16_f16(const RowConv& p);
+cudaError_t launch_rows_s2_o16_bf16(const RowConv& p);
+cudaError_t launch_rows_s2_o16_f16(const RowConv& p);
+cudaError_t launch_small_rows_o16_bf16(const RowConv& p);
+cudaError_t launch_small_rows_o16_f16(const RowConv& p);
+cudaError_t launch_s2_bwd_data_o16_bf16(const GeneralConv& p);
+cudaError_t launch_s2_bwd_data_o16_f16(const GeneralConv& p);
 
 // Stride-2 backward data (square filters of 3, 5 or 7 taps, C even, 8-byte aligned
 // tensors): a = dy, b = w, out = dx of the GeneralConv.

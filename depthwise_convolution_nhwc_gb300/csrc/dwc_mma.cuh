@@ -27,6 +27,8 @@
 // Backward data uses the same kernel with the filter read rotated by 180 degrees.
 #pragma once
 
+#include <type_traits>
+
 #include <algorithm>
 
 #include "dwc_rows.cuh"
@@ -41,7 +43,7 @@ constexpr int kMmaMaxKC = 4;    // K <= 64, i.e. FW <= 57
 struct MmaArgs {
     const void* x;
     const void* w;
-    float* y;
+    void* y;            // OutT elements
     int N, H, W, C, OH, OW, FH, FW, pad_h, pad_w;
     int G;       // groups of 8 output columns per row
     int RB;      // output rows per band
@@ -86,7 +88,7 @@ __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
                  : "memory");
 }
 
-template <typename T, bool FLIP>
+template <typename T, bool FLIP, class OutT = float>
 __global__ void __launch_bounds__(kMmaWarps * 32, 2) mma_rows_kernel(const MmaArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint16_t* xb = reinterpret_cast<uint16_t*>(smem);                 // [8][XR][XC]
@@ -266,8 +268,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 2) mma_rows_kernel(const MmaAr
             const int px = i >> 1, half = i & 1;
             const int r = px / a.OW, ow = px - r * a.OW;
             const float4 v = *reinterpret_cast<const float4*>(ob + static_cast<size_t>(px) * kMmaCB + 4 * half);
-            float* dst = a.y + ((static_cast<size_t>(n) * a.OH + oh0 + r) * a.OW + ow) * a.C + c0 + 4 * half;
-            __stcs(reinterpret_cast<float4*>(dst), v);
+            OutT* dst = static_cast<OutT*>(a.y) + ((static_cast<size_t>(n) * a.OH + oh0 + r) * a.OW + ow) * a.C + c0 + 4 * half;
+            if constexpr (std::is_same<OutT, float>::value) {
+                __stcs(reinterpret_cast<float4*>(dst), v);
+            } else {
+                store_out_pair(dst, make_float2(v.x, v.y));
+                store_out_pair(dst + 2, make_float2(v.z, v.w));
+            }
         }
         __syncthreads();  // the block is overwritten by the next unit's loads
     }
@@ -303,7 +310,7 @@ inline bool mma_plan(const RowConv& p, MmaArgs& a, size_t& smem) {
     return true;
 }
 
-template <typename T, bool FLIP>
+template <typename T, bool FLIP, class OutT = float>
 cudaError_t launch_mma_inst(const RowConv& p) {
     MmaArgs a;
     size_t smem = 0;
@@ -312,7 +319,7 @@ cudaError_t launch_mma_inst(const RowConv& p) {
     a.N = p.N; a.H = p.H; a.W = p.W; a.C = p.C; a.OH = p.OH; a.OW = p.OW;
     a.FH = p.FH; a.FW = p.FW; a.pad_h = p.pad_h; a.pad_w = p.pad_w;
     if (a.units == 0) return cudaSuccess;
-    auto kern = mma_rows_kernel<T, FLIP>;
+    auto kern = mma_rows_kernel<T, FLIP, OutT>;
     static bool attr = false;
     if (!attr) {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -337,13 +344,13 @@ inline bool mma_rows_wanted(const RowConv& p) {
     return p.FW >= kMmaMinFilter && p.OW >= kMmaMinWidth;
 }
 
-template <typename T>
+template <typename T, class OutT = float>
 cudaError_t launch_rows_or_mma(const RowConv& p) {
     if (mma_rows_wanted(p)) {
-        const cudaError_t err = p.flip ? launch_mma_inst<T, true>(p) : launch_mma_inst<T, false>(p);
+        const cudaError_t err = p.flip ? launch_mma_inst<T, true, OutT>(p) : launch_mma_inst<T, false, OutT>(p);
         if (err != cudaErrorNotSupported) return err;
     }
-    return launch_rows_dispatch<T>(p);
+    return launch_rows_dispatch<T, OutT>(p);
 }
 
 }  // namespace dwc

@@ -56,7 +56,7 @@ struct RowsTile {
 };
 
 struct RowsArgs {
-    float* out;
+    void* out;            // OutT elements
     unsigned int* status;
     int H, W;             // input rows / columns (rows and columns that lie in the padding)
     int OH, OW, C;
@@ -169,9 +169,10 @@ __device__ __forceinline__ void consume_rows(const T* __restrict__ xs, typename 
 }
 
 // SD: stride of both spatial axes (1, or 2 with one output row per band).  ACT: -1 plain
-// DWC, else BN + Act fused in front (0 identity, 1 ReLU, 2 ReLU6; forward only).
+// DWC, else BN + Act fused in front (0 identity, 1 ReLU, 2 ReLU6; forward only).  OutT:
+// output element type (fp32, or the 16-bit input type).
 template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64, int SD = 1,
-          int ACT = -1>
+          int ACT = -1, class OutT = float>
 __global__ void __launch_bounds__(kRowsMaxThreads, MINB)
 rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
             const RowsArgs a) {
@@ -409,16 +410,16 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             for (int r = 0; r < R; ++r) {
                 const int oh = oh0 + r;
                 if (oh >= a.OH) break;
-                float* row = a.out + ((static_cast<size_t>(n) * a.OH + oh) * a.OW + owl) * a.C + c;
+                OutT* row = static_cast<OutT*>(a.out) + ((static_cast<size_t>(n) * a.OH + oh) * a.OW + owl) * a.C + c;
                 if (owl + TM <= a.OW) {
 #pragma unroll
                     for (int t = 0; t < TM; ++t)
-                        store_pair_streaming(row + static_cast<size_t>(t) * a.C, P::unpack(acc[r][t]));
+                        store_out_pair(row + static_cast<size_t>(t) * a.C, P::unpack(acc[r][t]));
                 } else {
 #pragma unroll
                     for (int t = 0; t < TM; ++t)
                         if (owl + t < a.OW)
-                            store_pair_streaming(row + static_cast<size_t>(t) * a.C, P::unpack(acc[r][t]));
+                            store_out_pair(row + static_cast<size_t>(t) * a.C, P::unpack(acc[r][t]));
                 }
             }
         }
@@ -426,7 +427,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
 }
 
 template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64, int SD = 1,
-          int ACT = -1>
+          int ACT = -1, class OutT = float>
 cudaError_t launch_rows_inst(const RowConv& p) {
     const int e = static_cast<int>(sizeof(T));
     const DeviceInfo& dev = device_info();
@@ -490,7 +491,7 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     a.stage_stride = (a.x_bytes + a.w_bytes + 127u) & ~127u;
     if (a.units == 0) return cudaSuccess;
 
-    auto kern = rows_kernel<T, FH, FW, R, TM, MINB, FLIP, P, SD, ACT>;
+    auto kern = rows_kernel<T, FH, FW, R, TM, MINB, FLIP, P, SD, ACT, OutT>;
     const int threads = (nwc + 1) * 32;
     static int regs = -1;  // per instantiation
     if (regs < 0) {
@@ -520,15 +521,15 @@ cudaError_t launch_rows_inst(const RowConv& p) {
 }
 
 // Dispatch over the compiled odd square filter sizes.
-template <typename T>
+template <typename T, class OutT = float>
 cudaError_t launch_rows_dispatch(const RowConv& p) {
     if (p.FH != p.FW) return cudaErrorNotSupported;
 #define DWC_ROWS_CASE(F)                                                                     \
     case F:                                                                                  \
         return p.flip ? launch_rows_inst<T, F, F, RowsTile<F, F>::R, RowsTile<F, F>::TM,      \
-                                         RowsTile<F, F>::MINB, true>(p)                      \
+                                         RowsTile<F, F>::MINB, true, Pair64, 1, -1, OutT>(p) \
                       : launch_rows_inst<T, F, F, RowsTile<F, F>::R, RowsTile<F, F>::TM,      \
-                                         RowsTile<F, F>::MINB, false>(p);
+                                         RowsTile<F, F>::MINB, false, Pair64, 1, -1, OutT>(p);
     switch (p.FH) {
         DWC_ROWS_CASE(3)
         DWC_ROWS_CASE(5)
@@ -563,13 +564,13 @@ cudaError_t launch_rows_dispatch(const RowConv& p) {
 
 // Stride-2 forward: one output row per band, 8 outputs per lane (filters of 3, 5 and 7 taps,
 // the down-sampling layers of mobile networks).
-template <typename T>
+template <typename T, class OutT = float>
 cudaError_t launch_rows_s2_dispatch(const RowConv& p) {
     if (p.FH != p.FW || p.flip) return cudaErrorNotSupported;
     switch (p.FH) {
-        case 3: return launch_rows_inst<T, 3, 3, 1, 8, 3, false, Pair64, 2>(p);
-        case 5: return launch_rows_inst<T, 5, 5, 1, 8, 3, false, Pair64, 2>(p);
-        case 7: return launch_rows_inst<T, 7, 7, 1, 8, 3, false, Pair64, 2>(p);
+        case 3: return launch_rows_inst<T, 3, 3, 1, 8, 3, false, Pair64, 2, -1, OutT>(p);
+        case 5: return launch_rows_inst<T, 5, 5, 1, 8, 3, false, Pair64, 2, -1, OutT>(p);
+        case 7: return launch_rows_inst<T, 7, 7, 1, 8, 3, false, Pair64, 2, -1, OutT>(p);
         default: return cudaErrorNotSupported;
     }
 }

@@ -25,7 +25,7 @@
 namespace dwc {
 
 struct S2DataArgs {
-    float* dx;
+    void* dx;           // OutT elements
     int N, H, W, C, OH, OW, pad;
     int ncp;            // channel pairs (C / 2)
     int na, a_lo;       // cell rows a_lo .. a_lo + na - 1
@@ -44,7 +44,7 @@ struct S2DataTile {
     static constexpr int S = 8;
 };
 
-template <typename T, int F>
+template <typename T, int F, class OutT = float>
 __global__ void __launch_bounds__(128, 4)
 s2_bwd_data_kernel(const T* __restrict__ dy, const T* __restrict__ w, const S2DataArgs a) {
     using P = Pair64;
@@ -85,7 +85,7 @@ s2_bwd_data_kernel(const T* __restrict__ dy, const T* __restrict__ w, const S2Da
         for (int fw = 0; fw < F; ++fw) wr[fh][fw] = P::load(w + (fh * F + fw) * a.C + c);
 
     const int ih0 = 2 * cell_a - a.pad;
-    float* xrow0 = a.dx + ((n * a.H + ih0) * a.W) * a.C + c;
+    OutT* xrow0 = static_cast<OutT*>(a.dx) + ((n * a.H + ih0) * a.W) * a.C + c;
     const bool row_ok[2] = {ih0 >= 0 && ih0 < a.H, ih0 + 1 >= 0 && ih0 + 1 < a.H};
     // cell b0 + s: pixel (r, q) takes tap (r + 2k, q + 2j) from dy column b0 + s - j; cells
     // past the row's last one have no pixel inside the map and store nothing
@@ -108,7 +108,7 @@ s2_bwd_data_kernel(const T* __restrict__ dy, const T* __restrict__ w, const S2Da
                 }
                 const int iw = iw0 + q;
                 if (row_ok[r] && iw >= 0 && iw < a.W)
-                    store_pair_streaming(xrow0 + (static_cast<long long>(r) * a.W + iw) * a.C,
+                    store_out_pair(xrow0 + (static_cast<long long>(r) * a.W + iw) * a.C,
                                          P::unpack(acc));
             }
         }
@@ -119,7 +119,7 @@ s2_bwd_data_kernel(const T* __restrict__ dy, const T* __restrict__ w, const S2Da
 // columns that advances by one column per cell (K loads per cell).  Holding a whole strip's
 // dy values next to the 49 taps would take ~190 registers and halve the resident warps,
 // which measured slower (7x7 on 64x56x56x144: 77.5 -> 85.8 us fp32, 90 -> 147 us bf16).
-template <typename T, int F>
+template <typename T, int F, class OutT = float>
 __global__ void __launch_bounds__(128, 3)
 s2_bwd_data_stream_kernel(const T* __restrict__ dy, const T* __restrict__ w, const S2DataArgs a) {
     using P = Pair64;
@@ -166,7 +166,7 @@ s2_bwd_data_stream_kernel(const T* __restrict__ dy, const T* __restrict__ w, con
         for (int k = 0; k < K; ++k) win[k][K - j] = load_col(b0 - j, k);
 
     const int ih0 = 2 * cell_a - a.pad;
-    float* xrow0 = a.dx + ((n * a.H + ih0) * a.W) * a.C + c;
+    OutT* xrow0 = static_cast<OutT*>(a.dx) + ((n * a.H + ih0) * a.W) * a.C + c;
     const bool row_ok[2] = {ih0 >= 0 && ih0 < a.H, ih0 + 1 >= 0 && ih0 + 1 < a.H};
 
 #pragma unroll 1
@@ -194,7 +194,7 @@ s2_bwd_data_stream_kernel(const T* __restrict__ dy, const T* __restrict__ w, con
                     }
                     const int iw = iw0 + q;
                     if (row_ok[r] && iw >= 0 && iw < a.W)
-                        store_pair_streaming(xrow0 + (static_cast<long long>(r) * a.W + iw) * a.C,
+                        store_out_pair(xrow0 + (static_cast<long long>(r) * a.W + iw) * a.C,
                                              P::unpack(acc));
                 }
             }
@@ -202,7 +202,7 @@ s2_bwd_data_stream_kernel(const T* __restrict__ dy, const T* __restrict__ w, con
     }
 }
 
-template <typename T, int F>
+template <typename T, int F, class OutT = float>
 cudaError_t launch_s2_bwd_data_inst(const GeneralConv& p) {
     S2DataArgs a;
     a.dx = p.out;
@@ -223,21 +223,21 @@ cudaError_t launch_s2_bwd_data_inst(const GeneralConv& p) {
     const long long blocks = (threads + 127) / 128;
     if (blocks > 0x7fffffffLL) return cudaErrorNotSupported;
     if constexpr (F == 7)
-        s2_bwd_data_stream_kernel<T, F><<<static_cast<unsigned>(blocks), 128, 0, p.stream>>>(
+        s2_bwd_data_stream_kernel<T, F, OutT><<<static_cast<unsigned>(blocks), 128, 0, p.stream>>>(
             static_cast<const T*>(p.a), static_cast<const T*>(p.b), a);
     else
-        s2_bwd_data_kernel<T, F><<<static_cast<unsigned>(blocks), 128, 0, p.stream>>>(
+        s2_bwd_data_kernel<T, F, OutT><<<static_cast<unsigned>(blocks), 128, 0, p.stream>>>(
             static_cast<const T*>(p.a), static_cast<const T*>(p.b), a);
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, class OutT = float>
 cudaError_t launch_s2_bwd_data_dispatch(const GeneralConv& p) {
     if (p.FH != p.FW || p.stride != 2 || (p.C & 1)) return cudaErrorNotSupported;
     switch (p.FH) {
-        case 3: return launch_s2_bwd_data_inst<T, 3>(p);
-        case 5: return launch_s2_bwd_data_inst<T, 5>(p);
-        case 7: return launch_s2_bwd_data_inst<T, 7>(p);
+        case 3: return launch_s2_bwd_data_inst<T, 3, OutT>(p);
+        case 5: return launch_s2_bwd_data_inst<T, 5, OutT>(p);
+        case 7: return launch_s2_bwd_data_inst<T, 7, OutT>(p);
         default: return cudaErrorNotSupported;
     }
 }

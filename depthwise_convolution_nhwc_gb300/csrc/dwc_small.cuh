@@ -24,6 +24,8 @@
 // MAXW (8 or 16) bounds the map width; DR (3, 7, 11, 15) bounds the tap offsets.
 #pragma once
 
+#include <type_traits>
+
 #include <algorithm>
 
 #include "dwc_device.cuh"
@@ -95,7 +97,7 @@ __device__ __forceinline__ void stage_image(T* dst, const T* src_img, int rows, 
 struct SmallArgs {
     const void* in;
     const void* w;
-    float* out;
+    void* out;          // OutT elements
     int N, H, W, C, OH, OW, FH, FW, pad_h, pad_w;
     int flip;           // filter rotated by 180 degrees (backward data)
     int fh_lo, nfh;     // filter rows that meet the image for some output row
@@ -106,7 +108,7 @@ struct SmallArgs {
     uint32_t win_off;   // byte offset of the filter window
 };
 
-template <typename T, int MAXW, int DR>
+template <typename T, int MAXW, int DR, class OutT = float>
 __global__ void __launch_bounds__(kSmMaxWarps * 32, 1) small_rows_kernel(const SmallArgs a) {
     constexpr int NJ = 2 * DR + 1;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -202,11 +204,16 @@ __global__ void __launch_bounds__(kSmMaxWarps * 32, 1) small_rows_kernel(const S
                 }
             }
             if (lane_ok) {
-                float* o = a.out + (static_cast<size_t>(n) * a.OH + oh) * a.OW * a.C + c0 + lane;
+                OutT* o = static_cast<OutT*>(a.out) + (static_cast<size_t>(n) * a.OH + oh) * a.OW * a.C + c0 + lane;
 #pragma unroll
                 for (int k = 0; k < MAXW / 2; ++k) {
-                    if (2 * k < a.OW) __stcs(o + static_cast<size_t>(2 * k) * a.C, acc[k].x);
-                    if (2 * k + 1 < a.OW) __stcs(o + static_cast<size_t>(2 * k + 1) * a.C, acc[k].y);
+                    if constexpr (std::is_same<OutT, float>::value) {
+                        if (2 * k < a.OW) __stcs(o + static_cast<size_t>(2 * k) * a.C, acc[k].x);
+                        if (2 * k + 1 < a.OW) __stcs(o + static_cast<size_t>(2 * k + 1) * a.C, acc[k].y);
+                    } else {
+                        if (2 * k < a.OW) store_out(o + static_cast<size_t>(2 * k) * a.C, acc[k].x);
+                        if (2 * k + 1 < a.OW) store_out(o + static_cast<size_t>(2 * k + 1) * a.C, acc[k].y);
+                    }
                 }
             }
         }
@@ -391,7 +398,7 @@ inline void small_window_rows(int H, int OH, int FH, int pad_h, int& fh_lo, int&
     nfh = std::max(0, fh_hi - fh_lo + 1);
 }
 
-template <typename T, int MAXW, int DR>
+template <typename T, int MAXW, int DR, class OutT = float>
 cudaError_t launch_small_rows_inst(const RowConv& p) {
     constexpr int NJ = 2 * DR + 1;
     SmallArgs a;
@@ -420,7 +427,7 @@ cudaError_t launch_small_rows_inst(const RowConv& p) {
     const int pairs = G * p.OH;
     const int rounds = (pairs + kSmMaxWarps - 1) / kSmMaxWarps;
     const int nwarps = (pairs + rounds - 1) / rounds;
-    auto kern = small_rows_kernel<T, MAXW, DR>;
+    auto kern = small_rows_kernel<T, MAXW, DR, OutT>;
     // one CTA per SM: a CTA stages the filter window of each channel block it meets, so
     // fewer CTAs with more units each was faster on the stage shapes than two per SM
     const int per_sm = 1;
@@ -527,13 +534,13 @@ size_t small_fgrad_workspace_t(int N, int H, int W, int C, int OH, int OW, int F
 }
 
 
-template <typename T>
+template <typename T, class OutT = float>
 cudaError_t launch_small_rows_t(const RowConv& p) {
     int maxw = 0, dr = 0;
     if (!small_rows_wanted(p.W, p.OW, p.FW) || !small_shape(p.H, p.W, p.OH, p.OW, p.FW, p.pad_w, maxw, dr))
         return cudaErrorNotSupported;
 #define DWC_SMALL_ROWS_CASE(M, D) \
-    if (maxw == M && dr == D) return launch_small_rows_inst<T, M, D>(p);
+    if (maxw == M && dr == D) return launch_small_rows_inst<T, M, D, OutT>(p);
     DWC_SMALL_SHAPES(DWC_SMALL_ROWS_CASE)
 #undef DWC_SMALL_ROWS_CASE
     return cudaErrorNotSupported;

@@ -71,6 +71,22 @@ dwc_status_t dwc_fwd(const void* x, const void* w, float* y,
                      int N, int H, int W, int C, int FH, int FW, int stride, int pad,
                      dwc_dtype_t dtype, dwc_stream_t stream);
 
+/* Forward pass and backward data with a chosen output type.  Same operations, arguments and
+ * errors as dwc_fwd / dwc_bwd_data, plus:
+ *   out_dtype : DWC_F32, or the input's own 16-bit type (DWC_BF16 for bf16 inputs, DWC_F16 for
+ *               fp16 inputs).  A 16-bit output holds the fp32 result rounded to nearest even
+ *               once, at the store; it halves the output's HBM traffic.  Any other combination
+ *               (e.g. fp32 inputs with a 16-bit output) returns DWC_ERR_INVALID_ARG.
+ *   y, dx     : N x OH x OW x C / N x H x W x C elements of out_dtype, aligned to its size.
+ * (The paper keeps fp32 outputs; 16-bit outputs are an option of this library.  The filter
+ * gradient stays fp32: it is small and is an accumulation.) */
+dwc_status_t dwc_fwd_ex(const void* x, const void* w, void* y,
+                        int N, int H, int W, int C, int FH, int FW, int stride, int pad,
+                        dwc_dtype_t dtype, dwc_dtype_t out_dtype, dwc_stream_t stream);
+dwc_status_t dwc_bwd_data_ex(const void* dy, const void* w, void* dx,
+                             int N, int H, int W, int C, int FH, int FW, int stride, int pad,
+                             dwc_dtype_t dtype, dwc_dtype_t out_dtype, dwc_stream_t stream);
+
 /* Activation applied after the batch normalisation of dwc_fwd_bn_act. */
 typedef enum {
     DWC_ACT_NONE = 0,  /* identity */

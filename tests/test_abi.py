@@ -109,6 +109,18 @@ def test_fused_bn_act_path_selection(lib):
     assert p(C=8, dtype=1) == 1 and p(C=12, dtype=1) == 0
 
 
+def test_output_dtype_validated_on_host(lib):
+    a = dict(GOOD, C=16)
+    args = [a[k] for k in ("N", "H", "W", "C", "FH", "FW", "stride", "pad")]
+    for fn in (lib.dwc_fwd_ex, lib.dwc_bwd_data_ex):
+        assert fn(FAKE, FAKE, FAKE, *args, 0, 1, None) == 1      # fp32 inputs, bf16 output
+        assert fn(FAKE, FAKE, FAKE, *args, 1, 2, None) == 1      # bf16 inputs, fp16 output
+        assert fn(FAKE, FAKE, FAKE, *args, 2, 1, None) == 1
+        assert fn(FAKE, FAKE, FAKE, *args, 1, 7, None) == 1      # unknown output type
+        assert fn(FAKE, FAKE, FAKE + 1, *args, 1, 1, None) == 3  # 16-bit output, odd address
+        assert fn(FAKE, FAKE, None, *args, 1, 1, None) == 1
+
+
 def test_size_limits(lib):
     assert call_fwd(lib, N=1 << 20, H=1 << 12, W=1 << 12, C=1 << 10) == 2
 

@@ -364,3 +364,48 @@ def test_fwd_bn_act_full_workload_sampled():
     den = bnact_denominator(xn, wn, prm, 1e-5, case.stride, case.pad, idx)
     err = normalized_error(y.cpu().numpy().ravel()[idx], ref, den)
     assert err <= TOL["f32"], err
+
+
+# -- 16-bit outputs (forward and backward data, outputs of the input's own type) ----------
+
+OUT16 = [
+    C_(2, 17, 19, 64, 3),           # row kernels
+    C_(1, 23, 37, 128, 7),
+    C_(1, 20, 60, 64, 17),          # tensor-core kernels (wide rows, 17 taps)
+    C_(2, 7, 7, 128, 9),            # small-map kernels
+    C_(2, 17, 19, 64, 3, s=2),      # stride-2 kernels
+    C_(1, 23, 37, 128, 7, s=2),
+    C_(1, 10, 10, 16, 5, s=3, p=2), # general kernels
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("case", OUT16, ids=lambda c: f"n{c.N}_{c.H}x{c.W}_c{c.C}_f{c.FH}_s{c.stride}")
+def test_16bit_outputs(case, dtype):
+    case = Case(**{**case.__dict__, "dtype": dtype})
+    x, w, dy = case.x(), case.w(), case.dy()
+    td = x.dtype
+    y = dwc.fwd(x.cuda(), w.cuda(), case.stride, case.pad, out_dtype=td)
+    dx = dwc.bwd_data(dy.cuda(), w.cuda(), (case.H, case.W), case.stride, case.pad, out_dtype=td)
+    torch.cuda.synchronize()
+    assert y.dtype == td and dx.dtype == td
+    s, p = case.stride, case.pad
+    xn, wn, dyn = (t.double().numpy() for t in (x, w, dy))
+    # fp16 outputs below 2**-14 are subnormal: their rounding error is absolute, up to half
+    # the spacing 2**-24, on top of the normalised bound (bf16 keeps fp32's exponent range)
+    quantum = 2.0 ** -25 if dtype == "f16" else 0.0
+
+    def check(name, got, ref, den):
+        got = got.double().cpu().numpy()
+        assert np.all(np.isfinite(got))
+        bad = np.abs(got - ref) > TOL[dtype] * den + quantum
+        assert not bad.any(), f"{name} {case}: {int(bad.sum())} elements beyond the bound"
+
+    check("fwd", y, oracle.fwd(xn, wn, s, p), oracle.fwd(np.abs(xn), np.abs(wn), s, p))
+    check("bwd_data", dx, oracle.bwd_data(dyn, wn, (case.H, case.W), s, p),
+          oracle.bwd_data(np.abs(dyn), np.abs(wn), (case.H, case.W), s, p))
+    # the 16-bit output is the fp32 output rounded once to nearest even
+    y32 = dwc.fwd(x.cuda(), w.cuda(), s, p)
+    torch.cuda.synchronize()
+    assert torch.equal(y.cpu(), y32.cpu().to(td))
+
