@@ -149,7 +149,7 @@ bool valid_out_dtype(dwc_dtype_t dtype, dwc_dtype_t out_dtype) {
 
 bool fast_eligible(const Problem& P, const void* a, const void* b, const void* out) {
     if (P.s != 1) return false;
-    if (!rows_supported(P.FH, P.FW)) return false;
+    if (!rows_supported(P.FH, P.FW) && !stripe_supported(P.FH, P.FW)) return false;
     if (P.C % (16 / P.e) != 0) return false;  // TMA strides must be multiples of 16 bytes
     for (const void* q : {a, b, out})
         if (q != nullptr && !aligned(q, 16)) return false;
@@ -183,6 +183,20 @@ cudaError_t launch_rows_bnact(const RowConv& rc, int stride) {
 dwc_status_t map_cuda(cudaError_t err) { return err == cudaSuccess ? DWC_OK : DWC_ERR_CUDA; }
 
 cudaError_t launch_rows(const RowConv& rc) {
+    if (rc.FH != rc.FW) {
+        // stripe filter: the tensor-core kernel where it serves 16-bit inputs, else the row
+        // kernel with the filter height read at run time
+        cudaError_t err = cudaErrorNotSupported;
+        if (rc.dtype == kBF16) err = launch_rows_bf16(rc);
+        if (rc.dtype == kF16) err = launch_rows_f16(rc);
+        if (err != cudaErrorNotSupported) return err;
+        (void)cudaGetLastError();
+        switch (rc.dtype) {
+            case kF32: return launch_rows_stripe_f32(rc);
+            case kBF16: return launch_rows_stripe_bf16(rc);
+            default: return launch_rows_stripe_f16(rc);
+        }
+    }
     if (small_map_serves(rc.H, rc.W, rc.OH, rc.OW, rc.FW, rc.pad_w)) {
         cudaError_t err;
         switch (rc.dtype) {
@@ -200,7 +214,7 @@ cudaError_t launch_rows(const RowConv& rc) {
 }
 
 cudaError_t launch_fgrad(const FilterGrad& fg) {
-    {
+    if (fg.FH == fg.FW) {
         cudaError_t err;
         switch (fg.dtype) {
             case kF32: err = launch_small_fgrad_f32(fg); break;
@@ -233,6 +247,7 @@ cudaError_t launch_fgrad_s2(const FilterGrad& fg) {
 }
 
 size_t small_fgrad_floats(const Problem& P) {
+    if (P.FH != P.FW) return 0;
     switch (P.dtype) {
         case kF32: return small_fgrad_workspace_floats_f32(P.N, P.H, P.W, P.C, P.OH, P.OW, P.FH, P.FW, P.p);
         case kBF16: return small_fgrad_workspace_floats_bf16(P.N, P.H, P.W, P.C, P.OH, P.OW, P.FH, P.FW, P.p);
@@ -473,8 +488,8 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
         if (small_fgrad_floats(P) > 0) return 3;
         return P.e == 2 && tensor_core_fgrad(N, C, P.OH, P.OW, FH, FW) ? 2 : 1;
     }
-    if (pass == kPassFwd ? small_map_serves(H, W, P.OH, P.OW, FW, pad)
-                         : small_map_serves(P.OH, P.OW, H, W, FW, FW - 1 - pad))
+    if (FH == FW && (pass == kPassFwd ? small_map_serves(H, W, P.OH, P.OW, FW, pad)
+                                      : small_map_serves(P.OH, P.OW, H, W, FW, FW - 1 - pad)))
         return 3;
     if (P.e == 2) {
         // the same RowConv the entry points build (backward data: over dy, output H x W)

@@ -21,6 +21,9 @@ size_t filter_grad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW
 
 bool filter_grad_supported(int FH, int FW) { return FH == FW && FH >= 3 && FH <= 31 && (FH & 1); }
 bool rows_supported(int FH, int FW) { return FH == FW && FH >= 3 && FH <= 51 && (FH & 1); }
+bool stripe_supported(int FH, int FW) {
+    return FH != FW && FH >= 1 && FH <= 255 && FW >= 1 && FW <= 51 && (FW & 1);
+}
 cudaError_t launch_filter_grad_s2_f32(const FilterGrad& p) { return launch_fgrad_s2_dispatch<float>(p); }
 
 size_t fgrad_s2_workspace_floats_f32(int N, int OH, int OW, int C, int FH, int FW) {

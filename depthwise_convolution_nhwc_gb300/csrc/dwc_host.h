@@ -97,6 +97,12 @@ cudaError_t launch_rows_f32(const RowConv& p);
 cudaError_t launch_rows_bf16(const RowConv& p);
 cudaError_t launch_rows_f16(const RowConv& p);
 bool rows_supported(int FH, int FW);
+// Stripe (non-square) filters on the row kernel: any height from 1 to 255, odd widths 1..51,
+// fp32 outputs; rows_supported / stripe_supported tell the square and the stripe shapes.
+cudaError_t launch_rows_stripe_f32(const RowConv& p);
+cudaError_t launch_rows_stripe_bf16(const RowConv& p);
+cudaError_t launch_rows_stripe_f16(const RowConv& p);
+bool stripe_supported(int FH, int FW);
 // Stride-2 forward row kernels (square filters of 3, 5 or 7 taps; RowConv's OH/OW are the
 // strided output dims, pad_h/pad_w the forward pads).
 cudaError_t launch_rows_s2_f32(const RowConv& p);

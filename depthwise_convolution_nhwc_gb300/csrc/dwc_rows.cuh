@@ -61,6 +61,7 @@ struct RowsArgs {
     int H, W;             // input rows / columns (rows and columns that lie in the padding)
     int OH, OW, C;
     int pad_h, pad_w;
+    int FH;               // filter rows (the kernel's template FH, or any for FH = 0)
     int nwc;              // compute warps per CTA
     int ns;               // pipeline stages
     uint32_t cblocks, bands, ctiles;
@@ -179,7 +180,11 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     static_assert(SD == 1 || (R == 1 && !FLIP), "strided bands hold one output row (forward)");
     static_assert(ACT < 0 || !FLIP, "BN + Act fusion precedes the forward pass only");
     static_assert(ACT < 0 || SD * (TM - 1) + FW <= 32, "column mask holds 32 staged columns");
-    constexpr int S = R + FH - 1;  // input rows per band
+    static_assert(FH > 0 || R == 1, "a filter height chosen at run time needs one-row bands");
+    // filter rows: the template's, or (FH = 0, stripe filters) the launch's
+    const int fhn = FH > 0 ? FH : a.FH;
+    constexpr int SC = R + FH - 1;  // input rows per band (compile time, R > 1)
+    const int S = FH > 0 ? SC : R + fhn - 1;
 
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -226,13 +231,13 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
                 }
                 if (issued < static_cast<uint32_t>(a.ns)) ++issued;
                 unsigned char* st = stages + static_cast<size_t>(ring.slot) * a.stage_stride;
-                const bool wrow = i < FH;
+                const bool wrow = i < fhn;
                 mbar_arrive_expect_tx(&full[ring.slot], a.x_bytes + (wrow ? a.w_bytes : 0u));
                 tma_load_4d(st, &xmap, &full[ring.slot], cb * kBN, ow0 * SD - a.pad_w,
                             oh0 * SD - a.pad_h + i, n);
                 if (wrow)
                     tma_load_3d(st + a.x_bytes, &wmap, &full[ring.slot], cb * kBN, 0,
-                                FLIP ? FH - 1 - i : i);
+                                FLIP ? fhn - 1 - i : i);
             }
         }
         // Never leave the CTA with copies in flight: wait (bounded) for the stages still
@@ -334,7 +339,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             }
             const unsigned char* st = stages + static_cast<size_t>(ring.slot) * a.stage_stride;
             constexpr int slot = decltype(ic)::value % R;
-            if (i < FH) {
+            if (i < fhn) {
                 const T* ws = reinterpret_cast<const T*>(st + a.x_bytes) + 2 * lane;
 #pragma unroll
                 for (int f = 0; f < FW; ++f)
@@ -382,7 +387,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         } else if constexpr (R > 1) {
             // every input row of the band unrolled: output row r takes filter row i - r
             // from slot (i - r) % R
-            static_for<S>([&](auto I) {
+            static_for<SC>([&](auto I) {
                 constexpr int i = decltype(I)::value;
                 if (!ok) return;
                 const T* xs;
@@ -459,7 +464,7 @@ cudaError_t launch_rows_inst(const RowConv& p) {
             return cudaErrorNotSupported;  // the caller falls back to the general kernels
     }
     {
-        const cuuint64_t dims[3] = {(cuuint64_t)p.C, (cuuint64_t)FW, (cuuint64_t)FH};
+        const cuuint64_t dims[3] = {(cuuint64_t)p.C, (cuuint64_t)FW, (cuuint64_t)p.FH};
         const cuuint64_t strides[2] = {(cuuint64_t)p.C * e, (cuuint64_t)FW * p.C * e};
         const cuuint32_t box[3] = {(cuuint32_t)kBN, (cuuint32_t)FW, 1u};
         if (encode_tiled(&wmap, Elem<T>::kTmaType, 3, const_cast<void*>(p.w), dims, strides,
@@ -472,6 +477,7 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     a.status = p.status;
     a.H = p.H;
     a.W = p.W;
+    a.FH = p.FH;
     a.bn_mean = p.bn_mean; a.bn_var = p.bn_var; a.bn_gamma = p.bn_gamma; a.bn_beta = p.bn_beta;
     a.bn_eps = p.bn_eps;
     a.OH = p.OH; a.OW = p.OW; a.C = p.C;
@@ -611,6 +617,39 @@ cudaError_t launch_rows_bnact_dispatch(const RowConv& p) {
         case 5: return launch_rows_bnact_act<T, SD, 5>(p);
         case 7: return launch_rows_bnact_act<T, SD, 7>(p);
         default: return cudaErrorNotSupported;
+    }
+}
+
+// Stripe (non-square) filters: any filter height, odd widths 1..51, one output row per lane
+// with the filter height read at run time.  Narrow filters take 16 outputs per lane (more
+// taps per staged value), the others the tiles of the large square filters.
+template <int FW>
+struct StripeTile {
+    static constexpr int TM = FW <= 7 ? 16 : 14;
+    static constexpr int MINB = FW <= 7 ? 3 : (FW <= 31 ? 2 : 1);
+};
+
+template <typename T, int FW>
+cudaError_t launch_rows_stripe_inst(const RowConv& p) {
+    using St = StripeTile<FW>;
+    return p.flip ? launch_rows_inst<T, 0, FW, 1, St::TM, St::MINB, true>(p)
+                  : launch_rows_inst<T, 0, FW, 1, St::TM, St::MINB, false>(p);
+}
+
+#define DWC_STRIPE_WIDTHS(X) X(1) X(3) X(5) X(7) X(9) X(11) X(13) X(15) X(17) X(19) X(21) X(23) \
+    X(25) X(27) X(29) X(31) X(33) X(35) X(37) X(39) X(41) X(43) X(45) X(47) X(49) X(51)
+
+template <typename T>
+cudaError_t launch_rows_stripe_dispatch(const RowConv& p) {
+    if (p.FH == p.FW || p.FH < 1 || p.out_dtype != kF32) return cudaErrorNotSupported;
+    switch (p.FW) {
+#define DWC_STRIPE_CASE(F) \
+    case F:                \
+        return launch_rows_stripe_inst<T, F>(p);
+        DWC_STRIPE_WIDTHS(DWC_STRIPE_CASE)
+#undef DWC_STRIPE_CASE
+        default:
+            return cudaErrorNotSupported;
     }
 }
 

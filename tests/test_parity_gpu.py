@@ -409,3 +409,27 @@ def test_16bit_outputs(case, dtype):
     torch.cuda.synchronize()
     assert torch.equal(y.cpu(), y32.cpu().to(td))
 
+
+
+# -- stripe (non-square) filters: the row kernel with the filter height read at run time ----
+
+STRIPES = [
+    C_(2, 17, 19, 64, 7, FW=1, p=0),     # 7 x 1
+    C_(2, 17, 19, 64, 1, FW=7, p=0),     # 1 x 7
+    C_(1, 23, 37, 64, 5, FW=3, p=1),
+    C_(1, 23, 37, 64, 3, FW=7, p=1),
+    C_(1, 60, 40, 64, 51, FW=5, p=2),    # SLaK-style stripes
+    C_(1, 20, 70, 64, 5, FW=51, p=2),    # (16-bit: tensor-core kernel, rows >= 24 wide)
+    C_(2, 30, 45, 96, 13, FW=3, p=4),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("case", STRIPES, ids=lambda c: f"n{c.N}_{c.H}x{c.W}_c{c.C}_f{c.FH}x{c.FW}_p{c.pad}")
+def test_stripe_filters(case, dtype):
+    case = Case(**{**case.__dict__, "dtype": dtype})
+    code = {"f32": 0, "bf16": 1, "f16": 2}[dtype]
+    args = (case.N, case.H, case.W, case.C, case.FH, case.FW, case.stride, case.pad, code)
+    assert dwc.path("fwd", None, None, None, *args) in ((1,) if dtype == "f32" else (1, 2))
+    assert dwc.path("bwd_data", None, None, None, *args) in ((1,) if dtype == "f32" else (1, 2))
+    check_full(case)
