@@ -486,7 +486,7 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
     if (pass == kPassBwdFilter) {
         if (fast_fgrad_floats(P) == 0) return 0;
         if (small_fgrad_floats(P) > 0) return 3;
-        return P.e == 2 && tensor_core_fgrad(N, C, P.OH, P.OW, FH, FW) ? 2 : 1;
+        return P.e == 2 && FH == FW && tensor_core_fgrad(N, C, P.OH, P.OW, FH, FW) ? 2 : 1;
     }
     if (FH == FW && (pass == kPassFwd ? small_map_serves(H, W, P.OH, P.OW, FW, pad)
                                       : small_map_serves(P.OH, P.OW, H, W, FW, FW - 1 - pad)))

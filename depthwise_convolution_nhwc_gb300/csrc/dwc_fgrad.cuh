@@ -57,7 +57,7 @@ struct FgradTile {
     // rows per warp timed fastest on the stage shapes: 2 for 7x7, 1 for 5x5, 9x9 and
     // 11x11, else what about 120 registers hold
     static constexpr int kFit = FH == 7 ? 2 : ((FH == 5 || FH == 9 || FH == 11) ? 1 : 120 / (4 * FWC));
-    static constexpr int RF = RF_ > 0 ? RF_ : (kFit < 1 ? 1 : (kFit > FH ? FH : kFit));
+    static constexpr int RF = RF_ > 0 ? RF_ : (kFit < 1 ? 1 : ((FH > 0 && kFit > FH) ? FH : kFit));
     static constexpr int MINB = MINB_ > 0 ? MINB_ : 1;
     static constexpr int U = U_ > 0 ? U_ : (SD == 1 ? FWC : (KW <= 4 ? 4 : KW));
     static_assert(U >= KW, "the window must hold the columns one output column needs");
@@ -94,6 +94,7 @@ struct FgradArgs {
     float* part;           // [Z * ncp][FH][FW][C] partial sums
     unsigned int* status;
     int N, OH, C, pad;
+    int FH;                // filter rows (the template's, or any for a stripe tile, FH = 0)
     int ncp, owpart;       // column parts of a row, output columns per part
     int nwf, nwc;          // compute warps: filter-row groups x column strips
     int fhc, chunks, cblocks, Z;
@@ -266,7 +267,8 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 
     bool live[RF];
 #pragma unroll
-    for (int f = 0; f < RF; ++f) live[f] = (frow0 + f < a.fhc) && (fh0 + frow0 + f < FH);
+    const int fhn = FH > 0 ? FH : a.FH;
+    for (int f = 0; f < RF; ++f) live[f] = (frow0 + f < a.fhc) && (fh0 + frow0 + f < fhn);
 
     Ring xbase, yr;  // oldest x row of the current window; current dy row
     bool ok = true;
@@ -386,7 +388,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     s.x += v.x;
                     s.y += v.y;
                 }
-                float* dst = a.part + ((static_cast<size_t>(z * a.ncp + cp) * FH + fh) * FW + fw) * a.C + c;
+                float* dst = a.part + ((static_cast<size_t>(z * a.ncp + cp) * fhn + fh) * FW + fw) * a.C + c;
                 *reinterpret_cast<float2*>(dst) = s;
             }
         }
@@ -406,7 +408,7 @@ struct FgradPlan {
 // deepest lookahead between min_la output rows and the tile's that fits.
 template <typename T, int FH, int FW, class Tile>
 bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
-                      FgradPlan<FH, FW, Tile>& P) {
+                      FgradPlan<FH, FW, Tile>& P, int fhr) {
     const int e = static_cast<int>(sizeof(T));
     constexpr int RF = Tile::RF;
     const DeviceInfo& dev = device_info();
@@ -426,7 +428,7 @@ bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
     // most useful warp slots, counting warps up to 12 (about what hides the latencies of one
     // CTA per SM), discounted by the chunk count (each chunk streams every x and dy row of
     // its slice again); the weights were fitted to timings of the stage shapes.
-    const int groups = (FH + RF - 1) / RF;  // RF-row groups needed to cover the filter
+    const int groups = (fhr + RF - 1) / RF;  // RF-row groups needed to cover the filter
     // The lookahead (dy slots, and the x rows staged ahead of the window) is Tile::NY
     // output rows, or the deepest down to min_la that fits.
     double best = -1.0;
@@ -465,7 +467,7 @@ bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
     P.ny = best_la;
     P.nx = P.fhc + best_la * Tile::SD;
     P.smem = 512 + static_cast<size_t>(P.nx) * P.x_bytes + static_cast<size_t>(P.ny) * P.y_bytes;
-    P.chunks = (FH + P.fhc - 1) / P.fhc;
+    P.chunks = (fhr + P.fhc - 1) / P.fhc;
     // strip reduction buffer reuses the ring
     const size_t red = static_cast<size_t>(P.nwc) * P.nwf * NFC * RF * Tile::FWC * 32 * sizeof(float2);
     if (red > P.smem - 512) P.smem = 512 + red;
@@ -495,15 +497,16 @@ bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
 // 233 us), then the row cut into 2, 3 or 4 column parts (rows too wide for shared memory or
 // for one 256-column TMA box), each part a CTA of its own with its own partial-sum slot.
 template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
-bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P) {
+bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P, int fhr = FH) {
+    if (fhr < 1) return false;
     for (int ncp = 1; ncp <= 4; ++ncp) {
         if (ncp > 1 && (OW + ncp - 1) / ncp < Tile::U) break;
         if (Tile::SD > 1) {
-            if (fgrad_plan_parts<T, FH, FW, Tile>(N, OH, OW, C, ncp, 1, P)) return true;
+            if (fgrad_plan_parts<T, FH, FW, Tile>(N, OH, OW, C, ncp, 1, P, fhr)) return true;
             continue;
         }
         for (int min_la : {Tile::NY, 2, 1})
-            if (min_la <= Tile::NY && fgrad_plan_parts<T, FH, FW, Tile>(N, OH, OW, C, ncp, min_la, P))
+            if (min_la <= Tile::NY && fgrad_plan_parts<T, FH, FW, Tile>(N, OH, OW, C, ncp, min_la, P, fhr))
                 return true;
     }
     return false;
@@ -513,11 +516,12 @@ template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
 cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     const int e = static_cast<int>(sizeof(T));
     FgradPlan<FH, FW, Tile> P;
-    if (!fgrad_plan<T, FH, FW, Tile>(p.N, p.OH, p.OW, p.C, P)) return cudaErrorNotSupported;
+    const int fhr = FH > 0 ? FH : p.FH;
+    if (!fgrad_plan<T, FH, FW, Tile>(p.N, p.OH, p.OW, p.C, P, fhr)) return cudaErrorNotSupported;
     if (p.N == 0 || p.OH == 0 || p.OW == 0) {
-        return cudaMemsetAsync(p.dw, 0, sizeof(float) * FH * FW * p.C, p.stream);
+        return cudaMemsetAsync(p.dw, 0, sizeof(float) * fhr * FW * p.C, p.stream);
     }
-    const size_t need = static_cast<size_t>(P.Z) * P.ncp * FH * FW * p.C;
+    const size_t need = static_cast<size_t>(P.Z) * P.ncp * fhr * FW * p.C;
     if (p.workspace_floats < need || p.workspace == nullptr) return cudaErrorInvalidValue;
 
     CUtensorMap xmap, ymap;
@@ -544,6 +548,7 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     a.status = p.status;
     a.N = p.N; a.OH = p.OH; a.C = p.C; a.pad = p.pad;
     a.ncp = P.ncp; a.owpart = P.owpart;
+    a.FH = fhr;
     a.nwf = P.nwf; a.nwc = P.nwc; a.fhc = P.fhc; a.chunks = P.chunks; a.cblocks = P.cblocks;
     a.Z = P.Z; a.rows_per_slice = P.rows_per_slice; a.nblocks = P.nblocks; a.bps = P.bps;
     a.nx = P.nx; a.ny = P.ny; a.x_bytes = P.x_bytes; a.y_bytes = P.y_bytes; a.y_off = P.y_off;
@@ -561,15 +566,15 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     kern<<<grid, threads, P.smem, p.stream>>>(xmap, ymap, a);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    return launch_reduce_slices(p.workspace, P.Z * P.ncp, static_cast<size_t>(FH) * FW * p.C, p.dw,
+    return launch_reduce_slices(p.workspace, P.Z * P.ncp, static_cast<size_t>(fhr) * FW * p.C, p.dw,
                                 p.stream);
 }
 
 template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
-size_t fgrad_workspace_inst(int N, int OH, int OW, int C) {
+size_t fgrad_workspace_inst(int N, int OH, int OW, int C, int fhr = FH) {
     FgradPlan<FH, FW, Tile> P;
-    if (!fgrad_plan<T, FH, FW, Tile>(N, OH, OW, C, P)) return 0;
-    return static_cast<size_t>(P.Z) * P.ncp * FH * FW * static_cast<size_t>(C);
+    if (!fgrad_plan<T, FH, FW, Tile>(N, OH, OW, C, P, fhr)) return 0;
+    return static_cast<size_t>(P.Z) * P.ncp * fhr * FW * static_cast<size_t>(C);
 }
 
 // Workspace of the launch that launch_fgrad_dispatch makes for this problem.
@@ -666,5 +671,41 @@ cudaError_t launch_fgrad_dispatch(const FilterGrad& p) {
     }
 }
 
-}  // namespace dwc
+// Stripe (non-square) filters: the filter height read at run time, one filter row per warp,
+// odd widths 1..51 (past 31 taps in two chunks), window period a multiple of 7 of at least 4.
+template <int FW>
+struct FgradStripe {
+    static constexpr int FWC = FW > 31 ? (FW + 1) / 2 : FW;
+    static constexpr int U = FWC <= 3 ? 4 : (FWC <= 7 ? 7 : (FWC <= 14 ? 14 : (FWC <= 28 ? 28 : FWC)));
+    using Tile = FgradTile<0, FW, 1, 0, U, 0, 1, (FW > 31 ? FWC : 0)>;
+};
 
+template <typename T>
+cudaError_t launch_fgrad_stripe_dispatch(const FilterGrad& p) {
+    if (p.FH == p.FW) return cudaErrorNotSupported;
+    switch (p.FW) {
+#define DWC_FGRAD_STRIPE_CASE(F) \
+    case F:                      \
+        return launch_fgrad_inst<T, 0, F, typename FgradStripe<F>::Tile>(p);
+        DWC_STRIPE_WIDTHS(DWC_FGRAD_STRIPE_CASE)
+#undef DWC_FGRAD_STRIPE_CASE
+        default:
+            return cudaErrorNotSupported;
+    }
+}
+
+template <typename T>
+size_t fgrad_stripe_workspace_t(int N, int OH, int OW, int C, int FH, int FW) {
+    if (FH == FW || FH < 1 || FH > 255) return 0;
+    switch (FW) {
+#define DWC_FGRAD_STRIPE_WS(F) \
+    case F:                    \
+        return fgrad_workspace_inst<T, 0, F, typename FgradStripe<F>::Tile>(N, OH, OW, C, FH);
+        DWC_STRIPE_WIDTHS(DWC_FGRAD_STRIPE_WS)
+#undef DWC_FGRAD_STRIPE_WS
+        default:
+            return 0;
+    }
+}
+
+}  // namespace dwc

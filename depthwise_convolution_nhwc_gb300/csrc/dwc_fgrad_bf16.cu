@@ -4,6 +4,7 @@
 
 namespace dwc {
 cudaError_t launch_filter_grad_bf16(const FilterGrad& p) {
+    if (p.FH != p.FW) return launch_fgrad_stripe_bf16(p);
     // tensor-core kernel where it serves the shape, CUDA-core kernel otherwise
     const cudaError_t err = launch_mma_fgrad<__nv_bfloat16>(p);
     if (err != cudaErrorNotSupported) return err;

@@ -3,14 +3,23 @@
 #include "dwc_mma_fgrad.cuh"
 
 namespace dwc {
-cudaError_t launch_filter_grad_f32(const FilterGrad& p) { return launch_fgrad_dispatch<float>(p); }
+cudaError_t launch_filter_grad_f32(const FilterGrad& p) {
+    if (p.FH != p.FW) return launch_fgrad_stripe_f32(p);
+    return launch_fgrad_dispatch<float>(p);
+}
 
 size_t fgrad_workspace_floats_f32(int N, int OH, int OW, int C, int FH, int FW) {
     return fgrad_workspace_t<float>(N, OH, OW, C, FH, FW);
 }
 
 size_t filter_grad_workspace_floats(int N, int OH, int OW, int C, int FH, int FW, int dtype) {
-    if (FH != FW) return 0;
+    if (FH != FW) {
+        switch (dtype) {
+            case kF32: return fgrad_stripe_workspace_floats_f32(N, OH, OW, C, FH, FW);
+            case kBF16: return fgrad_stripe_workspace_floats_bf16(N, OH, OW, C, FH, FW);
+            default: return fgrad_stripe_workspace_floats_f16(N, OH, OW, C, FH, FW);
+        }
+    }
     if (dtype == kF32) return fgrad_workspace_floats_f32(N, OH, OW, C, FH, FW);
     // 16-bit inputs may run the tensor-core kernel: its slices must fit too
     const size_t mma = mma_fgrad_workspace_floats(N, C, OH, OW, FH, FW);

@@ -103,6 +103,12 @@ cudaError_t launch_rows_stripe_f32(const RowConv& p);
 cudaError_t launch_rows_stripe_bf16(const RowConv& p);
 cudaError_t launch_rows_stripe_f16(const RowConv& p);
 bool stripe_supported(int FH, int FW);
+cudaError_t launch_fgrad_stripe_f32(const FilterGrad& p);
+cudaError_t launch_fgrad_stripe_bf16(const FilterGrad& p);
+cudaError_t launch_fgrad_stripe_f16(const FilterGrad& p);
+size_t fgrad_stripe_workspace_floats_f32(int N, int OH, int OW, int C, int FH, int FW);
+size_t fgrad_stripe_workspace_floats_bf16(int N, int OH, int OW, int C, int FH, int FW);
+size_t fgrad_stripe_workspace_floats_f16(int N, int OH, int OW, int C, int FH, int FW);
 // Stride-2 forward row kernels (square filters of 3, 5 or 7 taps; RowConv's OH/OW are the
 // strided output dims, pad_h/pad_w the forward pads).
 cudaError_t launch_rows_s2_f32(const RowConv& p);

@@ -157,8 +157,9 @@ def test_path_selection_host_logic(lib):
     assert p(0, stride=2, FH=9, FW=9, pad=4, H=40, W=40) == 0 and p(0, stride=3) == 0
     assert p(0, stride=2, C=6) == 0
     assert p(0, FH=4, FW=4) == 0               # even filter
-    # stripe (non-square) filters: row kernel for odd widths 1..51, general filter gradient
-    assert p(0, FH=3, FW=5) == 1 and p(1, FH=3, FW=5) == 1 and p(2, FH=3, FW=5) == 0
+    # stripe (non-square) filters: row and filter-gradient kernels for odd widths 1..51
+    assert p(0, FH=3, FW=5) == 1 and p(1, FH=3, FW=5) == 1 and p(2, FH=3, FW=5) == 1
+    assert p(2, FH=51, FW=5, pad=2, H=60, W=60) == 1 and p(2, FH=5, FW=51, pad=2, H=60, W=60) == 1
     assert p(0, FH=51, FW=5, pad=2, H=60, W=60) == 1 and p(0, FH=1, FW=7, pad=0) == 1
     assert p(0, FH=5, FW=4) == 0               # even width
     assert p(0, FH=5, FW=53, pad=26, H=60, W=60) == 0

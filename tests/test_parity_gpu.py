@@ -411,7 +411,8 @@ def test_16bit_outputs(case, dtype):
 
 
 
-# -- stripe (non-square) filters: the row kernel with the filter height read at run time ----
+# -- stripe (non-square) filters: row and filter-gradient kernels with the filter height read
+# at run time ---------------------------------------------------------------------------------
 
 STRIPES = [
     C_(2, 17, 19, 64, 7, FW=1, p=0),     # 7 x 1
@@ -432,4 +433,5 @@ def test_stripe_filters(case, dtype):
     args = (case.N, case.H, case.W, case.C, case.FH, case.FW, case.stride, case.pad, code)
     assert dwc.path("fwd", None, None, None, *args) in ((1,) if dtype == "f32" else (1, 2))
     assert dwc.path("bwd_data", None, None, None, *args) in ((1,) if dtype == "f32" else (1, 2))
+    assert dwc.path("bwd_filter", None, None, None, *args) == 1
     check_full(case)
