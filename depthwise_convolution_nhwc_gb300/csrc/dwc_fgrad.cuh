@@ -265,9 +265,9 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 #pragma unroll
         for (int t = 0; t < FC; ++t) acc[f][t] = make_float2(0.f, 0.f);
 
+    const int fhn = FH > 0 ? FH : a.FH;
     bool live[RF];
 #pragma unroll
-    const int fhn = FH > 0 ? FH : a.FH;
     for (int f = 0; f < RF; ++f) live[f] = (frow0 + f < a.fhc) && (fh0 + frow0 + f < fhn);
 
     Ring xbase, yr;  // oldest x row of the current window; current dy row
@@ -501,13 +501,14 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P, int fh
     if (fhr < 1) return false;
     for (int ncp = 1; ncp <= 4; ++ncp) {
         if (ncp > 1 && (OW + ncp - 1) / ncp < Tile::U) break;
-        if (Tile::SD > 1) {
+        if constexpr (Tile::SD > 1) {
             if (fgrad_plan_parts<T, FH, FW, Tile>(N, OH, OW, C, ncp, 1, P, fhr)) return true;
-            continue;
+        } else {
+            for (int min_la : {Tile::NY, 2, 1})
+                if (min_la <= Tile::NY &&
+                    fgrad_plan_parts<T, FH, FW, Tile>(N, OH, OW, C, ncp, min_la, P, fhr))
+                    return true;
         }
-        for (int min_la : {Tile::NY, 2, 1})
-            if (min_la <= Tile::NY && fgrad_plan_parts<T, FH, FW, Tile>(N, OH, OW, C, ncp, min_la, P, fhr))
-                return true;
     }
     return false;
 }
