@@ -16,7 +16,8 @@
  *     W, dW : FH x FW x C          (filter and its gradient; channel last)
  *
  * Data types: the inputs (X, W, dY) of one call share one dtype (fp32, bf16 or fp16);
- * every output (Y, dX, dW) is fp32.  All arithmetic is fp32 multiply-add; 16-bit inputs
+ * every output (Y, dX, dW) is fp32, except that dwc_fwd_ex / dwc_bwd_data_ex may write Y /
+ * dX in the 16-bit input's own type.  All arithmetic is fp32 multiply-add; 16-bit inputs
  * are widened to fp32 exactly before use.
  *
  * Pointers and ownership: every tensor pointer is a DEVICE pointer allocated and owned by
@@ -32,9 +33,13 @@
  * ends; dwc_device_status() reports it as DWC_ERR_TIMEOUT.
  *
  * Every fp32 tensor must be 4-byte aligned and every 16-bit tensor 2-byte aligned.  The
- * fast kernels are used when stride == 1, the filter is square with odd FH in [3, 31],
- * C is a multiple of 4 (fp32) or 8 (16-bit) and all pointers are 16-byte aligned;
- * everything else runs on the general kernels (same results, slower).
+ * fast kernels are used when C is a multiple of 4 (fp32) or 8 (16-bit), all pointers are
+ * 16-byte aligned and either
+ *   - stride == 1 with a square filter of odd size 3..51, or a stripe (non-square) filter
+ *     of odd width 1..51 and any height 1..255, or
+ *   - stride == 2 with a square 3x3, 5x5 or 7x7 filter;
+ * everything else (strides above 2, even widths, ...) runs on the general kernels (same
+ * results, slower).
  */
 #ifndef DWC_GB300_H
 #define DWC_GB300_H
@@ -183,9 +188,9 @@ const char* dwc_status_string(dwc_status_t status);
 int dwc_version(void);
 
 /* Which kernel family a call with these arguments would use: 1 = fast CUDA-core kernels
- * (row-streaming, stride-2 and filter-gradient kernels: stride 1, and stride 2 with 3x3,
- * 5x5 or 7x7 filters), 2 = tensor-core kernels (16-bit inputs only), 3 = small-map kernels
- * (maps up to 16 x 16), 0 = general kernels, -1 = invalid arguments.  `pass` is 0 for
+ * (row-streaming, stride-2 and filter-gradient kernels, for the shapes listed at the top
+ * of this file), 2 = tensor-core kernels (16-bit inputs only), 3 = small-map kernels (maps
+ * up to 16 x 16), 0 = general kernels, -1 = invalid arguments.  `pass` is 0 for
  * dwc_fwd, 1 for dwc_bwd_data, 2 for dwc_bwd_filter, 3 for dwc_fwd_bn_act.  Pointer
  * alignment is checked with the pointers given (they may be NULL to mean "16-byte
  * aligned"). */
