@@ -435,3 +435,48 @@ def test_stripe_filters(case, dtype):
     assert dwc.path("bwd_data", None, None, None, *args) in ((1,) if dtype == "f32" else (1, 2))
     assert dwc.path("bwd_filter", None, None, None, *args) == 1
     check_full(case)
+
+
+# -- seeded random shapes across every dispatch branch ------------------------------------
+
+def random_cases(count=120, seed=20261203):
+    """Valid problems drawn at random: maps 1..70 (some up to 300 wide, some small maps),
+    channel counts that keep the fast-path layout rule or break it, square odd filters
+    3..51, stripes, even filters, strides 1..3, pads 0..F-1, every input dtype."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        dtype = ["f32", "bf16", "f16"][rng.integers(3)]
+        s = int(rng.choice([1, 1, 1, 1, 2, 2, 3]))
+        kind = rng.integers(5)
+        if kind == 0:
+            FH = FW = int(rng.choice([3, 5, 7]))
+        elif kind == 1:
+            FH = FW = int(rng.choice([9, 13, 17, 25, 31, 41, 51]))
+        elif kind == 2:
+            FH, FW = int(rng.integers(1, 32)), int(rng.choice([1, 3, 5, 7, 9, 15, 21]))
+        elif kind == 3:
+            FH = FW = int(rng.choice([9, 13, 21, 31]))
+        else:
+            FH = FW = int(rng.choice([2, 4, 6]))
+        pad = int(rng.integers(0, max(FH, FW)))
+        if kind == 3:   # small maps
+            H, W = int(rng.integers(max(1, FH - 2 * pad), 17)), int(rng.integers(max(1, FW - 2 * pad), 17))
+        else:
+            H = int(rng.integers(max(1, FH - 2 * pad), 40))
+            W = int(rng.choice([rng.integers(max(1, FW - 2 * pad), 70), rng.integers(100, 300)]))
+        C = int(rng.choice([8, 16, 24, 64, 96, 128, 136, 5]))
+        N = int(rng.integers(1, 3))
+        case = Case(N, H, W, C, FH, FW, s, pad, dtype, "normal", int(rng.integers(1 << 20)))
+        if case.OH < 1 or case.OW < 1:
+            continue
+        if N * H * W * C * FH * FW > 60_000_000:   # keep the fp64 oracle within seconds
+            continue
+        out.append(case)
+    return out
+
+
+@pytest.mark.parametrize("case", random_cases(),
+                         ids=lambda c: f"{c.dtype}_n{c.N}_{c.H}x{c.W}_c{c.C}_f{c.FH}x{c.FW}_s{c.stride}_p{c.pad}")
+def test_random_shapes_all_passes(case):
+    check_full(case)
