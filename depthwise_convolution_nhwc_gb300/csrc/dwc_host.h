@@ -38,6 +38,7 @@ struct RowConv {
     float bn_eps = 0.f;
     int act = -1;
     int out_dtype = kF32;   // kF32, or the input's type (kBF16 / kF16) for 16-bit outputs
+    int c_lo = 0, c_hi = -1; // channel range a row-kernel launch covers (c_hi < 0: up to C)
 };
 
 // Filter-gradient problem: dw[fh, fw, c] = sum_{n,oh,ow} x[n, oh+fh-pad, ow+fw-pad, c] * dy[n,oh,ow,c].

@@ -62,12 +62,14 @@ struct RowsArgs {
     int OH, OW, C;
     int pad_h, pad_w;
     int FH;               // filter rows (the kernel's template FH, or any for FH = 0)
+    int cbase;            // first channel of channel block 0
     int nwc;              // compute warps per CTA
     int ns;               // pipeline stages
     uint32_t cblocks, bands, ctiles;
     FastDiv fd_bands, fd_ctiles, fd_cblocks;   // the same three, as invariant divisors
     uint32_t units;
     uint32_t x_bytes;     // bytes of one staged input row box
+    uint32_t w_off;       // offset of the filter row in a stage (x_bytes rounded up to 128)
     uint32_t w_bytes;     // bytes of one staged filter row box
     uint32_t stage_stride;
     // fused BN + Act (ACT >= 0): batch statistics and affine parameters, C floats each
@@ -149,12 +151,12 @@ __host__ __device__ constexpr unsigned valid_rows(int i) {
 // With column stride SD, input column j of the lane feeds output t through tap
 // fw = j - SD * t.
 template <class P, typename T, int FW, int R, int TM, unsigned MASK, int ISLOT, int SD = 1,
-          class XF = NoXform>
+          class XF = NoXform, int PITCH = kBN>
 __device__ __forceinline__ void consume_rows(const T* __restrict__ xs, typename P::V (&acc)[R][TM],
                                              const typename P::V (&wwin)[R][FW], const XF& xf = XF{}) {
 #pragma unroll
     for (int j = 0; j < SD * (TM - 1) + FW; ++j) {
-        const typename P::V x = xf(P::load(xs + j * kBN), j);
+        const typename P::V x = xf(P::load(xs + j * PITCH), j);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             if (!((MASK >> r) & 1u)) continue;
@@ -172,8 +174,10 @@ __device__ __forceinline__ void consume_rows(const T* __restrict__ xs, typename 
 // SD: stride of both spatial axes (1, or 2 with one output row per band).  ACT: -1 plain
 // DWC, else BN + Act fused in front (0 identity, 1 ReLU, 2 ReLU6; forward only).  OutT:
 // output element type (fp32, or the 16-bit input type).
+// G: lane groups (1, or 2 / 4 for a tail block of at most 32 / 16 channels: each group of
+// 32 / G lanes covers the block's channels for its own TM columns, so no lane idles).
 template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64, int SD = 1,
-          int ACT = -1, class OutT = float>
+          int ACT = -1, class OutT = float, int G = 1>
 __global__ void __launch_bounds__(kRowsMaxThreads, MINB)
 rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
             const RowsArgs a) {
@@ -181,6 +185,10 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     static_assert(ACT < 0 || !FLIP, "BN + Act fusion precedes the forward pass only");
     static_assert(ACT < 0 || SD * (TM - 1) + FW <= 32, "column mask holds 32 staged columns");
     static_assert(FH > 0 || R == 1, "a filter height chosen at run time needs one-row bands");
+    static_assert(G == 1 || G == 2 || G == 4, "lane groups");
+    static_assert(G == 1 || ACT < 0, "lane groups run the plain DWC");
+    constexpr int PITCH = kBN / G;   // channels per staged pixel
+    constexpr int LPG = 32 / G;      // lanes per group
     // filter rows: the template's, or (FH = 0, stripe filters) the launch's
     const int fhn = FH > 0 ? FH : a.FH;
     constexpr int SC = R + FH - 1;  // input rows per band (compile time, R > 1)
@@ -203,7 +211,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     }
     __syncthreads();
 
-    const int TW = a.nwc * TM;
+    const int TW = a.nwc * G * TM;
 
     // ---------------- producer warp: TMA streaming of input and filter rows -------------
     if (warp == a.nwc) {
@@ -233,10 +241,10 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
                 unsigned char* st = stages + static_cast<size_t>(ring.slot) * a.stage_stride;
                 const bool wrow = i < fhn;
                 mbar_arrive_expect_tx(&full[ring.slot], a.x_bytes + (wrow ? a.w_bytes : 0u));
-                tma_load_4d(st, &xmap, &full[ring.slot], cb * kBN, ow0 * SD - a.pad_w,
+                tma_load_4d(st, &xmap, &full[ring.slot], a.cbase + cb * PITCH, ow0 * SD - a.pad_w,
                             oh0 * SD - a.pad_h + i, n);
                 if (wrow)
-                    tma_load_3d(st + a.x_bytes, &wmap, &full[ring.slot], cb * kBN, 0,
+                    tma_load_3d(st + a.w_off, &wmap, &full[ring.slot], a.cbase + cb * PITCH, 0,
                                 FLIP ? fhn - 1 - i : i);
             }
         }
@@ -255,6 +263,8 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
 
     // ---------------- compute warps ----------------------------------------------------
     const int wc = warp;
+    const int lg = lane / LPG;       // lane group: column sub-tile wc * G + lg
+    const int cl = lane % LPG;       // channel pair within the block
     Ring ring;
     for (uint32_t u = blockIdx.x; u < a.units; u += gridDim.x) {
         uint32_t r0, r1, r2;
@@ -262,8 +272,8 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         const int band = static_cast<int>(r0), ct = static_cast<int>(r1), cb = static_cast<int>(r2);
         const int n = static_cast<int>(q);
         const int oh0 = band * R;
-        const int owl = ct * TW + wc * TM;  // first output column of this lane
-        const int c = cb * kBN + 2 * lane;
+        const int owl = ct * TW + (wc * G + lg) * TM;  // first output column of this lane
+        const int c = a.cbase + cb * PITCH + 2 * cl;
 
         // BN + Act of this lane's two channels and the staged columns inside the image
         using XFull = typename std::conditional<(ACT >= 0), BnActXform<P, ACT, false>, NoXform>::type;
@@ -317,7 +327,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             constexpr unsigned M = decltype(mc)::value;
             constexpr int SL = decltype(sc)::value;
             if constexpr (ACT < 0) {
-                consume_rows<P, T, FW, R, TM, M, SL, SD>(xs, acc, wwin);
+                consume_rows<P, T, FW, R, TM, M, SL, SD, NoXform, PITCH>(xs, acc, wwin);
             } else if constexpr (R > 1) {
                 consume_rows<P, T, FW, R, TM, M, SL, SD>(xs, acc, wwin, xf);
             } else if (colfull) {
@@ -340,12 +350,12 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             const unsigned char* st = stages + static_cast<size_t>(ring.slot) * a.stage_stride;
             constexpr int slot = decltype(ic)::value % R;
             if (i < fhn) {
-                const T* ws = reinterpret_cast<const T*>(st + a.x_bytes) + 2 * lane;
+                const T* ws = reinterpret_cast<const T*>(st + a.w_off) + 2 * cl;
 #pragma unroll
                 for (int f = 0; f < FW; ++f)
-                    wwin[slot][f] = P::load(ws + (FLIP ? FW - 1 - f : f) * kBN);
+                    wwin[slot][f] = P::load(ws + (FLIP ? FW - 1 - f : f) * PITCH);
             }
-            xs = reinterpret_cast<const T*>(st) + (wc * TM * SD) * kBN + 2 * lane;
+            xs = reinterpret_cast<const T*>(st) + ((wc * G + lg) * TM * SD) * PITCH + 2 * cl;
             return true;
         };
         auto end_row = [&]() {
@@ -432,24 +442,30 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
 }
 
 template <typename T, int FH, int FW, int R, int TM, int MINB, bool FLIP, class P = Pair64, int SD = 1,
-          int ACT = -1, class OutT = float>
+          int ACT = -1, class OutT = float, int G = 1>
 cudaError_t launch_rows_inst(const RowConv& p) {
     const int e = static_cast<int>(sizeof(T));
     const DeviceInfo& dev = device_info();
+    constexpr int PITCH = kBN / G;
+    // channels [c_lo, c_hi) of the tensor (the tail launch of lane groups covers only the
+    // channels past the last multiple of 64)
+    const int c_lo = p.c_lo, c_hi = p.c_hi < 0 ? p.C : p.c_hi;
+    if (c_hi <= c_lo) return cudaSuccess;
 
-    // compute warps side by side along the row; the staged box (SD * (TW - 1) + FW pixels)
-    // must stay within the TMA box limit of 256
-    const int max_nwc = std::min(kMaxComputeWarps, (256 - FW + SD) / (SD * TM));
+    // compute warps side by side along the row (G column sub-tiles each); the staged box
+    // (SD * (TW - 1) + FW pixels) must stay within the TMA box limit of 256
+    const int max_nwc = std::min(kMaxComputeWarps, (256 - FW + SD) / (SD * G * TM));
     if (max_nwc < 1) return cudaErrorNotSupported;
     // warps per row tile: fewest computed columns plus half a halo per column tile
     int nwc = 1;
     long long best = LLONG_MAX;
     for (int n = 1; n <= max_nwc; ++n) {
-        const long long tiles = (p.OW + n * TM - 1) / (n * TM);
-        const long long cost = 2 * tiles * n * TM + tiles * (FW - 1);
+        const int tw = n * G * TM;
+        const long long tiles = (p.OW + tw - 1) / tw;
+        const long long cost = 2 * tiles * tw + tiles * (FW - 1);
         if (cost <= best) { best = cost; nwc = n; }
     }
-    const int TW = nwc * TM;
+    const int TW = nwc * G * TM;
     const int TWH = SD * (TW - 1) + FW;
 
     CUtensorMap xmap, wmap;
@@ -458,7 +474,7 @@ cudaError_t launch_rows_inst(const RowConv& p) {
                                     (cuuint64_t)p.N};
         const cuuint64_t strides[3] = {(cuuint64_t)p.C * e, (cuuint64_t)p.W * p.C * e,
                                        (cuuint64_t)p.H * p.W * p.C * e};
-        const cuuint32_t box[4] = {(cuuint32_t)kBN, (cuuint32_t)TWH, 1u, 1u};
+        const cuuint32_t box[4] = {(cuuint32_t)PITCH, (cuuint32_t)TWH, 1u, 1u};
         if (encode_tiled(&xmap, Elem<T>::kTmaType, 4, const_cast<void*>(p.in), dims, strides,
                          box) != CUDA_SUCCESS)
             return cudaErrorNotSupported;  // the caller falls back to the general kernels
@@ -466,7 +482,7 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     {
         const cuuint64_t dims[3] = {(cuuint64_t)p.C, (cuuint64_t)FW, (cuuint64_t)p.FH};
         const cuuint64_t strides[2] = {(cuuint64_t)p.C * e, (cuuint64_t)FW * p.C * e};
-        const cuuint32_t box[3] = {(cuuint32_t)kBN, (cuuint32_t)FW, 1u};
+        const cuuint32_t box[3] = {(cuuint32_t)PITCH, (cuuint32_t)FW, 1u};
         if (encode_tiled(&wmap, Elem<T>::kTmaType, 3, const_cast<void*>(p.w), dims, strides,
                          box) != CUDA_SUCCESS)
             return cudaErrorNotSupported;
@@ -483,7 +499,8 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     a.OH = p.OH; a.OW = p.OW; a.C = p.C;
     a.pad_h = p.pad_h; a.pad_w = p.pad_w;
     a.nwc = nwc;
-    a.cblocks = static_cast<uint32_t>((p.C + kBN - 1) / kBN);
+    a.cbase = c_lo;
+    a.cblocks = static_cast<uint32_t>((c_hi - c_lo + PITCH - 1) / PITCH);
     a.bands = static_cast<uint32_t>((p.OH + R - 1) / R);
     a.ctiles = static_cast<uint32_t>((p.OW + TW - 1) / TW);
     a.fd_bands.init(a.bands);
@@ -492,12 +509,16 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     const long long units = static_cast<long long>(p.N) * a.cblocks * a.bands * a.ctiles;
     if (units >= (1LL << 31)) return cudaErrorNotSupported;
     a.units = static_cast<uint32_t>(units);
-    a.x_bytes = static_cast<uint32_t>(TWH * kBN * e);
-    a.w_bytes = static_cast<uint32_t>(FW * kBN * e);
-    a.stage_stride = (a.x_bytes + a.w_bytes + 127u) & ~127u;
+    a.x_bytes = static_cast<uint32_t>(TWH * PITCH * e);
+    a.w_bytes = static_cast<uint32_t>(FW * PITCH * e);
+    // TMA writes shared memory at 128-byte aligned addresses: a stage and the filter row in
+    // it start on 128-byte boundaries (a staged pixel of a lane-group tail block holds only
+    // 32 or 64 bytes, so the input row's size need not be a multiple of 128)
+    a.w_off = (a.x_bytes + 127u) & ~127u;
+    a.stage_stride = (a.w_off + a.w_bytes + 127u) & ~127u;
     if (a.units == 0) return cudaSuccess;
 
-    auto kern = rows_kernel<T, FH, FW, R, TM, MINB, FLIP, P, SD, ACT, OutT>;
+    auto kern = rows_kernel<T, FH, FW, R, TM, MINB, FLIP, P, SD, ACT, OutT, G>;
     const int threads = (nwc + 1) * 32;
     static int regs = -1;  // per instantiation
     if (regs < 0) {
@@ -526,16 +547,44 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     return cudaGetLastError();
 }
 
+// Channel counts that are not a multiple of 64 (3x3, 5x5, 7x7, fp32 outputs): one launch
+// over the channels below the last multiple of 64, and one over the tail of at most 32
+// channels with 2 or 4 lane groups, so that the tail does not leave half the lanes idle.
+template <typename T, int F, int G>
+cudaError_t launch_rows_tail(const RowConv& p) {
+    using Tl = RowsTile<F, F>;
+    RowConv t = p;
+    t.c_lo = p.C / kBN * kBN;
+    return p.flip ? launch_rows_inst<T, F, F, Tl::R, Tl::TM, Tl::MINB, true, Pair64, 1, -1, float, G>(t)
+                  : launch_rows_inst<T, F, F, Tl::R, Tl::TM, Tl::MINB, false, Pair64, 1, -1, float, G>(t);
+}
+
+template <typename T, int F, class OutT>
+cudaError_t launch_rows_square(const RowConv& p) {
+    using Tl = RowsTile<F, F>;
+    if constexpr (F <= 7 && std::is_same<OutT, float>::value) {
+        const int rem = p.C % kBN;
+        if (rem != 0 && rem <= 32 && p.c_lo == 0 && p.c_hi < 0) {
+            if (p.C > kBN) {
+                RowConv q = p;
+                q.c_hi = p.C / kBN * kBN;
+                const cudaError_t err = launch_rows_square<T, F, OutT>(q);
+                if (err != cudaSuccess) return err;
+            }
+            return rem <= 16 ? launch_rows_tail<T, F, 4>(p) : launch_rows_tail<T, F, 2>(p);
+        }
+    }
+    return p.flip ? launch_rows_inst<T, F, F, Tl::R, Tl::TM, Tl::MINB, true, Pair64, 1, -1, OutT>(p)
+                  : launch_rows_inst<T, F, F, Tl::R, Tl::TM, Tl::MINB, false, Pair64, 1, -1, OutT>(p);
+}
+
 // Dispatch over the compiled odd square filter sizes.
 template <typename T, class OutT = float>
 cudaError_t launch_rows_dispatch(const RowConv& p) {
     if (p.FH != p.FW) return cudaErrorNotSupported;
-#define DWC_ROWS_CASE(F)                                                                     \
-    case F:                                                                                  \
-        return p.flip ? launch_rows_inst<T, F, F, RowsTile<F, F>::R, RowsTile<F, F>::TM,      \
-                                         RowsTile<F, F>::MINB, true, Pair64, 1, -1, OutT>(p) \
-                      : launch_rows_inst<T, F, F, RowsTile<F, F>::R, RowsTile<F, F>::TM,      \
-                                         RowsTile<F, F>::MINB, false, Pair64, 1, -1, OutT>(p);
+#define DWC_ROWS_CASE(F) \
+    case F:              \
+        return launch_rows_square<T, F, OutT>(p);
     switch (p.FH) {
         DWC_ROWS_CASE(3)
         DWC_ROWS_CASE(5)

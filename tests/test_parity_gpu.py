@@ -480,3 +480,18 @@ def random_cases(count=120, seed=20261203):
                          ids=lambda c: f"{c.dtype}_n{c.N}_{c.H}x{c.W}_c{c.C}_f{c.FH}x{c.FW}_s{c.stride}_p{c.pad}")
 def test_random_shapes_all_passes(case):
     check_full(case)
+
+
+# -- channel counts that are not a multiple of 64: the tail block on lane groups ----------
+
+TAILS = [C_(2, 13, 37, c, f) for c, f in
+         ((8, 3), (16, 5), (24, 7), (32, 3), (40, 5), (72, 7), (80, 3), (96, 5), (136, 7), (144, 3))]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", TAILS, ids=lambda c: f"c{c.C}_f{c.FH}")
+def test_channel_tail_lane_groups(case, dtype):
+    case = Case(**{**case.__dict__, "dtype": dtype})
+    if dtype != "f32" and case.C % 8:
+        pytest.skip("16-bit fast path needs C % 8 == 0")
+    check_full(case)
