@@ -234,6 +234,31 @@ def test_empty_batch():
     assert torch.all(dw == 0)
 
 
+def test_empty_batch_every_entry_point():
+    """N = 0 through the stride-2, stripe, fused and 16-bit-output paths: empty outputs and a
+    zero filter gradient, no launch errors."""
+    x = torch.zeros(0, 9, 9, 64, device="cuda", dtype=torch.bfloat16)
+    for (F, s) in ((3, 2), (7, 1)):
+        w = torch.randn(F, F, 64, device="cuda").bfloat16()
+        OH = (9 + 2 * ((F - 1) // 2) - F) // s + 1
+        y = dwc.fwd(x, w, s, (F - 1) // 2, out_dtype=torch.bfloat16)
+        dx = dwc.bwd_data(torch.zeros(0, OH, OH, 64, device="cuda").bfloat16(), w, (9, 9), s,
+                          (F - 1) // 2, out_dtype=torch.bfloat16)
+        dw = dwc.bwd_filter(x, torch.zeros(0, OH, OH, 64, device="cuda").bfloat16(), (F, F), s,
+                            (F - 1) // 2)
+        torch.cuda.synchronize()
+        assert y.shape == (0, OH, OH, 64) and dx.shape == (0, 9, 9, 64) and torch.all(dw == 0)
+    ws = torch.randn(7, 3, 64, device="cuda").bfloat16()       # stripe filter
+    dw = dwc.bwd_filter(x, torch.zeros(0, 5, 9, 64, device="cuda").bfloat16(), (7, 3), 1, 1)
+    y = dwc.fwd(x, ws, 1, 1)
+    prm = [torch.ones(64, device="cuda") for _ in range(4)]
+    yb = dwc.fwd_bn_act(torch.zeros(0, 9, 9, 64, device="cuda"), torch.randn(3, 3, 64, device="cuda"),
+                        *prm, 1e-5, "relu", 1, 1)
+    torch.cuda.synchronize()
+    assert torch.all(dw == 0) and y.shape == (0, 5, 9, 64) and yb.shape == (0, 9, 9, 64)
+    assert dwc.device_status() == 0
+
+
 # ---- full workload sizes: sampled outputs the oracle computes one by one ----------------
 
 def check_sampled(case: Case, passes, n_samples=2048, seed=0):
