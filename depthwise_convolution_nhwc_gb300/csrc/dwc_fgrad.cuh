@@ -101,7 +101,8 @@ struct FgradArgs {
     int rows_per_slice;    // flattened output rows per slice
     int nblocks, bps;      // U-wide column blocks per row, blocks per strip
     int nx, ny;            // ring slots for x rows and dy rows
-    uint32_t x_bytes, y_bytes;
+    uint32_t x_bytes, y_bytes;   // ring slot strides (multiples of 128 bytes)
+    uint32_t x_tx, y_tx;         // bytes one TMA box writes into a slot
     uint32_t y_off;        // byte offset of the dy ring after the x ring
 };
 
@@ -143,7 +144,9 @@ __device__ __forceinline__ void fgrad_row_s2(float2 (&acc)[RF][FW], const T* con
     }
 }
 
-template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
+// G: lane groups (1, or 2 / 4 when all channels fit in 32 / 16: each group of 32 / G lanes
+// covers them for its own column strip, so no lane idles).
+template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>, int G = 1>
 __global__ void __launch_bounds__((Tile::MAXCW + 1) * 32, Tile::MINB)
 fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
              const FgradArgs a) {
@@ -152,6 +155,9 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     constexpr int SD = Tile::SD;
     constexpr int FC = Tile::FWC;
     constexpr int NFC = Tile::NFC;
+    static_assert(G == 1 || (SD == 1 && (G == 2 || G == 4)), "lane groups at stride 1");
+    constexpr int PITCH = kBN / G;   // channels per staged pixel
+    constexpr int LPG = 32 / G;      // lanes per group
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* xfull = reinterpret_cast<uint64_t*>(smem);
     uint64_t* xempty = xfull + a.nx;
@@ -204,9 +210,9 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             if (xissued >= static_cast<uint32_t>(a.nx) && !mbar_wait(&xempty[xr.slot], xr.phase ^ 1u))
                 return false;
             if (xissued < static_cast<uint32_t>(a.nx)) ++xissued;
-            mbar_arrive_expect_tx(&xfull[xr.slot], a.x_bytes);
+            mbar_arrive_expect_tx(&xfull[xr.slot], a.x_tx);
             tma_load_4d(xring + static_cast<size_t>(xr.slot) * a.x_bytes, &xmap, &xfull[xr.slot],
-                        cb * kBN, ow_base * SD - a.pad, ih, n);
+                        cb * PITCH, ow_base * SD - a.pad, ih, n);
             xr.next(a.nx);
             return true;
         };
@@ -214,9 +220,9 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             if (yissued >= static_cast<uint32_t>(a.ny) && !mbar_wait(&yempty[yr.slot], yr.phase ^ 1u))
                 return false;
             if (yissued < static_cast<uint32_t>(a.ny)) ++yissued;
-            mbar_arrive_expect_tx(&yfull[yr.slot], a.y_bytes);
+            mbar_arrive_expect_tx(&yfull[yr.slot], a.y_tx);
             tma_load_4d(yring + static_cast<size_t>(yr.slot) * a.y_bytes, &ymap, &yfull[yr.slot],
-                        cb * kBN, ow_base, oh, n);
+                        cb * PITCH, ow_base, oh, n);
             yr.next(a.ny);
             return true;
         };
@@ -255,8 +261,10 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     const int wf = warp % a.nwf;
     const int fc = (warp / a.nwf) % NFC;           // tap chunk: taps fc*FC .. fc*FC + FC - 1
     const int wc = warp / (a.nwf * NFC);
+    const int lg = lane / LPG;                     // lane group: column strip wc * G + lg
+    const int cl = lane % LPG;                     // channel pair
     const int frow0 = wf * RF;                     // first owned row within the chunk
-    const int blk0 = wc * a.bps;
+    const int blk0 = (wc * G + lg) * a.bps;
     const int blk1 = std::min(blk0 + a.bps, a.nblocks);
 
     float2 acc[RF][FC];
@@ -300,14 +308,14 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             if (ok && !mbar_wait(&yfull[yr.slot], yr.phase)) ok = false;
             if (!ok) break;
 
-            const T* ys = reinterpret_cast<const T*>(yring + static_cast<size_t>(yr.slot) * a.y_bytes) + 2 * lane;
+            const T* ys = reinterpret_cast<const T*>(yring + static_cast<size_t>(yr.slot) * a.y_bytes) + 2 * cl;
             const T* xs[RF];
 #pragma unroll
             for (int f = 0; f < RF; ++f) {
                 uint32_t ph;
                 const uint32_t sl = xslot(static_cast<uint32_t>(frow0 + f), ph);
                 xs[f] = reinterpret_cast<const T*>(xring + static_cast<size_t>(sl) * a.x_bytes) +
-                        2 * lane + fc * FC * kBN;
+                        2 * cl + fc * FC * PITCH;
             }
             if constexpr (SD == 2) {
                 if (blk0 < blk1) fgrad_row_s2<T, FC, RF, U>(acc, xs, ys, blk0, blk1);
@@ -319,19 +327,19 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 for (int f = 0; f < RF; ++f)
 #pragma unroll
                     for (int m = 0; m < FC - 1; ++m)
-                        win[f][m] = Elem<T>::load_pair(xs[f] + (c0 + m) * kBN);
+                        win[f][m] = Elem<T>::load_pair(xs[f] + (c0 + m) * PITCH);
 #pragma unroll 1
                 for (int blk = blk0; blk < blk1; ++blk) {
                     const int cb0 = blk * U;
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
-                        const float2 g = Elem<T>::load_pair(ys + (cb0 + u) * kBN);
+                        const float2 g = Elem<T>::load_pair(ys + (cb0 + u) * PITCH);
 #pragma unroll
                         for (int f = 0; f < RF; ++f) {
                             // a row past the filter's last row (last chunk) computes from its
                             // staged window row like the others and is never written: no
                             // branch in this loop
-                            win[f][(u + FC - 1) % U] = Elem<T>::load_pair(xs[f] + (cb0 + u + FC - 1) * kBN);
+                            win[f][(u + FC - 1) % U] = Elem<T>::load_pair(xs[f] + (cb0 + u + FC - 1) * PITCH);
 #pragma unroll
                             for (int t = 0; t < FC; ++t) fma2(acc[f][t], win[f][(u + t) % U], g);
                         }
@@ -373,20 +381,23 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 #pragma unroll
         for (int t = 0; t < FC; ++t) mine[(f * FC + t) * 32 + lane] = acc[f][t];
     asm volatile("bar.sync 1, %0;" ::"r"(ncompute * 32) : "memory");
-    if (wc == 0) {
-        const int c = cb * kBN + 2 * lane;
+    if (wc == 0 && lg == 0) {
+        const int c = cb * PITCH + 2 * cl;
         for (int f = 0; f < RF; ++f) {
             const int fh = fh0 + frow0 + f;
             if (!live[f] || c >= a.C) continue;
             for (int t = 0; t < FC; ++t) {
                 const int fw = fc * FC + t;
                 if (fw >= FW) break;
-                const size_t off = static_cast<size_t>(wf * NFC + fc) * per_warp + (f * FC + t) * 32 + lane;
-                float2 s = red[off];
-                for (int k = 1; k < a.nwc; ++k) {
-                    const float2 v = red[static_cast<size_t>(k) * wslot * per_warp + off];
-                    s.x += v.x;
-                    s.y += v.y;
+                // column strips in a fixed order: warp strips k, lane groups g within
+                const size_t off = static_cast<size_t>(wf * NFC + fc) * per_warp + (f * FC + t) * 32 + cl;
+                float2 s = make_float2(0.f, 0.f);
+                for (int k = 0; k < a.nwc; ++k) {
+                    for (int g = 0; g < G; ++g) {
+                        const float2 v = red[static_cast<size_t>(k) * wslot * per_warp + off + g * LPG];
+                        s.x += v.x;
+                        s.y += v.y;
+                    }
                 }
                 float* dst = a.part + ((static_cast<size_t>(z * a.ncp + cp) * fhn + fh) * FW + fw) * a.C + c;
                 *reinterpret_cast<float2*>(dst) = s;
@@ -399,6 +410,7 @@ template <int FH, int FW, class Tile = FgradTile<FH, FW>>
 struct FgradPlan {
     int nwf, nwc, fhc, chunks, cblocks, Z, rows_per_slice, nblocks, bps, nx, ny;
     uint32_t x_bytes, y_bytes, y_off;
+    uint32_t x_tx, y_tx;   // bytes of one x / dy TMA box (the slots are these rounded to 128)
     size_t smem;
     int pwx, owp;
     int ncp, owpart;   // column parts per row and output columns per part
@@ -406,9 +418,10 @@ struct FgradPlan {
 
 // One candidate launch shape: the row cut into ncp column parts (one CTA each), with the
 // deepest lookahead between min_la output rows and the tile's that fits.
-template <typename T, int FH, int FW, class Tile>
+template <typename T, int FH, int FW, class Tile, int G = 1>
 bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
                       FgradPlan<FH, FW, Tile>& P, int fhr) {
+    constexpr int PITCH = kBN / G;
     const int e = static_cast<int>(sizeof(T));
     constexpr int RF = Tile::RF;
     const DeviceInfo& dev = device_info();
@@ -421,8 +434,11 @@ bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
     // (the last tap chunk may run past the filter's last tap: its x columns are staged too)
     P.pwx = Tile::SD * (P.owp - 1) + Tile::NFC * Tile::FWC;
     if (P.pwx > 256) return false;
-    P.x_bytes = static_cast<uint32_t>(P.pwx * kBN * e);
-    P.y_bytes = static_cast<uint32_t>(P.owp * kBN * e);
+    // TMA writes shared memory at 128-byte aligned addresses: ring slots are rounded up
+    P.x_tx = static_cast<uint32_t>(P.pwx * PITCH * e);
+    P.y_tx = static_cast<uint32_t>(P.owp * PITCH * e);
+    P.x_bytes = (P.x_tx + 127u) & ~127u;
+    P.y_bytes = (P.y_tx + 127u) & ~127u;
     // Filter-row groups per CTA (nwf, one warp each) and column strips (nwc): the x window of
     // nwf*RF rows must fit in shared memory; among the fitting choices take the one with the
     // most useful warp slots, counting warps up to 12 (about what hides the latencies of one
@@ -445,14 +461,15 @@ bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
         if (need(la) > smem_cap) continue;
         const int chunks = (groups + nwf - 1) / nwf;
         if ((groups + chunks - 1) / chunks != nwf) continue;  // same chunks, fewer warps: seen
-        const int nwc0 = std::max(1, std::min(Tile::MAXCW / (nwf * NFC), P.nblocks));
-        const int bps = (P.nblocks + nwc0 - 1) / nwc0;
-        const int nwc = (P.nblocks + bps - 1) / bps;
+        // column strips: G per warp (lane groups)
+        const int nwc0 = std::max(1, std::min(Tile::MAXCW / (nwf * NFC), (P.nblocks + G - 1) / G));
+        const int bps = (P.nblocks + nwc0 * G - 1) / (nwc0 * G);
+        const int nwc = (P.nblocks + bps * G - 1) / (bps * G);
         // the strip sums at the end reuse the ring: [nwc][nwf][NFC][RF][FWC][32] float2
         if (512 + static_cast<size_t>(nwc) * nwf * NFC * RF * Tile::FWC * 32 * sizeof(float2) > smem_cap)
             continue;
         const double useful = static_cast<double>(groups) / (chunks * nwf) *
-                              static_cast<double>(P.nblocks) / (nwc * bps);
+                              static_cast<double>(P.nblocks) / (nwc * G * bps);
         const double score = useful * std::min(nwf * NFC * nwc, 12) / (1.0 + 0.2 * chunks);
         if (score > best * (1.0 + 1e-9)) {
             best = score;
@@ -472,7 +489,7 @@ bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
     const size_t red = static_cast<size_t>(P.nwc) * P.nwf * NFC * RF * Tile::FWC * 32 * sizeof(float2);
     if (red > P.smem - 512) P.smem = 512 + red;
     P.y_off = static_cast<uint32_t>(P.nx) * P.x_bytes;
-    P.cblocks = (C + kBN - 1) / kBN;
+    P.cblocks = (C + PITCH - 1) / PITCH;
     const long long rows = static_cast<long long>(N) * OH;
     const long long per_z = static_cast<long long>(P.cblocks) * P.chunks * P.ncp;
     // One wave: every CTA runs the same number of rows, so a grid a few CTAs larger than
@@ -480,7 +497,7 @@ bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
     // filters up to 5 taps the capacity counts every CTA that shared memory, threads and
     // registers let an SM hold (measured faster there); larger filters keep one CTA per SM
     // (more, shorter slices measured slower from 7 taps on).
-    static const int regs = kernel_regs(fgrad_kernel<T, FH, FW, Tile>, 224);
+    static const int regs = kernel_regs(fgrad_kernel<T, FH, FW, Tile, G>, 224);
     const int ctas_per_sm = FW <= 5 ? std::max(Tile::MINB, resident_ctas(P.smem, (P.nwf * NFC * P.nwc + 1) * 32, regs))
                                     : Tile::MINB;
     long long Z = static_cast<long long>(dev.sm_count) * ctas_per_sm / per_z;
@@ -496,29 +513,30 @@ bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
 // filter rows per CTA timed faster than one row with more: 7x7 on 64x112x112x64, 177 against
 // 233 us), then the row cut into 2, 3 or 4 column parts (rows too wide for shared memory or
 // for one 256-column TMA box), each part a CTA of its own with its own partial-sum slot.
-template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
+template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>, int G = 1>
 bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P, int fhr = FH) {
     if (fhr < 1) return false;
     for (int ncp = 1; ncp <= 4; ++ncp) {
         if (ncp > 1 && (OW + ncp - 1) / ncp < Tile::U) break;
         if constexpr (Tile::SD > 1) {
-            if (fgrad_plan_parts<T, FH, FW, Tile>(N, OH, OW, C, ncp, 1, P, fhr)) return true;
+            if (fgrad_plan_parts<T, FH, FW, Tile, G>(N, OH, OW, C, ncp, 1, P, fhr)) return true;
         } else {
             for (int min_la : {Tile::NY, 2, 1})
                 if (min_la <= Tile::NY &&
-                    fgrad_plan_parts<T, FH, FW, Tile>(N, OH, OW, C, ncp, min_la, P, fhr))
+                    fgrad_plan_parts<T, FH, FW, Tile, G>(N, OH, OW, C, ncp, min_la, P, fhr))
                     return true;
         }
     }
     return false;
 }
 
-template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
+template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>, int G = 1>
 cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     const int e = static_cast<int>(sizeof(T));
     FgradPlan<FH, FW, Tile> P;
     const int fhr = FH > 0 ? FH : p.FH;
-    if (!fgrad_plan<T, FH, FW, Tile>(p.N, p.OH, p.OW, p.C, P, fhr)) return cudaErrorNotSupported;
+    constexpr int PITCH = kBN / G;
+    if (!fgrad_plan<T, FH, FW, Tile, G>(p.N, p.OH, p.OW, p.C, P, fhr)) return cudaErrorNotSupported;
     if (p.N == 0 || p.OH == 0 || p.OW == 0) {
         return cudaMemsetAsync(p.dw, 0, sizeof(float) * fhr * FW * p.C, p.stream);
     }
@@ -530,7 +548,7 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
         const cuuint64_t dims[4] = {(cuuint64_t)p.C, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.N};
         const cuuint64_t strides[3] = {(cuuint64_t)p.C * e, (cuuint64_t)p.W * p.C * e,
                                        (cuuint64_t)p.H * p.W * p.C * e};
-        const cuuint32_t box[4] = {(cuuint32_t)kBN, (cuuint32_t)P.pwx, 1u, 1u};
+        const cuuint32_t box[4] = {(cuuint32_t)PITCH, (cuuint32_t)P.pwx, 1u, 1u};
         if (encode_tiled(&xmap, Elem<T>::kTmaType, 4, const_cast<void*>(p.x), dims, strides, box) !=
             CUDA_SUCCESS)
             return cudaErrorNotSupported;
@@ -539,7 +557,7 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
         const cuuint64_t dims[4] = {(cuuint64_t)p.C, (cuuint64_t)p.OW, (cuuint64_t)p.OH, (cuuint64_t)p.N};
         const cuuint64_t strides[3] = {(cuuint64_t)p.C * e, (cuuint64_t)p.OW * p.C * e,
                                        (cuuint64_t)p.OH * p.OW * p.C * e};
-        const cuuint32_t box[4] = {(cuuint32_t)kBN, (cuuint32_t)P.owp, 1u, 1u};
+        const cuuint32_t box[4] = {(cuuint32_t)PITCH, (cuuint32_t)P.owp, 1u, 1u};
         if (encode_tiled(&ymap, Elem<T>::kTmaType, 4, const_cast<void*>(p.dy), dims, strides, box) !=
             CUDA_SUCCESS)
             return cudaErrorNotSupported;
@@ -553,8 +571,9 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     a.nwf = P.nwf; a.nwc = P.nwc; a.fhc = P.fhc; a.chunks = P.chunks; a.cblocks = P.cblocks;
     a.Z = P.Z; a.rows_per_slice = P.rows_per_slice; a.nblocks = P.nblocks; a.bps = P.bps;
     a.nx = P.nx; a.ny = P.ny; a.x_bytes = P.x_bytes; a.y_bytes = P.y_bytes; a.y_off = P.y_off;
+    a.x_tx = P.x_tx; a.y_tx = P.y_tx;
 
-    auto kern = fgrad_kernel<T, FH, FW, Tile>;
+    auto kern = fgrad_kernel<T, FH, FW, Tile, G>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -571,18 +590,38 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
                                 p.stream);
 }
 
-template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>>
+template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>, int G = 1>
 size_t fgrad_workspace_inst(int N, int OH, int OW, int C, int fhr = FH) {
     FgradPlan<FH, FW, Tile> P;
-    if (!fgrad_plan<T, FH, FW, Tile>(N, OH, OW, C, P, fhr)) return 0;
+    if (!fgrad_plan<T, FH, FW, Tile, G>(N, OH, OW, C, P, fhr)) return 0;
     return static_cast<size_t>(P.Z) * P.ncp * fhr * FW * static_cast<size_t>(C);
+}
+
+// 3x3, 5x5 and 7x7 with at most 32 (16) channels: 2 (4) lane groups, so that the single
+// partial channel block does not leave half the lanes idle.
+template <typename T, int F, class Tile>
+cudaError_t launch_fgrad_grouped(const FilterGrad& p) {
+    if constexpr (F <= 7) {
+        if (p.C <= 16) return launch_fgrad_inst<T, F, F, Tile, 4>(p);
+        if (p.C <= 32) return launch_fgrad_inst<T, F, F, Tile, 2>(p);
+    }
+    return launch_fgrad_inst<T, F, F, Tile>(p);
+}
+
+template <typename T, int F, class Tile>
+size_t fgrad_workspace_grouped(int N, int OH, int OW, int C) {
+    if constexpr (F <= 7) {
+        if (C <= 16) return fgrad_workspace_inst<T, F, F, Tile, 4>(N, OH, OW, C);
+        if (C <= 32) return fgrad_workspace_inst<T, F, F, Tile, 2>(N, OH, OW, C);
+    }
+    return fgrad_workspace_inst<T, F, F, Tile>(N, OH, OW, C);
 }
 
 // Workspace of the launch that launch_fgrad_dispatch makes for this problem.
 template <typename T, int F>
 size_t fgrad_workspace_dispatch(int N, int OH, int OW, int C) {
-    return fgrad_use_alt_period<F>(OW) ? fgrad_workspace_inst<T, F, F, FgradAltTile<F>>(N, OH, OW, C)
-                                       : fgrad_workspace_inst<T, F, F>(N, OH, OW, C);
+    return fgrad_use_alt_period<F>(OW) ? fgrad_workspace_grouped<T, F, FgradAltTile<F>>(N, OH, OW, C)
+                                       : fgrad_workspace_grouped<T, F, FgradTile<F, F>>(N, OH, OW, C);
 }
 
 #define DWC_FGRAD_FILTERS(X) X(3) X(5) X(7) X(9) X(11) X(13) X(15) X(17) X(19) X(21) X(23) X(25) X(27) X(29) X(31)
@@ -656,8 +695,8 @@ cudaError_t launch_fgrad_dispatch(const FilterGrad& p) {
 #define DWC_FGRAD_CASE(F)                                          \
     case F:                                                        \
         return fgrad_use_alt_period<F>(p.OW)                       \
-                   ? launch_fgrad_inst<T, F, F, FgradAltTile<F>>(p) \
-                   : launch_fgrad_inst<T, F, F>(p);
+                   ? launch_fgrad_grouped<T, F, FgradAltTile<F>>(p) \
+                   : launch_fgrad_grouped<T, F, FgradTile<F, F>>(p);
         DWC_FGRAD_FILTERS(DWC_FGRAD_CASE)
 #undef DWC_FGRAD_CASE
 #define DWC_FGRAD_BIG_CASE(F)                                             \
