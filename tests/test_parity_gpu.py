@@ -133,6 +133,8 @@ STRIDE2 = [
     C_(1, 30, 31, 64, 7, s=2, p=2),
     C_(6, 40, 40, 24, 3, s=2),        # many slices, C not a multiple of the channel block
     C_(1, 5, 5, 16, 7, s=2, p=3),     # map smaller than the filter
+    C_(2, 21, 27, 144, 3, s=2),       # channel tails on lane groups (16 and 40 channels)
+    C_(1, 20, 33, 40, 5, s=2),
 ]
 
 
