@@ -306,6 +306,33 @@ def test_fwd_bn_act_sampled_equals_full():
                           full.ravel()[idx])
 
 
+def _random_shapes(count=40, seed=77):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        FH, FW = int(rng.integers(1, 8)), int(rng.integers(1, 8))
+        s, p = int(rng.integers(1, 4)), int(rng.integers(0, max(FH, FW)))
+        H, W = int(rng.integers(1, 12)), int(rng.integers(1, 12))
+        if oracle.out_dim(H, FH, s, p) < 1 or oracle.out_dim(W, FW, s, p) < 1:
+            continue
+        out.append((int(rng.integers(1, 3)), H, W, int(rng.integers(1, 5)), FH, FW, s, p))
+    return out
+
+
+@pytest.mark.parametrize("shape", _random_shapes())
+def test_random_shapes_match_torch_fp64(shape):
+    """Seeded random problems (any filter 1..7 x 1..7, strides 1-3, pads 0..F-1): all three
+    passes against torch's fp64 grouped conv2d and its autograd gradients."""
+    N, H, W, C, FH, FW, s, p = shape
+    x, w = rand(N, H, W, C), rand(FH, FW, C)
+    y = oracle.fwd(x, w, s, p)
+    assert y.shape == torch_fwd(x, w, s, p).shape and rel_err(y, torch_fwd(x, w, s, p)) <= 1e-12
+    dy = rand(*y.shape)
+    dx_ref, dw_ref = torch_grads(x, w, dy, s, p)
+    assert rel_err(oracle.bwd_data(dy, w, (H, W), s, p), dx_ref) <= 1e-12
+    assert rel_err(oracle.bwd_filter(x, dy, (FH, FW), s, p), dw_ref) <= 1e-12
+
+
 def test_out_dim_and_empty_outputs():
     assert oracle.out_dim(56, 7, 1, 3) == 56
     assert oracle.out_dim(56, 31, 1, 15) == 56
