@@ -15,8 +15,6 @@ namespace dwc {
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 // Status word the kernels set when a wait runs out of time (one per device, in this
 // module's global memory; its address is looked up once per device).
 __device__ unsigned int g_status_word;
@@ -391,6 +389,27 @@ dwc_status_t dwc_bwd_data(const void* dy, const void* w, float* dx, int N, int H
                           dwc_stream_t stream) {
     return bwd_data_impl(dy, w, dx, N, H, W, C, FH, FW, stride, pad, dtype, DWC_F32, stream);
 }
+
+}  // extern "C"
+
+namespace dwc {
+
+// The argument and pointer checks of dwc_bwd_filter (without the workspace ones), for the
+// entry points that supply the workspace themselves.
+int validate_bwd_filter(const void* x, const void* dy, const float* dw, int N, int H, int W,
+                        int C, int FH, int FW, int stride, int pad, int dtype) {
+    Problem P;
+    const dwc_status_t st = check_problem(N, H, W, C, FH, FW, stride, pad,
+                                          static_cast<dwc_dtype_t>(dtype), P);
+    if (st != DWC_OK) return st;
+    return check_pointers(P, x, static_cast<long long>(N) * H * W * C, dy,
+                          static_cast<long long>(N) * P.OH * P.OW * C, dw,
+                          static_cast<long long>(FH) * FW * C);
+}
+
+}  // namespace dwc
+
+extern "C" {
 
 size_t dwc_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int FW, int stride,
                                      int pad, dwc_dtype_t dtype) {

@@ -6,11 +6,15 @@
 // and winds down instead of spinning forever.
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include "dwc_host.h"
 
 namespace dwc {
 
@@ -248,6 +252,28 @@ __device__ __forceinline__ void store_out(__half* p, float v) { *p = __float2hal
 
 
 // ------------------------------------------------------------------ host-side occupancy
+
+// Once-only flags of one kernel, one per device: cudaFuncSetAttribute applies to the current
+// device only, so a process that uses several GPUs opts a kernel in on each of them.
+struct DeviceOnce {
+    std::atomic<bool> done[kMaxDevices] = {};
+};
+
+// Let `kern` use the device's whole opt-in shared memory on the current device (once per
+// device; a failed attempt is retried at the next launch).  `once` belongs to the kernel:
+// instantiations of one kernel template share a function type, so the caller keeps one
+// DeviceOnce per instantiation (a function-local static next to the launch).
+template <class K>
+cudaError_t opt_in_smem(K kern, DeviceOnce& once, int max_smem_optin) {
+    int d = 0;
+    cudaError_t err = cudaGetDevice(&d);
+    if (err != cudaSuccess) return err;
+    const bool tracked = d >= 0 && d < kMaxDevices;
+    if (tracked && once.done[d].load(std::memory_order_acquire)) return cudaSuccess;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin);
+    if (err == cudaSuccess && tracked) once.done[d].store(true, std::memory_order_release);
+    return err;
+}
 
 // Registers per thread of a kernel (allocation granularity of 8), or `fallback` when the
 // runtime cannot say (no device).

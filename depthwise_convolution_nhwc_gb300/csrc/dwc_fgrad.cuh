@@ -574,12 +574,10 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     a.x_tx = P.x_tx; a.y_tx = P.y_tx;
 
     auto kern = fgrad_kernel<T, FH, FW, Tile, G>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               device_info().max_smem_optin);
+    static DeviceOnce smem_opt_in;
+    {
+        const cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
         if (err != cudaSuccess) return err;
-        attr_set = true;
     }
     const int threads = (P.nwf * Tile::NFC * P.nwc + 1) * 32;
     const unsigned grid = static_cast<unsigned>(P.Z) * P.ncp * P.cblocks * P.chunks;

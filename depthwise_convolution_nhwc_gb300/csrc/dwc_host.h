@@ -10,6 +10,9 @@ namespace dwc {
 
 enum ElemType { kF32 = 0, kBF16 = 1, kF16 = 2 };
 
+// Devices a process may use with this library (per-device state is kept in fixed tables).
+constexpr int kMaxDevices = 64;
+
 inline int elem_bytes(int t) { return t == kF32 ? 4 : 2; }
 
 // One stride-1 convolution over channels-last tensors, as the row-streaming kernel sees it:
@@ -179,6 +182,11 @@ size_t small_fgrad_workspace_floats_f16(int N, int H, int W, int C, int OH, int 
 // CUDA-core ones (forward / backward data as the RowConv describes it; filter gradient).
 bool tensor_core_rows(const RowConv& p);
 bool tensor_core_fgrad(int N, int C, int OH, int OW, int FH, int FW);
+
+// The argument and pointer checks of dwc_bwd_filter without its workspace checks; returns a
+// dwc_status_t value (0 = DWC_OK).
+int validate_bwd_filter(const void* x, const void* dy, const float* dw, int N, int H, int W,
+                        int C, int FH, int FW, int stride, int pad, int dtype);
 
 // Fallback kernels.
 cudaError_t launch_general_fwd(const GeneralConv& p);

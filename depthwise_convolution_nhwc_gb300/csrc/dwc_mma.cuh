@@ -320,12 +320,10 @@ cudaError_t launch_mma_inst(const RowConv& p) {
     a.FH = p.FH; a.FW = p.FW; a.pad_h = p.pad_h; a.pad_w = p.pad_w;
     if (a.units == 0) return cudaSuccess;
     auto kern = mma_rows_kernel<T, FLIP, OutT>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               device_info().max_smem_optin);
+    static DeviceOnce smem_opt_in;
+    {
+        const cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
         if (err != cudaSuccess) return err;
-        attr = true;
     }
     const int ctas = smem * 2 + 2048 <= 233472u ? 2 : 1;
     const long long grid = std::min<long long>(a.units, static_cast<long long>(device_info().sm_count) * ctas);

@@ -255,12 +255,10 @@ cudaError_t launch_mma_fgrad(const FilterGrad& p) {
     a.N = p.N; a.H = p.H; a.W = p.W; a.C = p.C; a.OH = p.OH; a.OW = p.OW;
     a.FH = p.FH; a.FW = p.FW; a.pad = p.pad;
     auto kern = mma_fgrad_kernel<T>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               device_info().max_smem_optin);
+    static DeviceOnce smem_opt_in;
+    {
+        const cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
         if (err != cudaSuccess) return err;
-        attr = true;
     }
     const unsigned grid = static_cast<unsigned>(a.Z) * static_cast<unsigned>(p.C / kMmaCB);
     kern<<<grid, kMmaWarps * 32, smem, p.stream>>>(a);

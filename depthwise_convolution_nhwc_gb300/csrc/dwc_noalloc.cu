@@ -40,7 +40,10 @@ float* scratch_for_current_device() {
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_scratch_ptr[d] == nullptr) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            (void)cudaGetLastError();  // the next call's launch check must not see this failure
+            return nullptr;
+        }
         g_scratch_ptr[d] = static_cast<float*>(p);
     }
     return g_scratch_ptr[d];
@@ -51,9 +54,13 @@ float* scratch_for_current_device() {
 extern "C" dwc_status_t dwc_bwd_filter_noalloc(const void* x, const void* dy, float* dw, int N,
                                                int H, int W, int C, int FH, int FW, int stride,
                                                int pad, dwc_dtype_t dtype, dwc_stream_t stream) {
-    // 0 means invalid arguments or an empty filter: dwc_bwd_filter reports those itself
+    // argument and pointer errors first, exactly as dwc_bwd_filter reports them; only a
+    // valid call that does not fit the fixed array is DWC_ERR_UNSUPPORTED
+    const int st = dwc::validate_bwd_filter(x, dy, dw, N, H, W, C, FH, FW, stride, pad,
+                                            static_cast<int>(dtype));
+    if (st != DWC_OK) return static_cast<dwc_status_t>(st);
     const size_t need = dwc_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, pad, dtype);
-    if (need == 0)
+    if (need == 0)  // empty problems and shapes that need no workspace
         return dwc_bwd_filter(x, dy, dw, N, H, W, C, FH, FW, stride, pad, dtype, nullptr, 0,
                               stream);
     if (need > kScratchFloats * sizeof(float)) return DWC_ERR_UNSUPPORTED;

@@ -520,14 +520,16 @@ cudaError_t launch_rows_inst(const RowConv& p) {
 
     auto kern = rows_kernel<T, FH, FW, R, TM, MINB, FLIP, P, SD, ACT, OutT, G>;
     const int threads = (nwc + 1) * 32;
-    static int regs = -1;  // per instantiation
+    static int regs = -1;  // per instantiation (the same code on every device)
     if (regs < 0) {
         cudaFuncAttributes fa;
-        cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+        const cudaError_t err = cudaFuncGetAttributes(&fa, kern);
         if (err != cudaSuccess) return err;
         regs = fa.numRegs;
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   dev.max_smem_optin);
+    }
+    static DeviceOnce smem_opt_in;
+    {
+        const cudaError_t err = opt_in_smem(kern, smem_opt_in, dev.max_smem_optin);
         if (err != cudaSuccess) return err;
     }
     // CTAs per SM allowed by registers, then split shared memory between them.

@@ -432,12 +432,10 @@ cudaError_t launch_small_rows_inst(const RowConv& p) {
     // fewer CTAs with more units each was faster on the stage shapes than two per SM
     const int per_sm = 1;
     const long long grid = std::min<long long>(units, static_cast<long long>(device_info().sm_count) * per_sm);
-    static bool attr = false;
-    if (!attr) {
-        const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     device_info().max_smem_optin);
+    static DeviceOnce smem_opt_in;
+    {
+        const cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
         if (err != cudaSuccess) return err;
-        attr = true;
     }
     kern<<<static_cast<unsigned>(grid), nwarps * 32, smem, p.stream>>>(a);
     return cudaGetLastError();
@@ -489,12 +487,10 @@ cudaError_t launch_small_fgrad_inst(const FilterGrad& p) {
     a.N = p.N; a.H = p.H; a.W = p.W; a.C = p.C; a.OH = p.OH; a.OW = p.OW;
     a.FH = p.FH; a.FW = p.FW; a.pad_h = p.pad; a.pad_w = p.pad;
     auto kern = small_fgrad_kernel<T, MAXW, DR>;
-    static bool attr = false;
-    if (!attr) {
-        const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     device_info().max_smem_optin);
+    static DeviceOnce smem_opt_in;
+    {
+        const cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
         if (err != cudaSuccess) return err;
-        attr = true;
     }
     const unsigned grid = static_cast<unsigned>(Z) * a.cblocks;
     kern<<<grid, nwarps * 32, smem, p.stream>>>(a);

@@ -164,14 +164,18 @@ dwc_status_t dwc_bwd_filter(const void* x, const void* dy, float* dw,
  * device code is loaded there (at the latest by the first call of this function on that
  * GPU) and stays reserved until the process exits.  A problem whose
  * dwc_bwd_filter_workspace_size() exceeds 32 MiB is rejected with DWC_ERR_UNSUPPORTED
- * before anything is launched (every benchmark shape of this library fits).
+ * before anything is launched (every benchmark shape of this library fits); argument and
+ * pointer errors are reported first, as dwc_bwd_filter reports them.
  *
  * Set-up: the first call on each device looks up the array's device address with that
  * device current (cudaGetSymbolAddress); make that first call before any stream capture.
  * Sharing: all calls use the same array and leave their partial sums in it; nothing in it
  * needs to start at zero.  Calls whose kernels overlap on the GPU (e.g. on two unordered
  * streams) race on the array: order them on one stream or with events.  The call itself
- * allocates and frees nothing. */
+ * allocates and frees nothing.
+ * Check dwc_device_status() before trusting dW: a kernel whose bounded wait ran out leaves
+ * some partial sums unwritten, and the final sum then adds an earlier call's leftovers, so
+ * dW can look finite and plausible although it is wrong. */
 dwc_status_t dwc_bwd_filter_noalloc(const void* x, const void* dy, float* dw,
                                     int N, int H, int W, int C, int FH, int FW, int stride,
                                     int pad, dwc_dtype_t dtype, dwc_stream_t stream);
