@@ -81,6 +81,9 @@ def parse_args():
                          "down-sampling shapes, or 41 and 51 taps over the stage shapes")
     ap.add_argument("--sweep-steps", type=int, default=20)
     ap.add_argument("--sweep-md", metavar="FILE", help="also write the sweep as a markdown table")
+    ap.add_argument("--no-per-filter", action="store_true",
+                    help="skip the per-filter-size table of the default line")
+    ap.add_argument("--per-filter-steps", type=int, default=5)
     return ap.parse_args()
 
 
@@ -344,12 +347,169 @@ def load_traffic(kernel_key):
     return ent.get("bytes_per_launch")
 
 
+def measure_alu_peaks(dev):
+    """Multiply-add rates of the CUDA cores measured in this run with the library's
+    microbenchmark (dwc_fma_rate_probe): 8 CTAs of 256 threads per SM, 8 independent chains
+    per thread, best of 3 launches timed with CUDA events.  TFLOP/s for each instruction kind
+    (a multiply-add is 2 FLOPs); "ffma2" (packed fp32x2) is the fp32 peak the CUDA-core
+    kernels are measured against."""
+    import torch
+    import depthwise_convolution_nhwc_gb300 as dwc
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = 8 * sms, 1024
+    out = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for kind, lanes in (("ffma", 1), ("ffma2", 2), ("hfma2", 2), ("bf16x2", 2)):
+        dwc.fma_rate_probe(kind, blocks, iters, out)
+        best = None
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dwc.fma_rate_probe(kind, blocks, iters, out)
+            e1.record(stream)
+            e1.synchronize()
+            t = e0.elapsed_time(e1) * 1e-3
+            best = t if best is None else min(best, t)
+        res[kind] = 2.0 * blocks * 256 * iters * 8 * lanes / best / 1e12
+    return {"tflops": res, "sms": sms, "launch": f"{blocks} CTAs x 256 threads x {iters} "
+            "iterations x 8 chains, best of 3, CUDA events"}
+
+
+def measure_link_rates(dev, nbytes):
+    """Standalone pinned host-to-device and device-to-host copy rates (GB/s) of a buffer of
+    `nbytes`, best of 3, each direction alone, CUDA events on one stream."""
+    import torch
+    n = max(1, nbytes // 4)
+    h = torch.empty(n, dtype=torch.float32).pin_memory()
+    d = torch.empty(n, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    rates = {}
+    for name, fn in (("h2d_gbs", lambda: d.copy_(h, non_blocking=True)),
+                     ("d2h_gbs", lambda: h.copy_(d, non_blocking=True))):
+        fn()
+        best = None
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            t = e0.elapsed_time(e1) * 1e-3
+            best = t if best is None else min(best, t)
+        rates[name] = 4 * n / best / 1e9
+    return rates
+
+
+def gpu_local_cpus(dev):
+    """CPUs the kernel lists as local to the GPU's PCI function (None if unknown)."""
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    try:
+        bus = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        txt = open(f"/sys/bus/pci/devices/{bus}/local_cpulist").read().strip()
+    except (AttributeError, OSError):
+        return None
+    cpus = set()
+    for part in txt.split(","):
+        if "-" in part:
+            lo, hi = part.split("-")
+            cpus.update(range(int(lo), int(hi) + 1))
+        elif part:
+            cpus.add(int(part))
+    allowed = os.sched_getaffinity(0)
+    return sorted(cpus & allowed) or None
+
+
+def per_filter_table(args, dev, peaks):
+    """Every pass of every sweep filter size on the first stage shape (N=64, 56x56, C=128,
+    pad (F-1)/2), fp32 and bf16 inputs: mean device time of --per-filter-steps launches
+    (L2 flushed before each, 2 warm-up launches) and the roofline fraction of the pass.  x
+    and dy are drawn once per dtype (they do not depend on F); W per filter size."""
+    import torch
+    import depthwise_convolution_nhwc_gb300 as dwc
+    from depthwise_convolution_nhwc_gb300 import roofline as rl
+    from depthwise_convolution_nhwc_gb300.inputs import SWEEP_FILTERS, SWEEP_SHAPES, Case
+    N, H, W, C = SWEEP_SHAPES[0]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    ab = {0: "gen", 1: "cc", 2: "tc", 3: "sm"}
+    points = []
+    for dt in ("f32", "bf16"):
+        base = Case(N, H, W, C, 3, 3, 1, 1, dt, "normal", 900)
+        x, dy = base.x().to(dev), base.dy().to(dev)
+        y = torch.empty((N, H, W, C), device=dev, dtype=torch.float32)
+        dx = torch.empty_like(y)
+        for F in SWEEP_FILTERS:
+            case = Case(N, H, W, C, F, F, 1, (F - 1) // 2, dt, "normal", 900)
+            w = case.w().to(dev)
+            dw = torch.empty((F, F, C), device=dev, dtype=torch.float32)
+            ws = dwc.workspace(dwc.bwd_filter_workspace_size(x.shape, (F, F), 1, case.pad,
+                                                             x.dtype), dev)
+            run = {"fwd": lambda: dwc.fwd(x, w, 1, case.pad, out=y),
+                   "bwd_data": lambda: dwc.bwd_data(dy, w, (H, W), 1, case.pad, out=dx),
+                   "bwd_filter": lambda: dwc.bwd_filter(x, dy, (F, F), 1, case.pad, out=dw,
+                                                        ws=ws)}
+            pt = {"dtype": dt, "F": F}
+            fams = []
+            for name in PASSES_ALL:
+                for _ in range(2):
+                    run[name]()
+                evs = []
+                for k in range(args.per_filter_steps):
+                    flush.fill_(float(k))
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    run[name]()
+                    e1.record(stream)
+                    evs.append((e0, e1))
+                torch.cuda.synchronize()
+                t = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e-3
+                fam = kernel_family(dwc, case, name)
+                tr, bound = rl.roofline_time_s(case, name, peaks, tensor=fam == 2)
+                pt[name] = {"us": round(t * 1e6, 2), "frac": round(tr / t, 3), "bound": bound,
+                            "tflops": round(rl.nominal_flops(case) / t / 1e12, 2)}
+                fams.append(ab[fam])
+            pt["families"] = "/".join(fams)
+            points.append(pt)
+    if dwc.device_status() != 0:
+        raise SystemExit("a kernel reported a timed-out wait in the per-filter table")
+    return {"workload": f"N={N} {H}x{W} C={C}, F x F filters, pad (F-1)/2, stride 1",
+            "timing": f"mean of {args.per_filter_steps} launches per pass, L2 flushed before "
+                      "each, CUDA events",
+            "frac": "roofline fraction of the pass (hbm: compulsory bytes at the measured HBM "
+                    "copy rate; alu: valid FLOPs at the measured fp32x2 FMA rate; tensor: "
+                    "valid FLOPs at the measured bf16 peak)",
+            "families": "fwd/bwd_data/bwd_filter kernel family: cc CUDA-core, tc tensor-core, "
+                        "sm small-map, gen general",
+            "points": points}
+
+
 def run_e2e(args, case, passes, x, w, dy, ws, world, flops_step):
     """Same step through the public API with every step's inputs copied from pinned host
     memory and its outputs copied back, inside the timed region.  Steps are pipelined over
     two device buffer sets and three streams (host-to-device copies, kernels, device-to-host
     copies), ordered by events, so that one step's copies overlap another step's kernels;
     every step still moves all of its own bytes."""
+    import torch
+    import depthwise_convolution_nhwc_gb300 as dwc
+    dev = x.device
+    # pinned buffers on the GPU's own NUMA node: allocate (first touch) from its local CPUs
+    old_aff = os.sched_getaffinity(0)
+    local = gpu_local_cpus(dev)
+    if local:
+        os.sched_setaffinity(0, local)
+    try:
+        out = _run_e2e_pinned(args, case, passes, x, w, dy, ws, world, flops_step)
+    finally:
+        os.sched_setaffinity(0, old_aff)
+    out[-1]["host_cpus"] = (f"{len(local)} CPUs local to the GPU" if local
+                            else "process affinity unchanged (GPU-local CPUs unknown)")
+    return out
+
+
+def _run_e2e_pinned(args, case, passes, x, w, dy, ws, world, flops_step):
     import torch
     import depthwise_convolution_nhwc_gb300 as dwc
     dev = x.device
@@ -421,7 +581,11 @@ def run_e2e(args, case, passes, x, w, dy, ws, world, flops_step):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t.item())
     e2e_value = world * args.e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
-    return e2e_value, h2d, d2h, e2e_ms / args.e2e_steps
+    link = measure_link_rates(dev, max(h2d, d2h))
+    # the copies of one step cannot take less than the slower direction alone
+    link["copy_bound_ms_per_step"] = max(h2d / (link["h2d_gbs"] * 1e9),
+                                         d2h / (link["d2h_gbs"] * 1e9)) * 1e3
+    return e2e_value, h2d, d2h, e2e_ms / args.e2e_steps, link
 
 
 def roofline_entry(rl, case, pass_name, family, seconds, peaks):
@@ -441,7 +605,9 @@ def roofline_entry(rl, case, pass_name, family, seconds, peaks):
     else:
         achieved = rl.valid_flops(case) / seconds / 1e12
         peak, unit = peaks["fp32_tflops"], "TFLOP/s"
-        src = "fp32 FFMA peak derived: 152 SMs x 128 lanes x 2 x 2070 MHz"
+        src = ("measured fp32x2 FMA rate (dwc_fma_rate_probe, all SMs, this run)"
+               if peaks.get("fp32_source") == "measured"
+               else "fp32 FMA peak derived: SMs x 128 lanes x 2 x 2070 MHz")
     return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "traffic": None,
             "kernel": kernel_name(case, pass_name, family), "pass": pass_name,
@@ -462,7 +628,8 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     dwc.load_library()
     stream = torch.cuda.current_stream()
-    peaks = rl.load_peaks()
+    alu = measure_alu_peaks(dev)
+    peaks = rl.load_peaks(fp32_tflops=alu["tflops"]["ffma2"])
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     rows = []
     cases = {"stride1": sweep_cases, "stride2": stride2_cases,
@@ -520,7 +687,8 @@ def write_sweep_md(args, rows):
            "launching stream, 256 MiB L2 flush before each launch, 3 warm-up launches). "
            "TFLOP/s are nominal (2·N·OH·OW·C·FH·FW); roofline fraction against the bound "
            "named (hbm: compulsory bytes at the measured HBM copy rate; alu: valid FLOPs at "
-           "the derived fp32 FFMA peak; tensor: valid FLOPs at the measured bf16 peak). "
+           "the fp32x2 FMA rate measured in the same run; tensor: valid FLOPs at the measured "
+           "bf16 peak). "
            "Kernel family: cc = CUDA-core row / filter-gradient kernels, tc = tensor-core, "
            "sm = small-map kernels.  BN+ReLU: the fused batch-norm + ReLU + forward pass "
            "(filters up to 7 taps).\n",
@@ -555,6 +723,8 @@ def run_ours(args, case, passes):
     dev = torch.device("cuda", torch.cuda.current_device())
     dwc.load_library()
     stream = torch.cuda.current_stream()
+    alu = measure_alu_peaks(dev)
+    peaks = rl.load_peaks(fp32_tflops=alu["tflops"]["ffma2"])
 
     x, w, dy = (t.to(dev) for t in (case.x(), case.w(), case.dy()))
     y = torch.empty((case.N, case.OH, case.OW, case.C), device=dev, dtype=torch.float32)
@@ -615,9 +785,10 @@ def run_ours(args, case, passes):
     flops_step = rl.nominal_flops(case) * len(passes)
     value = world * args.steps * flops_step / (total_ms * 1e-3) / 1e12
 
-    e2e_value, h2d, d2h, e2e_step_ms = None, 0, 0, None
+    e2e_value, h2d, d2h, e2e_step_ms, link = None, 0, 0, None, None
     if args.e2e_steps > 0:
-        e2e_value, h2d, d2h, e2e_step_ms = run_e2e(args, case, passes, x, w, dy, ws, world, flops_step)
+        e2e_value, h2d, d2h, e2e_step_ms, link = run_e2e(args, case, passes, x, w, dy, ws, world,
+                                                         flops_step)
 
     if rank != 0:
         if world > 1:
@@ -625,7 +796,6 @@ def run_ours(args, case, passes):
         return
 
     # --- roofline of the dominant kernel ----------------------------------------------
-    peaks = rl.load_peaks()
     fam = {n: kernel_family(dwc, case, n) for n in passes}
     mean_ms = {n: statistics.fmean(v) for n, v in per_pass.items()}
     dom = max(mean_ms, key=mean_ms.get)
@@ -651,11 +821,15 @@ def run_ours(args, case, passes):
             "e2e": ({"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                      "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": e2e_step_ms,
                      "pipelining": "two buffer sets; host-to-device copies, kernels and "
-                                   "device-to-host copies on three streams ordered by events"}
+                                   "device-to-host copies on three streams ordered by events",
+                     "link": link}
                     if e2e_value is not None else None),
+            "alu_peaks": alu,
             "gpu_launches": args.steps * sum(LAUNCHES[n] for n in passes),
             "kernels": {n: kernel_name(case, n, fam[n]) for n in passes},
             "clocks": clocks}
+    if not args.no_per_filter and world == 1:
+        line["per_filter"] = per_filter_table(args, dev, peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(case, passes, args.cpu_seconds)
     print(json.dumps(line), flush=True)

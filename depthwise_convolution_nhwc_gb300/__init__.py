@@ -30,10 +30,12 @@ STATUS = {0: "DWC_OK", 1: "DWC_ERR_INVALID_ARG", 2: "DWC_ERR_UNSUPPORTED",
           3: "DWC_ERR_ALIGNMENT", 4: "DWC_ERR_WORKSPACE", 5: "DWC_ERR_CUDA",
           6: "DWC_ERR_TIMEOUT"}
 
-# Every symbol include/dwc.h declares (checked by the tests).
-EXPORTS = ("dwc_fwd", "dwc_fwd_ex", "dwc_fwd_bn_act", "dwc_bwd_data", "dwc_bwd_data_ex", "dwc_bwd_filter_workspace_size", "dwc_bwd_filter",
-           "dwc_bwd_filter_noalloc", "dwc_device_status", "dwc_status_string", "dwc_version",
-           "dwc_path")
+# Every symbol include/*.h declares (checked by the tests).
+EXPORTS = ("dwc_fwd", "dwc_fwd_ex", "dwc_fwd_bn_act", "dwc_bwd_data", "dwc_bwd_data_ex",
+           "dwc_bwd_filter_workspace_size", "dwc_bwd_filter", "dwc_bwd_filter_noalloc",
+           "dwc_device_status", "dwc_set_wait_limit_ns", "dwc_fma_rate_probe",
+           "dwc_status_string", "dwc_version", "dwc_path", "dwc_testing_stall_next_row_launch")
+FMA_KINDS = {"ffma": 0, "ffma2": 1, "hfma2": 2, "bf16x2": 3}  # dwc_fma_rate_probe kinds
 
 _lock = threading.Lock()
 _lib = None
@@ -89,6 +91,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.dwc_version.restype = i
         lib.dwc_path.argtypes = [i, vp, vp, vp] + shape + [i]
         lib.dwc_path.restype = i
+        lib.dwc_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        lib.dwc_set_wait_limit_ns.restype = ctypes.c_ulonglong
+        lib.dwc_fma_rate_probe.argtypes = [i, i, i, vp, vp]
+        lib.dwc_fma_rate_probe.restype = i
+        lib.dwc_testing_stall_next_row_launch.argtypes = []
+        lib.dwc_testing_stall_next_row_launch.restype = None
         if path is None:
             _lib = lib
         return lib
@@ -248,6 +256,22 @@ def device_status(stream=None) -> int:
     return int(load_library().dwc_device_status(_stream_ptr(stream)))
 
 
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of every wait inside kernels launched from now on (0: the 2 s default); returns
+    the previous setting."""
+    return int(load_library().dwc_set_wait_limit_ns(int(ns)))
+
+
+def fma_rate_probe(kind: str, blocks: int, iters: int, out, stream=None) -> None:
+    """Launch the CUDA-core multiply-add rate microbenchmark (``kind`` in FMA_KINDS) on the
+    stream; ``out`` is a float32 device tensor of at least blocks * 256 elements."""
+    _check_cuda(out)
+    if out.numel() < blocks * 256:
+        raise ValueError("out needs blocks * 256 floats")
+    _call("dwc_fma_rate_probe", FMA_KINDS[kind], int(blocks), int(iters), out.data_ptr(),
+          _stream_ptr(stream))
+
+
 def path(pass_: str, a, b, out, N, H, W, C, FH, FW, stride, pad, dtype_code) -> int:
     """Kernel family of a call: 3 small-map kernels (maps up to 16x16), 2 tensor-core
     kernels (16-bit inputs), 1 fast CUDA-core kernels, 0 general kernels, -1 invalid."""
@@ -256,5 +280,6 @@ def path(pass_: str, a, b, out, N, H, W, C, FH, FW, stride, pad, dtype_code) -> 
                                        dtype_code))
 
 
-__all__ = ["build", "load_library", "fwd", "fwd_bn_act", "bwd_data", "bwd_filter", "bwd_filter_workspace_size",
-           "device_status", "path", "status_string", "DwcError", "EXPORTS", "LIB_PATH"]
+__all__ = ["build", "load_library", "fwd", "fwd_bn_act", "bwd_data", "bwd_filter",
+           "bwd_filter_workspace_size", "device_status", "set_wait_limit_ns", "fma_rate_probe",
+           "path", "status_string", "DwcError", "EXPORTS", "FMA_KINDS", "LIB_PATH"]

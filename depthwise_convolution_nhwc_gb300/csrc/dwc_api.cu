@@ -1,6 +1,7 @@
 // dwc_api.cu -- the C ABI declared in include/dwc.h: argument validation, choice between
 // the fast and the general kernels, TMA descriptor encoding and the device status word.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <climits>
 #include <cstdint>
@@ -9,6 +10,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/dwc.h"
+#include "../../include/dwc_testing.h"
 #include "dwc_host.h"
 
 namespace dwc {
@@ -27,6 +29,8 @@ struct PerDevice {
 
 PerDevice g_dev[kMaxDevices];
 std::mutex g_mu;
+std::atomic<unsigned long long> g_wait_limit_ns{0};  // 0: the kernels' default
+std::atomic<int> g_row_stall{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // One-time set-up for the current device; nullptr if CUDA is unusable.
@@ -82,6 +86,10 @@ CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t ran
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
+
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+int take_row_stall() { return g_row_stall.exchange(0, std::memory_order_acq_rel); }
 
 static unsigned int* status_word() {
     PerDevice* s = device_state();
@@ -277,12 +285,15 @@ dwc_status_t fwd_impl(const void* x, const void* w, void* y, int N, int H, int W
     if (fast_eligible(P, x, w, y)) {
         RowConv rc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype, s, status_word()};
         rc.out_dtype = od;
+        rc.wait_ns = wait_limit_ns();
+        rc.stall = take_row_stall();
         const cudaError_t err = launch_rows(rc);
         if (err != cudaErrorNotSupported) return map_cuda(err);
         (void)cudaGetLastError();
     } else if (fast_s2_eligible(P, x, w, y)) {
         RowConv rc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype, s, status_word()};
         rc.out_dtype = od;
+        rc.wait_ns = wait_limit_ns();
         cudaError_t err;
         switch (rc.dtype) {
             case kF32: err = launch_rows_s2_f32(rc); break;
@@ -317,6 +328,8 @@ dwc_status_t bwd_data_impl(const void* dy, const void* w, void* dx, int N, int H
         RowConv rc{dy, w, dx, N, P.OH, P.OW, C, H, W, FH, FW, FH - 1 - pad, FW - 1 - pad, true,
                    P.dtype, s, status_word()};
         rc.out_dtype = od;
+        rc.wait_ns = wait_limit_ns();
+        rc.stall = take_row_stall();
         const cudaError_t err = launch_rows(rc);
         if (err != cudaErrorNotSupported) return map_cuda(err);
         (void)cudaGetLastError();
@@ -375,6 +388,7 @@ dwc_status_t dwc_fwd_bn_act(const void* x, const float* mean, const float* var,
     if (bnact_fast_eligible(P, x, w, y)) {
         RowConv rc{x, w, y, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype, s, status_word(),
                    mean, var, gamma, beta, eps, static_cast<int>(act)};
+        rc.wait_ns = wait_limit_ns();
         const cudaError_t err = launch_rows_bnact(rc, stride);
         if (err != cudaErrorNotSupported) return map_cuda(err);
         (void)cudaGetLastError();
@@ -443,14 +457,14 @@ dwc_status_t dwc_bwd_filter(const void* x, const void* dy, float* dw, int N, int
     const size_t ws_floats = workspace_bytes / sizeof(float);
     if (fast_eligible(P, x, dy, dw) && fast_fgrad_floats(P) > 0) {
         FilterGrad fg{x, dy, dw, N, H, W, C, P.OH, P.OW, FH, FW, pad, P.dtype, ws, ws_floats, s,
-                      status_word()};
+                      status_word(), wait_limit_ns()};
         const cudaError_t err = launch_fgrad(fg);
         if (err != cudaErrorNotSupported) return map_cuda(err);
         (void)cudaGetLastError();
     } else if (fast_s2_eligible(P, x, dy, dw) &&
                filter_grad_s2_workspace_floats(N, P.OH, P.OW, C, FH, FW, P.dtype) > 0) {
         FilterGrad fg{x, dy, dw, N, H, W, C, P.OH, P.OW, FH, FW, pad, P.dtype, ws, ws_floats, s,
-                      status_word()};
+                      status_word(), wait_limit_ns()};
         const cudaError_t err = launch_fgrad_s2(fg);
         if (err != cudaErrorNotSupported) return map_cuda(err);
         (void)cudaGetLastError();
@@ -488,7 +502,13 @@ const char* dwc_status_string(dwc_status_t status) {
     }
 }
 
-int dwc_version(void) { return 100; }
+int dwc_version(void) { return 200; }
+
+unsigned long long dwc_set_wait_limit_ns(unsigned long long ns) {
+    return g_wait_limit_ns.exchange(ns, std::memory_order_acq_rel);
+}
+
+void dwc_testing_stall_next_row_launch(void) { g_row_stall.store(1, std::memory_order_release); }
 
 int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int H, int W, int C,
              int FH, int FW, int stride, int pad, dwc_dtype_t dtype) {

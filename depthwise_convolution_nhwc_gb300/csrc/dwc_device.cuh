@@ -23,8 +23,9 @@ enum : unsigned int {
     DWC_DEVSTAT_TIMEOUT = 1u,   // an mbarrier wait ran out of time
 };
 
-// Upper bound on one mbarrier wait.  A healthy wait lasts microseconds; this only ends a
-// kernel whose copies never arrive.
+// Default upper bound on one mbarrier wait.  A healthy wait lasts microseconds; the limit
+// only ends a kernel whose copies never arrive.  Launches carry the limit as an argument
+// (dwc_set_wait_limit_ns changes it for later launches).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -69,13 +70,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Returns false if the time limit
-// ran out (the caller then records the timeout and winds down).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete.  Returns false if `limit_ns` ran out
+// (the caller then records the timeout and winds down).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
 }

@@ -104,6 +104,7 @@ struct FgradArgs {
     uint32_t x_bytes, y_bytes;   // ring slot strides (multiples of 128 bytes)
     uint32_t x_tx, y_tx;         // bytes one TMA box writes into a slot
     uint32_t y_off;        // byte offset of the dy ring after the x ring
+    unsigned long long wait_ns;  // limit of every mbarrier wait
 };
 
 // One output row of a column strip at stride 2: acc[f][t] += x[2*ow + t] * dy[ow] over the
@@ -207,7 +208,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         uint32_t xissued = 0, yissued = 0;  // saturating counts, compared with the ring sizes
         bool ok = true;
         auto put_x = [&](int n, int ih) -> bool {
-            if (xissued >= static_cast<uint32_t>(a.nx) && !mbar_wait(&xempty[xr.slot], xr.phase ^ 1u))
+            if (xissued >= static_cast<uint32_t>(a.nx) && !mbar_wait(&xempty[xr.slot], xr.phase ^ 1u, a.wait_ns))
                 return false;
             if (xissued < static_cast<uint32_t>(a.nx)) ++xissued;
             mbar_arrive_expect_tx(&xfull[xr.slot], a.x_tx);
@@ -217,7 +218,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             return true;
         };
         auto put_y = [&](int n, int oh) -> bool {
-            if (yissued >= static_cast<uint32_t>(a.ny) && !mbar_wait(&yempty[yr.slot], yr.phase ^ 1u))
+            if (yissued >= static_cast<uint32_t>(a.ny) && !mbar_wait(&yempty[yr.slot], yr.phase ^ 1u, a.wait_ns))
                 return false;
             if (yissued < static_cast<uint32_t>(a.ny)) ++yissued;
             mbar_arrive_expect_tx(&yfull[yr.slot], a.y_tx);
@@ -246,7 +247,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             for (uint32_t j = 0; j < issued; ++j) {
                 r.slot = r.slot == 0 ? n - 1 : r.slot - 1;
                 if (r.slot == n - 1) r.phase ^= 1u;
-                if (!mbar_wait(&full[r.slot], r.phase)) {
+                if (!mbar_wait(&full[r.slot], r.phase, a.wait_ns)) {
                     record_status(a.status, DWC_DEVSTAT_TIMEOUT);
                     return;
                 }
@@ -300,12 +301,12 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             for (int d = (row == 0 ? 0 : a.fhc - nnew); d < a.fhc; ++d) {
                 uint32_t ph;
                 const uint32_t sl = xslot(static_cast<uint32_t>(d), ph);
-                if (!mbar_wait(&xfull[sl], ph)) {
+                if (!mbar_wait(&xfull[sl], ph, a.wait_ns)) {
                     ok = false;
                     break;
                 }
             }
-            if (ok && !mbar_wait(&yfull[yr.slot], yr.phase)) ok = false;
+            if (ok && !mbar_wait(&yfull[yr.slot], yr.phase, a.wait_ns)) ok = false;
             if (!ok) break;
 
             const T* ys = reinterpret_cast<const T*>(yring + static_cast<size_t>(yr.slot) * a.y_bytes) + 2 * cl;
@@ -565,6 +566,7 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     FgradArgs a;
     a.part = p.workspace;
     a.status = p.status;
+    a.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     a.N = p.N; a.OH = p.OH; a.C = p.C; a.pad = p.pad;
     a.ncp = P.ncp; a.owpart = P.owpart;
     a.FH = fhr;

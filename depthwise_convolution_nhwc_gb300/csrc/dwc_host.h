@@ -42,6 +42,8 @@ struct RowConv {
     int act = -1;
     int out_dtype = kF32;   // kF32, or the input's type (kBF16 / kF16) for 16-bit outputs
     int c_lo = 0, c_hi = -1; // channel range a row-kernel launch covers (c_hi < 0: up to C)
+    unsigned long long wait_ns = 0;  // limit of every wait in the kernel (0: the default)
+    int stall = 0;           // fault injection: CTA 0 of the row kernel issues no copy
 };
 
 // Filter-gradient problem: dw[fh, fw, c] = sum_{n,oh,ow} x[n, oh+fh-pad, ow+fw-pad, c] * dy[n,oh,ow,c].
@@ -58,6 +60,7 @@ struct FilterGrad {
     size_t workspace_floats;
     cudaStream_t stream;
     unsigned int* status;
+    unsigned long long wait_ns = 0;  // limit of every wait in the kernel (0: the default)
 };
 
 // General problem for the fallback kernels (any stride, any channel count or alignment).
@@ -82,6 +85,11 @@ struct GeneralConv {
     int act = -1;
     int out_dtype = kF32;
 };
+
+// Limit of the waits inside kernels launched from now on (nanoseconds), and the one-shot
+// fault-injection flag of the next row-kernel launch (both set through the C ABI).
+unsigned long long wait_limit_ns();
+int take_row_stall();
 
 // Device properties cached per device.
 struct DeviceInfo {

@@ -72,6 +72,8 @@ struct RowsArgs {
     uint32_t w_off;       // offset of the filter row in a stage (x_bytes rounded up to 128)
     uint32_t w_bytes;     // bytes of one staged filter row box
     uint32_t stage_stride;
+    unsigned long long wait_ns;  // limit of every mbarrier wait
+    int stall;            // fault injection (tests): CTA 0 issues no copy, so it times out
     // fused BN + Act (ACT >= 0): batch statistics and affine parameters, C floats each
     const float* bn_mean;
     const float* bn_var;
@@ -220,7 +222,9 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         prefetch_tensormap(&wmap);
         Ring ring;
         uint32_t issued = 0;  // stages issued so far (saturating; only compared with ns)
-        bool ok = true;
+        // fault injection: CTA 0 issues nothing, so no copy is ever in flight while its
+        // compute warps run out their wait limit
+        bool ok = !(a.stall && blockIdx.x == 0);
         for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
             uint32_t r0, r1, r2;
             const uint32_t q = a.fd_cblocks.divmod(a.fd_ctiles.divmod(a.fd_bands.divmod(u, r0), r1), r2);
@@ -232,7 +236,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
             for (int i = i_lo; i < i_hi; ++i, ring.next(a.ns)) {
                 // slot reuse: wait until every compute warp released its previous stage
                 if (issued >= static_cast<uint32_t>(a.ns) &&
-                    !mbar_wait(&empty[ring.slot], ring.phase ^ 1u)) {
+                    !mbar_wait(&empty[ring.slot], ring.phase ^ 1u, a.wait_ns)) {
                     record_status(a.status, DWC_DEVSTAT_TIMEOUT);
                     ok = false;
                     break;
@@ -253,7 +257,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         for (uint32_t j = 0; j < issued; ++j) {
             ring.slot = ring.slot == 0 ? a.ns - 1 : ring.slot - 1;
             if (ring.slot == static_cast<uint32_t>(a.ns) - 1) ring.phase ^= 1u;
-            if (!mbar_wait(&full[ring.slot], ring.phase)) {
+            if (!mbar_wait(&full[ring.slot], ring.phase, a.wait_ns)) {
                 record_status(a.status, DWC_DEVSTAT_TIMEOUT);
                 break;
             }
@@ -343,7 +347,7 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
         // return the row's shared-memory pointer.  The slot index is a compile-time
         // constant wherever the row loop is unrolled, so no register ever moves.
         auto begin_row = [&](auto ic, int i, const T*& xs) -> bool {
-            if (!mbar_wait(&full[ring.slot], ring.phase)) {
+            if (!mbar_wait(&full[ring.slot], ring.phase, a.wait_ns)) {
                 record_status(a.status, DWC_DEVSTAT_TIMEOUT);
                 return false;
             }
@@ -491,6 +495,8 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     RowsArgs a;
     a.out = p.out;
     a.status = p.status;
+    a.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
+    a.stall = p.stall;
     a.H = p.H;
     a.W = p.W;
     a.FH = p.FH;

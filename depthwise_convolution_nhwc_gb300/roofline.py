@@ -11,8 +11,9 @@ cuBLAS matching of §6.1.1, which count 2*N*OH*OW*C*FH*FW FLOPs per pass):
                    (fwd: X, W -> Y; bwd_data: dY, W -> dX; bwd_filter: X, dY -> dW).
 
 Peaks: HBM bandwidth and bf16 tensor throughput are the measured values of the machine's
-peak file; the fp32 FFMA peak is derived from the unit counts (SMs x 128 fp32 lanes x
-2 FLOP x maximum SM clock), since no measured value exists for it.
+peak file; the fp32 multiply-add peak is measured in the benchmark's own run (the packed
+fp32x2 FMA microbenchmark of the library, all SMs) and passed in; without a measurement it
+falls back to the unit counts (SMs x 128 fp32 lanes x 2 FLOP x maximum SM clock).
 """
 from __future__ import annotations
 
@@ -63,19 +64,31 @@ def compulsory_bytes(c: Case, which: str) -> int:
     raise ValueError(which)
 
 
-def load_peaks(path: str | None = None) -> dict:
-    """Measured peaks if the peak file exists, else the stated fallbacks."""
+def derived_fp32_tflops(sm_count: int = GB300_SMS, sm_mhz: float = GB300_MAX_SM_MHZ) -> float:
+    """fp32 multiply-add peak from the unit counts: SMs x 128 lanes x 2 FLOP x clock."""
+    return sm_count * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+
+
+def load_peaks(path: str | None = None, fp32_tflops: float | None = None,
+               sm_count: int | None = None) -> dict:
+    """Measured peaks if the peak file exists, else the stated fallbacks.  `fp32_tflops`: the
+    fp32 multiply-add peak measured in this run (else derived from `sm_count` SMs, default
+    152, at the maximum clock)."""
     path = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
-    fp32 = GB300_SMS * FP32_LANES_PER_SM * 2 * GB300_MAX_SM_MHZ * 1e6 / 1e12
+    if fp32_tflops:
+        fp32, fp32_src = float(fp32_tflops), "measured"
+    else:
+        fp32, fp32_src = derived_fp32_tflops(sm_count or GB300_SMS), "derived"
     try:
         with open(path) as f:
             m = json.load(f)
         return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
                 "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
-                "fp32_tflops": fp32, "source": "measured"}
+                "fp32_tflops": fp32, "fp32_source": fp32_src, "source": "measured"}
     except (OSError, KeyError, ValueError):
         return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
-                "bf16_tflops_sustained": 1700.0, "fp32_tflops": fp32, "source": "fallback"}
+                "bf16_tflops_sustained": 1700.0, "fp32_tflops": fp32, "fp32_source": fp32_src,
+                "source": "fallback"}
 
 
 def roofline_time_s(c: Case, which: str, peaks: dict, tensor: bool = False) -> tuple[float, str]:

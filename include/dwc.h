@@ -185,6 +185,26 @@ dwc_status_t dwc_bwd_filter_noalloc(const void* x, const void* dy, float* dw,
  * call, DWC_ERR_TIMEOUT if one did, DWC_ERR_CUDA if the synchronisation failed. */
 dwc_status_t dwc_device_status(dwc_stream_t stream);
 
+/* Upper bound, in nanoseconds, on every wait inside the kernels launched after this call (on
+ * any device and stream); 0 restores the default of 2 seconds.  A healthy wait lasts
+ * microseconds: the limit only decides how soon a kernel whose data never arrives gives up
+ * and reports DWC_ERR_TIMEOUT through dwc_device_status().  Returns the previous setting. */
+unsigned long long dwc_set_wait_limit_ns(unsigned long long ns);
+
+/* Multiply-add rate microbenchmark of the CUDA cores, the measured compute peak against
+ * which the CUDA-core kernels' roofline is stated (no counterpart in the paper).  Launches
+ * `blocks` x 256 threads on `stream`; every thread runs `iters` iterations of 8 independent
+ * chains of one multiply-add instruction:
+ *   kind 0: fp32 FMA (1 multiply-add per instruction)
+ *   kind 1: packed fp32x2 FMA (2 per instruction)
+ *   kind 2: packed fp16x2 FMA (2 per instruction)
+ *   kind 3: packed bf16x2 FMA (2 per instruction)
+ * so one launch performs blocks * 256 * iters * 8 * (1 or 2) multiply-adds (2 FLOPs each);
+ * the caller times it with events on `stream`.  `out` (device, blocks * 256 floats) receives
+ * one value per thread.  DWC_ERR_INVALID_ARG for an unknown kind, blocks or iters < 1 or a
+ * null `out`. */
+dwc_status_t dwc_fma_rate_probe(int kind, int blocks, int iters, float* out, dwc_stream_t stream);
+
 /* Static text for a status code (never NULL). */
 const char* dwc_status_string(dwc_status_t status);
 

@@ -1,0 +1,29 @@
+/*
+ * dwc_testing.h -- fault injection for tests of libdwc_gb300.so's failure path.
+ *
+ * No counterpart in the paper.  The injected failure is made on the host side and involves
+ * no GPU fault: a kernel is told not to issue some of its own input copies, so its compute
+ * warps wait until their wait limit (dwc_set_wait_limit_ns) runs out, record the timeout in
+ * the device status word and end.  No copy is in flight at that point.
+ */
+#ifndef DWC_GB300_TESTING_H
+#define DWC_GB300_TESTING_H
+
+#include "dwc.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The next launch of the row-streaming kernel (dwc_fwd / dwc_bwd_data on a shape that
+ * dwc_path reports as 1, stride 1) issues no input copy in its first CTA.  That CTA's
+ * outputs are left unwritten and dwc_device_status() then returns DWC_ERR_TIMEOUT.  The
+ * request is consumed by that one launch; launches of other kernels leave it pending.  Not
+ * for production use. */
+void dwc_testing_stall_next_row_launch(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DWC_GB300_TESTING_H */

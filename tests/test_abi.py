@@ -1,6 +1,7 @@
-"""C ABI checks that need no GPU: the library loads, exports every symbol include/dwc.h
+"""C ABI checks that need no GPU: the library loads, exports every symbol include/*.h
 declares, and rejects bad arguments on the host before touching CUDA."""
 import ctypes
+import glob
 import os
 import re
 
@@ -9,7 +10,7 @@ import pytest
 import depthwise_convolution_nhwc_gb300 as dwc
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "dwc.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 @pytest.fixture(scope="module")
@@ -20,9 +21,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dwc_[a-z_]+)\s*\(", text)))
+    names = set()
+    for header in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(header).read(), flags=re.S)
+        names.update(re.findall(r"\b(dwc_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_binding_exports():
@@ -180,3 +183,18 @@ def test_path_selection_host_logic(lib):
     assert p(0, **dict(big, W=16), dtype=1) == 1          # narrow rows: row-streaming kernel
     # an unaligned (but element-aligned) pointer falls back to the general kernels
     assert lib.dwc_path(0, FAKE + 4, None, None, 1, 8, 8, 16, 3, 3, 1, 1, 0) == 0
+
+
+def test_wait_limit_setting_round_trips(lib):
+    prev = lib.dwc_set_wait_limit_ns(5_000_000)
+    try:
+        assert lib.dwc_set_wait_limit_ns(7_000_000) == 5_000_000
+    finally:
+        assert lib.dwc_set_wait_limit_ns(prev) == 7_000_000
+
+
+@pytest.mark.parametrize("args", [(4, 1, 1), (-1, 1, 1), (0, 0, 1), (0, 1, 0)])
+def test_fma_probe_rejects_bad_arguments(lib, args):
+    kind, blocks, iters = args
+    assert lib.dwc_fma_rate_probe(kind, blocks, iters, FAKE, None) == 1
+    assert lib.dwc_fma_rate_probe(0, 1, 1, None, None) == 1

@@ -36,7 +36,8 @@ def test_reference_arm_line():
 
 @pytest.mark.gpu
 def test_cuda_arm_line():
-    d = run_bench("--steps", "5", "--warmup", "3", "--e2e-steps", "2", "--no-cpu-baseline")
+    d = run_bench("--steps", "5", "--warmup", "3", "--e2e-steps", "2", "--no-cpu-baseline",
+                  "--per-filter-steps", "1")
     for k in BASE_KEYS + ("roofline", "gpu_launches", "clocks", "per_pass"):
         assert k in d, k
     assert d["value"] > 0 and d["n_gpus"] == 1 and d["steps"] == 5 and d["warmup"] == 3
@@ -48,3 +49,14 @@ def test_cuda_arm_line():
     assert e["value"] < d["value"]  # the copies are inside the end-to-end region
     assert d["gpu_launches"] == 5 * 4  # fwd, bwd_data, filter gradient + slice sum
     assert set(d["per_pass"]) == {"fwd", "bwd_data", "bwd_filter"}
+    assert e["link"]["h2d_gbs"] > 0 and e["link"]["d2h_gbs"] > 0
+    # the alu roofline denominator is the fp32x2 rate measured in the same run
+    alu = d["alu_peaks"]["tflops"]
+    assert set(alu) == {"ffma", "ffma2", "hfma2", "bf16x2"} and all(v > 0 for v in alu.values())
+    from depthwise_convolution_nhwc_gb300.inputs import SWEEP_FILTERS
+    pts = d["per_filter"]["points"]
+    assert {(p["dtype"], p["F"]) for p in pts} == {(dt, F) for dt in ("f32", "bf16")
+                                                   for F in SWEEP_FILTERS}
+    for p in pts:
+        for name in ("fwd", "bwd_data", "bwd_filter"):
+            assert p[name]["us"] > 0 and 0 < p[name]["frac"] < 2
