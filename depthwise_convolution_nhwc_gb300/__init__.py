@@ -34,7 +34,8 @@ STATUS = {0: "DWC_OK", 1: "DWC_ERR_INVALID_ARG", 2: "DWC_ERR_UNSUPPORTED",
 EXPORTS = ("dwc_fwd", "dwc_fwd_ex", "dwc_fwd_bn_act", "dwc_bwd_data", "dwc_bwd_data_ex",
            "dwc_bwd_filter_workspace_size", "dwc_bwd_filter", "dwc_bwd_filter_noalloc",
            "dwc_device_status", "dwc_set_wait_limit_ns", "dwc_fma_rate_probe",
-           "dwc_status_string", "dwc_version", "dwc_path", "dwc_testing_stall_next_row_launch")
+           "dwc_status_string", "dwc_version", "dwc_path", "dwc_testing_stall_next_row_launch",
+           "dwc_testing_prefer_family")
 FMA_KINDS = {"ffma": 0, "ffma2": 1, "hfma2": 2, "bf16x2": 3}  # dwc_fma_rate_probe kinds
 
 _lock = threading.Lock()
@@ -97,6 +98,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.dwc_fma_rate_probe.restype = i
         lib.dwc_testing_stall_next_row_launch.argtypes = []
         lib.dwc_testing_stall_next_row_launch.restype = None
+        lib.dwc_testing_prefer_family.argtypes = [i]
+        lib.dwc_testing_prefer_family.restype = i
         if path is None:
             _lib = lib
         return lib
@@ -273,8 +276,9 @@ def fma_rate_probe(kind: str, blocks: int, iters: int, out, stream=None) -> None
 
 
 def path(pass_: str, a, b, out, N, H, W, C, FH, FW, stride, pad, dtype_code) -> int:
-    """Kernel family of a call: 3 small-map kernels (maps up to 16x16), 2 tensor-core
-    kernels (16-bit inputs), 1 fast CUDA-core kernels, 0 general kernels, -1 invalid."""
+    """Kernel family of a call: 4 warp-level MMA and 2 tcgen05 tensor-core kernels (16-bit
+    inputs), 3 small-map kernels (maps up to 16x16), 1 fast CUDA-core kernels, 0 general
+    kernels, -1 invalid."""
     p = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2, "fwd_bn_act": 3}[pass_]
     return int(load_library().dwc_path(p, a, b, out, N, H, W, C, FH, FW, stride, pad,
                                        dtype_code))

@@ -31,6 +31,7 @@ PerDevice g_dev[kMaxDevices];
 std::mutex g_mu;
 std::atomic<unsigned long long> g_wait_limit_ns{0};  // 0: the kernels' default
 std::atomic<int> g_row_stall{0};
+std::atomic<int> g_family_pref{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // One-time set-up for the current device; nullptr if CUDA is unusable.
@@ -90,6 +91,8 @@ CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t ran
 unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 int take_row_stall() { return g_row_stall.exchange(0, std::memory_order_acq_rel); }
+
+int family_preference() { return g_family_pref.load(std::memory_order_relaxed); }
 
 static unsigned int* status_word() {
     PerDevice* s = device_state();
@@ -203,7 +206,9 @@ cudaError_t launch_rows(const RowConv& rc) {
             default: return launch_rows_stripe_f16(rc);
         }
     }
-    if (small_map_serves(rc.H, rc.W, rc.OH, rc.OW, rc.FW, rc.pad_w)) {
+    // (a family preference for 16-bit inputs bypasses the small-map kernels)
+    const bool pref16 = rc.dtype != kF32 && family_preference() != 0;
+    if (!pref16 && small_map_serves(rc.H, rc.W, rc.OH, rc.OW, rc.FW, rc.pad_w)) {
         cudaError_t err;
         switch (rc.dtype) {
             case kF32: err = launch_small_rows_f32(rc); break;
@@ -510,6 +515,13 @@ unsigned long long dwc_set_wait_limit_ns(unsigned long long ns) {
 
 void dwc_testing_stall_next_row_launch(void) { g_row_stall.store(1, std::memory_order_release); }
 
+int dwc_testing_prefer_family(int family) {
+    if (family != 0 && family != kFamilyCudaCore && family != kFamilyTcgen05 &&
+        family != kFamilyMmaSync)
+        return -1;
+    return g_family_pref.exchange(family, std::memory_order_acq_rel);
+}
+
 int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int H, int W, int C,
              int FH, int FW, int stride, int pad, dwc_dtype_t dtype) {
     Problem P;
@@ -527,8 +539,10 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
         if (small_fgrad_floats(P) > 0) return 3;
         return P.e == 2 && FH == FW && tensor_core_fgrad(N, C, P.OH, P.OW, FH, FW) ? 2 : 1;
     }
-    if (FH == FW && (pass == kPassFwd ? small_map_serves(H, W, P.OH, P.OW, FW, pad)
-                                      : small_map_serves(P.OH, P.OW, H, W, FW, FW - 1 - pad)))
+    const bool pref16 = P.e == 2 && family_preference() != 0;
+    if (FH == FW && !pref16 &&
+        (pass == kPassFwd ? small_map_serves(H, W, P.OH, P.OW, FW, pad)
+                          : small_map_serves(P.OH, P.OW, H, W, FW, FW - 1 - pad)))
         return 3;
     if (P.e == 2) {
         // the same RowConv the entry points build (backward data: over dy, output H x W)
@@ -537,7 +551,7 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
                       nullptr, nullptr}
             : RowConv{a, b, nullptr, N, P.OH, P.OW, C, H, W, FH, FW, FH - 1 - pad, FW - 1 - pad,
                       true, P.dtype, nullptr, nullptr};
-        if (tensor_core_rows(rc)) return 2;
+        return tensor_core_rows(rc);
     }
     return 1;
 }

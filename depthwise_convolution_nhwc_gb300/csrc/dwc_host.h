@@ -186,9 +186,20 @@ size_t small_fgrad_workspace_floats_f32(int N, int H, int W, int C, int OH, int 
 size_t small_fgrad_workspace_floats_bf16(int N, int H, int W, int C, int OH, int OW, int FH, int FW, int pad);
 size_t small_fgrad_workspace_floats_f16(int N, int H, int W, int C, int OH, int OW, int FH, int FW, int pad);
 
-// Whether 16-bit inputs of this shape run on the tensor-core kernels rather than the
-// CUDA-core ones (forward / backward data as the RowConv describes it; filter gradient).
-bool tensor_core_rows(const RowConv& p);
+// tcgen05 tensor-core forward / backward-data kernels (16-bit inputs, stride 1; fp32 or the
+// input's 16-bit type as output); cudaErrorNotSupported when the shape does not fit.
+cudaError_t launch_tc_rows_bf16(const RowConv& p);
+cudaError_t launch_tc_rows_f16(const RowConv& p);
+bool tc_rows_fits(const RowConv& p);
+
+// Kernel family a 16-bit forward / backward-data call of this shape runs on (kFamily*), and
+// whether the filter gradient of 16-bit inputs runs on the tensor-core kernel.
+enum KernelFamily { kFamilyGeneral = 0, kFamilyCudaCore = 1, kFamilyTcgen05 = 2, kFamilySmall = 3,
+                    kFamilyMmaSync = 4 };
+int tensor_core_rows(const RowConv& p);
+// Family preference for 16-bit forward / backward-data calls (tests and kernel comparisons;
+// 0 = automatic choice), set through dwc_testing_prefer_family.
+int family_preference();
 bool tensor_core_fgrad(int N, int C, int OH, int OW, int FH, int FW);
 
 // The argument and pointer checks of dwc_bwd_filter without its workspace checks; returns a

@@ -342,11 +342,31 @@ inline bool mma_rows_wanted(const RowConv& p) {
     return p.FW >= kMmaMinFilter && p.OW >= kMmaMinWidth;
 }
 
+// Where the tcgen05 kernel serves 16-bit inputs (timed on the stage shapes: from 17 taps on
+// rows of at least 48 outputs it beat the warp-level MMA kernel, e.g. bf16 32x56x56x128
+// 31x31: 199 against 265 us; on 28-wide rows and at 13 taps it was slower).
+constexpr int kTcMinFilter = 17;
+constexpr int kTcMinWidth = 48;
+inline bool tc_rows_wanted(const RowConv& p) {
+    return p.FW >= kTcMinFilter && p.OW >= kTcMinWidth;
+}
+
+// 16-bit forward / backward data: the tcgen05 kernel, the warp-level MMA kernel or the row
+// kernel, in that order of preference where each serves the shape (a family preference set
+// for tests and kernel comparisons picks one of them where it can run).
 template <typename T, class OutT = float>
 cudaError_t launch_rows_or_mma(const RowConv& p) {
-    if (mma_rows_wanted(p)) {
+    const int pref = family_preference();
+    if ((pref == 0 && tc_rows_wanted(p)) || pref == kFamilyTcgen05) {
+        const cudaError_t err = std::is_same<T, __nv_bfloat16>::value ? launch_tc_rows_bf16(p)
+                                                                      : launch_tc_rows_f16(p);
+        if (err != cudaErrorNotSupported) return err;
+        (void)cudaGetLastError();
+    }
+    if ((pref == 0 && mma_rows_wanted(p)) || pref == kFamilyMmaSync) {
         const cudaError_t err = p.flip ? launch_mma_inst<T, true, OutT>(p) : launch_mma_inst<T, false, OutT>(p);
         if (err != cudaErrorNotSupported) return err;
+        (void)cudaGetLastError();
     }
     return launch_rows_dispatch<T, OutT>(p);
 }

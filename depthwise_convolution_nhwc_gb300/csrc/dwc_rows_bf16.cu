@@ -9,10 +9,16 @@ cudaError_t launch_rows_bf16(const RowConv& p) {
     return launch_rows_or_mma<__nv_bfloat16>(p);
 }
 
-bool tensor_core_rows(const RowConv& p) {
+int tensor_core_rows(const RowConv& p) {
+    // the choice of launch_rows_or_mma (no 16-bit input shape differs between bf16 and fp16)
+    const int pref = family_preference();
+    if (((pref == 0 && tc_rows_wanted(p)) || pref == kFamilyTcgen05) && tc_rows_fits(p))
+        return kFamilyTcgen05;
     MmaArgs a;
     size_t smem = 0;
-    return mma_rows_wanted(p) && mma_plan(p, a, smem);
+    if (((pref == 0 && mma_rows_wanted(p)) || pref == kFamilyMmaSync) && mma_plan(p, a, smem))
+        return kFamilyMmaSync;
+    return kFamilyCudaCore;
 }
 cudaError_t launch_rows_s2_bf16(const RowConv& p) {
     if (p.out_dtype != kF32) return launch_rows_s2_o16_bf16(p);

@@ -213,8 +213,10 @@ int dwc_version(void);
 
 /* Which kernel family a call with these arguments would use: 1 = fast CUDA-core kernels
  * (row-streaming, stride-2 and filter-gradient kernels, for the shapes listed at the top
- * of this file), 2 = tensor-core kernels (16-bit inputs only), 3 = small-map kernels (maps
- * up to 16 x 16), 0 = general kernels, -1 = invalid arguments.  `pass` is 0 for
+ * of this file), 2 = tensor-core kernels on the 5th-generation MMA (tcgen05, accumulators
+ * in tensor memory; 16-bit inputs only), 3 = small-map kernels (maps up to 16 x 16),
+ * 4 = tensor-core kernels on the warp-level MMA (mma.sync; 16-bit inputs only), 0 = general
+ * kernels, -1 = invalid arguments.  `pass` is 0 for
  * dwc_fwd, 1 for dwc_bwd_data, 2 for dwc_bwd_filter, 3 for dwc_fwd_bn_act.  Pointer
  * alignment is checked with the pointers given (they may be NULL to mean "16-byte
  * aligned"). */

@@ -22,6 +22,15 @@ extern "C" {
  * for production use. */
 void dwc_testing_stall_next_row_launch(void);
 
+/* Kernel family for the 16-bit forward / backward-data calls made from now on, where that
+ * family can run the shape (else the automatic choice): 0 = automatic (the default),
+ * 1 = CUDA-core row kernel, 2 = tcgen05 tensor-core kernel, 4 = warp-level MMA kernel (the
+ * family numbers of dwc_path, which reports the choice).  It also bypasses the small-map
+ * kernels for 16-bit inputs.  Lets tests run every kernel on the same shapes and benchmarks
+ * compare them.  Returns the previous preference, or -1 (nothing changed) for an unknown
+ * family.  Not for production use. */
+int dwc_testing_prefer_family(int family);
+
 #ifdef __cplusplus
 }
 #endif

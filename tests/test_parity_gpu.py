@@ -115,7 +115,7 @@ def test_fast_path_full_tensors(case, dtype):
         pytest.skip("16-bit fast path needs C % 8 == 0")
     fam = dwc.path("fwd", None, None, None, case.N, case.H, case.W, case.C, case.FH, case.FW,
                    case.stride, case.pad, {"f32": 0, "bf16": 1, "f16": 2}[dtype])
-    assert fam in (1, 3) or (fam == 2 and dtype != "f32")
+    assert fam in (1, 3) or (fam in (2, 4) and dtype != "f32")
     check_full(case)
 
 
@@ -458,8 +458,8 @@ def test_stripe_filters(case, dtype):
     case = Case(**{**case.__dict__, "dtype": dtype})
     code = {"f32": 0, "bf16": 1, "f16": 2}[dtype]
     args = (case.N, case.H, case.W, case.C, case.FH, case.FW, case.stride, case.pad, code)
-    assert dwc.path("fwd", None, None, None, *args) in ((1,) if dtype == "f32" else (1, 2))
-    assert dwc.path("bwd_data", None, None, None, *args) in ((1,) if dtype == "f32" else (1, 2))
+    assert dwc.path("fwd", None, None, None, *args) in ((1,) if dtype == "f32" else (1, 2, 4))
+    assert dwc.path("bwd_data", None, None, None, *args) in ((1,) if dtype == "f32" else (1, 2, 4))
     assert dwc.path("bwd_filter", None, None, None, *args) == 1
     check_full(case)
 
