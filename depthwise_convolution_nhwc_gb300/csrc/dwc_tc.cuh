@@ -28,13 +28,13 @@
 // of CG channels)):
 //  * 4 epilogue warps -- warp w reads the 32-lane quadrant w of the accumulators
 //    (tcgen05.ld), adds the two partial sums and writes CG channels of a pixel per store;
-//  * 2 MMA warps: one lane each issues MMAs, for the even and the odd filter rows into its
-//    own partial accumulator (one thread issues an MMA only every ~50-100 cycles, less than
-//    an M=128 N=64 MMA needs); the first also allocates the tensor memory;
-//  * kTcLoadWarps loader warps: gather the unit's input rows (CG channels per load) and
-//    store them transposed into the per-channel planes (zeros in the padding);
-//  * 4 builder warps, two per issuer: write the Toeplitz core matrices of every (channel,
-//    filter row) into the issuer's ring, taking turns; one of them stages the filters;
+//  * 4 MMA warps: one lane each issues the MMAs of half the channels and one filter-row
+//    parity into the partial sum of that parity (a single thread issues an MMA only every
+//    ~100 cycles, an M=128 N=64 MMA takes 48); the first also allocates the tensor memory;
+//  * 4 builder warps, one per issuer: write the Toeplitz core matrices of the issuer's
+//    (channel, filter row) items into its ring; one of them stages the filters;
+//  * 6 loader warps: gather the unit's input rows (CG channels per load) and store them
+//    transposed into the per-channel planes (zeros in the padding).
 // Stages pass through mbarrier rings; every wait has a time limit and a shared abort flag,
 // so a lost arrival ends the kernel (status word set) instead of hanging it.  Backward data
 // uses the same kernel with the filter read rotated by 180 degrees.
@@ -49,36 +49,36 @@
 namespace dwc {
 
 constexpr int kTcM = 128;           // MMA rows (tensor-memory lanes)
-// Warp w runs on sub-partition w % 4.  Roles (16 warps):
+// Roles (18 warps; warp w runs on sub-partition w % 4):
 //   0-3   epilogue, warp w reading the 32-lane quadrant w of tensor memory
-//   4, 5  MMA issuers (sub-partitions 0, 1; warp 4 also allocates tensor memory)
-//   6, 7, 10, 11  Toeplitz builders (sub-partitions 2, 3): ring r is fed by warps 6 + r and
-//         10 + r, taking alternate items
-//   8, 9, 12-15  loaders
+//   4-7   MMA issuers, one lane each: issuer i takes the channels c with c % 2 == i / 2 and
+//         the filter rows with fh % 2 == i % 2 (one thread issues an MMA only every ~100
+//         cycles, four keep the tensor core's 48-cycle pace); warp 4 also allocates the
+//         tensor memory
+//   8-11  Toeplitz builders, builder i feeding issuer i's ring
+//   12-17 loaders
 constexpr int kTcEpiWarps = 4;
 constexpr int kTcMmaWarp = 4;       // first MMA warp
-constexpr int kTcIssuers = 2;       // MMA-issuing threads (one per MMA warp)
+constexpr int kTcIssuers = 4;       // MMA-issuing threads (one per MMA warp)
+constexpr int kTcBuild0 = kTcMmaWarp + kTcIssuers;
 constexpr int kTcBuildWarps = 4;
+constexpr int kTcLoad0 = kTcBuild0 + kTcBuildWarps;
 constexpr int kTcLoadWarps = 6;
-constexpr int kTcWarps = kTcEpiWarps + kTcIssuers + kTcBuildWarps + kTcLoadWarps;
+constexpr int kTcWarps = kTcLoad0 + kTcLoadWarps;
 constexpr int kTcRingSlots = 4;     // Toeplitz slots per issuer ring (a power of two)
-
-__host__ __device__ constexpr bool tc_is_builder(int w) { return w == 6 || w == 7 || w == 10 || w == 11; }
-__host__ __device__ constexpr int tc_builder_index(int w) { return w < 10 ? w - 6 : w - 8; }  // 0..3
-__host__ __device__ constexpr bool tc_is_loader(int w) { return w == 8 || w == 9 || w >= 12; }
-__host__ __device__ constexpr int tc_loader_index(int w) { return w < 10 ? w - 8 : w - 10; }   // 0..5
+constexpr int kTcPartials = 2;      // partial sums per channel (one per filter-row parity)
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcTmemCols = 512;
 constexpr int kTcDCols = 256;       // columns of one accumulator buffer (two buffers)
 constexpr int kTcMaxPlanes = 8;
-constexpr int kTcMaxToep = 8;       // kTcIssuers rings of kTcRingSlots
+constexpr int kTcMaxToep = 16;      // kTcIssuers rings of kTcRingSlots
 // barriers (plane and Toeplitz rings, two accumulator buffers, the final MMA barrier), the
 // tensor-memory address and the abort flag
 constexpr int kTcMaxZ = 12;          // Toeplitz run of at most 32 * (kTcMaxZ - 1) rows
 constexpr int kTcBarBytes =
     ((2 * kTcMaxPlanes + 2 * kTcMaxToep + 2 * 2 + kTcIssuers + 2 * 2) * 8 + 8 + 127) / 128 * 128;
-static_assert(kTcBuildWarps == 2 * kTcIssuers && kTcIssuers * kTcRingSlots == kTcMaxToep,
-              "two builder warps feed each issuer's ring");
+static_assert(kTcBuildWarps == kTcIssuers && kTcIssuers * kTcRingSlots == kTcMaxToep,
+              "builder warp i feeds issuer i's ring");
 
 struct TcArgs {
     const void* x;      // N x H x W x C, 16-bit
@@ -299,7 +299,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.ps; ++s) {
             mbar_init(&plane_full[s], kTcLoadWarps);
-            mbar_init(&plane_empty[s], kTcIssuers);
+            mbar_init(&plane_empty[s], 2);   // the two filter-row parities of its channel
         }
         for (int s = 0; s < a.ts; ++s) {
             mbar_init(&toep_full[s], 1);
@@ -331,11 +331,12 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
 
     if (warp >= kTcMmaWarp && warp < kTcMmaWarp + kTcIssuers) {
         // ------------------------------------------------------------- MMA issue
-        // Issuer `is` takes the filter rows fh = is, is + kTcIssuers, ... of every channel
-        // and accumulates them into its own partial sum (the epilogue adds the partials).
+        // Issuer `is` takes the channels c of the group with c % 2 == is / 2 and the filter
+        // rows fh with fh % 2 == is % 2, and accumulates into the partial sum of its parity
+        // (the epilogue adds the two parities).
         const int is = warp - kTcMmaWarp;
+        const int par = is & 1, chs = is >> 1;
         if (lane == 0) {
-            Ring pr;
             uint32_t db = 0, dphase = 0;
             bool ok = true;
             // Descriptors are built once; the start-address field (bits 0-13, 16-byte units)
@@ -346,27 +347,34 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
             const uint32_t a_ks = 2u * a.MR;           // A advance per K-step (16-byte units)
             const uint32_t a_slot = a.plane_bytes >> 4, b_slot = a.toep_bytes >> 4;
             const uint32_t idesc = a.idesc;
+            const uint32_t ps = static_cast<uint32_t>(a.ps);
             // this issuer's Toeplitz ring: slots [is * kTcRingSlots, (is + 1) * kTcRingSlots),
-            // filled in order with the runs of exactly the filter rows this issuer takes
+            // filled in order with the runs of exactly the (channel, filter row) items it takes
             const uint32_t ring0 = static_cast<uint32_t>(is) * kTcRingSlots;
             uint32_t item = 0;
-            for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            uint32_t pos0 = 0;   // plane-ring position of the unit's first channel
+            for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x, pos0 += CG) {
                 if (!tc_wait(&d_empty[db], dphase ^ 1u, a, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t dcol = tmem + db * kTcDCols + static_cast<uint32_t>(is * CG * a.NN);
-                for (int ch = 0; ch < CG && ok; ++ch) {
-                    if (!tc_wait(&plane_full[pr.slot], pr.phase, a, abort_flag)) { ok = false; break; }
+                const uint32_t dcol = tmem + db * kTcDCols + static_cast<uint32_t>(par * CG * a.NN);
+                for (int ch = chs; ch < CG && ok; ch += 2) {
+                    // channel ch of this unit sits at plane-ring position pos0 + ch (the
+                    // loaders fill the ring in order; this issuer skips the other channels)
+                    const uint32_t pos = pos0 + static_cast<uint32_t>(ch);
+                    const uint32_t pslot = pos % ps, pphase = (pos / ps) & 1u;
+                    if (!tc_wait(&plane_full[pslot], pphase, a, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t ap = adesc0 + pr.slot * a_slot;
+                    const uint64_t ap = adesc0 + pslot * a_slot;
                     const uint32_t dch = dcol + static_cast<uint32_t>(ch * a.NN);
-                    for (int fh = is; fh < a.FH; fh += kTcIssuers, ++item) {
+                    for (int fh = par; fh < a.FH; fh += 2, ++item) {
                         const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
                         const uint32_t phase = (item / kTcRingSlots) & 1u;
-                        if (!tc_wait(&toep_full[slot], phase, a, abort_flag)) { ok = false; break; }
+                        if (!mbar_try_wait(&toep_full[slot], phase) &&
+                            !tc_wait(&toep_full[slot], phase, a, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                         uint64_t ad = ap + static_cast<uint32_t>(fh);
                         uint64_t bd = bdesc0 + slot * b_slot;
-                        tc_mma(dch, ad, bd, idesc, fh != is ? 1u : 0u);
+                        tc_mma(dch, ad, bd, idesc, fh != par ? 1u : 0u);
                         for (int ks = 1; ks < a.KS; ++ks) {
                             ad += a_ks;
                             bd += 16u;
@@ -375,8 +383,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
                         tc_commit(&toep_empty[slot]);   // slot free once these MMAs finish
                     }
                     if (!ok) break;
-                    tc_commit(&plane_empty[pr.slot]);
-                    pr.next(a.ps);
+                    tc_commit(&plane_empty[pslot]);
                 }
                 if (!ok) break;
                 tc_commit(&d_full[db]);
@@ -460,11 +467,11 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
             db ^= 1u;
             if (db == 0) dphase ^= 1u;
         }
-    } else if (tc_is_loader(warp)) {
+    } else if (warp >= kTcLoad0) {
         // ------------------------------------------------------------- loaders
         using Pix = TcPix<CG>;
         using V = typename Pix::V;
-        const int lt = tc_loader_index(warp) * 32 + lane;   // 0 .. 32*kTcLoadWarps-1
+        const int lt = (warp - kTcLoad0) * 32 + lane;   // 0 .. 32*kTcLoadWarps-1
         const T* X = static_cast<const T*>(a.x);
         const int KC = 2 * a.KS;
         const int tasks = a.MR * KC;  // (row, 8-column chunk), row fastest
@@ -543,17 +550,16 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
         }
     } else {
         // ------------------------------------------------------------- Toeplitz builders
-        // Builder warp bw writes, in order, the Toeplitz runs of the filter rows MMA issuer
-        // bw takes (fh = bw, bw + kTcIssuers, ...) into that issuer's ring.  The unit's
+        // Builder warp i writes, in order, the Toeplitz runs of the (channel, filter row)
+        // items MMA issuer i takes into that issuer's ring.  The unit's
         // filters (8 channels around the group) arrive by one TMA copy per unit into one of
         // the staging slots (two where they fit: the next unit's copy then travels while this
         // unit's runs are built).
-        const int bidx = tc_builder_index(warp);
-        const int bw = bidx % kTcIssuers;         // the ring (issuer) this warp feeds
-        const int bsub = bidx / kTcIssuers;       // which of the ring's alternate items it builds
+        const int bidx = warp - kTcBuild0;        // the ring (issuer) this warp feeds
+        const int bpar = bidx & 1, bchs = bidx >> 1;
         const int rows = 8 * a.NCM;
         const int nz = (rows + 7 + 31) / 32;   // z chunks a lane holds (<= kTcMaxZ)
-        const uint32_t ring0 = static_cast<uint32_t>(bw) * kTcRingSlots;
+        const uint32_t ring0 = static_cast<uint32_t>(bidx) * kTcRingSlots;
         uint32_t item = 0;
         bool ok = true;
         // Staging slot k % ws holds the filters of the CTA's unit k.  Builder warp 0's lane 0
@@ -587,9 +593,8 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
             // channel ch of the group sits at lane (g*CG) % 8 + ch of each staged tap
             const uint16_t* wtap = reinterpret_cast<const uint16_t*>(wst + sl * a.wst_bytes) +
                                    ((g * CG) & 7);
-            for (int ch = 0; ch < CG && ok; ++ch) {
-                for (int fh = bw; fh < a.FH; fh += kTcIssuers, ++item) {
-                    if (static_cast<int>(item & 1u) != bsub) continue;
+            for (int ch = bchs; ch < CG && ok; ch += 2) {
+                for (int fh = bpar; fh < a.FH; fh += 2, ++item) {
                     const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
                     const uint32_t phase = (item / kTcRingSlots) & 1u;
                     if (!tc_wait_warp(&toep_empty[slot], phase ^ 1u, a, abort_flag)) { ok = false; break; }
@@ -693,19 +698,25 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
                                            : static_cast<long long>(p.N) * a.bands;
     if (static_cast<long long>(p.N + 1) * a.S + 2 * kTcM >= (1LL << 31)) return false;
     a.MR = (p.FH + kTcM - 1 + 7) / 8 * 8;
-    // column tiles: the fewest MMA cycles per output column
+    // column tiles: the fewest MMA cycles per output column, among the tiles whose
+    // accumulators (two parities x at least two channels, double-buffered) and shared memory
+    // (Toeplitz rings, filter staging, three planes) fit
     const int cap = device_info().max_smem_optin;
+    const size_t wst_min = static_cast<size_t>((p.FH * p.FW * 16 + 127) / 128 * 128);
     double best = 1e30;
     int best_nt = 0;
-    for (int nt = 1; nt <= 16; ++nt) {
+    for (int nt = 1; nt <= 32; ++nt) {
         const int twc = (p.OW + nt - 1) / nt;
         const int nn = (twc + 15) / 16 * 16;
-        if (nn > 256 || (nt > 1 && (p.OW + twc - 1) / twc < nt)) continue;
+        if (kTcPartials * 2 * nn > kTcDCols || (nt > 1 && (p.OW + twc - 1) / twc < nt)) continue;
         const int ks = (nn + p.FW - 1 + 15) / 16;
-        if (8 * (nn / 8 + 2 * ks - 1) > 32 * (kTcMaxZ - 1)) continue;   // the builders' run limit
-        const double cost = nt * ks * tc_mma_cycles(nn);
+        const int ncm = nn / 8 + 2 * ks - 1;
+        if (8 * ncm > 32 * (kTcMaxZ - 1)) continue;   // the builders' run limit
         const size_t plane = static_cast<size_t>(2 * ks) * a.MR * 16;
-        if (plane * 4 + 4096 > static_cast<size_t>(cap)) continue;
+        const size_t need = 3 * plane + static_cast<size_t>(kTcMaxToep) * ncm * 128 + wst_min +
+                            kTcBarBytes;
+        if (need > static_cast<size_t>(cap)) continue;
+        const double cost = nt * ks * tc_mma_cycles(nn);
         if (cost < best) { best = cost; best_nt = nt; }
     }
     if (best_nt == 0) return false;
@@ -722,7 +733,7 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     int cg = 0;
     long long best_t = 0;
     for (int c = 8; c >= 2; c /= 2) {
-        if (kTcIssuers * c * a.NN > kTcDCols || p.C % c != 0) continue;
+        if (kTcPartials * c * a.NN > kTcDCols || p.C % c != 0) continue;
         const long long units = row_tiles * a.col_tiles * (p.C / c);
         const long long t = (units + sms - 1) / sms * c;
         if (cg == 0 || t < best_t) { cg = c; best_t = t; }
