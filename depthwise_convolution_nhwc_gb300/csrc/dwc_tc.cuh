@@ -25,16 +25,20 @@
 //    MMA covers, for example, two 56-row images; rows in the gaps are computed and dropped.
 //
 // Warp roles per CTA (one CTA per SM, persistent over units of (row tile, column tile, group
-// of CG channels)):
+// of CG = 4 or 8 channels)):
 //  * 4 epilogue warps -- warp w reads the 32-lane quadrant w of the accumulators
-//    (tcgen05.ld), adds the two partial sums and writes CG channels of a pixel per store;
-//  * 4 MMA warps: one lane each issues the MMAs of half the channels and one filter-row
-//    parity into the partial sum of that parity (a single thread issues an MMA only every
-//    ~100 cycles, an M=128 N=64 MMA takes 48); the first also allocates the tensor memory;
-//  * 4 builder warps, one per issuer: write the Toeplitz core matrices of the issuer's
-//    (channel, filter row) items into its ring; one of them stages the filters;
-//  * 6 loader warps: gather the unit's input rows (CG channels per load) and store them
-//    transposed into the per-channel planes (zeros in the padding).
+//    (tcgen05.ld) and writes the CG channels of a pixel with 16-byte stores;
+//  * 4 MMA warps: one lane each issues the MMAs of every fourth channel of the group (a
+//    single thread issues an MMA only every ~100 cycles, an M=128 N=32 MMA takes 40); the
+//    first also allocates the tensor memory;
+//  * 8 builder warps, two per issuer taking turns: write the Toeplitz core matrices of the
+//    issuer's (channel, filter row) items into its ring (one warp builds an item in about
+//    0.4 us, the tensor core takes four items, one per ring, in about 0.33 us); one of them
+//    stages the filters;
+//  * 6 loader warps: gather the unit's input rows (CG channels, 8 or 16 bytes, per load) and
+//    store them transposed into the per-channel planes (zeros in the padding).
+// Groups of at least four channels keep the scattered global accesses of the gather and the
+// stores (one cache line per pixel, whatever its width) well below the tensor core's time.
 // Stages pass through mbarrier rings; every wait has a time limit and a shared abort flag,
 // so a lost arrival ends the kernel (status word set) instead of hanging it.  Backward data
 // uses the same kernel with the filter read rotated by 180 degrees.
@@ -49,36 +53,35 @@
 namespace dwc {
 
 constexpr int kTcM = 128;           // MMA rows (tensor-memory lanes)
-// Roles (18 warps; warp w runs on sub-partition w % 4):
+// Roles (22 warps; warp w runs on sub-partition w % 4):
 //   0-3   epilogue, warp w reading the 32-lane quadrant w of tensor memory
-//   4-7   MMA issuers, one lane each: issuer i takes the channels c with c % 2 == i / 2 and
-//         the filter rows with fh % 2 == i % 2 (one thread issues an MMA only every ~100
-//         cycles, four keep the tensor core's 48-cycle pace); warp 4 also allocates the
-//         tensor memory
-//   8-11  Toeplitz builders, builder i feeding issuer i's ring
-//   12-17 loaders
+//   4-7   MMA issuers, one lane each: issuer i takes the channels c with c % 4 == i, every
+//         filter row of them (one thread issues an MMA only every ~100 cycles, four keep
+//         the tensor core's pace); warp 4 also allocates the tensor memory
+//   8-15  Toeplitz builders, warps 8 + i and 12 + i feeding issuer i's ring in turn
+//   16-21 loaders
 constexpr int kTcEpiWarps = 4;
 constexpr int kTcMmaWarp = 4;       // first MMA warp
 constexpr int kTcIssuers = 4;       // MMA-issuing threads (one per MMA warp)
 constexpr int kTcBuild0 = kTcMmaWarp + kTcIssuers;
-constexpr int kTcBuildWarps = 4;
+constexpr int kTcBuildWarps = 8;     // two per issuer ring
 constexpr int kTcLoad0 = kTcBuild0 + kTcBuildWarps;
 constexpr int kTcLoadWarps = 6;
 constexpr int kTcWarps = kTcLoad0 + kTcLoadWarps;
 constexpr int kTcRingSlots = 4;     // Toeplitz slots per issuer ring (a power of two)
-constexpr int kTcPartials = 2;      // partial sums per channel (one per filter-row parity)
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcTmemCols = 512;
 constexpr int kTcDCols = 256;       // columns of one accumulator buffer (two buffers)
-constexpr int kTcMaxPlanes = 8;
+constexpr int kTcMaxPlanes = 16;
 constexpr int kTcMaxToep = 16;      // kTcIssuers rings of kTcRingSlots
 // barriers (plane and Toeplitz rings, two accumulator buffers, the final MMA barrier), the
 // tensor-memory address and the abort flag
 constexpr int kTcMaxZ = 12;          // Toeplitz run of at most 32 * (kTcMaxZ - 1) rows
 constexpr int kTcBarBytes =
     ((2 * kTcMaxPlanes + 2 * kTcMaxToep + 2 * 2 + kTcIssuers + 2 * 2) * 8 + 8 + 127) / 128 * 128;
-static_assert(kTcBuildWarps == kTcIssuers && kTcIssuers * kTcRingSlots == kTcMaxToep,
-              "builder warp i feeds issuer i's ring");
+static_assert(kTcBuildWarps == 2 * kTcIssuers && kTcIssuers * kTcRingSlots == kTcMaxToep &&
+                  kTcRingSlots % 2 == 0,
+              "builder warps i and i + kTcIssuers feed issuer i's ring, alternate items");
 
 struct TcArgs {
     const void* x;      // N x H x W x C, 16-bit
@@ -239,11 +242,6 @@ __device__ __forceinline__ void tc_unit(const TcArgs& a, uint32_t u, int& t, int
 template <int CG>
 struct TcPix;   // CG 16-bit channels of one pixel, as loaded
 template <>
-struct TcPix<2> {
-    using V = uint32_t;
-    __device__ static __forceinline__ V zero() { return 0u; }
-};
-template <>
 struct TcPix<4> {
     using V = uint2;
     __device__ static __forceinline__ V zero() { return make_uint2(0u, 0u); }
@@ -258,9 +256,7 @@ struct TcPix<8> {
 // (the high half is garbage).
 template <int CG>
 __device__ __forceinline__ uint32_t tc_word(const typename TcPix<CG>::V& v, int ch) {
-    if constexpr (CG == 2) {
-        return v;
-    } else if constexpr (CG == 4) {
+    if constexpr (CG == 4) {
         return ch < 2 ? v.x : v.y;
     } else {
         return ch < 2 ? v.x : (ch < 4 ? v.y : (ch < 6 ? v.z : v.w));
@@ -274,9 +270,38 @@ __device__ __forceinline__ uint32_t tc_pair(const typename TcPix<CG>::V& lo,
     return __byte_perm(tc_word<CG>(lo, ch), tc_word<CG>(hi, ch), (ch & 1) ? 0x7632u : 0x5410u);
 }
 
+// The CG channels of one output pixel, one or two 16-byte streaming stores (fp32), or one
+// 8- or 16-byte store of values rounded to nearest even (bf16, fp16).
+template <class OutT, int CG>
+__device__ __forceinline__ void tc_store_pixel(OutT* dst, const float (&v)[CG]) {
+    if constexpr (std::is_same<OutT, float>::value) {
+#pragma unroll
+        for (int c = 0; c < CG; c += 4)
+            __stcs(reinterpret_cast<float4*>(dst + c), make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]));
+    } else {
+        uint32_t h[CG / 2];
+#pragma unroll
+        for (int c = 0; c < CG; c += 2) {
+            if constexpr (std::is_same<OutT, __nv_bfloat16>::value) {
+                const __nv_bfloat162 b = __float22bfloat162_rn(make_float2(v[c], v[c + 1]));
+                h[c / 2] = *reinterpret_cast<const uint32_t*>(&b);
+            } else {
+                const __half2 b = __float22half2_rn(make_float2(v[c], v[c + 1]));
+                h[c / 2] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+        }
+        if constexpr (CG == 4) {
+            __stcs(reinterpret_cast<uint2*>(dst), make_uint2(h[0], h[1]));
+        } else {
+            __stcs(reinterpret_cast<uint4*>(dst), make_uint4(h[0], h[1], h[2], h[3]));
+        }
+    }
+}
+
 template <typename T, bool FLIP, class OutT, int CG>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
+    static_assert(CG % kTcIssuers == 0, "every issuer takes whole channels of the group");
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* planes = smem;
     unsigned char* toep = smem + a.off_toep;
@@ -299,7 +324,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.ps; ++s) {
             mbar_init(&plane_full[s], kTcLoadWarps);
-            mbar_init(&plane_empty[s], 2);   // the two filter-row parities of its channel
+            mbar_init(&plane_empty[s], 1);   // the issuer of its channel
         }
         for (int s = 0; s < a.ts; ++s) {
             mbar_init(&toep_full[s], 1);
@@ -331,11 +356,8 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
 
     if (warp >= kTcMmaWarp && warp < kTcMmaWarp + kTcIssuers) {
         // ------------------------------------------------------------- MMA issue
-        // Issuer `is` takes the channels c of the group with c % 2 == is / 2 and the filter
-        // rows fh with fh % 2 == is % 2, and accumulates into the partial sum of its parity
-        // (the epilogue adds the two parities).
+        // Issuer `is` takes the channels c of the group with c % 4 == is, all filter rows.
         const int is = warp - kTcMmaWarp;
-        const int par = is & 1, chs = is >> 1;
         if (lane == 0) {
             uint32_t db = 0, dphase = 0;
             bool ok = true;
@@ -356,8 +378,8 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
             for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x, pos0 += CG) {
                 if (!tc_wait(&d_empty[db], dphase ^ 1u, a, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t dcol = tmem + db * kTcDCols + static_cast<uint32_t>(par * CG * a.NN);
-                for (int ch = chs; ch < CG && ok; ch += 2) {
+                const uint32_t dcol = tmem + db * kTcDCols;
+                for (int ch = is; ch < CG && ok; ch += kTcIssuers) {
                     // channel ch of this unit sits at plane-ring position pos0 + ch (the
                     // loaders fill the ring in order; this issuer skips the other channels)
                     const uint32_t pos = pos0 + static_cast<uint32_t>(ch);
@@ -366,7 +388,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
                     tc_fence_after();
                     const uint64_t ap = adesc0 + pslot * a_slot;
                     const uint32_t dch = dcol + static_cast<uint32_t>(ch * a.NN);
-                    for (int fh = par; fh < a.FH; fh += 2, ++item) {
+                    for (int fh = 0; fh < a.FH; ++fh, ++item) {
                         const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
                         const uint32_t phase = (item / kTcRingSlots) & 1u;
                         if (!mbar_try_wait(&toep_full[slot], phase) &&
@@ -374,7 +396,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
                         tc_fence_after();
                         uint64_t ad = ap + static_cast<uint32_t>(fh);
                         uint64_t bd = bdesc0 + slot * b_slot;
-                        tc_mma(dch, ad, bd, idesc, fh != par ? 1u : 0u);
+                        tc_mma(dch, ad, bd, idesc, fh != 0 ? 1u : 0u);
                         for (int ks = 1; ks < a.KS; ++ks) {
                             ad += a_ks;
                             bd += 16u;
@@ -397,10 +419,8 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
         __syncwarp();
     } else if (warp < kTcEpiWarps) {
         // ------------------------------------------------------------- epilogue
-        const int quad = warp, half = 0;   // one warp per quadrant, every column
+        const int quad = warp;   // one warp per quadrant, every column
         const int m = quad * 32 + lane;   // accumulator row = tensor-memory lane
-        // the second partial sum exists only when there is more than one filter row
-        const bool two = a.FH > 1;
         uint32_t db = 0, dphase = 0;
         for (uint32_t u = blockIdx.x; u < a.units; u += gridDim.x) {
             int t, j, g;
@@ -420,21 +440,13 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
                          (static_cast<size_t>(row_ok ? n : 0) * a.OH + (row_ok ? r : 0)) *
                              static_cast<size_t>(a.OW) * a.C + c0;
             const uint32_t dcol = tmem + db * kTcDCols + (static_cast<uint32_t>(quad * 32) << 16);
-            const uint32_t dcol1 = dcol + static_cast<uint32_t>(CG * a.NN);
             // columns per round: CG x CW sums in registers (32 values)
             constexpr int CW = 32 / CG;
-            for (int cc = half * CW; cc < a.NN; cc += CW) {
-                float acc[CG][CW];
+            for (int cc = 0; cc < a.NN; cc += CW) {
+                uint32_t acc[CG][CW];
 #pragma unroll
-                for (int ch = 0; ch < CG; ++ch) {
-                    uint32_t p0[CW], p1[CW];
-                    tc_ld(dcol + ch * a.NN + cc, p0);
-                    if (two) tc_ld(dcol1 + ch * a.NN + cc, p1);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int q = 0; q < CW; ++q)
-                        acc[ch][q] = __uint_as_float(p0[q]) + (two ? __uint_as_float(p1[q]) : 0.f);
-                }
+                for (int ch = 0; ch < CG; ++ch) tc_ld(dcol + ch * a.NN + cc, acc[ch]);
+                tc_wait_ld();
                 if (row_ok) {
 #pragma unroll
                     for (int q = 0; q < CW; ++q) {
@@ -442,22 +454,8 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
                         if (ow < ow0 || ow >= ow_end) continue;
                         float vals[CG];
 #pragma unroll
-                        for (int ch = 0; ch < CG; ++ch) vals[ch] = acc[ch][q];
-                        OutT* dst = orow + static_cast<size_t>(ow) * a.C;
-                        if constexpr (std::is_same<OutT, float>::value) {
-                            if constexpr (CG == 2) {
-                                __stcs(reinterpret_cast<float2*>(dst), make_float2(vals[0], vals[1]));
-                            } else {
-#pragma unroll
-                                for (int ch = 0; ch < CG; ch += 4)
-                                    __stcs(reinterpret_cast<float4*>(dst + ch),
-                                           make_float4(vals[ch], vals[ch + 1], vals[ch + 2], vals[ch + 3]));
-                            }
-                        } else {
-#pragma unroll
-                            for (int ch = 0; ch < CG; ch += 2)
-                                store_out_pair(dst + ch, make_float2(vals[ch], vals[ch + 1]));
-                        }
+                        for (int ch = 0; ch < CG; ++ch) vals[ch] = __uint_as_float(acc[ch][q]);
+                        tc_store_pixel<OutT, CG>(orow + static_cast<size_t>(ow) * a.C, vals);
                     }
                 }
             }
@@ -550,20 +548,21 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
         }
     } else {
         // ------------------------------------------------------------- Toeplitz builders
-        // Builder warp i writes, in order, the Toeplitz runs of the (channel, filter row)
-        // items MMA issuer i takes into that issuer's ring.  The unit's
+        // Builder warps i and i + 4 write, in turn (even and odd items), the Toeplitz runs of
+        // the (channel, filter row) items MMA issuer i takes into that issuer's ring.  The unit's
         // filters (8 channels around the group) arrive by one TMA copy per unit into one of
         // the staging slots (two where they fit: the next unit's copy then travels while this
         // unit's runs are built).
-        const int bidx = warp - kTcBuild0;        // the ring (issuer) this warp feeds
-        const int bpar = bidx & 1, bchs = bidx >> 1;
+        const int bidx = warp - kTcBuild0;
+        const int ring = bidx % kTcIssuers;                  // the ring (issuer) this warp feeds
+        const uint32_t turn = static_cast<uint32_t>(bidx / kTcIssuers);   // its items' parity
         const int rows = 8 * a.NCM;
         const int nz = (rows + 7 + 31) / 32;   // z chunks a lane holds (<= kTcMaxZ)
-        const uint32_t ring0 = static_cast<uint32_t>(bidx) * kTcRingSlots;
+        const uint32_t ring0 = static_cast<uint32_t>(ring) * kTcRingSlots;
         uint32_t item = 0;
         bool ok = true;
         // Staging slot k % ws holds the filters of the CTA's unit k.  Builder warp 0's lane 0
-        // issues the copies: units 0 .. ws-1 up front, unit k + ws once both builders have
+        // issues the copies: units 0 .. ws-1 up front, unit k + ws once every builder has
         // released unit k's slot.
         const uint32_t ws = static_cast<uint32_t>(a.ws);
         uint32_t issued = 0;   // filter copies issued
@@ -593,8 +592,9 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
             // channel ch of the group sits at lane (g*CG) % 8 + ch of each staged tap
             const uint16_t* wtap = reinterpret_cast<const uint16_t*>(wst + sl * a.wst_bytes) +
                                    ((g * CG) & 7);
-            for (int ch = bchs; ch < CG && ok; ch += 2) {
-                for (int fh = bpar; fh < a.FH; fh += 2, ++item) {
+            for (int ch = ring; ch < CG && ok; ch += kTcIssuers) {
+                for (int fh = 0; fh < a.FH; ++fh, ++item) {
+                    if ((item & 1u) != turn) continue;   // the other warp's item
                     const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
                     const uint32_t phase = (item / kTcRingSlots) & 1u;
                     if (!tc_wait_warp(&toep_empty[slot], phase ^ 1u, a, abort_flag)) { ok = false; break; }
@@ -698,26 +698,48 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
                                            : static_cast<long long>(p.N) * a.bands;
     if (static_cast<long long>(p.N + 1) * a.S + 2 * kTcM >= (1LL << 31)) return false;
     a.MR = (p.FH + kTcM - 1 + 7) / 8 * 8;
-    // column tiles: the fewest MMA cycles per output column, among the tiles whose
-    // accumulators (two parities x at least two channels, double-buffered) and shared memory
-    // (Toeplitz rings, filter staging, three planes) fit
+    // Column tile and channel group, chosen together by an estimate of the busiest SM's
+    // cycles: the MMAs of its units (units spread evenly over the SMs, whole units only),
+    // plus, where shared memory cannot hold the planes of two units (the next unit's gather
+    // then waits for the end of the current one), the gather's one cache line per pixel.
+    // Constraints: two accumulator buffers of CG x NN columns in tensor memory, the
+    // builders' run limit, and the planes, Toeplitz rings and filter staging in shared memory.
     const int cap = device_info().max_smem_optin;
-    const size_t wst_min = static_cast<size_t>((p.FH * p.FW * 16 + 127) / 128 * 128);
+    const int sms = device_info().sm_count;
+    const size_t wst_bytes = static_cast<size_t>((p.FH * p.FW * 16 + 127) / 128 * 128);
     double best = 1e30;
-    int best_nt = 0;
+    int best_nt = 0, best_cg = 0, best_ps = 0, best_ws = 0;
     for (int nt = 1; nt <= 32; ++nt) {
         const int twc = (p.OW + nt - 1) / nt;
         const int nn = (twc + 15) / 16 * 16;
-        if (kTcPartials * 2 * nn > kTcDCols || (nt > 1 && (p.OW + twc - 1) / twc < nt)) continue;
+        if (nt > 1 && (p.OW + twc - 1) / twc < nt) continue;
         const int ks = (nn + p.FW - 1 + 15) / 16;
         const int ncm = nn / 8 + 2 * ks - 1;
         if (8 * ncm > 32 * (kTcMaxZ - 1)) continue;   // the builders' run limit
         const size_t plane = static_cast<size_t>(2 * ks) * a.MR * 16;
-        const size_t need = 3 * plane + static_cast<size_t>(kTcMaxToep) * ncm * 128 + wst_min +
-                            kTcBarBytes;
-        if (need > static_cast<size_t>(cap)) continue;
-        const double cost = nt * ks * tc_mma_cycles(nn);
-        if (cost < best) { best = cost; best_nt = nt; }
+        const size_t toep_ring = static_cast<size_t>(kTcMaxToep) * ncm * 128;
+        const long long tiles = row_tiles * ((p.OW + twc - 1) / twc);
+        for (int cg = 8; cg >= 4; cg /= 2) {
+            if (cg * nn > kTcDCols || p.C % cg != 0) continue;
+            // plane slots beside one or two filter staging slots; two where that still
+            // leaves room for two units' planes (or costs no plane)
+            auto slots = [&](int w) -> int {
+                const size_t fixed = w * wst_bytes + kTcBarBytes + toep_ring;
+                if (fixed >= static_cast<size_t>(cap)) return 0;
+                return static_cast<int>(std::min<size_t>(kTcMaxPlanes, (cap - fixed) / plane));
+            };
+            const int ps2 = slots(2), ps1 = slots(1);
+            const int ws = (ps2 >= 2 * cg || ps2 == ps1) ? 2 : 1;
+            const int ps = ws == 2 ? ps2 : ps1;
+            if (ps < cg + 1) continue;   // the next unit's planes must fill while one computes
+            const long long units = tiles * (p.C / cg);
+            const double unit = cg * p.FH * ks * tc_mma_cycles(nn) +
+                                (ps >= 2 * cg ? 0.0 : static_cast<double>(a.MR) * 16 * ks);
+            const double cost = static_cast<double>((units + sms - 1) / sms) * unit;
+            if (cost < best) {
+                best = cost; best_nt = nt; best_cg = cg; best_ps = ps; best_ws = ws;
+            }
+        }
     }
     if (best_nt == 0) return false;
     a.TWc = (p.OW + best_nt - 1) / best_nt;
@@ -727,41 +749,21 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     a.NCM = a.NN / 8 + 2 * a.KS - 1;
     a.plane_bytes = static_cast<uint32_t>(2 * a.KS) * a.MR * 16u;
     a.toep_bytes = static_cast<uint32_t>(a.NCM) * 128u;
-    // channels per unit: as many as two accumulator buffers hold, then fewer where that
-    // evens out the units over the SMs
-    const int sms = device_info().sm_count;
-    int cg = 0;
-    long long best_t = 0;
-    for (int c = 8; c >= 2; c /= 2) {
-        if (kTcPartials * c * a.NN > kTcDCols || p.C % c != 0) continue;
-        const long long units = row_tiles * a.col_tiles * (p.C / c);
-        const long long t = (units + sms - 1) / sms * c;
-        if (cg == 0 || t < best_t) { cg = c; best_t = t; }
-    }
-    if (cg == 0) return false;
-    P.cg = cg;
-    a.ncg = p.C / cg;
+    P.cg = best_cg;
+    a.ncg = p.C / best_cg;
     const long long units = row_tiles * a.col_tiles * a.ncg;
     if (units >= (1LL << 31)) return false;
     a.units = static_cast<uint32_t>(units);
     a.fd_S.init(static_cast<uint32_t>(a.S));
-    // shared memory: plane ring, Toeplitz ring, filter staging, barriers
-    // two staging slots of the filter taps (8 channels of each tap, one TMA box)
+    // shared memory: plane ring, Toeplitz ring, filter staging slots (one TMA box of the
+    // FH x FW taps of 8 channels each), barriers
     a.wst_tx = static_cast<uint32_t>(p.FH) * p.FW * 16u;
     a.wst_bytes = (a.wst_tx + 127u) / 128u * 128u;
     a.ts = kTcMaxToep;
+    a.ws = best_ws;
+    a.ps = best_ps;
     const size_t toep_ring = static_cast<size_t>(a.ts) * a.toep_bytes;
-    // two staging slots where the next unit's filters fit beside the planes, else one
-    a.ws = 2;
-    if (2 * static_cast<size_t>(a.wst_bytes) + kTcBarBytes + toep_ring +
-            static_cast<size_t>(cg + 1) * a.plane_bytes > static_cast<size_t>(cap))
-        a.ws = 1;
     const size_t wst = static_cast<size_t>(a.ws) * a.wst_bytes;
-    const size_t fixed = wst + kTcBarBytes;
-    if (fixed + toep_ring + static_cast<size_t>(cg) * a.plane_bytes > static_cast<size_t>(cap))
-        return false;
-    a.ps = static_cast<int>(std::min<size_t>(kTcMaxPlanes, (cap - fixed - toep_ring) / a.plane_bytes));
-    if (a.ps < cg + 1) return false;   // the next unit's planes must fill while one computes
     a.off_toep = static_cast<uint32_t>(static_cast<size_t>(a.ps) * a.plane_bytes);
     a.off_wst = a.off_toep + static_cast<uint32_t>(toep_ring);
     a.off_bar = a.off_wst + static_cast<uint32_t>(wst);
@@ -812,9 +814,9 @@ cudaError_t launch_tc_rows(const RowConv& p) {
     if (!tc_plan(p, P)) return cudaErrorNotSupported;
     if (P.a.units == 0) return cudaSuccess;
     switch (P.cg) {
-        case 2: return p.flip ? launch_tc_inst<T, true, OutT, 2>(P, p) : launch_tc_inst<T, false, OutT, 2>(P, p);
         case 4: return p.flip ? launch_tc_inst<T, true, OutT, 4>(P, p) : launch_tc_inst<T, false, OutT, 4>(P, p);
-        default: return p.flip ? launch_tc_inst<T, true, OutT, 8>(P, p) : launch_tc_inst<T, false, OutT, 8>(P, p);
+        case 8: return p.flip ? launch_tc_inst<T, true, OutT, 8>(P, p) : launch_tc_inst<T, false, OutT, 8>(P, p);
+        default: return cudaErrorNotSupported;
     }
 }
 
