@@ -25,6 +25,7 @@ struct PerDevice {
     bool ready = false;
     DeviceInfo info{};
     unsigned int* status = nullptr;
+    cudaMemPool_t pool = nullptr;   // scratch of the kernels that need some (created on use)
 };
 
 PerDevice g_dev[kMaxDevices];
@@ -60,6 +61,38 @@ PerDevice* device_state() {
 }
 
 }  // namespace
+
+// Memory the pool keeps between calls instead of returning it to the driver.
+constexpr uint64_t kScratchKeepBytes = 512ull << 20;
+
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t stream) {
+    *p = nullptr;
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return cudaErrorInvalidDevice;
+    PerDevice* s = device_state();
+    if (s == nullptr) return cudaErrorInvalidDevice;
+    cudaMemPool_t pool = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (s->pool == nullptr) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = d;
+            cudaMemPool_t created = nullptr;
+            if (cudaMemPoolCreate(&created, &props) != cudaSuccess) return cudaErrorMemoryAllocation;
+            uint64_t keep = kScratchKeepBytes;
+            (void)cudaMemPoolSetAttribute(created, cudaMemPoolAttrReleaseThreshold, &keep);
+            s->pool = created;
+        }
+        pool = s->pool;
+    }
+    return cudaMallocFromPoolAsync(p, bytes, pool, stream);
+}
+
+void scratch_free(void* p, cudaStream_t stream) {
+    if (p != nullptr) (void)cudaFreeAsync(p, stream);
+}
 
 const DeviceInfo& device_info() {
     static const DeviceInfo fallback{152, 232448};  // GB300, used only when no device answers

@@ -98,6 +98,12 @@ struct DeviceInfo {
 };
 const DeviceInfo& device_info();
 
+// Stream-ordered scratch memory of one call, from a memory pool the library owns (one per
+// device, created on first use; it keeps up to 512 MiB between calls).  scratch_free
+// returns the block to the pool in stream order, after the work queued before it.
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t stream);
+void scratch_free(void* p, cudaStream_t stream);
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda needed).
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* base,
                       const cuuint64_t* dims, const cuuint64_t* strides_bytes,

@@ -17,31 +17,36 @@
 //    rows are 16 bytes apart, so the shift by fh is just a start address 16*fh bytes later.
 //  * T: a Toeplitz matrix is constant along its diagonals.  With the output columns taken in
 //    reverse order (n' = N-1-n) every 8x8 core matrix depends only on the sum of its block
-//    indices, so the whole matrix is N/8 + K/8 - 1 distinct core matrices laid end to end,
-//    and a descriptor with both strides 128 bytes reads every block of the K x N matrix.
-//    The epilogue undoes the reversal.
+//    indices, so the whole matrix is N/8 + K/8 - 1 distinct core matrices laid end to end
+//    (a "run"), and a descriptor with both strides 128 bytes reads every block of the K x N
+//    matrix.  The epilogue undoes the reversal.
 //  * Rows of the tile run through several images: image n occupies the S rows starting at
 //    virtual row n*S (S = image rows + padding shared with the next image), so one 128-row
 //    MMA covers, for example, two 56-row images; rows in the gaps are computed and dropped.
+//
+// Two launches.  A preparation kernel writes, into scratch memory of the call,
+//  * the input as per-channel planes in the layout above: channel-major, the images' rows
+//    stacked on the virtual rows (zero rows between images) and the columns padded so that
+//    every tile's first column falls on an 8-column boundary -- one TMA box then fills one
+//    8-column plane of a unit, with no gather and no transposition in the main kernel;
+//  * every Toeplitz run (channel, filter row), rotated by 180 degrees for backward data.
+// The main kernel then only moves data with the copy engines: TMA boxes for the planes,
+// bulk copies for the runs.  Gathering and transposing inside it (one cache line per
+// pixel and channel group, and shuffles to build the runs) tied up the load/store and
+// shared-memory pipes that the MMA issuers and their barriers also go through.
 //
 // Warp roles per CTA (one CTA per SM, persistent over units of (row tile, column tile, group
 // of CG = 4 or 8 channels)):
 //  * 4 epilogue warps -- warp w reads the 32-lane quadrant w of the accumulators
 //    (tcgen05.ld) and writes the CG channels of a pixel with 16-byte stores;
 //  * 4 MMA warps: one lane each issues the MMAs of every fourth channel of the group (a
-//    single thread issues an MMA only every ~100 cycles, an M=128 N=32 MMA takes 40); the
+//    single thread issues an MMA only every ~100 cycles, an M=128 N=32 MMA takes 46); the
 //    first also allocates the tensor memory;
-//  * 8 builder warps, two per issuer taking turns: write the Toeplitz core matrices of the
-//    issuer's (channel, filter row) items into its ring (one warp builds an item in about
-//    0.4 us, the tensor core takes four items, one per ring, in about 0.33 us); one of them
-//    stages the filters;
-//  * 6 loader warps: gather the unit's input rows (CG channels, 8 or 16 bytes, per load) and
-//    store them transposed into the per-channel planes (zeros in the padding).
-// Groups of at least four channels keep the scattered global accesses of the gather and the
-// stores (one cache line per pixel, whatever its width) well below the tensor core's time.
+//  * 4 run feeders: one lane each copies, in order, the runs of its issuer's items into
+//    that issuer's ring;
+//  * 1 plane feeder: one lane loads the units' planes into the plane ring.
 // Stages pass through mbarrier rings; every wait has a time limit and a shared abort flag,
-// so a lost arrival ends the kernel (status word set) instead of hanging it.  Backward data
-// uses the same kernel with the filter read rotated by 180 degrees.
+// so a lost arrival ends the kernel (status word set) instead of hanging it.
 #pragma once
 
 #include <algorithm>
@@ -53,60 +58,53 @@
 namespace dwc {
 
 constexpr int kTcM = 128;           // MMA rows (tensor-memory lanes)
-// Roles (22 warps; warp w runs on sub-partition w % 4):
+// Roles (13 warps; warp w runs on sub-partition w % 4):
 //   0-3   epilogue, warp w reading the 32-lane quadrant w of tensor memory
 //   4-7   MMA issuers, one lane each: issuer i takes the channels c with c % 4 == i, every
-//         filter row of them (one thread issues an MMA only every ~100 cycles, four keep
-//         the tensor core's pace); warp 4 also allocates the tensor memory
-//   8-15  Toeplitz builders, warps 8 + i and 12 + i feeding issuer i's ring in turn
-//   16-21 loaders
+//         filter row of them; warp 4 also allocates the tensor memory
+//   8-11  run feeders, feeder i filling issuer i's ring
+//   12    plane feeder
 constexpr int kTcEpiWarps = 4;
 constexpr int kTcMmaWarp = 4;       // first MMA warp
 constexpr int kTcIssuers = 4;       // MMA-issuing threads (one per MMA warp)
-constexpr int kTcBuild0 = kTcMmaWarp + kTcIssuers;
-constexpr int kTcBuildWarps = 8;     // two per issuer ring
-constexpr int kTcLoad0 = kTcBuild0 + kTcBuildWarps;
-constexpr int kTcLoadWarps = 6;
-constexpr int kTcWarps = kTcLoad0 + kTcLoadWarps;
-constexpr int kTcRingSlots = 4;     // Toeplitz slots per issuer ring (a power of two)
+constexpr int kTcFeed0 = kTcMmaWarp + kTcIssuers;
+constexpr int kTcPlaneWarp = kTcFeed0 + kTcIssuers;
+constexpr int kTcWarps = kTcPlaneWarp + 1;
 constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kTcRingSlots = 4;     // run slots per issuer ring (a power of two)
+constexpr int kTcRunsPerSlot = 2;   // most filter rows per ring item (runs per slot)
 constexpr int kTcTmemCols = 512;
 constexpr int kTcDCols = 256;       // columns of one accumulator buffer (two buffers)
 constexpr int kTcMaxPlanes = 16;
-constexpr int kTcMaxToep = 16;      // kTcIssuers rings of kTcRingSlots
-// barriers (plane and Toeplitz rings, two accumulator buffers, the final MMA barrier), the
+constexpr int kTcMaxToep = kTcIssuers * kTcRingSlots;
+constexpr int kTcMaxBox = 256;      // TMA box extent limit (plane rows)
+// barriers (plane and run rings, two accumulator buffers, the final MMA barriers), the
 // tensor-memory address and the abort flag
-constexpr int kTcMaxZ = 12;          // Toeplitz run of at most 32 * (kTcMaxZ - 1) rows
 constexpr int kTcBarBytes =
-    ((2 * kTcMaxPlanes + 2 * kTcMaxToep + 2 * 2 + kTcIssuers + 2 * 2) * 8 + 8 + 127) / 128 * 128;
-static_assert(kTcBuildWarps == 2 * kTcIssuers && kTcIssuers * kTcRingSlots == kTcMaxToep &&
-                  kTcRingSlots % 2 == 0,
-              "builder warps i and i + kTcIssuers feed issuer i's ring, alternate items");
+    ((2 * kTcMaxPlanes + 2 * kTcMaxToep + 2 * 2 + kTcIssuers) * 8 + 8 + 127) / 128 * 128;
 
 struct TcArgs {
-    const void* x;      // N x H x W x C, 16-bit
-    const void* w;      // FH x FW x C, 16-bit
+    const unsigned char* runs;   // Toeplitz runs [C][FH][NCM core matrices], 16-bit
     void* out;          // N x OH x OW x C, OutT
     unsigned int* status;
     unsigned long long wait_ns;
-    int N, H, W, C, OH, OW, FH, FW, pad_h, pad_w;
+    int N, C, OH, OW, FH;
     int S;              // virtual rows per image
     int kimg;           // images per row tile (0: tiles are 128-row bands of one image)
     int bands;          // row tiles per image when kimg == 0
     int NN;             // MMA N (output columns of a column tile, multiple of 16)
-    int TWc;            // output columns a column tile owns (<= NN)
+    int TWc;            // output columns a column tile owns (<= NN, multiple of 8)
     int KS;             // K-steps of 16
-    int MR;             // staged rows per plane (>= FH + 127, multiple of 8)
-    int NCM;            // Toeplitz core matrices: NN/8 + 2*KS - 1
+    int MR;             // staged rows per plane (>= FH + 127, multiple of 8, <= 256)
+    int NCM;            // core matrices of one run: NN/8 + 2*KS - 1
+    int x0;             // column of the stacked copy holding input column -pad_w (<= 0)
     int ncg;            // channel groups (C / CG)
-    int ps, ts;         // plane / Toeplitz ring slots
+    int ps;             // plane ring slots
+    int rps;            // filter rows per ring item (1 or kTcRunsPerSlot)
     uint32_t units, col_tiles;
     FastDiv fd_S;
-    uint32_t plane_bytes, toep_bytes;
-    uint32_t off_toep, off_wst, off_bar;   // byte offsets in shared memory
-    uint32_t wst_bytes;  // one filter staging slot: FH x FW taps x 8 channels, 16-bit, padded
-    uint32_t wst_tx;     // bytes one filter copy delivers (FH * FW * 16, unpadded)
-    int ws;              // filter staging slots (2, or 1 where two do not fit)
+    uint32_t plane_bytes, toep_bytes;   // one plane; one run
+    uint32_t off_toep, off_bar;         // byte offsets in shared memory
     uint32_t idesc;     // instruction descriptor (kind::f16, fp32 accumulation)
 };
 
@@ -144,10 +142,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// Generic-proxy shared-memory writes become visible to the tensor cores' async proxy.
-__device__ __forceinline__ void fence_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // 32 lanes x 16 consecutive 32-bit columns of tensor memory (lane = thread of the warp).
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -181,10 +175,21 @@ __device__ __forceinline__ void tc_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Bulk copy of `bytes` contiguous bytes (16-byte aligned, a multiple of 16) from global to
+// shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tc_bulk_load(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Bounded wait that also gives up as soon as another role has aborted the CTA.  On running
 // out of time it records the timeout and raises the abort flag itself.  Between polls the
 // warp sleeps, up to `max_sleep_ns`: the warps that wait most of the time (epilogue,
-// loaders) then leave the issue slots of their sub-partition to the issuers and builders.
+// feeders) then leave the issue slots of their sub-partition to the issuers.
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, const TcArgs& a,
                                         volatile int* abort_flag, uint32_t max_sleep_ns = 32) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -210,6 +215,18 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t* bar, uint32_t parity, con
     return __all_sync(0xffffffffu, tc_wait(bar, parity, a, abort_flag, max_sleep_ns));
 }
 
+// A feeder never leaves with copies in flight: after its last fill it waits (bounded, even
+// after an abort) for the fills still open in each of its `slots` ring slots, the fills
+// `count - slots` .. `count - 1` (earlier fills completed before their slot was refilled).
+__device__ __forceinline__ void tc_drain(uint64_t* full, uint32_t first_slot, uint32_t slots,
+                                         uint32_t count, const TcArgs& a) {
+    for (uint32_t k = count >= slots ? count - slots : 0; k < count; ++k)
+        if (!mbar_wait(&full[first_slot + k % slots], (k / slots) & 1u, a.wait_ns)) {
+            record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+            return;
+        }
+}
+
 // Row tile `t`: first virtual output row v0 and the rows [v_lo, v_hi) the tile owns.
 struct TcTile {
     int v0, v_lo, v_hi;
@@ -231,43 +248,12 @@ __device__ __forceinline__ TcTile tc_tile(const TcArgs& a, int t) {
 }
 
 // Unit u -> (row tile, column tile, channel group); the channel group is fastest, so CTAs
-// running at the same time read the same input pixels (other channels of them) from L2.
+// running at the same time read neighbouring planes of the stacked copy from L2.
 __device__ __forceinline__ void tc_unit(const TcArgs& a, uint32_t u, int& t, int& j, int& g) {
     g = static_cast<int>(u % static_cast<uint32_t>(a.ncg));
     const uint32_t q = u / static_cast<uint32_t>(a.ncg);
     j = static_cast<int>(q % a.col_tiles);
     t = static_cast<int>(q / a.col_tiles);
-}
-
-template <int CG>
-struct TcPix;   // CG 16-bit channels of one pixel, as loaded
-template <>
-struct TcPix<4> {
-    using V = uint2;
-    __device__ static __forceinline__ V zero() { return make_uint2(0u, 0u); }
-};
-template <>
-struct TcPix<8> {
-    using V = uint4;
-    __device__ static __forceinline__ V zero() { return make_uint4(0u, 0u, 0u, 0u); }
-};
-
-// 16-bit channel `ch` (0 <= ch < CG) of a loaded pixel, in the low half of a word
-// (the high half is garbage).
-template <int CG>
-__device__ __forceinline__ uint32_t tc_word(const typename TcPix<CG>::V& v, int ch) {
-    if constexpr (CG == 4) {
-        return ch < 2 ? v.x : v.y;
-    } else {
-        return ch < 2 ? v.x : (ch < 4 ? v.y : (ch < 6 ? v.z : v.w));
-    }
-}
-
-// Two adjacent columns of channel ch packed into one word (lo column in the low half).
-template <int CG>
-__device__ __forceinline__ uint32_t tc_pair(const typename TcPix<CG>::V& lo,
-                                            const typename TcPix<CG>::V& hi, int ch) {
-    return __byte_perm(tc_word<CG>(lo, ch), tc_word<CG>(hi, ch), (ch & 1) ? 0x7632u : 0x5410u);
 }
 
 // The CG channels of one output pixel, one or two 16-byte streaming stores (fp32), or one
@@ -298,14 +284,112 @@ __device__ __forceinline__ void tc_store_pixel(OutT* dst, const float (&v)[CG]) 
     }
 }
 
-template <typename T, bool FLIP, class OutT, int CG>
+// ------------------------------------------------------------------ preparation kernel
+
+struct TcPrepArgs {
+    const void* x;      // N x H x W x C, 16-bit
+    const void* w;      // FH x FW x C, 16-bit
+    void* planes;       // C x V x Wp stacked copy (V = N * S virtual rows), 16-bit
+    void* runs;         // C x FH runs of 8*NCM rows of 8 values, 16-bit
+    int N, H, W, C, FH, FW, pad_h, S, Lp, Wp, NN, NCM;
+    long long V;
+    long long plane_tasks;   // (C / 8) * V * (Wp / 8): 8 channels x 8 columns of one row
+    long long run_tasks;     // C * FH * 8 * NCM: one 16-byte row of a run
+    int plane_blocks;        // blocks [0, plane_blocks) write the copy, the rest the runs
+};
+
+// Two adjacent columns of channel ch (0..7) of two loaded 8-channel pixels, packed into one
+// word (the lo column in the low half).
+__device__ __forceinline__ uint32_t tc_pair8(const uint4& lo, const uint4& hi, int ch) {
+    const uint32_t wl = ch < 2 ? lo.x : (ch < 4 ? lo.y : (ch < 6 ? lo.z : lo.w));
+    const uint32_t wh = ch < 2 ? hi.x : (ch < 4 ? hi.y : (ch < 6 ? hi.z : hi.w));
+    return __byte_perm(wl, wh, (ch & 1) ? 0x7632u : 0x5410u);
+}
+
+template <typename T, bool FLIP>
+__global__ void __launch_bounds__(256) tc_prep_kernel(const TcPrepArgs a) {
+    if (static_cast<int>(blockIdx.x) < a.plane_blocks) {
+        // Stacked copy: planes[c][v][x] = x[n][h][x - Lp][c] with n = v / S, h = v % S - pad_h,
+        // zero outside the image.  One task: 8 channels x 8 columns of one virtual row,
+        // loaded as 8 pixels (16 bytes each), transposed in registers, stored as 8 rows of
+        // 16 bytes; consecutive threads take consecutive column chunks of one row.
+        const T* X = static_cast<const T*>(a.x);
+        T* P = static_cast<T*>(a.planes);
+        const int xch = a.Wp / 8;
+        const long long stride = static_cast<long long>(a.plane_blocks) * blockDim.x;
+        for (long long task = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+             task < a.plane_tasks; task += stride) {
+            const int k = static_cast<int>(task % xch);
+            const long long q = task / xch;
+            const long long v = q % a.V;
+            const int cb = static_cast<int>(q / a.V);
+            const int n = static_cast<int>(v / a.S);
+            const int h = static_cast<int>(v - static_cast<long long>(n) * a.S) - a.pad_h;
+            const bool row_in = h >= 0 && h < a.H;
+            const int w0 = 8 * k - a.Lp;
+            const T* src = X + (static_cast<size_t>(row_in ? n : 0) * a.H + (row_in ? h : 0)) *
+                                   static_cast<size_t>(a.W) * a.C + 8 * cb;
+            uint4 px[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int col = w0 + e;
+                px[e] = (row_in && col >= 0 && col < a.W)
+                            ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(col) * a.C))
+                            : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                uint4 o;
+                o.x = tc_pair8(px[0], px[1], ch);
+                o.y = tc_pair8(px[2], px[3], ch);
+                o.z = tc_pair8(px[4], px[5], ch);
+                o.w = tc_pair8(px[6], px[7], ch);
+                *reinterpret_cast<uint4*>(P + (static_cast<size_t>(8 * cb + ch) * a.V + v) * a.Wp +
+                                          8 * k) = o;
+            }
+        }
+    } else {
+        // Runs: row r of the run of (c, fh) holds z[r .. r+7], z[i] = filt(fh, i - (NN-1)),
+        // zero outside the filter; filt is w, or w rotated by 180 degrees (backward data).
+        const uint16_t* Wt = static_cast<const uint16_t*>(a.w);
+        uint16_t* R = static_cast<uint16_t*>(a.runs);
+        const int rows = 8 * a.NCM;
+        const long long stride = static_cast<long long>(gridDim.x - a.plane_blocks) * blockDim.x;
+        for (long long task = static_cast<long long>(blockIdx.x - a.plane_blocks) * blockDim.x +
+                              threadIdx.x;
+             task < a.run_tasks; task += stride) {
+            const int r = static_cast<int>(task % rows);
+            const long long q = task / rows;
+            const int fh = static_cast<int>(q % a.FH);
+            const int c = static_cast<int>(q / a.FH);
+            const int fhe = FLIP ? a.FH - 1 - fh : fh;
+            uint32_t z[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int f = r + e - (a.NN - 1);
+                z[e] = (f >= 0 && f < a.FW)
+                           ? Wt[(static_cast<size_t>(fhe) * a.FW + (FLIP ? a.FW - 1 - f : f)) * a.C + c]
+                           : 0u;
+            }
+            uint4 o;
+            o.x = z[0] | (z[1] << 16);
+            o.y = z[2] | (z[3] << 16);
+            o.z = z[4] | (z[5] << 16);
+            o.w = z[6] | (z[7] << 16);
+            *reinterpret_cast<uint4*>(R + (static_cast<size_t>(q) * rows + r) * 8) = o;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ main kernel
+
+template <typename T, class OutT, int CG>
 __global__ void __launch_bounds__(kTcThreads, 1)
-tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
+tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
     static_assert(CG % kTcIssuers == 0, "every issuer takes whole channels of the group");
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* planes = smem;
     unsigned char* toep = smem + a.off_toep;
-    unsigned char* wst = smem + a.off_wst;   // two filter staging slots [FH][FW][8 channels]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.off_bar);
     uint64_t* plane_full = bars;
     uint64_t* plane_empty = plane_full + kTcMaxPlanes;
@@ -314,19 +398,17 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
     uint64_t* d_full = toep_empty + kTcMaxToep;   // [2]
     uint64_t* d_empty = d_full + 2;               // [2]
     uint64_t* mma_done = d_empty + 2;             // [kTcIssuers]
-    uint64_t* w_full = mma_done + kTcIssuers;     // [2] filter staging slots
-    uint64_t* w_empty = w_full + 2;               // [2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(w_empty + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + kTcIssuers);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.ps; ++s) {
-            mbar_init(&plane_full[s], kTcLoadWarps);
+            mbar_init(&plane_full[s], 1);    // the plane feeder (plus the copies' bytes)
             mbar_init(&plane_empty[s], 1);   // the issuer of its channel
         }
-        for (int s = 0; s < a.ts; ++s) {
+        for (int s = 0; s < kTcMaxToep; ++s) {
             mbar_init(&toep_full[s], 1);
             mbar_init(&toep_empty[s], 1);
         }
@@ -335,10 +417,6 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
             mbar_init(&d_empty[s], kTcEpiWarps);
         }
         for (int i = 0; i < kTcIssuers; ++i) mbar_init(&mma_done[i], 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&w_full[s], 1);
-            mbar_init(&w_empty[s], kTcBuildWarps);
-        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -363,15 +441,16 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
             bool ok = true;
             // Descriptors are built once; the start-address field (bits 0-13, 16-byte units)
             // then advances by plain additions: a plane slot, a filter row (16 bytes), a
-            // K-step (two planes of A, two core matrices of T).
+            // K-step (two planes of A, two core matrices of T), a run.
             const uint64_t adesc0 = tc_sdesc(smem_addr(planes), a.MR * 16u, 128u);
             const uint64_t bdesc0 = tc_sdesc(smem_addr(toep), 128u, 128u);
             const uint32_t a_ks = 2u * a.MR;           // A advance per K-step (16-byte units)
-            const uint32_t a_slot = a.plane_bytes >> 4, b_slot = a.toep_bytes >> 4;
+            const uint32_t a_slot = a.plane_bytes >> 4, b_run = a.toep_bytes >> 4;
+            const uint32_t b_slot = static_cast<uint32_t>(a.rps) * b_run;
             const uint32_t idesc = a.idesc;
             const uint32_t ps = static_cast<uint32_t>(a.ps);
-            // this issuer's Toeplitz ring: slots [is * kTcRingSlots, (is + 1) * kTcRingSlots),
-            // filled in order with the runs of exactly the (channel, filter row) items it takes
+            // this issuer's ring: slots [is * kTcRingSlots, (is + 1) * kTcRingSlots), filled
+            // in order with the runs of exactly the (channel, filter rows) items it takes
             const uint32_t ring0 = static_cast<uint32_t>(is) * kTcRingSlots;
             uint32_t item = 0;
             uint32_t pos0 = 0;   // plane-ring position of the unit's first channel
@@ -381,26 +460,29 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
                 const uint32_t dcol = tmem + db * kTcDCols;
                 for (int ch = is; ch < CG && ok; ch += kTcIssuers) {
                     // channel ch of this unit sits at plane-ring position pos0 + ch (the
-                    // loaders fill the ring in order; this issuer skips the other channels)
+                    // plane feeder fills the ring in order; this issuer skips the others)
                     const uint32_t pos = pos0 + static_cast<uint32_t>(ch);
                     const uint32_t pslot = pos % ps, pphase = (pos / ps) & 1u;
                     if (!tc_wait(&plane_full[pslot], pphase, a, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ap = adesc0 + pslot * a_slot;
                     const uint32_t dch = dcol + static_cast<uint32_t>(ch * a.NN);
-                    for (int fh = 0; fh < a.FH; ++fh, ++item) {
+                    // item: filter rows fh0 .. fh0 + rps - 1 (fewer at the end)
+                    for (int fh0 = 0; fh0 < a.FH; fh0 += a.rps, ++item) {
                         const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
                         const uint32_t phase = (item / kTcRingSlots) & 1u;
-                        if (!mbar_try_wait(&toep_full[slot], phase) &&
-                            !tc_wait(&toep_full[slot], phase, a, abort_flag)) { ok = false; break; }
+                        if (!tc_wait(&toep_full[slot], phase, a, abort_flag)) { ok = false; break; }
                         tc_fence_after();
-                        uint64_t ad = ap + static_cast<uint32_t>(fh);
-                        uint64_t bd = bdesc0 + slot * b_slot;
-                        tc_mma(dch, ad, bd, idesc, fh != 0 ? 1u : 0u);
-                        for (int ks = 1; ks < a.KS; ++ks) {
-                            ad += a_ks;
-                            bd += 16u;
-                            tc_mma(dch, ad, bd, idesc, 1u);
+                        const int nr = min(a.rps, a.FH - fh0);
+                        for (int rr = 0; rr < nr; ++rr) {
+                            uint64_t ad = ap + static_cast<uint32_t>(fh0 + rr);
+                            uint64_t bd = bdesc0 + slot * b_slot + rr * b_run;
+                            tc_mma(dch, ad, bd, idesc, (fh0 + rr) != 0 ? 1u : 0u);
+                            for (int ks = 1; ks < a.KS; ++ks) {
+                                ad += a_ks;
+                                bd += 16u;
+                                tc_mma(dch, ad, bd, idesc, 1u);
+                            }
                         }
                         tc_commit(&toep_empty[slot]);   // slot free once these MMAs finish
                     }
@@ -465,189 +547,65 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
             db ^= 1u;
             if (db == 0) dphase ^= 1u;
         }
-    } else if (warp >= kTcLoad0) {
-        // ------------------------------------------------------------- loaders
-        using Pix = TcPix<CG>;
-        using V = typename Pix::V;
-        const int lt = (warp - kTcLoad0) * 32 + lane;   // 0 .. 32*kTcLoadWarps-1
-        const T* X = static_cast<const T*>(a.x);
-        const int KC = 2 * a.KS;
-        const int tasks = a.MR * KC;  // (row, 8-column chunk), row fastest
-        Ring pr;
-        for (uint32_t u = blockIdx.x; u < a.units; u += gridDim.x) {
-            int t, j, g;
-            tc_unit(a, u, t, j, g);
-            const TcTile tl = tc_tile(a, t);
-            const int col0 = j * a.TWc - a.pad_w;
-            const int c0 = g * CG;
-            // the CG planes of this unit: slots pr, pr+1, ... (each released by the MMA)
-            Ring q = pr;
+    } else if (warp < kTcPlaneWarp) {
+        // ------------------------------------------------------------- run feeders
+        // Feeder i copies, in order, the runs of the items issuer i takes: for each of its
+        // channels, rps filter rows at a time (the runs of one channel are consecutive in
+        // the run table, so an item is one bulk copy).
+        const int fi = warp - kTcFeed0;
+        if (lane == 0) {
+            const uint32_t ring0 = static_cast<uint32_t>(fi) * kTcRingSlots;
+            const uint32_t slot_bytes = static_cast<uint32_t>(a.rps) * a.toep_bytes;
+            uint32_t item = 0;
             bool ok = true;
-            uint32_t slots[CG];
-#pragma unroll
-            for (int ch = 0; ch < CG; ++ch) {
-                if (ok && !tc_wait_warp(&plane_empty[q.slot], q.phase ^ 1u, a, abort_flag, 512)) ok = false;
-                slots[ch] = q.slot;
-                q.next(a.ps);
-            }
-            if (!ok) break;
-            // TB tasks per thread per round: all their loads are in flight before the first
-            // transposed store (the loads are what takes time)
-            constexpr int TB = 8 / CG;   // 32 registers of loaded pixels
-            constexpr int NT = 32 * kTcLoadWarps;
-            for (int base = lt; base < tasks; base += TB * NT) {
-                V px[TB][8];
-                int tb_b[TB], tb_r[TB];
-#pragma unroll
-                for (int k = 0; k < TB; ++k) {
-                    const int task = base + k * NT;
-                    const int b = task / a.MR, rr = task - b * a.MR;
-                    tb_b[k] = b;
-                    tb_r[k] = rr;
-                    // rows no MMA reads (and tasks past the end) are neither loaded nor stored
-                    const bool live = task < tasks && rr < a.FH + kTcM - 1;
-                    uint32_t rem;
-                    const int vi = tl.v0 + rr;
-                    const int n = static_cast<int>(a.fd_S.divmod(static_cast<uint32_t>(vi), rem));
-                    const int h = static_cast<int>(rem) - a.pad_h;
-                    const bool row_in = live && n < a.N && h >= 0 && h < a.H;
-                    const int cb = col0 + 8 * b;
-                    const T* src = X + ((static_cast<size_t>(row_in ? n : 0) * a.H + (row_in ? h : 0)) *
-                                            a.W) * static_cast<size_t>(a.C) + c0;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int col = cb + e;
-                        px[k][e] = (row_in && col >= 0 && col < a.W)
-                                       ? __ldg(reinterpret_cast<const V*>(src + static_cast<size_t>(col) * a.C))
-                                       : Pix::zero();
-                    }
-                    if (!live) tb_r[k] = -1;
-                }
-#pragma unroll
-                for (int k = 0; k < TB; ++k) {
-                    if (tb_r[k] < 0) continue;
-#pragma unroll
-                    for (int ch = 0; ch < CG; ++ch) {
-                        uint4 o;
-                        o.x = tc_pair<CG>(px[k][0], px[k][1], ch);
-                        o.y = tc_pair<CG>(px[k][2], px[k][3], ch);
-                        o.z = tc_pair<CG>(px[k][4], px[k][5], ch);
-                        o.w = tc_pair<CG>(px[k][6], px[k][7], ch);
-                        *reinterpret_cast<uint4*>(planes + static_cast<size_t>(slots[ch]) * a.plane_bytes +
-                                                  (static_cast<size_t>(tb_b[k]) * a.MR + tb_r[k]) * 16u) = o;
+            for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                int t, j, g;
+                tc_unit(a, u, t, j, g);
+                for (int ch = fi; ch < CG && ok; ch += kTcIssuers) {
+                    const unsigned char* src =
+                        a.runs + static_cast<size_t>(g * CG + ch) * a.FH * a.toep_bytes;
+                    for (int fh0 = 0; fh0 < a.FH; fh0 += a.rps, ++item) {
+                        const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
+                        const uint32_t phase = (item / kTcRingSlots) & 1u;
+                        if (!tc_wait(&toep_empty[slot], phase ^ 1u, a, abort_flag)) { ok = false; break; }
+                        const uint32_t bytes = static_cast<uint32_t>(min(a.rps, a.FH - fh0)) * a.toep_bytes;
+                        mbar_arrive_expect_tx(&toep_full[slot], bytes);
+                        tc_bulk_load(toep + static_cast<size_t>(slot) * slot_bytes,
+                                     src + static_cast<size_t>(fh0) * a.toep_bytes, bytes, &toep_full[slot]);
                     }
                 }
             }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-#pragma unroll
-                for (int ch = 0; ch < CG; ++ch) mbar_arrive(&plane_full[slots[ch]]);
-            }
-            pr = q;
+            tc_drain(toep_full, ring0, kTcRingSlots, item, a);
         }
+        __syncwarp();
     } else {
-        // ------------------------------------------------------------- Toeplitz builders
-        // Builder warps i and i + 4 write, in turn (even and odd items), the Toeplitz runs of
-        // the (channel, filter row) items MMA issuer i takes into that issuer's ring.  The unit's
-        // filters (8 channels around the group) arrive by one TMA copy per unit into one of
-        // the staging slots (two where they fit: the next unit's copy then travels while this
-        // unit's runs are built).
-        const int bidx = warp - kTcBuild0;
-        const int ring = bidx % kTcIssuers;                  // the ring (issuer) this warp feeds
-        const uint32_t turn = static_cast<uint32_t>(bidx / kTcIssuers);   // its items' parity
-        const int rows = 8 * a.NCM;
-        const int nz = (rows + 7 + 31) / 32;   // z chunks a lane holds (<= kTcMaxZ)
-        const uint32_t ring0 = static_cast<uint32_t>(ring) * kTcRingSlots;
-        uint32_t item = 0;
-        bool ok = true;
-        // Staging slot k % ws holds the filters of the CTA's unit k.  Builder warp 0's lane 0
-        // issues the copies: units 0 .. ws-1 up front, unit k + ws once every builder has
-        // released unit k's slot.
-        const uint32_t ws = static_cast<uint32_t>(a.ws);
-        uint32_t issued = 0;   // filter copies issued
-        auto issue_stage = [&](uint32_t kk) -> bool {
-            const uint32_t uu = blockIdx.x + kk * gridDim.x;
-            const uint32_t sl = kk % ws, n = kk / ws;
-            if (!tc_wait(&w_empty[sl], (n & 1u) ^ 1u, a, abort_flag)) return false;
-            int t_, j_, g_;
-            tc_unit(a, uu, t_, j_, g_);
-            mbar_arrive_expect_tx(&w_full[sl], a.wst_tx);
-            tma_load_3d(wst + sl * a.wst_bytes, &wmap, &w_full[sl], (g_ * CG) & ~7, 0, 0);
-            ++issued;
-            return true;
-        };
-        if (bidx == 0 && lane == 0) {
-            prefetch_tensormap(&wmap);
-            for (uint32_t kk = 0; kk < ws && ok; ++kk)
-                if (blockIdx.x + kk * gridDim.x < a.units) ok = issue_stage(kk);
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        uint32_t k = 0;   // unit index within this CTA
-        for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++k) {
-            int t, j, g;
-            tc_unit(a, u, t, j, g);
-            const uint32_t sl = k % ws;
-            if (!tc_wait_warp(&w_full[sl], (k / ws) & 1u, a, abort_flag)) { ok = false; break; }
-            // channel ch of the group sits at lane (g*CG) % 8 + ch of each staged tap
-            const uint16_t* wtap = reinterpret_cast<const uint16_t*>(wst + sl * a.wst_bytes) +
-                                   ((g * CG) & 7);
-            for (int ch = ring; ch < CG && ok; ch += kTcIssuers) {
-                for (int fh = 0; fh < a.FH; ++fh, ++item) {
-                    if ((item & 1u) != turn) continue;   // the other warp's item
-                    const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
-                    const uint32_t phase = (item / kTcRingSlots) & 1u;
-                    if (!tc_wait_warp(&toep_empty[slot], phase ^ 1u, a, abort_flag)) { ok = false; break; }
-                    const int fhe = FLIP ? a.FH - 1 - fh : fh;
-                    const uint16_t* wr = wtap + static_cast<size_t>(fhe) * a.FW * 8 + ch;
-                    unsigned char* dst = toep + static_cast<size_t>(slot) * a.toep_bytes;
-                    // Row r of the core-matrix run is z[r .. r+7] with z[i] = filt(fh, i - (NN-1))
-                    // (zero outside the filter).  Lane l holds z[32c + l] for every chunk c and
-                    // gathers its rows r = 32c + l with 8 shuffles each; all loads first, then
-                    // all shuffles, so that their latencies overlap.
-                    uint32_t z[kTcMaxZ];
-#pragma unroll
-                    for (int c = 0; c < kTcMaxZ; ++c) {
-                        const int f = 32 * c + lane - (a.NN - 1);
-                        z[c] = (c < nz && f >= 0 && f < a.FW) ? wr[(FLIP ? a.FW - 1 - f : f) * 8] : 0u;
-                    }
-#pragma unroll
-                    for (int c = 0; c + 1 < kTcMaxZ; ++c) {
-                        if (32 * c >= rows) break;
-                        uint32_t wv[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            wv[e] = __shfl_sync(0xffffffffu, lane < e ? z[c + 1] : z[c], (lane + e) & 31);
-                        const int r = 32 * c + lane;
-                        if (r < rows) {
-                            uint4 v;
-                            v.x = __byte_perm(wv[0], wv[1], 0x5410);
-                            v.y = __byte_perm(wv[2], wv[3], 0x5410);
-                            v.z = __byte_perm(wv[4], wv[5], 0x5410);
-                            v.w = __byte_perm(wv[6], wv[7], 0x5410);
-                            *reinterpret_cast<uint4*>(dst + static_cast<size_t>(r) * 16u) = v;
-                        }
-                    }
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&toep_full[slot]);
+        // ------------------------------------------------------------- plane feeder
+        // The unit's CG planes, in channel order, at ring positions pos, pos+1, ...: one TMA
+        // box (8 columns x MR rows of one channel) per 8-column plane.
+        if (lane == 0) {
+            prefetch_tensormap(&xmap);
+            const uint32_t ps = static_cast<uint32_t>(a.ps);
+            const int kc = 2 * a.KS;
+            uint32_t pos = 0;
+            bool ok = true;
+            for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                int t, j, g;
+                tc_unit(a, u, t, j, g);
+                const TcTile tl = tc_tile(a, t);
+                const int xc = j * a.TWc + a.x0;
+                for (int ch = 0; ch < CG; ++ch, ++pos) {
+                    const uint32_t slot = pos % ps, phase = (pos / ps) & 1u;
+                    if (!tc_wait(&plane_empty[slot], phase ^ 1u, a, abort_flag)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&plane_full[slot], a.plane_bytes);
+                    unsigned char* dst = planes + static_cast<size_t>(slot) * a.plane_bytes;
+                    for (int b = 0; b < kc; ++b)
+                        tma_load_3d(dst + static_cast<size_t>(b) * a.MR * 16u, &xmap, &plane_full[slot],
+                                    xc + 8 * b, tl.v0, g * CG + ch);
                 }
             }
-            // this warp is done with the staged filters of unit k; the slot takes unit k + ws
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&w_empty[sl]);
-            if (bidx == 0 && lane == 0 && ok && u + ws * gridDim.x < a.units) ok = issue_stage(k + ws);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            tc_drain(plane_full, 0, ps, pos, a);
         }
-        // never leave with a filter copy in flight: wait (bounded) for the last copy of each
-        // staging slot (earlier ones completed before their slot was reused)
-        if (bidx == 0 && lane == 0) {
-            for (uint32_t kk = issued >= ws ? issued - ws : 0; kk < issued; ++kk)
-                if (!mbar_wait(&w_full[kk % ws], (kk / ws) & 1u, a.wait_ns)) {
-                    record_status(a.status, DWC_DEVSTAT_TIMEOUT);
-                    break;
-                }
-        }
+        __syncwarp();
     }
 
     // every role is done (or gave up): release the tensor memory
@@ -669,22 +627,25 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap wmap, const TcArgs a) {
 inline double tc_mma_cycles(int n) {
     return std::max({46.0, (kTcM + n) / 4.0, n / 2.0});
 }
+// An issuing thread's cycles per ring item (wait, fences, commit) and per MMA it issues.
+constexpr double kTcItemIssueCycles = 500.0;
+constexpr double kTcMmaIssueCycles = 110.0;
 
 struct TcPlan {
     TcArgs a;
     size_t smem;
     int cg;
+    int Lp, Wp;                       // stacked copy: left padding, row length (columns)
+    size_t planes_bytes, runs_bytes;  // scratch: stacked copy, run table
 };
 
 // Launch plan for a stride-1 problem as the row kernel sees it; false if the shape does not
 // fit the kernel (the caller then takes another kernel).
 inline bool tc_plan(const RowConv& p, TcPlan& P) {
     TcArgs& a = P.a;
-    // the filter copy is a TMA box of 8 channels x FW x FH (each at most 256)
-    if (p.C % 8 != 0 || p.FH < 1 || p.FW < 1 || p.FH > 256 || p.FW > 256 || p.OH < 1 || p.OW < 1)
-        return false;
-    a.N = p.N; a.H = p.H; a.W = p.W; a.C = p.C; a.OH = p.OH; a.OW = p.OW;
-    a.FH = p.FH; a.FW = p.FW; a.pad_h = p.pad_h; a.pad_w = p.pad_w;
+    // channel groups of 4 and 8 channels, 16-byte copies of 8 channels in the preparation
+    if (p.C % 8 != 0 || p.FH < 1 || p.FW < 1 || p.FW > 256 || p.OH < 1 || p.OW < 1) return false;
+    a.N = p.N; a.C = p.C; a.OH = p.OH; a.OW = p.OW; a.FH = p.FH;
     // virtual rows per image: the image's rows and padding, shared with the next image
     a.S = std::max({p.pad_h + p.H, p.OH + p.FH - 1 - p.pad_h, p.OH});
     if (p.OH <= kTcM) {
@@ -698,51 +659,50 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
                                            : static_cast<long long>(p.N) * a.bands;
     if (static_cast<long long>(p.N + 1) * a.S + 2 * kTcM >= (1LL << 31)) return false;
     a.MR = (p.FH + kTcM - 1 + 7) / 8 * 8;
-    // Column tile and channel group, chosen together by an estimate of the busiest SM's
-    // cycles: the MMAs of its units (units spread evenly over the SMs, whole units only),
-    // plus, where shared memory cannot hold the planes of two units (the next unit's gather
-    // then waits for the end of the current one), the gather's one cache line per pixel.
-    // Constraints: two accumulator buffers of CG x NN columns in tensor memory, the
-    // builders' run limit, and the planes, Toeplitz rings and filter staging in shared memory.
+    if (a.MR > kTcMaxBox) return false;   // one TMA box per plane
+    // Column tile, channel group and filter rows per ring item, chosen together by an
+    // estimate of the busiest SM's cycles: per unit (units spread evenly over the SMs, whole
+    // units only) the longer of the tensor core's MMA time and an issuer's time (a fixed cost
+    // per ring item and per MMA), plus, where shared memory cannot hold the planes of two
+    // units (the next unit's planes then wait for the end of the current one), the planes'
+    // copy time at 64 bytes per cycle.  Column tiles own a multiple of 8 columns (every
+    // tile's first plane starts on an 8-column boundary of the stacked copy).  Constraints:
+    // two accumulator buffers of CG x NN columns in tensor memory, the planes and the run
+    // rings in shared memory.
     const int cap = device_info().max_smem_optin;
     const int sms = device_info().sm_count;
-    const size_t wst_bytes = static_cast<size_t>((p.FH * p.FW * 16 + 127) / 128 * 128);
     double best = 1e30;
-    int best_nt = 0, best_cg = 0, best_ps = 0, best_ws = 0;
-    for (int nt = 1; nt <= 32; ++nt) {
-        const int twc = (p.OW + nt - 1) / nt;
-        const int nn = (twc + 15) / 16 * 16;
+    int best_nt = 0, best_cg = 0, best_ps = 0, best_rps = 0, best_twc = 0;
+    for (int nt = 1; nt <= 64; ++nt) {
+        const int twc = ((p.OW + nt - 1) / nt + 7) / 8 * 8;
         if (nt > 1 && (p.OW + twc - 1) / twc < nt) continue;
+        const int nn = (twc + 15) / 16 * 16;
+        if (nn > kTcDCols) continue;
         const int ks = (nn + p.FW - 1 + 15) / 16;
         const int ncm = nn / 8 + 2 * ks - 1;
-        if (8 * ncm > 32 * (kTcMaxZ - 1)) continue;   // the builders' run limit
         const size_t plane = static_cast<size_t>(2 * ks) * a.MR * 16;
-        const size_t toep_ring = static_cast<size_t>(kTcMaxToep) * ncm * 128;
         const long long tiles = row_tiles * ((p.OW + twc - 1) / twc);
+        for (int rps = kTcRunsPerSlot; rps >= 1; --rps)
         for (int cg = 8; cg >= 4; cg /= 2) {
             if (cg * nn > kTcDCols || p.C % cg != 0) continue;
-            // plane slots beside one or two filter staging slots; two where that still
-            // leaves room for two units' planes (or costs no plane)
-            auto slots = [&](int w) -> int {
-                const size_t fixed = w * wst_bytes + kTcBarBytes + toep_ring;
-                if (fixed >= static_cast<size_t>(cap)) return 0;
-                return static_cast<int>(std::min<size_t>(kTcMaxPlanes, (cap - fixed) / plane));
-            };
-            const int ps2 = slots(2), ps1 = slots(1);
-            const int ws = (ps2 >= 2 * cg || ps2 == ps1) ? 2 : 1;
-            const int ps = ws == 2 ? ps2 : ps1;
+            const size_t fixed = static_cast<size_t>(kTcMaxToep) * rps * ncm * 128 + kTcBarBytes;
+            if (fixed >= static_cast<size_t>(cap)) continue;
+            const int ps = static_cast<int>(std::min<size_t>(kTcMaxPlanes, (cap - fixed) / plane));
             if (ps < cg + 1) continue;   // the next unit's planes must fill while one computes
             const long long units = tiles * (p.C / cg);
-            const double unit = cg * p.FH * ks * tc_mma_cycles(nn) +
-                                (ps >= 2 * cg ? 0.0 : static_cast<double>(a.MR) * 16 * ks);
+            const double tensor = cg * p.FH * ks * tc_mma_cycles(nn);
+            const double issue = (cg / kTcIssuers) * ((p.FH + rps - 1) / rps) *
+                                 (kTcItemIssueCycles + rps * ks * kTcMmaIssueCycles);
+            const double unit = std::max(tensor, issue) +
+                                (ps >= 2 * cg ? 0.0 : static_cast<double>(cg) * plane / 64.0);
             const double cost = static_cast<double>((units + sms - 1) / sms) * unit;
             if (cost < best) {
-                best = cost; best_nt = nt; best_cg = cg; best_ps = ps; best_ws = ws;
+                best = cost; best_nt = nt; best_cg = cg; best_ps = ps; best_rps = rps; best_twc = twc;
             }
         }
     }
     if (best_nt == 0) return false;
-    a.TWc = (p.OW + best_nt - 1) / best_nt;
+    a.TWc = best_twc;
     a.NN = (a.TWc + 15) / 16 * 16;
     a.col_tiles = static_cast<uint32_t>((p.OW + a.TWc - 1) / a.TWc);
     a.KS = (a.NN + p.FW - 1 + 15) / 16;
@@ -755,18 +715,20 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     if (units >= (1LL << 31)) return false;
     a.units = static_cast<uint32_t>(units);
     a.fd_S.init(static_cast<uint32_t>(a.S));
-    // shared memory: plane ring, Toeplitz ring, filter staging slots (one TMA box of the
-    // FH x FW taps of 8 channels each), barriers
-    a.wst_tx = static_cast<uint32_t>(p.FH) * p.FW * 16u;
-    a.wst_bytes = (a.wst_tx + 127u) / 128u * 128u;
-    a.ts = kTcMaxToep;
-    a.ws = best_ws;
     a.ps = best_ps;
-    const size_t toep_ring = static_cast<size_t>(a.ts) * a.toep_bytes;
-    const size_t wst = static_cast<size_t>(a.ws) * a.wst_bytes;
+    a.rps = best_rps;
+    // stacked copy: input column w at column w + Lp, Lp = pad_w mod 8, so that a tile's first
+    // column j*TWc - pad_w lands on a multiple of 8 (x0 = Lp - pad_w); the copy spans the
+    // image and, to the right, every column a tile reads (beyond it the TMA box reads zeros)
+    P.Lp = p.pad_w % 8;
+    a.x0 = P.Lp - p.pad_w;
+    P.Wp = (P.Lp + p.W + 7) / 8 * 8;
+    P.planes_bytes = static_cast<size_t>(p.C) * static_cast<size_t>(p.N) * a.S * P.Wp * 2;
+    P.runs_bytes = static_cast<size_t>(p.C) * p.FH * a.toep_bytes;
+    // shared memory: plane ring, run rings, barriers
+    const size_t toep_ring = static_cast<size_t>(kTcMaxToep) * a.rps * a.toep_bytes;
     a.off_toep = static_cast<uint32_t>(static_cast<size_t>(a.ps) * a.plane_bytes);
-    a.off_wst = a.off_toep + static_cast<uint32_t>(toep_ring);
-    a.off_bar = a.off_wst + static_cast<uint32_t>(wst);
+    a.off_bar = a.off_toep + static_cast<uint32_t>(toep_ring);
     // one CTA per SM (each allocates all of tensor memory): ask for more than half of it
     P.smem = std::max<size_t>(a.off_bar + kTcBarBytes, static_cast<size_t>(cap) / 2 + 1024);
     return true;
@@ -779,33 +741,60 @@ inline uint32_t tc_idesc(int n) {
            (static_cast<uint32_t>(kTcM >> 4) << 24);
 }
 
-template <typename T, bool FLIP, class OutT, int CG>
+template <typename T, class OutT, int CG>
 cudaError_t launch_tc_inst(const TcPlan& P, const RowConv& p) {
     TcArgs a = P.a;
-    // filter taps as 8-channel TMA boxes: the whole FH x FW filter of 8 channels per copy
-    CUtensorMap wmap;
+    // scratch of this call: the stacked copy, then the run table (128-byte aligned)
+    const size_t runs_off = (P.planes_bytes + 127) / 128 * 128;
+    void* scratch = nullptr;
+    if (scratch_alloc(&scratch, runs_off + P.runs_bytes, p.stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return cudaErrorNotSupported;   // the caller takes another kernel
+    }
+    unsigned char* base = static_cast<unsigned char*>(scratch);
+    const long long V = static_cast<long long>(p.N) * a.S;
+    CUtensorMap xmap;
     {
-        const cuuint64_t dims[3] = {(cuuint64_t)p.C, (cuuint64_t)p.FW, (cuuint64_t)p.FH};
-        const cuuint64_t strides[2] = {(cuuint64_t)p.C * 2, (cuuint64_t)p.FW * p.C * 2};
-        const cuuint32_t box[3] = {8u, (cuuint32_t)p.FW, (cuuint32_t)p.FH};
-        if (encode_tiled(&wmap, Elem<T>::kTmaType, 3, const_cast<void*>(p.w), dims, strides,
-                         box) != CUDA_SUCCESS)
+        const cuuint64_t dims[3] = {(cuuint64_t)P.Wp, (cuuint64_t)V, (cuuint64_t)p.C};
+        const cuuint64_t strides[2] = {(cuuint64_t)P.Wp * 2, (cuuint64_t)V * P.Wp * 2};
+        const cuuint32_t box[3] = {8u, (cuuint32_t)a.MR, 1u};
+        if (encode_tiled(&xmap, Elem<T>::kTmaType, 3, base, dims, strides, box) != CUDA_SUCCESS) {
+            scratch_free(scratch, p.stream);
             return cudaErrorNotSupported;
+        }
     }
-    a.x = p.in; a.w = p.w; a.out = p.out;
-    a.status = p.status;
-    a.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
-    a.idesc = tc_idesc<T>(a.NN);
-    auto kern = tc_rows_kernel<T, FLIP, OutT, CG>;
-    static DeviceOnce smem_opt_in;
-    {
-        const cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
-        if (err != cudaSuccess) return err;
+    // preparation: the stacked copy and the runs
+    TcPrepArgs q;
+    q.x = p.in; q.w = p.w; q.planes = base; q.runs = base + runs_off;
+    q.N = p.N; q.H = p.H; q.W = p.W; q.C = p.C; q.FH = p.FH; q.FW = p.FW; q.pad_h = p.pad_h;
+    q.S = a.S; q.Lp = P.Lp; q.Wp = P.Wp; q.NN = a.NN; q.NCM = a.NCM; q.V = V;
+    q.plane_tasks = static_cast<long long>(p.C / 8) * V * (P.Wp / 8);
+    q.run_tasks = static_cast<long long>(p.C) * p.FH * 8 * a.NCM;
+    const int sms = device_info().sm_count;
+    q.plane_blocks = static_cast<int>(std::min<long long>((q.plane_tasks + 255) / 256, 8LL * sms));
+    const int run_blocks = static_cast<int>(std::min<long long>((q.run_tasks + 255) / 256, 2LL * sms));
+    if (p.flip) tc_prep_kernel<T, true><<<q.plane_blocks + run_blocks, 256, 0, p.stream>>>(q);
+    else tc_prep_kernel<T, false><<<q.plane_blocks + run_blocks, 256, 0, p.stream>>>(q);
+    cudaError_t err = cudaGetLastError();
+    if (err == cudaSuccess) {
+        a.runs = base + runs_off;
+        a.out = p.out;
+        a.status = p.status;
+        a.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
+        a.idesc = tc_idesc<T>(a.NN);
+        auto kern = tc_rows_kernel<T, OutT, CG>;
+        static DeviceOnce smem_opt_in;
+        err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
+        if (err == cudaSuccess) {
+            const unsigned grid = static_cast<unsigned>(
+                std::min<long long>(a.units, static_cast<long long>(sms)));
+            kern<<<grid, kTcThreads, P.smem, p.stream>>>(xmap, a);
+            err = cudaGetLastError();
+        }
     }
-    const unsigned grid = static_cast<unsigned>(
-        std::min<long long>(a.units, static_cast<long long>(device_info().sm_count)));
-    kern<<<grid, kTcThreads, P.smem, p.stream>>>(wmap, a);
-    return cudaGetLastError();
+    // stream-ordered: the memory returns to the pool once both kernels have run
+    scratch_free(scratch, p.stream);
+    return err;
 }
 
 template <typename T, class OutT = float>
@@ -814,8 +803,8 @@ cudaError_t launch_tc_rows(const RowConv& p) {
     if (!tc_plan(p, P)) return cudaErrorNotSupported;
     if (P.a.units == 0) return cudaSuccess;
     switch (P.cg) {
-        case 4: return p.flip ? launch_tc_inst<T, true, OutT, 4>(P, p) : launch_tc_inst<T, false, OutT, 4>(P, p);
-        case 8: return p.flip ? launch_tc_inst<T, true, OutT, 8>(P, p) : launch_tc_inst<T, false, OutT, 8>(P, p);
+        case 4: return launch_tc_inst<T, OutT, 4>(P, p);
+        case 8: return launch_tc_inst<T, OutT, 8>(P, p);
         default: return cudaErrorNotSupported;
     }
 }
