@@ -292,76 +292,90 @@ struct TcPrepArgs {
     void* planes;       // C x V x Wp stacked copy (V = N * S virtual rows), 16-bit
     void* runs;         // C x FH runs of 8*NCM rows of 8 values, 16-bit
     int N, H, W, C, FH, FW, pad_h, S, Lp, Wp, NN, NCM;
-    long long V;
-    long long plane_tasks;   // (C / 8) * V * (Wp / 8): 8 channels x 8 columns of one row
-    long long run_tasks;     // C * FH * 8 * NCM: one 16-byte row of a run
-    int plane_blocks;        // blocks [0, plane_blocks) write the copy, the rest the runs
+    int CT;                  // channels of a copy tile (64, 32, 16 or 8, dividing C)
+    int piece_shift;         // log2(CT / 8): 16-byte pieces of a pixel in a copy tile
+    int V;                   // N * S
+    int plane_tiles;         // V * (C / CT) * ceil(Wp / 64) tiles of one row
+    int run_tasks;           // C * FH * 8 * NCM: one 16-byte row of a run
+    int run_blocks;          // blocks [0, run_blocks) write the runs, the rest the copy
+    // divisions by launch constants (all operands below 2^31)
+    FastDiv fd_xt, fd_ct, fd_S, fd_C, fd_rows;
 };
 
-// Two adjacent columns of channel ch (0..7) of two loaded 8-channel pixels, packed into one
-// word (the lo column in the low half).
-__device__ __forceinline__ uint32_t tc_pair8(const uint4& lo, const uint4& hi, int ch) {
-    const uint32_t wl = ch < 2 ? lo.x : (ch < 4 ? lo.y : (ch < 6 ? lo.z : lo.w));
-    const uint32_t wh = ch < 2 ? hi.x : (ch < 4 ? hi.y : (ch < 6 ? hi.z : hi.w));
-    return __byte_perm(wl, wh, (ch & 1) ? 0x7632u : 0x5410u);
-}
+constexpr int kTcPrepThreads = 256;
+constexpr int kTcPrepCols = 64;      // copy tile: 64 columns x up to 64 channels of one row
+constexpr int kTcPrepRowWords = 33;  // shared row of a pixel: 64 channels + one pad word
 
 template <typename T, bool FLIP>
-__global__ void __launch_bounds__(256) tc_prep_kernel(const TcPrepArgs a) {
-    if (static_cast<int>(blockIdx.x) < a.plane_blocks) {
+__global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const TcPrepArgs a) {
+    __shared__ uint32_t tile[kTcPrepCols * kTcPrepRowWords];
+    if (static_cast<int>(blockIdx.x) >= a.run_blocks) {
         // Stacked copy: planes[c][v][x] = x[n][h][x - Lp][c] with n = v / S, h = v % S - pad_h,
-        // zero outside the image.  One task: 8 channels x 8 columns of one virtual row,
-        // loaded as 8 pixels (16 bytes each), transposed in registers, stored as 8 rows of
-        // 16 bytes; consecutive threads take consecutive column chunks of one row.
+        // zero outside the image.  A tile is 64 columns x CT channels of one virtual row:
+        // the pixels' channels are read as contiguous 16-byte pieces into a shared tile
+        // (one pixel per row, padded to spread the banks), then every thread writes 8
+        // columns of one channel as 16 bytes, consecutive threads along the row.
         const T* X = static_cast<const T*>(a.x);
         T* P = static_cast<T*>(a.planes);
-        const int xch = a.Wp / 8;
-        const long long stride = static_cast<long long>(a.plane_blocks) * blockDim.x;
-        for (long long task = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-             task < a.plane_tasks; task += stride) {
-            const int k = static_cast<int>(task % xch);
-            const long long q = task / xch;
-            const long long v = q % a.V;
-            const int cb = static_cast<int>(q / a.V);
-            const int n = static_cast<int>(v / a.S);
-            const int h = static_cast<int>(v - static_cast<long long>(n) * a.S) - a.pad_h;
+        const int pieces = a.CT / 8;                 // 16-byte pieces of a pixel
+        const int nb = static_cast<int>(gridDim.x) - a.run_blocks;
+        for (int tt = static_cast<int>(blockIdx.x) - a.run_blocks; tt < a.plane_tiles; tt += nb) {
+            uint32_t xb, cb, hr;
+            const uint32_t q = a.fd_xt.divmod(static_cast<uint32_t>(tt), xb);
+            const int v = static_cast<int>(a.fd_ct.divmod(q, cb));
+            const int n = static_cast<int>(a.fd_S.divmod(static_cast<uint32_t>(v), hr));
+            const int h = static_cast<int>(hr) - a.pad_h;
             const bool row_in = h >= 0 && h < a.H;
-            const int w0 = 8 * k - a.Lp;
-            const T* src = X + (static_cast<size_t>(row_in ? n : 0) * a.H + (row_in ? h : 0)) *
-                                   static_cast<size_t>(a.W) * a.C + 8 * cb;
-            uint4 px[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int col = w0 + e;
-                px[e] = (row_in && col >= 0 && col < a.W)
-                            ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(col) * a.C))
-                            : make_uint4(0u, 0u, 0u, 0u);
+            const int xa = kTcPrepCols * static_cast<int>(xb);
+            const int c0 = a.CT * static_cast<int>(cb);
+            __syncthreads();   // the previous tile's reads are done
+            if (row_in) {
+                const T* src = X + (static_cast<size_t>(n) * a.H + h) * static_cast<size_t>(a.W) * a.C + c0;
+                for (int idx = threadIdx.x; idx < kTcPrepCols * pieces; idx += kTcPrepThreads) {
+                    const int i = idx >> a.piece_shift, j = idx - (i << a.piece_shift);
+                    const int col = xa + i - a.Lp;
+                    const uint4 val = (col >= 0 && col < a.W)
+                                          ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(col) * a.C + 8 * j))
+                                          : make_uint4(0u, 0u, 0u, 0u);
+                    uint32_t* d = tile + i * kTcPrepRowWords + 4 * j;
+                    d[0] = val.x; d[1] = val.y; d[2] = val.z; d[3] = val.w;
+                }
             }
+            __syncthreads();
+            const int chunks = min(kTcPrepCols, a.Wp - xa) / 8;
+            for (int idx = threadIdx.x; idx < a.CT * 8; idx += kTcPrepThreads) {
+                const int k = idx & 7, c = idx >> 3;
+                if (k >= chunks) continue;
+                uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                if (row_in) {
+                    uint32_t e16[8];
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint4 o;
-                o.x = tc_pair8(px[0], px[1], ch);
-                o.y = tc_pair8(px[2], px[3], ch);
-                o.z = tc_pair8(px[4], px[5], ch);
-                o.w = tc_pair8(px[6], px[7], ch);
-                *reinterpret_cast<uint4*>(P + (static_cast<size_t>(8 * cb + ch) * a.V + v) * a.Wp +
-                                          8 * k) = o;
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t wd = tile[(8 * k + e) * kTcPrepRowWords + (c >> 1)];
+                        e16[e] = (c & 1) ? (wd >> 16) : (wd & 0xffffu);
+                    }
+                    o.x = e16[0] | (e16[1] << 16);
+                    o.y = e16[2] | (e16[3] << 16);
+                    o.z = e16[4] | (e16[5] << 16);
+                    o.w = e16[6] | (e16[7] << 16);
+                }
+                *reinterpret_cast<uint4*>(P + (static_cast<size_t>(c0 + c) * a.V + v) * a.Wp + xa + 8 * k) = o;
             }
         }
     } else {
         // Runs: row r of the run of (c, fh) holds z[r .. r+7], z[i] = filt(fh, i - (NN-1)),
         // zero outside the filter; filt is w, or w rotated by 180 degrees (backward data).
+        // The channel is the fastest task index, so a warp's tap loads are contiguous.
         const uint16_t* Wt = static_cast<const uint16_t*>(a.w);
         uint16_t* R = static_cast<uint16_t*>(a.runs);
         const int rows = 8 * a.NCM;
-        const long long stride = static_cast<long long>(gridDim.x - a.plane_blocks) * blockDim.x;
-        for (long long task = static_cast<long long>(blockIdx.x - a.plane_blocks) * blockDim.x +
-                              threadIdx.x;
-             task < a.run_tasks; task += stride) {
-            const int r = static_cast<int>(task % rows);
-            const long long q = task / rows;
-            const int fh = static_cast<int>(q % a.FH);
-            const int c = static_cast<int>(q / a.FH);
+        const int stride = a.run_blocks * static_cast<int>(blockDim.x);
+        for (int task = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); task < a.run_tasks;
+             task += stride) {
+            uint32_t cu, ru;
+            const uint32_t q = a.fd_C.divmod(static_cast<uint32_t>(task), cu);
+            const int fh = static_cast<int>(a.fd_rows.divmod(q, ru));
+            const int c = static_cast<int>(cu), r = static_cast<int>(ru);
             const int fhe = FLIP ? a.FH - 1 - fh : fh;
             uint32_t z[8];
 #pragma unroll
@@ -376,7 +390,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const TcPrepArgs a) {
             o.y = z[2] | (z[3] << 16);
             o.z = z[4] | (z[5] << 16);
             o.w = z[6] | (z[7] << 16);
-            *reinterpret_cast<uint4*>(R + (static_cast<size_t>(q) * rows + r) * 8) = o;
+            *reinterpret_cast<uint4*>(R + ((static_cast<size_t>(c) * a.FH + fh) * rows + r) * 8) = o;
         }
     }
 }
@@ -767,14 +781,31 @@ cudaError_t launch_tc_inst(const TcPlan& P, const RowConv& p) {
     TcPrepArgs q;
     q.x = p.in; q.w = p.w; q.planes = base; q.runs = base + runs_off;
     q.N = p.N; q.H = p.H; q.W = p.W; q.C = p.C; q.FH = p.FH; q.FW = p.FW; q.pad_h = p.pad_h;
-    q.S = a.S; q.Lp = P.Lp; q.Wp = P.Wp; q.NN = a.NN; q.NCM = a.NCM; q.V = V;
-    q.plane_tasks = static_cast<long long>(p.C / 8) * V * (P.Wp / 8);
-    q.run_tasks = static_cast<long long>(p.C) * p.FH * 8 * a.NCM;
+    q.S = a.S; q.Lp = P.Lp; q.Wp = P.Wp; q.NN = a.NN; q.NCM = a.NCM;
+    q.CT = p.C % 64 == 0 ? 64 : (p.C % 32 == 0 ? 32 : (p.C % 16 == 0 ? 16 : 8));
+    q.piece_shift = q.CT == 64 ? 3 : (q.CT == 32 ? 2 : (q.CT == 16 ? 1 : 0));
+    const long long xtiles = (P.Wp + kTcPrepCols - 1) / kTcPrepCols;
+    const long long plane_tiles = V * (p.C / q.CT) * xtiles;
+    const long long run_tasks = static_cast<long long>(p.C) * p.FH * 8 * a.NCM;
+    if (V >= (1LL << 31) || plane_tiles >= (1LL << 31) || run_tasks >= (1LL << 31)) {
+        scratch_free(scratch, p.stream);
+        return cudaErrorNotSupported;
+    }
+    q.V = static_cast<int>(V);
+    q.plane_tiles = static_cast<int>(plane_tiles);
+    q.run_tasks = static_cast<int>(run_tasks);
+    q.fd_xt.init(static_cast<uint32_t>(xtiles));
+    q.fd_ct.init(static_cast<uint32_t>(p.C / q.CT));
+    q.fd_S.init(static_cast<uint32_t>(a.S));
+    q.fd_C.init(static_cast<uint32_t>(p.C));
+    q.fd_rows.init(static_cast<uint32_t>(8 * a.NCM));
     const int sms = device_info().sm_count;
-    q.plane_blocks = static_cast<int>(std::min<long long>((q.plane_tasks + 255) / 256, 8LL * sms));
-    const int run_blocks = static_cast<int>(std::min<long long>((q.run_tasks + 255) / 256, 2LL * sms));
-    if (p.flip) tc_prep_kernel<T, true><<<q.plane_blocks + run_blocks, 256, 0, p.stream>>>(q);
-    else tc_prep_kernel<T, false><<<q.plane_blocks + run_blocks, 256, 0, p.stream>>>(q);
+    q.run_blocks = static_cast<int>(
+        std::min<long long>((run_tasks + kTcPrepThreads - 1) / kTcPrepThreads, 4LL * sms));
+    const int plane_blocks = static_cast<int>(std::min<long long>(q.plane_tiles, 16LL * sms));
+    const unsigned prep_grid = static_cast<unsigned>(q.run_blocks + plane_blocks);
+    if (p.flip) tc_prep_kernel<T, true><<<prep_grid, kTcPrepThreads, 0, p.stream>>>(q);
+    else tc_prep_kernel<T, false><<<prep_grid, kTcPrepThreads, 0, p.stream>>>(q);
     cudaError_t err = cudaGetLastError();
     if (err == cudaSuccess) {
         a.runs = base + runs_off;
