@@ -239,9 +239,11 @@ cudaError_t launch_rows(const RowConv& rc) {
             default: return launch_rows_stripe_f16(rc);
         }
     }
-    // (a family preference for 16-bit inputs bypasses the small-map kernels)
+    // (a family preference for 16-bit inputs, and the shapes the tcgen05 kernel takes,
+    // bypass the small-map kernels)
     const bool pref16 = rc.dtype != kF32 && family_preference() != 0;
-    if (!pref16 && small_map_serves(rc.H, rc.W, rc.OH, rc.OW, rc.FW, rc.pad_w)) {
+    const bool tc16 = !pref16 && tc_rows_preferred(rc);
+    if (!pref16 && !tc16 && small_map_serves(rc.H, rc.W, rc.OH, rc.OW, rc.FW, rc.pad_w)) {
         cudaError_t err;
         switch (rc.dtype) {
             case kF32: err = launch_small_rows_f32(rc); break;
@@ -573,19 +575,18 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
         return P.e == 2 && FH == FW && tensor_core_fgrad(N, C, P.OH, P.OW, FH, FW) ? 2 : 1;
     }
     const bool pref16 = P.e == 2 && family_preference() != 0;
-    if (FH == FW && !pref16 &&
+    // the same RowConv the entry points build (backward data: over dy, output H x W)
+    const RowConv rc = pass == kPassFwd
+        ? RowConv{a, b, nullptr, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype,
+                  nullptr, nullptr}
+        : RowConv{a, b, nullptr, N, P.OH, P.OW, C, H, W, FH, FW, FH - 1 - pad, FW - 1 - pad,
+                  true, P.dtype, nullptr, nullptr};
+    const bool tc16 = P.e == 2 && !pref16 && tc_rows_preferred(rc);
+    if (FH == FW && !pref16 && !tc16 &&
         (pass == kPassFwd ? small_map_serves(H, W, P.OH, P.OW, FW, pad)
                           : small_map_serves(P.OH, P.OW, H, W, FW, FW - 1 - pad)))
         return 3;
-    if (P.e == 2) {
-        // the same RowConv the entry points build (backward data: over dy, output H x W)
-        const RowConv rc = pass == kPassFwd
-            ? RowConv{a, b, nullptr, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false, P.dtype,
-                      nullptr, nullptr}
-            : RowConv{a, b, nullptr, N, P.OH, P.OW, C, H, W, FH, FW, FH - 1 - pad, FW - 1 - pad,
-                      true, P.dtype, nullptr, nullptr};
-        return tensor_core_rows(rc);
-    }
+    if (P.e == 2) return tensor_core_rows(rc);
     return 1;
 }
 

@@ -197,6 +197,19 @@ size_t small_fgrad_workspace_floats_f16(int N, int H, int W, int C, int OH, int 
 cudaError_t launch_tc_rows_bf16(const RowConv& p);
 cudaError_t launch_tc_rows_f16(const RowConv& p);
 bool tc_rows_fits(const RowConv& p);
+// Where the tcgen05 kernel is the one to run (timed against the row, warp-level MMA and
+// small-map kernels, bf16, fp32 outputs): from 9 taps on rows of at least 28 outputs
+// (64x56x56x128: 110 against 115 us at 9 taps, 110 against 161 at 11, 114 against 218 at 13;
+// 64x28x28x256 at 9 taps a tie, at 7 the row kernel 45 against 63 us), and from 17 taps on
+// 14- to 27-wide rows (64x14x14x512 31x31: 194 against 234 us of the small-map kernel, at
+// 13 taps a tie); never on narrower maps (64x7x7x1024 31x31: 33 us small-map, 262 tcgen05).
+inline bool tc_rows_wanted(const RowConv& p) {
+    return (p.FW >= 9 && p.OW >= 28) || (p.FW >= 17 && p.OW >= 14);
+}
+// tc_rows_wanted and a launch plan exists.
+inline bool tc_rows_preferred(const RowConv& p) {
+    return (p.dtype == kBF16 || p.dtype == kF16) && tc_rows_wanted(p) && tc_rows_fits(p);
+}
 
 // Kernel family a 16-bit forward / backward-data call of this shape runs on (kFamily*), and
 // whether the filter gradient of 16-bit inputs runs on the tensor-core kernel.

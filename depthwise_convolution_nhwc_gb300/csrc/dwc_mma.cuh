@@ -342,16 +342,6 @@ inline bool mma_rows_wanted(const RowConv& p) {
     return p.FW >= kMmaMinFilter && p.OW >= kMmaMinWidth;
 }
 
-// Where the tcgen05 kernel serves 16-bit inputs (timed on the stage shapes: from 17 taps on
-// rows of at least 28 outputs it beat the warp-level MMA kernel, e.g. bf16 32x56x56x128
-// 31x31: 172 against 264 us, 64x28x28x256 31x31: 252 against 264 us; at 13 taps the row
-// kernel was faster than both).
-constexpr int kTcMinFilter = 17;
-constexpr int kTcMinWidth = 28;
-inline bool tc_rows_wanted(const RowConv& p) {
-    return p.FW >= kTcMinFilter && p.OW >= kTcMinWidth;
-}
-
 // 16-bit forward / backward data: the tcgen05 kernel, the warp-level MMA kernel or the row
 // kernel, in that order of preference where each serves the shape (a family preference set
 // for tests and kernel comparisons picks one of them where it can run).

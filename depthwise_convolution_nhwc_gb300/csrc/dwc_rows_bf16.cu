@@ -1,5 +1,5 @@
-// dwc_rows_bf16.cu -- forward / backward-data kernels, bf16 inputs (tensor-core kernel for
-// filters from 15 taps on rows of at least 24 outputs, row-streaming kernel otherwise).
+// dwc_rows_bf16.cu -- forward / backward-data kernels, bf16 inputs (the tcgen05 kernel where
+// tc_rows_wanted says so, the warp-level MMA kernel or the row-streaming kernel otherwise).
 #include "dwc_mma.cuh"
 #include "dwc_s2data.cuh"
 

@@ -1,5 +1,5 @@
-// dwc_rows_f16.cu -- forward / backward-data kernels, f16 inputs (tensor-core kernel for
-// filters from 9 taps, row-streaming kernel below).
+// dwc_rows_f16.cu -- forward / backward-data kernels, f16 inputs (the tcgen05 kernel where
+// tc_rows_wanted says so, the warp-level MMA kernel or the row-streaming kernel otherwise).
 #include "dwc_mma.cuh"
 #include "dwc_s2data.cuh"
 
