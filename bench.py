@@ -30,21 +30,29 @@ METRIC = "DWC fwd+bwd TFLOP/s and GB/s on 1 GB300, % of roofline, per filter siz
 PASSES_ALL = ("fwd", "bwd_data", "bwd_filter")
 PASS_CODE = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2, "fwd_bn_act": 3}
 DTYPE_CODE = {"f32": 0, "bf16": 1, "f16": 2}
-# launches of this library's kernels per pass (every kernel family)
-LAUNCHES = {"fwd": 1, "bwd_data": 1, "bwd_filter": 2}
-FAMILY = {0: "general", 1: "cuda-core", 2: "tensor-core", 3: "small-map"}
+FAMILY = {0: "general", 1: "cuda-core", 2: "tensor-core", 3: "small-map", 4: "tensor-core"}
+TENSOR_FAMILIES = (2, 4)   # tcgen05 (forward / backward data) or warp-level MMA kernels
 # kernels per pass and family (the library's dwc_path tells which family serves a call)
 KERNEL_NAMES = {
     ("fwd", 0): "general_fwd_kernel", ("bwd_data", 0): "general_bwd_data_kernel",
     ("bwd_filter", 0): "general_bwd_filter_kernel + reduce_slices_kernel",
     ("fwd", 1): "rows_kernel<flip=false>", ("bwd_data", 1): "rows_kernel<flip=true>",
     ("bwd_filter", 1): "fgrad_kernel + reduce_slices_kernel",
-    ("fwd", 2): "mma_rows_kernel<flip=false>", ("bwd_data", 2): "mma_rows_kernel<flip=true>",
+    ("fwd", 2): "tc_prep_kernel + tc_rows_kernel", ("bwd_data", 2): "tc_prep_kernel + tc_rows_kernel",
     ("bwd_filter", 2): "mma_fgrad_kernel + reduce_slices_kernel",
+    ("fwd", 4): "mma_rows_kernel<flip=false>", ("bwd_data", 4): "mma_rows_kernel<flip=true>",
     ("fwd", 3): "small_rows_kernel", ("bwd_data", 3): "small_rows_kernel",
     ("bwd_filter", 3): "small_fgrad_kernel + reduce_slices_kernel",
     ("fwd_bn_act", 0): "general_fwd_bnact_kernel", ("fwd_bn_act", 1): "rows_kernel<act>",
 }
+
+
+def launches(pass_name, family):
+    """Launches of this library's kernels in one call of the pass (a filter gradient adds its
+    slice sum; the tcgen05 forward / backward data its preparation kernel)."""
+    if pass_name == "bwd_filter":
+        return 2
+    return 2 if family == 2 else 1
 
 
 def kernel_name(case, pass_name, family):
@@ -55,7 +63,8 @@ def kernel_name(case, pass_name, family):
 
 
 def kernel_family(dwc, case, pass_name):
-    """0 general, 1 CUDA-core, 2 tensor-core kernels (asked of the library itself)."""
+    """0 general, 1 CUDA-core, 2 tensor-core (tcgen05 / warp-level MMA filter gradient),
+    3 small-map, 4 warp-level MMA forward / backward data (asked of the library itself)."""
     return dwc.path(pass_name, None, None, None, case.N, case.H, case.W, case.C, case.FH,
                     case.FW, case.stride, case.pad, DTYPE_CODE[case.dtype])
 
@@ -299,6 +308,7 @@ def record_traffic(raw_csv, workload, passes=PASSES_ALL):
                    for k in ("dram__bytes_read.sum", "dram__bytes_write.sum"))
     per = {"fwd": 0.0, "bwd_data": 0.0, "bwd_filter": 0.0}
     small_rows_seen = 0
+    tc_flip = False
     for d in data:
         name = d[ix["Kernel Name"]]
         targs = name.split("<", 1)[1].split(",") if "<" in name else []
@@ -306,6 +316,11 @@ def record_traffic(raw_csv, workload, passes=PASSES_ALL):
             which = [p for p in passes if p in ("fwd", "bwd_data")]
             per[which[min(small_rows_seen, len(which) - 1)]] += dram(d)
             small_rows_seen += 1
+        elif "tc_prep_kernel" in name:   # <T, FLIP>; its main kernel follows
+            tc_flip = targs[1].split(">")[0].strip() in ("1", "true")
+            per["bwd_data" if tc_flip else "fwd"] += dram(d)
+        elif "tc_rows_kernel" in name:   # the pass of the preparation launched before it
+            per["bwd_data" if tc_flip else "fwd"] += dram(d)
         elif "mma_rows_kernel" in name:  # <T, FLIP>
             flip = targs[1].split(">")[0].strip()
             per["bwd_data" if flip in ("1", "true") else "fwd"] += dram(d)
@@ -433,7 +448,7 @@ def per_filter_table(args, dev, peaks):
     N, H, W, C = SWEEP_SHAPES[0]
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    ab = {0: "gen", 1: "cc", 2: "tc", 3: "sm"}
+    ab = {0: "gen", 1: "cc", 2: "tc", 3: "sm", 4: "mma"}
     points = []
     for dt in ("f32", "bf16"):
         base = Case(N, H, W, C, 3, 3, 1, 1, dt, "normal", 900)
@@ -467,7 +482,7 @@ def per_filter_table(args, dev, peaks):
                 torch.cuda.synchronize()
                 t = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e-3
                 fam = kernel_family(dwc, case, name)
-                tr, bound = rl.roofline_time_s(case, name, peaks, tensor=fam == 2)
+                tr, bound = rl.roofline_time_s(case, name, peaks, tensor=fam in TENSOR_FAMILIES)
                 pt[name] = {"us": round(t * 1e6, 2), "frac": round(tr / t, 3), "bound": bound,
                             "tflops": round(rl.nominal_flops(case) / t / 1e12, 2)}
                 fams.append(ab[fam])
@@ -481,8 +496,9 @@ def per_filter_table(args, dev, peaks):
             "frac": "roofline fraction of the pass (hbm: compulsory bytes at the measured HBM "
                     "copy rate; alu: valid FLOPs at the measured fp32x2 FMA rate; tensor: "
                     "valid FLOPs at the measured bf16 peak)",
-            "families": "fwd/bwd_data/bwd_filter kernel family: cc CUDA-core, tc tensor-core, "
-                        "sm small-map, gen general",
+            "families": "fwd/bwd_data/bwd_filter kernel family: cc CUDA-core, tc tensor-core "
+                        "(tcgen05 forward / backward data, warp-level MMA filter gradient), mma "
+                        "warp-level MMA forward / backward data, sm small-map, gen general",
             "points": points}
 
 
@@ -591,7 +607,7 @@ def _run_e2e_pinned(args, case, passes, x, w, dy, ws, world, flops_step):
 def roofline_entry(rl, case, pass_name, family, seconds, peaks):
     """Roofline of one pass: achieved algorithmic bytes or FLOPs per launch over the
     measured time, against the peak of the resource that bounds it."""
-    _, bound = rl.roofline_time_s(case, pass_name, peaks, tensor=family == 2)
+    _, bound = rl.roofline_time_s(case, pass_name, peaks, tensor=family in TENSOR_FAMILIES)
     if bound == "hbm":
         achieved = rl.compulsory_bytes(case, pass_name) / seconds / 1e9
         peak, unit = peaks["hbm_gbs"], "GB/s"
@@ -804,7 +820,7 @@ def run_ours(args, case, passes):
     passes_out = {}
     for n in passes:
         t = mean_ms[n] * 1e-3
-        tr, b = rl.roofline_time_s(case, n, peaks, tensor=fam[n] == 2)
+        tr, b = rl.roofline_time_s(case, n, peaks, tensor=fam[n] in TENSOR_FAMILIES)
         passes_out[n] = {"ms": mean_ms[n], "ms_median": statistics.median(per_pass[n]),
                          "kernel": kernel_name(case, n, fam[n]),
                          "tflops_nominal": rl.nominal_flops(case) / t / 1e12,
@@ -825,7 +841,7 @@ def run_ours(args, case, passes):
                      "link": link}
                     if e2e_value is not None else None),
             "alu_peaks": alu,
-            "gpu_launches": args.steps * sum(LAUNCHES[n] for n in passes),
+            "gpu_launches": args.steps * sum(launches(n, fam[n]) for n in passes),
             "kernels": {n: kernel_name(case, n, fam[n]) for n in passes},
             "clocks": clocks}
     if not args.no_per_filter and world == 1:
