@@ -201,10 +201,10 @@ bool tc_rows_fits(const RowConv& p);
 // small-map kernels, bf16, fp32 outputs): from 9 taps on rows of at least 28 outputs
 // (64x56x56x128: 110 against 115 us at 9 taps, 110 against 161 at 11, 114 against 218 at 13;
 // 64x28x28x256 at 9 taps a tie, at 7 the row kernel 45 against 63 us), and from 17 taps on
-// 14- to 27-wide rows (64x14x14x512 31x31: 194 against 234 us of the small-map kernel, at
-// 13 taps a tie); never on narrower maps (64x7x7x1024 31x31: 33 us small-map, 262 tcgen05).
+// rows of 17 to 27 outputs; maps up to 16 wide stay on the small-map kernel (64x14x14x512
+// 31x31: 134 us there against 194 on tcgen05; 64x7x7x1024 31x31: 33 against 262).
 inline bool tc_rows_wanted(const RowConv& p) {
-    return (p.FW >= 9 && p.OW >= 28) || (p.FW >= 17 && p.OW >= 14);
+    return (p.FW >= 9 && p.OW >= 28) || (p.FW >= 17 && p.OW >= 17);
 }
 // tc_rows_wanted and a launch plan exists.
 inline bool tc_rows_preferred(const RowConv& p) {

@@ -8,12 +8,16 @@
 // GPUs", §4.4) is taken here to its end for maps that fit in shared memory whole:
 //
 //  * A CTA owns a block of 32 channels (one per lane) and stages whole images of it
-//    (cp.async, 16-byte chunks, double-buffered across work units).
-//  * Forward / backward data: each warp computes one output row oh of one image; for every
-//    input row ih that meets a filter row (fh = ih - oh + pad_h), the input row is held in
-//    registers as two sets of column pairs, {x[2k], x[2k+1]} and {x[2k-1], x[2k]}, so that
-//    the packed FMA of tap offset d = fw - pad_w updates the output pair (2k, 2k+1) with the
-//    input pair starting at 2k + d.  Offsets run over [-DR, DR], the taps that can meet a
+//    (cp.async, 16-byte chunks) through a ring of up to 8 work units, so that the copies of
+//    the units ahead are in flight while one is computed (a 7x7 map's unit is a few KB: two
+//    buffers left every unit waiting for its copy).
+//  * Forward / backward data: on maps of at most 8 x 8 outputs each warp computes a whole
+//    image (all its output rows in registers, every input row loaded once and applied to
+//    each output row it meets); otherwise one output row oh of one image.  For every input row ih that
+//    meets a filter row (fh = ih - oh + pad_h), the input row is held in registers as two
+//    sets of column pairs, {x[2k], x[2k+1]} and {x[2k-1], x[2k]}, so that the packed FMA of
+//    tap offset d = fw - pad_w updates the output pair (2k, 2k+1) with the input pair
+//    starting at 2k + d.  Offsets run over [-DR, DR], the taps that can meet a
 //    map of this width; the window of filter rows that meet the image, 2*DR+1 taps each,
 //    is copied once per channel block (cp.async, zero fill for taps outside the filter).
 //  * Filter gradient: each warp owns two window rows fh (half a window apart, so that the
@@ -51,6 +55,19 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int K>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(K) : "memory");
+}
+// cp_async_wait<k> for a run-time k in [0, 7]
+__device__ __forceinline__ void cp_async_wait_n(int k) {
+    switch (k) {
+        case 0: cp_async_wait<0>(); break;
+        case 1: cp_async_wait<1>(); break;
+        case 2: cp_async_wait<2>(); break;
+        case 3: cp_async_wait<3>(); break;
+        case 4: cp_async_wait<4>(); break;
+        case 5: cp_async_wait<5>(); break;
+        case 6: cp_async_wait<6>(); break;
+        default: cp_async_wait<7>(); break;
+    }
 }
 
 // Pair of adjacent columns (x[i], x[i+1]) of a register row for i in [-1, MAXW - 1], with
@@ -103,17 +120,21 @@ struct SmallArgs {
     int fh_lo, nfh;     // filter rows that meet the image for some output row
     int G;              // images per work unit
     int groups;         // work units per channel block
+    int ns;             // staged work units in the ring (2..8, at most groups + 1)
     uint32_t units;     // cblocks * groups, channel block slowest
     uint32_t buf_elems; // elements of one staged buffer (G images)
-    uint32_t win_off;   // byte offset of the filter window
+    uint32_t win_off;   // byte offset of the filter-window slots
+    uint32_t win_elems; // elements of one filter-window slot
+    int win_slots;      // 2: windows staged ahead with their block's first unit; 1: staged
+                        // when the block starts (large windows)
 };
 
 template <typename T, int MAXW, int DR, class OutT = float>
 __global__ void __launch_bounds__(kSmMaxWarps * 32, 1) small_rows_kernel(const SmallArgs a) {
     constexpr int NJ = 2 * DR + 1;
     extern __shared__ __align__(128) unsigned char smem[];
-    T* xbuf = reinterpret_cast<T*>(smem);                          // [2][G][H][MAXW][32]
-    T* win = reinterpret_cast<T*>(smem + a.win_off);               // [nfh][NJ][32]
+    T* xbuf = reinterpret_cast<T*>(smem);                          // [ns][G][H][MAXW][32]
+    T* wins = reinterpret_cast<T*>(smem + a.win_off);              // [win_slots][nfh][NJ][32]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nthreads = blockDim.x, nwarps = nthreads >> 5;
     const T* X = static_cast<const T*>(a.in);
@@ -124,100 +145,163 @@ __global__ void __launch_bounds__(kSmMaxWarps * 32, 1) small_rows_kernel(const S
     const uint32_t u_begin = blockIdx.x * per_cta;
     const uint32_t u_end = min(a.units, u_begin + per_cta);
     if (u_begin >= u_end) return;
+    const uint32_t ns = static_cast<uint32_t>(a.ns);
 
     if (a.W < MAXW) {
         const int zc = MAXW - a.W;
-        for (int i = tid; i < 2 * a.G * a.H * zc * kSmCh; i += nthreads) {
+        for (int i = tid; i < a.ns * a.G * a.H * zc * kSmCh; i += nthreads) {
             const int ch = i % kSmCh, px = i / kSmCh;
-            const int col = a.W + px % zc, rr = px / zc;  // rr runs over [2][G][H]
+            const int col = a.W + px % zc, rr = px / zc;  // rr runs over [ns][G][H]
             xbuf[(rr * MAXW + col) * kSmCh + ch] = T(0.f);
         }
     }
-    auto stage = [&](uint32_t u, int buf) {
+    // Filter window of channel block cb into its slot: win[r][j] = filt(fh_lo + r,
+    // j - DR + pad_w), zero where the tap lies outside the filter (whole 16-byte chunks of
+    // channels).
+    auto stage_window = [&](int cb) {
+        constexpr int kPerChunk = 16 / static_cast<int>(sizeof(T));
+        constexpr int kChunks = kSmCh / kPerChunk;
+        const int c0 = cb * kSmCh;
+        const int cvalid = min(kSmCh, a.C - c0);
+        T* win = wins + (a.win_slots == 2 ? (cb & 1) : 0) * a.win_elems;
+        for (int i = tid; i < a.nfh * NJ * kChunks; i += nthreads) {
+            const int q = i % kChunks, rj = i / kChunks;
+            const int fh = a.fh_lo + rj / NJ, fw = rj % NJ - DR + a.pad_w;
+            const bool valid = fw >= 0 && fw < a.FW && q * kPerChunk < cvalid;
+            const int sh = a.flip ? a.FH - 1 - fh : fh;
+            const int sw = a.flip ? a.FW - 1 - fw : fw;
+            const T* src = valid ? Wt + (static_cast<size_t>(sh) * a.FW + sw) * a.C + c0 + q * kPerChunk
+                                 : Wt;
+            cp_async16_zfill(win + rj * kSmCh + q * kPerChunk, src, valid);
+        }
+    };
+    auto block_starts = [&](uint32_t u) { return u == u_begin || u % a.groups == 0; };
+    // One copy group per unit u, in unit order: the images of u into ring slot
+    // (u - u_begin) % ns and, with two window slots, where u is the CTA's first unit of a
+    // channel block, the block's window into slot cb % 2 (the ring holds at most groups + 1
+    // units, so a window slot is refilled only after every unit of the block that used it
+    // has been computed).  With one window slot the window is copied when its block's first
+    // unit comes up (every earlier unit is done then), as a group of its own.
+    auto stage = [&](uint32_t u) {
         const int cb = static_cast<int>(u / a.groups);
         const int n0 = static_cast<int>(u % a.groups) * a.G;
+        if (a.win_slots == 2 && block_starts(u)) stage_window(cb);
+        const int slot = static_cast<int>((u - u_begin) % ns);
         for (int g = 0; g < a.G && n0 + g < a.N; ++g)
-            stage_image<T, MAXW>(xbuf + buf * a.buf_elems + g * img,
+            stage_image<T, MAXW>(xbuf + slot * a.buf_elems + g * img,
                                  X + static_cast<size_t>(n0 + g) * a.H * a.W * a.C, a.H, a.W, a.C,
                                  cb * kSmCh, tid, nthreads);
         cp_async_commit();
     };
 
-    // Copy groups, in commit order: image(u_begin), then per unit u [window(u) when the
-    // channel block changes], image(u + 1) (empty at the end).  Waiting for all but the
-    // newest group therefore covers the window and the image of unit u.
-    stage(u_begin, 0);
-    int cur_cb = -1;
+    // groups u_begin .. u_begin + ns - 2 ahead; per unit one more, so that waiting for all
+    // but the newest ns - 1 groups covers unit u (empty groups past the end keep the count)
+    for (uint32_t k = 0; k + 1 < ns; ++k) {
+        if (u_begin + k < u_end) stage(u_begin + k);
+        else cp_async_commit();
+    }
     for (uint32_t u = u_begin; u < u_end; ++u) {
-        const int buf = static_cast<int>((u - u_begin) & 1u);
+        const int slot = static_cast<int>((u - u_begin) % ns);
         const int cb = static_cast<int>(u / a.groups);
         const int c0 = cb * kSmCh;
-        if (cb != cur_cb) {
-            // filter window of this channel block: win[r][j] = filt(fh_lo + r, j - DR + pad_w),
-            // zero where the tap lies outside the filter (whole 16-byte chunks of channels)
-            constexpr int kPerChunk = 16 / static_cast<int>(sizeof(T));
-            constexpr int kChunks = kSmCh / kPerChunk;
-            const int cvalid = min(kSmCh, a.C - c0);
-            for (int i = tid; i < a.nfh * NJ * kChunks; i += nthreads) {
-                const int q = i % kChunks, rj = i / kChunks;
-                const int fh = a.fh_lo + rj / NJ, fw = rj % NJ - DR + a.pad_w;
-                const bool valid = fw >= 0 && fw < a.FW && q * kPerChunk < cvalid;
-                const int sh = a.flip ? a.FH - 1 - fh : fh;
-                const int sw = a.flip ? a.FW - 1 - fw : fw;
-                const T* src = valid ? Wt + (static_cast<size_t>(sh) * a.FW + sw) * a.C + c0 + q * kPerChunk
-                                     : Wt;
-                cp_async16_zfill(win + rj * kSmCh + q * kPerChunk, src, valid);
-            }
+        const T* win = wins + (a.win_slots == 2 ? (cb & 1) : 0) * a.win_elems;
+        const bool win_now = a.win_slots == 1 && block_starts(u);
+        if (win_now) {
+            stage_window(cb);
             cp_async_commit();
-            cur_cb = cb;
         }
-        if (u + 1 < u_end) stage(u + 1, buf ^ 1);
-        else cp_async_commit();  // keeps the newest group the next image for the wait below
-        cp_async_wait<1>();
+        if (u + ns - 1 < u_end) stage(u + ns - 1);
+        else cp_async_commit();
+        // all but the newest ns - 1 groups (over-waiting where a window group sits among
+        // them is harmless); a window copied now is second newest
+        cp_async_wait_n(win_now ? 1 : a.ns - 1);
         __syncthreads();
 
         const int n0 = static_cast<int>(u % a.groups) * a.G;
         const bool lane_ok = c0 + lane < a.C;
-        for (int q = warp; q < a.G * a.OH; q += nwarps) {
-            const int g = q / a.OH, oh = q - g * a.OH;
-            const int n = n0 + g;
-            if (n >= a.N) break;
-            const T* xg = xbuf + buf * a.buf_elems + g * img;
-            float2 acc[MAXW / 2];
+        // packed FMAs of input row xe/xo into the output-row accumulators acc through window
+        // row wrow (tap offsets -DR..DR)
+        auto row_taps = [&](float2 (&acc)[MAXW / 2], const float2 (&xe)[MAXW / 2],
+                            const float2 (&xo)[MAXW / 2 + 1], const T* wr) {
 #pragma unroll
-            for (int k = 0; k < MAXW / 2; ++k) acc[k] = make_float2(0.f, 0.f);
-            const int ih_lo = max(0, oh - a.pad_h), ih_hi = min(a.H, oh - a.pad_h + a.FH);
-            for (int ih = ih_lo; ih < ih_hi; ++ih) {
-                float2 xe[MAXW / 2], xo[MAXW / 2 + 1];
-                load_row_pairs<T, MAXW>(xg + ih * MAXW * kSmCh, lane, xe, xo);
-                const T* wr = win + (ih - oh + a.pad_h - a.fh_lo) * NJ * kSmCh + lane;
-#pragma unroll
-                for (int j = 0; j < NJ; ++j) {
-                    const float wv = to_f32(wr[j * kSmCh]);
-                    const float2 w2 = make_float2(wv, wv);
-#pragma unroll
-                    for (int k = 0; k < MAXW / 2; ++k) {
-                        const int i = 2 * k + j - DR;  // first input column of the pair
-                        if (i < -1 || i > MAXW - 1) continue;
-                        fma2(acc[k], col_pair<MAXW>(xe, xo, i), w2);
-                    }
-                }
-            }
-            if (lane_ok) {
-                OutT* o = static_cast<OutT*>(a.out) + (static_cast<size_t>(n) * a.OH + oh) * a.OW * a.C + c0 + lane;
+            for (int j = 0; j < NJ; ++j) {
+                const float wv = to_f32(wr[j * kSmCh]);
+                const float2 w2 = make_float2(wv, wv);
 #pragma unroll
                 for (int k = 0; k < MAXW / 2; ++k) {
-                    if constexpr (std::is_same<OutT, float>::value) {
-                        if (2 * k < a.OW) __stcs(o + static_cast<size_t>(2 * k) * a.C, acc[k].x);
-                        if (2 * k + 1 < a.OW) __stcs(o + static_cast<size_t>(2 * k + 1) * a.C, acc[k].y);
-                    } else {
-                        if (2 * k < a.OW) store_out(o + static_cast<size_t>(2 * k) * a.C, acc[k].x);
-                        if (2 * k + 1 < a.OW) store_out(o + static_cast<size_t>(2 * k + 1) * a.C, acc[k].y);
-                    }
+                    const int i = 2 * k + j - DR;  // first input column of the pair
+                    if (i < -1 || i > MAXW - 1) continue;
+                    fma2(acc[k], col_pair<MAXW>(xe, xo, i), w2);
                 }
             }
+        };
+        auto store_row = [&](const float2 (&acc)[MAXW / 2], int n, int oh) {
+            if (!lane_ok) return;
+            OutT* o = static_cast<OutT*>(a.out) + (static_cast<size_t>(n) * a.OH + oh) * a.OW * a.C + c0 + lane;
+#pragma unroll
+            for (int k = 0; k < MAXW / 2; ++k) {
+                if constexpr (std::is_same<OutT, float>::value) {
+                    if (2 * k < a.OW) __stcs(o + static_cast<size_t>(2 * k) * a.C, acc[k].x);
+                    if (2 * k + 1 < a.OW) __stcs(o + static_cast<size_t>(2 * k + 1) * a.C, acc[k].y);
+                } else {
+                    if (2 * k < a.OW) store_out(o + static_cast<size_t>(2 * k) * a.C, acc[k].x);
+                    if (2 * k + 1 < a.OW) store_out(o + static_cast<size_t>(2 * k + 1) * a.C, acc[k].y);
+                }
+            }
+        };
+        auto per_row = [&]() {
+            for (int q = warp; q < a.G * a.OH; q += nwarps) {
+                const int g = q / a.OH, oh = q - g * a.OH;
+                const int n = n0 + g;
+                if (n >= a.N) break;
+                const T* xg = xbuf + slot * a.buf_elems + g * img;
+                float2 acc[MAXW / 2];
+#pragma unroll
+                for (int k = 0; k < MAXW / 2; ++k) acc[k] = make_float2(0.f, 0.f);
+                const int ih_lo = max(0, oh - a.pad_h), ih_hi = min(a.H, oh - a.pad_h + a.FH);
+                for (int ih = ih_lo; ih < ih_hi; ++ih) {
+                    float2 xe[MAXW / 2], xo[MAXW / 2 + 1];
+                    load_row_pairs<T, MAXW>(xg + ih * MAXW * kSmCh, lane, xe, xo);
+                    row_taps(acc, xe, xo, win + (ih - oh + a.pad_h - a.fh_lo) * NJ * kSmCh + lane);
+                }
+                store_row(acc, n, oh);
+            }
+        };
+        if constexpr (MAXW == 8) {
+          if (a.OH > MAXW) {
+            per_row();
+          } else {
+            // a warp per image: the output rows' accumulators stay in registers while each
+            // input row is loaded once (OH <= 8)
+            for (int g = warp; g < a.G; g += nwarps) {
+                const int n = n0 + g;
+                if (n >= a.N) break;
+                const T* xg = xbuf + slot * a.buf_elems + g * img;
+                float2 acc[MAXW][MAXW / 2];
+#pragma unroll
+                for (int r = 0; r < MAXW; ++r) {
+#pragma unroll
+                    for (int k = 0; k < MAXW / 2; ++k) acc[r][k] = make_float2(0.f, 0.f);
+                }
+                for (int ih = 0; ih < a.H; ++ih) {
+                    float2 xe[MAXW / 2], xo[MAXW / 2 + 1];
+                    load_row_pairs<T, MAXW>(xg + ih * MAXW * kSmCh, lane, xe, xo);
+#pragma unroll
+                    for (int oh = 0; oh < MAXW; ++oh) {
+                        const int wrow = ih - oh + a.pad_h - a.fh_lo;   // window row (fh - fh_lo)
+                        if (oh >= a.OH || wrow < 0 || wrow >= a.nfh) continue;
+                        row_taps(acc[oh], xe, xo, win + wrow * NJ * kSmCh + lane);
+                    }
+                }
+#pragma unroll
+                for (int oh = 0; oh < MAXW; ++oh)
+                    if (oh < a.OH) store_row(acc[oh], n, oh);
+            }
+          }
+        } else {
+            per_row();
         }
-        __syncthreads();  // the buffer is re-staged and the window may be replaced
+        __syncthreads();  // the slot is re-staged, and the other window slot may be refilled
     }
     cp_async_wait<0>();
 }
@@ -409,22 +493,34 @@ cudaError_t launch_small_rows_inst(const RowConv& p) {
     const size_t img_bytes = static_cast<size_t>(p.H) * MAXW * kSmCh * sizeof(T);
     const size_t win_bytes = static_cast<size_t>(std::max(a.nfh, 1)) * NJ * kSmCh * sizeof(T);
     const size_t cap = static_cast<size_t>(device_info().max_smem_optin);
-    // images per unit: enough output rows for the warps, within shared memory
-    int G = std::max(1, std::min(4, (kSmMaxWarps + p.OH - 1) / std::max(p.OH, 1)));
-    while (G > 1 && 2 * G * img_bytes + win_bytes > cap) --G;
-    if (2 * G * img_bytes + win_bytes > cap) return cudaErrorNotSupported;
+    // images per unit: maps of at most 8 x 8 outputs, one per warp (8); others, enough output rows
+    // for the warps; within shared memory
+    const bool per_image = MAXW == 8 && p.OH <= MAXW;   // the kernel's warp-per-image path
+    int G = per_image ? std::min(8, std::max(p.N, 1))
+                      : std::max(1, std::min(4, (kSmMaxWarps + p.OH - 1) / std::max(p.OH, 1)));
+    while (G > 1 && 2 * G * img_bytes + win_bytes + 128 > cap) --G;
+    if (2 * G * img_bytes + win_bytes + 128 > cap) return cudaErrorNotSupported;
     a.G = G;
     a.buf_elems = static_cast<uint32_t>(G * p.H * MAXW * kSmCh);
-    a.win_off = static_cast<uint32_t>((2 * G * img_bytes + 127) & ~size_t(127));
-    const size_t smem = a.win_off + win_bytes;
     const int cblocks = (p.C + kSmCh - 1) / kSmCh;
     a.groups = (p.N + G - 1) / G;
     const long long units = static_cast<long long>(cblocks) * a.groups;
     if (units == 0) return cudaSuccess;
     if (units >= (1LL << 31)) return cudaErrorNotSupported;
     a.units = static_cast<uint32_t>(units);
-    // warps: output rows of a unit spread evenly over at most 8 warps
-    const int pairs = G * p.OH;
+    // ring depth: the CTA's units up to 8, at most groups + 1 (a filter-window slot is
+    // refilled only after its block's units are done), within shared memory
+    const long long grid0 = std::min<long long>(units, static_cast<long long>(device_info().sm_count));
+    const long long per_cta = (units + grid0 - 1) / grid0;
+    int ns = static_cast<int>(std::min<long long>({8LL, std::max(2LL, per_cta), a.groups + 1LL}));
+    a.win_slots = 2 * G * img_bytes + 2 * win_bytes + 128 <= cap ? 2 : 1;
+    while (ns > 2 && ns * G * img_bytes + a.win_slots * win_bytes + 128 > cap) --ns;
+    a.ns = ns;
+    a.win_elems = static_cast<uint32_t>(std::max(a.nfh, 1) * NJ * kSmCh);
+    a.win_off = static_cast<uint32_t>((ns * G * img_bytes + 127) & ~size_t(127));
+    const size_t smem = a.win_off + a.win_slots * win_bytes;
+    // warps: the unit's images (maps up to 8 wide) or output rows, spread evenly
+    const int pairs = per_image ? G : G * p.OH;
     const int rounds = (pairs + kSmMaxWarps - 1) / kSmMaxWarps;
     const int nwarps = (pairs + rounds - 1) / rounds;
     auto kern = small_rows_kernel<T, MAXW, DR, OutT>;

@@ -180,15 +180,14 @@ def test_path_selection_host_logic(lib):
     assert p(0, **big, dtype=1) == 2 and p(1, **big, dtype=2) == 2 and p(2, **big, dtype=1) == 2
     assert p(0, **big) == 1 and p(2, **big) == 1          # fp32 stays on CUDA cores
     assert p(0, **dict(big, FH=7, FW=7, pad=3), dtype=1) == 1
-    # tcgen05 from 9 taps on rows of 28+ outputs, from 17 taps on 14- to 27-wide rows
+    # tcgen05 from 9 taps on rows of 28+ outputs, from 17 taps on 17- to 27-wide rows
     assert p(0, **dict(big, W=28, FH=9, FW=9, pad=4), dtype=1) == 2
     assert p(0, **dict(big, W=27, FH=9, FW=9, pad=4), dtype=1) == 1
-    assert p(0, **dict(big, W=16), dtype=1) == 2
-    assert p(0, **dict(big, W=12), dtype=1) == 1          # narrow rows: row-streaming kernel
-    # small maps: the tcgen05 kernel takes 14 x 14 maps from 17 taps, the small-map kernel
-    # the rest (and every 7 x 7 map)
+    assert p(0, **dict(big, W=17), dtype=1) == 2
+    assert p(0, **dict(big, W=16), dtype=1) == 1          # narrow rows: row-streaming kernel
+    # small maps stay on the small-map kernel (14 x 14 and 7 x 7, large filters)
     m14 = dict(H=14, W=14, C=64, dtype=1)
-    assert p(0, **m14, FH=31, FW=31, pad=15) == 2 and p(1, **m14, FH=31, FW=31, pad=15) == 2
+    assert p(0, **m14, FH=31, FW=31, pad=15) == 3 and p(1, **m14, FH=31, FW=31, pad=15) == 3
     assert p(0, **m14, FH=13, FW=13, pad=6) == 3
     assert p(0, H=7, W=7, C=64, dtype=1, FH=31, FW=31, pad=15) == 3
     # an unaligned (but element-aligned) pointer falls back to the general kernels
