@@ -343,23 +343,24 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const TcPrepArg
             }
             __syncthreads();
             const int chunks = min(kTcPrepCols, a.Wp - xa) / 8;
-            for (int idx = threadIdx.x; idx < a.CT * 8; idx += kTcPrepThreads) {
-                const int k = idx & 7, c = idx >> 3;
+            // a task: the 8 columns of chunk k of the channel pair (2cp, 2cp + 1), from the
+            // same 8 shared words (one word holds both channels of a column)
+            for (int idx = threadIdx.x; idx < (a.CT / 2) * 8; idx += kTcPrepThreads) {
+                const int k = idx & 7, cp = idx >> 3;
                 if (k >= chunks) continue;
-                uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
                 if (row_in) {
-                    uint32_t e16[8];
+                    uint32_t wd[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const uint32_t wd = tile[(8 * k + e) * kTcPrepRowWords + (c >> 1)];
-                        e16[e] = (c & 1) ? (wd >> 16) : (wd & 0xffffu);
-                    }
-                    o.x = e16[0] | (e16[1] << 16);
-                    o.y = e16[2] | (e16[3] << 16);
-                    o.z = e16[4] | (e16[5] << 16);
-                    o.w = e16[6] | (e16[7] << 16);
+                    for (int e = 0; e < 8; ++e) wd[e] = tile[(8 * k + e) * kTcPrepRowWords + cp];
+                    lo.x = __byte_perm(wd[0], wd[1], 0x5410); hi.x = __byte_perm(wd[0], wd[1], 0x7632);
+                    lo.y = __byte_perm(wd[2], wd[3], 0x5410); hi.y = __byte_perm(wd[2], wd[3], 0x7632);
+                    lo.z = __byte_perm(wd[4], wd[5], 0x5410); hi.z = __byte_perm(wd[4], wd[5], 0x7632);
+                    lo.w = __byte_perm(wd[6], wd[7], 0x5410); hi.w = __byte_perm(wd[6], wd[7], 0x7632);
                 }
-                *reinterpret_cast<uint4*>(P + (static_cast<size_t>(c0 + c) * a.V + v) * a.Wp + xa + 8 * k) = o;
+                T* dst = P + (static_cast<size_t>(c0 + 2 * cp) * a.V + v) * a.Wp + xa + 8 * k;
+                *reinterpret_cast<uint4*>(dst) = lo;
+                *reinterpret_cast<uint4*>(dst + static_cast<size_t>(a.V) * a.Wp) = hi;
             }
         }
     } else {
@@ -376,20 +377,24 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const TcPrepArg
             const uint32_t q = a.fd_C.divmod(static_cast<uint32_t>(task), cu);
             const int fh = static_cast<int>(a.fd_rows.divmod(q, ru));
             const int c = static_cast<int>(cu), r = static_cast<int>(ru);
-            const int fhe = FLIP ? a.FH - 1 - fh : fh;
-            uint32_t z[8];
+            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+            // rows r + 7 < NN - 1 or r > NN + FW - 2 hold no tap (most of a run): zeros, with no
+            // tap computed (the test is uniform over a warp, whose lanes differ in c only)
+            const int f0 = r - (a.NN - 1);
+            if (f0 + 7 >= 0 && f0 < a.FW) {
+                const int fhe = FLIP ? a.FH - 1 - fh : fh;
+                const uint16_t* wrow = Wt + static_cast<size_t>(fhe) * a.FW * a.C + c;
+                uint32_t z[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int f = r + e - (a.NN - 1);
-                z[e] = (f >= 0 && f < a.FW)
-                           ? Wt[(static_cast<size_t>(fhe) * a.FW + (FLIP ? a.FW - 1 - f : f)) * a.C + c]
-                           : 0u;
+                for (int e = 0; e < 8; ++e) {
+                    const int f = f0 + e;
+                    z[e] = (f >= 0 && f < a.FW) ? wrow[static_cast<size_t>(FLIP ? a.FW - 1 - f : f) * a.C] : 0u;
+                }
+                o.x = z[0] | (z[1] << 16);
+                o.y = z[2] | (z[3] << 16);
+                o.z = z[4] | (z[5] << 16);
+                o.w = z[6] | (z[7] << 16);
             }
-            uint4 o;
-            o.x = z[0] | (z[1] << 16);
-            o.y = z[2] | (z[3] << 16);
-            o.z = z[4] | (z[5] << 16);
-            o.w = z[6] | (z[7] << 16);
             *reinterpret_cast<uint4*>(R + ((static_cast<size_t>(c) * a.FH + fh) * rows + r) * 8) = o;
         }
     }
