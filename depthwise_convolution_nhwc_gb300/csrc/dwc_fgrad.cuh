@@ -662,7 +662,7 @@ size_t fgrad_workspace_t(int N, int OH, int OW, int C, int FH, int FW) {
 }
 
 
-// Stride-2 filter gradient: square filters of 3, 5 or 7 taps.
+// Stride-2 filter gradient: square filters of 3 to 13 taps.
 template <int F>
 using FgradS2Tile = FgradTile<F, F, 0, 0, 0, 0, 2>;
 
@@ -673,6 +673,9 @@ cudaError_t launch_fgrad_s2_dispatch(const FilterGrad& p) {
         case 3: return launch_fgrad_inst<T, 3, 3, FgradS2Tile<3>>(p);
         case 5: return launch_fgrad_inst<T, 5, 5, FgradS2Tile<5>>(p);
         case 7: return launch_fgrad_inst<T, 7, 7, FgradS2Tile<7>>(p);
+        case 9: return launch_fgrad_inst<T, 9, 9, FgradS2Tile<9>>(p);
+        case 11: return launch_fgrad_inst<T, 11, 11, FgradS2Tile<11>>(p);
+        case 13: return launch_fgrad_inst<T, 13, 13, FgradS2Tile<13>>(p);
         default: return cudaErrorNotSupported;
     }
 }
@@ -684,6 +687,9 @@ size_t fgrad_s2_workspace_t(int N, int OH, int OW, int C, int FH, int FW) {
         case 3: return fgrad_workspace_inst<T, 3, 3, FgradS2Tile<3>>(N, OH, OW, C);
         case 5: return fgrad_workspace_inst<T, 5, 5, FgradS2Tile<5>>(N, OH, OW, C);
         case 7: return fgrad_workspace_inst<T, 7, 7, FgradS2Tile<7>>(N, OH, OW, C);
+        case 9: return fgrad_workspace_inst<T, 9, 9, FgradS2Tile<9>>(N, OH, OW, C);
+        case 11: return fgrad_workspace_inst<T, 11, 11, FgradS2Tile<11>>(N, OH, OW, C);
+        case 13: return fgrad_workspace_inst<T, 13, 13, FgradS2Tile<13>>(N, OH, OW, C);
         default: return 0;
     }
 }

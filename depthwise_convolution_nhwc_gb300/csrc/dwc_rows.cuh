@@ -629,8 +629,8 @@ cudaError_t launch_rows_dispatch(const RowConv& p) {
 #undef DWC_ROWS_CASE
 }
 
-// Stride-2 forward: one output row per band, 8 outputs per lane (filters of 3, 5 and 7 taps,
-// the down-sampling layers of mobile networks).
+// Stride-2 forward: one output row per band, 8 outputs per lane (filters of 3 to 13 taps:
+// the down-sampling layers of mobile networks, 3 to 7, and of large-kernel networks).
 template <typename T, int F, class OutT>
 cudaError_t launch_rows_s2_square(const RowConv& p) {
     if constexpr (std::is_same<OutT, float>::value) {
@@ -660,6 +660,9 @@ cudaError_t launch_rows_s2_dispatch(const RowConv& p) {
         case 3: return launch_rows_s2_square<T, 3, OutT>(p);
         case 5: return launch_rows_s2_square<T, 5, OutT>(p);
         case 7: return launch_rows_s2_square<T, 7, OutT>(p);
+        case 9: return launch_rows_s2_square<T, 9, OutT>(p);
+        case 11: return launch_rows_s2_square<T, 11, OutT>(p);
+        case 13: return launch_rows_s2_square<T, 13, OutT>(p);
         default: return cudaErrorNotSupported;
     }
 }
