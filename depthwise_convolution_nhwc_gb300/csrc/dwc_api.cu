@@ -198,13 +198,11 @@ bool fast_eligible(const Problem& P, const void* a, const void* b, const void* o
     return true;
 }
 
-// Stride-2 fast paths, same layout rules: square filters of 3, 5 or 7 taps for every pass,
-// and of 9, 11 or 13 taps for the forward pass and the filter gradient (the backward-data
-// kernel holds all F x F taps in registers).
-bool fast_s2_eligible(const Problem& P, const void* a, const void* b, const void* out,
-                      bool data_pass = false) {
+// Stride-2 fast paths (forward, backward data, filter gradient): square odd filters of 3 to
+// 13 taps, same layout rules.
+bool fast_s2_eligible(const Problem& P, const void* a, const void* b, const void* out) {
     const int F = P.FH;
-    if (P.s != 2 || P.FH != P.FW || F < 3 || (F & 1) == 0 || F > (data_pass ? 7 : 13)) return false;
+    if (P.s != 2 || P.FH != P.FW || F < 3 || (F & 1) == 0 || F > 13) return false;
     if (P.C % (16 / P.e) != 0) return false;
     for (const void* q : {a, b, out})
         if (q != nullptr && !aligned(q, 16)) return false;
@@ -379,7 +377,7 @@ dwc_status_t bwd_data_impl(const void* dy, const void* w, void* dx, int N, int H
     }
     GeneralConv gc{dy, w, dx, N, H, W, C, P.OH, P.OW, FH, FW, stride, pad, P.dtype, nullptr, 0, s};
     gc.out_dtype = od;
-    if (fast_s2_eligible(P, dy, w, dx, true)) {
+    if (fast_s2_eligible(P, dy, w, dx)) {
         const cudaError_t err = launch_s2_bwd_data(gc);
         if (err != cudaErrorNotSupported) return map_cuda(err);
         (void)cudaGetLastError();
@@ -566,7 +564,7 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
     if (pass < 0 || pass > 3) return -1;
     if (check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P) != DWC_OK) return -1;
     if (pass == 3) return bnact_fast_eligible(P, a, b, out) ? 1 : 0;
-    if (fast_s2_eligible(P, a, b, out, pass == kPassBwdData)) {
+    if (fast_s2_eligible(P, a, b, out)) {
         if (pass == kPassBwdFilter)
             return filter_grad_s2_workspace_floats(N, P.OH, P.OW, C, FH, FW, P.dtype) > 0 ? 1 : 0;
         return 1;

@@ -1,5 +1,5 @@
-// dwc_s2data.cuh -- backward data ("input gradient") at stride 2 for square filters of 3, 5
-// or 7 taps.
+// dwc_s2data.cuh -- backward data ("input gradient") at stride 2 for square filters of 3 to
+// 13 taps.
 //
 //   dx[n, ih, iw, c] = sum over (oh, ow, fh, fw) with ih = 2*oh + fh - pad and
 //                      iw = 2*ow + fw - pad of dy[n, oh, ow, c] * w[fh, fw, c]
@@ -202,6 +202,90 @@ s2_bwd_data_stream_kernel(const T* __restrict__ dy, const T* __restrict__ w, con
     }
 }
 
+// 9 to 13 taps: a cell's F x F taps no longer fit in registers, so a thread takes one pixel
+// class (r, q) of its cells -- the sub-filter w[r + 2k][q + 2j], KR x KQ <= 7 x 7 taps -- in
+// a circular window of KQ dy columns (KR loads per cell); the class is the launch's
+// blockIdx.y.  Two accumulators split each pixel's chain of up to 49 dependent FMAs.
+template <typename T, int F, int R, int Q, class OutT>
+__device__ __forceinline__ void s2_data_class(const T* __restrict__ dy, const T* __restrict__ w,
+                                              const S2DataArgs& a, int c, long long n, int cell_a,
+                                              int b0, int b1) {
+    using P = Pair64;
+    using V = P::V;
+    constexpr int KR = (F - R + 1) / 2, KQ = (F - Q + 1) / 2;
+    V tp[KR][KQ];
+#pragma unroll
+    for (int k = 0; k < KR; ++k)
+#pragma unroll
+        for (int j = 0; j < KQ; ++j) tp[k][j] = P::load(w + ((R + 2 * k) * F + Q + 2 * j) * a.C + c);
+    const T* yrow[KR];
+    bool yok[KR];
+#pragma unroll
+    for (int k = 0; k < KR; ++k) {
+        const int oh = cell_a - k;
+        yok[k] = oh >= 0 && oh < a.OH;
+        yrow[k] = dy + ((n * a.OH + (yok[k] ? oh : 0)) * a.OW) * a.C + c;
+    }
+    auto load_col = [&](int ow, int k) -> V {
+        return (yok[k] && ow >= 0 && ow < a.OW) ? P::load(yrow[k] + static_cast<size_t>(ow) * a.C)
+                                                : P::zero();
+    };
+    // circular window: dy column b sits in slot (b - b0) mod KQ
+    V win[KR][KQ];
+#pragma unroll
+    for (int j = 1; j < KQ; ++j)
+#pragma unroll
+        for (int k = 0; k < KR; ++k) win[k][KQ - j] = load_col(b0 - j, k);
+    const int ih = 2 * cell_a - a.pad + R;
+    const bool row_ok = ih >= 0 && ih < a.H;
+    OutT* xrow = static_cast<OutT*>(a.dx) + ((n * a.H + (row_ok ? ih : 0)) * a.W) * a.C + c;
+#pragma unroll 1
+    for (int bb = b0; bb < b1; bb += KQ) {
+#pragma unroll
+        for (int u = 0; u < KQ; ++u) {
+            const int b = bb + u;
+            if (b >= b1) break;
+#pragma unroll
+            for (int k = 0; k < KR; ++k) win[k][u] = load_col(b, k);
+            V acc0 = P::zero(), acc1 = P::zero();
+#pragma unroll
+            for (int k = 0; k < KR; ++k)
+#pragma unroll
+                for (int j = 0; j < KQ; ++j) {
+                    if (k & 1) P::fma(acc1, win[k][(u - j + KQ) % KQ], tp[k][j]);
+                    else P::fma(acc0, win[k][(u - j + KQ) % KQ], tp[k][j]);
+                }
+            const int iw = 2 * b - a.pad + Q;
+            if (row_ok && iw >= 0 && iw < a.W) {
+                const float2 s0 = P::unpack(acc0), s1 = P::unpack(acc1);
+                store_out_pair(xrow + static_cast<size_t>(iw) * a.C, make_float2(s0.x + s1.x, s0.y + s1.y));
+            }
+        }
+    }
+}
+
+template <typename T, int F, class OutT = float>
+__global__ void __launch_bounds__(128)
+s2_bwd_data_class_kernel(const T* __restrict__ dy, const T* __restrict__ w, const S2DataArgs a) {
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int cp = static_cast<int>(tid % a.ncp);
+    long long rest = tid / a.ncp;
+    const int st = static_cast<int>(rest % a.nstrips);
+    rest /= a.nstrips;
+    const int ai = static_cast<int>(rest % a.na);
+    const long long n = rest / a.na;
+    if (n >= a.N) return;
+    const int cell_a = a.a_lo + ai;
+    const int b0 = a.b_lo + st * a.strip;
+    const int b1 = min(b0 + a.strip, a.b_lo + a.nb);
+    switch (blockIdx.y) {
+        case 0: s2_data_class<T, F, 0, 0, OutT>(dy, w, a, 2 * cp, n, cell_a, b0, b1); break;
+        case 1: s2_data_class<T, F, 0, 1, OutT>(dy, w, a, 2 * cp, n, cell_a, b0, b1); break;
+        case 2: s2_data_class<T, F, 1, 0, OutT>(dy, w, a, 2 * cp, n, cell_a, b0, b1); break;
+        default: s2_data_class<T, F, 1, 1, OutT>(dy, w, a, 2 * cp, n, cell_a, b0, b1); break;
+    }
+}
+
 template <typename T, int F, class OutT = float>
 cudaError_t launch_s2_bwd_data_inst(const GeneralConv& p) {
     S2DataArgs a;
@@ -213,16 +297,20 @@ cudaError_t launch_s2_bwd_data_inst(const GeneralConv& p) {
     a.na = ((p.H - 1 + p.pad) >> 1) - a.a_lo + 1;
     a.b_lo = p.pad >> 1;
     a.nb = ((p.W - 1 + p.pad) >> 1) - a.b_lo + 1;
-    // whole-strip kernel: S cells per strip; streamed 7x7 kernel: about eight cells, a
-    // multiple of its window period K
+    // whole-strip kernel: S cells per strip; streamed kernels (7 taps and up): about eight
+    // cells, a multiple of the window period K (of the class's KQ = K or K - 1 ... close
+    // enough: the strip only bounds the cells of a thread)
     constexpr int K = (F + 1) / 2;
-    a.strip = F == 7 ? (8 + K - 1) / K * K : S2DataTile<F>::S;
+    a.strip = F >= 7 ? (8 + K - 1) / K * K : S2DataTile<F>::S;
     a.nstrips = (a.nb + a.strip - 1) / a.strip;
     const long long threads = static_cast<long long>(p.N) * a.na * a.nstrips * a.ncp;
     if (threads == 0) return cudaSuccess;
     const long long blocks = (threads + 127) / 128;
     if (blocks > 0x7fffffffLL) return cudaErrorNotSupported;
-    if constexpr (F == 7)
+    if constexpr (F > 7)
+        s2_bwd_data_class_kernel<T, F, OutT><<<dim3(static_cast<unsigned>(blocks), 4), 128, 0, p.stream>>>(
+            static_cast<const T*>(p.a), static_cast<const T*>(p.b), a);
+    else if constexpr (F == 7)
         s2_bwd_data_stream_kernel<T, F, OutT><<<static_cast<unsigned>(blocks), 128, 0, p.stream>>>(
             static_cast<const T*>(p.a), static_cast<const T*>(p.b), a);
     else
@@ -238,6 +326,9 @@ cudaError_t launch_s2_bwd_data_dispatch(const GeneralConv& p) {
         case 3: return launch_s2_bwd_data_inst<T, 3, OutT>(p);
         case 5: return launch_s2_bwd_data_inst<T, 5, OutT>(p);
         case 7: return launch_s2_bwd_data_inst<T, 7, OutT>(p);
+        case 9: return launch_s2_bwd_data_inst<T, 9, OutT>(p);
+        case 11: return launch_s2_bwd_data_inst<T, 11, OutT>(p);
+        case 13: return launch_s2_bwd_data_inst<T, 13, OutT>(p);
         default: return cudaErrorNotSupported;
     }
 }

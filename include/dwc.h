@@ -43,7 +43,7 @@
  * 16-byte aligned and either
  *   - stride == 1 with a square filter of odd size 3..51, or a stripe (non-square) filter
  *     of odd width 1..51 and any height 1..255, or
- *   - stride == 2 with a square 3x3, 5x5 or 7x7 filter;
+ *   - stride == 2 with a square odd filter of 3 to 13 taps;
  * everything else (strides above 2, even widths, ...) runs on the general kernels (same
  * results, slower).
  */

@@ -135,7 +135,7 @@ STRIDE2 = [
     C_(1, 5, 5, 16, 7, s=2, p=3),     # map smaller than the filter
     C_(2, 21, 27, 144, 3, s=2),       # channel tails on lane groups (16 and 40 channels)
     C_(1, 20, 33, 40, 5, s=2),
-    # 9 to 13 taps: forward and filter gradient on the fast kernels, backward data general
+    # 9 to 13 taps (backward data on the per-pixel-class kernel)
     C_(2, 30, 34, 64, 9, s=2),
     C_(1, 25, 41, 128, 11, s=2),
     C_(2, 28, 28, 64, 13, s=2),
@@ -153,7 +153,7 @@ def test_stride2_fast_path(case, dtype):
     code = {"f32": 0, "bf16": 1, "f16": 2}[dtype]
     args = (case.N, case.H, case.W, case.C, case.FH, case.FW, case.stride, case.pad, code)
     assert dwc.path("fwd", None, None, None, *args) == 1
-    assert dwc.path("bwd_data", None, None, None, *args) == (1 if case.FH <= 7 else 0)
+    assert dwc.path("bwd_data", None, None, None, *args) == 1
     assert dwc.path("bwd_filter", None, None, None, *args) == 1
     check_full(case)
 
