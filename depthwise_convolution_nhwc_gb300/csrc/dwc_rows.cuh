@@ -555,23 +555,23 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     return cudaGetLastError();
 }
 
-// Channel counts that are not a multiple of 64 (3x3, 5x5, 7x7, fp32 outputs): the tail of at
-// most 32 channels runs with 2 or 4 lane groups, so that it does not leave half the lanes
-// idle; below 64 channels that is the only launch, above it a second one after the launch
-// over the channels below the last multiple of 64.
-template <typename T, int F, int G>
+// Channel counts that are not a multiple of 64 (3x3, 5x5, 7x7, fp32 or 16-bit outputs): the
+// tail of at most 32 channels runs with 2 or 4 lane groups, so that it does not leave half the
+// lanes idle; below 64 channels that is the only launch, above it a second one after the
+// launch over the channels below the last multiple of 64.
+template <typename T, int F, int G, class OutT>
 cudaError_t launch_rows_tail(const RowConv& p) {
     using Tl = RowsTile<F, F>;
     RowConv t = p;
     t.c_lo = p.C / kBN * kBN;
-    return p.flip ? launch_rows_inst<T, F, F, Tl::R, Tl::TM, Tl::MINB, true, Pair64, 1, -1, float, G>(t)
-                  : launch_rows_inst<T, F, F, Tl::R, Tl::TM, Tl::MINB, false, Pair64, 1, -1, float, G>(t);
+    return p.flip ? launch_rows_inst<T, F, F, Tl::R, Tl::TM, Tl::MINB, true, Pair64, 1, -1, OutT, G>(t)
+                  : launch_rows_inst<T, F, F, Tl::R, Tl::TM, Tl::MINB, false, Pair64, 1, -1, OutT, G>(t);
 }
 
 template <typename T, int F, class OutT>
 cudaError_t launch_rows_square(const RowConv& p) {
     using Tl = RowsTile<F, F>;
-    if constexpr (F <= 7 && std::is_same<OutT, float>::value) {
+    if constexpr (F <= 7) {
         // C > 64: a second, serialised launch for the tail pays only where the kernel is
         // near its compute bound (7x7); the HBM-bound 3x3 / 5x5 hide the idle lanes (3x3 at
         // stride 2 on 64x112x112x96 measured 71 us in one launch, 92 us split)
@@ -583,7 +583,7 @@ cudaError_t launch_rows_square(const RowConv& p) {
                 const cudaError_t err = launch_rows_square<T, F, OutT>(q);
                 if (err != cudaSuccess) return err;
             }
-            return rem <= 16 ? launch_rows_tail<T, F, 4>(p) : launch_rows_tail<T, F, 2>(p);
+            return rem <= 16 ? launch_rows_tail<T, F, 4, OutT>(p) : launch_rows_tail<T, F, 2, OutT>(p);
         }
     }
     return p.flip ? launch_rows_inst<T, F, F, Tl::R, Tl::TM, Tl::MINB, true, Pair64, 1, -1, OutT>(p)
@@ -633,7 +633,7 @@ cudaError_t launch_rows_dispatch(const RowConv& p) {
 // the down-sampling layers of mobile networks, 3 to 7, and of large-kernel networks).
 template <typename T, int F, class OutT>
 cudaError_t launch_rows_s2_square(const RowConv& p) {
-    if constexpr (std::is_same<OutT, float>::value) {
+    if constexpr (F <= 7) {
         // a tail of at most 32 channels past the last multiple of 64: lane groups, under the
         // rule of the stride-1 launch above
         const int rem = p.C % kBN;
@@ -641,13 +641,13 @@ cudaError_t launch_rows_s2_square(const RowConv& p) {
             if (p.C > kBN) {
                 RowConv q = p;
                 q.c_hi = p.C / kBN * kBN;
-                const cudaError_t err = launch_rows_inst<T, F, F, 1, 8, 3, false, Pair64, 2, -1, float>(q);
+                const cudaError_t err = launch_rows_inst<T, F, F, 1, 8, 3, false, Pair64, 2, -1, OutT>(q);
                 if (err != cudaSuccess) return err;
             }
             RowConv t = p;
             t.c_lo = p.C / kBN * kBN;
-            return rem <= 16 ? launch_rows_inst<T, F, F, 1, 8, 3, false, Pair64, 2, -1, float, 4>(t)
-                             : launch_rows_inst<T, F, F, 1, 8, 3, false, Pair64, 2, -1, float, 2>(t);
+            return rem <= 16 ? launch_rows_inst<T, F, F, 1, 8, 3, false, Pair64, 2, -1, OutT, 4>(t)
+                             : launch_rows_inst<T, F, F, 1, 8, 3, false, Pair64, 2, -1, OutT, 2>(t);
         }
     }
     return launch_rows_inst<T, F, F, 1, 8, 3, false, Pair64, 2, -1, OutT>(p);

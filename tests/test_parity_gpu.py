@@ -409,6 +409,14 @@ OUT16 = [
     C_(2, 17, 19, 64, 3, s=2),      # stride-2 kernels
     C_(1, 23, 37, 128, 7, s=2),
     C_(1, 10, 10, 16, 5, s=3, p=2), # general kernels
+    # channel tails on lane groups (16-bit outputs too): C below and above 64
+    C_(2, 15, 21, 40, 7),
+    C_(1, 19, 23, 88, 7),
+    C_(2, 16, 17, 24, 3),
+    C_(1, 21, 27, 144, 7, s=2),
+    C_(2, 20, 22, 48, 5, s=2),
+    # stride 2 with 9 to 13 taps
+    C_(1, 25, 29, 64, 11, s=2),
 ]
 
 
