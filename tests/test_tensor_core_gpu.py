@@ -156,3 +156,33 @@ def test_family_preference_rejects_unknown_families(lib):
     assert lib.dwc_testing_prefer_family(7) == -1
     assert lib.dwc_testing_prefer_family(3) == -1
     assert lib.dwc_testing_prefer_family(0) == 0
+
+
+def test_tcgen05_call_inside_a_cuda_graph(lib):
+    """The tcgen05 path takes stream-ordered scratch (the stacked copy and the Toeplitz runs)
+    during the call: captured into a CUDA graph it must record that allocation and its free,
+    and every replay must give the eager call's result (here on fresh inputs each replay)."""
+    assert lib.dwc_testing_prefer_family(0) >= 0
+    case = Case(4, 40, 44, 64, 17, 17, 1, 8, "bf16", "normal", 61)
+    x, w = case.x().cuda(), case.w().cuda()
+    assert dwc.path("fwd", None, None, None, case.N, case.H, case.W, case.C, case.FH, case.FW,
+                    1, case.pad, CODE["bf16"]) == 2
+    xs = torch.empty_like(x)
+    xs.copy_(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dwc.fwd(xs, w, 1, case.pad)          # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        yg = dwc.fwd(xs, w, 1, case.pad)
+    for seed in (62, 63):
+        other = Case(**{**case.__dict__, "seed": seed})
+        xn = other.x().cuda()
+        xs.copy_(xn)
+        g.replay()
+        torch.cuda.synchronize()
+        assert dwc.device_status() == 0
+        assert torch.equal(yg, dwc.fwd(xn, w, 1, case.pad))
