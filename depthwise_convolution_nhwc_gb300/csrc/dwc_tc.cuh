@@ -36,12 +36,13 @@
 // shared-memory pipes that the MMA issuers and their barriers also go through.
 //
 // Warp roles per CTA (one CTA per SM, persistent over units of (row tile, column tile, group
-// of CG = 4 or 8 channels)):
+// of CG = 2, 4 or 8 channels)):
 //  * 4 epilogue warps -- warp w reads the 32-lane quadrant w of the accumulators
 //    (tcgen05.ld) and writes the CG channels of a pixel with 16-byte stores;
-//  * 4 MMA warps: one lane each issues the MMAs of every fourth channel of the group (a
-//    single thread issues an MMA only every ~100 cycles, an M=128 N=32 MMA takes 46); the
-//    first also allocates the tensor memory;
+//  * 4 MMA warps: one lane each issues the MMAs of every fourth channel of the group, or,
+//    in groups of 2 channels, of one channel's even or odd filter rows into a partial sum of
+//    its own (a single thread issues an MMA only every ~100 cycles, an M=128 N=64 MMA takes
+//    48); the first also allocates the tensor memory;
 //  * 4 run feeders: one lane each copies, in order, the runs of its issuer's items into
 //    that issuer's ring;
 //  * 1 plane feeder: one lane loads the units' planes into the plane ring.
@@ -61,7 +62,8 @@ constexpr int kTcM = 128;           // MMA rows (tensor-memory lanes)
 // Roles (13 warps; warp w runs on sub-partition w % 4):
 //   0-3   epilogue, warp w reading the 32-lane quadrant w of tensor memory
 //   4-7   MMA issuers, one lane each: issuer i takes the channels c with c % 4 == i, every
-//         filter row of them; warp 4 also allocates the tensor memory
+//         filter row of them (groups of 2 channels: channel i / 2, the filter rows of
+//         parity i % 2); warp 4 also allocates the tensor memory
 //   8-11  run feeders, feeder i filling issuer i's ring
 //   12    plane feeder
 constexpr int kTcEpiWarps = 4;
@@ -260,7 +262,9 @@ __device__ __forceinline__ void tc_unit(const TcArgs& a, uint32_t u, int& t, int
 // 8- or 16-byte store of values rounded to nearest even (bf16, fp16).
 template <class OutT, int CG>
 __device__ __forceinline__ void tc_store_pixel(OutT* dst, const float (&v)[CG]) {
-    if constexpr (std::is_same<OutT, float>::value) {
+    if constexpr (std::is_same<OutT, float>::value && CG == 2) {
+        __stcs(reinterpret_cast<float2*>(dst), make_float2(v[0], v[1]));
+    } else if constexpr (std::is_same<OutT, float>::value) {
 #pragma unroll
         for (int c = 0; c < CG; c += 4)
             __stcs(reinterpret_cast<float4*>(dst + c), make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]));
@@ -276,7 +280,9 @@ __device__ __forceinline__ void tc_store_pixel(OutT* dst, const float (&v)[CG]) 
                 h[c / 2] = *reinterpret_cast<const uint32_t*>(&b);
             }
         }
-        if constexpr (CG == 4) {
+        if constexpr (CG == 2) {
+            __stcs(reinterpret_cast<uint32_t*>(dst), h[0]);
+        } else if constexpr (CG == 4) {
             __stcs(reinterpret_cast<uint2*>(dst), make_uint2(h[0], h[1]));
         } else {
             __stcs(reinterpret_cast<uint4*>(dst), make_uint4(h[0], h[1], h[2], h[3]));
@@ -405,7 +411,11 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const TcPrepArg
 template <typename T, class OutT, int CG>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
-    static_assert(CG % kTcIssuers == 0, "every issuer takes whole channels of the group");
+    // issuers per channel: 1 (each issuer owns whole channels), or 2 in groups of 2 channels
+    // (filter-row parities into two partial sums, one filter row per ring item)
+    constexpr int PART = CG >= kTcIssuers ? 1 : kTcIssuers / CG;
+    static_assert(CG * PART % kTcIssuers == 0 && PART <= 2, "issuers divide the group's channels");
+    constexpr int CH_STEP = kTcIssuers / PART;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* planes = smem;
     unsigned char* toep = smem + a.off_toep;
@@ -425,7 +435,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.ps; ++s) {
             mbar_init(&plane_full[s], 1);    // the plane feeder (plus the copies' bytes)
-            mbar_init(&plane_empty[s], 1);   // the issuer of its channel
+            mbar_init(&plane_empty[s], PART);   // the issuers of its channel
         }
         for (int s = 0; s < kTcMaxToep; ++s) {
             mbar_init(&toep_full[s], 1);
@@ -453,8 +463,10 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
 
     if (warp >= kTcMmaWarp && warp < kTcMmaWarp + kTcIssuers) {
         // ------------------------------------------------------------- MMA issue
-        // Issuer `is` takes the channels c of the group with c % 4 == is, all filter rows.
+        // Issuer `is` takes the channels c of the group with c % 4 == is, all filter rows; or
+        // (PART 2) channel is / 2, the filter rows of parity is % 2.
         const int is = warp - kTcMmaWarp;
+        const int par = is % PART;
         if (lane == 0) {
             uint32_t db = 0, dphase = 0;
             bool ok = true;
@@ -477,7 +489,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
                 if (!tc_wait(&d_empty[db], dphase ^ 1u, a, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t dcol = tmem + db * kTcDCols;
-                for (int ch = is; ch < CG && ok; ch += kTcIssuers) {
+                for (int ch = is / PART; ch < CG && ok; ch += CH_STEP) {
                     // channel ch of this unit sits at plane-ring position pos0 + ch (the
                     // plane feeder fills the ring in order; this issuer skips the others)
                     const uint32_t pos = pos0 + static_cast<uint32_t>(ch);
@@ -485,9 +497,10 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
                     if (!tc_wait(&plane_full[pslot], pphase, a, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ap = adesc0 + pslot * a_slot;
-                    const uint32_t dch = dcol + static_cast<uint32_t>(ch * a.NN);
-                    // item: filter rows fh0 .. fh0 + rps - 1 (fewer at the end)
-                    for (int fh0 = 0; fh0 < a.FH; fh0 += a.rps, ++item) {
+                    const uint32_t dch = dcol + static_cast<uint32_t>((par * CG + ch) * a.NN);
+                    // item: filter rows fh0 .. fh0 + rps - 1 (fewer at the end), or (PART 2)
+                    // filter row fh0 of this issuer's parity
+                    for (int fh0 = par; fh0 < a.FH; fh0 += PART * a.rps, ++item) {
                         const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
                         const uint32_t phase = (item / kTcRingSlots) & 1u;
                         if (!tc_wait(&toep_full[slot], phase, a, abort_flag)) { ok = false; break; }
@@ -496,7 +509,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
                         for (int rr = 0; rr < nr; ++rr) {
                             uint64_t ad = ap + static_cast<uint32_t>(fh0 + rr);
                             uint64_t bd = bdesc0 + slot * b_slot + rr * b_run;
-                            tc_mma(dch, ad, bd, idesc, (fh0 + rr) != 0 ? 1u : 0u);
+                            tc_mma(dch, ad, bd, idesc, (fh0 + rr) != par ? 1u : 0u);
                             for (int ks = 1; ks < a.KS; ++ks) {
                                 ad += a_ks;
                                 bd += 16u;
@@ -541,12 +554,14 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
                          (static_cast<size_t>(row_ok ? n : 0) * a.OH + (row_ok ? r : 0)) *
                              static_cast<size_t>(a.OW) * a.C + c0;
             const uint32_t dcol = tmem + db * kTcDCols + (static_cast<uint32_t>(quad * 32) << 16);
-            // columns per round: CG x CW sums in registers (32 values)
-            constexpr int CW = 32 / CG;
+            // columns per round: CG x CW sums (of PART partials each) in registers (32 values)
+            constexpr int CW = 32 / (CG * PART);
             for (int cc = 0; cc < a.NN; cc += CW) {
-                uint32_t acc[CG][CW];
+                uint32_t acc[PART][CG][CW];
 #pragma unroll
-                for (int ch = 0; ch < CG; ++ch) tc_ld(dcol + ch * a.NN + cc, acc[ch]);
+                for (int pp = 0; pp < PART; ++pp)
+#pragma unroll
+                    for (int ch = 0; ch < CG; ++ch) tc_ld(dcol + (pp * CG + ch) * a.NN + cc, acc[pp][ch]);
                 tc_wait_ld();
                 if (row_ok) {
 #pragma unroll
@@ -555,7 +570,10 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
                         if (ow < ow0 || ow >= ow_end) continue;
                         float vals[CG];
 #pragma unroll
-                        for (int ch = 0; ch < CG; ++ch) vals[ch] = __uint_as_float(acc[ch][q]);
+                        for (int ch = 0; ch < CG; ++ch) {
+                            vals[ch] = __uint_as_float(acc[0][ch][q]);
+                            if constexpr (PART == 2) vals[ch] += __uint_as_float(acc[1][ch][q]);
+                        }
                         tc_store_pixel<OutT, CG>(orow + static_cast<size_t>(ow) * a.C, vals);
                     }
                 }
@@ -572,6 +590,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
         // channels, rps filter rows at a time (the runs of one channel are consecutive in
         // the run table, so an item is one bulk copy).
         const int fi = warp - kTcFeed0;
+        const int fpar = fi % PART;
         if (lane == 0) {
             const uint32_t ring0 = static_cast<uint32_t>(fi) * kTcRingSlots;
             const uint32_t slot_bytes = static_cast<uint32_t>(a.rps) * a.toep_bytes;
@@ -580,10 +599,10 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
             for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
                 int t, j, g;
                 tc_unit(a, u, t, j, g);
-                for (int ch = fi; ch < CG && ok; ch += kTcIssuers) {
+                for (int ch = fi / PART; ch < CG && ok; ch += CH_STEP) {
                     const unsigned char* src =
                         a.runs + static_cast<size_t>(g * CG + ch) * a.FH * a.toep_bytes;
-                    for (int fh0 = 0; fh0 < a.FH; fh0 += a.rps, ++item) {
+                    for (int fh0 = fpar; fh0 < a.FH; fh0 += PART * a.rps, ++item) {
                         const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
                         const uint32_t phase = (item / kTcRingSlots) & 1u;
                         if (!tc_wait(&toep_empty[slot], phase ^ 1u, a, abort_flag)) { ok = false; break; }
@@ -646,9 +665,12 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
 inline double tc_mma_cycles(int n) {
     return std::max({46.0, (kTcM + n) / 4.0, n / 2.0});
 }
-// An issuing thread's cycles per ring item (wait, fences, commit) and per MMA it issues.
+// An issuing thread's cycles per ring item (wait, fences, commit) and per MMA it issues,
+// fitted to the kernel's measured unit times (bf16 32x56x56x128 31x31, N = 64: items of 6 and
+// 12 MMAs took ~1600 and ~2700 cycles): four issuers together then issue an MMA about every
+// 46 cycles, as fast as the tensor core runs the N = 64 MMAs.
 constexpr double kTcItemIssueCycles = 500.0;
-constexpr double kTcMmaIssueCycles = 110.0;
+constexpr double kTcMmaIssueCycles = 183.0;
 
 struct TcPlan {
     TcArgs a;
@@ -684,10 +706,12 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     // units only) the longer of the tensor core's MMA time and an issuer's time (a fixed cost
     // per ring item and per MMA), plus, where shared memory cannot hold the planes of two
     // units (the next unit's planes then wait for the end of the current one), the planes'
-    // copy time at 64 bytes per cycle.  Column tiles own a multiple of 8 columns (every
-    // tile's first plane starts on an 8-column boundary of the stacked copy).  Constraints:
-    // two accumulator buffers of CG x NN columns in tensor memory, the planes and the run
-    // rings in shared memory.
+    // copy time at 64 bytes per cycle.  Groups of 2 channels (two issuers per channel, two
+    // partial sums) make units half as large, which evens out the last wave of units over
+    // the SMs.  Column tiles own a multiple of 8 columns (every tile's first plane starts on
+    // an 8-column boundary of the stacked copy).  Constraints: two accumulator buffers of
+    // partials x CG x NN columns in tensor memory, the planes and the run rings in shared
+    // memory.
     const int cap = device_info().max_smem_optin;
     const int sms = device_info().sm_count;
     double best = 1e30;
@@ -702,18 +726,23 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
         const size_t plane = static_cast<size_t>(2 * ks) * a.MR * 16;
         const long long tiles = row_tiles * ((p.OW + twc - 1) / twc);
         for (int rps = kTcRunsPerSlot; rps >= 1; --rps)
-        for (int cg = 8; cg >= 4; cg /= 2) {
-            if (cg * nn > kTcDCols || p.C % cg != 0) continue;
+        for (int cg = 8; cg >= 2; cg /= 2) {
+            const int part = cg >= kTcIssuers ? 1 : kTcIssuers / cg;   // partial sums
+            if (part * cg * nn > kTcDCols || p.C % cg != 0 || (part > 1 && rps > 1)) continue;
             const size_t fixed = static_cast<size_t>(kTcMaxToep) * rps * ncm * 128 + kTcBarBytes;
             if (fixed >= static_cast<size_t>(cap)) continue;
             const int ps = static_cast<int>(std::min<size_t>(kTcMaxPlanes, (cap - fixed) / plane));
             if (ps < cg + 1) continue;   // the next unit's planes must fill while one computes
             const long long units = tiles * (p.C / cg);
             const double tensor = cg * p.FH * ks * tc_mma_cycles(nn);
-            const double issue = (cg / kTcIssuers) * ((p.FH + rps - 1) / rps) *
+            const int rows_per_issuer = (p.FH + part - 1) / part;
+            const double issue = (cg * part / kTcIssuers) * ((rows_per_issuer + rps - 1) / rps) *
                                  (kTcItemIssueCycles + rps * ks * kTcMmaIssueCycles);
-            const double unit = std::max(tensor, issue) +
-                                (ps >= 2 * cg ? 0.0 : static_cast<double>(cg) * plane / 64.0);
+            // (two partial sums cost the epilogue a second read of the accumulators and the
+            // stores carry half as many channels: measured ~10 % per unit)
+            const double unit = (std::max(tensor, issue) +
+                                 (ps >= 2 * cg ? 0.0 : static_cast<double>(cg) * plane / 64.0)) *
+                                (part > 1 ? 1.1 : 1.0);
             const double cost = static_cast<double>((units + sms - 1) / sms) * unit;
             if (cost < best) {
                 best = cost; best_nt = nt; best_cg = cg; best_ps = ps; best_rps = rps; best_twc = twc;
@@ -839,6 +868,7 @@ cudaError_t launch_tc_rows(const RowConv& p) {
     if (!tc_plan(p, P)) return cudaErrorNotSupported;
     if (P.a.units == 0) return cudaSuccess;
     switch (P.cg) {
+        case 2: return launch_tc_inst<T, OutT, 2>(P, p);
         case 4: return launch_tc_inst<T, OutT, 4>(P, p);
         case 8: return launch_tc_inst<T, OutT, 8>(P, p);
         default: return cudaErrorNotSupported;
