@@ -47,12 +47,11 @@ KERNEL_NAMES = {
 }
 
 
-def launches(pass_name, family):
-    """Launches of this library's kernels in one call of the pass (a filter gradient adds its
-    slice sum; the tcgen05 forward / backward data its preparation kernel)."""
-    if pass_name == "bwd_filter":
-        return 2
-    return 2 if family == 2 else 1
+def launches(dwc, case, pass_name):
+    """Launches of this library's kernels in one call of the pass, as the library counts them
+    (a filter gradient adds its slice sum; the tcgen05 path its preparation kernel)."""
+    return dwc.kernel_launches(pass_name, case.N, case.H, case.W, case.C, case.FH, case.FW,
+                               case.stride, case.pad, DTYPE_CODE[case.dtype])
 
 
 def kernel_name(case, pass_name, family):
@@ -841,7 +840,7 @@ def run_ours(args, case, passes):
                      "link": link}
                     if e2e_value is not None else None),
             "alu_peaks": alu,
-            "gpu_launches": args.steps * sum(launches(n, fam[n]) for n in passes),
+            "gpu_launches": args.steps * sum(launches(dwc, case, n) for n in passes),
             "kernels": {n: kernel_name(case, n, fam[n]) for n in passes},
             "clocks": clocks}
     if not args.no_per_filter and world == 1:

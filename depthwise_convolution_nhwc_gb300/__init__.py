@@ -34,8 +34,8 @@ STATUS = {0: "DWC_OK", 1: "DWC_ERR_INVALID_ARG", 2: "DWC_ERR_UNSUPPORTED",
 EXPORTS = ("dwc_fwd", "dwc_fwd_ex", "dwc_fwd_bn_act", "dwc_bwd_data", "dwc_bwd_data_ex",
            "dwc_bwd_filter_workspace_size", "dwc_bwd_filter", "dwc_bwd_filter_noalloc",
            "dwc_device_status", "dwc_set_wait_limit_ns", "dwc_fma_rate_probe",
-           "dwc_status_string", "dwc_version", "dwc_path", "dwc_testing_stall_next_row_launch",
-           "dwc_testing_prefer_family")
+           "dwc_status_string", "dwc_version", "dwc_path", "dwc_kernel_launches",
+           "dwc_testing_stall_next_row_launch", "dwc_testing_prefer_family")
 FMA_KINDS = {"ffma": 0, "ffma2": 1, "hfma2": 2, "bf16x2": 3}  # dwc_fma_rate_probe kinds
 
 _lock = threading.Lock()
@@ -92,6 +92,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.dwc_version.restype = i
         lib.dwc_path.argtypes = [i, vp, vp, vp] + shape + [i]
         lib.dwc_path.restype = i
+        lib.dwc_kernel_launches.argtypes = [i] + shape + [i]
+        lib.dwc_kernel_launches.restype = i
         lib.dwc_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         lib.dwc_set_wait_limit_ns.restype = ctypes.c_ulonglong
         lib.dwc_fma_rate_probe.argtypes = [i, i, i, vp, vp]
@@ -284,6 +286,13 @@ def path(pass_: str, a, b, out, N, H, W, C, FH, FW, stride, pad, dtype_code) -> 
                                        dtype_code))
 
 
+def kernel_launches(pass_: str, N, H, W, C, FH, FW, stride, pad, dtype_code) -> int:
+    """Kernel launches of this library that a call makes (aligned tensors), -1 invalid."""
+    p = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2, "fwd_bn_act": 3}[pass_]
+    return int(load_library().dwc_kernel_launches(p, N, H, W, C, FH, FW, stride, pad, dtype_code))
+
+
 __all__ = ["build", "load_library", "fwd", "fwd_bn_act", "bwd_data", "bwd_filter",
            "bwd_filter_workspace_size", "device_status", "set_wait_limit_ns", "fma_rate_probe",
-           "path", "status_string", "DwcError", "EXPORTS", "FMA_KINDS", "LIB_PATH"]
+           "path", "kernel_launches", "status_string", "DwcError", "EXPORTS", "FMA_KINDS",
+           "LIB_PATH"]

@@ -592,4 +592,34 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
     return 1;
 }
 
+int dwc_kernel_launches(int pass, int N, int H, int W, int C, int FH, int FW, int stride, int pad,
+                        dwc_dtype_t dtype) {
+    const int fam = dwc_path(pass, nullptr, nullptr, nullptr, N, H, W, C, FH, FW, stride, pad, dtype);
+    if (fam < 0) return -1;
+    Problem P;
+    if (check_problem(N, H, W, C, FH, FW, stride, pad, dtype, P) != DWC_OK) return -1;
+    const long long out = pass == kPassBwdFilter ? static_cast<long long>(FH) * FW * C
+                        : pass == kPassBwdData ? static_cast<long long>(N) * H * W * C
+                                               : static_cast<long long>(N) * P.OH * P.OW * C;
+    if (out == 0) return 0;
+    // filter gradients: the kernel and the fixed-order sum of its slices (or a fill of dW
+    // with zeros when nothing meets it: a memset, not a kernel of this library)
+    if (pass == kPassBwdFilter) return N == 0 ? 0 : 2;
+    if (pass == 3) return 1;
+    if (fam == 2) {
+        const RowConv rc = pass == kPassFwd
+            ? RowConv{nullptr, nullptr, nullptr, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false,
+                      P.dtype, nullptr, nullptr}
+            : RowConv{nullptr, nullptr, nullptr, N, P.OH, P.OW, C, H, W, FH, FW, FH - 1 - pad,
+                      FW - 1 - pad, true, P.dtype, nullptr, nullptr};
+        return tc_rows_launches(rc);
+    }
+    // row kernel, 3 to 7 taps (square): a channel tail of at most 32 past a multiple of 64
+    // runs as a second launch on lane groups (7 taps)
+    const bool rows = fam == 1 && FH == FW && FH <= 7 && !(stride == 2 && pass == kPassBwdData);
+    const int rem = C % 64;
+    if (rows && C > 64 && rem != 0 && rem <= 32 && FH == 7) return 2;
+    return 1;
+}
+
 }  // extern "C"

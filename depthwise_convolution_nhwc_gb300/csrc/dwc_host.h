@@ -206,6 +206,9 @@ bool tc_rows_fits(const RowConv& p);
 inline bool tc_rows_wanted(const RowConv& p) {
     return (p.FW >= 9 && p.OW >= 28) || (p.FW >= 17 && p.OW >= 17);
 }
+// Kernel launches of a tcgen05 call: the preparation and the main kernel (0 when the shape
+// has no plan).
+int tc_rows_launches(const RowConv& p);
 // tc_rows_wanted and a launch plan exists.
 inline bool tc_rows_preferred(const RowConv& p) {
     return (p.dtype == kBF16 || p.dtype == kF16) && tc_rows_wanted(p) && tc_rows_fits(p);

@@ -100,7 +100,8 @@ struct TcArgs {
     int MR;             // staged rows per plane (>= FH + 127, multiple of 8, <= 256)
     int NCM;            // core matrices of one run: NN/8 + 2*KS - 1
     int x0;             // column of the stacked copy holding input column -pad_w (<= 0)
-    int ncg;            // channel groups (C / CG)
+    int cbase;          // first channel of the launch's groups
+    int ncg;            // channel groups of the launch
     int ps;             // plane ring slots
     int rps;            // filter rows per ring item (1 or kTcRunsPerSlot)
     uint32_t units, col_tiles;
@@ -549,7 +550,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
             const bool row_ok = v >= tl.v_lo && v < tl.v_hi && r < a.OH;
             const int ow0 = j * a.TWc;
             const int ow_end = min(a.OW, ow0 + a.TWc);
-            const int c0 = g * CG;
+            const int c0 = a.cbase + g * CG;
             OutT* orow = static_cast<OutT*>(a.out) +
                          (static_cast<size_t>(row_ok ? n : 0) * a.OH + (row_ok ? r : 0)) *
                              static_cast<size_t>(a.OW) * a.C + c0;
@@ -601,7 +602,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
                 tc_unit(a, u, t, j, g);
                 for (int ch = fi / PART; ch < CG && ok; ch += CH_STEP) {
                     const unsigned char* src =
-                        a.runs + static_cast<size_t>(g * CG + ch) * a.FH * a.toep_bytes;
+                        a.runs + static_cast<size_t>(a.cbase + g * CG + ch) * a.FH * a.toep_bytes;
                     for (int fh0 = fpar; fh0 < a.FH; fh0 += PART * a.rps, ++item) {
                         const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
                         const uint32_t phase = (item / kTcRingSlots) & 1u;
@@ -638,7 +639,7 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
                     unsigned char* dst = planes + static_cast<size_t>(slot) * a.plane_bytes;
                     for (int b = 0; b < kc; ++b)
                         tma_load_3d(dst + static_cast<size_t>(b) * a.MR * 16u, &xmap, &plane_full[slot],
-                                    xc + 8 * b, tl.v0, g * CG + ch);
+                                    xc + 8 * b, tl.v0, a.cbase + g * CG + ch);
                 }
             }
             tc_drain(plane_full, 0, ps, pos, a);
@@ -758,8 +759,10 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     a.plane_bytes = static_cast<uint32_t>(2 * a.KS) * a.MR * 16u;
     a.toep_bytes = static_cast<uint32_t>(a.NCM) * 128u;
     P.cg = best_cg;
+    a.cbase = 0;
     a.ncg = p.C / best_cg;
-    const long long units = row_tiles * a.col_tiles * a.ncg;
+    const long long tiles = row_tiles * a.col_tiles;
+    const long long units = tiles * a.ncg;
     if (units >= (1LL << 31)) return false;
     a.units = static_cast<uint32_t>(units);
     a.fd_S.init(static_cast<uint32_t>(a.S));
@@ -773,11 +776,11 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     P.Wp = (P.Lp + p.W + 7) / 8 * 8;
     P.planes_bytes = static_cast<size_t>(p.C) * static_cast<size_t>(p.N) * a.S * P.Wp * 2;
     P.runs_bytes = static_cast<size_t>(p.C) * p.FH * a.toep_bytes;
-    // shared memory: plane ring, run rings, barriers
+    // shared memory: plane ring, run rings, barriers; one CTA per SM (each allocates all of
+    // tensor memory): ask for more than half of it
     const size_t toep_ring = static_cast<size_t>(kTcMaxToep) * a.rps * a.toep_bytes;
     a.off_toep = static_cast<uint32_t>(static_cast<size_t>(a.ps) * a.plane_bytes);
     a.off_bar = a.off_toep + static_cast<uint32_t>(toep_ring);
-    // one CTA per SM (each allocates all of tensor memory): ask for more than half of it
     P.smem = std::max<size_t>(a.off_bar + kTcBarBytes, static_cast<size_t>(cap) / 2 + 1024);
     return true;
 }
@@ -789,9 +792,36 @@ inline uint32_t tc_idesc(int n) {
            (static_cast<uint32_t>(kTcM >> 4) << 24);
 }
 
+// One launch of the main kernel with groups of CG channels.
 template <typename T, class OutT, int CG>
-cudaError_t launch_tc_inst(const TcPlan& P, const RowConv& p) {
-    TcArgs a = P.a;
+cudaError_t launch_tc_main(const TcArgs& a, size_t smem, const CUtensorMap& xmap, cudaStream_t stream) {
+    auto kern = tc_rows_kernel<T, OutT, CG>;
+    static DeviceOnce smem_opt_in;
+    const cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
+    if (err != cudaSuccess) return err;
+    const unsigned grid = static_cast<unsigned>(
+        std::min<long long>(a.units, static_cast<long long>(device_info().sm_count)));
+    kern<<<grid, kTcThreads, smem, stream>>>(xmap, a);
+    return cudaGetLastError();
+}
+
+template <typename T, class OutT>
+cudaError_t launch_tc_main_cg(int cg, const TcArgs& a, size_t smem, const CUtensorMap& xmap,
+                              cudaStream_t stream) {
+    switch (cg) {
+        case 2: return launch_tc_main<T, OutT, 2>(a, smem, xmap, stream);
+        case 4: return launch_tc_main<T, OutT, 4>(a, smem, xmap, stream);
+        case 8: return launch_tc_main<T, OutT, 8>(a, smem, xmap, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+template <typename T, class OutT = float>
+cudaError_t launch_tc_rows(const RowConv& p) {
+    TcPlan P;
+    if (!tc_plan(p, P)) return cudaErrorNotSupported;
+    if (P.a.units == 0) return cudaSuccess;
+    const TcArgs& a = P.a;
     // scratch of this call: the stacked copy, then the run table (128-byte aligned)
     const size_t runs_off = (P.planes_bytes + 127) / 128 * 128;
     void* scratch = nullptr;
@@ -841,38 +871,17 @@ cudaError_t launch_tc_inst(const TcPlan& P, const RowConv& p) {
     if (p.flip) tc_prep_kernel<T, true><<<prep_grid, kTcPrepThreads, 0, p.stream>>>(q);
     else tc_prep_kernel<T, false><<<prep_grid, kTcPrepThreads, 0, p.stream>>>(q);
     cudaError_t err = cudaGetLastError();
-    if (err == cudaSuccess) {
-        a.runs = base + runs_off;
-        a.out = p.out;
-        a.status = p.status;
-        a.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
-        a.idesc = tc_idesc<T>(a.NN);
-        auto kern = tc_rows_kernel<T, OutT, CG>;
-        static DeviceOnce smem_opt_in;
-        err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
-        if (err == cudaSuccess) {
-            const unsigned grid = static_cast<unsigned>(
-                std::min<long long>(a.units, static_cast<long long>(sms)));
-            kern<<<grid, kTcThreads, P.smem, p.stream>>>(xmap, a);
-            err = cudaGetLastError();
-        }
-    }
-    // stream-ordered: the memory returns to the pool once both kernels have run
+    // the main kernel
+    TcArgs m = a;
+    m.runs = base + runs_off;
+    m.out = p.out;
+    m.status = p.status;
+    m.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
+    m.idesc = tc_idesc<T>(a.NN);
+    if (err == cudaSuccess) err = launch_tc_main_cg<T, OutT>(P.cg, m, P.smem, xmap, p.stream);
+    // stream-ordered: the memory returns to the pool once the kernels have run
     scratch_free(scratch, p.stream);
     return err;
-}
-
-template <typename T, class OutT = float>
-cudaError_t launch_tc_rows(const RowConv& p) {
-    TcPlan P;
-    if (!tc_plan(p, P)) return cudaErrorNotSupported;
-    if (P.a.units == 0) return cudaSuccess;
-    switch (P.cg) {
-        case 2: return launch_tc_inst<T, OutT, 2>(P, p);
-        case 4: return launch_tc_inst<T, OutT, 4>(P, p);
-        case 8: return launch_tc_inst<T, OutT, 8>(P, p);
-        default: return cudaErrorNotSupported;
-    }
 }
 
 }  // namespace dwc

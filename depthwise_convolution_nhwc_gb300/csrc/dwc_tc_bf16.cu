@@ -11,4 +11,9 @@ bool tc_rows_fits(const RowConv& p) {
     TcPlan P;
     return tc_plan(p, P);
 }
+int tc_rows_launches(const RowConv& p) {
+    TcPlan P;
+    if (!tc_plan(p, P) || P.a.units == 0) return 0;
+    return 2;
+}
 }  // namespace dwc

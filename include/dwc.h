@@ -230,6 +230,13 @@ int dwc_version(void);
 int dwc_path(int pass, const void* a, const void* b, const void* out,
              int N, int H, int W, int C, int FH, int FW, int stride, int pad, dwc_dtype_t dtype);
 
+/* Kernel launches of this library that a call with these arguments and 16-byte aligned
+ * pointers makes (the tcgen05 path: a preparation kernel and the main kernel; a filter
+ * gradient: its kernel and the sum of its slices), 0 for an empty output, -1 for
+ * invalid arguments.  `pass` as for dwc_path.  For profiling and launch accounting. */
+int dwc_kernel_launches(int pass, int N, int H, int W, int C, int FH, int FW, int stride, int pad,
+                        dwc_dtype_t dtype);
+
 #ifdef __cplusplus
 }
 #endif

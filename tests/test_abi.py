@@ -198,6 +198,20 @@ def test_path_selection_host_logic(lib):
     assert lib.dwc_path(0, FAKE + 4, None, None, 1, 8, 8, 16, 3, 3, 1, 1, 0) == 0
 
 
+def test_kernel_launch_counts(lib):
+    n = lambda pass_, **kw: lib.dwc_kernel_launches(pass_, *[dict(GOOD, **kw)[k] for k in
+                                                    ("N", "H", "W", "C", "FH", "FW", "stride", "pad", "dtype")])
+    f7 = dict(N=64, H=56, W=56, C=128, FH=7, FW=7, pad=3)
+    assert n(0, **f7) == 1 and n(1, **f7) == 1 and n(2, **f7) == 2
+    assert n(0, **dict(f7, C=96)) == 2                     # lane-group tail: a second launch
+    assert n(0, **dict(f7, C=32)) == 1                     # the tail is the only launch
+    big = dict(N=32, H=56, W=56, C=128, FH=31, FW=31, pad=15, dtype=1)
+    assert n(0, **big) == 2 and n(1, **big) == 2          # tcgen05: preparation + main
+    assert n(0, **dict(big, N=0)) == 0
+    assert n(0, FH=4, FW=4, **{k: v for k, v in GOOD.items() if k not in ("FH", "FW")}) == 1
+    assert n(0, stride=0) == -1
+
+
 def test_wait_limit_setting_round_trips(lib):
     prev = lib.dwc_set_wait_limit_ns(5_000_000)
     try:
