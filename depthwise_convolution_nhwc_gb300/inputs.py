@@ -161,7 +161,10 @@ def large_filter_cases(dtypes=("f32", "bf16")):
 # the filter size, pad (F-1)/2.
 STRIDE2_SHAPES = ((64, 112, 112, 96, 3), (64, 56, 56, 144, 3), (64, 28, 28, 192, 3),
                   (64, 14, 14, 576, 3), (64, 56, 56, 128, 5), (64, 28, 28, 256, 5),
-                  (64, 56, 56, 144, 7), (64, 28, 28, 256, 7))
+                  (64, 56, 56, 144, 7), (64, 28, 28, 256, 7),
+                  # the down-sampling layers of large-kernel networks
+                  (64, 56, 56, 128, 9), (64, 56, 56, 128, 11), (64, 56, 56, 128, 13),
+                  (32, 112, 112, 96, 9))
 
 
 def stride2_cases(dtypes=("f32", "bf16")):
