@@ -102,6 +102,7 @@ FAST = [
     C_(9, 6, 6, 16, 5),
     C_(2, 16, 16, 8, 31),
     C_(7, 7, 7, 96, 7),
+    C_(8, 8, 8, 96, 31),            # warp per image with the largest window of 8-wide maps
     C_(4, 8, 6, 32, 5),
     C_(2, 16, 16, 24, 9),
 ]
@@ -406,6 +407,7 @@ OUT16 = [
     C_(1, 23, 37, 128, 7),
     C_(1, 20, 60, 64, 17),          # tensor-core kernels (wide rows, 17 taps)
     C_(2, 7, 7, 128, 9),            # small-map kernels
+    C_(8, 8, 8, 256, 31),           # warp per image, large window (shared-memory plan)
     C_(2, 17, 19, 64, 3, s=2),      # stride-2 kernels
     C_(1, 23, 37, 128, 7, s=2),
     C_(1, 10, 10, 16, 5, s=3, p=2), # general kernels
