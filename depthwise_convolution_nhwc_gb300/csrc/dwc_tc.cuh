@@ -73,8 +73,8 @@ constexpr int kTcFeed0 = kTcMmaWarp + kTcIssuers;
 constexpr int kTcPlaneWarp = kTcFeed0 + kTcIssuers;
 constexpr int kTcWarps = kTcPlaneWarp + 1;
 constexpr int kTcThreads = kTcWarps * 32;
-constexpr int kTcRingSlots = 4;     // run slots per issuer ring (a power of two)
-constexpr int kTcRunsPerSlot = 2;   // most filter rows per ring item (runs per slot)
+constexpr int kTcRingSlots = 4;     // most run slots per issuer ring (a power of two)
+constexpr int kTcRunsPerSlot = 4;   // most filter rows per ring item (runs per slot)
 constexpr int kTcTmemCols = 512;
 constexpr int kTcDCols = 256;       // columns of one accumulator buffer (two buffers)
 constexpr int kTcMaxPlanes = 16;
@@ -103,7 +103,8 @@ struct TcArgs {
     int cbase;          // first channel of the launch's groups
     int ncg;            // channel groups of the launch
     int ps;             // plane ring slots
-    int rps;            // filter rows per ring item (1 or kTcRunsPerSlot)
+    int rps;            // filter rows per ring item (1 .. kTcRunsPerSlot)
+    int rslots, rshift; // slots per run ring (4, or 2 for items of 3 or 4 rows) and its log2
     uint32_t units, col_tiles;
     FastDiv fd_S;
     uint32_t plane_bytes, toep_bytes;   // one plane; one run
@@ -481,9 +482,12 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
             const uint32_t b_slot = static_cast<uint32_t>(a.rps) * b_run;
             const uint32_t idesc = a.idesc;
             const uint32_t ps = static_cast<uint32_t>(a.ps);
-            // this issuer's ring: slots [is * kTcRingSlots, (is + 1) * kTcRingSlots), filled
-            // in order with the runs of exactly the (channel, filter rows) items it takes
+            // this issuer's ring: barrier slots is * kTcRingSlots + [0, rslots) and the shared
+            // memory slots is * rslots + [0, rslots), filled in order with the runs of exactly
+            // the (channel, filter rows) items it takes
             const uint32_t ring0 = static_cast<uint32_t>(is) * kTcRingSlots;
+            const uint32_t rmask = static_cast<uint32_t>(a.rslots) - 1u;
+            const uint32_t sring0 = static_cast<uint32_t>(is * a.rslots);
             uint32_t item = 0;
             uint32_t pos0 = 0;   // plane-ring position of the unit's first channel
             for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x, pos0 += CG) {
@@ -502,14 +506,15 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
                     // item: filter rows fh0 .. fh0 + rps - 1 (fewer at the end), or (PART 2)
                     // filter row fh0 of this issuer's parity
                     for (int fh0 = par; fh0 < a.FH; fh0 += PART * a.rps, ++item) {
-                        const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
-                        const uint32_t phase = (item / kTcRingSlots) & 1u;
+                        const uint32_t slot = ring0 + (item & rmask);
+                        const uint32_t phase = (item >> a.rshift) & 1u;
                         if (!tc_wait(&toep_full[slot], phase, a, abort_flag)) { ok = false; break; }
                         tc_fence_after();
+                        const uint32_t sslot = sring0 + (item & rmask);
                         const int nr = min(a.rps, a.FH - fh0);
                         for (int rr = 0; rr < nr; ++rr) {
                             uint64_t ad = ap + static_cast<uint32_t>(fh0 + rr);
-                            uint64_t bd = bdesc0 + slot * b_slot + rr * b_run;
+                            uint64_t bd = bdesc0 + sslot * b_slot + rr * b_run;
                             tc_mma(dch, ad, bd, idesc, (fh0 + rr) != par ? 1u : 0u);
                             for (int ks = 1; ks < a.KS; ++ks) {
                                 ad += a_ks;
@@ -594,6 +599,8 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
         const int fpar = fi % PART;
         if (lane == 0) {
             const uint32_t ring0 = static_cast<uint32_t>(fi) * kTcRingSlots;
+            const uint32_t rmask = static_cast<uint32_t>(a.rslots) - 1u;
+            const uint32_t sring0 = static_cast<uint32_t>(fi * a.rslots);
             const uint32_t slot_bytes = static_cast<uint32_t>(a.rps) * a.toep_bytes;
             uint32_t item = 0;
             bool ok = true;
@@ -604,17 +611,17 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
                     const unsigned char* src =
                         a.runs + static_cast<size_t>(a.cbase + g * CG + ch) * a.FH * a.toep_bytes;
                     for (int fh0 = fpar; fh0 < a.FH; fh0 += PART * a.rps, ++item) {
-                        const uint32_t slot = ring0 + (item & (kTcRingSlots - 1));
-                        const uint32_t phase = (item / kTcRingSlots) & 1u;
+                        const uint32_t slot = ring0 + (item & rmask);
+                        const uint32_t phase = (item >> a.rshift) & 1u;
                         if (!tc_wait(&toep_empty[slot], phase ^ 1u, a, abort_flag)) { ok = false; break; }
                         const uint32_t bytes = static_cast<uint32_t>(min(a.rps, a.FH - fh0)) * a.toep_bytes;
                         mbar_arrive_expect_tx(&toep_full[slot], bytes);
-                        tc_bulk_load(toep + static_cast<size_t>(slot) * slot_bytes,
+                        tc_bulk_load(toep + static_cast<size_t>(sring0 + (item & rmask)) * slot_bytes,
                                      src + static_cast<size_t>(fh0) * a.toep_bytes, bytes, &toep_full[slot]);
                     }
                 }
             }
-            tc_drain(toep_full, ring0, kTcRingSlots, item, a);
+            tc_drain(toep_full, ring0, static_cast<uint32_t>(a.rslots), item, a);
         }
         __syncwarp();
     } else {
@@ -716,7 +723,7 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     const int cap = device_info().max_smem_optin;
     const int sms = device_info().sm_count;
     double best = 1e30;
-    int best_nt = 0, best_cg = 0, best_ps = 0, best_rps = 0, best_twc = 0;
+    int best_nt = 0, best_cg = 0, best_ps = 0, best_rps = 0, best_twc = 0, best_rslots = 0;
     for (int nt = 1; nt <= 64; ++nt) {
         const int twc = ((p.OW + nt - 1) / nt + 7) / 8 * 8;
         if (nt > 1 && (p.OW + twc - 1) / twc < nt) continue;
@@ -730,7 +737,8 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
         for (int cg = 8; cg >= 2; cg /= 2) {
             const int part = cg >= kTcIssuers ? 1 : kTcIssuers / cg;   // partial sums
             if (part * cg * nn > kTcDCols || p.C % cg != 0 || (part > 1 && rps > 1)) continue;
-            const size_t fixed = static_cast<size_t>(kTcMaxToep) * rps * ncm * 128 + kTcBarBytes;
+            const int rslots = rps >= 3 ? 2 : kTcRingSlots;   // ring depth of larger items
+            const size_t fixed = static_cast<size_t>(kTcIssuers) * rslots * rps * ncm * 128 + kTcBarBytes;
             if (fixed >= static_cast<size_t>(cap)) continue;
             const int ps = static_cast<int>(std::min<size_t>(kTcMaxPlanes, (cap - fixed) / plane));
             if (ps < cg + 1) continue;   // the next unit's planes must fill while one computes
@@ -747,6 +755,7 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
             const double cost = static_cast<double>((units + sms - 1) / sms) * unit;
             if (cost < best) {
                 best = cost; best_nt = nt; best_cg = cg; best_ps = ps; best_rps = rps; best_twc = twc;
+                best_rslots = rslots;
             }
         }
     }
@@ -768,6 +777,8 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     a.fd_S.init(static_cast<uint32_t>(a.S));
     a.ps = best_ps;
     a.rps = best_rps;
+    a.rslots = best_rslots;
+    a.rshift = best_rslots == 4 ? 2 : 1;
     // stacked copy: input column w at column w + Lp, Lp = pad_w mod 8, so that a tile's first
     // column j*TWc - pad_w lands on a multiple of 8 (x0 = Lp - pad_w); the copy spans the
     // image and, to the right, every column a tile reads (beyond it the TMA box reads zeros)
@@ -778,7 +789,7 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     P.runs_bytes = static_cast<size_t>(p.C) * p.FH * a.toep_bytes;
     // shared memory: plane ring, run rings, barriers; one CTA per SM (each allocates all of
     // tensor memory): ask for more than half of it
-    const size_t toep_ring = static_cast<size_t>(kTcMaxToep) * a.rps * a.toep_bytes;
+    const size_t toep_ring = static_cast<size_t>(kTcIssuers) * a.rslots * a.rps * a.toep_bytes;
     a.off_toep = static_cast<uint32_t>(static_cast<size_t>(a.ps) * a.plane_bytes);
     a.off_bar = a.off_toep + static_cast<uint32_t>(toep_ring);
     P.smem = std::max<size_t>(a.off_bar + kTcBarBytes, static_cast<size_t>(cap) / 2 + 1024);

@@ -3,7 +3,8 @@ fp64 oracle, with the kernel family forced (dwc_testing_prefer_family) so that e
 below runs on the kernel under test, whatever the automatic choice would be.
 
 The tcgen05 kernel (family 2) tiles 128 virtual output rows that run through several
-images, N output columns per column tile, and groups of 2, 4 or 8 channels; the cases cover
+images, N output columns per column tile, groups of 2, 4 or 8 channels and ring items of 1
+to 4 filter rows; the cases cover
 several images per tile, tall images cut into 128-row bands, several column tiles, stripe
 filters, filters from 1 to 51 taps, pads from 0 to beyond (F-1)/2, channel counts that take
 every channel-group size, and both output types.  The warp-level MMA kernel (family 4) keeps
@@ -53,6 +54,10 @@ TC_CASES = [
     C_(3, 7, 7, 40, 31),              # channel groups of 8 (40 channels), map below filter
     C_(2, 56, 56, 16, 31),            # the large-kernel stage shape, few channels
     C_(1, 1, 1, 8, 3),                # single pixel
+    # groups of 4 channels with ring items of 3 or 4 filter rows, the last item shorter
+    C_(8, 28, 28, 64, 13),            # items of 4 rows (13 = 3 x 4 + 1)
+    C_(8, 56, 56, 64, 17),            # items of 3 rows (17 = 5 x 3 + 2)
+    C_(16, 30, 40, 64, 11),           # items of 4 rows, N = 48 columns
 ]
 
 
