@@ -35,7 +35,8 @@ EXPORTS = ("dwc_fwd", "dwc_fwd_ex", "dwc_fwd_bn_act", "dwc_bwd_data", "dwc_bwd_d
            "dwc_bwd_filter_workspace_size", "dwc_bwd_filter", "dwc_bwd_filter_noalloc",
            "dwc_device_status", "dwc_set_wait_limit_ns", "dwc_fma_rate_probe",
            "dwc_status_string", "dwc_version", "dwc_path", "dwc_kernel_launches",
-           "dwc_testing_stall_next_row_launch", "dwc_testing_prefer_family")
+           "dwc_testing_stall_next_row_launch", "dwc_testing_prefer_family",
+           "dwc_testing_tc_row_pairs")
 FMA_KINDS = {"ffma": 0, "ffma2": 1, "hfma2": 2, "bf16x2": 3}  # dwc_fma_rate_probe kinds
 
 _lock = threading.Lock()
@@ -102,6 +103,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.dwc_testing_stall_next_row_launch.restype = None
         lib.dwc_testing_prefer_family.argtypes = [i]
         lib.dwc_testing_prefer_family.restype = i
+        lib.dwc_testing_tc_row_pairs.argtypes = [i]
+        lib.dwc_testing_tc_row_pairs.restype = i
         if path is None:
             _lib = lib
         return lib

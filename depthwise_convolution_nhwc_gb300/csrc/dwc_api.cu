@@ -33,6 +33,7 @@ std::mutex g_mu;
 std::atomic<unsigned long long> g_wait_limit_ns{0};  // 0: the kernels' default
 std::atomic<int> g_row_stall{0};
 std::atomic<int> g_family_pref{0};
+std::atomic<int> g_tc_pairs{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 // One-time set-up for the current device; nullptr if CUDA is unusable.
@@ -126,6 +127,8 @@ unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_ord
 int take_row_stall() { return g_row_stall.exchange(0, std::memory_order_acq_rel); }
 
 int family_preference() { return g_family_pref.load(std::memory_order_relaxed); }
+
+int tc_row_pairs_mode() { return g_tc_pairs.load(std::memory_order_relaxed); }
 
 static unsigned int* status_word() {
     PerDevice* s = device_state();
@@ -556,6 +559,11 @@ int dwc_testing_prefer_family(int family) {
         family != kFamilyMmaSync)
         return -1;
     return g_family_pref.exchange(family, std::memory_order_acq_rel);
+}
+
+int dwc_testing_tc_row_pairs(int mode) {
+    if (mode < 0 || mode > 2) return -1;
+    return g_tc_pairs.exchange(mode, std::memory_order_acq_rel);
 }
 
 int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int H, int W, int C,

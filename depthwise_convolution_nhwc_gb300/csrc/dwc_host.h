@@ -199,12 +199,15 @@ cudaError_t launch_tc_rows_f16(const RowConv& p);
 bool tc_rows_fits(const RowConv& p);
 // Where the tcgen05 kernel is the one to run (timed against the row, warp-level MMA and
 // small-map kernels, bf16, fp32 outputs): from 9 taps on rows of at least 28 outputs
-// (64x56x56x128: 110 against 115 us at 9 taps, 110 against 161 at 11, 114 against 218 at 13;
-// 64x28x28x256 at 9 taps a tie, at 7 the row kernel 45 against 63 us), and from 17 taps on
-// rows of 17 to 27 outputs; maps up to 16 wide stay on the small-map kernel (64x14x14x512
-// 31x31: 134 us there against 194 on tcgen05; 64x7x7x1024 31x31: 33 against 262).
+// (64x56x56x128: 100 against 115 us at 9 taps, 111 against 162 at 11, 112 against 220 at 13;
+// 64x28x28x256: 59 against 66 us at 9 taps, at 7 the row kernel 46 against 58), from 17 taps
+// on rows of 17 to 27 outputs, and from 13 taps on rows of 14 to 16 outputs where the batch
+// carries enough channel planes (64x14x14x512: 55 against 74 us on the small-map kernel at 13
+// taps, 116 against 137 at 31; 32x14x14x512 31x31 a tie; at 9 taps the row kernel 45 against
+// 52); 7x7 maps stay on the small-map kernel (64x7x7x1024 31x31: 33 against 262 us).
 inline bool tc_rows_wanted(const RowConv& p) {
-    return (p.FW >= 9 && p.OW >= 28) || (p.FW >= 17 && p.OW >= 17);
+    return (p.FW >= 9 && p.OW >= 28) || (p.FW >= 17 && p.OW >= 17) ||
+           (p.FW >= 13 && p.OW >= 14 && static_cast<long long>(p.N) * p.C >= 16384);
 }
 // Kernel launches of a tcgen05 call: the preparation and the main kernel (0 when the shape
 // has no plan).
@@ -222,6 +225,9 @@ int tensor_core_rows(const RowConv& p);
 // Family preference for 16-bit forward / backward-data calls (tests and kernel comparisons;
 // 0 = automatic choice), set through dwc_testing_prefer_family.
 int family_preference();
+// Filter rows per MMA of the tcgen05 kernel (tests): 0 = the plan's choice, 1 = one, 2 = pairs;
+// set through dwc_testing_tc_row_pairs.
+int tc_row_pairs_mode();
 bool tensor_core_fgrad(int N, int C, int OH, int OW, int FH, int FW);
 
 // The argument and pointer checks of dwc_bwd_filter without its workspace checks; returns a

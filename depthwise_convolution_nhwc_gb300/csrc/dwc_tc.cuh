@@ -24,6 +24,21 @@
 //    virtual row n*S (S = image rows + padding shared with the next image), so one 128-row
 //    MMA covers, for example, two 56-row images; rows in the gaps are computed and dropped.
 //
+// Paired filter rows.  An MMA's time is set by reading its operands from shared memory (A's
+// 4 KB and T's N x 32 bytes at 128 bytes a clock) and a floor of ~46 cycles, so narrow MMAs
+// cost nearly as much as wide ones.  One MMA of N = 2 N' takes the Toeplitz matrices of filter
+// rows 2p and 2p+1 side by side against the same A (input rows shifted by 2p):
+//    D[m, (0, n)] = sum_p A_2p[m] T_2p    the even filter rows of output row m,
+//    D[m, (1, n)] = sum_p A_2p[m] T_2p+1  the odd filter rows of output row m - 1,
+// so output row m is D[m, (0, .)] + D[m+1, (1, .)]: A is read once for two filter rows (for
+// N' = 32, one N=64 MMA of 48 cycles instead of two N=32 ones of 46).  A tile then owns 127
+// rows; the epilogue takes the odd part from the next lane (a shuffle, and at the three
+// warp boundaries of the tile the next warp's first lane through shared memory).  The two
+// runs are interleaved core matrix by core matrix, so a descriptor with a K-direction stride
+// of 256 bytes and an N-direction stride of 128 reads both halves.  An odd last filter row is
+// paired with zeros.  Column tiles of up to 32 outputs keep a unit's 4 channels in 256
+// accumulator columns (two buffers).
+//
 // Two launches.  A preparation kernel writes, into scratch memory of the call,
 //  * the input as per-channel planes in the layout above: channel-major, the images' rows
 //    stacked on the virtual rows (zero rows between images) and the columns padded so that
@@ -36,7 +51,7 @@
 // shared-memory pipes that the MMA issuers and their barriers also go through.
 //
 // Warp roles per CTA (one CTA per SM, persistent over units of (row tile, column tile, group
-// of CG = 2, 4 or 8 channels)):
+// of CG = 2 or 4 channels)):
 //  * 4 epilogue warps -- warp w reads the 32-lane quadrant w of the accumulators
 //    (tcgen05.ld) and writes the CG channels of a pixel with 16-byte stores;
 //  * 4 MMA warps: one lane each issues the MMAs of every fourth channel of the group, or,
@@ -80,21 +95,30 @@ constexpr int kTcDCols = 256;       // columns of one accumulator buffer (two bu
 constexpr int kTcMaxPlanes = 16;
 constexpr int kTcMaxToep = kTcIssuers * kTcRingSlots;
 constexpr int kTcMaxBox = 256;      // TMA box extent limit (plane rows)
-// barriers (plane and run rings, two accumulator buffers, the final MMA barriers), the
-// tensor-memory address and the abort flag
+// barriers (plane and run rings, two accumulator buffers, the final MMA barriers, the
+// epilogue warps' exchange of paired rows), the tensor-memory address and the abort flag
 constexpr int kTcBarBytes =
-    ((2 * kTcMaxPlanes + 2 * kTcMaxToep + 2 * 2 + kTcIssuers) * 8 + 8 + 127) / 128 * 128;
+    ((2 * kTcMaxPlanes + 2 * kTcMaxToep + 2 * 2 + kTcIssuers + 2 * kTcEpiWarps * 2) * 8 + 8 + 127) /
+    128 * 128;
+// paired rows: per epilogue warp and accumulator buffer, its first lane's odd-row sums of 4
+// channels x up to 32 columns
+constexpr int kTcXFloats = 128;
+constexpr int kTcXBytes = kTcEpiWarps * 2 * kTcXFloats * 4;
 
 struct TcArgs {
-    const unsigned char* runs;   // Toeplitz runs [C][FH][NCM core matrices], 16-bit
+    const unsigned char* runs;   // Toeplitz runs [C][FHI][(pair + 1) * NCM core matrices], 16-bit
     void* out;          // N x OH x OW x C, OutT
     unsigned int* status;
     unsigned long long wait_ns;
     int N, C, OH, OW, FH;
+    int pair;           // 1: filter rows in pairs (N = 2 NN per MMA), 0: one row per MMA
+    int FHI;            // MMA rows of filters per channel: FH, or ceil(FH / 2) in pairs
+    int mrows;          // output rows a row tile owns: 128, or 127 in pairs
     int S;              // virtual rows per image
     int kimg;           // images per row tile (0: tiles are 128-row bands of one image)
     int bands;          // row tiles per image when kimg == 0
-    int NN;             // MMA N (output columns of a column tile, multiple of 16)
+    int NN;             // output columns of a column tile's accumulator (multiple of 16; in
+                        // pairs a multiple of 8 up to 32, the MMA's N being 2 NN)
     int TWc;            // output columns a column tile owns (<= NN, multiple of 8)
     int KS;             // K-steps of 16
     int MR;             // staged rows per plane (>= FH + 127, multiple of 8, <= 256)
@@ -107,8 +131,8 @@ struct TcArgs {
     int rslots, rshift; // slots per run ring (4, or 2 for items of 3 or 4 rows) and its log2
     uint32_t units, col_tiles;
     FastDiv fd_S;
-    uint32_t plane_bytes, toep_bytes;   // one plane; one run
-    uint32_t off_toep, off_bar;         // byte offsets in shared memory
+    uint32_t plane_bytes, toep_bytes;   // one plane; one run (a pair of runs in pairs)
+    uint32_t off_toep, off_bar, off_x;  // byte offsets in shared memory
     uint32_t idesc;     // instruction descriptor (kind::f16, fp32 accumulation)
 };
 
@@ -231,7 +255,8 @@ __device__ __forceinline__ void tc_drain(uint64_t* full, uint32_t first_slot, ui
         }
 }
 
-// Row tile `t`: first virtual output row v0 and the rows [v_lo, v_hi) the tile owns.
+// Row tile `t`: first virtual output row v0 and the rows [v_lo, v_hi) the tile owns (tiles of
+// one image's rows are mrows apart).
 struct TcTile {
     int v0, v_lo, v_hi;
 };
@@ -244,9 +269,9 @@ __device__ __forceinline__ TcTile tc_tile(const TcArgs& a, int t) {
         r.v_hi = min(a.N, n0 + a.kimg) * a.S;
     } else {
         const int n = t / a.bands, b = t - n * a.bands;
-        r.v0 = n * a.S + kTcM * b;
+        r.v0 = n * a.S + a.mrows * b;
         r.v_lo = r.v0;
-        r.v_hi = n * a.S + min(a.OH, kTcM * (b + 1));
+        r.v_hi = n * a.S + min(a.OH, a.mrows * (b + 1));
     }
     return r;
 }
@@ -298,13 +323,14 @@ struct TcPrepArgs {
     const void* x;      // N x H x W x C, 16-bit
     const void* w;      // FH x FW x C, 16-bit
     void* planes;       // C x V x Wp stacked copy (V = N * S virtual rows), 16-bit
-    void* runs;         // C x FH runs of 8*NCM rows of 8 values, 16-bit
+    void* runs;         // C x FHI runs of (pair + 1) * 8 * NCM rows of 8 values, 16-bit
     int N, H, W, C, FH, FW, pad_h, S, Lp, Wp, NN, NCM;
+    int FHI, pair;      // run items per channel; 1: two filter rows' runs interleaved
     int CT;                  // channels of a copy tile (64, 32, 16 or 8, dividing C)
     int piece_shift;         // log2(CT / 8): 16-byte pieces of a pixel in a copy tile
     int V;                   // N * S
     int plane_tiles;         // V * (C / CT) * ceil(Wp / 64) tiles of one row
-    int run_tasks;           // C * FH * 8 * NCM: one 16-byte row of a run
+    int run_tasks;           // C * FHI * (pair + 1) * 8 * NCM: one 16-byte row of a run
     int run_blocks;          // blocks [0, run_blocks) write the runs, the rest the copy
     // divisions by launch constants (all operands below 2^31)
     FastDiv fd_xt, fd_ct, fd_S, fd_C, fd_rows;
@@ -374,22 +400,30 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const TcPrepArg
     } else {
         // Runs: row r of the run of (c, fh) holds z[r .. r+7], z[i] = filt(fh, i - (NN-1)),
         // zero outside the filter; filt is w, or w rotated by 180 degrees (backward data).
-        // The channel is the fastest task index, so a warp's tap loads are contiguous.
+        // In pairs, item i holds the runs of filter rows 2i and 2i+1 (zeros past the filter)
+        // interleaved by core matrix: core matrix 2d + h of the item is core matrix d of row
+        // 2i + h.  The channel is the fastest task index, so a warp's tap loads are contiguous.
         const uint16_t* Wt = static_cast<const uint16_t*>(a.w);
         uint16_t* R = static_cast<uint16_t*>(a.runs);
-        const int rows = 8 * a.NCM;
+        const int rows = 8 * a.NCM * (a.pair + 1);
         const int stride = a.run_blocks * static_cast<int>(blockDim.x);
         for (int task = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); task < a.run_tasks;
              task += stride) {
             uint32_t cu, ru;
             const uint32_t q = a.fd_C.divmod(static_cast<uint32_t>(task), cu);
-            const int fh = static_cast<int>(a.fd_rows.divmod(q, ru));
-            const int c = static_cast<int>(cu), r = static_cast<int>(ru);
+            const int fi = static_cast<int>(a.fd_rows.divmod(q, ru));
+            const int c = static_cast<int>(cu);
+            int r = static_cast<int>(ru), fh = fi;
+            if (a.pair) {
+                const int cm = r >> 3;
+                fh = 2 * fi + (cm & 1);
+                r = ((cm >> 1) << 3) | (r & 7);
+            }
             uint4 o = make_uint4(0u, 0u, 0u, 0u);
             // rows r + 7 < NN - 1 or r > NN + FW - 2 hold no tap (most of a run): zeros, with no
             // tap computed (the test is uniform over a warp, whose lanes differ in c only)
             const int f0 = r - (a.NN - 1);
-            if (f0 + 7 >= 0 && f0 < a.FW) {
+            if (fh < a.FH && f0 + 7 >= 0 && f0 < a.FW) {
                 const int fhe = FLIP ? a.FH - 1 - fh : fh;
                 const uint16_t* wrow = Wt + static_cast<size_t>(fhe) * a.FW * a.C + c;
                 uint32_t z[8];
@@ -403,20 +437,22 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const TcPrepArg
                 o.z = z[4] | (z[5] << 16);
                 o.w = z[6] | (z[7] << 16);
             }
-            *reinterpret_cast<uint4*>(R + ((static_cast<size_t>(c) * a.FH + fh) * rows + r) * 8) = o;
+            *reinterpret_cast<uint4*>(R + ((static_cast<size_t>(c) * a.FHI + fi) * rows + ru) * 8) = o;
         }
     }
 }
 
 // ------------------------------------------------------------------ main kernel
 
-template <typename T, class OutT, int CG>
+template <typename T, class OutT, int CG, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
     // issuers per channel: 1 (each issuer owns whole channels), or 2 in groups of 2 channels
     // (filter-row parities into two partial sums, one filter row per ring item)
     constexpr int PART = CG >= kTcIssuers ? 1 : kTcIssuers / CG;
     static_assert(CG * PART % kTcIssuers == 0 && PART <= 2, "issuers divide the group's channels");
+    // paired rows: 4 channels, one per issuer, 2 NN <= 64 accumulator columns each
+    static_assert(!PAIR || CG == kTcIssuers, "paired rows take groups of 4 channels");
     constexpr int CH_STEP = kTcIssuers / PART;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* planes = smem;
@@ -429,7 +465,9 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
     uint64_t* d_full = toep_empty + kTcMaxToep;   // [2]
     uint64_t* d_empty = d_full + 2;               // [2]
     uint64_t* mma_done = d_empty + 2;             // [kTcIssuers]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + kTcIssuers);
+    uint64_t* x_full = mma_done + kTcIssuers;     // [epilogue warp][channel pair]
+    uint64_t* x_empty = x_full + 2 * kTcEpiWarps;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(x_empty + 2 * kTcEpiWarps);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -448,6 +486,10 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
             mbar_init(&d_empty[s], kTcEpiWarps);
         }
         for (int i = 0; i < kTcIssuers; ++i) mbar_init(&mma_done[i], 1);
+        for (int i = 0; i < 2 * kTcEpiWarps; ++i) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], 1);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -473,10 +515,12 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
             uint32_t db = 0, dphase = 0;
             bool ok = true;
             // Descriptors are built once; the start-address field (bits 0-13, 16-byte units)
-            // then advances by plain additions: a plane slot, a filter row (16 bytes), a
-            // K-step (two planes of A, two core matrices of T), a run.
+            // then advances by plain additions: a plane slot, a filter row (16 bytes; 32 for a
+            // pair), a K-step (two planes of A, two core matrices of T; four of a pair), a run.
             const uint64_t adesc0 = tc_sdesc(smem_addr(planes), a.MR * 16u, 128u);
-            const uint64_t bdesc0 = tc_sdesc(smem_addr(toep), 128u, 128u);
+            const uint64_t bdesc0 = tc_sdesc(smem_addr(toep), PAIR ? 256u : 128u, 128u);
+            const uint32_t a_row = PAIR ? 2u : 1u;     // A advance per item row
+            const uint32_t b_ks = PAIR ? 32u : 16u;    // T advance per K-step
             const uint32_t a_ks = 2u * a.MR;           // A advance per K-step (16-byte units)
             const uint32_t a_slot = a.plane_bytes >> 4, b_run = a.toep_bytes >> 4;
             const uint32_t b_slot = static_cast<uint32_t>(a.rps) * b_run;
@@ -502,23 +546,24 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
                     if (!tc_wait(&plane_full[pslot], pphase, a, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t ap = adesc0 + pslot * a_slot;
-                    const uint32_t dch = dcol + static_cast<uint32_t>((par * CG + ch) * a.NN);
-                    // item: filter rows fh0 .. fh0 + rps - 1 (fewer at the end), or (PART 2)
-                    // filter row fh0 of this issuer's parity
-                    for (int fh0 = par; fh0 < a.FH; fh0 += PART * a.rps, ++item) {
+                    const uint32_t dch =
+                        dcol + static_cast<uint32_t>(PAIR ? ch * 2 * a.NN : (par * CG + ch) * a.NN);
+                    // item: filter rows (pairs of rows) fh0 .. fh0 + rps - 1 (fewer at the end),
+                    // or (PART 2) filter row fh0 of this issuer's parity
+                    for (int fh0 = par; fh0 < a.FHI; fh0 += PART * a.rps, ++item) {
                         const uint32_t slot = ring0 + (item & rmask);
                         const uint32_t phase = (item >> a.rshift) & 1u;
                         if (!tc_wait(&toep_full[slot], phase, a, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t sslot = sring0 + (item & rmask);
-                        const int nr = min(a.rps, a.FH - fh0);
+                        const int nr = min(a.rps, a.FHI - fh0);
                         for (int rr = 0; rr < nr; ++rr) {
-                            uint64_t ad = ap + static_cast<uint32_t>(fh0 + rr);
+                            uint64_t ad = ap + static_cast<uint32_t>(fh0 + rr) * a_row;
                             uint64_t bd = bdesc0 + sslot * b_slot + rr * b_run;
                             tc_mma(dch, ad, bd, idesc, (fh0 + rr) != par ? 1u : 0u);
                             for (int ks = 1; ks < a.KS; ++ks) {
                                 ad += a_ks;
-                                bd += 16u;
+                                bd += b_ks;
                                 tc_mma(dch, ad, bd, idesc, 1u);
                             }
                         }
@@ -537,6 +582,94 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
             if (!mbar_wait(&mma_done[is], 0, a.wait_ns)) record_status(a.status, DWC_DEVSTAT_TIMEOUT);
         }
         __syncwarp();
+    } else if (warp < kTcEpiWarps && PAIR) {
+        // ------------------------------------------------------------- epilogue, paired rows
+        // Output row m of the tile = D[m, even half] + D[m + 1, odd half].  Per unit, warps
+        // 1-3 first publish their lane 0's odd halves (lane 31 of the warp before needs them),
+        // then every warp sums its lanes' even halves and the next lanes' odd halves.
+        const int quad = warp;
+        const int m = quad * 32 + lane;
+        float* xbuf = reinterpret_cast<float*>(smem + a.off_x);
+        const uint32_t nn2 = 2u * static_cast<uint32_t>(a.NN);
+        uint32_t db = 0, dphase = 0;
+        for (uint32_t u = blockIdx.x; u < a.units; u += gridDim.x) {
+            int t, j, g;
+            tc_unit(a, u, t, j, g);
+            if (!tc_wait_warp(&d_full[db], dphase, a, abort_flag, 1024)) break;
+            tc_fence_after();
+            const TcTile tl = tc_tile(a, t);
+            const int v = tl.v0 + m;
+            uint32_t rr;
+            const int n = static_cast<int>(a.fd_S.divmod(static_cast<uint32_t>(v), rr));
+            const int r = static_cast<int>(rr);
+            const bool row_ok = m < a.mrows && v >= tl.v_lo && v < tl.v_hi && r < a.OH;
+            const int ow0 = j * a.TWc;
+            const int ow_end = min(a.OW, ow0 + a.TWc);
+            const int c0 = a.cbase + g * CG;
+            OutT* orow = static_cast<OutT*>(a.out) +
+                         (static_cast<size_t>(row_ok ? n : 0) * a.OH + (row_ok ? r : 0)) *
+                             static_cast<size_t>(a.OW) * a.C + c0;
+            // columns of channel ch: ch * 2 NN + 16 b + 8 h + e, output column block b
+            // (reversed), half h
+            const uint32_t dbase = tmem + db * kTcDCols + (static_cast<uint32_t>(quad * 32) << 16);
+            const int xs = quad * 2 + static_cast<int>(db);   // this warp's exchange slot
+            if (quad > 0) {
+                if (!tc_wait_warp(&x_empty[xs], dphase ^ 1u, a, abort_flag, 1024)) break;
+                float* xb = xbuf + xs * kTcXFloats;
+                for (int cb = 0; cb < a.NN; cb += 8) {
+                    uint32_t h[CG][8];
+#pragma unroll
+                    for (int ch = 0; ch < CG; ++ch) tc_ld8(dbase + ch * nn2 + 2 * cb + 8, h[ch]);
+                    tc_wait_ld();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int ch = 0; ch < CG; ++ch)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) xb[ch * a.NN + cb + e] = __uint_as_float(h[ch][e]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&x_full[xs]);
+            }
+            const int xn_slot = xs + 2;                      // the next warp's slot
+            const float* xn = xbuf + (quad < kTcEpiWarps - 1 ? xn_slot : 0) * kTcXFloats;
+            if (quad < kTcEpiWarps - 1 && !tc_wait_warp(&x_full[xn_slot], dphase, a, abort_flag, 1024))
+                break;
+            for (int cb = 0; cb < a.NN; cb += 8) {
+                uint32_t d[CG][16];
+#pragma unroll
+                for (int ch = 0; ch < CG; ++ch) tc_ld16(dbase + ch * nn2 + 2 * cb, d[ch]);
+                tc_wait_ld();
+                float o[CG][8];
+#pragma unroll
+                for (int ch = 0; ch < CG; ++ch)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        float nx = __shfl_down_sync(0xffffffffu, __uint_as_float(d[ch][8 + e]), 1);
+                        if (lane == 31) nx = quad < kTcEpiWarps - 1 ? xn[ch * a.NN + cb + e] : 0.f;
+                        o[ch][e] = __uint_as_float(d[ch][e]) + nx;
+                    }
+                if (row_ok) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int ow = ow0 + a.NN - 1 - (cb + e);   // reversed columns
+                        if (ow < ow0 || ow >= ow_end) continue;
+                        float vals[CG];
+#pragma unroll
+                        for (int ch = 0; ch < CG; ++ch) vals[ch] = o[ch][e];
+                        tc_store_pixel<OutT, CG>(orow + static_cast<size_t>(ow) * a.C, vals);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (quad < kTcEpiWarps - 1) mbar_arrive(&x_empty[xn_slot]);
+                mbar_arrive(&d_empty[db]);
+            }
+            db ^= 1u;
+            if (db == 0) dphase ^= 1u;
+        }
     } else if (warp < kTcEpiWarps) {
         // ------------------------------------------------------------- epilogue
         const int quad = warp;   // one warp per quadrant, every column
@@ -609,12 +742,12 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
                 tc_unit(a, u, t, j, g);
                 for (int ch = fi / PART; ch < CG && ok; ch += CH_STEP) {
                     const unsigned char* src =
-                        a.runs + static_cast<size_t>(a.cbase + g * CG + ch) * a.FH * a.toep_bytes;
-                    for (int fh0 = fpar; fh0 < a.FH; fh0 += PART * a.rps, ++item) {
+                        a.runs + static_cast<size_t>(a.cbase + g * CG + ch) * a.FHI * a.toep_bytes;
+                    for (int fh0 = fpar; fh0 < a.FHI; fh0 += PART * a.rps, ++item) {
                         const uint32_t slot = ring0 + (item & rmask);
                         const uint32_t phase = (item >> a.rshift) & 1u;
                         if (!tc_wait(&toep_empty[slot], phase ^ 1u, a, abort_flag)) { ok = false; break; }
-                        const uint32_t bytes = static_cast<uint32_t>(min(a.rps, a.FH - fh0)) * a.toep_bytes;
+                        const uint32_t bytes = static_cast<uint32_t>(min(a.rps, a.FHI - fh0)) * a.toep_bytes;
                         mbar_arrive_expect_tx(&toep_full[slot], bytes);
                         tc_bulk_load(toep + static_cast<size_t>(sring0 + (item & rmask)) * slot_bytes,
                                      src + static_cast<size_t>(fh0) * a.toep_bytes, bytes, &toep_full[slot]);
@@ -679,11 +812,17 @@ inline double tc_mma_cycles(int n) {
 // 46 cycles, as fast as the tensor core runs the N = 64 MMAs.
 constexpr double kTcItemIssueCycles = 500.0;
 constexpr double kTcMmaIssueCycles = 183.0;
+// The epilogue's cycles per output pixel of a unit (128 rows x the tile's columns; every lane
+// stores its own row, so each store touches 32 cache lines), fitted to the kernel's measured
+// times where it, not the MMAs, sets the pace (small filters: bf16 64x56x56x128 9x9 and 17x17,
+// 64x28x28x256 13x13); paired rows read the accumulators half as often again.
+constexpr double kTcEpiPixelCycles = 1.5;
 
 struct TcPlan {
     TcArgs a;
     size_t smem;
     int cg;
+    bool pair;
     int Lp, Wp;                       // stacked copy: left padding, row length (columns)
     size_t planes_bytes, runs_bytes;  // scratch: stacked copy, run table
 };
@@ -692,82 +831,100 @@ struct TcPlan {
 // fit the kernel (the caller then takes another kernel).
 inline bool tc_plan(const RowConv& p, TcPlan& P) {
     TcArgs& a = P.a;
-    // channel groups of 4 and 8 channels, 16-byte copies of 8 channels in the preparation
+    // 16-byte copies of 8 channels in the preparation
     if (p.C % 8 != 0 || p.FH < 1 || p.FW < 1 || p.FW > 256 || p.OH < 1 || p.OW < 1) return false;
     a.N = p.N; a.C = p.C; a.OH = p.OH; a.OW = p.OW; a.FH = p.FH;
     // virtual rows per image: the image's rows and padding, shared with the next image
     a.S = std::max({p.pad_h + p.H, p.OH + p.FH - 1 - p.pad_h, p.OH});
-    if (p.OH <= kTcM) {
-        a.kimg = std::min(p.N, (kTcM - p.OH) / a.S + 1);
-        a.bands = 1;
-    } else {
-        a.kimg = 0;
-        a.bands = (p.OH + kTcM - 1) / kTcM;
-    }
-    const long long row_tiles = a.kimg > 0 ? (p.N + a.kimg - 1) / a.kimg
-                                           : static_cast<long long>(p.N) * a.bands;
+    // row tiles of `mrows` output rows: whole images, or bands of one image
+    auto row_layout = [&](int mrows, int& kimg, int& bands) -> long long {
+        if (p.OH <= mrows) {
+            kimg = std::min(p.N, (mrows - p.OH) / a.S + 1);
+            bands = 1;
+            return kimg > 0 ? (p.N + kimg - 1) / kimg : 0;   // (no images: no tiles)
+        }
+        kimg = 0;
+        bands = (p.OH + mrows - 1) / mrows;
+        return static_cast<long long>(p.N) * bands;
+    };
     if (static_cast<long long>(p.N + 1) * a.S + 2 * kTcM >= (1LL << 31)) return false;
     a.MR = (p.FH + kTcM - 1 + 7) / 8 * 8;
     if (a.MR > kTcMaxBox) return false;   // one TMA box per plane
-    // Column tile, channel group and filter rows per ring item, chosen together by an
-    // estimate of the busiest SM's cycles: per unit (units spread evenly over the SMs, whole
-    // units only) the longer of the tensor core's MMA time and an issuer's time (a fixed cost
-    // per ring item and per MMA), plus, where shared memory cannot hold the planes of two
-    // units (the next unit's planes then wait for the end of the current one), the planes'
-    // copy time at 64 bytes per cycle.  Groups of 2 channels (two issuers per channel, two
+    // Row pairing, column tile, channel group and filter rows per ring item, chosen together
+    // by an estimate of the busiest SM's cycles: per unit (units spread evenly over the SMs,
+    // whole units only) the longer of the tensor core's MMA time and an issuer's time (a fixed
+    // cost per ring item and per MMA) and the epilogue's time, plus, where shared memory cannot
+    // hold the planes of two units (the next unit's planes then wait for the end of the
+    // current one), the planes' copy time at 64 bytes per cycle.  Groups of 2 channels (two issuers per channel, two
     // partial sums) make units half as large, which evens out the last wave of units over
     // the SMs.  Column tiles own a multiple of 8 columns (every tile's first plane starts on
     // an 8-column boundary of the stacked copy).  Constraints: two accumulator buffers of
-    // partials x CG x NN columns in tensor memory, the planes and the run rings in shared
-    // memory.
+    // partials x CG x NN columns (paired rows: of 4 channels x 2 NN columns) in tensor memory,
+    // the planes and the run rings in shared memory.
     const int cap = device_info().max_smem_optin;
     const int sms = device_info().sm_count;
     double best = 1e30;
     int best_nt = 0, best_cg = 0, best_ps = 0, best_rps = 0, best_twc = 0, best_rslots = 0;
-    for (int nt = 1; nt <= 64; ++nt) {
-        const int twc = ((p.OW + nt - 1) / nt + 7) / 8 * 8;
-        if (nt > 1 && (p.OW + twc - 1) / twc < nt) continue;
-        const int nn = (twc + 15) / 16 * 16;
-        if (nn > kTcDCols) continue;
-        const int ks = (nn + p.FW - 1 + 15) / 16;
-        const int ncm = nn / 8 + 2 * ks - 1;
-        const size_t plane = static_cast<size_t>(2 * ks) * a.MR * 16;
-        const long long tiles = row_tiles * ((p.OW + twc - 1) / twc);
-        for (int rps = kTcRunsPerSlot; rps >= 1; --rps)
-        for (int cg = 8; cg >= 2; cg /= 2) {
-            const int part = cg >= kTcIssuers ? 1 : kTcIssuers / cg;   // partial sums
-            if (part * cg * nn > kTcDCols || p.C % cg != 0 || (part > 1 && rps > 1)) continue;
-            const int rslots = rps >= 3 ? 2 : kTcRingSlots;   // ring depth of larger items
-            const size_t fixed = static_cast<size_t>(kTcIssuers) * rslots * rps * ncm * 128 + kTcBarBytes;
-            if (fixed >= static_cast<size_t>(cap)) continue;
-            const int ps = static_cast<int>(std::min<size_t>(kTcMaxPlanes, (cap - fixed) / plane));
-            if (ps < cg + 1) continue;   // the next unit's planes must fill while one computes
-            const long long units = tiles * (p.C / cg);
-            const double tensor = cg * p.FH * ks * tc_mma_cycles(nn);
-            const int rows_per_issuer = (p.FH + part - 1) / part;
-            const double issue = (cg * part / kTcIssuers) * ((rows_per_issuer + rps - 1) / rps) *
-                                 (kTcItemIssueCycles + rps * ks * kTcMmaIssueCycles);
-            // (two partial sums cost the epilogue a second read of the accumulators and the
-            // stores carry half as many channels: measured ~10 % per unit)
-            const double unit = (std::max(tensor, issue) +
-                                 (ps >= 2 * cg ? 0.0 : static_cast<double>(cg) * plane / 64.0)) *
-                                (part > 1 ? 1.1 : 1.0);
-            const double cost = static_cast<double>((units + sms - 1) / sms) * unit;
-            if (cost < best) {
-                best = cost; best_nt = nt; best_cg = cg; best_ps = ps; best_rps = rps; best_twc = twc;
-                best_rslots = rslots;
+    int best_pair = 0;
+    const int mode = tc_row_pairs_mode();
+    for (int pair = mode == 2 ? 1 : 0; pair <= (mode == 1 ? 0 : 1); ++pair) {
+        int kimg, bands;
+        const long long row_tiles = row_layout(kTcM - pair, kimg, bands);
+        const int fhi = pair ? (p.FH + 1) / 2 : p.FH;
+        for (int nt = 1; nt <= 64; ++nt) {
+            const int twc = ((p.OW + nt - 1) / nt + 7) / 8 * 8;
+            if (nt > 1 && (p.OW + twc - 1) / twc < nt) continue;
+            const int nn = pair ? twc : (twc + 15) / 16 * 16;
+            if ((pair ? 2 * kTcIssuers * nn : nn) > kTcDCols) continue;
+            const int ks = (nn + p.FW - 1 + 15) / 16;
+            const int ncm = nn / 8 + 2 * ks - 1;
+            const size_t run = static_cast<size_t>(pair + 1) * ncm * 128;
+            const size_t plane = static_cast<size_t>(2 * ks) * a.MR * 16;
+            const long long tiles = row_tiles * ((p.OW + twc - 1) / twc);
+            for (int rps = kTcRunsPerSlot; rps >= 1; --rps)
+            for (int cg = 4; cg >= 2; cg /= 2)
+            for (int rslots = kTcRingSlots; rslots >= 2; rslots /= 2) {
+                const int part = cg >= kTcIssuers ? 1 : kTcIssuers / cg;   // partial sums
+                if (part * cg * nn > kTcDCols || p.C % cg != 0 || (part > 1 && rps > 1)) continue;
+                if (pair && cg != kTcIssuers) continue;
+                const size_t fixed = static_cast<size_t>(kTcIssuers) * rslots * rps * run + kTcBarBytes +
+                                     (pair ? kTcXBytes : 0);
+                if (fixed >= static_cast<size_t>(cap)) continue;
+                const int ps = static_cast<int>(std::min<size_t>(kTcMaxPlanes, (cap - fixed) / plane));
+                if (ps < cg + 1) continue;   // the next unit's planes must fill while one computes
+                const long long units = tiles * (p.C / cg);
+                const double tensor = cg * fhi * ks * tc_mma_cycles((pair + 1) * nn);
+                const int rows_per_issuer = (fhi + part - 1) / part;
+                const double issue = (cg * part / kTcIssuers) * ((rows_per_issuer + rps - 1) / rps) *
+                                     (kTcItemIssueCycles + rps * ks * kTcMmaIssueCycles);
+                const double epi = kTcEpiPixelCycles * kTcM * twc * (pair ? 1.1 : 1.0);
+                // (two partial sums cost the epilogue a second read of the accumulators and the
+                // stores carry half as many channels: measured ~10 % per unit)
+                const double unit = (std::max({tensor, issue, epi}) +
+                                     (ps >= 2 * cg ? 0.0 : static_cast<double>(cg) * plane / 64.0)) *
+                                    (part > 1 ? 1.1 : 1.0);
+                const double cost = static_cast<double>((units + sms - 1) / sms) * unit;
+                if (cost < best) {
+                    best = cost; best_nt = nt; best_cg = cg; best_ps = ps; best_rps = rps; best_twc = twc;
+                    best_rslots = rslots; best_pair = pair;
+                }
             }
         }
     }
     if (best_nt == 0) return false;
+    a.pair = best_pair;
+    a.mrows = kTcM - best_pair;
+    a.FHI = best_pair ? (p.FH + 1) / 2 : p.FH;
+    const long long row_tiles = row_layout(a.mrows, a.kimg, a.bands);
     a.TWc = best_twc;
-    a.NN = (a.TWc + 15) / 16 * 16;
+    a.NN = best_pair ? a.TWc : (a.TWc + 15) / 16 * 16;
     a.col_tiles = static_cast<uint32_t>((p.OW + a.TWc - 1) / a.TWc);
     a.KS = (a.NN + p.FW - 1 + 15) / 16;
     a.NCM = a.NN / 8 + 2 * a.KS - 1;
     a.plane_bytes = static_cast<uint32_t>(2 * a.KS) * a.MR * 16u;
-    a.toep_bytes = static_cast<uint32_t>(a.NCM) * 128u;
+    a.toep_bytes = static_cast<uint32_t>(a.pair + 1) * a.NCM * 128u;
     P.cg = best_cg;
+    P.pair = best_pair != 0;
     a.cbase = 0;
     a.ncg = p.C / best_cg;
     const long long tiles = row_tiles * a.col_tiles;
@@ -786,13 +943,14 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     a.x0 = P.Lp - p.pad_w;
     P.Wp = (P.Lp + p.W + 7) / 8 * 8;
     P.planes_bytes = static_cast<size_t>(p.C) * static_cast<size_t>(p.N) * a.S * P.Wp * 2;
-    P.runs_bytes = static_cast<size_t>(p.C) * p.FH * a.toep_bytes;
-    // shared memory: plane ring, run rings, barriers; one CTA per SM (each allocates all of
-    // tensor memory): ask for more than half of it
+    P.runs_bytes = static_cast<size_t>(p.C) * a.FHI * a.toep_bytes;
+    // shared memory: plane ring, run rings, barriers, the paired rows' exchange; one CTA per
+    // SM (each allocates all of tensor memory): ask for more than half of it
     const size_t toep_ring = static_cast<size_t>(kTcIssuers) * a.rslots * a.rps * a.toep_bytes;
     a.off_toep = static_cast<uint32_t>(static_cast<size_t>(a.ps) * a.plane_bytes);
     a.off_bar = a.off_toep + static_cast<uint32_t>(toep_ring);
-    P.smem = std::max<size_t>(a.off_bar + kTcBarBytes, static_cast<size_t>(cap) / 2 + 1024);
+    a.off_x = a.off_bar + kTcBarBytes;
+    P.smem = std::max<size_t>(a.off_x + (a.pair ? kTcXBytes : 0), static_cast<size_t>(cap) / 2 + 1024);
     return true;
 }
 
@@ -803,10 +961,10 @@ inline uint32_t tc_idesc(int n) {
            (static_cast<uint32_t>(kTcM >> 4) << 24);
 }
 
-// One launch of the main kernel with groups of CG channels.
-template <typename T, class OutT, int CG>
+// One launch of the main kernel with groups of CG channels (filter rows in pairs or single).
+template <typename T, class OutT, int CG, bool PAIR>
 cudaError_t launch_tc_main(const TcArgs& a, size_t smem, const CUtensorMap& xmap, cudaStream_t stream) {
-    auto kern = tc_rows_kernel<T, OutT, CG>;
+    auto kern = tc_rows_kernel<T, OutT, CG, PAIR>;
     static DeviceOnce smem_opt_in;
     const cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
     if (err != cudaSuccess) return err;
@@ -817,12 +975,12 @@ cudaError_t launch_tc_main(const TcArgs& a, size_t smem, const CUtensorMap& xmap
 }
 
 template <typename T, class OutT>
-cudaError_t launch_tc_main_cg(int cg, const TcArgs& a, size_t smem, const CUtensorMap& xmap,
+cudaError_t launch_tc_main_cg(int cg, bool pair, const TcArgs& a, size_t smem, const CUtensorMap& xmap,
                               cudaStream_t stream) {
+    if (pair) return cg == 4 ? launch_tc_main<T, OutT, 4, true>(a, smem, xmap, stream) : cudaErrorNotSupported;
     switch (cg) {
-        case 2: return launch_tc_main<T, OutT, 2>(a, smem, xmap, stream);
-        case 4: return launch_tc_main<T, OutT, 4>(a, smem, xmap, stream);
-        case 8: return launch_tc_main<T, OutT, 8>(a, smem, xmap, stream);
+        case 2: return launch_tc_main<T, OutT, 2, false>(a, smem, xmap, stream);
+        case 4: return launch_tc_main<T, OutT, 4, false>(a, smem, xmap, stream);
         default: return cudaErrorNotSupported;
     }
 }
@@ -857,11 +1015,12 @@ cudaError_t launch_tc_rows(const RowConv& p) {
     q.x = p.in; q.w = p.w; q.planes = base; q.runs = base + runs_off;
     q.N = p.N; q.H = p.H; q.W = p.W; q.C = p.C; q.FH = p.FH; q.FW = p.FW; q.pad_h = p.pad_h;
     q.S = a.S; q.Lp = P.Lp; q.Wp = P.Wp; q.NN = a.NN; q.NCM = a.NCM;
+    q.FHI = a.FHI; q.pair = a.pair;
     q.CT = p.C % 64 == 0 ? 64 : (p.C % 32 == 0 ? 32 : (p.C % 16 == 0 ? 16 : 8));
     q.piece_shift = q.CT == 64 ? 3 : (q.CT == 32 ? 2 : (q.CT == 16 ? 1 : 0));
     const long long xtiles = (P.Wp + kTcPrepCols - 1) / kTcPrepCols;
     const long long plane_tiles = V * (p.C / q.CT) * xtiles;
-    const long long run_tasks = static_cast<long long>(p.C) * p.FH * 8 * a.NCM;
+    const long long run_tasks = static_cast<long long>(p.C) * a.FHI * 8 * a.NCM * (a.pair + 1);
     if (V >= (1LL << 31) || plane_tiles >= (1LL << 31) || run_tasks >= (1LL << 31)) {
         scratch_free(scratch, p.stream);
         return cudaErrorNotSupported;
@@ -873,7 +1032,7 @@ cudaError_t launch_tc_rows(const RowConv& p) {
     q.fd_ct.init(static_cast<uint32_t>(p.C / q.CT));
     q.fd_S.init(static_cast<uint32_t>(a.S));
     q.fd_C.init(static_cast<uint32_t>(p.C));
-    q.fd_rows.init(static_cast<uint32_t>(8 * a.NCM));
+    q.fd_rows.init(static_cast<uint32_t>(8 * a.NCM * (a.pair + 1)));
     const int sms = device_info().sm_count;
     q.run_blocks = static_cast<int>(
         std::min<long long>((run_tasks + kTcPrepThreads - 1) / kTcPrepThreads, 4LL * sms));
@@ -888,8 +1047,8 @@ cudaError_t launch_tc_rows(const RowConv& p) {
     m.out = p.out;
     m.status = p.status;
     m.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
-    m.idesc = tc_idesc<T>(a.NN);
-    if (err == cudaSuccess) err = launch_tc_main_cg<T, OutT>(P.cg, m, P.smem, xmap, p.stream);
+    m.idesc = tc_idesc<T>(a.NN * (a.pair + 1));
+    if (err == cudaSuccess) err = launch_tc_main_cg<T, OutT>(P.cg, P.pair, m, P.smem, xmap, p.stream);
     // stream-ordered: the memory returns to the pool once the kernels have run
     scratch_free(scratch, p.stream);
     return err;

@@ -1,5 +1,6 @@
 /*
- * dwc_testing.h -- fault injection for tests of libdwc_gb300.so's failure path.
+ * dwc_testing.h -- fault injection for tests of libdwc_gb300.so's failure path, and kernel
+ * selection for tests that run every kernel on the same shapes.
  *
  * No counterpart in the paper.  The injected failure is made on the host side and involves
  * no GPU fault: a kernel is told not to issue some of its own input copies, so its compute
@@ -30,6 +31,14 @@ void dwc_testing_stall_next_row_launch(void);
  * compare them.  Returns the previous preference, or -1 (nothing changed) for an unknown
  * family.  Not for production use. */
 int dwc_testing_prefer_family(int family);
+
+/* Filter rows per MMA of the tcgen05 kernel for the calls made from now on: 0 = the launch
+ * plan's choice (the default), 1 = one filter row per MMA, 2 = two filter rows per MMA (the
+ * paired-row form: one MMA of twice the width against the same input rows).  A shape the
+ * forced form cannot run takes another kernel.  Lets tests run both forms of the kernel on
+ * the same shapes.  Returns the previous mode, or -1 (nothing changed) for an unknown mode.
+ * Not for production use. */
+int dwc_testing_tc_row_pairs(int mode);
 
 #ifdef __cplusplus
 }

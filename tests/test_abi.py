@@ -189,7 +189,11 @@ def test_path_selection_host_logic(lib):
     assert p(0, **dict(big, W=27, FH=9, FW=9, pad=4), dtype=1) == 1
     assert p(0, **dict(big, W=17), dtype=1) == 2
     assert p(0, **dict(big, W=16), dtype=1) == 1          # narrow rows: row-streaming kernel
-    # small maps stay on the small-map kernel (14 x 14 and 7 x 7, large filters)
+    # 14 x 14 maps: tcgen05 from 13 taps on large batches of channel planes
+    l14 = dict(N=64, H=14, W=14, C=512, dtype=1)
+    assert p(0, **l14, FH=13, FW=13, pad=6) == 2 and p(1, **l14, FH=31, FW=31, pad=15) == 2
+    assert p(0, **l14, FH=9, FW=9, pad=4) != 2
+    # small maps stay on the small-map kernel (14 x 14 with few planes, and 7 x 7)
     m14 = dict(H=14, W=14, C=64, dtype=1)
     assert p(0, **m14, FH=31, FW=31, pad=15) == 3 and p(1, **m14, FH=31, FW=31, pad=15) == 3
     assert p(0, **m14, FH=13, FW=13, pad=6) == 3

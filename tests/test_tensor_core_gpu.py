@@ -3,8 +3,9 @@ fp64 oracle, with the kernel family forced (dwc_testing_prefer_family) so that e
 below runs on the kernel under test, whatever the automatic choice would be.
 
 The tcgen05 kernel (family 2) tiles 128 virtual output rows that run through several
-images, N output columns per column tile, groups of 2, 4 or 8 channels and ring items of 1
-to 4 filter rows; the cases cover
+images, N output columns per column tile, groups of 2 or 4 channels and ring items of 1
+to 4 filter rows, with one filter row per MMA or two (dwc_testing_tc_row_pairs: every case
+runs in both forms); the cases cover
 several images per tile, tall images cut into 128-row bands, several column tiles, stripe
 filters, filters from 1 to 51 taps, pads from 0 to beyond (F-1)/2, channel counts that take
 every channel-group size, and both output types.  The warp-level MMA kernel (family 4) keeps
@@ -29,6 +30,7 @@ def lib():
     lib = dwc.load_library()
     yield lib
     assert lib.dwc_testing_prefer_family(0) >= 0
+    assert lib.dwc_testing_tc_row_pairs(0) >= 0
 
 
 def C_(N, H, W, C, F, p=None, FW=None, seed=31):
@@ -51,13 +53,16 @@ TC_CASES = [
     C_(1, 12, 30, 8, 7, FW=21, p=3),  # stripe filters
     C_(1, 40, 24, 16, 31, FW=5, p=2),
     C_(1, 13, 50, 8, 1, FW=13, p=0),
-    C_(3, 7, 7, 40, 31),              # channel groups of 8 (40 channels), map below filter
+    C_(3, 7, 7, 40, 31),              # 40 channels, map below the filter
     C_(2, 56, 56, 16, 31),            # the large-kernel stage shape, few channels
     C_(1, 1, 1, 8, 3),                # single pixel
     # groups of 4 channels with ring items of 3 or 4 filter rows, the last item shorter
     C_(8, 28, 28, 64, 13),            # items of 4 rows (13 = 3 x 4 + 1)
     C_(8, 56, 56, 64, 17),            # items of 3 rows (17 = 5 x 3 + 2)
     C_(16, 30, 40, 64, 11),           # items of 4 rows, N = 48 columns
+    # even filter heights (stripe filters): the last pair of filter rows is full
+    C_(2, 20, 30, 16, 8, FW=9, p=4),
+    C_(1, 33, 40, 8, 12, FW=5, p=2),
 ]
 
 
@@ -69,8 +74,9 @@ def oracle_pair(case, name, x, w, dy):
             oracle.bwd_data(np.abs(dy), np.abs(w), (case.H, case.W), s, p))
 
 
-def run_family(lib, family, case, out16=False):
+def run_family(lib, family, case, out16=False, pairs=0):
     prev = lib.dwc_testing_prefer_family(family)
+    prev_pairs = lib.dwc_testing_tc_row_pairs(pairs)
     try:
         args = (case.N, case.H, case.W, case.C, case.FH, case.FW, case.stride, case.pad,
                 CODE[case.dtype])
@@ -83,15 +89,20 @@ def run_family(lib, family, case, out16=False):
         torch.cuda.synchronize()
     finally:
         lib.dwc_testing_prefer_family(prev)
+        lib.dwc_testing_tc_row_pairs(prev_pairs)
     assert dwc.device_status() == 0
     return fams, x, w, dy, {"fwd": y, "bwd_data": dx}
 
 
+ROWS = {1: "single_rows", 2: "row_pairs"}
+
+
+@pytest.mark.parametrize("pairs", [1, 2], ids=ROWS.get)
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("case", TC_CASES, ids=lambda c: f"n{c.N}_{c.H}x{c.W}_c{c.C}_f{c.FH}x{c.FW}_p{c.pad}")
-def test_tcgen05_kernel_full_tensors(lib, case, dtype):
+def test_tcgen05_kernel_full_tensors(lib, case, dtype, pairs):
     case = Case(**{**case.__dict__, "dtype": dtype})
-    fams, x, w, dy, got = run_family(lib, 2, case)
+    fams, x, w, dy, got = run_family(lib, 2, case, pairs=pairs)
     assert fams == [2, 2], fams
     xn, wn, dyn = (t.double().numpy() for t in (x, w, dy))
     for name, g in got.items():
@@ -100,13 +111,14 @@ def test_tcgen05_kernel_full_tensors(lib, case, dtype):
         assert err <= TOL[dtype], f"{name} {case}: normalized error {err:.3e}"
 
 
+@pytest.mark.parametrize("pairs", [1, 2], ids=ROWS.get)
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("case", [TC_CASES[1], TC_CASES[3], TC_CASES[6], TC_CASES[11]],
                          ids=lambda c: f"n{c.N}_{c.H}x{c.W}_c{c.C}_f{c.FH}x{c.FW}")
-def test_tcgen05_kernel_16bit_outputs_are_the_fp32_outputs_rounded(lib, case, dtype):
+def test_tcgen05_kernel_16bit_outputs_are_the_fp32_outputs_rounded(lib, case, dtype, pairs):
     case = Case(**{**case.__dict__, "dtype": dtype})
-    _, _, _, _, g16 = run_family(lib, 2, case, out16=True)
-    _, _, _, _, g32 = run_family(lib, 2, case)
+    _, _, _, _, g16 = run_family(lib, 2, case, out16=True, pairs=pairs)
+    _, _, _, _, g32 = run_family(lib, 2, case, pairs=pairs)
     for name in g16:
         assert g16[name].dtype == case.x().dtype
         assert torch.equal(g16[name].cpu(), g32[name].cpu().to(g16[name].dtype)), name
@@ -161,6 +173,9 @@ def test_family_preference_rejects_unknown_families(lib):
     assert lib.dwc_testing_prefer_family(7) == -1
     assert lib.dwc_testing_prefer_family(3) == -1
     assert lib.dwc_testing_prefer_family(0) == 0
+    assert lib.dwc_testing_tc_row_pairs(3) == -1
+    assert lib.dwc_testing_tc_row_pairs(-1) == -1
+    assert lib.dwc_testing_tc_row_pairs(0) == 0
 
 
 def test_tcgen05_call_inside_a_cuda_graph(lib):
