@@ -8,7 +8,8 @@ as described in depthwise_convolution_nhwc_gb300/inputs.py.
 
 Prints ONE JSON line (rank 0).  `value` is device-timed throughput with inputs resident in
 HBM (CUDA events on the launching stream around each step, L2 flushed between steps by a
-256 MiB write that is not timed); `e2e` is the same metric through the C ABI with the inputs
+256 MiB write that is not timed, then an untimed device-side spin so that the step's launches
+are all enqueued before its first event is reached); `e2e` is the same metric through the C ABI with the inputs
 copied from pinned host memory and the outputs copied back inside the timed region.
 `--impl reference` times the fp64 CPU oracle on bounded samples of the same workload.
 """
@@ -28,6 +29,14 @@ sys.path.insert(0, ROOT)
 
 METRIC = "DWC fwd+bwd TFLOP/s and GB/s on 1 GB300, % of roofline, per filter size"
 PASSES_ALL = ("fwd", "bwd_data", "bwd_filter")
+# Device-side spin (untimed) between the L2 flush and each timed window: the host enqueues the
+# timed launches while the GPU is still busy, so no host-side launch gap falls inside the
+# window (a pass of a few microseconds is shorter than a call's host-side cost).
+HOLD_CYCLES = 400_000
+
+
+def hold_device(torch):
+    torch.cuda._sleep(HOLD_CYCLES)
 PASS_CODE = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2, "fwd_bn_act": 3}
 DTYPE_CODE = {"f32": 0, "bf16": 1, "f16": 2}
 FAMILY = {0: "general", 1: "cuda-core", 2: "tensor-core", 3: "small-map", 4: "tensor-core"}
@@ -273,6 +282,7 @@ def config_dict(case, passes):
             "stride": case.stride, "pad": case.pad, "input_dtype": case.dtype,
             "output_dtype": "f32", "layout": "NHWC / FHxFWxC",
             "l2": "flushed between timed steps by an untimed 256 MiB write",
+            "hold": f"untimed device spin of {HOLD_CYCLES} cycles before each timed window",
             "inputs": f"{case.dist} draws, seed {case.seed}"}
 
 
@@ -472,6 +482,7 @@ def per_filter_table(args, dev, peaks):
                 evs = []
                 for k in range(args.per_filter_steps):
                     flush.fill_(float(k))
+                    hold_device(torch)
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
@@ -491,7 +502,7 @@ def per_filter_table(args, dev, peaks):
         raise SystemExit("a kernel reported a timed-out wait in the per-filter table")
     return {"workload": f"N={N} {H}x{W} C={C}, F x F filters, pad (F-1)/2, stride 1",
             "timing": f"mean of {args.per_filter_steps} launches per pass, L2 flushed before "
-                      "each, CUDA events",
+                      "each (then an untimed device spin), CUDA events",
             "frac": "roofline fraction of the pass (hbm: compulsory bytes at the measured HBM "
                     "copy rate; alu: valid FLOPs at the measured fp32x2 FMA rate; tensor: "
                     "valid FLOPs at the measured bf16 peak)",
@@ -672,6 +683,7 @@ def run_sweep(args):
             evs = []
             for k in range(args.sweep_steps):
                 flush.fill_(float(k))
+                hold_device(torch)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 run[name]()
@@ -699,7 +711,8 @@ def write_sweep_md(args, rows):
     out = [f"# Filter sweep, every pass, one GB300\n",
            f"Command: `{cmd}`\n",
            f"Mean device time of {args.sweep_steps} launches per pass (CUDA events on the "
-           "launching stream, 256 MiB L2 flush before each launch, 3 warm-up launches). "
+           "launching stream, 256 MiB L2 flush and an untimed device spin before each launch, "
+           "3 warm-up launches). "
            "TFLOP/s are nominal (2·N·OH·OW·C·FH·FW); roofline fraction against the bound "
            "named (hbm: compulsory bytes at the measured HBM copy rate; alu: valid FLOPs at "
            "the fp32x2 FMA rate measured in the same run; tensor: valid FLOPs at the measured "
@@ -773,6 +786,7 @@ def run_ours(args, case, passes):
         t_wall0 = time.time()
         for k in range(args.steps):
             flush.fill_(float(k))
+            hold_device(torch)
             ev[k][0].record(stream)
             for j, name in enumerate(passes):
                 run_pass(name, x, w, dy)

@@ -606,10 +606,229 @@ cudaError_t launch_small_fgrad_inst(const FilterGrad& p) {
     return launch_reduce_slices(p.workspace, Z, count, p.dw + a.fh_lo * row, p.stream);
 }
 
+
+// ------------------------------------------------------------------ 7 x 7 maps, 3 to 7 taps
+// The last stage of the networks the pages evaluate ("Flash-DWC", §6.3: 7 x 7 maps, "same"
+// padding) has little independent work: one 49-pixel plane per (image, channel).  A warp per
+// image and lane per channel (the kernels above) leaves 8 warps on an SM and spends most of its
+// instructions assembling column pairs.  Here a thread owns a channel PAIR of one image
+// (consecutive lanes, consecutive pairs: 8-byte loads and stores coalesce across the warp),
+// every packed FMA takes both channels at once (no pair assembly), and every loop is
+// unrolled for the fixed map and filter, so only the taps that meet the image are issued:
+// 37 x 37 of the 49 x 49 products per pixel plane at 7 taps.
+//  * forward / backward data: the thread's 49 input pairs sit in registers (loaded at once:
+//    one memory latency), the filter rows come from L1; the two warps of a CTA take the even
+//    and the odd output rows of the same 32 channel pairs of an image;
+//  * filter gradient: the two warps of a CTA take the even and the odd filter rows; each
+//    thread accumulates its dw rows in registers over a range of images (the input image in
+//    registers, one output-gradient row at a time) and writes them to a slice of the
+//    workspace; the slices are summed afterwards in a fixed order.
+constexpr int kTinyMap = 7;
+constexpr int kTinyPairs = 32;   // channel pairs per CTA (one per lane)
+
+inline bool tiny_shape(int H, int W, int OH, int OW, int FH, int FW, int pad_h, int pad_w) {
+    return H == kTinyMap && W == kTinyMap && OH == kTinyMap && OW == kTinyMap && FH == FW &&
+           (FH == 3 || FH == 5 || FH == 7) && pad_h == (FH - 1) / 2 && pad_w == (FW - 1) / 2;
+}
+
+struct TinyArgs {
+    const void* in;     // N x 7 x 7 x C
+    const void* w;      // F x F x C
+    void* out;          // N x 7 x 7 x C, OutT
+    int N, C, flip;
+    int cblocks;        // blocks of 32 channel pairs
+};
+
+// Output rows oh = PART, PART + 2, ... of one image and channel pair.
+template <typename T, int F, class OutT, int PART>
+__device__ __forceinline__ void tiny_rows_part(const T* __restrict__ X, const T* __restrict__ Wt,
+                                               OutT* __restrict__ O, int C, bool flip) {
+    constexpr int M = kTinyMap, P = (F - 1) / 2;
+    float2 x[M][M];
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+#pragma unroll
+        for (int j = 0; j < M; ++j) x[i][j] = Elem<T>::load_pair(X + static_cast<size_t>(i * M + j) * C);
+#pragma unroll
+    for (int oh = PART; oh < M; oh += 2) {
+        float2 acc[M];
+#pragma unroll
+        for (int ow = 0; ow < M; ++ow) acc[ow] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int fh = 0; fh < F; ++fh) {
+            const int ih = oh + fh - P;
+            if (ih < 0 || ih >= M) continue;
+            const int sh = flip ? F - 1 - fh : fh;   // backward data: the filter rotated by 180
+            float2 wr[F];
+#pragma unroll
+            for (int fw = 0; fw < F; ++fw)
+                wr[fw] = Elem<T>::load_pair(Wt + static_cast<size_t>(sh * F + (flip ? F - 1 - fw : fw)) * C);
+#pragma unroll
+            for (int fw = 0; fw < F; ++fw)
+#pragma unroll
+                for (int ow = 0; ow < M; ++ow) {
+                    const int iw = ow + fw - P;
+                    if (iw < 0 || iw >= M) continue;
+                    fma2(acc[ow], x[ih][iw], wr[fw]);
+                }
+        }
+#pragma unroll
+        for (int ow = 0; ow < M; ++ow) store_out_pair(O + static_cast<size_t>(oh * M + ow) * C, acc[ow]);
+    }
+}
+
+// Grid: cblocks x N CTAs of 2 warps (even / odd output rows).
+template <typename T, int F, class OutT>
+__global__ void __launch_bounds__(64) tiny_rows_kernel(const TinyArgs a) {
+    const int lane = threadIdx.x & 31, part = threadIdx.x >> 5;
+    const int cb = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.cblocks));
+    const int n = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.cblocks));
+    const int c = 2 * (cb * kTinyPairs + lane);
+    if (n >= a.N || c >= a.C) return;
+    const size_t img = static_cast<size_t>(n) * kTinyMap * kTinyMap * a.C + c;
+    const T* X = static_cast<const T*>(a.in) + img;
+    const T* Wt = static_cast<const T*>(a.w) + c;
+    OutT* O = static_cast<OutT*>(a.out) + img;
+    if (part == 0) tiny_rows_part<T, F, OutT, 0>(X, Wt, O, a.C, a.flip != 0);
+    else tiny_rows_part<T, F, OutT, 1>(X, Wt, O, a.C, a.flip != 0);
+}
+
+template <typename T, class OutT>
+cudaError_t launch_tiny_rows(const RowConv& p) {
+    TinyArgs a;
+    a.in = p.in; a.w = p.w; a.out = p.out;
+    a.N = p.N; a.C = p.C; a.flip = p.flip ? 1 : 0;
+    a.cblocks = (p.C / 2 + kTinyPairs - 1) / kTinyPairs;
+    const long long grid = static_cast<long long>(a.cblocks) * p.N;
+    if (grid == 0) return cudaSuccess;
+    if (grid >= (1LL << 31) || p.C % 2 != 0) return cudaErrorNotSupported;
+    const unsigned g = static_cast<unsigned>(grid);
+    switch (p.FH) {
+        case 3: tiny_rows_kernel<T, 3, OutT><<<g, 64, 0, p.stream>>>(a); break;
+        case 5: tiny_rows_kernel<T, 5, OutT><<<g, 64, 0, p.stream>>>(a); break;
+        case 7: tiny_rows_kernel<T, 7, OutT><<<g, 64, 0, p.stream>>>(a); break;
+        default: return cudaErrorNotSupported;
+    }
+    return cudaGetLastError();
+}
+
+struct TinyFgArgs {
+    const void* x;      // N x 7 x 7 x C
+    const void* dy;     // N x 7 x 7 x C
+    float* ws;          // Z slices of F x F x C
+    int N, C;
+    int ipb;            // images per CTA (slice)
+    int cblocks;
+};
+
+// Filter rows fh = PART, PART + 2, ... of one channel pair, summed over images [n0, n1).
+template <typename T, int F, int PART>
+__device__ __forceinline__ void tiny_fgrad_part(const T* __restrict__ X, const T* __restrict__ D,
+                                                float* __restrict__ out, int C, int n0, int n1) {
+    constexpr int M = kTinyMap, P = (F - 1) / 2, NR = (F - PART + 1) / 2;
+    float2 acc[NR][F];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int fw = 0; fw < F; ++fw) acc[r][fw] = make_float2(0.f, 0.f);
+    const size_t img = static_cast<size_t>(M) * M * C;
+    for (int n = n0; n < n1; ++n) {
+        const T* Xn = X + static_cast<size_t>(n) * img;
+        const T* Dn = D + static_cast<size_t>(n) * img;
+        float2 x[M][M];
+#pragma unroll
+        for (int i = 0; i < M; ++i)
+#pragma unroll
+            for (int j = 0; j < M; ++j) x[i][j] = Elem<T>::load_pair(Xn + static_cast<size_t>(i * M + j) * C);
+#pragma unroll
+        for (int oh = 0; oh < M; ++oh) {
+            float2 d[M];
+#pragma unroll
+            for (int ow = 0; ow < M; ++ow) d[ow] = Elem<T>::load_pair(Dn + static_cast<size_t>(oh * M + ow) * C);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const int ih = oh + PART + 2 * r - P;
+                if (ih < 0 || ih >= M) continue;
+#pragma unroll
+                for (int fw = 0; fw < F; ++fw)
+#pragma unroll
+                    for (int ow = 0; ow < M; ++ow) {
+                        const int iw = ow + fw - P;
+                        if (iw < 0 || iw >= M) continue;
+                        fma2(acc[r][fw], x[ih][iw], d[ow]);
+                    }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int fw = 0; fw < F; ++fw)
+            *reinterpret_cast<float2*>(out + static_cast<size_t>((PART + 2 * r) * F + fw) * C) = acc[r][fw];
+}
+
+// Grid: cblocks x Z CTAs of 2 warps (even / odd filter rows); slice z covers images
+// [z * ipb, (z + 1) * ipb).
+template <typename T, int F>
+__global__ void __launch_bounds__(64) tiny_fgrad_kernel(const TinyFgArgs a) {
+    const int lane = threadIdx.x & 31, part = threadIdx.x >> 5;
+    const int cb = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.cblocks));
+    const int z = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.cblocks));
+    const int c = 2 * (cb * kTinyPairs + lane);
+    if (c >= a.C) return;
+    const int n0 = z * a.ipb, n1 = min(a.N, n0 + a.ipb);
+    const T* X = static_cast<const T*>(a.x) + c;
+    const T* D = static_cast<const T*>(a.dy) + c;
+    float* out = a.ws + static_cast<size_t>(z) * F * F * a.C + c;
+    if (part == 0) tiny_fgrad_part<T, F, 0>(X, D, out, a.C, n0, n1);
+    else tiny_fgrad_part<T, F, 1>(X, D, out, a.C, n0, n1);
+}
+
+// Images per slice: enough CTAs for about four per SM.
+inline int tiny_fgrad_ipb(int N, int C) {
+    const long long cblocks = (C / 2 + kTinyPairs - 1) / kTinyPairs;
+    const long long want = 4LL * device_info().sm_count;
+    const long long z = std::max(1LL, std::min<long long>(N, want / std::max(1LL, cblocks)));
+    return static_cast<int>((N + z - 1) / z);
+}
+
+inline size_t tiny_fgrad_workspace_floats(int N, int C, int F) {
+    if (N <= 0) return 0;
+    const int ipb = tiny_fgrad_ipb(N, C);
+    return static_cast<size_t>((N + ipb - 1) / ipb) * F * F * C;
+}
+
+template <typename T>
+cudaError_t launch_tiny_fgrad(const FilterGrad& p) {
+    TinyFgArgs a;
+    a.x = p.x; a.dy = p.dy;
+    a.N = p.N; a.C = p.C;
+    a.ipb = tiny_fgrad_ipb(p.N, p.C);
+    a.cblocks = (p.C / 2 + kTinyPairs - 1) / kTinyPairs;
+    const int Z = (p.N + a.ipb - 1) / a.ipb;
+    const size_t count = static_cast<size_t>(p.FH) * p.FW * p.C;
+    if (p.workspace == nullptr || p.workspace_floats < static_cast<size_t>(Z) * count) return cudaErrorInvalidValue;
+    a.ws = p.workspace;
+    const long long grid = static_cast<long long>(a.cblocks) * Z;
+    if (grid >= (1LL << 31) || p.C % 2 != 0) return cudaErrorNotSupported;
+    const unsigned g = static_cast<unsigned>(grid);
+    switch (p.FH) {
+        case 3: tiny_fgrad_kernel<T, 3><<<g, 64, 0, p.stream>>>(a); break;
+        case 5: tiny_fgrad_kernel<T, 5><<<g, 64, 0, p.stream>>>(a); break;
+        case 7: tiny_fgrad_kernel<T, 7><<<g, 64, 0, p.stream>>>(a); break;
+        default: return cudaErrorNotSupported;
+    }
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_reduce_slices(p.workspace, Z, count, p.dw, p.stream);
+}
+
+
 #define DWC_SMALL_SHAPES(X) X(8, 3) X(8, 7) X(16, 3) X(16, 7) X(16, 11) X(16, 15)
 
 template <typename T>
 size_t small_fgrad_workspace_t(int N, int H, int W, int C, int OH, int OW, int FH, int FW, int pad) {
+    if (tiny_shape(H, W, OH, OW, FH, FW, pad, pad)) return tiny_fgrad_workspace_floats(N, C, FH);
     int maxw = 0, dr = 0;
     if (!small_fgrad_wanted(W, OW, FW) || !small_shape(H, W, OH, OW, FW, pad, maxw, dr)) return 0;
     SmallFgArgs a;
@@ -628,6 +847,7 @@ size_t small_fgrad_workspace_t(int N, int H, int W, int C, int OH, int OW, int F
 
 template <typename T, class OutT = float>
 cudaError_t launch_small_rows_t(const RowConv& p) {
+    if (tiny_shape(p.H, p.W, p.OH, p.OW, p.FH, p.FW, p.pad_h, p.pad_w)) return launch_tiny_rows<T, OutT>(p);
     int maxw = 0, dr = 0;
     if (!small_rows_wanted(p.W, p.OW, p.FW) || !small_shape(p.H, p.W, p.OH, p.OW, p.FW, p.pad_w, maxw, dr))
         return cudaErrorNotSupported;
@@ -640,6 +860,7 @@ cudaError_t launch_small_rows_t(const RowConv& p) {
 
 template <typename T>
 cudaError_t launch_small_fgrad_t(const FilterGrad& p) {
+    if (tiny_shape(p.H, p.W, p.OH, p.OW, p.FH, p.FW, p.pad, p.pad)) return launch_tiny_fgrad<T>(p);
     int maxw = 0, dr = 0;
     if (!small_fgrad_wanted(p.W, p.OW, p.FW) || !small_shape(p.H, p.W, p.OH, p.OW, p.FW, p.pad, maxw, dr))
         return cudaErrorNotSupported;

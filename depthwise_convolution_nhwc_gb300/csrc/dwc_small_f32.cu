@@ -10,6 +10,7 @@ size_t small_fgrad_workspace_floats_f32(int N, int H, int W, int C, int OH, int 
 }
 
 bool small_map_serves(int H, int W, int OH, int OW, int FW, int pad_w) {
+    if (tiny_shape(H, W, OH, OW, FW, FW, pad_w, pad_w)) return true;
     int maxw = 0, dr = 0;
     return small_rows_wanted(W, OW, FW) && small_shape(H, W, OH, OW, FW, pad_w, maxw, dr);
 }

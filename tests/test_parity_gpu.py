@@ -105,6 +105,13 @@ FAST = [
     C_(8, 8, 8, 96, 31),            # warp per image with the largest window of 8-wide maps
     C_(4, 8, 6, 32, 5),
     C_(2, 16, 16, 24, 9),
+    # 7 x 7 maps with 3 to 7 taps and "same" padding (a thread per image and channel pair):
+    # a channel tail inside one block of 32 pairs, image slices of the filter gradient with a
+    # short last slice, and another padding (not that kernel)
+    C_(3, 7, 7, 40, 3),
+    C_(2, 7, 7, 64, 5),
+    C_(77, 7, 7, 1024, 5),
+    C_(2, 7, 7, 64, 5, p=1),
 ]
 
 
