@@ -40,7 +40,7 @@ def hold_device(torch):
 PASS_CODE = {"fwd": 0, "bwd_data": 1, "bwd_filter": 2, "fwd_bn_act": 3}
 DTYPE_CODE = {"f32": 0, "bf16": 1, "f16": 2}
 FAMILY = {0: "general", 1: "cuda-core", 2: "tensor-core", 3: "small-map", 4: "tensor-core"}
-TENSOR_FAMILIES = (2, 4)   # tcgen05 (forward / backward data) or warp-level MMA kernels
+TENSOR_FAMILIES = (2, 4)   # tcgen05 or warp-level MMA kernels
 # kernels per pass and family (the library's dwc_path tells which family serves a call)
 KERNEL_NAMES = {
     ("fwd", 0): "general_fwd_kernel", ("bwd_data", 0): "general_bwd_data_kernel",
@@ -48,7 +48,8 @@ KERNEL_NAMES = {
     ("fwd", 1): "rows_kernel<flip=false>", ("bwd_data", 1): "rows_kernel<flip=true>",
     ("bwd_filter", 1): "fgrad_kernel + reduce_slices_kernel",
     ("fwd", 2): "tc_prep_kernel + tc_rows_kernel", ("bwd_data", 2): "tc_prep_kernel + tc_rows_kernel",
-    ("bwd_filter", 2): "mma_fgrad_kernel + reduce_slices_kernel",
+    ("bwd_filter", 2): "tc_stack_pm_kernel + tc_fgrad_kernel",
+    ("bwd_filter", 4): "mma_fgrad_kernel + reduce_slices_kernel",
     ("fwd", 4): "mma_rows_kernel<flip=false>", ("bwd_data", 4): "mma_rows_kernel<flip=true>",
     ("fwd", 3): "small_rows_kernel", ("bwd_data", 3): "small_rows_kernel",
     ("bwd_filter", 3): "small_fgrad_kernel + reduce_slices_kernel",

@@ -582,7 +582,15 @@ int dwc_path(int pass, const void* a, const void* b, const void* out, int N, int
     if (pass == kPassBwdFilter) {
         if (fast_fgrad_floats(P) == 0) return 0;
         if (small_fgrad_floats(P) > 0) return 3;
-        return P.e == 2 && FH == FW && tensor_core_fgrad(N, C, P.OH, P.OW, FH, FW) ? 2 : 1;
+        if (P.e == 2 && FH == FW) {
+            FilterGrad fg{};
+            fg.N = N; fg.H = H; fg.W = W; fg.C = C; fg.OH = P.OH; fg.OW = P.OW;
+            fg.FH = FH; fg.FW = FW; fg.pad = pad; fg.dtype = P.dtype;
+            const int pref = family_preference();
+            if (tc_fgrad_taken(fg)) return 2;
+            if ((pref == 0 || pref == 4) && tensor_core_fgrad(N, C, P.OH, P.OW, FH, FW)) return 4;
+        }
+        return 1;
     }
     const bool pref16 = P.e == 2 && family_preference() != 0;
     // the same RowConv the entry points build (backward data: over dy, output H x W)
@@ -611,8 +619,18 @@ int dwc_kernel_launches(int pass, int N, int H, int W, int C, int FH, int FW, in
                                                : static_cast<long long>(N) * P.OH * P.OW * C;
     if (out == 0) return 0;
     // filter gradients: the kernel and the fixed-order sum of its slices (or a fill of dW
-    // with zeros when nothing meets it: a memset, not a kernel of this library)
-    if (pass == kPassBwdFilter) return N == 0 ? 0 : 2;
+    // with zeros when nothing meets it: a memset, not a kernel of this library); the tcgen05
+    // filter gradient: the stacked copies of x and dy, then the kernel
+    if (pass == kPassBwdFilter) {
+        if (N == 0) return 0;
+        if (fam == 2) {
+            FilterGrad fg{};
+            fg.N = N; fg.H = H; fg.W = W; fg.C = C; fg.OH = P.OH; fg.OW = P.OW;
+            fg.FH = FH; fg.FW = FW; fg.pad = pad; fg.dtype = P.dtype;
+            if (tc_fgrad_taken(fg)) return 3;
+        }
+        return 2;
+    }
     if (pass == 3) return 1;
     if (fam == 2) {
         const RowConv rc = pass == kPassFwd

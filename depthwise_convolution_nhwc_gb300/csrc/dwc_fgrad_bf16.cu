@@ -5,10 +5,25 @@
 namespace dwc {
 cudaError_t launch_filter_grad_bf16(const FilterGrad& p) {
     if (p.FH != p.FW) return launch_fgrad_stripe_bf16(p);
-    // tensor-core kernel where it serves the shape, CUDA-core kernel otherwise
-    const cudaError_t err = launch_mma_fgrad<__nv_bfloat16>(p);
-    if (err != cudaErrorNotSupported) return err;
+    // tensor-core kernels where they serve the shape (tcgen05 first, then the warp-level
+    // MMA kernel), the CUDA-core kernel otherwise; a family preference picks one of them
+    const int pref = family_preference();
+    if (tc_fgrad_taken(p)) {
+        const cudaError_t err = launch_tc_fgrad_bf16(p);
+        if (err != cudaErrorNotSupported) return err;
+    }
+    if (pref == 0 || pref == 4) {
+        const cudaError_t err = launch_mma_fgrad<__nv_bfloat16>(p);
+        if (err != cudaErrorNotSupported) return err;
+    }
     return launch_fgrad_dispatch<__nv_bfloat16>(p);
+}
+
+bool tc_fgrad_taken(const FilterGrad& p) {
+    if (p.FH != p.FW || (p.dtype != kBF16 && p.dtype != kF16)) return false;
+    const int pref = family_preference();
+    if (pref != 0 && pref != 2) return false;
+    return (pref == 2 || tc_fgrad_wanted(p.FW, p.OW)) && tc_fgrad_fits(p);
 }
 
 bool tensor_core_fgrad(int N, int C, int OH, int OW, int FH, int FW) {

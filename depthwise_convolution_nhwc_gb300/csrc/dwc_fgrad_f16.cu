@@ -5,9 +5,17 @@
 namespace dwc {
 cudaError_t launch_filter_grad_f16(const FilterGrad& p) {
     if (p.FH != p.FW) return launch_fgrad_stripe_f16(p);
-    // tensor-core kernel where it serves the shape, CUDA-core kernel otherwise
-    const cudaError_t err = launch_mma_fgrad<__half>(p);
-    if (err != cudaErrorNotSupported) return err;
+    // tensor-core kernels where they serve the shape (tcgen05 first, then the warp-level
+    // MMA kernel), the CUDA-core kernel otherwise; a family preference picks one of them
+    const int pref = family_preference();
+    if (tc_fgrad_taken(p)) {
+        const cudaError_t err = launch_tc_fgrad_f16(p);
+        if (err != cudaErrorNotSupported) return err;
+    }
+    if (pref == 0 || pref == 4) {
+        const cudaError_t err = launch_mma_fgrad<__half>(p);
+        if (err != cudaErrorNotSupported) return err;
+    }
     return launch_fgrad_dispatch<__half>(p);
 }
 

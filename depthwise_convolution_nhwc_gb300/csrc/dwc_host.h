@@ -222,13 +222,28 @@ inline bool tc_rows_preferred(const RowConv& p) {
 enum KernelFamily { kFamilyGeneral = 0, kFamilyCudaCore = 1, kFamilyTcgen05 = 2, kFamilySmall = 3,
                     kFamilyMmaSync = 4 };
 int tensor_core_rows(const RowConv& p);
-// Family preference for 16-bit forward / backward-data calls (tests and kernel comparisons;
-// 0 = automatic choice), set through dwc_testing_prefer_family.
+// Family preference for 16-bit forward / backward-data calls and filter gradients (tests and
+// kernel comparisons; 0 = automatic choice), set through dwc_testing_prefer_family.
 int family_preference();
 // Filter rows per MMA of the tcgen05 kernel (tests): 0 = the plan's choice, 1 = one, 2 = pairs;
 // set through dwc_testing_tc_row_pairs.
 int tc_row_pairs_mode();
 bool tensor_core_fgrad(int N, int C, int OH, int OW, int FH, int FW);
+// tcgen05 filter gradient (16-bit inputs, square filters; scratch for the stacked copies of x
+// and dy comes from the library's pool): cudaErrorNotSupported when the shape does not fit.
+cudaError_t launch_tc_fgrad_bf16(const FilterGrad& p);
+cudaError_t launch_tc_fgrad_f16(const FilterGrad& p);
+bool tc_fgrad_fits(const FilterGrad& p);
+// Where the tcgen05 filter gradient is the one to run (the automatic choice; timed against the
+// warp-level MMA and CUDA-core kernels, bf16): from 13 taps on rows of at least 44 outputs.
+// Its work grows with the rows, columns and filter height but not the width (the whole x
+// band of a dy tile is multiplied), so narrow rows and small filters stay elsewhere
+// (64x56x56x128: 205 against 229 us at 13 taps, 166 against 158 at 11; 64x112x112x64 13x13:
+// 358 against 426; 32x40x40x128 31x31 a tie; 64x28x28x256 at any size slower).
+inline bool tc_fgrad_wanted(int FW, int OW) { return OW >= 44 && FW >= 13; }
+// The tcgen05 filter gradient serves this 16-bit call: the automatic choice or the family
+// preference (tcgen05 forced: 2; other families: never).
+bool tc_fgrad_taken(const FilterGrad& p);
 
 // The argument and pointer checks of dwc_bwd_filter without its workspace checks; returns a
 // dwc_status_t value (0 = DWC_OK).

@@ -218,7 +218,8 @@ __device__ __forceinline__ void tc_bulk_load(void* dst, const void* src, uint32_
 // out of time it records the timeout and raises the abort flag itself.  Between polls the
 // warp sleeps, up to `max_sleep_ns`: the warps that wait most of the time (epilogue,
 // feeders) then leave the issue slots of their sub-partition to the issuers.
-__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, const TcArgs& a,
+template <class Args>
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, const Args& a,
                                         volatile int* abort_flag, uint32_t max_sleep_ns = 32) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
@@ -238,7 +239,8 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, const Tc
 
 // The same wait by every lane of a warp, with one outcome for the whole warp (a warp that
 // goes on runs warp-collective instructions, so no lane may have given up alone).
-__device__ __forceinline__ bool tc_wait_warp(uint64_t* bar, uint32_t parity, const TcArgs& a,
+template <class Args>
+__device__ __forceinline__ bool tc_wait_warp(uint64_t* bar, uint32_t parity, const Args& a,
                                              volatile int* abort_flag, uint32_t max_sleep_ns = 32) {
     return __all_sync(0xffffffffu, tc_wait(bar, parity, a, abort_flag, max_sleep_ns));
 }
@@ -246,8 +248,9 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t* bar, uint32_t parity, con
 // A feeder never leaves with copies in flight: after its last fill it waits (bounded, even
 // after an abort) for the fills still open in each of its `slots` ring slots, the fills
 // `count - slots` .. `count - 1` (earlier fills completed before their slot was refilled).
+template <class Args>
 __device__ __forceinline__ void tc_drain(uint64_t* full, uint32_t first_slot, uint32_t slots,
-                                         uint32_t count, const TcArgs& a) {
+                                         uint32_t count, const Args& a) {
     for (uint32_t k = count >= slots ? count - slots : 0; k < count; ++k)
         if (!mbar_wait(&full[first_slot + k % slots], (k / slots) & 1u, a.wait_ns)) {
             record_status(a.status, DWC_DEVSTAT_TIMEOUT);

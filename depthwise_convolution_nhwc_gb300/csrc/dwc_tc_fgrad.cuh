@@ -1,0 +1,464 @@
+// dwc_tc_fgrad.cuh -- filter gradient on the 5th-generation tensor cores (tcgen05 MMA,
+// accumulators in tensor memory) for 16-bit inputs, fp32 accumulation.
+//
+// The filter gradient of "Flash-DWC: Making Depthwise Convolution Compute-Efficient on GPUs"
+// (§3.3, the reduction of x * dy over images and output pixels for every tap), written as
+// an MMA whose two operands are plain input rows.  For one channel and the stacked rows of
+// every image (the layout of the forward kernel's preparation: image n on the S virtual rows
+// from n*S, zero rows between images, so that dy row v meets x row v + fh for filter row fh):
+//
+//   D_j[m, n] = sum_r x[r + fh0, X0 + m] * dy[r - j, n0 + n]     (j = 0..3)
+//   dw[fh0 + j, fw] = sum_n D_j[n + fw, n]                        (a diagonal of D_j)
+//
+// where X0 = n0 - pad_w (the x column of output column n0 at tap 0), m < 128 runs over the x
+// columns a 64-column tile of dy can meet and r over all virtual rows.  Per K-step of 16 rows
+// four MMAs of M=128, N=64, K=16 share A = 16 rows of 128 x columns; MMA j takes B = the
+// staged dy band read from a start address j rows earlier: the dy rows j above A's rows.
+// (Two rows per MMA -- N=128 over two dy bands staged one row apart, two issuers -- halves
+// the MMAs but was 10 % slower: two threads do not issue N=128 MMAs as fast as the tensor
+// core runs them, and one accumulator cannot take MMAs from two threads.  Four shifted dy
+// copies in one N=256 MMA moved twice the bytes from L2.)  kTfgRowsPerMma keeps both forms.
+// Both operands are
+// read in the MN-major core-matrix layout: 8 columns of a row are 16 contiguous bytes,
+// consecutive rows 16 bytes apart, so a band of an 8-column plane lands in shared memory
+// exactly as the stacked copy holds it.  A unit is (channel, group of four
+// filter rows) over every row and column tile: its accumulators hold the whole sum, so the
+// epilogue writes dw directly (no partial slices) after summing the diagonals.
+//
+// Three launches: a preparation kernel writes the stacked copies of x (the forward's padding)
+// and of dy (no padding), plane-major -- every 8-column plane of a channel holds its virtual
+// rows contiguously, with zero rows before and after -- then the main kernel, which moves
+// each stage's plane bands with bulk copies (2 KB contiguous each).  Tensor-map boxes of
+// these bands (16-byte inner rows) ran at one row per clock: 3300 clocks a stage, twice the
+// stage's MMA time.  Warp roles (9 warps, one persistent CTA per SM): warps 0-3 epilogue
+// (warp w reads the 32-lane quadrant w of the accumulators), warps 4-7 the MMA issuers (one
+// lane each; issuer j owns filter row fh0 + j of every unit; warp 4 allocates the tensor
+// memory), warp 8 the copy producer (lane i copies plane band i of a stage: 16 x bands of
+// 128 rows, 8 dy bands of 131 rows).  Every wait is bounded.
+#pragma once
+
+#include "dwc_tc.cuh"
+
+namespace dwc {
+
+constexpr int kTfgKB = 128;          // virtual rows per stage (8 K-steps of 16)
+constexpr int kTfgXPlanes = 16;      // 128 x columns
+constexpr int kTfgDyPlanes = 8;      // 64 dy columns
+constexpr int kTfgCopies = 4;        // filter rows per unit
+constexpr int kTfgRowsPerMma = 1;    // filter rows per MMA (N = 64 per row)
+constexpr int kTfgIssuers = kTfgCopies / kTfgRowsPerMma;   // issuer q: rows R q .. R q + R - 1
+constexpr int kTfgDyCopies = kTfgRowsPerMma;   // dy bands per stage, band h from row r0 - 3 - h
+constexpr int kTfgStages = kTfgRowsPerMma == 1 ? 4 : 3;
+constexpr int kTfgDyRows = kTfgKB + kTfgCopies - 1;   // 131 rows of a dy band
+constexpr int kTfgRO = kTfgCopies - 1 + (kTfgRowsPerMma - 1);   // zero rows before row 0
+constexpr int kTfgEpiWarps = 4;
+constexpr int kTfgMmaWarp = 4;
+constexpr int kTfgTmaWarp = kTfgMmaWarp + kTfgIssuers;
+constexpr int kTfgThreads = (kTfgTmaWarp + 1) * 32;
+constexpr int kTfgXBytes = kTfgXPlanes * kTfgKB * 16;                    // 32 KB
+constexpr int kTfgDyBytes = kTfgDyCopies * kTfgDyPlanes * kTfgDyRows * 16;   // 32.75 KB
+constexpr int kTfgStageBytes = kTfgXBytes + kTfgDyBytes;
+constexpr int kTfgRowFloats = 65;    // epilogue staging: 128 rows of 64 columns + 1 pad
+constexpr int kTfgEpiBytes = 128 * kTfgRowFloats * 4;
+constexpr int kTfgBarOff = kTfgStages * kTfgStageBytes + kTfgEpiBytes;
+// barriers: full and empty per stage, two accumulator buffers, the epilogue's own, one per
+// issuer; then the tensor-memory address and the abort flag
+constexpr int kTfgBarBytes = (2 * kTfgStages + 2 * 2 + 1 + kTfgIssuers) * 8 + 8;
+constexpr int kTfgSmem = kTfgBarOff + 256;
+static_assert(kTfgBarBytes <= 256, "barrier area");
+
+struct TcFgArgs {
+    const unsigned char* xpl;    // stacked x: C x npx planes x vp rows x 16 bytes
+    const unsigned char* dypl;   // stacked dy: C x npd planes x vp rows x 16 bytes
+    const unsigned char* zeros;  // kTfgDyRows * 16 zero bytes
+    float* dw;          // FH x FW x C
+    unsigned int* status;
+    unsigned long long wait_ns;
+    int npx, npd;       // planes of the stacked copies
+    uint32_t vp;        // rows of a plane (virtual row v at row v + kTfgRO)
+    int C, FH, FW;
+    int groups;         // filter-row groups of four per channel
+    int col_tiles;      // 64-column tiles of dy
+    int row_blocks;     // stages of kTfgKB virtual rows per column tile
+    int x0;             // stacked x column of dy column 0 at tap 0 (a multiple of 8, <= 0)
+    uint32_t units;     // C * groups
+    uint32_t idesc;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kTfgThreads, 1)
+tc_fgrad_kernel(const TcFgArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    float* stage_d = reinterpret_cast<float*>(smem + kTfgStages * kTfgStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTfgBarOff);
+    uint64_t* full = bars;                        // [kTfgStages]
+    uint64_t* empty = full + kTfgStages;          // [kTfgStages]
+    uint64_t* d_full = empty + kTfgStages;        // [2]
+    uint64_t* d_empty = d_full + 2;               // [2]
+    uint64_t* epi_bar = d_empty + 2;              // the epilogue warps' own barrier
+    uint64_t* mma_done = epi_bar + 1;             // [kTfgIssuers]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + kTfgIssuers);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTfgStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kTfgIssuers);   // every issuer's MMAs on the stage
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&d_full[s], kTfgIssuers);
+            mbar_init(&d_empty[s], kTfgEpiWarps);
+        }
+        mbar_init(epi_bar, kTfgEpiWarps);
+        for (int q = 0; q < kTfgIssuers; ++q) mbar_init(&mma_done[q], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kTfgMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(kTcTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t iters = static_cast<uint32_t>(a.col_tiles * a.row_blocks);   // stages per unit
+
+    if (warp == kTfgTmaWarp) {
+        // ------------------------------------------------------------- copy producer
+        // Lanes 0-15: x rows r0 + fh0 .. +127 of the 16 planes from column 64 t + x0; lanes
+        // 16 + 8 h + p: dy band h, rows r0 - 3 - h .. +130 of plane p from column 64 t.  A
+        // plane outside
+        // a stacked copy comes from the zero buffer (with several column tiles its rows would
+        // otherwise enter accumulator rows that other tiles fill).
+        const size_t pbytes = static_cast<size_t>(a.vp) * 16;
+        uint32_t k = 0;
+        bool ok = true;
+        for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            const int c = static_cast<int>(u / static_cast<uint32_t>(a.groups));
+            const int fh0 = 4 * static_cast<int>(u % static_cast<uint32_t>(a.groups));
+            for (uint32_t it = 0; it < iters; ++it, ++k) {
+                const int t = static_cast<int>(it / static_cast<uint32_t>(a.row_blocks));
+                const int r0 = static_cast<int>(it % static_cast<uint32_t>(a.row_blocks)) * kTfgKB;
+                const uint32_t s = k % kTfgStages, ph = (k / kTfgStages) & 1u;
+                if (!tc_wait_warp(&empty[s], ph ^ 1u, a, abort_flag)) { ok = false; break; }
+                unsigned char* st = smem + s * kTfgStageBytes;
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], kTfgStageBytes);
+                __syncwarp();
+                if (lane < kTfgXPlanes) {
+                    const int pl = (64 * t + a.x0) / 8 + lane;
+                    const unsigned char* src =
+                        pl >= 0 && pl < a.npx
+                            ? a.xpl + (static_cast<size_t>(c) * a.npx + pl) * pbytes +
+                                  static_cast<size_t>(kTfgRO + r0 + fh0) * 16
+                            : a.zeros;
+                    tc_bulk_load(st + lane * (kTfgKB * 16), src, kTfgKB * 16, &full[s]);
+                } else if (lane < kTfgXPlanes + kTfgDyCopies * kTfgDyPlanes) {
+                    const int i = lane - kTfgXPlanes;   // band h = i / 8, plane i % 8
+                    const int h = i / kTfgDyPlanes, pl = 8 * t + i % kTfgDyPlanes;
+                    const unsigned char* src =
+                        pl < a.npd ? a.dypl + (static_cast<size_t>(c) * a.npd + pl) * pbytes +
+                                         static_cast<size_t>(kTfgRO + r0 - (kTfgCopies - 1) - h) * 16
+                                   : a.zeros;
+                    tc_bulk_load(st + kTfgXBytes + i * (kTfgDyRows * 16), src, kTfgDyRows * 16, &full[s]);
+                }
+            }
+        }
+        if (lane == 0) tc_drain(full, 0, kTfgStages, k, a);
+        __syncwarp();
+    } else if (warp >= kTfgMmaWarp) {
+        // ------------------------------------------------------------- MMA issue
+        // filter rows fh0 + R q + h (dy band h): accumulator columns 64 (R q + h) ..
+        const int q = warp - kTfgMmaWarp;
+        if (lane == 0) {
+            // MN-major descriptors: K-direction groups of 8 rows 128 bytes apart, M/N-direction
+            // groups of 8 columns (planes) one plane band apart; a K-step is 16 rows (256 B).
+            // B starts 3 - R q rows into the staged dy bands: band h then holds the dy rows
+            // R q + h above A's rows.
+            const uint64_t xd0 = tc_sdesc(smem_addr(smem), 128u, kTfgKB * 16u);
+            const uint64_t dd0 = tc_sdesc(smem_addr(smem + kTfgXBytes), 128u, kTfgDyRows * 16u) +
+                                 static_cast<uint32_t>(kTfgCopies - 1 - kTfgRowsPerMma * q);
+            const uint32_t stage16 = kTfgStageBytes >> 4;
+            uint32_t db = 0, dphase = 0, k = 0;
+            bool ok = true;
+            for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                if (!tc_wait(&d_empty[db], dphase ^ 1u, a, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem + db * kTcDCols + static_cast<uint32_t>(64 * kTfgRowsPerMma * q);
+                for (uint32_t it = 0; it < iters; ++it, ++k) {
+                    const uint32_t s = k % kTfgStages, ph = (k / kTfgStages) & 1u;
+                    if (!tc_wait(&full[s], ph, a, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    uint64_t ad = xd0 + s * stage16, bd = dd0 + s * stage16;
+#pragma unroll
+                    for (int ks = 0; ks < kTfgKB / 16; ++ks) {
+                        tc_mma(d, ad, bd, a.idesc, (it | ks) != 0 ? 1u : 0u);
+                        ad += 16u;   // 16 rows = 256 bytes
+                        bd += 16u;
+                    }
+                    tc_commit(&empty[s]);
+                }
+                if (!ok) break;
+                tc_commit(&d_full[db]);
+                db ^= 1u;
+                if (db == 0) dphase ^= 1u;
+            }
+            tc_commit(&mma_done[q]);
+            if (!mbar_wait(&mma_done[q], 0, a.wait_ns)) record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------- epilogue
+        // Per filter row j of the unit: the 128 x 64 accumulator tile goes to shared memory
+        // (row m = lane of quadrant w), then thread t sums diagonal fw = t (and t + 128):
+        // dw[fh0 + j][fw] = sum_n D_j[n + fw][n].
+        const int quad = warp;
+        const int m = quad * 32 + lane;
+        uint32_t db = 0, dphase = 0, eph = 0;
+        bool ok = true;
+        for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            const int c = static_cast<int>(u / static_cast<uint32_t>(a.groups));
+            const int fh0 = 4 * static_cast<int>(u % static_cast<uint32_t>(a.groups));
+            if (!tc_wait_warp(&d_full[db], dphase, a, abort_flag, 1024)) break;
+            tc_fence_after();
+            const uint32_t dq = tmem + db * kTcDCols + (static_cast<uint32_t>(quad * 32) << 16);
+            for (int j = 0; j < kTfgCopies && ok; ++j) {
+                for (int cb = 0; cb < 64; cb += 16) {
+                    uint32_t v[16];
+                    tc_ld16(dq + j * 64 + cb, v);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) stage_d[m * kTfgRowFloats + cb + e] = __uint_as_float(v[e]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(epi_bar);
+                if (!tc_wait_warp(epi_bar, eph, a, abort_flag, 256)) { ok = false; break; }
+                eph ^= 1u;
+                const int fh = fh0 + j;
+                if (fh < a.FH) {
+                    for (int fw = m; fw < a.FW; fw += 128) {
+                        float sum = 0.f;
+#pragma unroll 8
+                        for (int n = 0; n < 64; ++n) sum += stage_d[(n + fw) * kTfgRowFloats + n];
+                        a.dw[(static_cast<size_t>(fh) * a.FW + fw) * a.C + c] = sum;
+                    }
+                }
+                // every thread is done reading before the next filter row overwrites the tile
+                __syncwarp();
+                if (lane == 0) mbar_arrive(epi_bar);
+                if (!tc_wait_warp(epi_bar, eph, a, abort_flag, 256)) { ok = false; break; }
+                eph ^= 1u;
+            }
+            if (!ok) break;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&d_empty[db]);
+            db ^= 1u;
+            if (db == 0) dphase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kTfgMmaWarp) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTcTmemCols)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+// The stacked copies of x and dy (the forward preparation's layout; dy without padding).
+struct TcFgPlan {
+    int S;              // virtual rows per image
+    long long V;        // N * S
+    int Lp, Wp;         // x copy: left padding, row length (a multiple of 8)
+    int Wdp;            // dy copy: row length (a multiple of 8)
+    size_t x_bytes, dy_bytes;
+    TcFgArgs a;
+};
+
+inline bool tc_fgrad_plan(const FilterGrad& p, TcFgPlan& P) {
+    if (p.FH < 1 || p.FW < 1 || p.FW > 128 - 64 + 1 || p.C % 8 != 0 || p.N < 1) return false;
+    if (device_info().max_smem_optin < kTfgSmem) return false;
+    P.S = std::max({p.pad + p.H, p.OH + p.FH - 1 - p.pad, p.OH});
+    P.V = static_cast<long long>(p.N) * P.S;
+    if (P.V + 2 * kTfgKB >= (1LL << 31)) return false;
+    P.Lp = p.pad % 8;
+    P.Wp = (P.Lp + p.W + 7) / 8 * 8;
+    P.Wdp = (p.OW + 7) / 8 * 8;
+    TcFgArgs& a = P.a;
+    a.C = p.C; a.FH = p.FH; a.FW = p.FW;
+    a.groups = (p.FH + kTfgCopies - 1) / kTfgCopies;
+    a.col_tiles = (p.OW + 63) / 64;
+    a.row_blocks = static_cast<int>((P.V + kTfgCopies - 1 + kTfgKB - 1) / kTfgKB);
+    a.x0 = P.Lp - p.pad;
+    a.npx = P.Wp / 8;
+    a.npd = P.Wdp / 8;
+    // rows of a plane: kTfgRO zero rows, the V virtual rows, and zero rows up to the last
+    // stage's x rows (r0 + fh0 + 127 for the last row block and filter-row group)
+    const long long vp = kTfgRO + static_cast<long long>(a.row_blocks) * kTfgKB + kTfgCopies * a.groups;
+    if (vp >= (1LL << 31)) return false;
+    a.vp = static_cast<uint32_t>(vp);
+    P.x_bytes = static_cast<size_t>(p.C) * a.npx * a.vp * 16;
+    P.dy_bytes = static_cast<size_t>(p.C) * a.npd * a.vp * 16;
+    const long long units = static_cast<long long>(p.C) * a.groups;
+    if (units >= (1LL << 31)) return false;
+    a.units = static_cast<uint32_t>(units);
+    return true;
+}
+
+// Instruction descriptor: kind::f16, fp32 accumulation, both operands MN-major, M=128,
+// N = 64 per filter row of an MMA.
+template <typename T>
+inline uint32_t tc_fgrad_idesc() {
+    const uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+    return (1u << 4) | (ab << 7) | (ab << 10) | (1u << 15) | (1u << 16) |
+           (static_cast<uint32_t>(64 * kTfgRowsPerMma >> 3) << 17) | (static_cast<uint32_t>(kTcM >> 4) << 24);
+}
+
+// Plane-major stacked copy of `src` (nn x h x w x C, 16-bit):
+//   dst[c][p][ro + v][e] = src[n][v % S - pad_h][8 p + e - lp][c],  n = v / S,  zero outside,
+// for planes p < wp / 8 and plane rows ro + v in [0, vp) (zero rows before and after the
+// V = nn * S virtual rows).  A tile is 16 virtual rows x one plane x
+// CT channels: pixels are read as 16-byte pieces of 8 channels (whole 128-byte lines for 64
+// channels), and every thread writes the 8 columns of one channel and row as 16 bytes,
+// consecutive threads along the rows of a plane.
+struct TcStackArgs {
+    const void* src;
+    void* dst;
+    int nn, h, w, C, pad_h, S, lp, np;   // np: planes (wp / 8)
+    int V, ro, vp;      // virtual rows; zero rows before them; rows of a plane
+    int CT, piece_shift;
+    int tiles;          // ceil(vp / 16) * np * (C / CT)
+    FastDiv fd_np, fd_ct, fd_S;
+};
+
+constexpr int kStackRows = 16;
+constexpr int kStackWords = 33;   // a (column, row) pixel's 64 channels as 32 words + 1 pad
+
+template <typename T>
+__global__ void __launch_bounds__(256) tc_stack_pm_kernel(const TcStackArgs a) {
+    __shared__ uint32_t tile[8 * kStackRows * kStackWords];   // [column][row][words]
+    const T* X = static_cast<const T*>(a.src);
+    T* P = static_cast<T*>(a.dst);
+    const int pieces = a.CT / 8;
+    for (int tt = blockIdx.x; tt < a.tiles; tt += gridDim.x) {
+        uint32_t cb, pl;
+        const uint32_t q = a.fd_ct.divmod(static_cast<uint32_t>(tt), cb);
+        const int rb = static_cast<int>(a.fd_np.divmod(q, pl));
+        const int c0 = a.CT * static_cast<int>(cb);
+        const int v0 = rb * kStackRows;
+        __syncthreads();   // the previous tile's reads are done
+        for (int idx = threadIdx.x; idx < kStackRows * 8 * pieces; idx += blockDim.x) {
+            const int i = idx >> a.piece_shift, j = idx - (i << a.piece_shift);
+            const int r = i >> 3, e = i & 7;   // row of the tile, column of the plane
+            const int v = v0 + r - a.ro;        // virtual row
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (v >= 0 && v < a.V) {
+                uint32_t hr;
+                const int n = static_cast<int>(a.fd_S.divmod(static_cast<uint32_t>(v), hr));
+                const int hh = static_cast<int>(hr) - a.pad_h;
+                const int col = 8 * static_cast<int>(pl) + e - a.lp;
+                if (hh >= 0 && hh < a.h && col >= 0 && col < a.w)
+                    val = __ldg(reinterpret_cast<const uint4*>(
+                        X + ((static_cast<size_t>(n) * a.h + hh) * a.w + col) * a.C + c0 + 8 * j));
+            }
+            uint32_t* d = tile + (e * kStackRows + r) * kStackWords + 4 * j;
+            d[0] = val.x; d[1] = val.y; d[2] = val.z; d[3] = val.w;
+        }
+        __syncthreads();
+        // task (channel pair cp, row r): the pair's word of the plane's 8 columns
+        for (int idx = threadIdx.x; idx < (a.CT / 2) * kStackRows; idx += blockDim.x) {
+            const int r = idx & (kStackRows - 1), cp = idx >> 4;
+            const int v = v0 + r;               // plane row
+            if (v >= a.vp) continue;
+            uint32_t wd[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wd[e] = tile[(e * kStackRows + r) * kStackWords + cp];
+            uint4 lo, hi;
+            lo.x = __byte_perm(wd[0], wd[1], 0x5410); hi.x = __byte_perm(wd[0], wd[1], 0x7632);
+            lo.y = __byte_perm(wd[2], wd[3], 0x5410); hi.y = __byte_perm(wd[2], wd[3], 0x7632);
+            lo.z = __byte_perm(wd[4], wd[5], 0x5410); hi.z = __byte_perm(wd[4], wd[5], 0x7632);
+            lo.w = __byte_perm(wd[6], wd[7], 0x5410); hi.w = __byte_perm(wd[6], wd[7], 0x7632);
+            const size_t plane = static_cast<size_t>(a.vp) * 8;   // elements of one plane
+            T* dst = P + (static_cast<size_t>(c0 + 2 * cp) * a.np + pl) * plane + static_cast<size_t>(v) * 8;
+            *reinterpret_cast<uint4*>(dst) = lo;
+            *reinterpret_cast<uint4*>(dst + static_cast<size_t>(a.np) * plane) = hi;
+        }
+    }
+}
+
+template <typename T>
+cudaError_t tc_fgrad_stack(const void* src, void* dst, int nn, int h, int w, int C, int pad_h, int S,
+                           int lp, int wp, int vp, cudaStream_t stream) {
+    TcStackArgs q;
+    q.src = src; q.dst = dst;
+    q.nn = nn; q.h = h; q.w = w; q.C = C; q.pad_h = pad_h; q.S = S; q.lp = lp; q.np = wp / 8;
+    q.CT = C % 64 == 0 ? 64 : (C % 32 == 0 ? 32 : (C % 16 == 0 ? 16 : 8));
+    q.piece_shift = q.CT == 64 ? 3 : (q.CT == 32 ? 2 : (q.CT == 16 ? 1 : 0));
+    const long long V = static_cast<long long>(nn) * S;
+    const long long tiles = (static_cast<long long>(vp) + kStackRows - 1) / kStackRows * q.np * (C / q.CT);
+    if (V >= (1LL << 31) || tiles >= (1LL << 31)) return cudaErrorNotSupported;
+    q.V = static_cast<int>(V);
+    q.ro = kTfgRO;
+    q.vp = vp;
+    q.tiles = static_cast<int>(tiles);
+    q.fd_np.init(static_cast<uint32_t>(q.np));
+    q.fd_ct.init(static_cast<uint32_t>(C / q.CT));
+    q.fd_S.init(static_cast<uint32_t>(S));
+    const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, 16LL * device_info().sm_count));
+    tc_stack_pm_kernel<T><<<grid, 256, 0, stream>>>(q);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_tc_fgrad(const FilterGrad& p) {
+    TcFgPlan P;
+    if (!tc_fgrad_plan(p, P)) return cudaErrorNotSupported;
+    // scratch of this call: the stacked x, the stacked dy, a zero band (128-byte aligned parts)
+    const size_t dy_off = (P.x_bytes + 127) / 128 * 128;
+    const size_t z_off = dy_off + (P.dy_bytes + 127) / 128 * 128;
+    const size_t z_bytes = (kTfgDyRows * 16 + 127) / 128 * 128;
+    void* scratch = nullptr;
+    if (scratch_alloc(&scratch, z_off + z_bytes, p.stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return cudaErrorNotSupported;   // the caller takes another kernel
+    }
+    unsigned char* base = static_cast<unsigned char*>(scratch);
+    const int vp = static_cast<int>(P.a.vp);
+    cudaError_t err = cudaMemsetAsync(base + z_off, 0, z_bytes, p.stream);
+    if (err == cudaSuccess)
+        err = tc_fgrad_stack<T>(p.x, base, p.N, p.H, p.W, p.C, p.pad, P.S, P.Lp, P.Wp, vp, p.stream);
+    if (err == cudaSuccess)
+        err = tc_fgrad_stack<T>(p.dy, base + dy_off, p.N, p.OH, p.OW, p.C, 0, P.S, 0, P.Wdp, vp, p.stream);
+    if (err == cudaSuccess) {
+        TcFgArgs a = P.a;
+        a.xpl = base;
+        a.dypl = base + dy_off;
+        a.zeros = base + z_off;
+        a.dw = p.dw;
+        a.status = p.status;
+        a.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
+        a.idesc = tc_fgrad_idesc<T>();
+        auto kern = tc_fgrad_kernel<T>;
+        static DeviceOnce smem_opt_in;
+        err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
+        if (err == cudaSuccess) {
+            const unsigned grid = static_cast<unsigned>(
+                std::min<long long>(a.units, static_cast<long long>(device_info().sm_count)));
+            kern<<<grid, kTfgThreads, kTfgSmem, p.stream>>>(a);
+            err = cudaGetLastError();
+        }
+    }
+    scratch_free(scratch, p.stream);
+    return err;
+}
+
+}  // namespace dwc

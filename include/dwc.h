@@ -24,13 +24,14 @@
  * the caller.  Inputs are only read; outputs are overwritten (never accumulated into).
  * Outputs must not overlap inputs.  Calls are asynchronous on `stream` (0 = legacy default
  * stream): they enqueue work and return; the caller synchronises.  Device memory: the
- * 16-bit forward and backward-data calls that run on the tcgen05 tensor-core kernel (see
- * dwc_path) take scratch for a re-laid-out copy of their input and the filter's Toeplitz
- * runs (about 1.5x the input's bytes) with cudaMallocFromPoolAsync on `stream`, from a
- * memory pool the library creates per device on first use and that keeps up to 512 MiB
- * between calls; the scratch returns to the pool in stream order (cudaFreeAsync) after the
- * call's kernels.  If the allocation fails the call runs on another kernel.  No other call
- * allocates device memory (dwc_bwd_filter takes a caller workspace).
+ * 16-bit calls that run on the tcgen05 tensor-core kernels (see dwc_path) take scratch with
+ * cudaMallocFromPoolAsync on `stream` -- forward and backward data for a re-laid-out copy of
+ * their input and the filter's Toeplitz runs (about 1.5x the input's bytes), the filter
+ * gradient for re-laid-out copies of x and dy (about 1.3x their bytes) -- from a memory pool
+ * the library creates per device on first use and that keeps up to 512 MiB between calls;
+ * the scratch returns to the pool in stream order (cudaFreeAsync) after the call's kernels.
+ * If the allocation fails the call runs on another kernel.  No other call allocates device
+ * memory (dwc_bwd_filter otherwise takes a caller workspace).
  *
  * Errors: every call validates its arguments on the host and returns a dwc_status_t
  * without launching anything when they are wrong.  No call aborts or throws.  A CUDA
@@ -219,10 +220,9 @@ int dwc_version(void);
 
 /* Which kernel family a call with these arguments would use: 1 = fast CUDA-core kernels
  * (row-streaming, stride-2 and filter-gradient kernels, for the shapes listed at the top
- * of this file), 2 = tensor-core kernels (16-bit inputs only: forward and backward data on
- * the 5th-generation MMA, tcgen05 with accumulators in tensor memory; the filter gradient on
- * the warp-level MMA), 3 = small-map kernels (maps up to 16 x 16), 4 = forward / backward
- * data on the warp-level MMA (mma.sync; 16-bit inputs only), 0 = general
+ * of this file), 2 = tensor-core kernels on the 5th-generation MMA (tcgen05, accumulators in
+ * tensor memory; 16-bit inputs only), 3 = small-map kernels (maps up to 16 x 16), 4 =
+ * tensor-core kernels on the warp-level MMA (mma.sync; 16-bit inputs only), 0 = general
  * kernels, -1 = invalid arguments.  `pass` is 0 for
  * dwc_fwd, 1 for dwc_bwd_data, 2 for dwc_bwd_filter, 3 for dwc_fwd_bn_act.  Pointer
  * alignment is checked with the pointers given (they may be NULL to mean "16-byte
@@ -231,8 +231,9 @@ int dwc_path(int pass, const void* a, const void* b, const void* out,
              int N, int H, int W, int C, int FH, int FW, int stride, int pad, dwc_dtype_t dtype);
 
 /* Kernel launches of this library that a call with these arguments and 16-byte aligned
- * pointers makes (the tcgen05 path: a preparation kernel and the main kernel; a filter
- * gradient: its kernel and the sum of its slices), 0 for an empty output, -1 for
+ * pointers makes (the tcgen05 forward / backward data: a preparation kernel and the main
+ * kernel; the tcgen05 filter gradient: two preparation kernels and the main kernel; other
+ * filter gradients: the kernel and the sum of its slices), 0 for an empty output, -1 for
  * invalid arguments.  `pass` as for dwc_path.  For profiling and launch accounting. */
 int dwc_kernel_launches(int pass, int N, int H, int W, int C, int FH, int FW, int stride, int pad,
                         dwc_dtype_t dtype);

@@ -27,7 +27,9 @@ void dwc_testing_stall_next_row_launch(void);
  * family can run the shape (else the automatic choice): 0 = automatic (the default),
  * 1 = CUDA-core row kernel, 2 = tcgen05 tensor-core kernel, 4 = warp-level MMA kernel (the
  * family numbers of dwc_path, which reports the choice).  It also bypasses the small-map
- * kernels for 16-bit inputs.  Lets tests run every kernel on the same shapes and benchmarks
+ * kernels for 16-bit inputs.  For 16-bit filter gradients of square filters outside the
+ * small-map shapes: 2 takes the tcgen05 kernel where it fits, 4 the warp-level MMA kernel
+ * where it fits, 1 the CUDA-core kernel.  Lets tests run every kernel on the same shapes and benchmarks
  * compare them.  Returns the previous preference, or -1 (nothing changed) for an unknown
  * family.  Not for production use. */
 int dwc_testing_prefer_family(int family);

@@ -183,6 +183,11 @@ def test_path_selection_host_logic(lib):
     big = dict(H=56, W=56, C=64, FH=31, FW=31, pad=15)
     assert p(0, **big, dtype=1) == 2 and p(1, **big, dtype=2) == 2 and p(2, **big, dtype=1) == 2
     assert p(0, **big) == 1 and p(2, **big) == 1          # fp32 stays on CUDA cores
+    # 16-bit filter gradients: tcgen05 from 13 taps on rows of 44+ outputs, else the
+    # warp-level MMA kernel (family 4) for large filters on narrower rows
+    assert p(2, **dict(big, FH=13, FW=13, pad=6), dtype=1) == 2
+    assert p(2, **dict(big, FH=11, FW=11, pad=5), dtype=1) == 1
+    assert p(2, **dict(big, W=28), dtype=1) == 4
     assert p(0, **dict(big, FH=7, FW=7, pad=3), dtype=1) == 1
     # tcgen05 from 9 taps on rows of 28+ outputs, from 17 taps on 17- to 27-wide rows
     assert p(0, **dict(big, W=28, FH=9, FW=9, pad=4), dtype=1) == 2
@@ -211,6 +216,8 @@ def test_kernel_launch_counts(lib):
     assert n(0, **dict(f7, C=32)) == 1                     # the tail is the only launch
     big = dict(N=32, H=56, W=56, C=128, FH=31, FW=31, pad=15, dtype=1)
     assert n(0, **big) == 2 and n(1, **big) == 2          # tcgen05: preparation + main
+    assert n(2, **big) == 3                               # tcgen05 gradient: 2 copies + main
+    assert n(2, **dict(big, dtype=0)) == 2                # fp32: kernel + slice sum
     assert n(0, **dict(big, N=0)) == 0
     assert n(0, FH=4, FW=4, **{k: v for k, v in GOOD.items() if k not in ("FH", "FW")}) == 1
     assert n(0, stride=0) == -1

@@ -154,6 +154,57 @@ def test_tcgen05_kernel_full_workload_sampled(lib, name):
         assert err <= TOL[case.dtype], f"{pname} {name}: normalized error {err:.3e}"
 
 
+# The tcgen05 filter gradient (forced with family 2): the square-filter cases above that are
+# not small maps (those take the small-map filter gradient first).  They cover several
+# column tiles of 64 (300-wide rows), filter heights that are not a multiple of 4, filters
+# to 51 taps, pads beyond (F-1)/2 and none, and tall images.
+FG_CASES = [c for c in TC_CASES if c.FH == c.FW]
+
+
+def run_fgrad(lib, case, family):
+    prev = lib.dwc_testing_prefer_family(family)
+    try:
+        fam = dwc.path("bwd_filter", None, None, None, case.N, case.H, case.W, case.C, case.FH,
+                       case.FW, case.stride, case.pad, CODE[case.dtype])
+        x, dy = case.x(), case.dy()
+        dw = dwc.bwd_filter(x.cuda(), dy.cuda(), (case.FH, case.FW), case.stride, case.pad)
+        torch.cuda.synchronize()
+    finally:
+        lib.dwc_testing_prefer_family(prev)
+    assert dwc.device_status() == 0
+    return fam, x, dy, dw
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("case", FG_CASES, ids=lambda c: f"n{c.N}_{c.H}x{c.W}_c{c.C}_f{c.FH}_p{c.pad}")
+def test_tcgen05_filter_gradient_full_tensors(lib, case, dtype):
+    case = Case(**{**case.__dict__, "dtype": dtype})
+    fam, x, dy, dw = run_fgrad(lib, case, 2)
+    if fam != 2:
+        pytest.skip("a small map: the small-map filter gradient serves it")
+    xn, dyn = x.double().numpy(), dy.double().numpy()
+    f_hw = (case.FH, case.FW)
+    ref = oracle.bwd_filter(xn, dyn, f_hw, case.stride, case.pad)
+    den = oracle.bwd_filter(np.abs(xn), np.abs(dyn), f_hw, case.stride, case.pad)
+    err = normalized_error(dw.cpu().numpy(), ref, den)
+    assert err <= TOL[dtype], f"{case}: normalized error {err:.3e}"
+
+
+def test_tcgen05_filter_gradient_is_deterministic_and_matches_the_warp_mma_kernel(lib):
+    """Every dw element is one thread's fixed-order sum of one unit's accumulator diagonal:
+    two runs are bit-identical; the warp-level MMA kernel agrees within the 16-bit tolerance."""
+    case = Case(3, 30, 70, 64, 27, 27, 1, 13, "bf16", "normal", 17)
+    fam, x, dy, a = run_fgrad(lib, case, 2)
+    assert fam == 2
+    _, _, _, b = run_fgrad(lib, case, 2)
+    assert torch.equal(a, b)
+    fam4, _, _, c = run_fgrad(lib, case, 4)
+    assert fam4 == 4
+    den = oracle.bwd_filter(np.abs(x.double().numpy()), np.abs(dy.double().numpy()),
+                            (case.FH, case.FW), 1, case.pad)
+    assert normalized_error(a.cpu().numpy(), c.cpu().double().numpy(), den) <= TOL["bf16"]
+
+
 MMA_CASES = [C_(2, 19, 26, 32, 15), C_(1, 20, 60, 16, 31), C_(1, 5, 223, 8, 13)]
 
 
