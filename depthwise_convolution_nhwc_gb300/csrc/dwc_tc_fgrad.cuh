@@ -14,10 +14,11 @@
 // columns a 64-column tile of dy can meet and r over all virtual rows.  Per K-step of 16 rows
 // four MMAs of M=128, N=64, K=16 share A = 16 rows of 128 x columns; MMA j takes B = the
 // staged dy band read from a start address j rows earlier: the dy rows j above A's rows.
-// (Two rows per MMA -- N=128 over two dy bands staged one row apart, two issuers -- halves
-// the MMAs but was 10 % slower: two threads do not issue N=128 MMAs as fast as the tensor
-// core runs them, and one accumulator cannot take MMAs from two threads.  Four shifted dy
-// copies in one N=256 MMA moved twice the bytes from L2.)  kTfgRowsPerMma keeps both forms.
+// (Rows per MMA R = 2 or 4 -- N = 64 R over R dy bands staged one row apart, 4 / R issuers
+// -- read A once per R rows but took 1.1x (R = 2) and 1.7x (R = 4) the time on bf16
+// 32x56x56x128 31x31: fewer threads do not issue the wider MMAs as fast as the tensor core
+// runs them, and one accumulator cannot take MMAs from two threads.)  kTfgRowsPerMma keeps
+// the three forms.
 // Both operands are
 // read in the MN-major core-matrix layout: 8 columns of a row are 16 contiguous bytes,
 // consecutive rows 16 bytes apart, so a band of an 8-column plane lands in shared memory
@@ -41,14 +42,15 @@
 
 namespace dwc {
 
-constexpr int kTfgKB = 128;          // virtual rows per stage (8 K-steps of 16)
-constexpr int kTfgXPlanes = 16;      // 128 x columns
-constexpr int kTfgDyPlanes = 8;      // 64 dy columns
 constexpr int kTfgCopies = 4;        // filter rows per unit
 constexpr int kTfgRowsPerMma = 1;    // filter rows per MMA (N = 64 per row)
 constexpr int kTfgIssuers = kTfgCopies / kTfgRowsPerMma;   // issuer q: rows R q .. R q + R - 1
 constexpr int kTfgDyCopies = kTfgRowsPerMma;   // dy bands per stage, band h from row r0 - 3 - h
-constexpr int kTfgStages = kTfgRowsPerMma == 1 ? 4 : 3;
+// virtual rows per stage (K-steps of 16) and stages, within shared memory
+constexpr int kTfgKB = kTfgRowsPerMma == 4 ? 112 : 128;
+constexpr int kTfgStages = kTfgRowsPerMma == 1 ? 4 : (kTfgRowsPerMma == 2 ? 3 : 2);
+constexpr int kTfgXPlanes = 16;      // 128 x columns
+constexpr int kTfgDyPlanes = 8;      // 64 dy columns
 constexpr int kTfgDyRows = kTfgKB + kTfgCopies - 1;   // 131 rows of a dy band
 constexpr int kTfgRO = kTfgCopies - 1 + (kTfgRowsPerMma - 1);   // zero rows before row 0
 constexpr int kTfgEpiWarps = 4;
@@ -130,11 +132,11 @@ tc_fgrad_kernel(const TcFgArgs a) {
 
     if (warp == kTfgTmaWarp) {
         // ------------------------------------------------------------- copy producer
-        // Lanes 0-15: x rows r0 + fh0 .. +127 of the 16 planes from column 64 t + x0; lanes
-        // 16 + 8 h + p: dy band h, rows r0 - 3 - h .. +130 of plane p from column 64 t.  A
-        // plane outside
-        // a stacked copy comes from the zero buffer (with several column tiles its rows would
-        // otherwise enter accumulator rows that other tiles fill).
+        // Copy i (lane i, then lane i - 32): i < 16 the x rows r0 + fh0 .. + kTfgKB - 1 of
+        // plane i from column 64 t + x0; i = 16 + 8 h + p the dy band h, rows r0 - 3 - h ..
+        // + kTfgDyRows - 1 of plane p from column 64 t.  A plane outside a stacked copy comes
+        // from the zero buffer (with several column tiles its rows would otherwise enter
+        // accumulator rows that other tiles fill).
         const size_t pbytes = static_cast<size_t>(a.vp) * 16;
         uint32_t k = 0;
         bool ok = true;
@@ -149,22 +151,24 @@ tc_fgrad_kernel(const TcFgArgs a) {
                 unsigned char* st = smem + s * kTfgStageBytes;
                 if (lane == 0) mbar_arrive_expect_tx(&full[s], kTfgStageBytes);
                 __syncwarp();
-                if (lane < kTfgXPlanes) {
-                    const int pl = (64 * t + a.x0) / 8 + lane;
-                    const unsigned char* src =
-                        pl >= 0 && pl < a.npx
-                            ? a.xpl + (static_cast<size_t>(c) * a.npx + pl) * pbytes +
-                                  static_cast<size_t>(kTfgRO + r0 + fh0) * 16
-                            : a.zeros;
-                    tc_bulk_load(st + lane * (kTfgKB * 16), src, kTfgKB * 16, &full[s]);
-                } else if (lane < kTfgXPlanes + kTfgDyCopies * kTfgDyPlanes) {
-                    const int i = lane - kTfgXPlanes;   // band h = i / 8, plane i % 8
-                    const int h = i / kTfgDyPlanes, pl = 8 * t + i % kTfgDyPlanes;
-                    const unsigned char* src =
-                        pl < a.npd ? a.dypl + (static_cast<size_t>(c) * a.npd + pl) * pbytes +
-                                         static_cast<size_t>(kTfgRO + r0 - (kTfgCopies - 1) - h) * 16
-                                   : a.zeros;
-                    tc_bulk_load(st + kTfgXBytes + i * (kTfgDyRows * 16), src, kTfgDyRows * 16, &full[s]);
+                for (int i = lane; i < kTfgXPlanes + kTfgDyCopies * kTfgDyPlanes; i += 32) {
+                    if (i < kTfgXPlanes) {
+                        const int pl = (64 * t + a.x0) / 8 + i;
+                        const unsigned char* src =
+                            pl >= 0 && pl < a.npx
+                                ? a.xpl + (static_cast<size_t>(c) * a.npx + pl) * pbytes +
+                                      static_cast<size_t>(kTfgRO + r0 + fh0) * 16
+                                : a.zeros;
+                        tc_bulk_load(st + i * (kTfgKB * 16), src, kTfgKB * 16, &full[s]);
+                    } else {
+                        const int b = i - kTfgXPlanes;   // band h = b / 8, plane b % 8
+                        const int h = b / kTfgDyPlanes, pl = 8 * t + b % kTfgDyPlanes;
+                        const unsigned char* src =
+                            pl < a.npd ? a.dypl + (static_cast<size_t>(c) * a.npd + pl) * pbytes +
+                                             static_cast<size_t>(kTfgRO + r0 - (kTfgCopies - 1) - h) * 16
+                                       : a.zeros;
+                        tc_bulk_load(st + kTfgXBytes + b * (kTfgDyRows * 16), src, kTfgDyRows * 16, &full[s]);
+                    }
                 }
             }
         }
