@@ -620,17 +620,8 @@ int dwc_kernel_launches(int pass, int N, int H, int W, int C, int FH, int FW, in
     if (out == 0) return 0;
     // filter gradients: the kernel and the fixed-order sum of its slices (or a fill of dW
     // with zeros when nothing meets it: a memset, not a kernel of this library); the tcgen05
-    // filter gradient: the stacked copies of x and dy, then the kernel
-    if (pass == kPassBwdFilter) {
-        if (N == 0) return 0;
-        if (fam == 2) {
-            FilterGrad fg{};
-            fg.N = N; fg.H = H; fg.W = W; fg.C = C; fg.OH = P.OH; fg.OW = P.OW;
-            fg.FH = FH; fg.FW = FW; fg.pad = pad; fg.dtype = P.dtype;
-            if (tc_fgrad_taken(fg)) return 3;
-        }
-        return 2;
-    }
+    // filter gradient: the stacked copies of x and dy (one kernel), then the main kernel
+    if (pass == kPassBwdFilter) return N == 0 ? 0 : 2;
     if (pass == 3) return 1;
     if (fam == 2) {
         const RowConv rc = pass == kPassFwd

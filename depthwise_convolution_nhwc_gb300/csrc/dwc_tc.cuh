@@ -40,13 +40,15 @@
 // accumulator columns (two buffers).
 //
 // Two launches.  A preparation kernel writes, into scratch memory of the call,
-//  * the input as per-channel planes in the layout above: channel-major, the images' rows
-//    stacked on the virtual rows (zero rows between images) and the columns padded so that
-//    every tile's first column falls on an 8-column boundary -- one TMA box then fills one
-//    8-column plane of a unit, with no gather and no transposition in the main kernel;
+//  * the input as per-channel planes in the layout above, plane-major: for each channel and
+//    8-column plane all the virtual rows (the images' rows stacked, zero rows between
+//    images) lie contiguously, and the columns are padded so that every tile's first column
+//    falls on an 8-column boundary -- one bulk copy of a contiguous band then fills one
+//    8-column plane of a unit, with no gather and no transposition in the main kernel (a
+//    row-major copy read by tensor-map boxes of 16-byte rows moved one row per clock);
 //  * every Toeplitz run (channel, filter row), rotated by 180 degrees for backward data.
-// The main kernel then only moves data with the copy engines: TMA boxes for the planes,
-// bulk copies for the runs.  Gathering and transposing inside it (one cache line per
+// The main kernel then only moves data with the copy engines: bulk copies for the planes
+// and for the runs.  Gathering and transposing inside it (one cache line per
 // pixel and channel group, and shuffles to build the runs) tied up the load/store and
 // shared-memory pipes that the MMA issuers and their barriers also go through.
 //
@@ -60,7 +62,7 @@
 //    48); the first also allocates the tensor memory;
 //  * 4 run feeders: one lane each copies, in order, the runs of its issuer's items into
 //    that issuer's ring;
-//  * 1 plane feeder: one lane loads the units' planes into the plane ring.
+//  * 1 plane feeder: lane b copies plane b of each of the units' channels into the plane ring.
 // Stages pass through mbarrier rings; every wait has a time limit and a shared abort flag,
 // so a lost arrival ends the kernel (status word set) instead of hanging it.
 #pragma once
@@ -94,7 +96,7 @@ constexpr int kTcTmemCols = 512;
 constexpr int kTcDCols = 256;       // columns of one accumulator buffer (two buffers)
 constexpr int kTcMaxPlanes = 16;
 constexpr int kTcMaxToep = kTcIssuers * kTcRingSlots;
-constexpr int kTcMaxBox = 256;      // TMA box extent limit (plane rows)
+constexpr int kTcMaxBox = 256;      // most staged rows per plane
 // barriers (plane and run rings, two accumulator buffers, the final MMA barriers, the
 // epilogue warps' exchange of paired rows), the tensor-memory address and the abort flag
 constexpr int kTcBarBytes =
@@ -106,6 +108,8 @@ constexpr int kTcXFloats = 128;
 constexpr int kTcXBytes = kTcEpiWarps * 2 * kTcXFloats * 4;
 
 struct TcArgs {
+    const unsigned char* planes; // plane-major stacked copy [C][np][vp rows][8 columns], 16-bit
+    const unsigned char* zeros;  // MR * 16 zero bytes (planes outside the copy)
     const unsigned char* runs;   // Toeplitz runs [C][FHI][(pair + 1) * NCM core matrices], 16-bit
     void* out;          // N x OH x OW x C, OutT
     unsigned int* status;
@@ -130,6 +134,8 @@ struct TcArgs {
     int rps;            // filter rows per ring item (1 .. kTcRunsPerSlot)
     int rslots, rshift; // slots per run ring (4, or 2 for items of 3 or 4 rows) and its log2
     uint32_t units, col_tiles;
+    int np;             // planes of the stacked copy
+    uint32_t vp;        // rows of a plane (the V virtual rows, then zero rows)
     FastDiv fd_S;
     uint32_t plane_bytes, toep_bytes;   // one plane; one run (a pair of runs in pairs)
     uint32_t off_toep, off_bar, off_x;  // byte offsets in shared memory
@@ -320,86 +326,124 @@ __device__ __forceinline__ void tc_store_pixel(OutT* dst, const float (&v)[CG]) 
     }
 }
 
+// ------------------------------------------------------------------ plane-major stacked copy
+
+// Plane-major stacked copy of `src` (nn x h x w x C, 16-bit):
+//   dst[c][p][ro + v][e] = src[n][v % S - pad_h][8 p + e - lp][c],  n = v / S,  zero outside,
+// for planes p < wp / 8 and plane rows ro + v in [0, vp) (zero rows before and after the
+// V = nn * S virtual rows).  A tile is 16 virtual rows x one plane x
+// CT channels: pixels are read as 16-byte pieces of 8 channels (whole 128-byte lines for 64
+// channels), and every thread writes the 8 columns of one channel and row as 16 bytes,
+// consecutive threads along the rows of a plane.
+struct TcStackArgs {
+    const void* src;
+    void* dst;
+    int nn, h, w, C, pad_h, S, lp, np;   // np: planes (wp / 8)
+    int V, ro, vp;      // virtual rows; zero rows before them; rows of a plane
+    int CT, piece_shift;
+    int tiles;          // ceil(vp / 16) * np * (C / CT)
+    FastDiv fd_np, fd_ct, fd_S;
+};
+
+constexpr int kStackRows = 16;
+constexpr int kStackWords = 33;   // a (column, row) pixel's 64 channels as 32 words + 1 pad
+
+// One tile of copy `a` (the block's threads; `tile` is the block's shared staging).
+template <typename T>
+__device__ __forceinline__ void tc_stack_tile(const TcStackArgs& a, int tt, uint32_t* tile) {
+    const T* X = static_cast<const T*>(a.src);
+    T* P = static_cast<T*>(a.dst);
+    const int pieces = a.CT / 8;
+    {
+        uint32_t cb, pl;
+        const uint32_t q = a.fd_ct.divmod(static_cast<uint32_t>(tt), cb);
+        const int rb = static_cast<int>(a.fd_np.divmod(q, pl));
+        const int c0 = a.CT * static_cast<int>(cb);
+        const int v0 = rb * kStackRows;
+        __syncthreads();   // the previous tile's reads are done
+        for (int idx = threadIdx.x; idx < kStackRows * 8 * pieces; idx += blockDim.x) {
+            const int i = idx >> a.piece_shift, j = idx - (i << a.piece_shift);
+            const int r = i >> 3, e = i & 7;   // row of the tile, column of the plane
+            const int v = v0 + r - a.ro;        // virtual row
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (v >= 0 && v < a.V) {
+                uint32_t hr;
+                const int n = static_cast<int>(a.fd_S.divmod(static_cast<uint32_t>(v), hr));
+                const int hh = static_cast<int>(hr) - a.pad_h;
+                const int col = 8 * static_cast<int>(pl) + e - a.lp;
+                if (hh >= 0 && hh < a.h && col >= 0 && col < a.w)
+                    val = __ldg(reinterpret_cast<const uint4*>(
+                        X + ((static_cast<size_t>(n) * a.h + hh) * a.w + col) * a.C + c0 + 8 * j));
+            }
+            uint32_t* d = tile + (e * kStackRows + r) * kStackWords + 4 * j;
+            d[0] = val.x; d[1] = val.y; d[2] = val.z; d[3] = val.w;
+        }
+        __syncthreads();
+        // task (channel pair cp, row r): the pair's word of the plane's 8 columns
+        for (int idx = threadIdx.x; idx < (a.CT / 2) * kStackRows; idx += blockDim.x) {
+            const int r = idx & (kStackRows - 1), cp = idx >> 4;
+            const int v = v0 + r;               // plane row
+            if (v >= a.vp) continue;
+            uint32_t wd[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wd[e] = tile[(e * kStackRows + r) * kStackWords + cp];
+            uint4 lo, hi;
+            lo.x = __byte_perm(wd[0], wd[1], 0x5410); hi.x = __byte_perm(wd[0], wd[1], 0x7632);
+            lo.y = __byte_perm(wd[2], wd[3], 0x5410); hi.y = __byte_perm(wd[2], wd[3], 0x7632);
+            lo.z = __byte_perm(wd[4], wd[5], 0x5410); hi.z = __byte_perm(wd[4], wd[5], 0x7632);
+            lo.w = __byte_perm(wd[6], wd[7], 0x5410); hi.w = __byte_perm(wd[6], wd[7], 0x7632);
+            const size_t plane = static_cast<size_t>(a.vp) * 8;   // elements of one plane
+            T* dst = P + (static_cast<size_t>(c0 + 2 * cp) * a.np + pl) * plane + static_cast<size_t>(v) * 8;
+            *reinterpret_cast<uint4*>(dst) = lo;
+            *reinterpret_cast<uint4*>(dst + static_cast<size_t>(a.np) * plane) = hi;
+        }
+    }
+}
+
+inline bool tc_stack_args(TcStackArgs& q, const void* src, void* dst, int nn, int h, int w, int C, int pad_h,
+                          int S, int lp, int wp, int ro, int vp) {
+    q.src = src; q.dst = dst;
+    q.nn = nn; q.h = h; q.w = w; q.C = C; q.pad_h = pad_h; q.S = S; q.lp = lp; q.np = wp / 8;
+    q.CT = C % 64 == 0 ? 64 : (C % 32 == 0 ? 32 : (C % 16 == 0 ? 16 : 8));
+    q.piece_shift = q.CT == 64 ? 3 : (q.CT == 32 ? 2 : (q.CT == 16 ? 1 : 0));
+    const long long V = static_cast<long long>(nn) * S;
+    const long long tiles = (static_cast<long long>(vp) + kStackRows - 1) / kStackRows * q.np * (C / q.CT);
+    if (V >= (1LL << 31) || tiles >= (1LL << 30)) return false;
+    q.V = static_cast<int>(V);
+    q.ro = ro;
+    q.vp = vp;
+    q.tiles = static_cast<int>(tiles);
+    q.fd_np.init(static_cast<uint32_t>(q.np));
+    q.fd_ct.init(static_cast<uint32_t>(C / q.CT));
+    q.fd_S.init(static_cast<uint32_t>(S));
+    return true;
+}
+
+
 // ------------------------------------------------------------------ preparation kernel
 
 struct TcPrepArgs {
-    const void* x;      // N x H x W x C, 16-bit
+    TcStackArgs st;     // the plane-major stacked copy of the input
     const void* w;      // FH x FW x C, 16-bit
-    void* planes;       // C x V x Wp stacked copy (V = N * S virtual rows), 16-bit
     void* runs;         // C x FHI runs of (pair + 1) * 8 * NCM rows of 8 values, 16-bit
-    int N, H, W, C, FH, FW, pad_h, S, Lp, Wp, NN, NCM;
+    int C, FH, FW, NN, NCM;
     int FHI, pair;      // run items per channel; 1: two filter rows' runs interleaved
-    int CT;                  // channels of a copy tile (64, 32, 16 or 8, dividing C)
-    int piece_shift;         // log2(CT / 8): 16-byte pieces of a pixel in a copy tile
-    int V;                   // N * S
-    int plane_tiles;         // V * (C / CT) * ceil(Wp / 64) tiles of one row
     int run_tasks;           // C * FHI * (pair + 1) * 8 * NCM: one 16-byte row of a run
     int run_blocks;          // blocks [0, run_blocks) write the runs, the rest the copy
     // divisions by launch constants (all operands below 2^31)
-    FastDiv fd_xt, fd_ct, fd_S, fd_C, fd_rows;
+    FastDiv fd_C, fd_rows;
 };
 
 constexpr int kTcPrepThreads = 256;
-constexpr int kTcPrepCols = 64;      // copy tile: 64 columns x up to 64 channels of one row
-constexpr int kTcPrepRowWords = 33;  // shared row of a pixel: 64 channels + one pad word
 
 template <typename T, bool FLIP>
 __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const TcPrepArgs a) {
-    __shared__ uint32_t tile[kTcPrepCols * kTcPrepRowWords];
+    __shared__ uint32_t tile[8 * kStackRows * kStackWords];
     if (static_cast<int>(blockIdx.x) >= a.run_blocks) {
-        // Stacked copy: planes[c][v][x] = x[n][h][x - Lp][c] with n = v / S, h = v % S - pad_h,
-        // zero outside the image.  A tile is 64 columns x CT channels of one virtual row:
-        // the pixels' channels are read as contiguous 16-byte pieces into a shared tile
-        // (one pixel per row, padded to spread the banks), then every thread writes 8
-        // columns of one channel as 16 bytes, consecutive threads along the row.
-        const T* X = static_cast<const T*>(a.x);
-        T* P = static_cast<T*>(a.planes);
-        const int pieces = a.CT / 8;                 // 16-byte pieces of a pixel
+        // the plane-major stacked copy, tile by tile
         const int nb = static_cast<int>(gridDim.x) - a.run_blocks;
-        for (int tt = static_cast<int>(blockIdx.x) - a.run_blocks; tt < a.plane_tiles; tt += nb) {
-            uint32_t xb, cb, hr;
-            const uint32_t q = a.fd_xt.divmod(static_cast<uint32_t>(tt), xb);
-            const int v = static_cast<int>(a.fd_ct.divmod(q, cb));
-            const int n = static_cast<int>(a.fd_S.divmod(static_cast<uint32_t>(v), hr));
-            const int h = static_cast<int>(hr) - a.pad_h;
-            const bool row_in = h >= 0 && h < a.H;
-            const int xa = kTcPrepCols * static_cast<int>(xb);
-            const int c0 = a.CT * static_cast<int>(cb);
-            __syncthreads();   // the previous tile's reads are done
-            if (row_in) {
-                const T* src = X + (static_cast<size_t>(n) * a.H + h) * static_cast<size_t>(a.W) * a.C + c0;
-                for (int idx = threadIdx.x; idx < kTcPrepCols * pieces; idx += kTcPrepThreads) {
-                    const int i = idx >> a.piece_shift, j = idx - (i << a.piece_shift);
-                    const int col = xa + i - a.Lp;
-                    const uint4 val = (col >= 0 && col < a.W)
-                                          ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(col) * a.C + 8 * j))
-                                          : make_uint4(0u, 0u, 0u, 0u);
-                    uint32_t* d = tile + i * kTcPrepRowWords + 4 * j;
-                    d[0] = val.x; d[1] = val.y; d[2] = val.z; d[3] = val.w;
-                }
-            }
-            __syncthreads();
-            const int chunks = min(kTcPrepCols, a.Wp - xa) / 8;
-            // a task: the 8 columns of chunk k of the channel pair (2cp, 2cp + 1), from the
-            // same 8 shared words (one word holds both channels of a column)
-            for (int idx = threadIdx.x; idx < (a.CT / 2) * 8; idx += kTcPrepThreads) {
-                const int k = idx & 7, cp = idx >> 3;
-                if (k >= chunks) continue;
-                uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                if (row_in) {
-                    uint32_t wd[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) wd[e] = tile[(8 * k + e) * kTcPrepRowWords + cp];
-                    lo.x = __byte_perm(wd[0], wd[1], 0x5410); hi.x = __byte_perm(wd[0], wd[1], 0x7632);
-                    lo.y = __byte_perm(wd[2], wd[3], 0x5410); hi.y = __byte_perm(wd[2], wd[3], 0x7632);
-                    lo.z = __byte_perm(wd[4], wd[5], 0x5410); hi.z = __byte_perm(wd[4], wd[5], 0x7632);
-                    lo.w = __byte_perm(wd[6], wd[7], 0x5410); hi.w = __byte_perm(wd[6], wd[7], 0x7632);
-                }
-                T* dst = P + (static_cast<size_t>(c0 + 2 * cp) * a.V + v) * a.Wp + xa + 8 * k;
-                *reinterpret_cast<uint4*>(dst) = lo;
-                *reinterpret_cast<uint4*>(dst + static_cast<size_t>(a.V) * a.Wp) = hi;
-            }
-        }
+        for (int tt = static_cast<int>(blockIdx.x) - a.run_blocks; tt < a.st.tiles; tt += nb)
+            tc_stack_tile<T>(a.st, tt, tile);
     } else {
         // Runs: row r of the run of (c, fh) holds z[r .. r+7], z[i] = filt(fh, i - (NN-1)),
         // zero outside the filter; filt is w, or w rotated by 180 degrees (backward data).
@@ -449,7 +493,7 @@ __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const TcPrepArg
 
 template <typename T, class OutT, int CG, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
-tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
+tc_rows_kernel(const TcArgs a) {
     // issuers per channel: 1 (each issuer owns whole channels), or 2 in groups of 2 channels
     // (filter-row parities into two partial sums, one filter row per ring item)
     constexpr int PART = CG >= kTcIssuers ? 1 : kTcIssuers / CG;
@@ -762,31 +806,38 @@ tc_rows_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
         __syncwarp();
     } else {
         // ------------------------------------------------------------- plane feeder
-        // The unit's CG planes, in channel order, at ring positions pos, pos+1, ...: one TMA
-        // box (8 columns x MR rows of one channel) per 8-column plane.
-        if (lane == 0) {
-            prefetch_tensormap(&xmap);
-            const uint32_t ps = static_cast<uint32_t>(a.ps);
-            const int kc = 2 * a.KS;
-            uint32_t pos = 0;
-            bool ok = true;
-            for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                int t, j, g;
-                tc_unit(a, u, t, j, g);
-                const TcTile tl = tc_tile(a, t);
-                const int xc = j * a.TWc + a.x0;
-                for (int ch = 0; ch < CG; ++ch, ++pos) {
-                    const uint32_t slot = pos % ps, phase = (pos / ps) & 1u;
-                    if (!tc_wait(&plane_empty[slot], phase ^ 1u, a, abort_flag)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&plane_full[slot], a.plane_bytes);
-                    unsigned char* dst = planes + static_cast<size_t>(slot) * a.plane_bytes;
-                    for (int b = 0; b < kc; ++b)
-                        tma_load_3d(dst + static_cast<size_t>(b) * a.MR * 16u, &xmap, &plane_full[slot],
-                                    xc + 8 * b, tl.v0, a.cbase + g * CG + ch);
+        // The unit's CG planes, in channel order, at ring positions pos, pos+1, ...: lane b
+        // copies plane b of the channel (MR rows from the tile's first virtual row, one bulk
+        // copy of a contiguous band of the plane-major copy; a plane outside the copy comes
+        // from the zero band).
+        const size_t pbytes = static_cast<size_t>(a.vp) * 16;
+        const uint32_t ps = static_cast<uint32_t>(a.ps);
+        const int kc = 2 * a.KS;
+        const uint32_t band = static_cast<uint32_t>(a.MR) * 16u;
+        uint32_t pos = 0;
+        bool ok = true;
+        for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            int t, j, g;
+            tc_unit(a, u, t, j, g);
+            const TcTile tl = tc_tile(a, t);
+            const int p0 = (j * a.TWc + a.x0) / 8;   // first plane of the column tile
+            for (int ch = 0; ch < CG; ++ch, ++pos) {
+                const uint32_t slot = pos % ps, phase = (pos / ps) & 1u;
+                if (!tc_wait_warp(&plane_empty[slot], phase ^ 1u, a, abort_flag)) { ok = false; break; }
+                if (lane == 0) mbar_arrive_expect_tx(&plane_full[slot], a.plane_bytes);
+                __syncwarp();
+                if (lane < kc) {
+                    const int c = a.cbase + g * CG + ch, pl = p0 + lane;
+                    const unsigned char* src =
+                        pl >= 0 && pl < a.np
+                            ? a.planes + (static_cast<size_t>(c) * a.np + pl) * pbytes + static_cast<size_t>(tl.v0) * 16
+                            : a.zeros;
+                    tc_bulk_load(planes + static_cast<size_t>(slot) * a.plane_bytes + static_cast<size_t>(lane) * band,
+                                 src, band, &plane_full[slot]);
                 }
             }
-            tc_drain(plane_full, 0, ps, pos, a);
         }
+        if (lane == 0) tc_drain(plane_full, 0, ps, pos, a);
         __syncwarp();
     }
 
@@ -852,7 +903,7 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     };
     if (static_cast<long long>(p.N + 1) * a.S + 2 * kTcM >= (1LL << 31)) return false;
     a.MR = (p.FH + kTcM - 1 + 7) / 8 * 8;
-    if (a.MR > kTcMaxBox) return false;   // one TMA box per plane
+    if (a.MR > kTcMaxBox) return false;   // staged rows per plane
     // Row pairing, column tile, channel group and filter rows per ring item, chosen together
     // by an estimate of the busiest SM's cycles: per unit (units spread evenly over the SMs,
     // whole units only) the longer of the tensor core's MMA time and an issuer's time (a fixed
@@ -941,11 +992,17 @@ inline bool tc_plan(const RowConv& p, TcPlan& P) {
     a.rshift = best_rslots == 4 ? 2 : 1;
     // stacked copy: input column w at column w + Lp, Lp = pad_w mod 8, so that a tile's first
     // column j*TWc - pad_w lands on a multiple of 8 (x0 = Lp - pad_w); the copy spans the
-    // image and, to the right, every column a tile reads (beyond it the TMA box reads zeros)
+    // image (planes outside it are read from a zero band)
     P.Lp = p.pad_w % 8;
     a.x0 = P.Lp - p.pad_w;
     P.Wp = (P.Lp + p.W + 7) / 8 * 8;
-    P.planes_bytes = static_cast<size_t>(p.C) * static_cast<size_t>(p.N) * a.S * P.Wp * 2;
+    // plane-major copy: the V virtual rows of every 8-column plane, then MR zero rows (the
+    // last tile's band reads past V)
+    a.np = P.Wp / 8;
+    const long long vp = static_cast<long long>(p.N) * a.S + a.MR;
+    if (vp >= (1LL << 31)) return false;
+    a.vp = static_cast<uint32_t>(vp);
+    P.planes_bytes = static_cast<size_t>(p.C) * a.np * a.vp * 16;
     P.runs_bytes = static_cast<size_t>(p.C) * a.FHI * a.toep_bytes;
     // shared memory: plane ring, run rings, barriers, the paired rows' exchange; one CTA per
     // SM (each allocates all of tensor memory): ask for more than half of it
@@ -966,24 +1023,23 @@ inline uint32_t tc_idesc(int n) {
 
 // One launch of the main kernel with groups of CG channels (filter rows in pairs or single).
 template <typename T, class OutT, int CG, bool PAIR>
-cudaError_t launch_tc_main(const TcArgs& a, size_t smem, const CUtensorMap& xmap, cudaStream_t stream) {
+cudaError_t launch_tc_main(const TcArgs& a, size_t smem, cudaStream_t stream) {
     auto kern = tc_rows_kernel<T, OutT, CG, PAIR>;
     static DeviceOnce smem_opt_in;
     const cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
     if (err != cudaSuccess) return err;
     const unsigned grid = static_cast<unsigned>(
         std::min<long long>(a.units, static_cast<long long>(device_info().sm_count)));
-    kern<<<grid, kTcThreads, smem, stream>>>(xmap, a);
+    kern<<<grid, kTcThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
 template <typename T, class OutT>
-cudaError_t launch_tc_main_cg(int cg, bool pair, const TcArgs& a, size_t smem, const CUtensorMap& xmap,
-                              cudaStream_t stream) {
-    if (pair) return cg == 4 ? launch_tc_main<T, OutT, 4, true>(a, smem, xmap, stream) : cudaErrorNotSupported;
+cudaError_t launch_tc_main_cg(int cg, bool pair, const TcArgs& a, size_t smem, cudaStream_t stream) {
+    if (pair) return cg == 4 ? launch_tc_main<T, OutT, 4, true>(a, smem, stream) : cudaErrorNotSupported;
     switch (cg) {
-        case 2: return launch_tc_main<T, OutT, 2, false>(a, smem, xmap, stream);
-        case 4: return launch_tc_main<T, OutT, 4, false>(a, smem, xmap, stream);
+        case 2: return launch_tc_main<T, OutT, 2, false>(a, smem, stream);
+        case 4: return launch_tc_main<T, OutT, 4, false>(a, smem, stream);
         default: return cudaErrorNotSupported;
     }
 }
@@ -994,64 +1050,51 @@ cudaError_t launch_tc_rows(const RowConv& p) {
     if (!tc_plan(p, P)) return cudaErrorNotSupported;
     if (P.a.units == 0) return cudaSuccess;
     const TcArgs& a = P.a;
-    // scratch of this call: the stacked copy, then the run table (128-byte aligned)
+    // scratch of this call: the stacked copy, the run table, a zero band (128-byte aligned)
     const size_t runs_off = (P.planes_bytes + 127) / 128 * 128;
+    const size_t z_off = runs_off + (P.runs_bytes + 127) / 128 * 128;
+    const size_t z_bytes = (static_cast<size_t>(a.MR) * 16 + 127) / 128 * 128;
+    const long long run_tasks = static_cast<long long>(p.C) * a.FHI * 8 * a.NCM * (a.pair + 1);
+    if (run_tasks >= (1LL << 31)) return cudaErrorNotSupported;
+    // preparation: the plane-major stacked copy, the runs, and the zero band
+    TcPrepArgs q;
+    if (!tc_stack_args(q.st, p.in, nullptr, p.N, p.H, p.W, p.C, p.pad_h, a.S, P.Lp, P.Wp, 0,
+                       static_cast<int>(a.vp)))
+        return cudaErrorNotSupported;
     void* scratch = nullptr;
-    if (scratch_alloc(&scratch, runs_off + P.runs_bytes, p.stream) != cudaSuccess) {
+    if (scratch_alloc(&scratch, z_off + z_bytes, p.stream) != cudaSuccess) {
         (void)cudaGetLastError();
         return cudaErrorNotSupported;   // the caller takes another kernel
     }
     unsigned char* base = static_cast<unsigned char*>(scratch);
-    const long long V = static_cast<long long>(p.N) * a.S;
-    CUtensorMap xmap;
-    {
-        const cuuint64_t dims[3] = {(cuuint64_t)P.Wp, (cuuint64_t)V, (cuuint64_t)p.C};
-        const cuuint64_t strides[2] = {(cuuint64_t)P.Wp * 2, (cuuint64_t)V * P.Wp * 2};
-        const cuuint32_t box[3] = {8u, (cuuint32_t)a.MR, 1u};
-        if (encode_tiled(&xmap, Elem<T>::kTmaType, 3, base, dims, strides, box) != CUDA_SUCCESS) {
-            scratch_free(scratch, p.stream);
-            return cudaErrorNotSupported;
-        }
-    }
-    // preparation: the stacked copy and the runs
-    TcPrepArgs q;
-    q.x = p.in; q.w = p.w; q.planes = base; q.runs = base + runs_off;
-    q.N = p.N; q.H = p.H; q.W = p.W; q.C = p.C; q.FH = p.FH; q.FW = p.FW; q.pad_h = p.pad_h;
-    q.S = a.S; q.Lp = P.Lp; q.Wp = P.Wp; q.NN = a.NN; q.NCM = a.NCM;
+    q.st.dst = base;
+    q.w = p.w; q.runs = base + runs_off;
+    q.C = p.C; q.FH = p.FH; q.FW = p.FW; q.NN = a.NN; q.NCM = a.NCM;
     q.FHI = a.FHI; q.pair = a.pair;
-    q.CT = p.C % 64 == 0 ? 64 : (p.C % 32 == 0 ? 32 : (p.C % 16 == 0 ? 16 : 8));
-    q.piece_shift = q.CT == 64 ? 3 : (q.CT == 32 ? 2 : (q.CT == 16 ? 1 : 0));
-    const long long xtiles = (P.Wp + kTcPrepCols - 1) / kTcPrepCols;
-    const long long plane_tiles = V * (p.C / q.CT) * xtiles;
-    const long long run_tasks = static_cast<long long>(p.C) * a.FHI * 8 * a.NCM * (a.pair + 1);
-    if (V >= (1LL << 31) || plane_tiles >= (1LL << 31) || run_tasks >= (1LL << 31)) {
-        scratch_free(scratch, p.stream);
-        return cudaErrorNotSupported;
-    }
-    q.V = static_cast<int>(V);
-    q.plane_tiles = static_cast<int>(plane_tiles);
     q.run_tasks = static_cast<int>(run_tasks);
-    q.fd_xt.init(static_cast<uint32_t>(xtiles));
-    q.fd_ct.init(static_cast<uint32_t>(p.C / q.CT));
-    q.fd_S.init(static_cast<uint32_t>(a.S));
     q.fd_C.init(static_cast<uint32_t>(p.C));
     q.fd_rows.init(static_cast<uint32_t>(8 * a.NCM * (a.pair + 1)));
     const int sms = device_info().sm_count;
     q.run_blocks = static_cast<int>(
         std::min<long long>((run_tasks + kTcPrepThreads - 1) / kTcPrepThreads, 4LL * sms));
-    const int plane_blocks = static_cast<int>(std::min<long long>(q.plane_tiles, 16LL * sms));
+    const int plane_blocks = static_cast<int>(std::min<long long>(q.st.tiles, 16LL * sms));
     const unsigned prep_grid = static_cast<unsigned>(q.run_blocks + plane_blocks);
-    if (p.flip) tc_prep_kernel<T, true><<<prep_grid, kTcPrepThreads, 0, p.stream>>>(q);
-    else tc_prep_kernel<T, false><<<prep_grid, kTcPrepThreads, 0, p.stream>>>(q);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = cudaMemsetAsync(base + z_off, 0, z_bytes, p.stream);
+    if (err == cudaSuccess) {
+        if (p.flip) tc_prep_kernel<T, true><<<prep_grid, kTcPrepThreads, 0, p.stream>>>(q);
+        else tc_prep_kernel<T, false><<<prep_grid, kTcPrepThreads, 0, p.stream>>>(q);
+        err = cudaGetLastError();
+    }
     // the main kernel
     TcArgs m = a;
+    m.planes = base;
+    m.zeros = base + z_off;
     m.runs = base + runs_off;
     m.out = p.out;
     m.status = p.status;
     m.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     m.idesc = tc_idesc<T>(a.NN * (a.pair + 1));
-    if (err == cudaSuccess) err = launch_tc_main_cg<T, OutT>(P.cg, P.pair, m, P.smem, xmap, p.stream);
+    if (err == cudaSuccess) err = launch_tc_main_cg<T, OutT>(P.cg, P.pair, m, P.smem, p.stream);
     // stream-ordered: the memory returns to the pool once the kernels have run
     scratch_free(scratch, p.stream);
     return err;

@@ -26,7 +26,7 @@
 // filter rows) over every row and column tile: its accumulators hold the whole sum, so the
 // epilogue writes dw directly (no partial slices) after summing the diagonals.
 //
-// Three launches: a preparation kernel writes the stacked copies of x (the forward's padding)
+// Two launches: a preparation kernel writes the stacked copies of x (the forward's padding)
 // and of dy (no padding), plane-major -- every 8-column plane of a channel holds its virtual
 // rows contiguously, with zero rows before and after -- then the main kernel, which moves
 // each stage's plane bands with bulk copies (2 KB contiguous each).  Tensor-map boxes of
@@ -327,99 +327,17 @@ inline uint32_t tc_fgrad_idesc() {
            (static_cast<uint32_t>(64 * kTfgRowsPerMma >> 3) << 17) | (static_cast<uint32_t>(kTcM >> 4) << 24);
 }
 
-// Plane-major stacked copy of `src` (nn x h x w x C, 16-bit):
-//   dst[c][p][ro + v][e] = src[n][v % S - pad_h][8 p + e - lp][c],  n = v / S,  zero outside,
-// for planes p < wp / 8 and plane rows ro + v in [0, vp) (zero rows before and after the
-// V = nn * S virtual rows).  A tile is 16 virtual rows x one plane x
-// CT channels: pixels are read as 16-byte pieces of 8 channels (whole 128-byte lines for 64
-// channels), and every thread writes the 8 columns of one channel and row as 16 bytes,
-// consecutive threads along the rows of a plane.
-struct TcStackArgs {
-    const void* src;
-    void* dst;
-    int nn, h, w, C, pad_h, S, lp, np;   // np: planes (wp / 8)
-    int V, ro, vp;      // virtual rows; zero rows before them; rows of a plane
-    int CT, piece_shift;
-    int tiles;          // ceil(vp / 16) * np * (C / CT)
-    FastDiv fd_np, fd_ct, fd_S;
-};
-
-constexpr int kStackRows = 16;
-constexpr int kStackWords = 33;   // a (column, row) pixel's 64 channels as 32 words + 1 pad
-
+// Both stacked copies of a call (the tiles of x, then those of dy) and the zero band.
 template <typename T>
-__global__ void __launch_bounds__(256) tc_stack_pm_kernel(const TcStackArgs a) {
+__global__ void __launch_bounds__(256) tc_stack_pm_kernel(const TcStackArgs ax, const TcStackArgs ady,
+                                                          uint4* zeros, int zero_words) {
     __shared__ uint32_t tile[8 * kStackRows * kStackWords];   // [column][row][words]
-    const T* X = static_cast<const T*>(a.src);
-    T* P = static_cast<T*>(a.dst);
-    const int pieces = a.CT / 8;
-    for (int tt = blockIdx.x; tt < a.tiles; tt += gridDim.x) {
-        uint32_t cb, pl;
-        const uint32_t q = a.fd_ct.divmod(static_cast<uint32_t>(tt), cb);
-        const int rb = static_cast<int>(a.fd_np.divmod(q, pl));
-        const int c0 = a.CT * static_cast<int>(cb);
-        const int v0 = rb * kStackRows;
-        __syncthreads();   // the previous tile's reads are done
-        for (int idx = threadIdx.x; idx < kStackRows * 8 * pieces; idx += blockDim.x) {
-            const int i = idx >> a.piece_shift, j = idx - (i << a.piece_shift);
-            const int r = i >> 3, e = i & 7;   // row of the tile, column of the plane
-            const int v = v0 + r - a.ro;        // virtual row
-            uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            if (v >= 0 && v < a.V) {
-                uint32_t hr;
-                const int n = static_cast<int>(a.fd_S.divmod(static_cast<uint32_t>(v), hr));
-                const int hh = static_cast<int>(hr) - a.pad_h;
-                const int col = 8 * static_cast<int>(pl) + e - a.lp;
-                if (hh >= 0 && hh < a.h && col >= 0 && col < a.w)
-                    val = __ldg(reinterpret_cast<const uint4*>(
-                        X + ((static_cast<size_t>(n) * a.h + hh) * a.w + col) * a.C + c0 + 8 * j));
-            }
-            uint32_t* d = tile + (e * kStackRows + r) * kStackWords + 4 * j;
-            d[0] = val.x; d[1] = val.y; d[2] = val.z; d[3] = val.w;
-        }
-        __syncthreads();
-        // task (channel pair cp, row r): the pair's word of the plane's 8 columns
-        for (int idx = threadIdx.x; idx < (a.CT / 2) * kStackRows; idx += blockDim.x) {
-            const int r = idx & (kStackRows - 1), cp = idx >> 4;
-            const int v = v0 + r;               // plane row
-            if (v >= a.vp) continue;
-            uint32_t wd[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) wd[e] = tile[(e * kStackRows + r) * kStackWords + cp];
-            uint4 lo, hi;
-            lo.x = __byte_perm(wd[0], wd[1], 0x5410); hi.x = __byte_perm(wd[0], wd[1], 0x7632);
-            lo.y = __byte_perm(wd[2], wd[3], 0x5410); hi.y = __byte_perm(wd[2], wd[3], 0x7632);
-            lo.z = __byte_perm(wd[4], wd[5], 0x5410); hi.z = __byte_perm(wd[4], wd[5], 0x7632);
-            lo.w = __byte_perm(wd[6], wd[7], 0x5410); hi.w = __byte_perm(wd[6], wd[7], 0x7632);
-            const size_t plane = static_cast<size_t>(a.vp) * 8;   // elements of one plane
-            T* dst = P + (static_cast<size_t>(c0 + 2 * cp) * a.np + pl) * plane + static_cast<size_t>(v) * 8;
-            *reinterpret_cast<uint4*>(dst) = lo;
-            *reinterpret_cast<uint4*>(dst + static_cast<size_t>(a.np) * plane) = hi;
-        }
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zeros[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int tt = blockIdx.x; tt < ax.tiles + ady.tiles; tt += gridDim.x) {
+        if (tt < ax.tiles) tc_stack_tile<T>(ax, tt, tile);
+        else tc_stack_tile<T>(ady, tt - ax.tiles, tile);
     }
-}
-
-template <typename T>
-cudaError_t tc_fgrad_stack(const void* src, void* dst, int nn, int h, int w, int C, int pad_h, int S,
-                           int lp, int wp, int vp, cudaStream_t stream) {
-    TcStackArgs q;
-    q.src = src; q.dst = dst;
-    q.nn = nn; q.h = h; q.w = w; q.C = C; q.pad_h = pad_h; q.S = S; q.lp = lp; q.np = wp / 8;
-    q.CT = C % 64 == 0 ? 64 : (C % 32 == 0 ? 32 : (C % 16 == 0 ? 16 : 8));
-    q.piece_shift = q.CT == 64 ? 3 : (q.CT == 32 ? 2 : (q.CT == 16 ? 1 : 0));
-    const long long V = static_cast<long long>(nn) * S;
-    const long long tiles = (static_cast<long long>(vp) + kStackRows - 1) / kStackRows * q.np * (C / q.CT);
-    if (V >= (1LL << 31) || tiles >= (1LL << 31)) return cudaErrorNotSupported;
-    q.V = static_cast<int>(V);
-    q.ro = kTfgRO;
-    q.vp = vp;
-    q.tiles = static_cast<int>(tiles);
-    q.fd_np.init(static_cast<uint32_t>(q.np));
-    q.fd_ct.init(static_cast<uint32_t>(C / q.CT));
-    q.fd_S.init(static_cast<uint32_t>(S));
-    const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, 16LL * device_info().sm_count));
-    tc_stack_pm_kernel<T><<<grid, 256, 0, stream>>>(q);
-    return cudaGetLastError();
 }
 
 template <typename T>
@@ -437,11 +355,17 @@ cudaError_t launch_tc_fgrad(const FilterGrad& p) {
     }
     unsigned char* base = static_cast<unsigned char*>(scratch);
     const int vp = static_cast<int>(P.a.vp);
-    cudaError_t err = cudaMemsetAsync(base + z_off, 0, z_bytes, p.stream);
-    if (err == cudaSuccess)
-        err = tc_fgrad_stack<T>(p.x, base, p.N, p.H, p.W, p.C, p.pad, P.S, P.Lp, P.Wp, vp, p.stream);
-    if (err == cudaSuccess)
-        err = tc_fgrad_stack<T>(p.dy, base + dy_off, p.N, p.OH, p.OW, p.C, 0, P.S, 0, P.Wdp, vp, p.stream);
+    TcStackArgs sx, sdy;
+    if (!tc_stack_args(sx, p.x, base, p.N, p.H, p.W, p.C, p.pad, P.S, P.Lp, P.Wp, kTfgRO, vp) ||
+        !tc_stack_args(sdy, p.dy, base + dy_off, p.N, p.OH, p.OW, p.C, 0, P.S, 0, P.Wdp, kTfgRO, vp)) {
+        scratch_free(scratch, p.stream);
+        return cudaErrorNotSupported;
+    }
+    const unsigned sgrid = static_cast<unsigned>(
+        std::min<long long>(static_cast<long long>(sx.tiles) + sdy.tiles, 16LL * device_info().sm_count));
+    tc_stack_pm_kernel<T><<<sgrid, 256, 0, p.stream>>>(sx, sdy, reinterpret_cast<uint4*>(base + z_off),
+                                                       static_cast<int>(z_bytes / 16));
+    cudaError_t err = cudaGetLastError();
     if (err == cudaSuccess) {
         TcFgArgs a = P.a;
         a.xpl = base;

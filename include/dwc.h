@@ -232,7 +232,7 @@ int dwc_path(int pass, const void* a, const void* b, const void* out,
 
 /* Kernel launches of this library that a call with these arguments and 16-byte aligned
  * pointers makes (the tcgen05 forward / backward data: a preparation kernel and the main
- * kernel; the tcgen05 filter gradient: two preparation kernels and the main kernel; other
+ * kernel; the tcgen05 filter gradient: one preparation kernel and the main kernel; other
  * filter gradients: the kernel and the sum of its slices), 0 for an empty output, -1 for
  * invalid arguments.  `pass` as for dwc_path.  For profiling and launch accounting. */
 int dwc_kernel_launches(int pass, int N, int H, int W, int C, int FH, int FW, int stride, int pad,

@@ -216,7 +216,7 @@ def test_kernel_launch_counts(lib):
     assert n(0, **dict(f7, C=32)) == 1                     # the tail is the only launch
     big = dict(N=32, H=56, W=56, C=128, FH=31, FW=31, pad=15, dtype=1)
     assert n(0, **big) == 2 and n(1, **big) == 2          # tcgen05: preparation + main
-    assert n(2, **big) == 3                               # tcgen05 gradient: 2 copies + main
+    assert n(2, **big) == 2                               # tcgen05 gradient: copies + main
     assert n(2, **dict(big, dtype=0)) == 2                # fp32: kernel + slice sum
     assert n(0, **dict(big, N=0)) == 0
     assert n(0, FH=4, FW=4, **{k: v for k, v in GOOD.items() if k not in ("FH", "FW")}) == 1
