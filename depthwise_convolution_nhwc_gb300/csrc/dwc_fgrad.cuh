@@ -94,6 +94,7 @@ struct FgradArgs {
     float* part;           // [Z * ncp][FH][FW][C] partial sums
     unsigned int* status;
     int N, OH, C, pad;
+    int c_lo;              // first channel of the launch's channel blocks
     int FH;                // filter rows (the template's, or any for a stripe tile, FH = 0)
     int ncp, owpart;       // column parts of a row, output columns per part
     int nwf, nwc;          // compute warps: filter-row groups x column strips
@@ -213,7 +214,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             if (xissued < static_cast<uint32_t>(a.nx)) ++xissued;
             mbar_arrive_expect_tx(&xfull[xr.slot], a.x_tx);
             tma_load_4d(xring + static_cast<size_t>(xr.slot) * a.x_bytes, &xmap, &xfull[xr.slot],
-                        cb * PITCH, ow_base * SD - a.pad, ih, n);
+                        a.c_lo + cb * PITCH, ow_base * SD - a.pad, ih, n);
             xr.next(a.nx);
             return true;
         };
@@ -223,7 +224,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             if (yissued < static_cast<uint32_t>(a.ny)) ++yissued;
             mbar_arrive_expect_tx(&yfull[yr.slot], a.y_tx);
             tma_load_4d(yring + static_cast<size_t>(yr.slot) * a.y_bytes, &ymap, &yfull[yr.slot],
-                        cb * PITCH, ow_base, oh, n);
+                        a.c_lo + cb * PITCH, ow_base, oh, n);
             yr.next(a.ny);
             return true;
         };
@@ -383,7 +384,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         for (int t = 0; t < FC; ++t) mine[(f * FC + t) * 32 + lane] = acc[f][t];
     asm volatile("bar.sync 1, %0;" ::"r"(ncompute * 32) : "memory");
     if (wc == 0 && lg == 0) {
-        const int c = cb * PITCH + 2 * cl;
+        const int c = a.c_lo + cb * PITCH + 2 * cl;
         for (int f = 0; f < RF; ++f) {
             const int fh = fh0 + frow0 + f;
             if (!live[f] || c >= a.C) continue;
@@ -531,19 +532,12 @@ bool fgrad_plan(int N, int OH, int OW, int C, FgradPlan<FH, FW, Tile>& P, int fh
     return false;
 }
 
-template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>, int G = 1>
-cudaError_t launch_fgrad_inst(const FilterGrad& p) {
+// The kernel launch of plan P over the channel blocks from channel c_lo (its partial sums go
+// to the workspace slices; the caller sums them).
+template <typename T, int FH, int FW, class Tile, int G>
+cudaError_t fgrad_enqueue(const FilterGrad& p, const FgradPlan<FH, FW, Tile>& P, int fhr, int c_lo) {
     const int e = static_cast<int>(sizeof(T));
-    FgradPlan<FH, FW, Tile> P;
-    const int fhr = FH > 0 ? FH : p.FH;
     constexpr int PITCH = kBN / G;
-    if (!fgrad_plan<T, FH, FW, Tile, G>(p.N, p.OH, p.OW, p.C, P, fhr)) return cudaErrorNotSupported;
-    if (p.N == 0 || p.OH == 0 || p.OW == 0) {
-        return cudaMemsetAsync(p.dw, 0, sizeof(float) * fhr * FW * p.C, p.stream);
-    }
-    const size_t need = static_cast<size_t>(P.Z) * P.ncp * fhr * FW * p.C;
-    if (p.workspace_floats < need || p.workspace == nullptr) return cudaErrorInvalidValue;
-
     CUtensorMap xmap, ymap;
     {
         const cuuint64_t dims[4] = {(cuuint64_t)p.C, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.N};
@@ -568,6 +562,7 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     a.status = p.status;
     a.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     a.N = p.N; a.OH = p.OH; a.C = p.C; a.pad = p.pad;
+    a.c_lo = c_lo;
     a.ncp = P.ncp; a.owpart = P.owpart;
     a.FH = fhr;
     a.nwf = P.nwf; a.nwc = P.nwc; a.fhc = P.fhc; a.chunks = P.chunks; a.cblocks = P.cblocks;
@@ -584,7 +579,20 @@ cudaError_t launch_fgrad_inst(const FilterGrad& p) {
     const int threads = (P.nwf * Tile::NFC * P.nwc + 1) * 32;
     const unsigned grid = static_cast<unsigned>(P.Z) * P.ncp * P.cblocks * P.chunks;
     kern<<<grid, threads, P.smem, p.stream>>>(xmap, ymap, a);
-    cudaError_t err = cudaGetLastError();
+    return cudaGetLastError();
+}
+
+template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>, int G = 1>
+cudaError_t launch_fgrad_inst(const FilterGrad& p) {
+    FgradPlan<FH, FW, Tile> P;
+    const int fhr = FH > 0 ? FH : p.FH;
+    if (!fgrad_plan<T, FH, FW, Tile, G>(p.N, p.OH, p.OW, p.C, P, fhr)) return cudaErrorNotSupported;
+    if (p.N == 0 || p.OH == 0 || p.OW == 0) {
+        return cudaMemsetAsync(p.dw, 0, sizeof(float) * fhr * FW * p.C, p.stream);
+    }
+    const size_t need = static_cast<size_t>(P.Z) * P.ncp * fhr * FW * p.C;
+    if (p.workspace_floats < need || p.workspace == nullptr) return cudaErrorInvalidValue;
+    const cudaError_t err = fgrad_enqueue<T, FH, FW, Tile, G>(p, P, fhr, 0);
     if (err != cudaSuccess) return err;
     return launch_reduce_slices(p.workspace, P.Z * P.ncp, static_cast<size_t>(fhr) * FW * p.C, p.dw,
                                 p.stream);
@@ -598,7 +606,11 @@ size_t fgrad_workspace_inst(int N, int OH, int OW, int C, int fhr = FH) {
 }
 
 // 3x3, 5x5 and 7x7 with at most 32 (16) channels: 2 (4) lane groups, so that the single
-// partial channel block does not leave half the lanes idle.
+// partial channel block does not leave half the lanes idle.  (A tail of at most 32 channels
+// past a multiple of 64 as a second launch on lane groups, sharing the first launch's slices,
+// was slower at 7x7 -- 64x56x56: 96 channels 88 against 84 us for 128, 160 channels 131
+// against 115 for 192 -- since every launch pays the kernel's fixed costs: the blocks of a
+// tail stay in the one launch.)
 template <typename T, int F, class Tile>
 cudaError_t launch_fgrad_grouped(const FilterGrad& p) {
     if constexpr (F <= 7) {

@@ -72,6 +72,11 @@ FAST = [
     C_(2, 17, 19, 64, 3),
     C_(1, 23, 37, 128, 7),
     C_(2, 9, 70, 96, 5),            # two column tiles, channel tail of 32
+    # 7x7 channel tails past a multiple of 64 (the forward and backward data run the tail as a
+    # second launch on 2 / 4 lane groups)
+    C_(2, 17, 29, 96, 7),
+    C_(1, 20, 40, 80, 7),
+    C_(1, 12, 33, 160, 7),
     C_(1, 14, 14, 32, 3, p=1),      # fewer channels than one block
     C_(3, 11, 13, 8, 9),            # 8 channels
     C_(1, 30, 30, 64, 13),
