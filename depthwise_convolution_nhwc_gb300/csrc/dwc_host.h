@@ -235,12 +235,15 @@ cudaError_t launch_tc_fgrad_bf16(const FilterGrad& p);
 cudaError_t launch_tc_fgrad_f16(const FilterGrad& p);
 bool tc_fgrad_fits(const FilterGrad& p);
 // Where the tcgen05 filter gradient is the one to run (the automatic choice; timed against the
-// warp-level MMA and CUDA-core kernels, bf16): from 13 taps on rows of at least 44 outputs.
-// Its work grows with the rows, columns and filter height but not the width (the whole x
-// band of a dy tile is multiplied), so narrow rows and small filters stay elsewhere
-// (64x56x56x128: 205 against 229 us at 13 taps, 166 against 158 at 11; 64x112x112x64 13x13:
-// 358 against 426; 32x40x40x128 31x31 a tie; 64x28x28x256 at any size slower).
-inline bool tc_fgrad_wanted(int FW, int OW) { return OW >= 44 && FW >= 13; }
+// warp-level MMA and CUDA-core kernels, bf16): from 13 taps on rows of at least 44 outputs
+// (wide tiles) or of 17 to 32 outputs (narrow tiles, up to 33 taps).  Its work grows with the
+// rows, columns and filter height but not the width (the whole x band of a dy tile is
+// multiplied), so small filters stay elsewhere (64x56x56x128: 205 against 229 us at 13 taps,
+// 166 against 158 at 11; 64x112x112x64 13x13: 358 against 426; 64x28x28x256: 113 against 131
+// us at 13 taps, 198 against 338 at 31; 32x40x40x128 31x31 a tie on a wide tile).
+inline bool tc_fgrad_wanted(int FW, int OW) {
+    return FW >= 13 && (OW >= 44 || (OW >= 17 && OW <= 32 && FW <= 33));
+}
 // The tcgen05 filter gradient serves this 16-bit call: the automatic choice or the family
 // preference (tcgen05 forced: 2; other families: never).
 bool tc_fgrad_taken(const FilterGrad& p);

@@ -10,21 +10,23 @@
 //   D_j[m, n] = sum_r x[r + fh0, X0 + m] * dy[r - j, n0 + n]     (j = 0..3)
 //   dw[fh0 + j, fw] = sum_n D_j[n + fw, n]                        (a diagonal of D_j)
 //
-// where X0 = n0 - pad_w (the x column of output column n0 at tap 0), m < 128 runs over the x
-// columns a 64-column tile of dy can meet and r over all virtual rows.  Per K-step of 16 rows
-// four MMAs of M=128, N=64, K=16 share A = 16 rows of 128 x columns; MMA j takes B = the
-// staged dy band read from a start address j rows earlier: the dy rows j above A's rows.
-// (Rows per MMA R = 2 or 4 -- N = 64 R over R dy bands staged one row apart, 4 / R issuers
-// -- read A once per R rows but took 1.1x (R = 2) and 1.7x (R = 4) the time on bf16
-// 32x56x56x128 31x31: fewer threads do not issue the wider MMAs as fast as the tensor core
-// runs them, and one accumulator cannot take MMAs from two threads.)  kTfgRowsPerMma keeps
-// the three forms.
-// Both operands are
-// read in the MN-major core-matrix layout: 8 columns of a row are 16 contiguous bytes,
-// consecutive rows 16 bytes apart, so a band of an 8-column plane lands in shared memory
-// exactly as the stacked copy holds it.  A unit is (channel, group of four
-// filter rows) over every row and column tile: its accumulators hold the whole sum, so the
-// epilogue writes dw directly (no partial slices) after summing the diagonals.
+// where X0 = n0 - pad_w (the x column of output column n0 at tap 0), m runs over the x
+// columns a tile of dy can meet and r over all virtual rows.  Per K-step of 16 rows four MMAs
+// of M=128, K=16 share A = 16 rows of x; MMA j takes B = the staged dy band read from a start
+// address j rows earlier: the dy rows j above A's rows.  Two shapes of a tile:
+//  * wide (rows of 44+ outputs): 64 dy columns (N=64) against 128 x columns;
+//  * narrow (rows of at most 32 outputs): 32 dy columns (N=32) against two bands of 64 x
+//    columns stacked in M, the second staged 4 rows lower -- its half of D_j holds filter row
+//    fh0 + 4 + j -- so that a unit of 8 filter rows uses all of M for a narrow dy tile.
+// (Rows per MMA of 2 or 4 -- N = 128 or 256 over shifted dy bands, 2 or 1 issuers -- read A
+// once per 2 or 4 rows but took 1.1x and 1.7x the time on bf16 32x56x56x128 31x31: fewer
+// threads do not issue the wider MMAs as fast as the tensor core runs them, and one
+// accumulator cannot take MMAs from two threads.)  Both operands are read in the MN-major
+// core-matrix layout: 8 columns of a row are 16 contiguous bytes, consecutive rows 16 bytes
+// apart, so a band of an 8-column plane lands in shared memory exactly as the stacked copy
+// holds it.  A unit is (channel, group of filter rows) over every row and column tile: its
+// accumulators hold the whole sum, so the epilogue writes dw directly (no partial slices)
+// after summing the diagonals.
 //
 // Two launches: a preparation kernel writes the stacked copies of x (the forward's padding)
 // and of dy (no padding), plane-major -- every 8-column plane of a channel holds its virtual
@@ -33,41 +35,49 @@
 // these bands (16-byte inner rows) ran at one row per clock: 3300 clocks a stage, twice the
 // stage's MMA time.  Warp roles (9 warps, one persistent CTA per SM): warps 0-3 epilogue
 // (warp w reads the 32-lane quadrant w of the accumulators), warps 4-7 the MMA issuers (one
-// lane each; issuer j owns filter row fh0 + j of every unit; warp 4 allocates the tensor
-// memory), warp 8 the copy producer (lane i copies plane band i of a stage: 16 x bands of
-// 128 rows, 8 dy bands of 131 rows).  Every wait is bounded.
+// lane each; issuer j owns the filter rows of shift j of every unit; warp 4 allocates the
+// tensor memory), warp 8 the copy producer (lane i copies plane band i of a stage: 16 x bands
+// of 128 rows, 8 or 4 dy bands of 131 rows).  Every wait is bounded.
 #pragma once
 
 #include "dwc_tc.cuh"
 
 namespace dwc {
 
-constexpr int kTfgCopies = 4;        // filter rows per unit
-constexpr int kTfgRowsPerMma = 1;    // filter rows per MMA (N = 64 per row)
-constexpr int kTfgIssuers = kTfgCopies / kTfgRowsPerMma;   // issuer q: rows R q .. R q + R - 1
-constexpr int kTfgDyCopies = kTfgRowsPerMma;   // dy bands per stage, band h from row r0 - 3 - h
-// virtual rows per stage (K-steps of 16) and stages, within shared memory
-constexpr int kTfgKB = kTfgRowsPerMma == 4 ? 112 : 128;
-constexpr int kTfgStages = kTfgRowsPerMma == 1 ? 4 : (kTfgRowsPerMma == 2 ? 3 : 2);
-constexpr int kTfgXPlanes = 16;      // 128 x columns
-constexpr int kTfgDyPlanes = 8;      // 64 dy columns
-constexpr int kTfgDyRows = kTfgKB + kTfgCopies - 1;   // 131 rows of a dy band
-constexpr int kTfgRO = kTfgCopies - 1 + (kTfgRowsPerMma - 1);   // zero rows before row 0
+constexpr int kTfgKB = 128;          // virtual rows per stage (8 K-steps of 16)
+constexpr int kTfgStages = 4;
+constexpr int kTfgXPlanes = 16;      // 128 x columns of A (one or two bands)
+constexpr int kTfgShifts = 4;        // dy row shifts: MMAs (and issuers) per K-step
+constexpr int kTfgDyRows = kTfgKB + kTfgShifts - 1;   // 131 rows of a dy band
+constexpr int kTfgRO = kTfgShifts - 1;                // zero rows before row 0 of a plane
 constexpr int kTfgEpiWarps = 4;
 constexpr int kTfgMmaWarp = 4;
-constexpr int kTfgTmaWarp = kTfgMmaWarp + kTfgIssuers;
+constexpr int kTfgTmaWarp = kTfgMmaWarp + kTfgShifts;
 constexpr int kTfgThreads = (kTfgTmaWarp + 1) * 32;
 constexpr int kTfgXBytes = kTfgXPlanes * kTfgKB * 16;                    // 32 KB
-constexpr int kTfgDyBytes = kTfgDyCopies * kTfgDyPlanes * kTfgDyRows * 16;   // 32.75 KB
-constexpr int kTfgStageBytes = kTfgXBytes + kTfgDyBytes;
-constexpr int kTfgRowFloats = 65;    // epilogue staging: 128 rows of 64 columns + 1 pad
+constexpr int kTfgRowFloats = 65;    // epilogue staging: 128 rows of up to 64 columns + 1 pad
 constexpr int kTfgEpiBytes = 128 * kTfgRowFloats * 4;
-constexpr int kTfgBarOff = kTfgStages * kTfgStageBytes + kTfgEpiBytes;
-// barriers: full and empty per stage, two accumulator buffers, the epilogue's own, one per
-// issuer; then the tensor-memory address and the abort flag
-constexpr int kTfgBarBytes = (2 * kTfgStages + 2 * 2 + 1 + kTfgIssuers) * 8 + 8;
-constexpr int kTfgSmem = kTfgBarOff + 256;
-static_assert(kTfgBarBytes <= 256, "barrier area");
+
+// The two tile shapes (NARROW: 32 dy columns against two x bands of 64 columns).
+template <bool NARROW>
+struct TfgShape {
+    static constexpr int kDyCols = NARROW ? 32 : 64;          // dy columns of a tile (MMA N)
+    static constexpr int kDyPlanes = kDyCols / 8;
+    static constexpr int kXBands = NARROW ? 2 : 1;            // x bands stacked in M
+    static constexpr int kBandPlanes = kTfgXPlanes / kXBands;  // planes of a band
+    static constexpr int kBandShift = 4;                      // rows between the x bands
+    static constexpr int kRows = kTfgShifts * kXBands;        // filter rows of a unit
+    static constexpr int kMaxFW = kBandPlanes * 8 - kDyCols + 1;
+    static constexpr int kDyBytes = kDyPlanes * kTfgDyRows * 16;
+    static constexpr int kStageBytes = kTfgXBytes + kDyBytes;
+    static constexpr int kBarOff = kTfgStages * kStageBytes + kTfgEpiBytes;
+    // barriers: full and empty per stage, two accumulator buffers, the epilogue's own, one
+    // per issuer; then the tensor-memory address and the abort flag
+    static constexpr int kBarBytes = (2 * kTfgStages + 2 * 2 + 1 + kTfgShifts) * 8 + 8;
+    static constexpr int kSmem = kBarOff + 256;
+    static_assert(kBarBytes <= 256, "barrier area");
+    static_assert(kTfgShifts * kDyCols <= kTcDCols, "a unit's accumulators in one buffer");
+};
 
 struct TcFgArgs {
     const unsigned char* xpl;    // stacked x: C x npx planes x vp rows x 16 bytes
@@ -79,41 +89,42 @@ struct TcFgArgs {
     int npx, npd;       // planes of the stacked copies
     uint32_t vp;        // rows of a plane (virtual row v at row v + kTfgRO)
     int C, FH, FW;
-    int groups;         // filter-row groups of four per channel
-    int col_tiles;      // 64-column tiles of dy
+    int groups;         // filter-row groups (of the tile shape's kRows) per channel
+    int col_tiles;      // dy column tiles
     int row_blocks;     // stages of kTfgKB virtual rows per column tile
     int x0;             // stacked x column of dy column 0 at tap 0 (a multiple of 8, <= 0)
     uint32_t units;     // C * groups
     uint32_t idesc;
 };
 
-template <typename T>
+template <typename T, bool NARROW>
 __global__ void __launch_bounds__(kTfgThreads, 1)
 tc_fgrad_kernel(const TcFgArgs a) {
+    using Sh = TfgShape<NARROW>;
     extern __shared__ __align__(1024) unsigned char smem[];
-    float* stage_d = reinterpret_cast<float*>(smem + kTfgStages * kTfgStageBytes);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTfgBarOff);
+    float* stage_d = reinterpret_cast<float*>(smem + kTfgStages * Sh::kStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::kBarOff);
     uint64_t* full = bars;                        // [kTfgStages]
     uint64_t* empty = full + kTfgStages;          // [kTfgStages]
     uint64_t* d_full = empty + kTfgStages;        // [2]
     uint64_t* d_empty = d_full + 2;               // [2]
     uint64_t* epi_bar = d_empty + 2;              // the epilogue warps' own barrier
-    uint64_t* mma_done = epi_bar + 1;             // [kTfgIssuers]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + kTfgIssuers);
+    uint64_t* mma_done = epi_bar + 1;             // [kTfgShifts]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + kTfgShifts);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTfgStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kTfgIssuers);   // every issuer's MMAs on the stage
+            mbar_init(&empty[s], kTfgShifts);   // every issuer's MMAs on the stage
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&d_full[s], kTfgIssuers);
+            mbar_init(&d_full[s], kTfgShifts);
             mbar_init(&d_empty[s], kTfgEpiWarps);
         }
         mbar_init(epi_bar, kTfgEpiWarps);
-        for (int q = 0; q < kTfgIssuers; ++q) mbar_init(&mma_done[q], 1);
+        for (int q = 0; q < kTfgShifts; ++q) mbar_init(&mma_done[q], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -132,9 +143,9 @@ tc_fgrad_kernel(const TcFgArgs a) {
 
     if (warp == kTfgTmaWarp) {
         // ------------------------------------------------------------- copy producer
-        // Copy i (lane i, then lane i - 32): i < 16 the x rows r0 + fh0 .. + kTfgKB - 1 of
-        // plane i from column 64 t + x0; i = 16 + 8 h + p the dy band h, rows r0 - 3 - h ..
-        // + kTfgDyRows - 1 of plane p from column 64 t.  A plane outside a stacked copy comes
+        // Lane i < 16: x plane p = i % kBandPlanes of band h = i / kBandPlanes, rows
+        // r0 + fh0 + 4 h .. + 127, from column kDyCols t + x0; lane 16 + p: dy plane p, rows
+        // r0 - 3 .. r0 + 127, from column kDyCols t.  A plane outside a stacked copy comes
         // from the zero buffer (with several column tiles its rows would otherwise enter
         // accumulator rows that other tiles fill).
         const size_t pbytes = static_cast<size_t>(a.vp) * 16;
@@ -142,33 +153,31 @@ tc_fgrad_kernel(const TcFgArgs a) {
         bool ok = true;
         for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
             const int c = static_cast<int>(u / static_cast<uint32_t>(a.groups));
-            const int fh0 = 4 * static_cast<int>(u % static_cast<uint32_t>(a.groups));
+            const int fh0 = Sh::kRows * static_cast<int>(u % static_cast<uint32_t>(a.groups));
             for (uint32_t it = 0; it < iters; ++it, ++k) {
                 const int t = static_cast<int>(it / static_cast<uint32_t>(a.row_blocks));
                 const int r0 = static_cast<int>(it % static_cast<uint32_t>(a.row_blocks)) * kTfgKB;
                 const uint32_t s = k % kTfgStages, ph = (k / kTfgStages) & 1u;
                 if (!tc_wait_warp(&empty[s], ph ^ 1u, a, abort_flag)) { ok = false; break; }
-                unsigned char* st = smem + s * kTfgStageBytes;
-                if (lane == 0) mbar_arrive_expect_tx(&full[s], kTfgStageBytes);
+                unsigned char* st = smem + s * Sh::kStageBytes;
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], Sh::kStageBytes);
                 __syncwarp();
-                for (int i = lane; i < kTfgXPlanes + kTfgDyCopies * kTfgDyPlanes; i += 32) {
-                    if (i < kTfgXPlanes) {
-                        const int pl = (64 * t + a.x0) / 8 + i;
-                        const unsigned char* src =
-                            pl >= 0 && pl < a.npx
-                                ? a.xpl + (static_cast<size_t>(c) * a.npx + pl) * pbytes +
-                                      static_cast<size_t>(kTfgRO + r0 + fh0) * 16
-                                : a.zeros;
-                        tc_bulk_load(st + i * (kTfgKB * 16), src, kTfgKB * 16, &full[s]);
-                    } else {
-                        const int b = i - kTfgXPlanes;   // band h = b / 8, plane b % 8
-                        const int h = b / kTfgDyPlanes, pl = 8 * t + b % kTfgDyPlanes;
-                        const unsigned char* src =
-                            pl < a.npd ? a.dypl + (static_cast<size_t>(c) * a.npd + pl) * pbytes +
-                                             static_cast<size_t>(kTfgRO + r0 - (kTfgCopies - 1) - h) * 16
-                                       : a.zeros;
-                        tc_bulk_load(st + kTfgXBytes + b * (kTfgDyRows * 16), src, kTfgDyRows * 16, &full[s]);
-                    }
+                if (lane < kTfgXPlanes) {
+                    const int h = lane / Sh::kBandPlanes;
+                    const int pl = (Sh::kDyCols * t + a.x0) / 8 + lane % Sh::kBandPlanes;
+                    const unsigned char* src =
+                        pl >= 0 && pl < a.npx
+                            ? a.xpl + (static_cast<size_t>(c) * a.npx + pl) * pbytes +
+                                  static_cast<size_t>(kTfgRO + r0 + fh0 + Sh::kBandShift * h) * 16
+                            : a.zeros;
+                    tc_bulk_load(st + lane * (kTfgKB * 16), src, kTfgKB * 16, &full[s]);
+                } else if (lane < kTfgXPlanes + Sh::kDyPlanes) {
+                    const int i = lane - kTfgXPlanes, pl = Sh::kDyPlanes * t + i;
+                    const unsigned char* src =
+                        pl < a.npd ? a.dypl + (static_cast<size_t>(c) * a.npd + pl) * pbytes +
+                                         static_cast<size_t>(kTfgRO + r0 - (kTfgShifts - 1)) * 16
+                                   : a.zeros;
+                    tc_bulk_load(st + kTfgXBytes + i * (kTfgDyRows * 16), src, kTfgDyRows * 16, &full[s]);
                 }
             }
         }
@@ -176,23 +185,22 @@ tc_fgrad_kernel(const TcFgArgs a) {
         __syncwarp();
     } else if (warp >= kTfgMmaWarp) {
         // ------------------------------------------------------------- MMA issue
-        // filter rows fh0 + R q + h (dy band h): accumulator columns 64 (R q + h) ..
-        const int q = warp - kTfgMmaWarp;
+        // shift j: accumulator columns kDyCols j .. (both x bands in the MMA's M)
+        const int j = warp - kTfgMmaWarp;
         if (lane == 0) {
             // MN-major descriptors: K-direction groups of 8 rows 128 bytes apart, M/N-direction
             // groups of 8 columns (planes) one plane band apart; a K-step is 16 rows (256 B).
-            // B starts 3 - R q rows into the staged dy bands: band h then holds the dy rows
-            // R q + h above A's rows.
+            // B starts 3 - j rows into the staged dy band: the dy rows j above A's rows.
             const uint64_t xd0 = tc_sdesc(smem_addr(smem), 128u, kTfgKB * 16u);
             const uint64_t dd0 = tc_sdesc(smem_addr(smem + kTfgXBytes), 128u, kTfgDyRows * 16u) +
-                                 static_cast<uint32_t>(kTfgCopies - 1 - kTfgRowsPerMma * q);
-            const uint32_t stage16 = kTfgStageBytes >> 4;
+                                 static_cast<uint32_t>(kTfgShifts - 1 - j);
+            const uint32_t stage16 = Sh::kStageBytes >> 4;
             uint32_t db = 0, dphase = 0, k = 0;
             bool ok = true;
             for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
                 if (!tc_wait(&d_empty[db], dphase ^ 1u, a, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d = tmem + db * kTcDCols + static_cast<uint32_t>(64 * kTfgRowsPerMma * q);
+                const uint32_t d = tmem + db * kTcDCols + static_cast<uint32_t>(Sh::kDyCols * j);
                 for (uint32_t it = 0; it < iters; ++it, ++k) {
                     const uint32_t s = k % kTfgStages, ph = (k / kTfgStages) & 1u;
                     if (!tc_wait(&full[s], ph, a, abort_flag)) { ok = false; break; }
@@ -211,29 +219,29 @@ tc_fgrad_kernel(const TcFgArgs a) {
                 db ^= 1u;
                 if (db == 0) dphase ^= 1u;
             }
-            tc_commit(&mma_done[q]);
-            if (!mbar_wait(&mma_done[q], 0, a.wait_ns)) record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+            tc_commit(&mma_done[j]);
+            if (!mbar_wait(&mma_done[j], 0, a.wait_ns)) record_status(a.status, DWC_DEVSTAT_TIMEOUT);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------- epilogue
-        // Per filter row j of the unit: the 128 x 64 accumulator tile goes to shared memory
-        // (row m = lane of quadrant w), then thread t sums diagonal fw = t (and t + 128):
-        // dw[fh0 + j][fw] = sum_n D_j[n + fw][n].
+        // Per shift j of the unit: the 128 x kDyCols accumulator tile goes to shared memory
+        // (row m = lane of quadrant w), then thread t sums diagonals t, t + 128, ... of the
+        // kXBands x FW (band h, tap fw): dw[fh0 + 4 h + j][fw] = sum_n D_j[64 h + n + fw][n].
         const int quad = warp;
         const int m = quad * 32 + lane;
         uint32_t db = 0, dphase = 0, eph = 0;
         bool ok = true;
         for (uint32_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
             const int c = static_cast<int>(u / static_cast<uint32_t>(a.groups));
-            const int fh0 = 4 * static_cast<int>(u % static_cast<uint32_t>(a.groups));
+            const int fh0 = Sh::kRows * static_cast<int>(u % static_cast<uint32_t>(a.groups));
             if (!tc_wait_warp(&d_full[db], dphase, a, abort_flag, 1024)) break;
             tc_fence_after();
             const uint32_t dq = tmem + db * kTcDCols + (static_cast<uint32_t>(quad * 32) << 16);
-            for (int j = 0; j < kTfgCopies && ok; ++j) {
-                for (int cb = 0; cb < 64; cb += 16) {
+            for (int j = 0; j < kTfgShifts && ok; ++j) {
+                for (int cb = 0; cb < Sh::kDyCols; cb += 16) {
                     uint32_t v[16];
-                    tc_ld16(dq + j * 64 + cb, v);
+                    tc_ld16(dq + j * Sh::kDyCols + cb, v);
                     tc_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; ++e) stage_d[m * kTfgRowFloats + cb + e] = __uint_as_float(v[e]);
@@ -242,16 +250,17 @@ tc_fgrad_kernel(const TcFgArgs a) {
                 if (lane == 0) mbar_arrive(epi_bar);
                 if (!tc_wait_warp(epi_bar, eph, a, abort_flag, 256)) { ok = false; break; }
                 eph ^= 1u;
-                const int fh = fh0 + j;
-                if (fh < a.FH) {
-                    for (int fw = m; fw < a.FW; fw += 128) {
-                        float sum = 0.f;
+                for (int task = m; task < Sh::kXBands * a.FW; task += 128) {
+                    const int h = task / a.FW, fw = task - h * a.FW;
+                    const int fh = fh0 + Sh::kBandShift * h + j;
+                    if (fh >= a.FH) continue;
+                    const float* col = stage_d + (Sh::kBandPlanes * 8 * h + fw) * kTfgRowFloats;
+                    float sum = 0.f;
 #pragma unroll 8
-                        for (int n = 0; n < 64; ++n) sum += stage_d[(n + fw) * kTfgRowFloats + n];
-                        a.dw[(static_cast<size_t>(fh) * a.FW + fw) * a.C + c] = sum;
-                    }
+                    for (int n = 0; n < Sh::kDyCols; ++n) sum += col[n * (kTfgRowFloats + 1)];
+                    a.dw[(static_cast<size_t>(fh) * a.FW + fw) * a.C + c] = sum;
                 }
-                // every thread is done reading before the next filter row overwrites the tile
+                // every thread is done reading before the next shift overwrites the tile
                 __syncwarp();
                 if (lane == 0) mbar_arrive(epi_bar);
                 if (!tc_wait_warp(epi_bar, eph, a, abort_flag, 256)) { ok = false; break; }
@@ -285,12 +294,19 @@ struct TcFgPlan {
     int Lp, Wp;         // x copy: left padding, row length (a multiple of 8)
     int Wdp;            // dy copy: row length (a multiple of 8)
     size_t x_bytes, dy_bytes;
+    bool narrow;        // the narrow tile shape (rows of at most 32 outputs)
     TcFgArgs a;
 };
 
 inline bool tc_fgrad_plan(const FilterGrad& p, TcFgPlan& P) {
-    if (p.FH < 1 || p.FW < 1 || p.FW > 128 - 64 + 1 || p.C % 8 != 0 || p.N < 1) return false;
-    if (device_info().max_smem_optin < kTfgSmem) return false;
+    using Wide = TfgShape<false>;
+    using Narrow = TfgShape<true>;
+    if (p.FH < 1 || p.FW < 1 || p.C % 8 != 0 || p.N < 1) return false;
+    P.narrow = p.OW <= Narrow::kDyCols && p.FW <= Narrow::kMaxFW;
+    if (!P.narrow && p.FW > Wide::kMaxFW) return false;
+    const int rows = P.narrow ? Narrow::kRows : Wide::kRows;
+    const int dycols = P.narrow ? Narrow::kDyCols : Wide::kDyCols;
+    if (device_info().max_smem_optin < (P.narrow ? Narrow::kSmem : Wide::kSmem)) return false;
     P.S = std::max({p.pad + p.H, p.OH + p.FH - 1 - p.pad, p.OH});
     P.V = static_cast<long long>(p.N) * P.S;
     if (P.V + 2 * kTfgKB >= (1LL << 31)) return false;
@@ -299,15 +315,15 @@ inline bool tc_fgrad_plan(const FilterGrad& p, TcFgPlan& P) {
     P.Wdp = (p.OW + 7) / 8 * 8;
     TcFgArgs& a = P.a;
     a.C = p.C; a.FH = p.FH; a.FW = p.FW;
-    a.groups = (p.FH + kTfgCopies - 1) / kTfgCopies;
-    a.col_tiles = (p.OW + 63) / 64;
-    a.row_blocks = static_cast<int>((P.V + kTfgCopies - 1 + kTfgKB - 1) / kTfgKB);
+    a.groups = (p.FH + rows - 1) / rows;
+    a.col_tiles = (p.OW + dycols - 1) / dycols;
+    a.row_blocks = static_cast<int>((P.V + kTfgShifts - 1 + kTfgKB - 1) / kTfgKB);
     a.x0 = P.Lp - p.pad;
     a.npx = P.Wp / 8;
     a.npd = P.Wdp / 8;
     // rows of a plane: kTfgRO zero rows, the V virtual rows, and zero rows up to the last
-    // stage's x rows (r0 + fh0 + 127 for the last row block and filter-row group)
-    const long long vp = kTfgRO + static_cast<long long>(a.row_blocks) * kTfgKB + kTfgCopies * a.groups;
+    // stage's x rows (r0 + fh0 + 4 h + 127 for the last row block, filter-row group and band)
+    const long long vp = kTfgRO + static_cast<long long>(a.row_blocks) * kTfgKB + rows * a.groups;
     if (vp >= (1LL << 31)) return false;
     a.vp = static_cast<uint32_t>(vp);
     P.x_bytes = static_cast<size_t>(p.C) * a.npx * a.vp * 16;
@@ -318,13 +334,12 @@ inline bool tc_fgrad_plan(const FilterGrad& p, TcFgPlan& P) {
     return true;
 }
 
-// Instruction descriptor: kind::f16, fp32 accumulation, both operands MN-major, M=128,
-// N = 64 per filter row of an MMA.
+// Instruction descriptor: kind::f16, fp32 accumulation, both operands MN-major, M=128, N=n.
 template <typename T>
-inline uint32_t tc_fgrad_idesc() {
+inline uint32_t tc_fgrad_idesc(int n) {
     const uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
     return (1u << 4) | (ab << 7) | (ab << 10) | (1u << 15) | (1u << 16) |
-           (static_cast<uint32_t>(64 * kTfgRowsPerMma >> 3) << 17) | (static_cast<uint32_t>(kTcM >> 4) << 24);
+           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kTcM >> 4) << 24);
 }
 
 // Both stacked copies of a call (the tiles of x, then those of dy) and the zero band.
@@ -338,6 +353,18 @@ __global__ void __launch_bounds__(256) tc_stack_pm_kernel(const TcStackArgs ax, 
         if (tt < ax.tiles) tc_stack_tile<T>(ax, tt, tile);
         else tc_stack_tile<T>(ady, tt - ax.tiles, tile);
     }
+}
+
+template <typename T, bool NARROW>
+cudaError_t launch_tc_fgrad_main(const TcFgArgs& a, cudaStream_t stream) {
+    auto kern = tc_fgrad_kernel<T, NARROW>;
+    static DeviceOnce smem_opt_in;
+    const cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
+    if (err != cudaSuccess) return err;
+    const unsigned grid = static_cast<unsigned>(
+        std::min<long long>(a.units, static_cast<long long>(device_info().sm_count)));
+    kern<<<grid, kTfgThreads, TfgShape<NARROW>::kSmem, stream>>>(a);
+    return cudaGetLastError();
 }
 
 template <typename T>
@@ -374,16 +401,8 @@ cudaError_t launch_tc_fgrad(const FilterGrad& p) {
         a.dw = p.dw;
         a.status = p.status;
         a.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
-        a.idesc = tc_fgrad_idesc<T>();
-        auto kern = tc_fgrad_kernel<T>;
-        static DeviceOnce smem_opt_in;
-        err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
-        if (err == cudaSuccess) {
-            const unsigned grid = static_cast<unsigned>(
-                std::min<long long>(a.units, static_cast<long long>(device_info().sm_count)));
-            kern<<<grid, kTfgThreads, kTfgSmem, p.stream>>>(a);
-            err = cudaGetLastError();
-        }
+        a.idesc = tc_fgrad_idesc<T>(P.narrow ? TfgShape<true>::kDyCols : TfgShape<false>::kDyCols);
+        err = P.narrow ? launch_tc_fgrad_main<T, true>(a, p.stream) : launch_tc_fgrad_main<T, false>(a, p.stream);
     }
     scratch_free(scratch, p.stream);
     return err;

@@ -183,11 +183,13 @@ def test_path_selection_host_logic(lib):
     big = dict(H=56, W=56, C=64, FH=31, FW=31, pad=15)
     assert p(0, **big, dtype=1) == 2 and p(1, **big, dtype=2) == 2 and p(2, **big, dtype=1) == 2
     assert p(0, **big) == 1 and p(2, **big) == 1          # fp32 stays on CUDA cores
-    # 16-bit filter gradients: tcgen05 from 13 taps on rows of 44+ outputs, else the
-    # warp-level MMA kernel (family 4) for large filters on narrower rows
+    # 16-bit filter gradients: tcgen05 from 13 taps on rows of 44+ outputs (wide tiles) or of
+    # 17 to 32 outputs (narrow tiles, up to 33 taps), else the warp-level MMA kernel
+    # (family 4) for large filters
     assert p(2, **dict(big, FH=13, FW=13, pad=6), dtype=1) == 2
     assert p(2, **dict(big, FH=11, FW=11, pad=5), dtype=1) == 1
-    assert p(2, **dict(big, W=28), dtype=1) == 4
+    assert p(2, **dict(big, W=28), dtype=1) == 2
+    assert p(2, **dict(big, W=40), dtype=1) == 4
     assert p(0, **dict(big, FH=7, FW=7, pad=3), dtype=1) == 1
     # tcgen05 from 9 taps on rows of 28+ outputs, from 17 taps on 17- to 27-wide rows
     assert p(0, **dict(big, W=28, FH=9, FW=9, pad=4), dtype=1) == 2
