@@ -72,8 +72,8 @@ def kernel_name(case, pass_name, family):
 
 
 def kernel_family(dwc, case, pass_name):
-    """0 general, 1 CUDA-core, 2 tensor-core (tcgen05 / warp-level MMA filter gradient),
-    3 small-map, 4 warp-level MMA forward / backward data (asked of the library itself)."""
+    """0 general, 1 CUDA-core, 2 tcgen05 tensor-core, 3 small-map, 4 warp-level MMA
+    (asked of the library itself)."""
     return dwc.path(pass_name, None, None, None, case.N, case.H, case.W, case.C, case.FH,
                     case.FW, case.stride, case.pad, DTYPE_CODE[case.dtype])
 
@@ -508,8 +508,7 @@ def per_filter_table(args, dev, peaks):
                     "copy rate; alu: valid FLOPs at the measured fp32x2 FMA rate; tensor: "
                     "valid FLOPs at the measured bf16 peak)",
             "families": "fwd/bwd_data/bwd_filter kernel family: cc CUDA-core, tc tensor-core "
-                        "(tcgen05 forward / backward data, warp-level MMA filter gradient), mma "
-                        "warp-level MMA forward / backward data, sm small-map, gen general",
+                        "(tcgen05), mma warp-level MMA, sm small-map, gen general",
             "points": points}
 
 

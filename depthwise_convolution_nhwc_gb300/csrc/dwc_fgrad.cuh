@@ -38,7 +38,7 @@ namespace dwc {
 // x window (any U >= FW works; output columns are processed in blocks of U, so a U that
 // divides the row width leaves no padded columns).
 template <int FH, int FW, int RF_ = 0, int MINB_ = 0, int U_ = 0, int NY_ = 0, int SD_ = 1,
-          int FWC_ = 0, int MAXCW_ = 0>
+          int FWC_ = 0, int MAXCW_ = 0, int ROT_ = 0>
 struct FgradTile {
     // convolution stride (1, or 2 for the strided 3x3 / 5x5 / 7x7 filter gradient)
     static constexpr int SD = SD_;
@@ -66,7 +66,19 @@ struct FgradTile {
     // (7x7 at stride 1, two rows per warp: 12 warps timed 2.5 % faster than 8 on 56x56x128)
     static constexpr int MAXCW = MAXCW_ > 0 ? MAXCW_ :
         ((RF == 1 && FWC <= 19) || (FW == 7 && RF == 2 && SD == 1) ? 12 : ((RF == 1 && FWC <= 27) ? 11 : 8));
+    // Rotated layout (ROT_ = 1, 7x7 at stride 1): 7 filter rows at two rows per warp make
+    // four row groups, the last with one live row (whose warps compute only that row).
+    // With 16 compute warps (the four groups x four column strips of equal width) the warps
+    // of a strip take the groups in a rotated order, so that each of the SM's four
+    // schedulers (warp w issues on scheduler w mod 4) holds one warp of every group and the
+    // same number of packed FMAs.
+    static constexpr bool ROT = ROT_ != 0 && SD == 1 && RF == 2 && FWC == FW && FH == 7;
+    // compute warps the launch bound allows
+    static constexpr int MAXW = ROT ? 16 : MAXCW;
 };
+
+template <int F>
+using FgradRotTile = FgradTile<F, F, 0, 0, 0, 0, 1, 0, 0, 1>;
 
 // A second window period per filter width: a multiple of 7 (the widths of the usual
 // 224-pixel pyramids, 112/56/28/14/7, are multiples of 7) at least FW, where the longer
@@ -146,10 +158,38 @@ __device__ __forceinline__ void fgrad_row_s2(float2 (&acc)[RF][FW], const T* con
     }
 }
 
+// One output row of a column strip at stride 1, for the first R of the RF rows xs[f]:
+// acc[f][t] += x[ow + t] * dy[ow] over the strip's output columns (ow from blk0 * U to
+// blk1 * U).  Column c of the padded x row sits in slot c mod U of a circular register window.
+template <typename T, int FC, int RF, int R, int U, int PITCH>
+__device__ __forceinline__ void fgrad_row_s1(float2 (&acc)[RF][FC], const T* const (&xs)[RF],
+                                             const T* ys, int blk0, int blk1) {
+    float2 win[R][U];
+    const int c0 = blk0 * U;
+#pragma unroll
+    for (int f = 0; f < R; ++f)
+#pragma unroll
+        for (int m = 0; m < FC - 1; ++m) win[f][m] = Elem<T>::load_pair(xs[f] + (c0 + m) * PITCH);
+#pragma unroll 1
+    for (int blk = blk0; blk < blk1; ++blk) {
+        const int cb0 = blk * U;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float2 g = Elem<T>::load_pair(ys + (cb0 + u) * PITCH);
+#pragma unroll
+            for (int f = 0; f < R; ++f) {
+                win[f][(u + FC - 1) % U] = Elem<T>::load_pair(xs[f] + (cb0 + u + FC - 1) * PITCH);
+#pragma unroll
+                for (int t = 0; t < FC; ++t) fma2(acc[f][t], win[f][(u + t) % U], g);
+            }
+        }
+    }
+}
+
 // G: lane groups (1, or 2 / 4 when all channels fit in 32 / 16: each group of 32 / G lanes
 // covers them for its own column strip, so no lane idles).
 template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>, int G = 1>
-__global__ void __launch_bounds__((Tile::MAXCW + 1) * 32, Tile::MINB)
+__global__ void __launch_bounds__((Tile::MAXW + 1) * 32, Tile::MINB)
 fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
              const FgradArgs a) {
     constexpr int RF = Tile::RF;
@@ -260,9 +300,11 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     }
 
     // ---------------- compute warps -----------------------------------------------------
-    const int wf = warp % a.nwf;
-    const int fc = (warp / a.nwf) % NFC;           // tap chunk: taps fc*FC .. fc*FC + FC - 1
-    const int wc = warp / (a.nwf * NFC);
+    static_assert(!Tile::ROT || G == 1, "the rotated layout has no lane groups");
+    // (rotated layout: warp w -> strip w / 4, row group (w + strip) mod 4)
+    const int wc = Tile::ROT ? warp >> 2 : warp / (a.nwf * NFC);
+    const int wf = Tile::ROT ? (warp + wc) & 3 : warp % a.nwf;
+    const int fc = Tile::ROT ? 0 : (warp / a.nwf) % NFC;  // tap chunk: taps fc*FC .. fc*FC + FC - 1
     const int lg = lane / LPG;                     // lane group: column strip wc * G + lg
     const int cl = lane % LPG;                     // channel pair
     const int frow0 = wf * RF;                     // first owned row within the chunk
@@ -321,6 +363,12 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             }
             if constexpr (SD == 2) {
                 if (blk0 < blk1) fgrad_row_s2<T, FC, RF, U>(acc, xs, ys, blk0, blk1);
+            } else if constexpr (Tile::ROT) {
+                // the last group (one live row of two) computes its live row only
+                if (!live[RF - 1])
+                    fgrad_row_s1<T, FC, RF, 1, U, PITCH>(acc, xs, ys, blk0, blk1);
+                else
+                    fgrad_row_s1<T, FC, RF, RF, U, PITCH>(acc, xs, ys, blk0, blk1);
             } else if (blk0 < blk1) {
                 // circular window: column c of the padded x row sits in slot c mod U
                 float2 win[RF][U];
@@ -453,7 +501,25 @@ bool fgrad_plan_parts(int N, int OH, int OW, int C, int ncp, int min_la,
     P.nwf = 0;
     int best_la = 0;
     constexpr int NFC = Tile::NFC;
-    for (int nwf = std::min(groups, Tile::MAXCW / NFC); nwf >= 1; --nwf) {
+    if constexpr (Tile::ROT) {
+        // The rotated layout, or no plan: the whole filter in one chunk of four groups and
+        // the row's blocks in four equal strips of at least two blocks (strips of one block,
+        // 28-wide rows, timed slower than the default tile's eight warps of two blocks).
+        static_assert(G == 1, "the rotated layout has no lane groups");
+        if (fhr != FH || ncp != 1 || P.nblocks % 4 != 0 || P.nblocks < 8) return false;
+        if (512 + static_cast<size_t>(16) * RF * Tile::FWC * 32 * sizeof(float2) > smem_cap) return false;
+        int la = Tile::NY;
+        auto need = [&](int l) {
+            return 512 + static_cast<size_t>(4 * RF + l) * P.x_bytes + static_cast<size_t>(l) * P.y_bytes;
+        };
+        while (la > min_la && need(la) > smem_cap) --la;
+        if (need(la) > smem_cap) return false;
+        P.nwf = 4;
+        P.nwc = 4;
+        P.bps = P.nblocks / 4;
+        best_la = la;
+    }
+    for (int nwf = Tile::ROT ? 0 : std::min(groups, Tile::MAXCW / NFC); nwf >= 1; --nwf) {
         int la = Tile::NY;
         auto need = [&](int l) {
             return 512 + static_cast<size_t>(nwf * RF + l * Tile::SD) * P.x_bytes +
@@ -611,11 +677,17 @@ size_t fgrad_workspace_inst(int N, int OH, int OW, int C, int fhr = FH) {
 // was slower at 7x7 -- 64x56x56: 96 channels 88 against 84 us for 128, 160 channels 131
 // against 115 for 192 -- since every launch pays the kernel's fixed costs: the blocks of a
 // tail stay in the one launch.)
+// 7x7 takes the rotated layout wherever it has a plan.
 template <typename T, int F, class Tile>
 cudaError_t launch_fgrad_grouped(const FilterGrad& p) {
     if constexpr (F <= 7) {
         if (p.C <= 16) return launch_fgrad_inst<T, F, F, Tile, 4>(p);
         if (p.C <= 32) return launch_fgrad_inst<T, F, F, Tile, 2>(p);
+    }
+    if constexpr (FgradRotTile<F>::ROT) {
+        FgradPlan<F, F, FgradRotTile<F>> P;
+        if (fgrad_plan<T, F, F, FgradRotTile<F>>(p.N, p.OH, p.OW, p.C, P))
+            return launch_fgrad_inst<T, F, F, FgradRotTile<F>>(p);
     }
     return launch_fgrad_inst<T, F, F, Tile>(p);
 }
@@ -625,6 +697,10 @@ size_t fgrad_workspace_grouped(int N, int OH, int OW, int C) {
     if constexpr (F <= 7) {
         if (C <= 16) return fgrad_workspace_inst<T, F, F, Tile, 4>(N, OH, OW, C);
         if (C <= 32) return fgrad_workspace_inst<T, F, F, Tile, 2>(N, OH, OW, C);
+    }
+    if constexpr (FgradRotTile<F>::ROT) {
+        const size_t rot = fgrad_workspace_inst<T, F, F, FgradRotTile<F>>(N, OH, OW, C);
+        if (rot > 0) return rot;
     }
     return fgrad_workspace_inst<T, F, F, Tile>(N, OH, OW, C);
 }

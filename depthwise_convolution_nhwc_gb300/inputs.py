@@ -120,6 +120,9 @@ _WORKLOADS = {
     # wide maps (the early stages of 224-pixel networks), 7x7 filter
     "f32_n64_112x112_c64_f7": Case(64, 112, 112, 64, 7, 7, 1, 3, "f32", "normal", 4),
     "f32_n16_224x224_c32_f7": Case(16, 224, 224, 32, 7, 7, 1, 3, "f32", "normal", 5),
+    # last stage of 224-pixel networks (7x7 maps), 3x3 and 7x7 filters
+    "f32_n64_7x7_c1024_f3": Case(64, 7, 7, 1024, 3, 3, 1, 1, "f32", "normal", 6),
+    "f32_n64_7x7_c1024_f7": Case(64, 7, 7, 1024, 7, 7, 1, 3, "f32", "normal", 7),
 }
 WORKLOADS = {k: replace(v, name=k) for k, v in _WORKLOADS.items()}
 

@@ -77,6 +77,8 @@ FAST = [
     C_(2, 17, 29, 96, 7),
     C_(1, 20, 40, 80, 7),
     C_(1, 12, 33, 160, 7),
+    C_(2, 13, 53, 96, 7),           # 7x7 filter gradient, rotated layout: padded columns, tail
+    C_(3, 9, 56, 192, 7),           # rotated layout, several slices per image
     C_(1, 14, 14, 32, 3, p=1),      # fewer channels than one block
     C_(3, 11, 13, 8, 9),            # 8 channels
     C_(1, 30, 30, 64, 13),
