@@ -65,9 +65,15 @@ def launches(dwc, case, pass_name):
 
 
 def kernel_name(case, pass_name, family):
-    """The kernel(s) serving a pass (the stride-2 backward data has its own kernel)."""
+    """The kernel(s) serving a pass (the stride-2 backward data has its own kernel; 7x7 maps
+    with 3 to 7 taps and "same" padding have their own small-map kernels)."""
     if case.stride == 2 and family == 1 and pass_name == "bwd_data":
         return "s2_bwd_data_kernel"
+    if (family == 3 and case.stride == 1 and case.H == case.W == 7 and case.FH == case.FW
+            and case.FH in (3, 5, 7) and case.pad == (case.FH - 1) // 2):
+        if pass_name != "bwd_filter":
+            return "tiny_rows_kernel"
+        return "tiny_fgrad_cluster_kernel" if case.FH == 3 else "tiny_fgrad_kernel + reduce_slices_kernel"
     return KERNEL_NAMES[(pass_name, family)]
 
 

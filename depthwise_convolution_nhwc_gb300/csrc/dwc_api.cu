@@ -620,8 +620,13 @@ int dwc_kernel_launches(int pass, int N, int H, int W, int C, int FH, int FW, in
     if (out == 0) return 0;
     // filter gradients: the kernel and the fixed-order sum of its slices (or a fill of dW
     // with zeros when nothing meets it: a memset, not a kernel of this library); the tcgen05
-    // filter gradient: the stacked copies of x and dy (one kernel), then the main kernel
-    if (pass == kPassBwdFilter) return N == 0 ? 0 : 2;
+    // filter gradient: the stacked copies of x and dy (one kernel), then the main kernel;
+    // 7x7 maps: one kernel (its clusters sum the slices)
+    if (pass == kPassBwdFilter) {
+        if (N == 0) return 0;
+        if (fam == 3 && stride == 1 && tiny_fgrad_single_launch(P.dtype, N, H, W, C, FH, FW, pad)) return 1;
+        return 2;
+    }
     if (pass == 3) return 1;
     if (fam == 2) {
         const RowConv rc = pass == kPassFwd

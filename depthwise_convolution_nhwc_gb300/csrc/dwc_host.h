@@ -182,6 +182,9 @@ size_t fgrad_s2_workspace_floats_f16(int N, int OH, int OW, int C, int FH, int F
 // enough for the other kernels to be faster; small_map_serves tells the forward /
 // backward-data choice, a nonzero small_fgrad_workspace_floats_* the filter-gradient one.
 bool small_map_serves(int H, int W, int OH, int OW, int FW, int pad_w);
+// Whether the filter gradient of a 7x7 map ("same" padding, stride 1) runs as one launch
+// (the cluster form, 3 taps) rather than a kernel and a slice sum.
+bool tiny_fgrad_single_launch(int dtype, int N, int H, int W, int C, int FH, int FW, int pad);
 cudaError_t launch_small_rows_f32(const RowConv& p);
 cudaError_t launch_small_rows_bf16(const RowConv& p);
 cudaError_t launch_small_rows_f16(const RowConv& p);

@@ -798,8 +798,15 @@ inline size_t tiny_fgrad_workspace_floats(int N, int C, int F) {
     return static_cast<size_t>((N + ipb - 1) / ipb) * F * F * C;
 }
 
+template <typename T, int F>
+cudaError_t launch_tiny_fgrad_cluster(const FilterGrad& p);
+
 template <typename T>
 cudaError_t launch_tiny_fgrad(const FilterGrad& p) {
+    if (p.FH == 3) {
+        const cudaError_t err = launch_tiny_fgrad_cluster<T, 3>(p);
+        if (err != cudaErrorNotSupported) return err;
+    }
     TinyFgArgs a;
     a.x = p.x; a.dy = p.dy;
     a.N = p.N; a.C = p.C;
@@ -821,6 +828,323 @@ cudaError_t launch_tiny_fgrad(const FilterGrad& p) {
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     return launch_reduce_slices(p.workspace, Z, count, p.dw, p.stream);
+}
+
+
+// ---- 7x7 maps, filter gradient in one launch (thread-block clusters) -----------------
+//
+// The two-launch form above reads its images straight from global memory into registers
+// (one thread per channel pair holds a whole image) and sums its slices in a second kernel.
+// Here a CTA owns one 64-channel block and a range of images, and a producer warp stages
+// those images (x and dy, 49 pixels x 64 channels each) into a ring of shared-memory slots
+// with tensor copies.  The work of one image is its NP (filter row fh, output row oh) pairs
+// that meet the map (37 at 7 taps: filter row fh meets 7 - |fh - P| output rows); compute
+// warp w takes pairs 3w .. 3w + 2 of every image, loads the pair's dy row and the x row fh
+// away (7 channel pairs each) from shared memory and adds their products into its own
+// F accumulators per pair, so the warps carry equal work.  After the last image the pair
+// partials go to shared memory, the CTA sums each filter row's pairs in list order, and the
+// Z CTAs of a channel block, one cluster along the image axis, sum their CTA partials in
+// rank order by reading each other's shared memory.  The result is bit-reproducible and
+// needs no workspace or second launch.  It serves 3 taps: fp32 64x7x7x1024 20.4 -> 14.6 us
+// (bf16 16.7 -> 14.7 us, CUDA events).  At 5 and 7 taps it measured 19.1 / 24.6 us against
+// 19.0 / 19.4 us for the two-launch form: a CTA works through its 8 images one ring slot at
+// a time (ncu: 33 % issue, fixed-latency and barrier stalls), and the cluster scheduler
+// places two CTAs on some SMs while others get none (busiest SM 37 k cycles against 22 k on
+// average), so the form is kept for 3 taps only.
+constexpr int kTfcMaxZ = 8;     // CTAs per cluster (images split Z ways)
+constexpr int kTfcBarBytes = 256;
+constexpr int kTfcPairsPerWarp = 3;
+// Shared memory per CTA: at most half an SM's, so that two CTAs fit on an SM and every
+// cluster of a launch of 16 channel blocks is resident at once (at one CTA per SM the
+// 8-CTA clusters of such a launch ran in two waves).
+constexpr size_t kTfcSmemCap = 115712;
+
+template <int F>
+struct TinyFgcShape {
+    static constexpr int M = kTinyMap, P = (F - 1) / 2;
+    // (fh, oh) pairs that meet the map: filter row fh meets M - |fh - P| output rows
+    static constexpr int NP = F * M - P * (P + 1);
+    static constexpr int NWC = (NP + kTfcPairsPerWarp - 1) / kTfcPairsPerWarp;   // compute warps
+    static constexpr int THREADS = (NWC + 1) * 32;
+    // pair partials [NWC * 3][F][64] and the CTA partial [F][F][64], fp32, in the ring
+    static constexpr int PAIR_FLOATS = NWC * kTfcPairsPerWarp * F * 64;
+    static constexpr int RED_BYTES = (PAIR_FLOATS + F * F * 64) * 4;
+    static constexpr int RING_OFF = kTfcBarBytes;
+};
+
+struct TinyFgcArgs {
+    float* dw;                  // F x F x C
+    unsigned int* status;
+    unsigned long long wait_ns;
+    int N, C, ipb, ns;          // images per CTA, ring slots
+    uint32_t img_bytes;         // one staged image: 49 pixels x 64 channels
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Two floats at the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ float2 ld_cluster_f2(const float* local, uint32_t rank) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(r) : "memory");
+    return v;
+}
+
+// Pair p of the list (filter rows in order, each with its output rows in order): its
+// filter row and output row, or false past the list's end.
+template <int F>
+__device__ __forceinline__ bool tiny_pair(int p, int& fh, int& oh) {
+    constexpr int M = kTinyMap, P = (F - 1) / 2;
+#pragma unroll
+    for (int f = 0; f < F; ++f) {
+        const int lo = f < P ? P - f : 0;              // first output row filter row f meets
+        const int n = M - (f < P ? P - f : f - P);     // output rows it meets
+        if (p < n) {
+            fh = f;
+            oh = lo + p;
+            return true;
+        }
+        p -= n;
+    }
+    return false;
+}
+
+// Grid: (channel blocks, Z), clusters of (1, Z, 1): CTA z of a cluster takes the images
+// [z * ipb, (z + 1) * ipb).
+template <typename T, int F>
+__global__ void __launch_bounds__(TinyFgcShape<F>::THREADS, 2)
+tiny_fgrad_cluster_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap dmap,
+                          const TinyFgcArgs a) {
+    using Sh = TinyFgcShape<F>;
+    constexpr int M = kTinyMap, P = Sh::P, NWC = Sh::NWC, K = kTfcPairsPerWarp;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + a.ns;
+    unsigned char* ring = smem + Sh::RING_OFF;
+    float* pairs = reinterpret_cast<float*>(ring);   // after the last image is consumed
+    float* part = pairs + Sh::PAIR_FLOATS;            // the CTA partial [F][F][64]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cb = blockIdx.x;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t nrank = gridDim.y;
+    const int n0 = static_cast<int>(blockIdx.y) * a.ipb;
+    const int nimg = max(0, min(a.N, n0 + a.ipb) - n0);
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < a.ns; ++k) {
+            mbar_init(&full[k], 1);
+            mbar_init(&empty[k], NWC);   // every compute warp reads every image
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == NWC) {
+        // ---- producer: image i -> slot i mod ns ----
+        if (lane == 0) {
+            prefetch_tensormap(&xmap);
+            prefetch_tensormap(&dmap);
+            bool ok = true;
+            for (int i = 0; i < nimg && ok; ++i) {
+                const int k = i % a.ns;
+                const uint32_t ph = static_cast<uint32_t>(i / a.ns) & 1u;
+                if (i >= a.ns && !mbar_wait(&empty[k], ph ^ 1u, a.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char* dst = ring + static_cast<size_t>(k) * 2 * a.img_bytes;
+                mbar_arrive_expect_tx(&full[k], 2 * a.img_bytes);
+                tma_load_4d(dst, &xmap, &full[k], cb * 64, 0, 0, n0 + i);
+                tma_load_4d(dst + a.img_bytes, &dmap, &full[k], cb * 64, 0, 0, n0 + i);
+            }
+            if (!ok) record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+            // the copies still in flight land before the ring is reused or the CTA leaves
+            for (int i = max(0, nimg - a.ns); i < nimg; ++i)
+                if (!mbar_wait(&full[i % a.ns], static_cast<uint32_t>(i / a.ns) & 1u, a.wait_ns)) {
+                    record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+                    break;
+                }
+        }
+        __syncwarp();
+    }
+    // ---- compute warp w: pairs K*w .. K*w + K - 1 of every image ----
+    int pfh[K], poh[K];
+    bool pok[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) pok[j] = warp < NWC && tiny_pair<F>(warp * K + j, pfh[j], poh[j]);
+    float2 acc[K][F];
+#pragma unroll
+    for (int j = 0; j < K; ++j)
+#pragma unroll
+        for (int fw = 0; fw < F; ++fw) acc[j][fw] = make_float2(0.f, 0.f);
+    if (warp < NWC) {
+        for (int i = 0; i < nimg; ++i) {
+            const int k = i % a.ns;
+            if (!mbar_wait(&full[k], static_cast<uint32_t>(i / a.ns) & 1u, a.wait_ns)) {
+                record_status(a.status, DWC_DEVSTAT_TIMEOUT);
+                break;
+            }
+            const T* X = reinterpret_cast<const T*>(ring + static_cast<size_t>(k) * 2 * a.img_bytes) + 2 * lane;
+            const T* D = reinterpret_cast<const T*>(ring + static_cast<size_t>(k) * 2 * a.img_bytes + a.img_bytes) + 2 * lane;
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                if (!pok[j]) continue;
+                const int ih = poh[j] + pfh[j] - P;
+                float2 d[M], x[M];
+#pragma unroll
+                for (int c = 0; c < M; ++c) {
+                    d[c] = Elem<T>::load_pair(D + (poh[j] * M + c) * 64);
+                    x[c] = Elem<T>::load_pair(X + (ih * M + c) * 64);
+                }
+#pragma unroll
+                for (int fw = 0; fw < F; ++fw)
+#pragma unroll
+                    for (int ow = 0; ow < M; ++ow) {
+                        const int iw = ow + fw - P;
+                        if (iw < 0 || iw >= M) continue;
+                        fma2(acc[j][fw], x[iw], d[ow]);
+                    }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[k]);
+        }
+    }
+    // every image consumed and every copy landed (the producer drained): the ring becomes
+    // the pair partials, then the CTA partial (filter row fh: its pairs in list order)
+    __syncthreads();
+    if (warp < NWC) {
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int fw = 0; fw < F; ++fw)
+                *reinterpret_cast<float2*>(pairs + ((warp * K + j) * F + fw) * 64 + 2 * lane) = acc[j][fw];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < F * F * 32; e += blockDim.x) {
+        const int fh = e / (F * 32), fw = (e / 32) % F, cp = e % 32;
+        int p0 = 0;
+        for (int f = 0; f < fh; ++f) p0 += M - (f < P ? P - f : f - P);
+        const int n = M - (fh < P ? P - fh : fh - P);
+        float2 v = make_float2(0.f, 0.f);
+        for (int r = 0; r < n; ++r) {
+            const float2 t = *reinterpret_cast<const float2*>(pairs + ((p0 + r) * F + fw) * 64 + 2 * cp);
+            v.x += t.x;
+            v.y += t.y;
+        }
+        *reinterpret_cast<float2*>(part + (fh * F + fw) * 64 + 2 * cp) = v;
+    }
+    // every CTA's partial is in its shared memory
+    __syncwarp();
+    cluster_sync_all();
+    // this CTA's share of the F x F x 64 outputs (channel pairs e), summed over the
+    // cluster's CTAs in rank order (all loads issued first)
+    constexpr int E2 = F * F * 32;
+    for (int e = static_cast<int>(rank * blockDim.x + threadIdx.x); e < E2; e += static_cast<int>(nrank * blockDim.x)) {
+        float2 t[kTfcMaxZ];
+#pragma unroll
+        for (int q = 0; q < kTfcMaxZ; ++q)
+            t[q] = static_cast<uint32_t>(q) < nrank ? ld_cluster_f2(part + 2 * e, q) : make_float2(0.f, 0.f);
+        float2 v = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < kTfcMaxZ; ++q) {
+            v.x += t[q].x;
+            v.y += t[q].y;
+        }
+        const int c = cb * 64 + 2 * (e % 32);
+        if (c < a.C) *reinterpret_cast<float2*>(a.dw + static_cast<size_t>(e / 32) * a.C + c) = v;
+    }
+    // no CTA leaves while another still reads its shared memory
+    cluster_sync_all();
+}
+
+// Plan of the cluster form: Z CTAs per channel block (at most 8, one cluster), ipb images
+// each, ring slots a multiple of S that fit in shared memory.  False where the channels
+// cannot be copied with tensor copies (rows of C elements must be 16-byte multiples).
+template <typename T, int F>
+bool tiny_fgrad_cluster_plan(int N, int C, int& Z, int& ipb, int& ns, size_t& smem) {
+    using Sh = TinyFgcShape<F>;
+    if (N <= 0 || C <= 0 || (static_cast<size_t>(C) * sizeof(T)) % 16 != 0) return false;
+    Z = std::min(N, kTfcMaxZ);
+    ipb = (N + Z - 1) / Z;
+    Z = (N + ipb - 1) / ipb;
+    const size_t img = static_cast<size_t>(kTinyMap) * kTinyMap * 64 * sizeof(T);
+    const size_t cap = std::min(kTfcSmemCap, static_cast<size_t>(device_info().max_smem_optin));
+    const int fit = static_cast<int>((cap - Sh::RING_OFF) / (2 * img));
+    ns = std::min(fit, ipb);
+    if (ns < std::min(2, ipb) || 2 * ns * sizeof(uint64_t) > static_cast<size_t>(kTfcBarBytes)) return false;
+    smem = Sh::RING_OFF + std::max(static_cast<size_t>(ns) * 2 * img, static_cast<size_t>(Sh::RED_BYTES));
+    return smem <= cap;
+}
+
+template <typename T, int F>
+cudaError_t launch_tiny_fgrad_cluster(const FilterGrad& p) {
+    using Sh = TinyFgcShape<F>;
+    int Z = 0, ipb = 0, ns = 0;
+    size_t smem = 0;
+    if (!tiny_fgrad_cluster_plan<T, F>(p.N, p.C, Z, ipb, ns, smem)) return cudaErrorNotSupported;
+    auto kern = tiny_fgrad_cluster_kernel<T, F>;
+    static DeviceOnce smem_opt_in;
+    cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
+    if (err != cudaSuccess) return err;
+    const int e = static_cast<int>(sizeof(T));
+    CUtensorMap xmap, dmap;
+    const cuuint64_t dims[4] = {(cuuint64_t)p.C, (cuuint64_t)kTinyMap, (cuuint64_t)kTinyMap, (cuuint64_t)p.N};
+    const cuuint64_t strides[3] = {(cuuint64_t)p.C * e, (cuuint64_t)kTinyMap * p.C * e,
+                                   (cuuint64_t)kTinyMap * kTinyMap * p.C * e};
+    const cuuint32_t box[4] = {64u, (cuuint32_t)kTinyMap, (cuuint32_t)kTinyMap, 1u};
+    if (encode_tiled(&xmap, Elem<T>::kTmaType, 4, const_cast<void*>(p.x), dims, strides, box) != CUDA_SUCCESS ||
+        encode_tiled(&dmap, Elem<T>::kTmaType, 4, const_cast<void*>(p.dy), dims, strides, box) != CUDA_SUCCESS)
+        return cudaErrorNotSupported;
+    TinyFgcArgs a;
+    a.dw = p.dw;
+    a.status = p.status;
+    a.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
+    a.N = p.N;
+    a.C = p.C;
+    a.ipb = ipb;
+    a.ns = ns;
+    a.img_bytes = static_cast<uint32_t>(kTinyMap * kTinyMap * 64 * e);
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((p.C + 63) / 64), static_cast<unsigned>(Z), 1);
+    cfg.blockDim = dim3(Sh::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = p.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = static_cast<unsigned>(Z);
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (err != cudaSuccess || clusters < 1) {
+        (void)cudaGetLastError();
+        return cudaErrorNotSupported;
+    }
+    err = cudaLaunchKernelEx(&cfg, kern, xmap, dmap, a);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+// Whether the one-launch cluster form serves a 7x7-map filter gradient of these sizes
+// (3 taps only).
+template <typename T>
+bool tiny_fgrad_cluster_fits(int N, int C, int F) {
+    int Z, ipb, ns;
+    size_t smem;
+    return F == 3 && tiny_fgrad_cluster_plan<T, 3>(N, C, Z, ipb, ns, smem);
 }
 
 

@@ -148,7 +148,9 @@ size_t dwc_bwd_filter_workspace_size(int N, int H, int W, int C, int FH, int FW,
  *                                                             * dY[n, oh, ow, c].
  * The accumulation axis N*OH*OW is split into slices (§5.1, "accumulation-axis
  * parallelism"); slice partials go to `workspace` and are summed in a fixed order, so the
- * result is bit-identical from run to run (no atomics).
+ * result is bit-identical from run to run (no atomics).  (On 7x7 maps with 3 taps the
+ * slices of a channel block form one thread-block cluster and are summed through
+ * distributed shared memory, in a fixed order too; the workspace is then left untouched.)
  *   x : N x H x W x C, dtype   dy : N x OH x OW x C, dtype   dw : FH x FW x C, fp32 (out)
  *   workspace : device buffer of at least dwc_bwd_filter_workspace_size(...) bytes, owned by
  *               the caller, 16-byte aligned, contents ignored on entry and clobbered.
@@ -232,8 +234,9 @@ int dwc_path(int pass, const void* a, const void* b, const void* out,
 
 /* Kernel launches of this library that a call with these arguments and 16-byte aligned
  * pointers makes (the tcgen05 forward / backward data: a preparation kernel and the main
- * kernel; the tcgen05 filter gradient: one preparation kernel and the main kernel; other
- * filter gradients: the kernel and the sum of its slices), 0 for an empty output, -1 for
+ * kernel; the tcgen05 filter gradient: one preparation kernel and the main kernel; the
+ * filter gradient of 7x7 maps with 3 taps: one kernel; other filter gradients: the
+ * kernel and the sum of its slices), 0 for an empty output, -1 for
  * invalid arguments.  `pass` as for dwc_path.  For profiling and launch accounting. */
 int dwc_kernel_launches(int pass, int N, int H, int W, int C, int FH, int FW, int stride, int pad,
                         dwc_dtype_t dtype);

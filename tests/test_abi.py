@@ -220,6 +220,10 @@ def test_kernel_launch_counts(lib):
     assert n(0, **big) == 2 and n(1, **big) == 2          # tcgen05: preparation + main
     assert n(2, **big) == 2                               # tcgen05 gradient: copies + main
     assert n(2, **dict(big, dtype=0)) == 2                # fp32: kernel + slice sum
+    m7 = dict(N=64, H=7, W=7, C=1024, FH=3, FW=3, pad=1)
+    assert n(2, **m7) == 1                               # 7x7 maps, 3 taps: clusters sum
+    assert n(2, **dict(m7, FH=7, FW=7, pad=3)) == 2       # 7 taps: kernel + slice sum
+    assert n(2, **dict(m7, C=1026)) == 2                 # rows not 16-byte multiples: two launches
     assert n(0, **dict(big, N=0)) == 0
     assert n(0, FH=4, FW=4, **{k: v for k, v in GOOD.items() if k not in ("FH", "FW")}) == 1
     assert n(0, stride=0) == -1

@@ -220,12 +220,15 @@ def test_delta_filter_is_identity_bit_exact():
         assert torch.equal(dx, x.float())
 
 
-def test_bwd_filter_is_deterministic():
-    case = C_(4, 28, 28, 128, 13)
+@pytest.mark.parametrize("case", [C_(4, 28, 28, 128, 13),
+                                  C_(64, 7, 7, 256, 3)],     # 7x7 maps: slices summed in clusters
+                         ids=lambda c: f"{c.N}x{c.H}x{c.W}x{c.C}_f{c.FH}")
+def test_bwd_filter_is_deterministic(case):
     x, dy = case.x().cuda(), case.dy().cuda()
-    a = dwc.bwd_filter(x, dy, (13, 13), 1, 6).clone()
+    f, p = (case.FH, case.FW), case.pad
+    a = dwc.bwd_filter(x, dy, f, 1, p).clone()
     for _ in range(3):
-        b = dwc.bwd_filter(x, dy, (13, 13), 1, 6)
+        b = dwc.bwd_filter(x, dy, f, 1, p)
         assert torch.equal(a, b)
 
 
