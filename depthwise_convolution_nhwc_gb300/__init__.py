@@ -144,6 +144,15 @@ def _check_cuda(*ts):
             raise ValueError("tensors must be contiguous (channels-last dims N,H,W,C)")
 
 
+def _check_buffer(t, shape, dtype, device, what):
+    """A caller-supplied tensor must be exactly what the kernels read or write: the library
+    sees only its pointer."""
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device:
+        raise ValueError(f"{what} must be a {tuple(shape)} {dtype} tensor on {device} "
+                         f"(got {tuple(t.shape)} {t.dtype} on {t.device})")
+    _check_cuda(t)
+
+
 def _call(fn: str, *args):
     code = getattr(load_library(), fn)(*args)
     if code != 0:
@@ -163,6 +172,8 @@ def fwd(x, w, stride: int = 1, pad: int = 0, out=None, stream=None, out_dtype=No
     OH, OW = out_dim(H, FH, stride, pad), out_dim(W, FW, stride, pad)
     if out is None:
         out = torch.empty((N, max(OH, 0), max(OW, 0), C), device=x.device, dtype=od)
+    else:
+        _check_buffer(out, (N, max(OH, 0), max(OW, 0), C), od, x.device, "out")
     if od == torch.float32:
         _call("dwc_fwd", x.data_ptr(), w.data_ptr(), out.data_ptr(), N, H, W, C, FH, FW, stride,
               pad, _dtype_code(x), _stream_ptr(stream))
@@ -189,6 +200,8 @@ def fwd_bn_act(x, w, mean, var, gamma, beta, eps: float = 1e-5, act: str = "relu
     OH, OW = out_dim(H, FH, stride, pad), out_dim(W, FW, stride, pad)
     if out is None:
         out = torch.empty((N, max(OH, 0), max(OW, 0), C), device=x.device, dtype=torch.float32)
+    else:
+        _check_buffer(out, (N, max(OH, 0), max(OW, 0), C), torch.float32, x.device, "out")
     _call("dwc_fwd_bn_act", x.data_ptr(), mean.data_ptr(), var.data_ptr(), gamma.data_ptr(),
           beta.data_ptr(), float(eps), ACTS[act], w.data_ptr(), out.data_ptr(), N, H, W, C, FH,
           FW, stride, pad, _dtype_code(x), _stream_ptr(stream))
@@ -205,9 +218,13 @@ def bwd_data(dy, w, in_hw, stride: int = 1, pad: int = 0, out=None, stream=None,
     H, W = (int(v) for v in in_hw)
     if (out_dim(H, FH, stride, pad), out_dim(W, FW, stride, pad)) != (OH, OW):
         raise ValueError("dy spatial size does not match the forward output of in_hw")
+    if w.dtype != dy.dtype:
+        raise ValueError("filter must have dy's dtype")
     od = torch.float32 if out_dtype is None else out_dtype
     if out is None:
         out = torch.empty((N, H, W, C), device=dy.device, dtype=od)
+    else:
+        _check_buffer(out, (N, H, W, C), od, dy.device, "out")
     if od == torch.float32:
         _call("dwc_bwd_data", dy.data_ptr(), w.data_ptr(), out.data_ptr(), N, H, W, C, FH, FW,
               stride, pad, _dtype_code(dy), _stream_ptr(stream))
@@ -247,8 +264,12 @@ def bwd_filter(x, dy, f_hw, stride: int = 1, pad: int = 0, out=None, ws=None, st
     _check_cuda(x, dy)
     N, H, W, C = x.shape
     FH, FW = (int(v) for v in f_hw)
+    OH, OW = out_dim(H, FH, stride, pad), out_dim(W, FW, stride, pad)
+    _check_buffer(dy, (N, max(OH, 0), max(OW, 0), C), x.dtype, x.device, "dy")
     if out is None:
         out = torch.empty((FH, FW, C), device=x.device, dtype=torch.float32)
+    else:
+        _check_buffer(out, (FH, FW, C), torch.float32, x.device, "out")
     nbytes = load_library().dwc_bwd_filter_workspace_size(N, H, W, C, FH, FW, stride, pad,
                                                           _dtype_code(x))
     if ws is None:

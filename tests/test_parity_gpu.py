@@ -251,6 +251,28 @@ def test_outputs_do_not_write_outside_their_buffers():
         assert torch.all(buf[:pad] == 1234.5) and torch.all(buf[pad + n:] == 1234.5), name
 
 
+def test_mismatched_buffers_are_rejected():
+    """A caller-supplied buffer of the wrong dtype, shape or layout is refused before any
+    launch (the library sees only its pointer: a 16-bit tensor taking fp32 outputs would be
+    written past its end)."""
+    case = C_(2, 9, 9, 64, 3, dtype="bf16")
+    x, w, dy = case.x().cuda(), case.w().cuda(), case.dy().cuda()
+    with pytest.raises(ValueError):
+        dwc.fwd(x, w, 1, 1, out=torch.empty(x.shape, dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError):
+        dwc.bwd_data(dy, w, (9, 9), 1, 1, out=torch.empty((2, 9, 9, 32), device="cuda"))
+    with pytest.raises(ValueError):
+        dwc.bwd_data(dy, w, (9, 9), 1, 1, out=torch.empty((2, 9, 64, 9), device="cuda").transpose(2, 3))
+    with pytest.raises(ValueError):
+        dwc.bwd_filter(x, dy[:1], (3, 3), 1, 1)
+    with pytest.raises(ValueError):
+        dwc.bwd_filter(x, dy, (3, 3), 1, 1, out=torch.empty((3, 3, 64), dtype=torch.bfloat16, device="cuda"))
+    y = dwc.fwd(x, w, 1, 1, out=torch.empty(x.shape, dtype=torch.bfloat16, device="cuda"),
+                out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert y.dtype == torch.bfloat16
+
+
 def test_empty_batch():
     x = torch.zeros(0, 8, 8, 64, device="cuda")
     w = torch.randn(3, 3, 64, device="cuda")
