@@ -273,6 +273,24 @@ def test_mismatched_buffers_are_rejected():
     assert y.dtype == torch.bfloat16
 
 
+@pytest.mark.skipif(torch.cuda.device_count() < 2, reason="needs two visible GPUs")
+def test_second_device_after_first():
+    """Kernels that opt in to more than 48 KiB of shared memory do so on every device they
+    run on (the opt-in is per device): the same calls on GPU 1 after GPU 0 agree bit for bit."""
+    case = C_(2, 28, 28, 128, 7)
+    res = []
+    for d in (0, 1):
+        with torch.cuda.device(d):
+            x, w, dy = (t.to(f"cuda:{d}") for t in (case.x(), case.w(), case.dy()))
+            y = dwc.fwd(x, w, 1, 3)
+            dx = dwc.bwd_data(dy, w, (28, 28), 1, 3)
+            dw = dwc.bwd_filter(x, dy, (7, 7), 1, 3)
+            torch.cuda.synchronize()
+            res.append([t.cpu() for t in (y, dx, dw)])
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+
+
 def test_empty_batch():
     x = torch.zeros(0, 8, 8, 64, device="cuda")
     w = torch.randn(3, 3, 64, device="cuda")
