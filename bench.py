@@ -69,6 +69,9 @@ def kernel_name(case, pass_name, family):
     with 3 to 7 taps and "same" padding have their own small-map kernels)."""
     if case.stride == 2 and family == 1 and pass_name == "bwd_data":
         return "s2_bwd_data_kernel"
+    if (pass_name == "fwd_bn_act" and family == 1 and case.stride == 1 and case.FH == case.FW == 7
+            and case.C % 4 == 0 and case.W >= 28):
+        return "bnact_apply_kernel + rows_kernel"
     if (family == 3 and case.stride == 1 and case.H == case.W == 7 and case.FH == case.FW
             and case.FH in (3, 5, 7) and case.pad == (case.FH - 1) // 2):
         if pass_name != "bwd_filter":

@@ -219,6 +219,10 @@ bool bnact_fast_eligible(const Problem& P, const void* a, const void* b, const v
 }
 
 cudaError_t launch_rows_bnact(const RowConv& rc, int stride) {
+    if (bnact_split_serves(rc.FH, rc.FW, stride, rc.C, rc.W)) {
+        const cudaError_t err = launch_bnact_split(rc, stride);
+        if (err != cudaErrorNotSupported) return err;
+    }
     switch (rc.dtype) {
         case kF32: return launch_rows_bnact_f32(rc, stride);
         case kBF16: return launch_rows_bnact_bf16(rc, stride);
@@ -627,7 +631,16 @@ int dwc_kernel_launches(int pass, int N, int H, int W, int C, int FH, int FW, in
         if (fam == 3 && stride == 1 && tiny_fgrad_single_launch(P.dtype, N, H, W, C, FH, FW, pad)) return 1;
         return 2;
     }
-    if (pass == 3) return 1;
+    if (pass == 3) {
+        // 7x7 at stride 1 on the fast path: act(BN(x)) into scratch (and 16-bit filters
+        // widened), then the plain fp32 forward (a second launch for a tail of at most 32
+        // channels past a multiple of 64)
+        if (fam == 1 && bnact_split_serves(FH, FW, stride, C, W)) {
+            const int rem = C % 64;
+            return (dtype == DWC_F32 ? 2 : 3) + (C > 64 && rem != 0 && rem <= 32 ? 1 : 0);
+        }
+        return 1;
+    }
     if (fam == 2) {
         const RowConv rc = pass == kPassFwd
             ? RowConv{nullptr, nullptr, nullptr, N, H, W, C, P.OH, P.OW, FH, FW, pad, pad, false,

@@ -135,6 +135,10 @@ cudaError_t launch_rows_s2_f16(const RowConv& p);
 // BN + Act + forward DWC on the row kernels (square filters of 3, 5 or 7 taps, stride 1 or
 // 2, the layout rules of the fast paths; RowConv carries the BN parameters and act >= 0).
 cudaError_t launch_rows_bnact_f32(const RowConv& p, int stride);
+// BN + Act + forward as two passes (act(BN(x)) once per element into fp32 scratch, then the
+// plain fp32 forward): 7x7 filters at stride 1, C a multiple of 4, rows of 28 or more.
+bool bnact_split_serves(int FH, int FW, int stride, int C, int W);
+cudaError_t launch_bnact_split(const RowConv& p, int stride);
 cudaError_t launch_rows_bnact_bf16(const RowConv& p, int stride);
 cudaError_t launch_rows_bnact_f16(const RowConv& p, int stride);
 

@@ -120,7 +120,12 @@ typedef enum {
  * The fused fast path covers square 3x3, 5x5 and 7x7 filters at stride 1 or 2 under the
  * layout rules of the fast kernels; other problems run a general fused kernel.  Errors as
  * dwc_fwd; DWC_ERR_INVALID_ARG also for a null BN pointer (C > 0), an unknown activation or
- * a negative or non-finite eps; DWC_ERR_ALIGNMENT for a BN pointer not 4-byte aligned. */
+ * a negative or non-finite eps; DWC_ERR_ALIGNMENT for a BN pointer not 4-byte aligned.
+ * Exception to "one pass": 7x7 filters at stride 1 (C a multiple of 4, rows of 28 or more
+ * pixels) measured faster as two
+ * passes (the fused 7x7 kernel's per-element transforms cost more than the HBM round trip of
+ * Z), so there Z is written once as fp32 to stream-ordered scratch memory from the library's
+ * pool and the plain forward reads it: the same arithmetic and results. */
 dwc_status_t dwc_fwd_bn_act(const void* x, const float* mean, const float* var,
                             const float* gamma, const float* beta, float eps, dwc_act_t act,
                             const void* w, float* y, int N, int H, int W, int C, int FH, int FW,

@@ -215,6 +215,8 @@ def test_kernel_launch_counts(lib):
     f7 = dict(N=64, H=56, W=56, C=128, FH=7, FW=7, pad=3)
     assert n(0, **f7) == 1 and n(1, **f7) == 1 and n(2, **f7) == 2
     assert n(0, **dict(f7, C=96)) == 2                     # lane-group tail: a second launch
+    assert n(3, **f7) == 2 and n(3, **dict(f7, dtype=1)) == 3   # BN + Act 7x7: apply (+ widen w) + forward
+    assert n(3, **dict(f7, H=14, W=14)) == 1                # narrow rows: the fused kernel
     assert n(0, **dict(f7, C=32)) == 1                     # the tail is the only launch
     big = dict(N=32, H=56, W=56, C=128, FH=31, FW=31, pad=15, dtype=1)
     assert n(0, **big) == 2 and n(1, **big) == 2          # tcgen05: preparation + main
