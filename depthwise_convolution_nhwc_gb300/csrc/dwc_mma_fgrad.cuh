@@ -43,6 +43,7 @@ struct MmaFgArgs {
 
 template <typename T>
 __global__ void __launch_bounds__(kMmaWarps * 32, 2) mma_fgrad_kernel(const MmaFgArgs a) {
+    pdl_trigger();   // the slice sum may be scheduled now (it waits for this grid)
     extern __shared__ __align__(128) unsigned char smem[];
     uint16_t* xb = reinterpret_cast<uint16_t*>(smem);               // [8][XR][XC]
     uint16_t* db = reinterpret_cast<uint16_t*>(smem + a.dy_off);    // [8][RB][DC]

@@ -339,6 +339,7 @@ __device__ __forceinline__ void fgrad_row(float2 (&acc)[DR + 1], const float2 (&
 
 template <typename T, int MAXW, int DR>
 __global__ void __launch_bounds__(kSmMaxWarps * 32, 1) small_fgrad_kernel(const SmallFgArgs a) {
+    pdl_trigger();   // the slice sum may be scheduled now (it waits for this grid)
     constexpr int NP = DR + 1;
     extern __shared__ __align__(128) unsigned char smem[];
     T* xbuf = reinterpret_cast<T*>(smem);                       // [2][G][H][MAXW][32]
@@ -771,6 +772,7 @@ __device__ __forceinline__ void tiny_fgrad_part(const T* __restrict__ X, const T
 // [z * ipb, (z + 1) * ipb).
 template <typename T, int F>
 __global__ void __launch_bounds__(64) tiny_fgrad_kernel(const TinyFgArgs a) {
+    pdl_trigger();   // the slice sum may be scheduled now (it waits for this grid)
     const int lane = threadIdx.x & 31, part = threadIdx.x >> 5;
     const int cb = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.cblocks));
     const int z = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.cblocks));
