@@ -438,6 +438,7 @@ constexpr int kTcPrepThreads = 256;
 
 template <typename T, bool FLIP>
 __global__ void __launch_bounds__(kTcPrepThreads) tc_prep_kernel(const TcPrepArgs a) {
+    pdl_trigger();   // the main kernel may be scheduled now (it waits for this grid)
     __shared__ uint32_t tile[8 * kStackRows * kStackWords];
     if (static_cast<int>(blockIdx.x) >= a.run_blocks) {
         // the plane-major stacked copy, tile by tile
@@ -551,6 +552,9 @@ tc_rows_kernel(const TcArgs a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // launched as a programmatic dependent of the preparation kernel: its stacked copy and
+    // runs are complete and visible past this point
+    pdl_wait();
 
     if (warp >= kTcMmaWarp && warp < kTcMmaWarp + kTcIssuers) {
         // ------------------------------------------------------------- MMA issue
@@ -1030,8 +1034,19 @@ cudaError_t launch_tc_main(const TcArgs& a, size_t smem, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     const unsigned grid = static_cast<unsigned>(
         std::min<long long>(a.units, static_cast<long long>(device_info().sm_count)));
-    kern<<<grid, kTcThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    // a programmatic dependent of the preparation kernel before it: its set-up (barriers,
+    // tensor memory) overlaps the preparation's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <typename T, class OutT>

@@ -140,6 +140,9 @@ tc_fgrad_kernel(const TcFgArgs a) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t iters = static_cast<uint32_t>(a.col_tiles * a.row_blocks);   // stages per unit
+    // launched as a programmatic dependent of the stacking kernel: both copies and the zero
+    // band are complete and visible past this point
+    pdl_wait();
 
     if (warp == kTfgTmaWarp) {
         // ------------------------------------------------------------- copy producer
@@ -346,6 +349,7 @@ inline uint32_t tc_fgrad_idesc(int n) {
 template <typename T>
 __global__ void __launch_bounds__(256) tc_stack_pm_kernel(const TcStackArgs ax, const TcStackArgs ady,
                                                           uint4* zeros, int zero_words) {
+    pdl_trigger();   // the main kernel may be scheduled now (it waits for this grid)
     __shared__ uint32_t tile[8 * kStackRows * kStackWords];   // [column][row][words]
     if (blockIdx.x == 0)
         for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zeros[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -363,8 +367,19 @@ cudaError_t launch_tc_fgrad_main(const TcFgArgs& a, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     const unsigned grid = static_cast<unsigned>(
         std::min<long long>(a.units, static_cast<long long>(device_info().sm_count)));
-    kern<<<grid, kTfgThreads, TfgShape<NARROW>::kSmem, stream>>>(a);
-    return cudaGetLastError();
+    // a programmatic dependent of the stacking kernel before it: its set-up overlaps the
+    // stacking's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTfgThreads);
+    cfg.dynamicSmemBytes = TfgShape<NARROW>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <typename T>
