@@ -101,6 +101,24 @@ struct Ring {
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Launch `kern` as a programmatic dependent of the kernel before it in the stream.  The
+// kernel must call pdl_wait() before it touches global memory: the previous grid (whatever
+// wrote its inputs or still reads its outputs) has then finished.
+template <class K, class... Args>
+cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 __device__ __forceinline__ void record_status(unsigned int* status, unsigned int bits) {
     if (status) atomicOr(status, bits);
 }

@@ -201,7 +201,10 @@ fgrad_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     constexpr int PITCH = kBN / G;   // channels per staged pixel
     constexpr int LPG = 32 / G;      // lanes per group
     extern __shared__ __align__(128) unsigned char smem[];
-    pdl_trigger();   // the slice sum may be scheduled now (it waits for this grid)
+    // the slice sum may be scheduled now (it waits for this grid); a programmatic dependent
+    // of the kernel before it, this grid touches no global memory before that one finished
+    pdl_trigger();
+    pdl_wait();
     uint64_t* xfull = reinterpret_cast<uint64_t*>(smem);
     uint64_t* xempty = xfull + a.nx;
     uint64_t* yfull = xempty + a.nx;
@@ -645,8 +648,7 @@ cudaError_t fgrad_enqueue(const FilterGrad& p, const FgradPlan<FH, FW, Tile>& P,
     }
     const int threads = (P.nwf * Tile::NFC * P.nwc + 1) * 32;
     const unsigned grid = static_cast<unsigned>(P.Z) * P.ncp * P.cblocks * P.chunks;
-    kern<<<grid, threads, P.smem, p.stream>>>(xmap, ymap, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(threads), P.smem, p.stream, xmap, ymap, a);
 }
 
 template <typename T, int FH, int FW, class Tile = FgradTile<FH, FW>, int G = 1>

@@ -197,6 +197,10 @@ rows_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CU
     const int S = FH > 0 ? SC : R + fhn - 1;
 
     extern __shared__ __align__(128) unsigned char smem[];
+    // a programmatic dependent of the kernel before it: the next kernel may be scheduled
+    // now, and nothing in global memory is touched before the previous grid has finished
+    pdl_trigger();
+    pdl_wait();
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + a.ns;
     unsigned char* stages = smem + 128;
@@ -551,8 +555,7 @@ cudaError_t launch_rows_inst(const RowConv& p) {
     a.ns = ns;
     const size_t smem = 128 + static_cast<size_t>(ns) * a.stage_stride;
     const long long grid = std::min<long long>(units, static_cast<long long>(dev.sm_count) * ctas);
-    kern<<<static_cast<unsigned>(grid), threads, smem, p.stream>>>(xmap, wmap, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, p.stream, xmap, wmap, a);
 }
 
 // Channel counts that are not a multiple of 64 (3x3, 5x5, 7x7, fp32 or 16-bit outputs): the
