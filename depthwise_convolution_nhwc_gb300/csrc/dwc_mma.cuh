@@ -90,6 +90,10 @@ __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
 
 template <typename T, bool FLIP, class OutT = float>
 __global__ void __launch_bounds__(kMmaWarps * 32, 2) mma_rows_kernel(const MmaArgs a) {
+    // a programmatic dependent of the kernel before it: nothing in global memory is touched
+    // before that grid has finished
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ __align__(128) unsigned char smem[];
     uint16_t* xb = reinterpret_cast<uint16_t*>(smem);                 // [8][XR][XC]
     float* ob = reinterpret_cast<float*>(smem);                        // [RB][OW][8], after compute
@@ -327,8 +331,7 @@ cudaError_t launch_mma_inst(const RowConv& p) {
     }
     const int ctas = smem * 2 + 2048 <= 233472u ? 2 : 1;
     const long long grid = std::min<long long>(a.units, static_cast<long long>(device_info().sm_count) * ctas);
-    kern<<<static_cast<unsigned>(grid), kMmaWarps * 32, smem, p.stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kMmaWarps * 32), smem, p.stream, a);
 }
 
 // Where the tensor-core kernel beats the row-streaming kernel for 16-bit inputs (timed on

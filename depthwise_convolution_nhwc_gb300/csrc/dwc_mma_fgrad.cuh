@@ -44,6 +44,7 @@ struct MmaFgArgs {
 template <typename T>
 __global__ void __launch_bounds__(kMmaWarps * 32, 2) mma_fgrad_kernel(const MmaFgArgs a) {
     pdl_trigger();   // the slice sum may be scheduled now (it waits for this grid)
+    pdl_wait();      // (a programmatic dependent itself: the grid before it has finished)
     extern __shared__ __align__(128) unsigned char smem[];
     uint16_t* xb = reinterpret_cast<uint16_t*>(smem);               // [8][XR][XC]
     uint16_t* db = reinterpret_cast<uint16_t*>(smem + a.dy_off);    // [8][RB][DC]
@@ -262,8 +263,7 @@ cudaError_t launch_mma_fgrad(const FilterGrad& p) {
         if (err != cudaSuccess) return err;
     }
     const unsigned grid = static_cast<unsigned>(a.Z) * static_cast<unsigned>(p.C / kMmaCB);
-    kern<<<grid, kMmaWarps * 32, smem, p.stream>>>(a);
-    cudaError_t err = cudaGetLastError();
+    const cudaError_t err = launch_pdl(kern, dim3(grid), dim3(kMmaWarps * 32), smem, p.stream, a);
     if (err != cudaSuccess) return err;
     return launch_reduce_slices(p.workspace, a.Z, count, p.dw, p.stream);
 }

@@ -131,6 +131,10 @@ struct SmallArgs {
 
 template <typename T, int MAXW, int DR, class OutT = float>
 __global__ void __launch_bounds__(kSmMaxWarps * 32, 1) small_rows_kernel(const SmallArgs a) {
+    // a programmatic dependent of the kernel before it: nothing in global memory is touched
+    // before that grid has finished
+    pdl_trigger();
+    pdl_wait();
     constexpr int NJ = 2 * DR + 1;
     extern __shared__ __align__(128) unsigned char smem[];
     T* xbuf = reinterpret_cast<T*>(smem);                          // [ns][G][H][MAXW][32]
@@ -340,6 +344,7 @@ __device__ __forceinline__ void fgrad_row(float2 (&acc)[DR + 1], const float2 (&
 template <typename T, int MAXW, int DR>
 __global__ void __launch_bounds__(kSmMaxWarps * 32, 1) small_fgrad_kernel(const SmallFgArgs a) {
     pdl_trigger();   // the slice sum may be scheduled now (it waits for this grid)
+    pdl_wait();      // (a programmatic dependent itself: the grid before it has finished)
     constexpr int NP = DR + 1;
     extern __shared__ __align__(128) unsigned char smem[];
     T* xbuf = reinterpret_cast<T*>(smem);                       // [2][G][H][MAXW][32]
@@ -534,8 +539,7 @@ cudaError_t launch_small_rows_inst(const RowConv& p) {
         const cudaError_t err = opt_in_smem(kern, smem_opt_in, device_info().max_smem_optin);
         if (err != cudaSuccess) return err;
     }
-    kern<<<static_cast<unsigned>(grid), nwarps * 32, smem, p.stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(nwarps * 32), smem, p.stream, a);
 }
 
 // Launch plan of the small-map filter gradient (shared by the workspace query and launch).
@@ -590,8 +594,7 @@ cudaError_t launch_small_fgrad_inst(const FilterGrad& p) {
         if (err != cudaSuccess) return err;
     }
     const unsigned grid = static_cast<unsigned>(Z) * a.cblocks;
-    kern<<<grid, nwarps * 32, smem, p.stream>>>(a);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(kern, dim3(grid), dim3(nwarps * 32), smem, p.stream, a);
     if (err != cudaSuccess) return err;
     // rows of dw outside the window never meet the image
     const size_t row = static_cast<size_t>(p.FW) * p.C;
@@ -681,6 +684,10 @@ __device__ __forceinline__ void tiny_rows_part(const T* __restrict__ X, const T*
 // Grid: cblocks x N CTAs of 2 warps (even / odd output rows).
 template <typename T, int F, class OutT>
 __global__ void __launch_bounds__(64) tiny_rows_kernel(const TinyArgs a) {
+    // a programmatic dependent of the kernel before it: nothing in global memory is touched
+    // before that grid has finished
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31, part = threadIdx.x >> 5;
     const int cb = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.cblocks));
     const int n = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.cblocks));
@@ -705,12 +712,11 @@ cudaError_t launch_tiny_rows(const RowConv& p) {
     if (grid >= (1LL << 31) || p.C % 2 != 0) return cudaErrorNotSupported;
     const unsigned g = static_cast<unsigned>(grid);
     switch (p.FH) {
-        case 3: tiny_rows_kernel<T, 3, OutT><<<g, 64, 0, p.stream>>>(a); break;
-        case 5: tiny_rows_kernel<T, 5, OutT><<<g, 64, 0, p.stream>>>(a); break;
-        case 7: tiny_rows_kernel<T, 7, OutT><<<g, 64, 0, p.stream>>>(a); break;
+        case 3: return launch_pdl(tiny_rows_kernel<T, 3, OutT>, dim3(g), dim3(64), 0, p.stream, a);
+        case 5: return launch_pdl(tiny_rows_kernel<T, 5, OutT>, dim3(g), dim3(64), 0, p.stream, a);
+        case 7: return launch_pdl(tiny_rows_kernel<T, 7, OutT>, dim3(g), dim3(64), 0, p.stream, a);
         default: return cudaErrorNotSupported;
     }
-    return cudaGetLastError();
 }
 
 struct TinyFgArgs {
@@ -773,6 +779,7 @@ __device__ __forceinline__ void tiny_fgrad_part(const T* __restrict__ X, const T
 template <typename T, int F>
 __global__ void __launch_bounds__(64) tiny_fgrad_kernel(const TinyFgArgs a) {
     pdl_trigger();   // the slice sum may be scheduled now (it waits for this grid)
+    pdl_wait();      // (a programmatic dependent itself: the grid before it has finished)
     const int lane = threadIdx.x & 31, part = threadIdx.x >> 5;
     const int cb = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.cblocks));
     const int z = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.cblocks));
@@ -821,13 +828,13 @@ cudaError_t launch_tiny_fgrad(const FilterGrad& p) {
     const long long grid = static_cast<long long>(a.cblocks) * Z;
     if (grid >= (1LL << 31) || p.C % 2 != 0) return cudaErrorNotSupported;
     const unsigned g = static_cast<unsigned>(grid);
+    cudaError_t err = cudaErrorNotSupported;
     switch (p.FH) {
-        case 3: tiny_fgrad_kernel<T, 3><<<g, 64, 0, p.stream>>>(a); break;
-        case 5: tiny_fgrad_kernel<T, 5><<<g, 64, 0, p.stream>>>(a); break;
-        case 7: tiny_fgrad_kernel<T, 7><<<g, 64, 0, p.stream>>>(a); break;
-        default: return cudaErrorNotSupported;
+        case 3: err = launch_pdl(tiny_fgrad_kernel<T, 3>, dim3(g), dim3(64), 0, p.stream, a); break;
+        case 5: err = launch_pdl(tiny_fgrad_kernel<T, 5>, dim3(g), dim3(64), 0, p.stream, a); break;
+        case 7: err = launch_pdl(tiny_fgrad_kernel<T, 7>, dim3(g), dim3(64), 0, p.stream, a); break;
+        default: break;
     }
-    const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     return launch_reduce_slices(p.workspace, Z, count, p.dw, p.stream);
 }
