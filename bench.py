@@ -334,7 +334,8 @@ def record_traffic(raw_csv, workload, passes=PASSES_ALL):
     for d in data:
         name = d[ix["Kernel Name"]]
         targs = name.split("<", 1)[1].split(",") if "<" in name else []
-        if "small_rows_kernel" in name:  # rotation is a runtime argument: launch order
+        if "small_rows_kernel" in name or "tiny_rows_kernel" in name:
+            # rotation is a runtime argument: launch order
             which = [p for p in passes if p in ("fwd", "bwd_data")]
             per[which[min(small_rows_seen, len(which) - 1)]] += dram(d)
             small_rows_seen += 1
@@ -349,7 +350,7 @@ def record_traffic(raw_csv, workload, passes=PASSES_ALL):
         elif "rows_kernel" in name:      # <T, FH, FW, R, TM, MINB, FLIP, P>
             flip = targs[6].strip()
             per["bwd_data" if flip in ("1", "true") else "fwd"] += dram(d)
-        elif "fgrad_kernel" in name or "reduce_slices" in name:
+        elif ("fgrad" in name or "reduce_slices" in name or "tc_stack_pm_kernel" in name):
             per["bwd_filter"] += dram(d)
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
