@@ -793,17 +793,20 @@ __global__ void __launch_bounds__(64) tiny_fgrad_kernel(const TinyFgArgs a) {
     else tiny_fgrad_part<T, F, 1>(X, D, out, a.C, n0, n1);
 }
 
-// Images per slice: enough CTAs for about four per SM.
-inline int tiny_fgrad_ipb(int N, int C) {
+// Images per slice: CTAs for about 8 (up to 5 taps) or 4 (7 taps) per SM.  fp32 64x7x7x1024
+// at 5 taps: one image per CTA (64 slices) 16.9 -> 14.9 us; at 7 taps (254 registers, 4 CTAs
+// per SM) two images per CTA stay faster (17.2 against 18.7 us), and fewer slices were slower
+// for both (3 images 18.7 / 18.8 us, 4 images 22.1 / 19.9 us).
+inline int tiny_fgrad_ipb(int N, int C, int F) {
     const long long cblocks = (C / 2 + kTinyPairs - 1) / kTinyPairs;
-    const long long want = 4LL * device_info().sm_count;
+    const long long want = (F <= 5 ? 8LL : 4LL) * device_info().sm_count;
     const long long z = std::max(1LL, std::min<long long>(N, want / std::max(1LL, cblocks)));
     return static_cast<int>((N + z - 1) / z);
 }
 
 inline size_t tiny_fgrad_workspace_floats(int N, int C, int F) {
     if (N <= 0) return 0;
-    const int ipb = tiny_fgrad_ipb(N, C);
+    const int ipb = tiny_fgrad_ipb(N, C, F);
     return static_cast<size_t>((N + ipb - 1) / ipb) * F * F * C;
 }
 
@@ -819,7 +822,7 @@ cudaError_t launch_tiny_fgrad(const FilterGrad& p) {
     TinyFgArgs a;
     a.x = p.x; a.dy = p.dy;
     a.N = p.N; a.C = p.C;
-    a.ipb = tiny_fgrad_ipb(p.N, p.C);
+    a.ipb = tiny_fgrad_ipb(p.N, p.C, p.FH);
     a.cblocks = (p.C / 2 + kTinyPairs - 1) / kTinyPairs;
     const int Z = (p.N + a.ipb - 1) / a.ipb;
     const size_t count = static_cast<size_t>(p.FH) * p.FW * p.C;
