@@ -464,6 +464,8 @@ OUT16 = [
     C_(1, 23, 37, 128, 7),
     C_(1, 20, 60, 64, 17),          # tensor-core kernels (wide rows, 17 taps)
     C_(2, 7, 7, 128, 9),            # small-map kernels
+    C_(3, 7, 7, 64, 3),             # 7x7 maps, thread per image and channel pair
+    C_(2, 7, 7, 128, 7),
     C_(8, 8, 8, 256, 31),           # warp per image, large window (shared-memory plan)
     C_(2, 17, 19, 64, 3, s=2),      # stride-2 kernels
     C_(1, 23, 37, 128, 7, s=2),
