@@ -30,8 +30,20 @@
  * gradient for re-laid-out copies of x and dy (about 1.3x their bytes) -- from a memory pool
  * the library creates per device on first use and that keeps up to 512 MiB between calls;
  * the scratch returns to the pool in stream order (cudaFreeAsync) after the call's kernels.
- * If the allocation fails the call runs on another kernel.  No other call allocates device
- * memory (dwc_bwd_filter otherwise takes a caller workspace).
+ * If the allocation fails the call runs on another kernel.  dwc_fwd_bn_act with 7x7 filters
+ * at stride 1 on rows of 28 or more takes scratch from the same pool for an fp32 copy of
+ * act(BN(X)) (4 bytes per input element, plus the filter widened to fp32 for 16-bit
+ * inputs).  No other call allocates device memory (dwc_bwd_filter otherwise takes a caller
+ * workspace).
+ *
+ * Stream order and dependent launches: the library launches its kernels with programmatic
+ * stream serialization.  Each kernel lets the next kernel of the stream be scheduled as it
+ * starts, and waits (griddepcontrol.wait) for the kernel before it to complete before it
+ * touches memory, so the results are those of plain stream order.  A caller kernel launched
+ * right after a call WITH the programmatic-serialization attribute must likewise wait
+ * (griddepcontrol.wait / cudaGridDependencySynchronize) before reading the call's outputs,
+ * as the CUDA model asks of every programmatic dependent; ordinary launches, events, copies
+ * and CUDA-graph capture see plain stream order.
  *
  * Errors: every call validates its arguments on the host and returns a dwc_status_t
  * without launching anything when they are wrong.  No call aborts or throws.  A CUDA
