@@ -313,13 +313,12 @@ def _sources_sha():
     return rels, h.hexdigest()
 
 
-def record_traffic(raw_csv, workload, passes=PASSES_ALL):
-    """Write profiles/traffic.json from `ncu -i <report> --page raw --csv` output that holds
-    the kernels of one timed step (in launch order, of the passes given): DRAM bytes per
-    launch of each pass, with a hash of the kernel sources so that the entry is ignored once
-    a kernel changes."""
+def traffic_per_pass(raw_csv, passes=PASSES_ALL):
+    """DRAM bytes (read + write) of each pass from `ncu -i <report> --page raw --csv` output
+    holding the kernels of one step in launch order: a pass's kernels are told apart by name
+    and, where the name does not say (the rotation of the small-map and 7x7-map row kernels,
+    the tcgen05 main kernel), by the launch order."""
     import csv
-    case = get_case(workload)
     rows = list(csv.reader(open(raw_csv)))
     hdr, units, data = rows[0], rows[1], rows[2:]
     ix = {h: i for i, h in enumerate(hdr)}
@@ -352,6 +351,16 @@ def record_traffic(raw_csv, workload, passes=PASSES_ALL):
             per["bwd_data" if flip in ("1", "true") else "fwd"] += dram(d)
         elif ("fgrad" in name or "reduce_slices" in name or "tc_stack_pm_kernel" in name):
             per["bwd_filter"] += dram(d)
+    return per
+
+
+def record_traffic(raw_csv, workload, passes=PASSES_ALL):
+    """Write profiles/traffic.json from `ncu -i <report> --page raw --csv` output that holds
+    the kernels of one timed step (in launch order, of the passes given): DRAM bytes per
+    launch of each pass, with a hash of the kernel sources so that the entry is ignored once
+    a kernel changes."""
+    case = get_case(workload)
+    per = traffic_per_pass(raw_csv, passes)
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         tab = json.load(open(path))
